@@ -1,0 +1,57 @@
+/*
+ * Stage hooks of libswin_wattn, for tests: each runs one kernel of the
+ * three-kernel path on caller buffers, so that every step of the block can be
+ * compared with the float64 oracle on its own.  Same conventions as
+ * swin_wattn.h (device pointers, bf16 tensors, asynchronous on `stream`,
+ * status codes).  Intermediate layout, window order: row r = win*N + t with
+ * win = (b*(H/M) + wi)*(W/M) + wj and t = ti*M + tj (N = M*M tokens per
+ * window).
+ */
+#ifndef SWIN_WATTN_TEST_H
+#define SWIN_WATTN_TEST_H
+
+#include "swin_wattn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Cyclic shift by -s, window partition and QKV projection with bias
+ * (pages: "Boosting Swin Transformer Speed", Training Optimization -- the
+ * partition/shift index maps; Inference Optimization -- QKV GEMM with bias).
+ *   qkv[r, o] = sum_c x[b, (wi*M+ti+s) mod H, (wj*M+tj+s) mod W, c] * Wqkv[o, c] + bqkv[o]
+ * qkv is [B*H*W, 3C] bf16 in window order.  bf16 mode only. */
+int swin_wattn_test_qkv(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv,
+                        const void *bqkv, void *qkv, swin_stream_t stream);
+
+/* Per-window, per-head attention on a window-ordered qkv buffer: logits (V1 or
+ * V2) + relative bias + shift mask, softmax, P.V.  attn is [B*H*W, C] bf16 in
+ * window order, channel head*d + e.  bf16 mode only. */
+int swin_wattn_test_attn(swin_wattn_t h, const void *qkv, int B, int H, int W,
+                         const void *bias_table, const float *logit_scale, void *attn,
+                         swin_stream_t stream);
+
+/* Output projection with bias, window reverse and roll by +s:
+ *   out[b, (wi*M+ti+s) mod H, (wj*M+tj+s) mod W, :] = attn[r, :] Wproj^T + bproj
+ * bf16 mode only. */
+int swin_wattn_test_proj(swin_wattn_t h, const void *attn, int B, int H, int W,
+                         const void *Wproj, const void *bproj, void *out, swin_stream_t stream);
+
+/* The tensor-core GEMM building block alone, no index maps:
+ *   D[m, n] = sum_k A[m, k] * Bw[n, k] + bias[n]
+ * A [rows, K], Bw [N, K], D [rows, N], bias [N] (may be NULL), bf16,
+ * row-major.  K and N multiples of 16 (N <= 2048), rows >= 0. */
+int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *D, int rows, int N,
+                         int K, swin_stream_t stream);
+
+/* Runs a one-block kernel that waits on a barrier nothing completes, with the
+ * handle's wait limit, so that the bounded-wait path can be tested: the
+ * kernel records a timeout in the handle's error word and returns; the
+ * caller then reads ETIMEOUT from swin_wattn_sync_status. */
+int swin_wattn_test_watchdog(swin_wattn_t h, swin_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIN_WATTN_TEST_H */

@@ -1,0 +1,288 @@
+"""GPU parity: every kernel against the float64 oracle, through the C ABI.
+
+Index maps are compared bit-exactly on integer-tagged tokens; floating-point
+results within the tolerances in tests/helpers.py.  Small cases span several
+128-row tiles and a ragged tail; full-size workloads are checked on sampled
+windows (corners, where the mask and the wrap-around act, plus random ones).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from vision_transformer_shifted_gb300 import binding as sw
+from vision_transformer_shifted_gb300.inputs import V1, V2, WORKLOADS, generate, sample_windows
+
+from helpers import compare, device_inputs, oracle_forward, oracle_table, to_f64, window_tokens
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    sw.load()
+
+
+def run_forward(w, t, table, path=sw.PATH_AUTO):
+    h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode | (sw.FP32 if w.dtype == "fp32" else 0))
+    try:
+        if path:
+            sw.swin_wattn_set_option(h, sw.OPT_PATH, path)
+        out = torch.full_like(t["x"], float("nan"))
+        sw.swin_wattn_forward(h, t["x"], t["Wqkv"], t["bqkv"], table, t.get("tau"), t["Wproj"], t["bproj"], out)
+        assert sw.swin_wattn_sync_status(h) == sw.OK
+        return out
+    finally:
+        sw.swin_wattn_destroy(h)
+
+
+# ---- the tensor-core GEMM building block ------------------------------------
+
+@pytest.mark.parametrize("rows,N,K", [(128, 64, 64), (300, 288, 96), (77, 16, 16), (1000, 1536, 512),
+                                      (513, 576, 192), (256, 384, 128)])
+def test_gemm_block(rows, N, K):
+    g = torch.Generator().manual_seed(rows + N + K)
+    A = torch.randn(rows, K, generator=g).bfloat16()
+    Bw = (torch.randn(N, K, generator=g) * 0.1).bfloat16()
+    bias = (torch.randn(N, generator=g) * 0.1).bfloat16()
+    D = torch.empty(rows, N, dtype=torch.bfloat16, device=DEV)
+    sw.swin_wattn_test_gemm(A.to(DEV), Bw.to(DEV), bias.to(DEV), D)
+    torch.cuda.synchronize()
+    ref = A.double() @ Bw.double().T + bias.double()
+    err = (D.double().cpu() - ref).abs()
+    # one bf16 rounding of the fp32 result (relative 2^-9) plus fp32 accumulation
+    assert (err <= ref.abs() * 2.0 ** -8 + 1e-4).all(), float(err.max())
+
+
+# ---- index maps, bit-exact ----------------------------------------------------
+
+def tagged(B, H, W, C):
+    """Integer-valued tokens (exact in bf16): channels 0..2 carry b, i, j."""
+    b, i, j, c = np.meshgrid(np.arange(B), np.arange(H), np.arange(W), np.arange(C), indexing="ij")
+    x = ((b * 7 + i * 3 + j * 5 + c * 11) % 61 - 30).astype(np.float64)
+    x[..., 0] = b[..., 0]
+    x[..., 1] = i[..., 0] % 251
+    x[..., 2] = j[..., 0] % 251 + 0.5 * (i[..., 0] // 251)
+    return x
+
+
+@pytest.mark.parametrize("B,H,W,C,M,s", [(2, 14, 21, 96, 7, 3), (1, 16, 24, 64, 8, 4), (2, 14, 14, 96, 7, 0),
+                                         (1, 48, 48, 64, 24, 12)])
+def test_qkv_gather_and_proj_scatter_bit_exact(B, H, W, C, M, s):
+    heads = C // 32
+    h = sw.swin_wattn_create(C, heads, M, s, V1)
+    try:
+        x = tagged(B, H, W, C)
+        xt = torch.from_numpy(x).bfloat16().to(DEV)
+        Wqkv = torch.zeros(3 * C, C, dtype=torch.bfloat16)
+        Wqkv[:C] = torch.eye(C)
+        qkv = torch.full((B * H * W, 3 * C), float("nan"), dtype=torch.bfloat16, device=DEV)
+        sw.swin_wattn_test_qkv(h, xt, Wqkv.to(DEV), None, qkv)
+        # projection with the identity on a window-ordered tagged tensor
+        attn = torch.from_numpy(tagged(1, B * H * W, 1, C).reshape(B * H * W, C)).bfloat16().to(DEV)
+        out = torch.full((B, H, W, C), float("nan"), dtype=torch.bfloat16, device=DEV)
+        sw.swin_wattn_test_proj(h, attn, B, H, W, torch.eye(C).bfloat16().to(DEV), None, out)
+        assert sw.swin_wattn_sync_status(h) == sw.OK
+    finally:
+        sw.swin_wattn_destroy(h)
+    want_q = oracle.partition(oracle.roll(x, -s), M).reshape(B * H * W, C)
+    got = qkv.double().cpu().numpy()
+    assert np.array_equal(got[:, :C], want_q)
+    assert np.array_equal(got[:, C:], np.zeros((B * H * W, 2 * C)))
+    want_out = oracle.roll(oracle.reverse(attn.double().cpu().numpy().reshape(-1, M * M, C), B, H, W, M), s)
+    assert np.array_equal(out.double().cpu().numpy(), want_out)
+
+
+# ---- attention stage alone ------------------------------------------------------
+
+@pytest.mark.parametrize("key,B,H,W", [("swin_t_s1", 2, 14, 21), ("swinv2_t_s1", 1, 16, 24),
+                                       ("swinv2_l_w24", 1, 48, 72)])
+def test_attention_stage(key, B, H, W):
+    w = WORKLOADS[key].with_(B=B, H=H, W=W)
+    g = generate(w, nonzero_bias=True)
+    table = oracle_table(w, g)
+    t = device_inputs(g)
+    h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
+    try:
+        qkv = torch.empty(w.tokens, 3 * w.C, dtype=torch.bfloat16, device=DEV)
+        attn = torch.full((w.tokens, w.C), float("nan"), dtype=torch.bfloat16, device=DEV)
+        sw.swin_wattn_test_qkv(h, t["x"], t["Wqkv"], t["bqkv"], qkv)
+        sw.swin_wattn_test_attn(h, qkv, B, H, W, table.to(DEV), t.get("tau"), attn)
+        assert sw.swin_wattn_sync_status(h) == sw.OK
+    finally:
+        sw.swin_wattn_destroy(h)
+    # oracle o in window order: forward with Wproj = I, bproj = 0, then roll(-s) + partition
+    o_img = oracle_forward(w, g, table, Wproj=np.eye(w.C), bproj=None)
+    o_win = oracle.partition(oracle.roll(o_img, -w.shift), w.M).reshape(w.tokens, w.C)
+    compare(attn.double().cpu().numpy(), o_win, "bf16")
+
+
+# ---- whole block, small grids (several tiles, ragged tails) ----------------------
+
+SMALL = [
+    ("swin_t_s1", 2, 14, 21, False), ("swin_t_s1", 3, 7, 21, True),     # odd window count
+    ("swin_b_s1", 2, 28, 28, True), ("swin_b_s3", 3, 14, 14, False),
+    ("swinv2_t_s1", 2, 16, 24, True), ("swinv2_t_s1", 1, 8, 8, False),   # one window, mask everywhere
+    ("swinv2_l_w24", 1, 48, 48, True),
+]
+
+
+@pytest.mark.parametrize("key,B,H,W,bias", SMALL)
+def test_forward_small(key, B, H, W, bias):
+    w = WORKLOADS[key].with_(B=B, H=H, W=W)
+    g = generate(w, nonzero_bias=bias)
+    table = oracle_table(w, g)
+    out = run_forward(w, device_inputs(g), table.to(DEV))
+    compare(out.double().cpu().numpy(), oracle_forward(w, g, table), w.dtype)
+
+
+def test_forward_global_window_no_shift():
+    """M = H = W and s = 0: one window per image (plain attention with bias)."""
+    w = WORKLOADS["swinv2_t_s1"].with_(B=3, H=8, W=8, shift=0)
+    g = generate(w, nonzero_bias=True)
+    table = oracle_table(w, g)
+    out = run_forward(w, device_inputs(g), table.to(DEV))
+    compare(out.double().cpu().numpy(), oracle_forward(w, g, table), w.dtype)
+
+
+def test_tiny_fp32_workload():
+    w = WORKLOADS["tiny"]
+    for bias in (False, True):
+        g = generate(w, nonzero_bias=bias)
+        out = run_forward(w, device_inputs(g), g["table"].to(DEV))
+        compare(out.double().cpu().numpy(), oracle_forward(w, g, g["table"]), "fp32")
+
+
+def test_fp32_v2_small():
+    w = WORKLOADS["swinv2_t_s1"].with_(B=2, H=16, W=16, dtype="fp32")
+    g = generate(w, nonzero_bias=True)
+    table = oracle_table(w, g)
+    out = run_forward(w, device_inputs(g), table.to(DEV))
+    compare(out.double().cpu().numpy(), oracle_forward(w, g, table), "fp32")
+
+
+# ---- full-size workloads on sampled windows ------------------------------------
+
+@pytest.mark.parametrize("key", ["swin_t_s1", "swin_b_s1", "swin_b_s3", "swinv2_t_s1", "swinv2_l_w24"])
+def test_forward_full_size_sampled(key):
+    w = WORKLOADS[key]
+    g = generate(w)
+    table = oracle_table(w, g)
+    out = run_forward(w, device_inputs(g), table.to(DEV))
+    wins = sample_windows(w, 8 if w.M > 8 else 24)
+    ref = oracle_forward(w, g, table, windows=wins)
+    tok = window_tokens(w, wins)
+    got = out.double().cpu().numpy().reshape(-1, w.C)[tok]
+    compare(got, ref.reshape(-1, w.C)[tok], w.dtype)
+    assert torch.isfinite(out).all()
+
+
+# ---- meta-network G table ---------------------------------------------------------
+
+@pytest.mark.parametrize("key", ["swinv2_t_s1", "swinv2_l_w24"])
+def test_cpb_table(key):
+    w = WORKLOADS[key]
+    g = generate(w)
+    ref = oracle.cpb_table(to_f64(g["W1"]), to_f64(g["b1"]), to_f64(g["W2"]), M=w.M, heads=w.heads)
+    for fp32 in (True, False):
+        h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode | (sw.FP32 if fp32 else 0))
+        try:
+            dt = torch.float32 if fp32 else torch.bfloat16
+            tab = torch.full(((2 * w.M - 1) ** 2, w.heads), float("nan"), dtype=dt, device=DEV)
+            sw.swin_wattn_cpb_table(h, g["W1"].to(DEV), g["b1"].to(DEV), g["W2"].to(DEV), tab)
+            assert sw.swin_wattn_sync_status(h) == sw.OK
+        finally:
+            sw.swin_wattn_destroy(h)
+        got = tab.double().cpu().numpy()
+        if fp32:
+            assert np.max(np.abs(got - ref)) <= 1e-6 * max(1.0, np.abs(ref).max())
+        else:
+            assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-7)
+
+
+# ---- host-buffer entry point, edge cases, argument errors, watchdog ---------------
+
+def test_forward_host_matches_device_forward():
+    w = WORKLOADS["swin_t_s1"].with_(B=2, H=14, W=14)
+    g = generate(w, nonzero_bias=True)
+    t = device_inputs(g)
+    dev_out = run_forward(w, t, t["table"])
+    h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
+    try:
+        x_host = g["x"].pin_memory()
+        out_host = torch.empty_like(x_host).pin_memory()
+        sw.swin_wattn_forward_host(h, x_host, t["Wqkv"], t["bqkv"], t["table"], None, t["Wproj"], t["bproj"],
+                                   out_host)
+        assert sw.swin_wattn_sync_status(h) == sw.OK
+    finally:
+        sw.swin_wattn_destroy(h)
+    assert torch.equal(out_host, dev_out.cpu())
+
+
+def test_empty_batch_is_a_no_op():
+    w = WORKLOADS["swin_t_s1"]
+    h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
+    try:
+        buf = torch.zeros(3 * w.C * w.C, dtype=torch.bfloat16, device=DEV)
+        out = torch.zeros(16, dtype=torch.bfloat16, device=DEV)
+        p = ctypes.c_void_p(buf.data_ptr())
+        rc = sw.load().swin_wattn_forward(h, p, 0, 14, 14, p, None, p, None, p, None,
+                                          ctypes.c_void_p(out.data_ptr()), None)
+        assert rc == sw.OK
+        assert sw.swin_wattn_last_launches(h) == 0
+        assert sw.swin_wattn_sync_status(h) == sw.OK
+    finally:
+        sw.swin_wattn_destroy(h)
+
+
+def test_bad_forward_arguments_are_rejected():
+    w = WORKLOADS["swin_t_s1"].with_(B=1, H=14, W=14)
+    g = device_inputs(generate(w))
+    h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
+    try:
+        out = torch.empty_like(g["x"])
+
+        def fwd(**kw):
+            a = dict(x=g["x"], Wqkv=g["Wqkv"], bqkv=g["bqkv"], bias_table=g["table"], logit_scale=None,
+                     Wproj=g["Wproj"], bproj=g["bproj"], out=out)
+            a.update(kw)
+            with pytest.raises(sw.SwinWAttnError) as ei:
+                sw.swin_wattn_forward(h, **a)
+            return ei.value.code
+
+        assert fwd(x=torch.zeros(1, 15, 14, w.C, dtype=torch.bfloat16, device=DEV)) == sw.EINVAL  # H % M
+        assert fwd(out=g["x"]) == sw.EINVAL                                                      # aliasing
+        flat = torch.zeros(14 * 14 * w.C + 8, dtype=torch.bfloat16, device=DEV)
+        assert fwd(out=flat[1:1 + 14 * 14 * w.C].view(1, 14, 14, w.C)) == sw.EINVAL               # misaligned
+        assert fwd(bias_table=None) == sw.EINVAL
+        assert sw.swin_wattn_last_launches(h) == 0
+    finally:
+        sw.swin_wattn_destroy(h)
+    h2 = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, V2)
+    try:
+        with pytest.raises(sw.SwinWAttnError) as ei:   # V2 needs logit_scale
+            sw.swin_wattn_forward(h2, g["x"], g["Wqkv"], g["bqkv"], g["table"], None, g["Wproj"], g["bproj"], out)
+        assert ei.value.code == sw.EINVAL
+    finally:
+        sw.swin_wattn_destroy(h2)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    w = WORKLOADS["swin_t_s1"].with_(B=1, H=14, W=14)
+    h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
+    try:
+        sw.swin_wattn_set_option(h, sw.OPT_WAIT_LIMIT_US, 20000)
+        sw.swin_wattn_test_watchdog(h)
+        assert sw.swin_wattn_sync_status(h) == sw.ETIMEOUT
+        assert sw.swin_wattn_sync_status(h) == sw.OK   # cleared
+    finally:
+        sw.swin_wattn_destroy(h)
+    g = generate(w, nonzero_bias=True)
+    out = run_forward(w, device_inputs(g), g["table"].to(DEV))
+    compare(out.double().cpu().numpy(), oracle_forward(w, g, g["table"]), "bf16")

@@ -1,0 +1,335 @@
+// C ABI of libswin_wattn: argument checks, path choice, workspace, launches.
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/swin_wattn.h"
+#include "../../include/swin_wattn_test.h"
+#include "common.cuh"
+
+using namespace swin;
+
+struct swin_wattn_s {
+    int C, heads, d, M, shift, mode;
+    bool fp32;
+    int path_opt;
+    uint64_t wait_ns;
+    int device;
+    int *d_err;
+    void *ws;          // three-kernel workspace: qkv [T,3C] then attn [T,C] (bf16)
+    size_t ws_bytes;
+    void *stage_x, *stage_out; // device staging of swin_wattn_forward_host
+    size_t stage_bytes;
+    int last_launches;
+};
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SWIN_WATTN_OK : SWIN_WATTN_ECUDA; }
+
+size_t elem_bytes(const swin_wattn_s *h) { return h->fp32 ? 4 : 2; }
+
+// Shape checks shared by every entry point that takes B, H, W.
+int check_grid(const swin_wattn_s *h, int B, int H, int W)
+{
+    if (B < 0 || H <= 0 || W <= 0) return SWIN_WATTN_EINVAL;
+    if (H % h->M || W % h->M) return SWIN_WATTN_EINVAL;
+    if ((int64_t)B * H * W * h->C > (int64_t)1 << 40) return SWIN_WATTN_EINVAL;
+    return SWIN_WATTN_OK;
+}
+
+int choose_path(const swin_wattn_s *h)
+{
+    if (h->fp32) return 3;
+    return 1;
+}
+
+int ensure_buffer(void **buf, size_t *have, size_t need)
+{
+    if (*have >= need) return SWIN_WATTN_OK;
+    if (*buf) {
+        cudaFree(*buf);
+        *buf = nullptr;
+        *have = 0;
+    }
+    if (cudaMalloc(buf, need) != cudaSuccess) {
+        *buf = nullptr;
+        cudaGetLastError();
+        return SWIN_WATTN_ENOMEM;
+    }
+    *have = need;
+    return SWIN_WATTN_OK;
+}
+
+DeviceStatus dstatus(const swin_wattn_s *h) { return DeviceStatus{h->d_err, h->wait_ns}; }
+
+int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
+                const void *table, const float *tau, const void *Wproj, const void *bproj, void *out,
+                cudaStream_t stream)
+{
+    const Geom g = make_geom(B, H, W, h->C, h->M, h->shift);
+    h->last_launches = 0;
+    if (B == 0) return SWIN_WATTN_OK;
+    const int path = h->path_opt ? h->path_opt : choose_path(h);
+    if (h->fp32) {
+        Fp32Args a;
+        a.x = (const float *)x; a.Wqkv = (const float *)Wqkv; a.bqkv = (const float *)bqkv;
+        a.table = (const float *)table; a.tau = tau; a.Wproj = (const float *)Wproj; a.bproj = (const float *)bproj;
+        a.out = (float *)out; a.heads = h->heads; a.mode = h->mode; a.g = g;
+        cudaError_t e = launch_fp32_block(a, stream);
+        if (e == cudaErrorInvalidConfiguration) return SWIN_WATTN_EUNSUPPORTED;
+        h->last_launches = 1;
+        return cuda_status(e);
+    }
+    if (path != 1) return SWIN_WATTN_EUNSUPPORTED;
+    const size_t qkv_bytes = (size_t)g.T * 3 * h->C * 2, attn_bytes = (size_t)g.T * h->C * 2;
+    int rc = ensure_buffer(&h->ws, &h->ws_bytes, qkv_bytes + attn_bytes);
+    if (rc) return rc;
+    bf16 *qkv = (bf16 *)h->ws;
+    bf16 *attn = (bf16 *)((char *)h->ws + qkv_bytes);
+    GemmArgs k1{};
+    k1.A = (const bf16 *)x; k1.lda = h->C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
+    k1.D = qkv; k1.ldd = 3 * h->C; k1.rows = g.T; k1.N = 3 * h->C; k1.K = h->C; k1.g = g;
+    cudaError_t e = launch_gemm(k1, LOAD_GATHER, STORE_PLAIN, dstatus(h), stream);
+    if (e != cudaSuccess) return SWIN_WATTN_ECUDA;
+    AttnArgs k2{};
+    k2.qkv = qkv; k2.attn = attn; k2.table = (const bf16 *)table; k2.tau = tau; k2.heads = h->heads;
+    k2.mode = h->mode; k2.g = g;
+    e = launch_attention(k2, dstatus(h), stream);
+    if (e != cudaSuccess) return SWIN_WATTN_ECUDA;
+    GemmArgs k3{};
+    k3.A = attn; k3.lda = h->C; k3.Bw = (const bf16 *)Wproj; k3.bias = (const bf16 *)bproj;
+    k3.D = (bf16 *)out; k3.ldd = h->C; k3.rows = g.T; k3.N = h->C; k3.K = h->C; k3.g = g;
+    e = launch_gemm(k3, LOAD_PLAIN, STORE_SCATTER, dstatus(h), stream);
+    if (e != cudaSuccess) return SWIN_WATTN_ECUDA;
+    h->last_launches = 3;
+    return SWIN_WATTN_OK;
+}
+
+int check_forward_args(const swin_wattn_s *h, const void *x, int B, int H, int W, const void *Wqkv,
+                       const void *bqkv, const void *table, const float *tau, const void *Wproj, const void *bproj,
+                       const void *out, bool device_io)
+{
+    if (!h || !x || !Wqkv || !table || !Wproj || !out) return SWIN_WATTN_EINVAL;
+    if (h->mode == SWIN_WATTN_V2 && !tau) return SWIN_WATTN_EINVAL;
+    int rc = check_grid(h, B, H, W);
+    if (rc) return rc;
+    const void *dev_ptrs[] = {Wqkv, bqkv, table, tau, Wproj, bproj};
+    for (const void *p : dev_ptrs)
+        if (p && !aligned16(p)) return SWIN_WATTN_EINVAL;
+    if (device_io) {
+        if (!aligned16(x) || !aligned16(out)) return SWIN_WATTN_EINVAL;
+        const size_t bytes = (size_t)B * H * W * h->C * elem_bytes(h);
+        const char *xa = (const char *)x, *oa = (const char *)out;
+        if (bytes && xa < oa + bytes && oa < xa + bytes) return SWIN_WATTN_EINVAL;
+    }
+    return SWIN_WATTN_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+int swin_wattn_create(swin_wattn_t *out, int C, int heads, int M, int shift, int mode)
+{
+    if (!out) return SWIN_WATTN_EINVAL;
+    *out = nullptr;
+    if (C <= 0 || heads <= 0 || M <= 0 || C % heads) return SWIN_WATTN_EINVAL;
+    if (shift < 0 || shift >= M) return SWIN_WATTN_EINVAL;
+    if (mode & ~(SWIN_WATTN_V2 | SWIN_WATTN_FP32)) return SWIN_WATTN_EINVAL;
+    const bool fp32 = (mode & SWIN_WATTN_FP32) != 0;
+    const int d = C / heads;
+    if (!fp32 && (d != 32 || C % 32)) return SWIN_WATTN_EUNSUPPORTED;
+    if (!fp32 && M > 64) return SWIN_WATTN_EUNSUPPORTED;
+    if (fp32 && fp32_block_smem_bytes(M * M, C) > 200 * 1024) return SWIN_WATTN_EUNSUPPORTED;
+    swin_wattn_s *h = new (std::nothrow) swin_wattn_s();
+    if (!h) return SWIN_WATTN_ENOMEM;
+    h->C = C; h->heads = heads; h->d = d; h->M = M; h->shift = shift;
+    h->mode = mode & SWIN_WATTN_V2; h->fp32 = fp32;
+    h->path_opt = 0;
+    h->wait_ns = 2000000000ull;
+    if (cudaGetDevice(&h->device) != cudaSuccess) { delete h; cudaGetLastError(); return SWIN_WATTN_ECUDA; }
+    if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess) { delete h; cudaGetLastError(); return SWIN_WATTN_ENOMEM; }
+    if (cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess) { cudaFree(h->d_err); delete h; return SWIN_WATTN_ECUDA; }
+    *out = h;
+    return SWIN_WATTN_OK;
+}
+
+int swin_wattn_destroy(swin_wattn_t h)
+{
+    if (!h) return SWIN_WATTN_OK;
+    cudaDeviceSynchronize();
+    if (h->ws) cudaFree(h->ws);
+    if (h->stage_x) cudaFree(h->stage_x);
+    if (h->stage_out) cudaFree(h->stage_out);
+    if (h->d_err) cudaFree(h->d_err);
+    delete h;
+    return SWIN_WATTN_OK;
+}
+
+int swin_wattn_forward(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
+                       const void *bias_table, const float *logit_scale, const void *Wproj, const void *bproj,
+                       void *out, swin_stream_t stream)
+{
+    int rc = check_forward_args(h, x, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out, true);
+    if (rc) return rc;
+    return run_forward(h, x, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out, (cudaStream_t)stream);
+}
+
+int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, int W, const void *Wqkv,
+                            const void *bqkv, const void *bias_table, const float *logit_scale, const void *Wproj,
+                            const void *bproj, void *out_host, swin_stream_t stream)
+{
+    int rc = check_forward_args(h, x_host, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out_host,
+                                false);
+    if (rc) return rc;
+    const size_t bytes = (size_t)B * H * W * h->C * elem_bytes(h);
+    if (bytes == 0) return SWIN_WATTN_OK;
+    if (h->stage_bytes < bytes) {
+        size_t have_x = h->stage_bytes, have_o = h->stage_bytes;
+        rc = ensure_buffer(&h->stage_x, &have_x, bytes);
+        if (!rc) rc = ensure_buffer(&h->stage_out, &have_o, bytes);
+        if (rc) return rc;
+        h->stage_bytes = bytes;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(h->stage_x, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    rc = run_forward(h, h->stage_x, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, h->stage_out, s);
+    if (rc) return rc;
+    if (cudaMemcpyAsync(out_host, h->stage_out, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    return SWIN_WATTN_OK;
+}
+
+int swin_wattn_cpb_table(swin_wattn_t h, const float *W1, const float *b1, const float *W2, int hidden, void *table,
+                         swin_stream_t stream)
+{
+    if (!h || !W1 || !W2 || !table || hidden <= 0 || hidden > 4096) return SWIN_WATTN_EINVAL;
+    return cuda_status(launch_cpb_table(W1, b1, W2, hidden, h->M, h->heads, !h->fp32, table, (cudaStream_t)stream));
+}
+
+int swin_wattn_sync_status(swin_wattn_t h, swin_stream_t stream)
+{
+    if (!h) return SWIN_WATTN_EINVAL;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    int err = 0;
+    if (cudaMemcpy(&err, h->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    if (err) {
+        if (cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess) return SWIN_WATTN_ECUDA;
+        if (err & ERR_TIMEOUT) return SWIN_WATTN_ETIMEOUT;
+    }
+    return SWIN_WATTN_OK;
+}
+
+int swin_wattn_set_option(swin_wattn_t h, int option, int64_t value)
+{
+    if (!h) return SWIN_WATTN_EINVAL;
+    switch (option) {
+    case SWIN_WATTN_OPT_PATH:
+        if (value < 0 || value > 2) return SWIN_WATTN_EINVAL;
+        h->path_opt = (int)value;
+        return SWIN_WATTN_OK;
+    case SWIN_WATTN_OPT_WAIT_LIMIT_US:
+        if (value <= 0 || value > 60000000) return SWIN_WATTN_EINVAL;
+        h->wait_ns = (uint64_t)value * 1000ull;
+        return SWIN_WATTN_OK;
+    default:
+        return SWIN_WATTN_EINVAL;
+    }
+}
+
+int swin_wattn_path(swin_wattn_t h, int B, int H, int W)
+{
+    if (!h) return SWIN_WATTN_EINVAL;
+    int rc = check_grid(h, B, H, W);
+    if (rc) return rc;
+    if (h->fp32) return 3;
+    const int path = h->path_opt ? h->path_opt : choose_path(h);
+    return path == 1 ? 1 : SWIN_WATTN_EUNSUPPORTED;
+}
+
+int swin_wattn_last_launches(swin_wattn_t h) { return h ? h->last_launches : 0; }
+
+const char *swin_wattn_strerror(int code)
+{
+    switch (code) {
+    case SWIN_WATTN_OK: return "ok";
+    case SWIN_WATTN_EINVAL: return "invalid argument";
+    case SWIN_WATTN_EUNSUPPORTED: return "unsupported shape for the compiled kernels";
+    case SWIN_WATTN_ECUDA: return "CUDA runtime error";
+    case SWIN_WATTN_ENOMEM: return "device allocation failed";
+    case SWIN_WATTN_ETIMEOUT: return "a kernel gave up a bounded wait";
+    default: return "unknown status";
+    }
+}
+
+// ---- stage hooks ------------------------------------------------------------
+
+int swin_wattn_test_qkv(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
+                        void *qkv, swin_stream_t stream)
+{
+    if (!h || !x || !Wqkv || !qkv || h->fp32) return SWIN_WATTN_EINVAL;
+    int rc = check_grid(h, B, H, W);
+    if (rc) return rc;
+    if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(qkv) || (bqkv && !aligned16(bqkv))) return SWIN_WATTN_EINVAL;
+    if (B == 0) return SWIN_WATTN_OK;
+    const Geom g = make_geom(B, H, W, h->C, h->M, h->shift);
+    GemmArgs k1{};
+    k1.A = (const bf16 *)x; k1.lda = h->C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
+    k1.D = (bf16 *)qkv; k1.ldd = 3 * h->C; k1.rows = g.T; k1.N = 3 * h->C; k1.K = h->C; k1.g = g;
+    return cuda_status(launch_gemm(k1, LOAD_GATHER, STORE_PLAIN, dstatus(h), (cudaStream_t)stream));
+}
+
+int swin_wattn_test_attn(swin_wattn_t h, const void *qkv, int B, int H, int W, const void *bias_table,
+                         const float *logit_scale, void *attn, swin_stream_t stream)
+{
+    if (!h || !qkv || !bias_table || !attn || h->fp32) return SWIN_WATTN_EINVAL;
+    if (h->mode == SWIN_WATTN_V2 && !logit_scale) return SWIN_WATTN_EINVAL;
+    int rc = check_grid(h, B, H, W);
+    if (rc) return rc;
+    if (!aligned16(qkv) || !aligned16(attn)) return SWIN_WATTN_EINVAL;
+    if (B == 0) return SWIN_WATTN_OK;
+    AttnArgs k2{};
+    k2.qkv = (const bf16 *)qkv; k2.attn = (bf16 *)attn; k2.table = (const bf16 *)bias_table; k2.tau = logit_scale;
+    k2.heads = h->heads; k2.mode = h->mode; k2.g = make_geom(B, H, W, h->C, h->M, h->shift);
+    return cuda_status(launch_attention(k2, dstatus(h), (cudaStream_t)stream));
+}
+
+int swin_wattn_test_proj(swin_wattn_t h, const void *attn, int B, int H, int W, const void *Wproj, const void *bproj,
+                         void *out, swin_stream_t stream)
+{
+    if (!h || !attn || !Wproj || !out || h->fp32) return SWIN_WATTN_EINVAL;
+    int rc = check_grid(h, B, H, W);
+    if (rc) return rc;
+    if (!aligned16(attn) || !aligned16(Wproj) || !aligned16(out) || (bproj && !aligned16(bproj))) return SWIN_WATTN_EINVAL;
+    if (B == 0) return SWIN_WATTN_OK;
+    const Geom g = make_geom(B, H, W, h->C, h->M, h->shift);
+    GemmArgs k3{};
+    k3.A = (const bf16 *)attn; k3.lda = h->C; k3.Bw = (const bf16 *)Wproj; k3.bias = (const bf16 *)bproj;
+    k3.D = (bf16 *)out; k3.ldd = h->C; k3.rows = g.T; k3.N = h->C; k3.K = h->C; k3.g = g;
+    return cuda_status(launch_gemm(k3, LOAD_PLAIN, STORE_SCATTER, dstatus(h), (cudaStream_t)stream));
+}
+
+int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *D, int rows, int N, int K,
+                         swin_stream_t stream)
+{
+    if (!A || !Bw || !D || rows < 0 || N <= 0 || K <= 0 || N % 16 || K % 16 || N > 2048) return SWIN_WATTN_EINVAL;
+    if (!aligned16(A) || !aligned16(Bw) || !aligned16(D) || (bias && !aligned16(bias))) return SWIN_WATTN_EINVAL;
+    if (rows == 0) return SWIN_WATTN_OK;
+    GemmArgs a{};
+    a.A = (const bf16 *)A; a.lda = K; a.Bw = (const bf16 *)Bw; a.bias = (const bf16 *)bias;
+    a.D = (bf16 *)D; a.ldd = N; a.rows = rows; a.N = N; a.K = K;
+    // the hook has no handle: its error word is a private one, never read
+    static int *d_err = nullptr;
+    if (!d_err && cudaMalloc(&d_err, sizeof(int)) != cudaSuccess) return SWIN_WATTN_ENOMEM;
+    return cuda_status(launch_gemm(a, LOAD_PLAIN, STORE_PLAIN, DeviceStatus{d_err, 2000000000ull}, (cudaStream_t)stream));
+}
+
+int swin_wattn_test_watchdog(swin_wattn_t h, swin_stream_t stream)
+{
+    if (!h) return SWIN_WATTN_EINVAL;
+    return cuda_status(launch_watchdog(dstatus(h), (cudaStream_t)stream));
+}
+
+} // extern "C"

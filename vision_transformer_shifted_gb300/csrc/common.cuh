@@ -1,0 +1,117 @@
+// Internal declarations shared by the kernels and the C ABI of libswin_wattn.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace swin {
+
+using bf16 = __nv_bfloat16;
+
+// Geometry of one forward call: a [B, H, W, C] token grid cut into M x M
+// windows after a cyclic shift by -s.
+struct Geom {
+    int B, H, W, C, M, s;
+    int nh, nw, N; // windows per column / row, tokens per window
+    int64_t T;     // B*H*W tokens
+    int64_t nwin;  // B*nh*nw windows
+};
+
+inline Geom make_geom(int B, int H, int W, int C, int M, int s)
+{
+    Geom g;
+    g.B = B; g.H = H; g.W = W; g.C = C; g.M = M; g.s = s;
+    g.nh = H / M; g.nw = W / M; g.N = M * M;
+    g.T = (int64_t)B * H * W;
+    g.nwin = (int64_t)B * g.nh * g.nw;
+    return g;
+}
+
+// Window-order row r = win*N + t (win = (b*nh + wi)*nw + wj, t = ti*M + tj)
+// -> token index b*H*W + i*W + j of its place in the original frame, where
+// (i, j) = (wi*M+ti+s mod H, wj*M+tj+s mod W).  The cyclic shift by -s reads
+// the token at (i+s, j+s) into shifted position (i, j); the window reverse
+// followed by the roll by +s writes the result back to that same place, so
+// one map serves the gather in front of the QKV projection and the scatter
+// behind the output projection.
+__device__ __forceinline__ int64_t window_row_to_token(const Geom &g, int64_t r)
+{
+    const int64_t win = r / g.N;
+    const int t = (int)(r - win * g.N);
+    const int per = g.nh * g.nw;
+    const int b = (int)(win / per);
+    const int rem = (int)(win - (int64_t)b * per);
+    const int wi = rem / g.nw, wj = rem - (rem / g.nw) * g.nw;
+    const int ti = t / g.M, tj = t - (t / g.M) * g.M;
+    int i = wi * g.M + ti + g.s;
+    if (i >= g.H) i -= g.H;
+    int j = wj * g.M + tj + g.s;
+    if (j >= g.W) j -= g.W;
+    return ((int64_t)b * g.H + i) * g.W + j;
+}
+
+// Band of a shifted-frame coordinate p on an axis of length n (shift s > 0):
+// 0 for [0, n-M), 1 for [n-M, n-s), 2 for [n-s, n).  Pairs of tokens whose
+// (row band, column band) differ are masked.
+__device__ __forceinline__ int shift_band(int p, int n, int M, int s)
+{
+    return p < n - M ? 0 : (p < n - s ? 1 : 2);
+}
+
+// Device error word bits.
+enum : int { ERR_TIMEOUT = 1 };
+
+struct DeviceStatus {
+    int *err;          // device error word (atomicOr of ERR_* bits)
+    uint64_t wait_ns;  // limit of every bounded wait
+};
+
+// ---- kernel launchers (return cudaSuccess or the error) ----------------------
+
+enum { LOAD_PLAIN = 0, LOAD_GATHER = 1 };
+enum { STORE_PLAIN = 0, STORE_SCATTER = 1 };
+
+struct GemmArgs {
+    const bf16 *A;   // LOAD_PLAIN: [rows, lda]; LOAD_GATHER: x [B, H, W, K]
+    int64_t lda;
+    const bf16 *Bw;  // [N, K] row-major
+    const bf16 *bias; // [N] or null
+    bf16 *D;         // STORE_PLAIN: [rows, ldd]; STORE_SCATTER: out [B, H, W, N]
+    int64_t ldd;
+    int64_t rows;
+    int N, K;
+    Geom g;          // index maps of LOAD_GATHER / STORE_SCATTER
+};
+
+cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, DeviceStatus st,
+                        cudaStream_t stream);
+
+struct AttnArgs {
+    const bf16 *qkv;      // [T, 3C] window order
+    bf16 *attn;           // [T, C] window order
+    const bf16 *table;    // [(2M-1)^2, heads]
+    const float *tau;     // [heads] (V2)
+    int heads, mode;      // mode 0 = V1, 1 = V2
+    Geom g;
+};
+
+cudaError_t launch_attention(const AttnArgs &a, DeviceStatus st, cudaStream_t stream);
+
+struct Fp32Args {
+    const float *x, *Wqkv, *bqkv, *table, *tau, *Wproj, *bproj;
+    float *out;
+    int heads, mode;
+    Geom g;
+};
+
+// fp32 block, one CTA per window; returns cudaErrorInvalidConfiguration if
+// the window does not fit in shared memory.
+cudaError_t launch_fp32_block(const Fp32Args &a, cudaStream_t stream);
+size_t fp32_block_smem_bytes(int N, int C);
+
+cudaError_t launch_cpb_table(const float *W1, const float *b1, const float *W2, int hidden, int M,
+                             int heads, bool out_bf16, void *table, cudaStream_t stream);
+
+cudaError_t launch_watchdog(DeviceStatus st, cudaStream_t stream);
+
+} // namespace swin

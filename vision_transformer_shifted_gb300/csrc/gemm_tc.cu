@@ -1,0 +1,221 @@
+// Tensor-core GEMM of the block's two projections, tcgen05 + TMEM on sm_103a.
+//
+//   D[r, n] = sum_k A[r, k] * Bw[n, k] + bias[n]      (bf16 in, fp32 accumulate)
+//
+// QKV projection ("Boosting Swin Transformer Speed", Inference Optimization:
+// QKV GEMM fused with its bias, no separate transpose): the A rows are read
+// straight from x through the cyclic-shift + window-partition map (Training
+// Optimization: the partition/shift index maps), so no partitioned copy of x
+// is ever written.  Output projection: the epilogue writes each row through
+// the window-reverse + roll(+s) map into the original [B, H, W, C] layout.
+//
+// Tile: 128 rows x BN columns (BN <= 256, multiple of 16), K in blocks of 64
+// (one 128-byte swizzle atom per row), a 3-stage cp.async ring into the
+// K-major 128B-swizzled layout, one thread issuing tcgen05.mma, the fp32
+// accumulator in TMEM, and a 4-warp epilogue reading one TMEM lane (= one
+// output row) per thread.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace swin {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 3;
+constexpr int THREADS = 128;
+
+struct GemmSmem {
+    // dynamic layout: [A stages][B stages] (1024-aligned), then row offsets,
+    // bias, barriers and the TMEM address.
+    static constexpr int a_stage = BM * BK * 2; // 16 KB
+    static size_t bytes(int BN)
+    {
+        return 1024 + (size_t)STAGES * (a_stage + BN * BK * 2) + BM * sizeof(int64_t) + 256 * sizeof(float) +
+               STAGES * 8 + 8 + 16;
+    }
+};
+
+__device__ __forceinline__ void store_row_bf16(bf16 *dst, const float *v, const float *bias, int n)
+{
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    for (int q = 0; q < n / 8; ++q) {
+        uint4 u;
+        u.x = pack_bf16x2(v[8 * q + 0] + bias[8 * q + 0], v[8 * q + 1] + bias[8 * q + 1]);
+        u.y = pack_bf16x2(v[8 * q + 2] + bias[8 * q + 2], v[8 * q + 3] + bias[8 * q + 3]);
+        u.z = pack_bf16x2(v[8 * q + 4] + bias[8 * q + 4], v[8 * q + 5] + bias[8 * q + 5]);
+        u.w = pack_bf16x2(v[8 * q + 6] + bias[8 * q + 6], v[8 * q + 7] + bias[8 * q + 7]);
+        d4[q] = u;
+    }
+}
+
+template <int LOAD, int STORE>
+__global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, DeviceStatus st)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int b_stage = BN * BK * 2;
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * GemmSmem::a_stage;
+    int64_t *row_off = reinterpret_cast<int64_t *>(sB + STAGES * b_stage);
+    float *sbias = reinterpret_cast<float *>(row_off + BM);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbias + 256);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + STAGES + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t m0 = (int64_t)blockIdx.x * BM;
+    const int n0 = blockIdx.y * BN;
+    const int KB = (a.K + BK - 1) / BK;
+    const uint32_t tmem_cols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+
+    // source offset (elements) of each tile row; -1 past the end
+    for (int r = tid; r < BM; r += THREADS) {
+        const int64_t R = m0 + r;
+        int64_t off = -1;
+        if (R < a.rows) off = LOAD == LOAD_GATHER ? window_row_to_token(a.g, R) * a.K : R * a.lda;
+        row_off[r] = off;
+    }
+    for (int n = tid; n < BN; n += THREADS) sbias[n] = a.bias ? __bfloat162float(a.bias[n0 + n]) : 0.f;
+    if (tid == 0) {
+        for (int s = 0; s < STAGES + 1; ++s) mbar_init(smem_u32(&bars[s]), 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto load_stage = [&](int kb, int s) {
+        const uint32_t a_base = smem_u32(sA + s * GemmSmem::a_stage);
+        const uint32_t b_base = smem_u32(sB + s * b_stage);
+        const int c = tid & 7;
+        const int k0 = kb * BK + c * 8;
+        const bool kin = k0 < a.K;
+#pragma unroll
+        for (int i = 0; i < BM / 16; ++i) {
+            const int r = (tid >> 3) + 16 * i;
+            const int64_t off = row_off[r];
+            const bool ok = kin && off >= 0;
+            const bf16 *src = ok ? a.A + off + k0 : a.A;
+            cp_async16(a_base + sw128_offset(r, c), src, ok ? 16u : 0u);
+        }
+        for (int n = tid >> 3; n < BN; n += 16) {
+            const bf16 *src = kin ? a.Bw + (int64_t)(n0 + n) * a.K + k0 : a.Bw;
+            cp_async16(b_base + sw128_offset(n, c), src, kin ? 16u : 0u);
+        }
+    };
+
+    const uint32_t idesc = idesc_bf16(BM, BN);
+    bool failed = false;
+
+#pragma unroll 1
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < KB) load_stage(s, s);
+        cp_async_commit();
+    }
+#pragma unroll 1
+    for (int kb = 0; kb < KB; ++kb) {
+        const int nk = kb + STAGES - 1;
+        if (nk < KB) {
+            // stage nk % STAGES was last read by the MMAs of block kb - 1
+            if (kb >= 1 && !failed) {
+                const int pk = kb - 1;
+                if (!mbar_wait(smem_u32(&bars[pk % STAGES]), (pk / STAGES) & 1, st.wait_ns)) failed = true;
+            }
+            if (!failed) load_stage(nk, nk % STAGES);
+        }
+        cp_async_commit();
+        cp_async_wait<STAGES - 1>();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(failed)) { failed = true; break; }
+        tc_fence_after();
+        if (tid == 0) {
+            const int s = kb % STAGES;
+            const uint32_t a_base = smem_u32(sA + s * GemmSmem::a_stage);
+            const uint32_t b_base = smem_u32(sB + s * b_stage);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+                if (kb * BK + k * 16 < a.K)
+                    mma_bf16(tmem, desc_kmajor_sw128(a_base + 32 * k), desc_kmajor_sw128(b_base + 32 * k), idesc,
+                             (kb | k) != 0);
+            }
+            mma_commit(smem_u32(&bars[s]));
+        }
+    }
+    cp_async_wait<0>();
+    if (!failed) {
+        const int lk = KB - 1;
+        if (!mbar_wait(smem_u32(&bars[lk % STAGES]), (lk / STAGES) & 1, st.wait_ns)) failed = true;
+    }
+    if (__syncthreads_or(failed)) failed = true;
+    tc_fence_after();
+
+    if (!failed) {
+        const int r = warp * 32 + lane;
+        const int64_t R = m0 + r;
+        bf16 *dst_row = nullptr;
+        if (R < a.rows) {
+            if (STORE == STORE_SCATTER) dst_row = a.D + window_row_to_token(a.g, R) * (int64_t)a.N + n0;
+            else dst_row = a.D + R * a.ldd + n0;
+        }
+        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        int c0 = 0;
+        for (; c0 + 32 <= BN; c0 += 32) {
+            float v[32];
+            tmem_ld32(t_lane + c0, v);
+            tmem_wait_ld();
+            if (dst_row) store_row_bf16(dst_row + c0, v, sbias + c0, 32);
+        }
+        if (c0 < BN) { // 16-column tail
+            float v[16];
+            tmem_ld16(t_lane + c0, v);
+            tmem_wait_ld();
+            if (dst_row) store_row_bf16(dst_row + c0, v, sbias + c0, 16);
+        }
+    } else if (tid == 0) {
+        atomicOr(st.err, ERR_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, tmem_cols);
+}
+
+// Largest N tile <= 256 that divides N and is a multiple of 16.
+int pick_bn(int N)
+{
+    for (int bn = 256; bn >= 16; bn -= 16)
+        if (N % bn == 0) return bn;
+    return 0;
+}
+
+template <int LOAD, int STORE>
+cudaError_t launch_impl(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
+{
+    const int BN = pick_bn(a.N);
+    if (BN == 0 || a.K % 16 != 0 || a.rows <= 0) return cudaErrorInvalidValue;
+    const size_t smem = GemmSmem::bytes(BN);
+    auto kern = gemm_tc_kernel<LOAD, STORE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)((a.rows + BM - 1) / BM), (unsigned)(a.N / BN));
+    kern<<<grid, THREADS, smem, stream>>>(a, BN, st);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, DeviceStatus st, cudaStream_t stream)
+{
+    if (load_mode == LOAD_GATHER && store_mode == STORE_PLAIN) return launch_impl<LOAD_GATHER, STORE_PLAIN>(a, st, stream);
+    if (load_mode == LOAD_PLAIN && store_mode == STORE_SCATTER) return launch_impl<LOAD_PLAIN, STORE_SCATTER>(a, st, stream);
+    if (load_mode == LOAD_PLAIN && store_mode == STORE_PLAIN) return launch_impl<LOAD_PLAIN, STORE_PLAIN>(a, st, stream);
+    return cudaErrorInvalidValue;
+}
+
+} // namespace swin
