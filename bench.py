@@ -1,0 +1,397 @@
+"""Throughput of the Swin shifted-window attention block on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one forward of the whole block (cyclic shift, partition, QKV
+projection, windowed attention with relative bias and shift mask, softmax,
+P.V, reverse, roll back, output projection) over one batch of synthetic
+inputs already resident in HBM.  Default workload: the Swin-T stage-1 shifted
+block (B=64, 56x56 tokens, C=96, 3 heads, M=7, s=3, bf16, V1).  Inputs are
+rotated over several buffer sets whose total exceeds twice the L2, so no step
+reads what the previous one left in L2.  Multi-GPU: one process per GPU
+(torchrun), each rank runs its own batch (weak scaling, no collective in the
+data path), times are the max over ranks.
+
+Prints one JSON line: tokens/s (value), TFLOP/s, the roofline of the dominant
+kernel (CUDA events inside this run), the whole block's roofline fraction, the
+end-to-end number through swin_wattn_forward_host (pinned host buffers, copies
+inside the timed region), the clocks seen during the run, and the float64
+oracle timed on the host cores on a bounded sample (cpu_baseline).
+--impl reference times that oracle alone as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from vision_transformer_shifted_gb300.inputs import V2, WORKLOADS, generate  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "fused shifted-window attn block tokens/s & TFLOP/s; % of bf16/HBM roofline"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sust=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(v, dist):
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample_rate(w, g, table_np, seconds=10.0, threads=None):
+    """Tokens/s of the float64 oracle on a bounded sample of windows."""
+    import oracle
+    a = {k: (v.double().numpy() if v is not None else None) for k, v in g.items()}
+    threads = threads or len(os.sched_getaffinity(0))
+    rng = np.random.default_rng(0)
+    n = max(threads, 4)
+    done_windows, elapsed = 0, 0.0
+    while elapsed < seconds:
+        wins = rng.integers(0, w.n_windows, size=n)
+        t0 = time.perf_counter()
+        oracle.forward(a["x"], a["Wqkv"], a["bqkv"], table_np, a.get("tau"), a["Wproj"], a["bproj"],
+                       heads=w.heads, M=w.M, shift=w.shift, mode=w.mode, windows=wins, nthreads=threads)
+        dt = time.perf_counter() - t0
+        done_windows += n
+        elapsed += dt
+        if dt < seconds / 8:
+            n *= 2
+    return done_windows * w.N / elapsed, threads, done_windows
+
+
+def table_for(w, g, dev, h=None):
+    """Relative-bias table: V1 draws it; V2 builds it on the GPU with the
+    meta-network kernel (swin_wattn_cpb_table), as a user would once."""
+    from vision_transformer_shifted_gb300 import binding as sw
+    if w.mode != V2:
+        return g["table"].to(dev)
+    tab = torch.empty(((2 * w.M - 1) ** 2, w.heads), dtype=torch.bfloat16 if w.dtype == "bf16" else torch.float32,
+                      device=dev)
+    sw.swin_wattn_cpb_table(h, g["W1"].to(dev), g["b1"].to(dev), g["W2"].to(dev), tab)
+    return tab
+
+
+def run_reference(args, w):
+    rank, world, local, dist = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    import oracle
+    g = generate(w)
+    if w.mode == V2:
+        table = oracle.cpb_table(g["W1"].double().numpy(), g["b1"].double().numpy(), g["W2"].double().numpy(),
+                                 M=w.M, heads=w.heads)
+    else:
+        table = g["table"].double().numpy()
+    per_step = []
+    threads = len(os.sched_getaffinity(0))
+    # each step is a bounded sample, sized so the whole run stays near 2.5 minutes
+    step_s = max(0.2, min(args.ref_seconds, 150.0 / (args.steps + args.warmup)))
+    for _ in range(args.warmup + args.steps):
+        rate, threads, nw = oracle_sample_rate(w, g, table, seconds=step_s, threads=threads)
+        per_step.append(rate)
+    rate = statistics.median(per_step[args.warmup:])
+    line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.tokens / rate * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": w.C, "heads": w.heads, "M": w.M,
+                       "shift": w.shift, "mode": "V2" if w.mode == V2 else "V1"},
+            "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": "random windows per step, about %.2f s of float64 CPU work each; "
+                                       "tokens/s scaled from the windows done" % step_s},
+            "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    from vision_transformer_shifted_gb300 import binding as sw
+    rank, world, local, dist = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    sw.load()
+    pk = peaks()
+    mode = w.mode | (sw.FP32 if w.dtype == "fp32" else 0)
+    h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, mode)
+    if args.path:
+        sw.swin_wattn_set_option(h, sw.OPT_PATH, args.path)
+    g = generate(w.with_(seed=w.seed + rank))
+    t = {k: (v.to(dev) if v is not None else None) for k, v in g.items()}
+    table = table_for(w, g, dev, h)
+    io_bytes = w.tokens * w.C * w.elem_bytes * 2
+    nsets = max(2, -(-(2 * L2_BYTES) // io_bytes) + 1)
+    xs = [t["x"]] + [torch.randn_like(t["x"], dtype=torch.float32).to(t["x"].dtype) for _ in range(nsets - 1)]
+    outs = [torch.empty_like(t["x"]) for _ in range(nsets)]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        k = i % nsets
+        sw.swin_wattn_forward(h, xs[k], t["Wqkv"], t["bqkv"], table, t.get("tau"), t["Wproj"], t["bproj"],
+                              outs[k], stream)
+
+    for i in range(args.warmup):
+        step(i)
+    assert sw.swin_wattn_sync_status(h, stream) == sw.OK
+    launches_per_step = sw.swin_wattn_last_launches(h)
+
+    with ClockSampler(dev.index) as clk:
+        # soak (untimed) so that the clock record covers a loaded GPU, then time K steps
+        t_soak = time.perf_counter()
+        i = 0
+        while time.perf_counter() - t_soak < args.soak:
+            step(i)
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    ms = max_over_ranks(e0.elapsed_time(e1), dist) / args.steps
+    assert sw.swin_wattn_sync_status(h, stream) == sw.OK
+    tokens_s = w.tokens * world / (ms * 1e-3)
+    tflops = w.flops * world / (ms * 1e-3) / 1e12
+
+    # whole-block roofline: min(dense bf16 peak, HBM x algorithmic intensity)
+    ai = w.flops / w.io_bytes
+    bound_tf = min(pk["bf16_sust"], pk["hbm"] * 1e9 * ai / 1e12)
+    block_roof = {"achieved_tflops": tflops / world, "roof_tflops": bound_tf, "frac": tflops / world / bound_tf,
+                  "ai_flop_per_byte": ai, "algorithmic_bytes": w.io_bytes, "algorithmic_flops": w.flops,
+                  "peak_source": pk["source"] + " (sustained bf16 / copy GB/s)"}
+
+    # per-kernel durations of the three-kernel path (stage hooks, same stream)
+    kernels = {}
+    if launches_per_step == 3:
+        kernels = per_kernel_times(sw, h, w, t, table, xs, stream, args.steps)
+    roof = dominant_roofline(w, kernels, pk, ms)
+
+    # end to end through the host-buffer entry point (pinned buffers)
+    x_host = g["x"].pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    for _ in range(2):
+        sw.swin_wattn_forward_host(h, x_host, t["Wqkv"], t["bqkv"], table, t.get("tau"), t["Wproj"], t["bproj"],
+                                   out_host, stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    k_e2e = max(3, args.steps // 4)
+    t0 = time.perf_counter()
+    for _ in range(k_e2e):
+        sw.swin_wattn_forward_host(h, x_host, t["Wqkv"], t["bqkv"], table, t.get("tau"), t["Wproj"], t["bproj"],
+                                   out_host, stream)
+        stream.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / k_e2e, dist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        if w.mode == V2:
+            tab_np = oracle.cpb_table(g["W1"].double().numpy(), g["b1"].double().numpy(), g["W2"].double().numpy(),
+                                      M=w.M, heads=w.heads)
+        else:
+            tab_np = g["table"].double().numpy()
+        rate, threads, nw = oracle_sample_rate(w, g, tab_np, seconds=args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": "%d random windows of this workload (%d tokens), float64, OpenMP over windows" %
+                         (nw, nw * w.N)}
+    sw.swin_wattn_destroy(h)
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": w.C, "heads": w.heads, "M": w.M,
+                       "shift": w.shift, "mode": "V2" if w.mode == V2 else "V1",
+                       "path": ("three kernels" if launches_per_step == 3 else
+                                "fp32 block" if w.dtype == "fp32" else "fused"),
+                       "l2": "inputs rotated over %d buffer sets of %.0f MB (x + out), %.0f MB > 2x L2" %
+                             (nsets, io_bytes / 2 ** 20, nsets * io_bytes / 2 ** 20),
+                       "parallelism": "dp%d (independent batches)" % world},
+            "tflops": tflops, "block_roofline": block_roof, "roofline": roof, "kernels_us": kernels,
+            "cpu_baseline": cpu,
+            "e2e": {"value": w.tokens * world / e2e_s, "unit": "tokens/s",
+                    "h2d_bytes_per_step": w.tokens * w.C * w.elem_bytes,
+                    "d2h_bytes_per_step": w.tokens * w.C * w.elem_bytes},
+            "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
+def per_kernel_times(sw, h, w, t, table, xs, stream, steps):
+    """Average duration (us) of each kernel of the three-kernel path, timed
+    with CUDA events on the launching stream over `steps` launches."""
+    qkv = torch.empty(w.tokens, 3 * w.C, dtype=torch.bfloat16, device=xs[0].device)
+    attn = torch.empty(w.tokens, w.C, dtype=torch.bfloat16, device=xs[0].device)
+    out = torch.empty_like(xs[0])
+    n = len(xs)
+    res = {}
+    stages = {
+        "qkv_gemm": lambda i: sw.swin_wattn_test_qkv(h, xs[i % n], t["Wqkv"], t["bqkv"], qkv, stream),
+        "window_attention": lambda i: sw.swin_wattn_test_attn(h, qkv, w.B, w.H, w.W, table, t.get("tau"), attn,
+                                                              stream),
+        "proj_gemm": lambda i: sw.swin_wattn_test_proj(h, attn, w.B, w.H, w.W, t["Wproj"], t["bproj"], out,
+                                                       stream),
+    }
+    for name, fn in stages.items():
+        for i in range(3):
+            fn(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) / steps * 1e3
+    return res
+
+
+def dominant_roofline(w, kernels, pk, ms):
+    """Roofline of the kernel that takes the most time: its algorithmic bytes
+    (its own inputs and outputs, read or written once) or FLOPs per launch
+    over its measured duration."""
+    T, C, e = w.tokens, w.C, w.elem_bytes
+    wb = lambda rows: rows * C * e  # noqa: E731
+    model = {
+        # name: (flops, bytes)
+        "qkv_gemm": (6 * T * C * C, wb(T) + 3 * wb(T) + 3 * C * C * e),
+        "window_attention": (4 * T * w.N * C, 3 * wb(T) + wb(T)),
+        "proj_gemm": (2 * T * C * C, wb(T) + wb(T) + C * C * e),
+        "block": (w.flops, w.io_bytes),
+    }
+    if not kernels:
+        kernels = {"block": ms * 1e3}
+    name = max(kernels, key=kernels.get)
+    flops, nbytes = model[name]
+    us = kernels[name]
+    ai = flops / nbytes
+    ridge = pk["bf16"] * 1e12 / (pk["hbm"] * 1e9)
+    if ai < ridge:
+        ach = nbytes / (us * 1e-6) / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": ach / pk["hbm"], "traffic": None, "us_per_launch": us, "algorithmic_bytes": nbytes,
+                "peak_source": pk["source"] + " copy bandwidth"}
+    ach = flops / (us * 1e-6) / 1e12
+    return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
+            "frac": ach / pk["bf16"], "traffic": None, "us_per_launch": us, "algorithmic_flops": flops,
+            "peak_source": pk["source"] + " bf16 burst"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="swin_t_s1", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 three kernels, 2 fused")
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=3.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()
