@@ -39,6 +39,28 @@ import torch  # noqa: E402
 from vision_transformer_shifted_gb300.inputs import V2, WORKLOADS, generate  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
+
+# DRAM bytes (read + write) per launch from ncu captures (profiles/*.md), keyed by
+# workload and kernel, with the sha1 prefix of the kernel source they were taken
+# on: reported only while the source is unchanged.
+PROFILED_TRAFFIC = {
+    ("swin_t_s1", "window_attention"): (221.16e6, "attn_tc.cu", "31933b3a9ac5"),
+    ("swin_t_s1", "qkv_gemm"): (126.96e6, "gemm_tc.cu", "8d07f3f64912"),
+    ("swin_t_s1", "proj_gemm"): (38.76e6, "gemm_tc.cu", "8d07f3f64912"),
+}
+
+
+def profiled_traffic(workload, kernel):
+    import hashlib
+    ent = PROFILED_TRAFFIC.get((workload, kernel))
+    if not ent:
+        return None
+    path = os.path.join(ROOT, "vision_transformer_shifted_gb300", "csrc", ent[1])
+    try:
+        sha = hashlib.sha1(open(path, "rb").read()).hexdigest()[:12]
+    except OSError:
+        return None
+    return ent[0] if sha == ent[2] else None
 METRIC = "fused shifted-window attn block tokens/s & TFLOP/s; % of bf16/HBM roofline"
 
 
@@ -261,6 +283,7 @@ def run_ours(args, w):
     if launches_per_step == 3:
         kernels = per_kernel_times(sw, h, w, t, table, xs, stream, args.steps)
     roof = dominant_roofline(w, kernels, pk, ms)
+    roof["traffic"] = profiled_traffic(w.key, roof["kernel"])
 
     # end to end through the host-buffer entry point (pinned buffers)
     x_host = g["x"].pin_memory()
