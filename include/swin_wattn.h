@@ -54,8 +54,10 @@ enum {
     SWIN_WATTN_EUNSUPPORTED = -2, /* valid block, but no kernel for this shape */
     SWIN_WATTN_ECUDA = -3,        /* a CUDA runtime call failed (launch, copy, alloc) */
     SWIN_WATTN_ENOMEM = -4,       /* device allocation of the handle's workspace failed */
-    SWIN_WATTN_ETIMEOUT = -5      /* a kernel gave up a bounded wait (reported by
+    SWIN_WATTN_ETIMEOUT = -5,     /* a kernel gave up a bounded wait (reported by
                                      swin_wattn_sync_status) */
+    SWIN_WATTN_ESCRATCH = -6      /* the call needs more intermediate memory than the
+                                     fixed scratch of swin_wattn_forward_noalloc holds */
 };
 
 /* Options for swin_wattn_set_option. */
@@ -143,6 +145,52 @@ int swin_wattn_last_launches(swin_wattn_t h);
 
 /* Static text for a status code. */
 const char *swin_wattn_strerror(int code);
+
+/* Size of the scratch array compiled into the library for
+ * swin_wattn_forward_noalloc (64 MiB per GPU that loads the library, held
+ * until the process exits), and the part of it that holds the intermediates
+ * (the first 256 bytes are a status word). */
+#define SWIN_WATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+#define SWIN_WATTN_NOALLOC_MAX_INTERMEDIATE_BYTES (SWIN_WATTN_NOALLOC_SCRATCH_BYTES - 256)
+
+/* The forward pass of swin_wattn_forward for callers that cannot allocate
+ * device memory.  The paper has no counterpart: this is a deployment
+ * convenience of this library.
+ *
+ * Who needs it: code that runs where it does not own the device allocator
+ * (inside a framework whose caching allocator must see every allocation,
+ * or an embedded runtime that fixes its memory budget at start-up), and code
+ * that must not allocate after start-up (a latency-critical serving loop,
+ * where cudaMalloc would synchronise the device).  swin_wattn_create
+ * allocates an error word and swin_wattn_forward a workspace for the q/k/v
+ * and attention intermediates; this entry point takes no handle and calls
+ * no cudaMalloc, cudaFree or other allocating routine.  Its intermediates
+ * live in a fixed array compiled into the library (see
+ * SWIN_WATTN_NOALLOC_SCRATCH_BYTES).
+ *
+ * Arguments: the block parameters of swin_wattn_create (C, heads, M, shift,
+ * mode; bf16 mode only, d = 32, M <= 64), then those of swin_wattn_forward
+ * with the same layouts and rules.  The caller still owns and passes every
+ * input and the output.
+ * Limit: 8 * B * H * W * C bytes of intermediates must fit in
+ * SWIN_WATTN_NOALLOC_MAX_INTERMEDIATE_BYTES (for C = 96 that is about 87,000
+ * tokens, e.g. B = 27 at 56 x 56); larger calls return SWIN_WATTN_ESCRATCH
+ * before any launch.
+ * Set-up: the first call on a device looks up the device address of the
+ * array (this can load the library's device code on that device); make that
+ * first call before any stream capture.  Later calls reuse the address.
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents; the call clears the status word it needs itself.  Calls
+ * whose work overlaps on the GPU (different streams, or several host threads)
+ * race on the array and corrupt each other's results: serialise them.
+ * A bounded-wait timeout inside the kernels is not reported by this call.
+ * Errors: EINVAL / EUNSUPPORTED as swin_wattn_create and swin_wattn_forward
+ * (fp32 mode is EUNSUPPORTED), ESCRATCH as above, ECUDA if a launch fails.
+ * B == 0 is a no-op. */
+int swin_wattn_forward_noalloc(int C, int heads, int M, int shift, int mode, const void *x, int B, int H,
+                               int W, const void *Wqkv, const void *bqkv, const void *bias_table,
+                               const float *logit_scale, const void *Wproj, const void *bproj, void *out,
+                               swin_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,90 @@
+"""swin_wattn_forward_noalloc: the forward for callers that cannot allocate.
+
+Some callers cannot call cudaMalloc: code running under an allocator it does
+not own (a framework caching allocator that must account for every byte, an
+embedded runtime with a fixed budget) or code that must not allocate once it
+is serving (a cudaMalloc would synchronise the device).  The entry point
+keeps its intermediates in a fixed array inside the library.  These tests
+call it through the C ABI and check it against swin_wattn_forward, the entry
+point with a handle-owned workspace, on two calls in a row (the array keeps
+the previous call's contents, so the second call must not depend on them),
+and check that a call too large for the array is refused before any launch.
+
+This file is collected last on purpose, and it needs no state from the
+other test files.
+"""
+import pytest
+import torch
+
+from vision_transformer_shifted_gb300 import binding as sw
+from vision_transformer_shifted_gb300.inputs import V2, WORKLOADS, generate
+
+from helpers import compare, device_inputs, oracle_table
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    sw.load()
+
+
+def forward_with_handle(w, t, table):
+    h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
+    try:
+        out = torch.full_like(t["x"], float("nan"))
+        sw.swin_wattn_forward(h, t["x"], t["Wqkv"], t["bqkv"], table, t.get("tau"), t["Wproj"], t["bproj"], out)
+        assert sw.swin_wattn_sync_status(h) == sw.OK
+        return out
+    finally:
+        sw.swin_wattn_destroy(h)
+
+
+@pytest.mark.parametrize("key,B,H,W", [("swin_t_s1", 4, 56, 56), ("swinv2_t_s1", 2, 64, 64),
+                                       ("swinv2_l_w24", 1, 48, 96)])
+def test_noalloc_matches_forward_on_two_calls_in_a_row(key, B, H, W):
+    w = WORKLOADS[key].with_(B=B, H=H, W=W)
+    assert 8 * w.tokens * w.C <= sw.NOALLOC_MAX_INTERMEDIATE_BYTES
+    results = []
+    for seed_shift in (0, 1):   # two different inputs, one call after the other
+        g = generate(w.with_(seed=w.seed + 17 * seed_shift), nonzero_bias=True)
+        t = device_inputs(g)
+        table = oracle_table(w, g).to(DEV)
+        out = torch.full_like(t["x"], float("nan"))
+        sw.swin_wattn_forward_noalloc(w.C, w.heads, w.M, w.shift, w.mode, t["x"], t["Wqkv"], t["bqkv"], table,
+                                      t.get("tau"), t["Wproj"], t["bproj"], out)
+        torch.cuda.synchronize()
+        results.append((out, forward_with_handle(w, t, table)))
+    for got, want in results:
+        compare(got.double().cpu().numpy(), want.double().cpu().numpy(), "bf16")
+    assert not torch.equal(results[0][0], results[1][0])
+
+
+def test_noalloc_refuses_calls_larger_than_its_scratch():
+    w = WORKLOADS["swin_t_s1"]          # B = 64: 154 MB of intermediates
+    assert 8 * w.tokens * w.C > sw.NOALLOC_MAX_INTERMEDIATE_BYTES
+    t = device_inputs(generate(w.with_(B=1)))
+    x = torch.zeros(w.B, w.H, w.W, w.C, dtype=torch.bfloat16, device=DEV)
+    out = torch.full_like(x, 7.0)
+    with pytest.raises(sw.SwinWAttnError) as ei:
+        sw.swin_wattn_forward_noalloc(w.C, w.heads, w.M, w.shift, w.mode, x, t["Wqkv"], t["bqkv"], t["table"],
+                                      None, t["Wproj"], t["bproj"], out)
+    assert ei.value.code == sw.ESCRATCH
+    assert "scratch" in sw.strerror(sw.ESCRATCH)
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())     # nothing was launched
+
+
+def test_noalloc_rejects_bad_arguments():
+    w = WORKLOADS["swin_t_s1"].with_(B=1, H=14, W=14)
+    t = device_inputs(generate(w))
+    out = torch.empty_like(t["x"])
+    args = (t["x"], t["Wqkv"], t["bqkv"], t["table"], None, t["Wproj"], t["bproj"], out)
+    for params, code in [((96, 5, 7, 3, 0), sw.EINVAL), ((96, 3, 7, 7, 0), sw.EINVAL),
+                         ((96, 3, 7, 3, sw.FP32), sw.EUNSUPPORTED), ((96, 3, 7, 3, V2), sw.EINVAL)]:
+        with pytest.raises(sw.SwinWAttnError) as ei:
+            sw.swin_wattn_forward_noalloc(*params, *args)
+        assert ei.value.code == code

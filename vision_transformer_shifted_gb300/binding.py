@@ -15,7 +15,8 @@ import torch
 from . import build as _build
 
 V1, V2, FP32 = 0, 1, 0x10
-OK, EINVAL, EUNSUPPORTED, ECUDA, ENOMEM, ETIMEOUT = 0, -1, -2, -3, -4, -5
+OK, EINVAL, EUNSUPPORTED, ECUDA, ENOMEM, ETIMEOUT, ESCRATCH = 0, -1, -2, -3, -4, -5, -6
+NOALLOC_MAX_INTERMEDIATE_BYTES = (64 << 20) - 256
 OPT_PATH, OPT_WAIT_LIMIT_US = 1, 2
 PATH_AUTO, PATH_THREE_KERNELS, PATH_FUSED, PATH_FP32 = 0, 1, 2, 3
 
@@ -43,6 +44,8 @@ _SIGNATURES = {
     "swin_wattn_test_proj": ["p", "p", "i", "i", "i", "p", "p", "p", "p"],
     "swin_wattn_test_gemm": ["p", "p", "p", "p", "i", "i", "i", "p"],
     "swin_wattn_test_watchdog": ["p", "p"],
+    "swin_wattn_forward_noalloc": ["i", "i", "i", "i", "i", "p", "i", "i", "i", "p", "p", "p", "p", "p", "p", "p",
+                                   "p"],
 }
 _CT = {"p": ctypes.c_void_p, "pp": ctypes.POINTER(ctypes.c_void_p), "i": ctypes.c_int, "l": ctypes.c_int64}
 
@@ -144,6 +147,14 @@ def swin_wattn_path(h, B, H, W):
 
 def swin_wattn_last_launches(h):
     return load().swin_wattn_last_launches(h)
+
+
+def swin_wattn_forward_noalloc(C, heads, M, shift, mode, x, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj,
+                               out, stream=None):
+    B, H, W, _ = x.shape
+    return _check("swin_wattn_forward_noalloc", load().swin_wattn_forward_noalloc(
+        C, heads, M, shift, mode, _p(x), B, H, W, _p(Wqkv), _p(bqkv), _p(bias_table), _p(logit_scale), _p(Wproj),
+        _p(bproj), _p(out), _stream(stream)))
 
 
 def swin_wattn_test_qkv(h, x, Wqkv, bqkv, qkv, stream=None):

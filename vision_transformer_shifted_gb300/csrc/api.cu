@@ -260,6 +260,7 @@ const char *swin_wattn_strerror(int code)
     case SWIN_WATTN_ECUDA: return "CUDA runtime error";
     case SWIN_WATTN_ENOMEM: return "device allocation failed";
     case SWIN_WATTN_ETIMEOUT: return "a kernel gave up a bounded wait";
+    case SWIN_WATTN_ESCRATCH: return "intermediates exceed the fixed scratch of swin_wattn_forward_noalloc";
     default: return "unknown status";
     }
 }
