@@ -374,10 +374,10 @@ def dominant_roofline(w, kernels, pk, ms):
         "qkv_gemm": (6 * T * C * C, wb(T) + 3 * wb(T) + 3 * C * C * e),
         "window_attention": (4 * T * w.N * C, 3 * wb(T) + wb(T)),
         "proj_gemm": (2 * T * C * C, wb(T) + wb(T) + C * C * e),
-        "block": (w.flops, w.io_bytes),
+        "fused_block": (w.flops, w.io_bytes),
     }
     if not kernels:
-        kernels = {"block": ms * 1e3}
+        kernels = {"fused_block": ms * 1e3}
     name = max(kernels, key=kernels.get)
     flops, nbytes = model[name]
     us = kernels[name]

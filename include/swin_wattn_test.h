@@ -40,9 +40,11 @@ int swin_wattn_test_proj(swin_wattn_t h, const void *attn, int B, int H, int W,
 /* The tensor-core GEMM building block alone, no index maps:
  *   D[m, n] = sum_k A[m, k] * Bw[n, k] + bias[n]
  * A [rows, K], Bw [N, K], D [rows, N], bias [N] (may be NULL), bf16,
- * row-major.  K and N multiples of 16 (N <= 2048), rows >= 0. */
+ * row-major.  K and N multiples of 16 (N <= 2048), rows >= 0.
+ * swizzle_bytes selects the shared-memory operand layout: 128 (K blocks of
+ * 64, as the three-kernel path) or 64 (K blocks of 32, as the fused kernel). */
 int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *D, int rows, int N,
-                         int K, swin_stream_t stream);
+                         int K, int swizzle_bytes, swin_stream_t stream);
 
 /* Runs a one-block kernel that waits on a barrier nothing completes, with the
  * handle's wait limit, so that the bounded-wait path can be tested: the

@@ -60,6 +60,8 @@ def test_null_handle_calls():
     assert lib.swin_wattn_set_option(None, 1, 0) == sw.EINVAL
     assert lib.swin_wattn_path(None, 1, 7, 7) == sw.EINVAL
     assert lib.swin_wattn_sync_status(None, None) == sw.EINVAL
-    assert lib.swin_wattn_test_gemm(None, None, None, None, 1, 16, 16, None) == sw.EINVAL
+    assert lib.swin_wattn_test_gemm(None, None, None, None, 1, 16, 16, 128, None) == sw.EINVAL
     assert lib.swin_wattn_test_gemm(ctypes.c_void_p(16), ctypes.c_void_p(16), None, ctypes.c_void_p(16),
-                                    1, 24, 16, None) == sw.EINVAL  # N % 16
+                                    1, 24, 16, 128, None) == sw.EINVAL  # N % 16
+    assert lib.swin_wattn_test_gemm(ctypes.c_void_p(16), ctypes.c_void_p(16), None, ctypes.c_void_p(16),
+                                    1, 16, 16, 32, None) == sw.EINVAL  # swizzle

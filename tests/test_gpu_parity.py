@@ -44,15 +44,16 @@ def run_forward(w, t, table, path=sw.PATH_AUTO):
 
 # ---- the tensor-core GEMM building block ------------------------------------
 
+@pytest.mark.parametrize("swizzle", [128, 64])
 @pytest.mark.parametrize("rows,N,K", [(128, 64, 64), (300, 288, 96), (77, 16, 16), (1000, 1536, 512),
-                                      (513, 576, 192), (256, 384, 128)])
-def test_gemm_block(rows, N, K):
+                                      (513, 576, 192), (256, 384, 128), (129, 96, 32)])
+def test_gemm_block(rows, N, K, swizzle):
     g = torch.Generator().manual_seed(rows + N + K)
     A = torch.randn(rows, K, generator=g).bfloat16()
     Bw = (torch.randn(N, K, generator=g) * 0.1).bfloat16()
     bias = (torch.randn(N, generator=g) * 0.1).bfloat16()
     D = torch.empty(rows, N, dtype=torch.bfloat16, device=DEV)
-    sw.swin_wattn_test_gemm(A.to(DEV), Bw.to(DEV), bias.to(DEV), D)
+    sw.swin_wattn_test_gemm(A.to(DEV), Bw.to(DEV), bias.to(DEV), D, swizzle)
     torch.cuda.synchronize()
     ref = A.double() @ Bw.double().T + bias.double()
     err = (D.double().cpu() - ref).abs()
@@ -133,21 +134,50 @@ SMALL = [
 ]
 
 
+PATHS = [sw.PATH_AUTO, sw.PATH_THREE_KERNELS]
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("key,B,H,W,bias", SMALL)
-def test_forward_small(key, B, H, W, bias):
+def test_forward_small(key, B, H, W, bias, path):
     w = WORKLOADS[key].with_(B=B, H=H, W=W)
     g = generate(w, nonzero_bias=bias)
     table = oracle_table(w, g)
-    out = run_forward(w, device_inputs(g), table.to(DEV))
+    out = run_forward(w, device_inputs(g), table.to(DEV), path)
     compare(out.double().cpu().numpy(), oracle_forward(w, g, table), w.dtype)
 
 
-def test_forward_global_window_no_shift():
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("key,B,H,W", [("swin_t_s1", 1, 7, 7), ("swin_t_s1", 1, 14, 7), ("swinv2_t_s1", 3, 8, 24),
+                                       ("swin_t_s1", 5, 21, 14)])
+def test_forward_ragged_tiles(key, B, H, W, path):
+    """Window counts 1, 2, 9 and 30: a lone window in the last two-window
+    tile, tiles per CTA > 1 on small grids, images that end mid-tile."""
+    w = WORKLOADS[key].with_(B=B, H=H, W=W, shift=min(WORKLOADS[key].shift, 3) if H > 7 else 0)
+    g = generate(w, nonzero_bias=True)
+    table = oracle_table(w, g)
+    out = run_forward(w, device_inputs(g), table.to(DEV), path)
+    compare(out.double().cpu().numpy(), oracle_forward(w, g, table), w.dtype)
+
+
+def test_fused_path_is_chosen_where_supported():
+    for key, want in [("swin_t_s1", sw.PATH_FUSED), ("swinv2_t_s1", sw.PATH_FUSED), ("swin_b_s1", 1),
+                      ("swin_b_s3", 1), ("swinv2_l_w24", 1), ("tiny", sw.PATH_FP32)]:
+        w = WORKLOADS[key]
+        h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode | (sw.FP32 if w.dtype == "fp32" else 0))
+        try:
+            assert sw.swin_wattn_path(h, w.B, w.H, w.W) == want, key
+        finally:
+            sw.swin_wattn_destroy(h)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_forward_global_window_no_shift(path):
     """M = H = W and s = 0: one window per image (plain attention with bias)."""
     w = WORKLOADS["swinv2_t_s1"].with_(B=3, H=8, W=8, shift=0)
     g = generate(w, nonzero_bias=True)
     table = oracle_table(w, g)
-    out = run_forward(w, device_inputs(g), table.to(DEV))
+    out = run_forward(w, device_inputs(g), table.to(DEV), path)
     compare(out.double().cpu().numpy(), oracle_forward(w, g, table), w.dtype)
 
 
@@ -169,12 +199,15 @@ def test_fp32_v2_small():
 
 # ---- full-size workloads on sampled windows ------------------------------------
 
-@pytest.mark.parametrize("key", ["swin_t_s1", "swin_b_s1", "swin_b_s3", "swinv2_t_s1", "swinv2_l_w24"])
-def test_forward_full_size_sampled(key):
+@pytest.mark.parametrize("key,path", [("swin_t_s1", sw.PATH_AUTO), ("swin_t_s1", sw.PATH_THREE_KERNELS),
+                                      ("swin_b_s1", sw.PATH_AUTO), ("swin_b_s3", sw.PATH_AUTO),
+                                      ("swinv2_t_s1", sw.PATH_AUTO), ("swinv2_t_s1", sw.PATH_THREE_KERNELS),
+                                      ("swinv2_l_w24", sw.PATH_AUTO)])
+def test_forward_full_size_sampled(key, path):
     w = WORKLOADS[key]
     g = generate(w)
     table = oracle_table(w, g)
-    out = run_forward(w, device_inputs(g), table.to(DEV))
+    out = run_forward(w, device_inputs(g), table.to(DEV), path)
     wins = sample_windows(w, 8 if w.M > 8 else 24)
     ref = oracle_forward(w, g, table, windows=wins)
     tok = window_tokens(w, wins)

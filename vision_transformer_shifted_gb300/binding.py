@@ -42,7 +42,7 @@ _SIGNATURES = {
     "swin_wattn_test_qkv": ["p", "p", "i", "i", "i", "p", "p", "p", "p"],
     "swin_wattn_test_attn": ["p", "p", "i", "i", "i", "p", "p", "p", "p"],
     "swin_wattn_test_proj": ["p", "p", "i", "i", "i", "p", "p", "p", "p"],
-    "swin_wattn_test_gemm": ["p", "p", "p", "p", "i", "i", "i", "p"],
+    "swin_wattn_test_gemm": ["p", "p", "p", "p", "i", "i", "i", "i", "p"],
     "swin_wattn_test_watchdog": ["p", "p"],
     "swin_wattn_forward_noalloc": ["i", "i", "i", "i", "i", "p", "i", "i", "i", "p", "p", "p", "p", "p", "p", "p",
                                    "p"],
@@ -173,11 +173,11 @@ def swin_wattn_test_proj(h, attn, B, H, W, Wproj, bproj, out, stream=None):
         h, _p(attn), B, H, W, _p(Wproj), _p(bproj), _p(out), _stream(stream)))
 
 
-def swin_wattn_test_gemm(A, Bw, bias, D, stream=None):
+def swin_wattn_test_gemm(A, Bw, bias, D, swizzle_bytes=128, stream=None):
     rows, K = A.shape
     N = Bw.shape[0]
     return _check("swin_wattn_test_gemm", load().swin_wattn_test_gemm(
-        _p(A), _p(Bw), _p(bias), _p(D), rows, N, K, _stream(stream)))
+        _p(A), _p(Bw), _p(bias), _p(D), rows, N, K, swizzle_bytes, _stream(stream)))
 
 
 def swin_wattn_test_watchdog(h, stream=None):

@@ -3,8 +3,8 @@
 #include <cstring>
 #include <new>
 
-#include "../../include/swin_wattn.h"
-#include "../../include/swin_wattn_test.h"
+#include "swin_wattn.h"
+#include "swin_wattn_test.h"
 #include "common.cuh"
 
 using namespace swin;
@@ -43,7 +43,7 @@ int check_grid(const swin_wattn_s *h, int B, int H, int W)
 int choose_path(const swin_wattn_s *h)
 {
     if (h->fp32) return 3;
-    return 1;
+    return fused_supported(h->M, h->C, h->heads) ? 2 : 1;
 }
 
 int ensure_buffer(void **buf, size_t *have, size_t need)
@@ -82,6 +82,15 @@ int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void 
         if (e == cudaErrorInvalidConfiguration) return SWIN_WATTN_EUNSUPPORTED;
         h->last_launches = 1;
         return cuda_status(e);
+    }
+    if (path == 2) {
+        if (!fused_supported(h->M, h->C, h->heads) || g.T >= ((int64_t)1 << 31)) return SWIN_WATTN_EUNSUPPORTED;
+        cudaError_t e = launch_fused((const bf16 *)x, (const bf16 *)Wqkv, (const bf16 *)bqkv, (const bf16 *)table, tau,
+                                     (const bf16 *)Wproj, (const bf16 *)bproj, (bf16 *)out, h->mode, g, dstatus(h),
+                                     stream);
+        if (e != cudaSuccess) return SWIN_WATTN_ECUDA;
+        h->last_launches = 1;
+        return SWIN_WATTN_OK;
     }
     if (path != 1) return SWIN_WATTN_EUNSUPPORTED;
     const size_t qkv_bytes = (size_t)g.T * 3 * h->C * 2, attn_bytes = (size_t)g.T * h->C * 2;
@@ -246,7 +255,8 @@ int swin_wattn_path(swin_wattn_t h, int B, int H, int W)
     if (rc) return rc;
     if (h->fp32) return 3;
     const int path = h->path_opt ? h->path_opt : choose_path(h);
-    return path == 1 ? 1 : SWIN_WATTN_EUNSUPPORTED;
+    if (path == 2 && !fused_supported(h->M, h->C, h->heads)) return SWIN_WATTN_EUNSUPPORTED;
+    return path;
 }
 
 int swin_wattn_last_launches(swin_wattn_t h) { return h ? h->last_launches : 0; }
@@ -313,9 +323,10 @@ int swin_wattn_test_proj(swin_wattn_t h, const void *attn, int B, int H, int W, 
 }
 
 int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *D, int rows, int N, int K,
-                         swin_stream_t stream)
+                         int swizzle_bytes, swin_stream_t stream)
 {
     if (!A || !Bw || !D || rows < 0 || N <= 0 || K <= 0 || N % 16 || K % 16 || N > 2048) return SWIN_WATTN_EINVAL;
+    if (swizzle_bytes != 64 && swizzle_bytes != 128) return SWIN_WATTN_EINVAL;
     if (!aligned16(A) || !aligned16(Bw) || !aligned16(D) || (bias && !aligned16(bias))) return SWIN_WATTN_EINVAL;
     if (rows == 0) return SWIN_WATTN_OK;
     GemmArgs a{};
@@ -324,7 +335,9 @@ int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *
     // the hook has no handle: its error word is a private one, never read
     static int *d_err = nullptr;
     if (!d_err && cudaMalloc(&d_err, sizeof(int)) != cudaSuccess) return SWIN_WATTN_ENOMEM;
-    return cuda_status(launch_gemm(a, LOAD_PLAIN, STORE_PLAIN, DeviceStatus{d_err, 2000000000ull}, (cudaStream_t)stream));
+    const DeviceStatus st{d_err, 2000000000ull};
+    if (swizzle_bytes == 64) return cuda_status(launch_gemm_sw64(a, st, (cudaStream_t)stream));
+    return cuda_status(launch_gemm(a, LOAD_PLAIN, STORE_PLAIN, st, (cudaStream_t)stream));
 }
 
 int swin_wattn_test_watchdog(swin_wattn_t h, swin_stream_t stream)

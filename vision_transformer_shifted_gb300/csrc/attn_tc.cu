@@ -160,11 +160,11 @@ struct KernelCommon {
 __device__ __forceinline__ KernelCommon setup_smem(uint8_t *smem_raw, int M)
 {
     KernelCommon k;
-    k.smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    k.smem = smem_align(smem_raw, 1024);
     k.sbias = reinterpret_cast<float *>(k.smem + AttnSmem::end);
     const int L2 = (2 * M - 1) * (2 * M - 1);
     uint8_t *after = reinterpret_cast<uint8_t *>(k.sbias + L2);
-    after = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(after) + 7) & ~uintptr_t(7));
+    after = smem_align(after, 8);
     k.bar = reinterpret_cast<uint64_t *>(after);
     k.tmem_slot = reinterpret_cast<uint32_t *>(k.bar + 1);
     return k;
@@ -259,21 +259,28 @@ __global__ void __launch_bounds__(THREADS) attn_pack2_kernel(AttnArgs a, DeviceS
 #pragma unroll
             for (int j = 0; j < 32; ++j) { s[j] = c0[j]; s[32 + j] = c1[j]; }
         }
-        const int my_region = key_region[slot][t];
-        const int base = (ti + M - 1) * L + (tj + M - 1);
+        const int my_region = key_region[slot][t];   // -1 for a padding row: nothing matches
+        const int tb = row_ok ? t : 0;                 // padding rows read a valid bias row
+        const int base = (tb / M + M - 1) * L + (tb % M + M - 1);
         float mx = -INFINITY;
+        // branch-free over the lanes: every lane computes the logit and a select
+        // applies the mask (j < N is the same for the whole warp)
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
             float v = -INFINITY;
-            if (j < N && key_region[slot][j] == my_region) v = fmaf(s[j], scale, kc.sbias[base - key_off[j]]);
+            if (j < N) {
+                const float lv = fmaf(s[j], scale, kc.sbias[base - key_off[j]]);
+                v = key_region[slot][j] == my_region ? lv : -INFINITY;
+            }
             s[j] = v;
             mx = fmaxf(mx, v);
         }
+        if (!row_ok) mx = 0.f;
         float sum = 0.f;
         uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < 64; j += 2) {
-            const float p0 = exp2f(s[j] - mx), p1 = exp2f(s[j + 1] - mx);
+            const float p0 = ex2_approx(s[j] - mx), p1 = ex2_approx(s[j + 1] - mx);
             sum += p0 + p1;
             pk[j / 2] = pack_bf16x2(p0, p1);
         }
@@ -303,7 +310,7 @@ __global__ void __launch_bounds__(THREADS) attn_pack2_kernel(AttnArgs a, DeviceS
         float o[32];
         tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), o);
         tmem_wait_ld();
-        if (row_ok && !failed) store_o_row(a.attn + (win * N + t) * (int64_t)C + head * 32, o, 1.0f / l);
+        if (row_ok && !failed) store_o_row(a.attn + (win * N + t) * (int64_t)C + head * 32, o, rcp_approx(l));
     }
     if (failed) atomicOr(st.err, ERR_TIMEOUT);
     tc_fence_before();
@@ -408,36 +415,35 @@ __global__ void __launch_bounds__(THREADS) attn_flash_kernel(AttnArgs a, DeviceS
         phase ^= 1;
         tc_fence_after();
 
-        // pass 1: tile max
-        float mt = -INFINITY;
-#pragma unroll 1
+        // logits of the tile's 128 keys in registers; mask by select, not by branch
+        float sv[128];
+#pragma unroll
         for (int c = 0; c < 4; ++c) {
             float s[32];
             tmem_ld32(t_lane + 32 * c, s);
-            tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int jj = 32 * c + j;
-                if (key_region[jj] == my_region) mt = fmaxf(mt, fmaf(s[j], scale, kc.sbias[base - key_off[jj]]));
-            }
+            for (int j = 0; j < 32; ++j) sv[32 * c + j] = s[j];
+        }
+        tmem_wait_ld();
+        float mt = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 128; ++j) {
+            const float lv = fmaf(sv[j], scale, kc.sbias[base - key_off[j]]);
+            sv[j] = key_region[j] == my_region ? lv : -INFINITY;
+            mt = fmaxf(mt, sv[j]);
         }
         const float m_new = fmaxf(m_run, mt);
-        const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
-        // pass 2: probabilities
+        // no key seen yet: use 0 as the reference (every p below is then 0, and
+        // alpha = 0 leaves o = 0, l = 0 as they are)
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = ex2_approx(m_run - m_use);
         float sum = 0.f;
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < 4; ++c) {
-            float s[32];
-            tmem_ld32(t_lane + 32 * c, s);
-            tmem_wait_ld();
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-                const int jj = 32 * c + j;
-                float p0 = 0.f, p1 = 0.f;
-                if (key_region[jj] == my_region) p0 = exp2f(fmaf(s[j], scale, kc.sbias[base - key_off[jj]]) - m_new);
-                if (key_region[jj + 1] == my_region)
-                    p1 = exp2f(fmaf(s[j + 1], scale, kc.sbias[base - key_off[jj + 1]]) - m_new);
+                const float p0 = ex2_approx(sv[32 * c + j] - m_use), p1 = ex2_approx(sv[32 * c + j + 1] - m_use);
                 sum += p0 + p1;
                 pk[j / 2] = pack_bf16x2(p0, p1);
             }
@@ -475,7 +481,7 @@ __global__ void __launch_bounds__(THREADS) attn_flash_kernel(AttnArgs a, DeviceS
         tc_fence_before();
         if (__syncthreads_or(failed)) { failed = true; break; }
     }
-    if (!failed && row_ok) store_o_row(a.attn + (win * N + qt) * (int64_t)C + head * 32, o, 1.0f / l_run);
+    if (!failed && row_ok) store_o_row(a.attn + (win * N + qt) * (int64_t)C + head * 32, o, rcp_approx(l_run));
     if (failed && tid == 0) atomicOr(st.err, ERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();

@@ -50,6 +50,23 @@ __device__ __forceinline__ int64_t window_row_to_token(const Geom &g, int64_t r)
     return ((int64_t)b * g.H + i) * g.W + j;
 }
 
+// 32-bit form of window_row_to_token for callers that know B*H*W < 2^31.
+__device__ __forceinline__ int window_row_to_token32(const Geom &g, int r)
+{
+    const int win = r / g.N;
+    const int t = r - win * g.N;
+    const int per = g.nh * g.nw;
+    const int b = win / per;
+    const int rem = win - b * per;
+    const int wi = rem / g.nw, wj = rem - (rem / g.nw) * g.nw;
+    const int ti = t / g.M, tj = t - (t / g.M) * g.M;
+    int i = wi * g.M + ti + g.s;
+    if (i >= g.H) i -= g.H;
+    int j = wj * g.M + tj + g.s;
+    if (j >= g.W) j -= g.W;
+    return (b * g.H + i) * g.W + j;
+}
+
 // Band of a shifted-frame coordinate p on an axis of length n (shift s > 0):
 // 0 for [0, n-M), 1 for [n-M, n-s), 2 for [n-s, n).  Pairs of tokens whose
 // (row band, column band) differ are masked.
@@ -85,6 +102,9 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, DeviceStatus st,
                         cudaStream_t stream);
+// Plain GEMM with 32-wide K blocks in the 64-byte-swizzled layout (tests the
+// layout the fused kernel uses).
+cudaError_t launch_gemm_sw64(const GemmArgs &a, DeviceStatus st, cudaStream_t stream);
 
 struct AttnArgs {
     const bf16 *qkv;      // [T, 3C] window order
@@ -108,6 +128,12 @@ struct Fp32Args {
 // the window does not fit in shared memory.
 cudaError_t launch_fp32_block(const Fp32Args &a, cudaStream_t stream);
 size_t fp32_block_smem_bytes(int N, int C);
+
+// The whole block in one persistent kernel (windows of <= 64 tokens, C = 64 or 96).
+bool fused_supported(int M, int C, int heads);
+cudaError_t launch_fused(const bf16 *x, const bf16 *Wqkv, const bf16 *bqkv, const bf16 *table, const float *tau,
+                         const bf16 *Wproj, const bf16 *bproj, bf16 *out, int mode, const Geom &g, DeviceStatus st,
+                         cudaStream_t stream);
 
 cudaError_t launch_cpb_table(const float *W1, const float *b1, const float *W2, int hidden, int M,
                              int heads, bool out_bf16, void *table, cudaStream_t stream);

@@ -9,11 +9,11 @@
 // is ever written.  Output projection: the epilogue writes each row through
 // the window-reverse + roll(+s) map into the original [B, H, W, C] layout.
 //
-// Tile: 128 rows x BN columns (BN <= 256, multiple of 16), K in blocks of 64
-// (one 128-byte swizzle atom per row), a 3-stage cp.async ring into the
-// K-major 128B-swizzled layout, one thread issuing tcgen05.mma, the fp32
-// accumulator in TMEM, and a 4-warp epilogue reading one TMEM lane (= one
-// output row) per thread.
+// Tile: 128 rows x BN columns (BN <= 256, multiple of 16), K in blocks of BK
+// (64: one 128-byte swizzle atom per row, 3-stage ring; 32: one 64-byte
+// swizzle atom per row, 4-stage ring), cp.async into the K-major swizzled
+// layout, one thread issuing tcgen05.mma, the fp32 accumulator in TMEM, and a
+// 4-warp epilogue reading one TMEM lane (= one output row) per thread.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -22,18 +22,27 @@ namespace swin {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;
-constexpr int STAGES = 3;
 constexpr int THREADS = 128;
 
+template <int BK>
 struct GemmSmem {
     // dynamic layout: [A stages][B stages] (1024-aligned), then row offsets,
     // bias, barriers and the TMEM address.
-    static constexpr int a_stage = BM * BK * 2; // 16 KB
+    static constexpr int STAGES = BK == 64 ? 3 : 4;
+    static constexpr int CPR = BK / 8;          // 16-byte chunks per row
+    static constexpr int a_stage = BM * BK * 2;
     static size_t bytes(int BN)
     {
         return 1024 + (size_t)STAGES * (a_stage + BN * BK * 2) + BM * sizeof(int64_t) + 256 * sizeof(float) +
                STAGES * 8 + 8 + 16;
+    }
+    static __device__ __forceinline__ uint32_t offset(uint32_t row, uint32_t chunk)
+    {
+        return BK == 64 ? sw128_offset(row, chunk) : sw64_offset(row, chunk);
+    }
+    static __device__ __forceinline__ uint64_t desc(uint32_t addr)
+    {
+        return BK == 64 ? desc_kmajor_sw128(addr) : desc_kmajor_sw64(addr);
     }
 };
 
@@ -50,14 +59,16 @@ __device__ __forceinline__ void store_row_bf16(bf16 *dst, const float *v, const 
     }
 }
 
-template <int LOAD, int STORE>
+template <int LOAD, int STORE, int BK>
 __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, DeviceStatus st)
 {
+    using L = GemmSmem<BK>;
+    constexpr int STAGES = L::STAGES, CPR = L::CPR;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_align(smem_raw, 1024);
     const int b_stage = BN * BK * 2;
     uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * GemmSmem::a_stage;
+    uint8_t *sB = smem + STAGES * L::a_stage;
     int64_t *row_off = reinterpret_cast<int64_t *>(sB + STAGES * b_stage);
     float *sbias = reinterpret_cast<float *>(row_off + BM);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbias + 256);
@@ -91,22 +102,22 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
     const uint32_t tmem = *tmem_slot;
 
     auto load_stage = [&](int kb, int s) {
-        const uint32_t a_base = smem_u32(sA + s * GemmSmem::a_stage);
+        const uint32_t a_base = smem_u32(sA + s * L::a_stage);
         const uint32_t b_base = smem_u32(sB + s * b_stage);
-        const int c = tid & 7;
+        const int c = tid % CPR;
         const int k0 = kb * BK + c * 8;
         const bool kin = k0 < a.K;
 #pragma unroll
-        for (int i = 0; i < BM / 16; ++i) {
-            const int r = (tid >> 3) + 16 * i;
+        for (int i = 0; i < CPR; ++i) {
+            const int r = tid / CPR + (THREADS / CPR) * i;
             const int64_t off = row_off[r];
             const bool ok = kin && off >= 0;
             const bf16 *src = ok ? a.A + off + k0 : a.A;
-            cp_async16(a_base + sw128_offset(r, c), src, ok ? 16u : 0u);
+            cp_async16(a_base + L::offset(r, c), src, ok ? 16u : 0u);
         }
-        for (int n = tid >> 3; n < BN; n += 16) {
+        for (int n = tid / CPR; n < BN; n += THREADS / CPR) {
             const bf16 *src = kin ? a.Bw + (int64_t)(n0 + n) * a.K + k0 : a.Bw;
-            cp_async16(b_base + sw128_offset(n, c), src, kin ? 16u : 0u);
+            cp_async16(b_base + L::offset(n, c), src, kin ? 16u : 0u);
         }
     };
 
@@ -137,13 +148,12 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
         tc_fence_after();
         if (tid == 0) {
             const int s = kb % STAGES;
-            const uint32_t a_base = smem_u32(sA + s * GemmSmem::a_stage);
+            const uint32_t a_base = smem_u32(sA + s * L::a_stage);
             const uint32_t b_base = smem_u32(sB + s * b_stage);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
                 if (kb * BK + k * 16 < a.K)
-                    mma_bf16(tmem, desc_kmajor_sw128(a_base + 32 * k), desc_kmajor_sw128(b_base + 32 * k), idesc,
-                             (kb | k) != 0);
+                    mma_bf16(tmem, L::desc(a_base + 32 * k), L::desc(b_base + 32 * k), idesc, (kb | k) != 0);
             }
             mma_commit(smem_u32(&bars[s]));
         }
@@ -194,13 +204,13 @@ int pick_bn(int N)
     return 0;
 }
 
-template <int LOAD, int STORE>
+template <int LOAD, int STORE, int BK = 64>
 cudaError_t launch_impl(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
 {
     const int BN = pick_bn(a.N);
     if (BN == 0 || a.K % 16 != 0 || a.rows <= 0) return cudaErrorInvalidValue;
-    const size_t smem = GemmSmem::bytes(BN);
-    auto kern = gemm_tc_kernel<LOAD, STORE>;
+    const size_t smem = GemmSmem<BK>::bytes(BN);
+    auto kern = gemm_tc_kernel<LOAD, STORE, BK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.rows + BM - 1) / BM), (unsigned)(a.N / BN));
@@ -216,6 +226,11 @@ cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, Device
     if (load_mode == LOAD_PLAIN && store_mode == STORE_SCATTER) return launch_impl<LOAD_PLAIN, STORE_SCATTER>(a, st, stream);
     if (load_mode == LOAD_PLAIN && store_mode == STORE_PLAIN) return launch_impl<LOAD_PLAIN, STORE_PLAIN>(a, st, stream);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_sw64(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
+{
+    return launch_impl<LOAD_PLAIN, STORE_PLAIN, 32>(a, st, stream);
 }
 
 } // namespace swin

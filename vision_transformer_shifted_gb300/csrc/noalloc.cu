@@ -10,7 +10,7 @@
 // a workspace the handle allocates.
 #include <mutex>
 
-#include "../../include/swin_wattn.h"
+#include "swin_wattn.h"
 #include "common.cuh"
 
 using namespace swin;

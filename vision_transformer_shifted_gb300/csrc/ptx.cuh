@@ -12,6 +12,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Rounds a pointer into shared memory up to a multiple of `align` (a power of
+// two) by pointer arithmetic, so the compiler still sees a shared-memory
+// pointer and emits ld.shared / st.shared (an integer round trip through
+// uintptr_t would turn every access into a slower generic one).
+template <typename T>
+__device__ __forceinline__ T *smem_align(T *p, uint32_t align)
+{
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    return reinterpret_cast<T *>(reinterpret_cast<uint8_t *>(p) + ((align - (a & (align - 1u))) & (align - 1u)));
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns()
 {
     uint64_t t;
@@ -44,6 +55,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to ~hint_ns nanoseconds
+// (woken early when the phase completes), so waiting warps do not spin.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for phase `parity` of the barrier to complete, for at most limit_ns
 // nanoseconds of wall time.  Returns false on timeout (the caller records the
 // error and leaves); never traps and never spins without bound.
@@ -52,7 +78,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
@@ -86,6 +112,36 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait()
 {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---- bulk copies (TMA, non-tensor) ----------------------------------------------
+
+// Copies `bytes` (multiple of 16) from shared memory to global memory
+// asynchronously; both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until the shared-memory sources of this thread's bulk copies have been read.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Waits until this thread's bulk copies have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// ---- fast SFU math (hardware approximations) ---------------------------------------
+
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // ---- tcgen05 -------------------------------------------------------------------
@@ -193,6 +249,18 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t addr) { return sm
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// K-major operand, 64-byte swizzle: rows of 32 bf16 (64 B), 8-row atoms of
+// 512 B stacked densely (stride byte offset 512).
+__device__ __forceinline__ uint64_t desc_kmajor_sw64(uint32_t addr) { return smem_desc(addr, 16, 512, SWZ_64B); }
+
+// Byte offset of the 16-byte chunk `chunk` (0..3) of row `row` inside a
+// K-major 64B-swizzled tile of 64-byte rows (8-row atoms of 512 bytes): the
+// chunk index is XOR-ed with address bits 7..8, i.e. (row / 2) mod 4.
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t chunk)
+{
+    return (row >> 3) * 512u + (row & 7u) * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
 }
 
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a
