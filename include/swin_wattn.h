@@ -146,6 +146,10 @@ int swin_wattn_last_launches(swin_wattn_t h);
 /* Static text for a status code. */
 const char *swin_wattn_strerror(int code);
 
+/* Text of the CUDA runtime error behind the handle's most recent ECUDA from a
+ * launch in swin_wattn_forward (or "no CUDA error recorded").  Static string. */
+const char *swin_wattn_last_cuda_error(swin_wattn_t h);
+
 /* Size of the scratch array compiled into the library for
  * swin_wattn_forward_noalloc (64 MiB per GPU that loads the library, held
  * until the process exits), and the part of it that holds the intermediates

@@ -41,8 +41,10 @@ int swin_wattn_test_proj(swin_wattn_t h, const void *attn, int B, int H, int W,
  *   D[m, n] = sum_k A[m, k] * Bw[n, k] + bias[n]
  * A [rows, K], Bw [N, K], D [rows, N], bias [N] (may be NULL), bf16,
  * row-major.  K and N multiples of 16 (N <= 2048), rows >= 0.
- * swizzle_bytes selects the shared-memory operand layout: 128 (K blocks of
- * 64, as the three-kernel path) or 64 (K blocks of 32, as the fused kernel). */
+ * swizzle_bytes selects the operand layout: 128 (K blocks of 64 in 128-byte
+ * swizzled shared memory, as the three-kernel path), 64 (K blocks of 32 in
+ * 64-byte swizzled shared memory, as the fused kernel) or 0 (A staged in
+ * tensor memory, the MMA form that reads A from TMEM; K <= 128, N <= 256). */
 int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *D, int rows, int N,
                          int K, int swizzle_bytes, swin_stream_t stream);
 

@@ -61,6 +61,21 @@ def test_gemm_block(rows, N, K, swizzle):
     assert (err <= ref.abs() * 2.0 ** -8 + 1e-4).all(), float(err.max())
 
 
+@pytest.mark.parametrize("rows,N,K", [(128, 32, 32), (200, 128, 128), (77, 256, 64), (384, 96, 96)])
+def test_gemm_a_from_tmem(rows, N, K):
+    """The MMA form that reads A from tensor memory (two bf16 of K per column)."""
+    g = torch.Generator().manual_seed(7 * rows + N + K)
+    A = torch.randn(rows, K, generator=g).bfloat16()
+    Bw = (torch.randn(N, K, generator=g) * 0.1).bfloat16()
+    bias = (torch.randn(N, generator=g) * 0.1).bfloat16()
+    D = torch.empty(rows, N, dtype=torch.bfloat16, device=DEV)
+    sw.swin_wattn_test_gemm(A.to(DEV), Bw.to(DEV), bias.to(DEV), D, 0)
+    torch.cuda.synchronize()
+    ref = A.double() @ Bw.double().T + bias.double()
+    err = (D.double().cpu() - ref).abs()
+    assert (err <= ref.abs() * 2.0 ** -8 + 1e-4).all(), float(err.max())
+
+
 # ---- index maps, bit-exact ----------------------------------------------------
 
 def tagged(B, H, W, C):

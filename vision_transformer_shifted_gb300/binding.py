@@ -67,13 +67,15 @@ def load(build_if_missing: bool = True):
         fn.restype = ctypes.c_int
     lib.swin_wattn_strerror.argtypes = [ctypes.c_int]
     lib.swin_wattn_strerror.restype = ctypes.c_char_p
+    lib.swin_wattn_last_cuda_error.argtypes = [ctypes.c_void_p]
+    lib.swin_wattn_last_cuda_error.restype = ctypes.c_char_p
     _lib = lib
     return lib
 
 
 def exported_symbols():
     """Names of the functions the C headers declare."""
-    return sorted(list(_SIGNATURES) + ["swin_wattn_strerror"])
+    return sorted(list(_SIGNATURES) + ["swin_wattn_strerror", "swin_wattn_last_cuda_error"])
 
 
 def strerror(code: int) -> str:
@@ -115,9 +117,16 @@ def swin_wattn_destroy(h):
 
 def swin_wattn_forward(h, x, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out, stream=None):
     B, H, W, _ = x.shape
-    return _check("swin_wattn_forward", load().swin_wattn_forward(
+    rc = load().swin_wattn_forward(
         h, _p(x), B, H, W, _p(Wqkv), _p(bqkv), _p(bias_table), _p(logit_scale), _p(Wproj), _p(bproj), _p(out),
-        _stream(stream)))
+        _stream(stream))
+    if rc == ECUDA:
+        raise SwinWAttnError("swin_wattn_forward (%s)" % swin_wattn_last_cuda_error(h), rc)
+    return _check("swin_wattn_forward", rc)
+
+
+def swin_wattn_last_cuda_error(h):
+    return load().swin_wattn_last_cuda_error(h).decode()
 
 
 def swin_wattn_forward_host(h, x_host, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out_host, stream=None):

@@ -21,6 +21,7 @@ struct swin_wattn_s {
     void *stage_x, *stage_out; // device staging of swin_wattn_forward_host
     size_t stage_bytes;
     int last_launches;
+    cudaError_t last_cuda_error;
 };
 
 namespace {
@@ -80,6 +81,7 @@ int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void 
         a.out = (float *)out; a.heads = h->heads; a.mode = h->mode; a.g = g;
         cudaError_t e = launch_fp32_block(a, stream);
         if (e == cudaErrorInvalidConfiguration) return SWIN_WATTN_EUNSUPPORTED;
+        if (e != cudaSuccess) h->last_cuda_error = e;
         h->last_launches = 1;
         return cuda_status(e);
     }
@@ -88,7 +90,10 @@ int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void 
         cudaError_t e = launch_fused((const bf16 *)x, (const bf16 *)Wqkv, (const bf16 *)bqkv, (const bf16 *)table, tau,
                                      (const bf16 *)Wproj, (const bf16 *)bproj, (bf16 *)out, h->mode, g, dstatus(h),
                                      stream);
-        if (e != cudaSuccess) return SWIN_WATTN_ECUDA;
+        if (e != cudaSuccess) {
+            h->last_cuda_error = e;
+            return SWIN_WATTN_ECUDA;
+        }
         h->last_launches = 1;
         return SWIN_WATTN_OK;
     }
@@ -102,17 +107,17 @@ int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void 
     k1.A = (const bf16 *)x; k1.lda = h->C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
     k1.D = qkv; k1.ldd = 3 * h->C; k1.rows = g.T; k1.N = 3 * h->C; k1.K = h->C; k1.g = g;
     cudaError_t e = launch_gemm(k1, LOAD_GATHER, STORE_PLAIN, dstatus(h), stream);
-    if (e != cudaSuccess) return SWIN_WATTN_ECUDA;
+    if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
     AttnArgs k2{};
     k2.qkv = qkv; k2.attn = attn; k2.table = (const bf16 *)table; k2.tau = tau; k2.heads = h->heads;
     k2.mode = h->mode; k2.g = g;
     e = launch_attention(k2, dstatus(h), stream);
-    if (e != cudaSuccess) return SWIN_WATTN_ECUDA;
+    if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
     GemmArgs k3{};
     k3.A = attn; k3.lda = h->C; k3.Bw = (const bf16 *)Wproj; k3.bias = (const bf16 *)bproj;
     k3.D = (bf16 *)out; k3.ldd = h->C; k3.rows = g.T; k3.N = h->C; k3.K = h->C; k3.g = g;
     e = launch_gemm(k3, LOAD_PLAIN, STORE_SCATTER, dstatus(h), stream);
-    if (e != cudaSuccess) return SWIN_WATTN_ECUDA;
+    if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
     h->last_launches = 3;
     return SWIN_WATTN_OK;
 }
@@ -261,6 +266,12 @@ int swin_wattn_path(swin_wattn_t h, int B, int H, int W)
 
 int swin_wattn_last_launches(swin_wattn_t h) { return h ? h->last_launches : 0; }
 
+const char *swin_wattn_last_cuda_error(swin_wattn_t h)
+{
+    if (!h || h->last_cuda_error == cudaSuccess) return "no CUDA error recorded";
+    return cudaGetErrorString(h->last_cuda_error);
+}
+
 const char *swin_wattn_strerror(int code)
 {
     switch (code) {
@@ -326,7 +337,8 @@ int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *
                          int swizzle_bytes, swin_stream_t stream)
 {
     if (!A || !Bw || !D || rows < 0 || N <= 0 || K <= 0 || N % 16 || K % 16 || N > 2048) return SWIN_WATTN_EINVAL;
-    if (swizzle_bytes != 64 && swizzle_bytes != 128) return SWIN_WATTN_EINVAL;
+    if (swizzle_bytes != 0 && swizzle_bytes != 64 && swizzle_bytes != 128) return SWIN_WATTN_EINVAL;
+    if (swizzle_bytes == 0 && (K % 32 || K > 128 || N > 256)) return SWIN_WATTN_EINVAL;
     if (!aligned16(A) || !aligned16(Bw) || !aligned16(D) || (bias && !aligned16(bias))) return SWIN_WATTN_EINVAL;
     if (rows == 0) return SWIN_WATTN_OK;
     GemmArgs a{};
@@ -337,6 +349,7 @@ int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *
     if (!d_err && cudaMalloc(&d_err, sizeof(int)) != cudaSuccess) return SWIN_WATTN_ENOMEM;
     const DeviceStatus st{d_err, 2000000000ull};
     if (swizzle_bytes == 64) return cuda_status(launch_gemm_sw64(a, st, (cudaStream_t)stream));
+    if (swizzle_bytes == 0) return cuda_status(launch_gemm_ts_test(a, st, (cudaStream_t)stream));
     return cuda_status(launch_gemm(a, LOAD_PLAIN, STORE_PLAIN, st, (cudaStream_t)stream));
 }
 

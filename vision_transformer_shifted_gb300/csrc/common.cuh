@@ -105,6 +105,9 @@ cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, Device
 // Plain GEMM with 32-wide K blocks in the 64-byte-swizzled layout (tests the
 // layout the fused kernel uses).
 cudaError_t launch_gemm_sw64(const GemmArgs &a, DeviceStatus st, cudaStream_t stream);
+// Plain GEMM with the A operand staged in TMEM (K <= 128, N <= 256): tests the
+// TMEM-A MMA form.
+cudaError_t launch_gemm_ts_test(const GemmArgs &a, DeviceStatus st, cudaStream_t stream);
 
 struct AttnArgs {
     const bf16 *qkv;      // [T, 3C] window order

@@ -22,9 +22,15 @@
 // Nothing but x, the weights and out touches HBM.  The next tile's x is
 // fetched with cp.async while the current one is computed.
 //
-// 256 threads: warp w serves TMEM lane quarter w % 4 (tile rows 32(w%4) ..
-// +31) and column half w / 4; every drain and the softmax split their
-// columns between the two halves.  Thread 0 issues the MMAs.
+// Warp roles: warps 0..7 compute (warp w serves TMEM lane quarter w % 4 =
+// tile rows 32(w%4)..+31 and column half w / 4; every drain and the softmax
+// split their columns between the two halves); warp 8 issues every tcgen05
+// MMA.  They hand over through mbarriers: the compute warps arrive on
+// "ready" barriers (one arrival per warp) once operands are in shared memory,
+// the MMA warp commits "done" barriers.  The MMA warp issues the next tile's
+// QKV projection as soon as the current tile's last softmax has freed TMEM
+// columns 0..2C+127, so it runs under the current tile's P.V, o drain,
+// projection and store.
 #include <type_traits>
 
 #include "common.cuh"
@@ -34,7 +40,9 @@ namespace swin {
 
 namespace {
 
-constexpr int FTHREADS = 256;
+constexpr int FTHREADS = 288;          // 8 compute warps + 1 MMA warp
+constexpr int NCOMPUTE = 256;
+constexpr int NCWARPS = NCOMPUTE / 32;
 constexpr float FLOG2E = 1.4426950408889634f;
 
 // Optional phase trace (builds with -DSWIN_PHASE_TRACE only): thread 0 of
@@ -79,7 +87,7 @@ struct FusedCfg {
     static constexpr int P = VT + 2 * VT_BLK;           // 2 x [128 rows][64 keys] SW128
     static constexpr int SMALL = P + 2 * 128 * 128;
     static constexpr int BYTES = SMALL + HEADS * L * L * 4 + 3 * C * 4 + C * 4 + HEADS * 4 + 2 * 128 * 4 +
-                                 HEADS * 2 * 128 * 4 + 3 * 128 * 4 + 2 * 64 * 4 + 8 * 8 + 16;
+                                 HEADS * 2 * 128 * 4 + 3 * 128 * 4 + 2 * 64 * 4 + 16 * 8 + 16 + 16;
     // TMEM columns
     static constexpr int T_QK = 0;                      // 2C
     static constexpr int T_VT = 2 * C;                  // 128 (v^T), then S
@@ -98,6 +106,47 @@ struct FusedArgs {
     Geom g;
 };
 
+// Barrier among the 256 compute threads (named barrier 1); returns the OR of
+// `v` over them, so that a failure seen by one thread is seen by all.
+__device__ __forceinline__ bool compute_sync_or(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+// Bounded wait that also gives up as soon as another thread has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t limit_ns, volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// One arrival per warp on a ready barrier: every lane's prior shared-memory
+// writes (made visible to the async proxy by the caller) and TMEM loads
+// happen before it.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane)
+{
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
 template <int M, int C>
 __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, DeviceStatus st)
 {
@@ -109,61 +158,71 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
     float *sbqkv = sbias + HEADS * L * L;                             // [3C]
     float *sbproj = sbqkv + 3 * C;                                    // [C]
     float *sscale = sbproj + C;                                       // [HEADS]
-    float *smax = sscale + HEADS;                                     // [2][128]
-    float *spart = smax + 2 * 128;                                    // [HEADS][2][128]
+    float *smax = sscale + HEADS;                                     // [2][128] partial row maxima
+    float *spart = smax + 2 * 128;                                    // [HEADS][2][128] partial row sums
     // token of each tile row (-1 if none), three rotating copies: tile k uses
     // copy k % 3 and fills copy (k + 1) % 3 for the next tile while other warps
     // may still read copy (k - 1) % 3 for the previous tile's stores
     int *rowtok = reinterpret_cast<int *>(spart + HEADS * 2 * 128);   // [3][128]
     int *key_region = rowtok + 3 * 128;                               // [2][64]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem_align(reinterpret_cast<uint8_t *>(key_region + 2 * 64), 8));
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
     __shared__ int slot_masked[2];
 
     const Geom g = a.g;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
+    const bool is_mma = warp == NCWARPS;
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;       // tile row = TMEM lane
     const int slot = row >> 6, t = row & 63;   // window slot and token of the row
     const uint32_t base = smem_u32(sm);
-    const uint32_t bar_qkv = smem_u32(&bars[0]), bar_s = smem_u32(&bars[1]), bar_pv = smem_u32(&bars[2]),
-                   bar_y = smem_u32(&bars[3]);
+    // done barriers (tcgen05.commit) and ready barriers (one arrival per compute warp)
+    const uint32_t B_QKV = smem_u32(&bars[0]), B_S = smem_u32(&bars[1]), B_PV = smem_u32(&bars[2]),
+                   B_Y = smem_u32(&bars[3]);
+    const uint32_t R_QK = smem_u32(&bars[4]), R_P = smem_u32(&bars[5]), R_O = smem_u32(&bars[6]),
+                   R_FREE = smem_u32(&bars[7]);
     const int64_t ntiles = (g.nwin + 1) / 2;
+    auto xbuf = [&](int buf) { return buf ? F::X1 : F::X0; };
 
     // ---- once per CTA: weights, biases, tables, barriers, TMEM ---------------
-    for (int q = tid; q < (2 * C) * (C / 8); q += FTHREADS) {         // Wq, Wk rows
-        const int r = q / (C / 8), c16 = q % (C / 8);
-        cp_async16(base + F::WQK + (c16 >> 2) * (2 * C * 64) + sw64_offset(r, c16 & 3), a.Wqkv + (int64_t)r * C + c16 * 8,
-                   16);
+    if (!is_mma) {
+        for (int q = tid; q < (2 * C) * (C / 8); q += NCOMPUTE) {     // Wq, Wk rows
+            const int r = q / (C / 8), c16 = q % (C / 8);
+            cp_async16(base + F::WQK + (c16 >> 2) * (2 * C * 64) + sw64_offset(r, c16 & 3),
+                       a.Wqkv + (int64_t)r * C + c16 * 8, 16);
+        }
+        for (int q = tid; q < 128 * (C / 8); q += NCOMPUTE) {         // Wv rows, zero past C
+            const int r = q / (C / 8), c16 = q % (C / 8);
+            const bool ok = r < C;
+            cp_async16(base + F::WV + (c16 >> 2) * (128 * 64) + sw64_offset(r, c16 & 3),
+                       ok ? a.Wqkv + (int64_t)(2 * C + r) * C + c16 * 8 : a.Wqkv, ok ? 16u : 0u);
+        }
+        for (int q = tid; q < C * (C / 8); q += NCOMPUTE) {           // Wproj
+            const int r = q / (C / 8), c16 = q % (C / 8);
+            cp_async16(base + F::WP + (c16 >> 2) * (C * 64) + sw64_offset(r, c16 & 3),
+                       a.Wproj + (int64_t)r * C + c16 * 8, 16);
+        }
+        for (int i = tid; i < HEADS * L * L; i += NCOMPUTE) {
+            const int hd = i / (L * L), e = i % (L * L);
+            sbias[i] = __bfloat162float(a.table[(int64_t)e * HEADS + hd]) * FLOG2E;
+        }
+        for (int i = tid; i < 3 * C; i += NCOMPUTE) sbqkv[i] = a.bqkv ? __bfloat162float(a.bqkv[i]) : 0.f;
+        for (int i = tid; i < C; i += NCOMPUTE) sbproj[i] = a.bproj ? __bfloat162float(a.bproj[i]) : 0.f;
+        if (tid < HEADS)
+            sscale[tid] = a.mode == 1 ? FLOG2E / fmaxf(a.tau[tid], 0.01f) : FLOG2E * rsqrtf(32.0f);
+        // P: the off-diagonal blocks (slot 0 rows x window-B keys and the
+        // reverse) stay zero for the whole kernel
+        for (int i = tid; i < 2 * 128 * 128 / 16; i += NCOMPUTE)
+            reinterpret_cast<uint4 *>(sm + F::P)[i] = make_uint4(0, 0, 0, 0);
     }
-    for (int q = tid; q < 128 * (C / 8); q += FTHREADS) {             // Wv rows, zero past C
-        const int r = q / (C / 8), c16 = q % (C / 8);
-        const bool ok = r < C;
-        cp_async16(base + F::WV + (c16 >> 2) * (128 * 64) + sw64_offset(r, c16 & 3),
-                   ok ? a.Wqkv + (int64_t)(2 * C + r) * C + c16 * 8 : a.Wqkv, ok ? 16u : 0u);
-    }
-    for (int q = tid; q < C * (C / 8); q += FTHREADS) {               // Wproj
-        const int r = q / (C / 8), c16 = q % (C / 8);
-        cp_async16(base + F::WP + (c16 >> 2) * (C * 64) + sw64_offset(r, c16 & 3), a.Wproj + (int64_t)r * C + c16 * 8,
-                   16);
-    }
-    for (int i = tid; i < HEADS * L * L; i += FTHREADS) {
-        const int hd = i / (L * L), e = i % (L * L);
-        sbias[i] = __bfloat162float(a.table[(int64_t)e * HEADS + hd]) * FLOG2E;
-    }
-    for (int i = tid; i < 3 * C; i += FTHREADS) sbqkv[i] = a.bqkv ? __bfloat162float(a.bqkv[i]) : 0.f;
-    for (int i = tid; i < C; i += FTHREADS) sbproj[i] = a.bproj ? __bfloat162float(a.bproj[i]) : 0.f;
-    if (tid < HEADS)
-        sscale[tid] = a.mode == 1 ? FLOG2E / fmaxf(a.tau[tid], 0.01f) : FLOG2E * rsqrtf(32.0f);
-    // P: the off-diagonal blocks (slot 0 rows x window-B keys and the reverse)
-    // stay zero for the whole kernel
-    for (int i = tid; i < 2 * 128 * 128 / 16; i += FTHREADS)
-        reinterpret_cast<uint4 *>(sm + F::P)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        for (int i = 4; i < 8; ++i) mbar_init(smem_u32(&bars[i]), NCWARPS);
+        *abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == 0) {
+    if (is_mma) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -178,13 +237,12 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
         }
     };
     // x rows of the tile whose row tokens are in `tok` into X buffer `buf`
-    // (zeros where tok < 0)
-    auto xbuf = [&](int buf) { return buf ? F::X1 : F::X0; };
+    // (zeros where tok < 0); compute threads only
     auto load_x = [&](const int *tok, int buf) {
         const uint32_t xb = base + xbuf(buf);
 #pragma unroll
-        for (int i = 0; i < 128 * (C / 8) / FTHREADS; ++i) {
-            const int q = tid + FTHREADS * i;
+        for (int i = 0; i < 128 * (C / 8) / NCOMPUTE; ++i) {
+            const int q = tid + NCOMPUTE * i;
             const int r = q / (C / 8), c16 = q % (C / 8);
             const int tk = tok[r];
             const bf16 *src = tk >= 0 ? a.x + (int64_t)tk * C + c16 * 8 : a.x;
@@ -197,132 +255,159 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
 #endif
     row_tokens(blockIdx.x, rowtok);
     __syncthreads();
-    load_x(rowtok, 0);
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-
-    uint32_t ph_qkv = 0, ph_s = 0, ph_pv = 0, ph_y = 0;
-    int pv_pending = 0;
-    bool failed = false;
-
-    int k = 0;
-#pragma unroll 1
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
-        const int buf = k & 1;
-        const uint32_t xb = base + xbuf(buf);
-
-        // this tile's window geometry: key regions and whether a window is cut
-        // by the shift; the next tile's row tokens
-        if (tid < 128) {
-            const int sl = tid >> 6, tt = tid & 63;
-            const int win = (int)(2 * tile) + sl;
-            int reg = -1;
-            if (tt < N && win < g.nwin) {
-                const int rem = win % (g.nh * g.nw);
-                const int wi = rem / g.nw, wj = rem % g.nw;
-                reg = 0;
-                if (g.s > 0)
-                    reg = 3 * shift_band(wi * M + tt / M, g.H, M, g.s) + shift_band(wj * M + tt % M, g.W, M, g.s);
-                if (tt == 0)
-                    slot_masked[sl] = g.s > 0 && (wi == g.nh - 1 || wj == g.nw - 1);
-            } else if (tt == 0) {
-                slot_masked[sl] = 0;
-            }
-            key_region[sl * 64 + tt] = reg;
-        }
-        PHASE(k, 0);
-        int *tok_cur = rowtok + (k % 3) * 128, *tok_next = rowtok + ((k + 1) % 3) * 128;
-        row_tokens(tile + gridDim.x, tok_next);
+    if (!is_mma) {
+        load_x(rowtok, 0);
         cp_async_wait<0>();
         fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(failed)) { failed = true; break; }
-        tc_fence_after();
-        // prefetch the next tile into the other buffer (its o was consumed by
-        // the previous tile's projection, which has completed)
-        PHASE(k, 1);
-        if (tile + gridDim.x < ntiles) load_x(tok_next, buf ^ 1);
-        else cp_async_commit();
-        PHASE(k, 2);
+    }
+    tc_fence_before();
+    __syncthreads();   // weights, tables, the first tile's x, barriers, TMEM address
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
-        // ---- S2: [q|k] and v^T ----------------------------------------------------
-        if (tid == 0) {
+    if (is_mma) {
+        // ===================== MMA warp (lane 0 issues) =====================
+        if (lane == 0) {
+            uint32_t ph_qk = 0, ph_p = 0, ph_o = 0, ph_free = 0;
             const uint32_t id_qk = idesc_bf16(128, 2 * C), id_vt = idesc_bf16(128, 128);
+            const uint32_t id_s = idesc_bf16(128, 128), id_pv = idesc_bf16(128, 32), id_y = idesc_bf16(128, C);
+            auto issue_qkv = [&](int buf) {
+                const uint32_t xb = base + xbuf(buf);
 #pragma unroll
-            for (int kb = 0; kb < KB; ++kb)
+                for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
-                    mma_bf16(tmem + F::T_QK, desc_kmajor_sw64(xb + kb * (128 * 64) + 32 * ks),
-                             desc_kmajor_sw64(base + F::WQK + kb * (2 * C * 64) + 32 * ks), id_qk, (kb | ks) != 0);
+                    for (int ks = 0; ks < 2; ++ks)
+                        mma_bf16(tmem + F::T_QK, desc_kmajor_sw64(xb + kb * (128 * 64) + 32 * ks),
+                                 desc_kmajor_sw64(base + F::WQK + kb * (2 * C * 64) + 32 * ks), id_qk, (kb | ks) != 0);
 #pragma unroll
-            for (int kb = 0; kb < KB; ++kb)
+                for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
-                    mma_bf16(tmem + F::T_VT, desc_kmajor_sw64(base + F::WV + kb * (128 * 64) + 32 * ks),
-                             desc_kmajor_sw64(xb + kb * (128 * 64) + 32 * ks), id_vt, (kb | ks) != 0);
-            mma_commit(bar_qkv);
-        }
-        if (!mbar_wait(bar_qkv, ph_qkv, st.wait_ns)) failed = true;
-        ph_qkv ^= 1;
-        tc_fence_after();
-        PHASE(k, 3);
-
-        // v^T drain: lane = v channel, this half's 64 token columns -> V^T K block `half`
-        {
-            float v0[32], v1[32];
-            tmem_ld32(t_lane + F::T_VT + 64 * half, v0);
-            tmem_ld32(t_lane + F::T_VT + 64 * half + 32, v1);
-            tmem_wait_ld();
-            if (row < C) {
-                const float bv = sbqkv[2 * C + row];
-                uint8_t *dst = sm + F::VT + half * F::VT_BLK;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(dst + sw128_offset(row, c)) =
-                        make_uint4(pack_bf16x2(v0[8 * c] + bv, v0[8 * c + 1] + bv),
-                                   pack_bf16x2(v0[8 * c + 2] + bv, v0[8 * c + 3] + bv),
-                                   pack_bf16x2(v0[8 * c + 4] + bv, v0[8 * c + 5] + bv),
-                                   pack_bf16x2(v0[8 * c + 6] + bv, v0[8 * c + 7] + bv));
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(dst + sw128_offset(row, 4 + c)) =
-                        make_uint4(pack_bf16x2(v1[8 * c] + bv, v1[8 * c + 1] + bv),
-                                   pack_bf16x2(v1[8 * c + 2] + bv, v1[8 * c + 3] + bv),
-                                   pack_bf16x2(v1[8 * c + 4] + bv, v1[8 * c + 5] + bv),
-                                   pack_bf16x2(v1[8 * c + 6] + bv, v1[8 * c + 7] + bv));
-            }
-        }
-
-        const bool row_ok = key_region[slot * 64 + t] >= 0;
-        // keys this row may attend to (bit j = key j of its window): all N keys,
-        // or those in its own shift region; none for a padding row
-        uint32_t allow_lo = 0, allow_hi = 0;
-        if (row_ok) {
-            if (slot_masked[slot]) {
-                const int my_region = key_region[slot * 64 + t];
-                for (int j = 0; j < N; ++j) {
-                    if (key_region[slot * 64 + j] == my_region) {
-                        if (j < 32) allow_lo |= 1u << j;
-                        else allow_hi |= 1u << (j - 32);
-                    }
-                }
-            } else {
-                allow_lo = 0xffffffffu;
-                allow_hi = N >= 64 ? 0xffffffffu : ((1u << (N - 32)) - 1u);
-            }
-        }
-        const uint32_t allow = half == 0 ? allow_lo : allow_hi;
-        const int tb = row_ok ? t : 0;   // padding rows read a valid bias row (then masked)
-        const int bias_base = (tb / M + M - 1) * L + (tb % M + M - 1);
-
+                    for (int ks = 0; ks < 2; ++ks)
+                        mma_bf16(tmem + F::T_VT, desc_kmajor_sw64(base + F::WV + kb * (128 * 64) + 32 * ks),
+                                 desc_kmajor_sw64(xb + kb * (128 * 64) + 32 * ks), id_vt, (kb | ks) != 0);
+                mma_commit(B_QKV);
+            };
+            int k = 0;
+            if ((int64_t)blockIdx.x < ntiles) issue_qkv(0);
 #pragma unroll 1
-        for (int hd = 0; hd < HEADS; ++hd) {
-            // ---- q_h (half 0) or k_h (half 1) to shared memory ---------------------
+            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+                const int buf = k & 1;
+                bool ok = true;
+#pragma unroll 1
+                for (int hd = 0; hd < HEADS && ok; ++hd) {
+                    ok = wait_or_abort(R_QK, ph_qk, st.wait_ns, abort_flag);
+                    ph_qk ^= 1;
+                    if (!ok) break;
+                    tc_fence_after();
+                    mma_bf16(tmem + F::T_S, desc_kmajor_sw64(base + F::Q), desc_kmajor_sw64(base + F::K), id_s, 0);
+                    mma_bf16(tmem + F::T_S, desc_kmajor_sw64(base + F::Q + 32), desc_kmajor_sw64(base + F::K + 32),
+                             id_s, 1);
+                    mma_commit(B_S);
+                    ok = wait_or_abort(R_P, ph_p, st.wait_ns, abort_flag);
+                    ph_p ^= 1;
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const int kb = kk >> 2, ks = kk & 3;
+                        mma_bf16(tmem + F::T_O + 32 * hd, desc_kmajor_sw128(base + F::P + kb * (128 * 128) + 32 * ks),
+                                 desc_kmajor_sw128(base + F::VT + kb * F::VT_BLK + (hd * 32 / 8) * 1024 + 32 * ks),
+                                 id_pv, kk != 0);
+                    }
+                    mma_commit(B_PV);
+                }
+                if (!ok) break;
+                // next tile's QKV as soon as this tile's softmax has freed its TMEM
+                // columns and the next x tile has landed
+                if (tile + gridDim.x < ntiles) {
+                    if (!wait_or_abort(R_FREE, ph_free, st.wait_ns, abort_flag)) break;
+                    ph_free ^= 1;
+                    tc_fence_after();
+                    issue_qkv(buf ^ 1);
+                }
+                if (!wait_or_abort(R_O, ph_o, st.wait_ns, abort_flag)) break;
+                ph_o ^= 1;
+                tc_fence_after();
+                const uint32_t xb = base + xbuf(buf);
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks)
+                        mma_bf16(tmem + F::T_Y, desc_kmajor_sw64(xb + kb * (128 * 64) + 32 * ks),
+                                 desc_kmajor_sw64(base + F::WP + kb * (C * 64) + 32 * ks), id_y, (kb | ks) != 0);
+                mma_commit(B_Y);
+            }
+        }
+    } else {
+        // ===================== compute warps =====================
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        uint32_t ph_qkv = 0, ph_s = 0, ph_pv = 0, ph_y = 0;
+        bool failed = false;
+        int k = 0;
+#pragma unroll 1
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+            const int buf = k & 1;
+            const bool has_next = tile + gridDim.x < ntiles;
+            PHASE(k, 0);
+            int *tok_cur = rowtok + (k % 3) * 128, *tok_next = rowtok + ((k + 1) % 3) * 128;
+            // this tile's window geometry: key regions and whether a window is cut
+            // by the shift; the next tile's row tokens
+            if (tid < 128) {
+                const int sl = tid >> 6, tt = tid & 63;
+                const int win = (int)(2 * tile) + sl;
+                int reg = -1;
+                if (tt < N && win < g.nwin) {
+                    const int rem = win % (g.nh * g.nw);
+                    const int wi = rem / g.nw, wj = rem % g.nw;
+                    reg = 0;
+                    if (g.s > 0)
+                        reg = 3 * shift_band(wi * M + tt / M, g.H, M, g.s) + shift_band(wj * M + tt % M, g.W, M, g.s);
+                    if (tt == 0) slot_masked[sl] = g.s > 0 && (wi == g.nh - 1 || wj == g.nw - 1);
+                } else if (tt == 0) {
+                    slot_masked[sl] = 0;
+                }
+                key_region[sl * 64 + tt] = reg;
+            }
+            row_tokens(tile + gridDim.x, tok_next);
+            if (compute_sync_or(failed)) { failed = true; break; }
+            PHASE(k, 1);
+            // prefetch the next tile into the other buffer (its o and staging
+            // were consumed by the previous tile, which has completed)
+            if (has_next) load_x(tok_next, buf ^ 1);
+            PHASE(k, 2);
+
+            if (!wait_or_abort(B_QKV, ph_qkv, st.wait_ns, abort_flag)) failed = true;
+            ph_qkv ^= 1;
+            tc_fence_after();
+            PHASE(k, 3);
+
+            // v^T drain: lane = v channel, this half's 64 token columns -> V^T K block `half`
             {
+                float v0[32], v1[32];
+                tmem_ld32(t_lane + F::T_VT + 64 * half, v0);
+                tmem_ld32(t_lane + F::T_VT + 64 * half + 32, v1);
+                tmem_wait_ld();
+                if (row < C) {
+                    const float bv = sbqkv[2 * C + row];
+                    uint8_t *dst = sm + F::VT + half * F::VT_BLK;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(dst + sw128_offset(row, c)) =
+                            make_uint4(pack_bf16x2(v0[8 * c] + bv, v0[8 * c + 1] + bv),
+                                       pack_bf16x2(v0[8 * c + 2] + bv, v0[8 * c + 3] + bv),
+                                       pack_bf16x2(v0[8 * c + 4] + bv, v0[8 * c + 5] + bv),
+                                       pack_bf16x2(v0[8 * c + 6] + bv, v0[8 * c + 7] + bv));
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(dst + sw128_offset(row, 4 + c)) =
+                            make_uint4(pack_bf16x2(v1[8 * c] + bv, v1[8 * c + 1] + bv),
+                                       pack_bf16x2(v1[8 * c + 2] + bv, v1[8 * c + 3] + bv),
+                                       pack_bf16x2(v1[8 * c + 4] + bv, v1[8 * c + 5] + bv),
+                                       pack_bf16x2(v1[8 * c + 6] + bv, v1[8 * c + 7] + bv));
+                }
+            }
+            // q_h (half 0) or k_h (half 1) of head hd to shared memory
+            auto drain_qk = [&](int hd) {
                 const int col = half == 0 ? hd * 32 : C + hd * 32;
                 float v[32];
                 tmem_ld32(t_lane + F::T_QK + col, v);
@@ -343,198 +428,195 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
                     *reinterpret_cast<uint4 *>(dst + sw64_offset(row, c)) =
                         make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
                                    pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (__syncthreads_or(failed)) { failed = true; break; }
-            tc_fence_after();
-            PHASE(k, 4 + 4 * hd);
-            if (tid == 0) {
-                const uint32_t id = idesc_bf16(128, 128);
-                mma_bf16(tmem + F::T_S, desc_kmajor_sw64(base + F::Q), desc_kmajor_sw64(base + F::K), id, 0);
-                mma_bf16(tmem + F::T_S, desc_kmajor_sw64(base + F::Q + 32), desc_kmajor_sw64(base + F::K + 32), id, 1);
-                mma_commit(bar_s);
-            }
-            if (!mbar_wait(bar_s, ph_s, st.wait_ns)) failed = true;
-            ph_s ^= 1;
-            tc_fence_after();
-            PHASE(k, 5 + 4 * hd);
+                fence_proxy_async_smem();
+                warp_arrive(R_QK, lane);
+            };
+            drain_qk(0);
 
-            // ---- softmax over this row's own window, keys 32*half .. +31 -----------
-            float s[32];
-            tmem_ld32(t_lane + F::T_S + 64 * slot + 32 * half, s);
-            tmem_wait_ld();
-            if (hd == 0) PHASE(k, 21);
-            const float scale = sscale[hd];
-            const float *bias = sbias + hd * L * L + bias_base;
-            float mx = -INFINITY;
-            // key j of the row's window: relative-bias row bias_base - ((j/M)*L + j%M);
-            // j is a compile-time constant in each unrolled loop
-            if (half == 0) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float v = fmaf(s[j], scale, bias[-((j / M) * L + j % M)]);
-                    s[j] = (allow >> j) & 1u ? v : -INFINITY;
-                    mx = fmaxf(mx, s[j]);
-                }
-            } else {
-#pragma unroll
-                for (int j = 32; j < 64; ++j) {
-                    if (j < N) {
-                        const float v = fmaf(s[j - 32], scale, bias[-((j / M) * L + j % M)]);
-                        s[j - 32] = (allow >> (j - 32)) & 1u ? v : -INFINITY;
-                    } else {
-                        s[j - 32] = -INFINITY;
+            const bool row_ok = key_region[slot * 64 + t] >= 0;
+            // keys this row may attend to (bit j = key j of its window): all N keys,
+            // or those in its own shift region; none for a padding row
+            uint32_t allow_lo = 0, allow_hi = 0;
+            if (row_ok) {
+                if (slot_masked[slot]) {
+                    const int my_region = key_region[slot * 64 + t];
+                    for (int j = 0; j < N; ++j) {
+                        if (key_region[slot * 64 + j] == my_region) {
+                            if (j < 32) allow_lo |= 1u << j;
+                            else allow_hi |= 1u << (j - 32);
+                        }
                     }
-                    mx = fmaxf(mx, s[j - 32]);
+                } else {
+                    allow_lo = 0xffffffffu;
+                    allow_hi = N >= 64 ? 0xffffffffu : ((1u << (N - 32)) - 1u);
                 }
             }
-            if (hd == 0) PHASE(k, 22);
-            smax[half * 128 + row] = mx;
-            // P may be rewritten only once the previous head's P.V has read it
-            if (pv_pending) {
-                if (!mbar_wait(bar_pv, ph_pv, st.wait_ns)) failed = true;
-                ph_pv ^= 1;
-                pv_pending = 0;
-            }
-            if (hd == 0) PHASE(k, 23);
-            __syncthreads();
-            if (hd == 0) PHASE(k, 24);
-            mx = row_ok ? fmaxf(smax[row], smax[128 + row]) : 0.f;   // padding rows: all -inf -> p = 0
-            float sum = 0.f;
-            uint32_t pk[16];
-#pragma unroll
-            for (int jj = 0; jj < 32; jj += 2) {
-                const float p0 = ex2_approx(s[jj] - mx), p1 = ex2_approx(s[jj + 1] - mx);
-                sum += p0 + p1;
-                pk[jj / 2] = pack_bf16x2(p0, p1);
-            }
-            spart[(hd * 2 + half) * 128 + row] = sum;
-            PHASE(k, 6 + 4 * hd);
-            {
-                uint8_t *dst = sm + F::P + slot * (128 * 128);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(dst + sw128_offset(row, 4 * half + c)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (__syncthreads_or(failed)) { failed = true; break; }
-            tc_fence_after();
-            if (tid == 0) {
-                const uint32_t id = idesc_bf16(128, 32);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const int kb = kk >> 2, ks = kk & 3;
-                    mma_bf16(tmem + F::T_O + 32 * hd, desc_kmajor_sw128(base + F::P + kb * (128 * 128) + 32 * ks),
-                             desc_kmajor_sw128(base + F::VT + kb * F::VT_BLK + (hd * 32 / 8) * 1024 + 32 * ks), id,
-                             kk != 0);
-                }
-                mma_commit(bar_pv);
-            }
-            PHASE(k, 7 + 4 * hd);
-            pv_pending = 1;
-        }
-        if (failed) break;
-        if (pv_pending) {
-            if (!mbar_wait(bar_pv, ph_pv, st.wait_ns)) failed = true;
-            ph_pv ^= 1;
-            pv_pending = 0;
-        }
-        tc_fence_after();
+            const uint32_t allow = half == 0 ? allow_lo : allow_hi;
+            const int tb = row_ok ? t : 0;   // padding rows read a valid bias row (then masked)
+            const int bias_base = (tb / M + M - 1) * L + (tb % M + M - 1);
 
-        PHASE(k, 17);
-        // ---- o / rowsum -> bf16 -> X buffer (A operand of the projection) --------
-#pragma unroll
-        for (int hd = 0; hd < HEADS; ++hd) {
-            float o[16];
-            tmem_ld16(t_lane + F::T_O + 32 * hd + 16 * half, o);
-            tmem_wait_ld();
-            const float l = spart[(hd * 2) * 128 + row] + spart[(hd * 2 + 1) * 128 + row];
-            const float inv = row_ok ? rcp_approx(l) : 0.f;
-            uint8_t *dst = sm + xbuf(buf) + hd * (128 * 64);
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-                *reinterpret_cast<uint4 *>(dst + sw64_offset(row, 2 * half + c)) =
-                    make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
-                               pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                               pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                               pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(failed)) { failed = true; break; }
-        tc_fence_after();
-        if (tid == 0) {
-            const uint32_t id = idesc_bf16(128, C);
-#pragma unroll
-            for (int kb = 0; kb < KB; ++kb)
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
-                    mma_bf16(tmem + F::T_Y, desc_kmajor_sw64(xb + kb * (128 * 64) + 32 * ks),
-                             desc_kmajor_sw64(base + F::WP + kb * (C * 64) + 32 * ks), id, (kb | ks) != 0);
-            mma_commit(bar_y);
-        }
-        PHASE(k, 18);
-        if (!mbar_wait(bar_y, ph_y, st.wait_ns)) failed = true;
-        ph_y ^= 1;
-        tc_fence_after();
-        PHASE(k, 19);
+#pragma unroll 1
+            for (int hd = 0; hd < HEADS; ++hd) {
+                PHASE(k, 4 + 4 * hd);
+                if (!wait_or_abort(B_S, ph_s, st.wait_ns, abort_flag)) failed = true;
+                ph_s ^= 1;
+                tc_fence_after();
+                PHASE(k, 5 + 4 * hd);
 
-        // ---- y + bproj -> bf16 staging rows -> out through window reverse + roll(+s) ----
-        // (thread = row reads its half of y from TMEM into a staging row with a
-        // padded, bank-conflict-free stride; then all threads copy the rows out
-        // in 16-byte chunks, consecutive lanes on consecutive chunks, so each
-        // warp store covers whole rows that are contiguous in out within a
-        // window row)
-        {
-            constexpr int HC = C / 2;
-            uint8_t *stage = sm + xbuf(buf);
-            uint8_t *srow = stage + row * F::SROW + half * HC * 2;
-#pragma unroll
-            for (int c0 = 0; c0 < HC; c0 += 16) {
-                float y[16];
-                tmem_ld16(t_lane + F::T_Y + half * HC + c0, y);
+                // ---- softmax over this row's own window, keys 32*half .. +31 -------
+                float s[32];
+                tmem_ld32(t_lane + F::T_S + 64 * slot + 32 * half, s);
                 tmem_wait_ld();
-                const float *bp = sbproj + half * HC + c0;
-                uint4 *d4 = reinterpret_cast<uint4 *>(srow + c0 * 2);
+                const float scale = sscale[hd];
+                const float *bias = sbias + hd * L * L + bias_base;
+                float mx = -INFINITY;
+                // key j of the row's window: relative-bias row bias_base - ((j/M)*L + j%M);
+                // j is a compile-time constant in each unrolled loop
+                if (half == 0) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float v = fmaf(s[j], scale, bias[-((j / M) * L + j % M)]);
+                        s[j] = (allow >> j) & 1u ? v : -INFINITY;
+                        mx = fmaxf(mx, s[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 32; j < 64; ++j) {
+                        if (j < N) {
+                            const float v = fmaf(s[j - 32], scale, bias[-((j / M) * L + j % M)]);
+                            s[j - 32] = (allow >> (j - 32)) & 1u ? v : -INFINITY;
+                        } else {
+                            s[j - 32] = -INFINITY;
+                        }
+                        mx = fmaxf(mx, s[j - 32]);
+                    }
+                }
+                smax[half * 128 + row] = mx;
+                if (hd == HEADS - 1 && has_next) {
+                    // this tile's last TMEM reads of the QK and S columns are done, and
+                    // the next x tile is in place: the MMA warp may start its QKV
+                    cp_async_wait<0>();
+                    fence_proxy_async_smem();
+                    warp_arrive(R_FREE, lane);
+                }
+                if (compute_sync_or(failed)) { failed = true; break; }
+                mx = row_ok ? fmaxf(smax[row], smax[128 + row]) : 0.f;   // padding rows: all -inf -> p = 0
+                float sum = 0.f;
+                uint32_t pk[16];
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 2) {
+                    const float p0 = ex2_approx(s[jj] - mx), p1 = ex2_approx(s[jj + 1] - mx);
+                    sum += p0 + p1;
+                    pk[jj / 2] = pack_bf16x2(p0, p1);
+                }
+                spart[(hd * 2 + half) * 128 + row] = sum;
+                PHASE(k, 6 + 4 * hd);
+                // P may be rewritten only once the previous head's P.V has read it
+                if (hd > 0) {
+                    if (!wait_or_abort(B_PV, ph_pv, st.wait_ns, abort_flag)) failed = true;
+                    ph_pv ^= 1;
+                }
+                {
+                    uint8_t *dst = sm + F::P + slot * (128 * 128);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(dst + sw128_offset(row, 4 * half + c)) =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                }
+                fence_proxy_async_smem();
+                warp_arrive(R_P, lane);
+                PHASE(k, 7 + 4 * hd);
+                if (hd + 1 < HEADS) drain_qk(hd + 1);
+            }
+            // (a failure here is not uniform across threads yet: carry on to the
+            // next barrier-with-OR, which makes every compute thread leave together;
+            // waits return at once once the abort flag is set)
+            if (!wait_or_abort(B_PV, ph_pv, st.wait_ns, abort_flag)) failed = true;
+            ph_pv ^= 1;
+            tc_fence_after();
+            PHASE(k, 17);
+
+            // ---- o / rowsum -> bf16 -> X buffer (A operand of the projection) ------
+#pragma unroll
+            for (int hd = 0; hd < HEADS; ++hd) {
+                float o[16];
+                tmem_ld16(t_lane + F::T_O + 32 * hd + 16 * half, o);
+                tmem_wait_ld();
+                const float l = spart[(hd * 2) * 128 + row] + spart[(hd * 2 + 1) * 128 + row];
+                const float inv = row_ok ? rcp_approx(l) : 0.f;
+                uint8_t *dst = sm + xbuf(buf) + hd * (128 * 64);
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
-                    d4[c] = make_uint4(pack_bf16x2(y[8 * c] + bp[8 * c], y[8 * c + 1] + bp[8 * c + 1]),
-                                       pack_bf16x2(y[8 * c + 2] + bp[8 * c + 2], y[8 * c + 3] + bp[8 * c + 3]),
-                                       pack_bf16x2(y[8 * c + 4] + bp[8 * c + 4], y[8 * c + 5] + bp[8 * c + 5]),
-                                       pack_bf16x2(y[8 * c + 6] + bp[8 * c + 6], y[8 * c + 7] + bp[8 * c + 7]));
+                    *reinterpret_cast<uint4 *>(dst + sw64_offset(row, 2 * half + c)) =
+                        make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                   pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                   pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                   pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
             }
-            tc_fence_before();
-            if (__syncthreads_or(failed)) { failed = true; break; }
-            constexpr int CH = C / 8;   // 16-byte chunks per row
-#pragma unroll 2
-            for (int q = tid; q < 128 * CH; q += FTHREADS) {
-                const int r = q / CH, c16 = q % CH;
-                const int tk = tok_cur[r];
-                if (tk >= 0)
-                    *reinterpret_cast<uint4 *>(a.out + (int64_t)tk * C + c16 * 8) =
-                        *reinterpret_cast<const uint4 *>(stage + r * F::SROW + c16 * 16);
+            fence_proxy_async_smem();
+            warp_arrive(R_O, lane);
+            PHASE(k, 18);
+            if (!wait_or_abort(B_Y, ph_y, st.wait_ns, abort_flag)) failed = true;
+            ph_y ^= 1;
+            tc_fence_after();
+            PHASE(k, 19);
+
+            // ---- y + bproj -> bf16 staging rows -> out through window reverse + roll(+s) ----
+            // (thread = row reads its half of y from TMEM into a staging row with a
+            // padded, bank-conflict-free stride; then all compute threads copy the
+            // rows out in 16-byte chunks, consecutive lanes on consecutive chunks,
+            // so each warp store covers whole rows that are contiguous in out
+            // within a window row)
+            {
+                constexpr int HC = C / 2;
+                uint8_t *stage = sm + xbuf(buf);
+                uint8_t *srow = stage + row * F::SROW + half * HC * 2;
+#pragma unroll
+                for (int c0 = 0; c0 < HC; c0 += 16) {
+                    float y[16];
+                    tmem_ld16(t_lane + F::T_Y + half * HC + c0, y);
+                    tmem_wait_ld();
+                    const float *bp = sbproj + half * HC + c0;
+                    uint4 *d4 = reinterpret_cast<uint4 *>(srow + c0 * 2);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        d4[c] = make_uint4(pack_bf16x2(y[8 * c] + bp[8 * c], y[8 * c + 1] + bp[8 * c + 1]),
+                                           pack_bf16x2(y[8 * c + 2] + bp[8 * c + 2], y[8 * c + 3] + bp[8 * c + 3]),
+                                           pack_bf16x2(y[8 * c + 4] + bp[8 * c + 4], y[8 * c + 5] + bp[8 * c + 5]),
+                                           pack_bf16x2(y[8 * c + 6] + bp[8 * c + 6], y[8 * c + 7] + bp[8 * c + 7]));
+                }
+                tc_fence_before();
+                if (compute_sync_or(failed)) { failed = true; break; }
+                constexpr int CH = C / 8;   // 16-byte chunks per row
+#pragma unroll 1
+                for (int q = tid; q < 128 * CH; q += NCOMPUTE) {
+                    const int r = q / CH, c16 = q % CH;
+                    const int tk = tok_cur[r];
+                    if (tk >= 0)
+                        *reinterpret_cast<uint4 *>(a.out + (int64_t)tk * C + c16 * 8) =
+                            *reinterpret_cast<const uint4 *>(stage + r * F::SROW + c16 * 16);
+                }
             }
+            PHASE(k, 20);
         }
-        PHASE(k, 20);
-        tc_fence_before();
+        cp_async_wait<0>();
+        if (failed) *abort_flag = 1;
     }
-    cp_async_wait<0>();
 #ifdef SWIN_PHASE_TRACE
     if (tid == 0) {
         unsigned smid;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
         g_cta_trace[blockIdx.x * 4 + 1] = (long long)global_timer_ns();
-        g_cta_trace[blockIdx.x * 4 + 2] = k;
         g_cta_trace[blockIdx.x * 4 + 3] = smid;
     }
 #endif
-    if (failed) atomicOr(st.err, ERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (tid == 0 && *abort_flag) atomicOr(st.err, ERR_TIMEOUT);
+    if (is_mma) {
+        __syncwarp();
+        tmem_dealloc(tmem, 512);
+    }
 }
 
 int num_sms()

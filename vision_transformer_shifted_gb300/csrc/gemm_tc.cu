@@ -218,7 +218,98 @@ cudaError_t launch_impl(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+// Test kernel of the TMEM-A form of the MMA: each thread writes its A row
+// (K <= 128 bf16, packed in pairs) into TMEM columns 256.., B (N <= 256 rows,
+// K-major, 128-byte swizzle) goes to shared memory, then K/16 MMAs read A from
+// TMEM and accumulate D in columns 0..N-1.
+__global__ void __launch_bounds__(THREADS) gemm_ts_test_kernel(GemmArgs a, DeviceStatus st)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_align(smem_raw, 1024);
+    uint8_t *sB = smem;                                          // 2 K blocks x [N rows][128 B]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 2 * 256 * 128);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int64_t m0 = (int64_t)blockIdx.x * BM;
+    const int N = a.N, K = a.K;
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(smem_u32(bar), 1);
+        mbar_init_fence();
+    }
+    // B rows -> shared memory (zero past K)
+    for (int q = tid; q < N * 16; q += THREADS) {
+        const int n = q / 16, c16 = q % 16;
+        const int k0 = c16 * 8;
+        const bool ok = k0 < K;
+        cp_async16(smem_u32(sB) + (c16 >> 3) * (256 * 128) + sw128_offset(n, c16 & 7),
+                   ok ? a.Bw + (int64_t)n * K + k0 : a.Bw, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    // A row of this thread -> TMEM columns 256 + (K/2), zeros past the end
+    {
+        const int64_t R = m0 + tid;
+        for (int c0 = 0; c0 < K / 2; c0 += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int k = 2 * (c0 + i);
+                r[i] = R < a.rows ? *reinterpret_cast<const uint32_t *>(a.A + R * a.lda + k) : 0u;
+            }
+            tmem_st16(t_lane + 256 + c0, r);
+        }
+        tmem_wait_st();
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        const uint32_t id = idesc_bf16(BM, N);
+        for (int kk = 0; kk < K / 16; ++kk)
+            mma_bf16_ts(tmem, tmem + 256 + 8 * kk,
+                        desc_kmajor_sw128(smem_u32(sB) + (kk >> 2) * (256 * 128) + 32 * (kk & 3)), id, kk != 0);
+        mma_commit(smem_u32(bar));
+    }
+    const bool ok = mbar_wait(smem_u32(bar), 0, st.wait_ns);
+    tc_fence_after();
+    const int64_t R = m0 + tid;
+    for (int c0 = 0; c0 < N; c0 += 16) {
+        float v[16];
+        tmem_ld16(t_lane + c0, v);
+        tmem_wait_ld();
+        if (R < a.rows && ok) {
+            float b[16];
+            for (int i = 0; i < 16; ++i) b[i] = a.bias ? __bfloat162float(a.bias[c0 + i]) : 0.f;
+            store_row_bf16(a.D + R * a.ldd + c0, v, b, 16);
+        }
+    }
+    if (!ok && tid == 0) atomicOr(st.err, ERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 } // namespace
+
+cudaError_t launch_gemm_ts_test(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
+{
+    if (a.K % 32 || a.K > 128 || a.N % 16 || a.N > 256 || a.rows <= 0) return cudaErrorInvalidValue;
+    const size_t smem = 1024 + 2 * 256 * 128 + 64;
+    cudaError_t e = cudaFuncSetAttribute(gemm_ts_test_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    gemm_ts_test_kernel<<<(unsigned)((a.rows + BM - 1) / BM), THREADS, smem, stream>>>(a, st);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, DeviceStatus st, cudaStream_t stream)
 {
