@@ -13,8 +13,10 @@
 //       normalises q and k to unit length in fp32 while draining
 //   S3-S5 per head: S = q k^T (128 x 128 x 32) into TMEM; softmax of each
 //       row over its own window's keys with the relative bias and the shift
-//       mask computed from coordinates (fp32, exp2); P to shared memory
-//   S6  o_h = P v_h (128 x 32 x 128) into TMEM
+//       mask computed from coordinates (fp32, exp2); P (bf16) back into TMEM
+//       over the S columns
+//   S6  o_h = P v_h (128 x 32 x 128) into TMEM, with P read from TMEM as the
+//       A operand (so P never touches shared memory)
 //   S7  y = (o / rowsum) Wproj^T on tcgen05, o staged as bf16 in the freed X
 //       buffer
 //   S8  y + bproj written straight from registers through the window
@@ -211,10 +213,6 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
         for (int i = tid; i < C; i += NCOMPUTE) sbproj[i] = a.bproj ? __bfloat162float(a.bproj[i]) : 0.f;
         if (tid < HEADS)
             sscale[tid] = a.mode == 1 ? FLOG2E / fmaxf(a.tau[tid], 0.01f) : FLOG2E * rsqrtf(32.0f);
-        // P: the off-diagonal blocks (slot 0 rows x window-B keys and the
-        // reverse) stay zero for the whole kernel
-        for (int i = tid; i < 2 * 128 * 128 / 16; i += NCOMPUTE)
-            reinterpret_cast<uint4 *>(sm + F::P)[i] = make_uint4(0, 0, 0, 0);
     }
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
@@ -268,7 +266,7 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
     if (is_mma) {
         // ===================== MMA warp (lane 0 issues) =====================
         if (lane == 0) {
-            uint32_t ph_qk = 0, ph_p = 0, ph_o = 0, ph_free = 0;
+            uint32_t ph_qk = 0, ph_p = 0, ph_o = 0, ph_free = 0, ph_pv_m = 0;
             const uint32_t id_qk = idesc_bf16(128, 2 * C), id_vt = idesc_bf16(128, 128);
             const uint32_t id_s = idesc_bf16(128, 128), id_pv = idesc_bf16(128, 32), id_y = idesc_bf16(128, C);
             auto issue_qkv = [&](int buf) {
@@ -310,11 +308,16 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const int kb = kk >> 2, ks = kk & 3;
-                        mma_bf16(tmem + F::T_O + 32 * hd, desc_kmajor_sw128(base + F::P + kb * (128 * 128) + 32 * ks),
-                                 desc_kmajor_sw128(base + F::VT + kb * F::VT_BLK + (hd * 32 / 8) * 1024 + 32 * ks),
-                                 id_pv, kk != 0);
+                        mma_bf16_ts(tmem + F::T_O + 32 * hd, tmem + F::T_S + 8 * kk,
+                                    desc_kmajor_sw128(base + F::VT + kb * F::VT_BLK + (hd * 32 / 8) * 1024 + 32 * ks),
+                                    id_pv, kk != 0);
                     }
                     mma_commit(B_PV);
+                    // the next MMA that writes these TMEM columns (S of the next head,
+                    // or the next tile's QKV) waits until P.V has read P
+                    ok = wait_or_abort(B_PV, ph_pv_m, st.wait_ns, abort_flag);
+                    ph_pv_m ^= 1;
+                    if (!ok) break;
                 }
                 if (!ok) break;
                 // next tile's QKV as soon as this tile's softmax has freed its TMEM
@@ -516,14 +519,15 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
                     if (!wait_or_abort(B_PV, ph_pv, st.wait_ns, abort_flag)) failed = true;
                     ph_pv ^= 1;
                 }
+                // P (bf16, two keys per 32-bit column) goes to TMEM over the first 64
+                // columns of S, the A operand of the P.V MMA: row r holds its window's
+                // keys in columns 32*slot .. +31 and zeros for the other window's
                 {
-                    uint8_t *dst = sm + F::P + slot * (128 * 128);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4 *>(dst + sw128_offset(row, 4 * half + c)) =
-                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    tmem_st16(t_lane + F::T_S + 32 * slot + 16 * half, pk);
+                    const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                    tmem_st16(t_lane + F::T_S + 32 * (slot ^ 1) + 16 * half, zero);
+                    tmem_wait_st();
                 }
-                fence_proxy_async_smem();
                 warp_arrive(R_P, lane);
                 PHASE(k, 7 + 4 * hd);
                 if (hd + 1 < HEADS) drain_qk(hd + 1);
