@@ -20,13 +20,17 @@ extern "C" {
  * (pages: "Boosting Swin Transformer Speed", Training Optimization -- the
  * partition/shift index maps; Inference Optimization -- QKV GEMM with bias).
  *   qkv[r, o] = sum_c x[b, (wi*M+ti+s) mod H, (wj*M+tj+s) mod W, c] * Wqkv[o, c] + bqkv[o]
- * qkv is [B*H*W, 3C] bf16 in window order.  bf16 mode only. */
+ * qkv is [B*H*W, 3C] bf16 in window order.  In V2 mode every q and k head
+ * (32 columns) is scaled to unit L2 norm (norm clamped at 1e-12) after the
+ * bias, before rounding, as the attention stage expects.  bf16 mode only. */
 int swin_wattn_test_qkv(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv,
                         const void *bqkv, void *qkv, swin_stream_t stream);
 
 /* Per-window, per-head attention on a window-ordered qkv buffer: logits (V1 or
- * V2) + relative bias + shift mask, softmax, P.V.  attn is [B*H*W, C] bf16 in
- * window order, channel head*d + e.  bf16 mode only. */
+ * V2) + relative bias + shift mask, softmax, P.V.  In V2 mode q and k must
+ * already be unit vectors (as swin_wattn_test_qkv writes them), so q.k is the
+ * cosine.  attn is [B*H*W, C] bf16 in window order, channel head*d + e.  bf16
+ * mode only. */
 int swin_wattn_test_attn(swin_wattn_t h, const void *qkv, int B, int H, int W,
                          const void *bias_table, const float *logit_scale, void *attn,
                          swin_stream_t stream);
@@ -44,7 +48,9 @@ int swin_wattn_test_proj(swin_wattn_t h, const void *attn, int B, int H, int W,
  * swizzle_bytes selects the operand layout: 128 (K blocks of 64 in 128-byte
  * swizzled shared memory, as the three-kernel path), 64 (K blocks of 32 in
  * 64-byte swizzled shared memory, as the fused kernel) or 0 (A staged in
- * tensor memory, the MMA form that reads A from TMEM; K <= 128, N <= 256). */
+ * tensor memory, the MMA form that reads A from TMEM; K <= 128, N <= 256) or
+ * -64 (Bw given as [K, N] row-major and used as an N-major operand, 64-byte
+ * swizzle; N = 32 or 64, K <= 128). */
 int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *D, int rows, int N,
                          int K, int swizzle_bytes, swin_stream_t stream);
 

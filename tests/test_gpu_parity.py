@@ -61,6 +61,26 @@ def test_gemm_block(rows, N, K, swizzle):
     assert (err <= ref.abs() * 2.0 ** -8 + 1e-4).all(), float(err.max())
 
 
+@pytest.mark.parametrize("rows,N,K", [(128, 32, 32), (200, 32, 128), (77, 64, 64), (300, 64, 112)])
+def test_gemm_b_mn_major(rows, N, K):
+    """An N-major B operand (64-byte swizzle): B given as [K, N] row-major."""
+    g = torch.Generator().manual_seed(11 * rows + N + K)
+    A = torch.randn(rows, K, generator=g).bfloat16()
+    Bkn = (torch.randn(K, N, generator=g) * 0.1).bfloat16()
+    bias = (torch.randn(N, generator=g) * 0.1).bfloat16()
+    D = torch.empty(rows, N, dtype=torch.bfloat16, device=DEV)
+    # the hook reads N from Bw.shape[0]: pass a [N, K]-shaped view of the [K, N] data
+    Ad, Bd, bd = A.to(DEV), Bkn.to(DEV), bias.to(DEV)
+    rc = sw.load().swin_wattn_test_gemm(ctypes.c_void_p(Ad.data_ptr()), ctypes.c_void_p(Bd.data_ptr()),
+                                        ctypes.c_void_p(bd.data_ptr()), ctypes.c_void_p(D.data_ptr()),
+                                        rows, N, K, -64, None)
+    assert rc == sw.OK
+    torch.cuda.synchronize()
+    ref = A.double() @ Bkn.double() + bias.double()
+    err = (D.double().cpu() - ref).abs()
+    assert (err <= ref.abs() * 2.0 ** -8 + 1e-4).all(), float(err.max())
+
+
 @pytest.mark.parametrize("rows,N,K", [(128, 32, 32), (200, 128, 128), (77, 256, 64), (384, 96, 96)])
 def test_gemm_a_from_tmem(rows, N, K):
     """The MMA form that reads A from tensor memory (two bf16 of K per column)."""

@@ -106,6 +106,7 @@ int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void 
     GemmArgs k1{};
     k1.A = (const bf16 *)x; k1.lda = h->C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
     k1.D = qkv; k1.ldd = 3 * h->C; k1.rows = g.T; k1.N = 3 * h->C; k1.K = h->C; k1.g = g;
+    k1.norm_cols = h->mode == SWIN_WATTN_V2 ? 2 * h->C : 0;
     cudaError_t e = launch_gemm(k1, LOAD_GATHER, STORE_PLAIN, dstatus(h), stream);
     if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
     AttnArgs k2{};
@@ -300,6 +301,7 @@ int swin_wattn_test_qkv(swin_wattn_t h, const void *x, int B, int H, int W, cons
     GemmArgs k1{};
     k1.A = (const bf16 *)x; k1.lda = h->C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
     k1.D = (bf16 *)qkv; k1.ldd = 3 * h->C; k1.rows = g.T; k1.N = 3 * h->C; k1.K = h->C; k1.g = g;
+    k1.norm_cols = h->mode == SWIN_WATTN_V2 ? 2 * h->C : 0;
     return cuda_status(launch_gemm(k1, LOAD_GATHER, STORE_PLAIN, dstatus(h), (cudaStream_t)stream));
 }
 
@@ -337,8 +339,9 @@ int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *
                          int swizzle_bytes, swin_stream_t stream)
 {
     if (!A || !Bw || !D || rows < 0 || N <= 0 || K <= 0 || N % 16 || K % 16 || N > 2048) return SWIN_WATTN_EINVAL;
-    if (swizzle_bytes != 0 && swizzle_bytes != 64 && swizzle_bytes != 128) return SWIN_WATTN_EINVAL;
+    if (swizzle_bytes != 0 && swizzle_bytes != 64 && swizzle_bytes != 128 && swizzle_bytes != -64) return SWIN_WATTN_EINVAL;
     if (swizzle_bytes == 0 && (K % 32 || K > 128 || N > 256)) return SWIN_WATTN_EINVAL;
+    if (swizzle_bytes == -64 && (K > 128 || (N != 32 && N != 64))) return SWIN_WATTN_EINVAL;
     if (!aligned16(A) || !aligned16(Bw) || !aligned16(D) || (bias && !aligned16(bias))) return SWIN_WATTN_EINVAL;
     if (rows == 0) return SWIN_WATTN_OK;
     GemmArgs a{};
@@ -350,6 +353,7 @@ int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *
     const DeviceStatus st{d_err, 2000000000ull};
     if (swizzle_bytes == 64) return cuda_status(launch_gemm_sw64(a, st, (cudaStream_t)stream));
     if (swizzle_bytes == 0) return cuda_status(launch_gemm_ts_test(a, st, (cudaStream_t)stream));
+    if (swizzle_bytes == -64) return cuda_status(launch_gemm_mn_test(a, st, (cudaStream_t)stream));
     return cuda_status(launch_gemm(a, LOAD_PLAIN, STORE_PLAIN, st, (cudaStream_t)stream));
 }
 

@@ -12,15 +12,23 @@
 // coordinates).  The mask and the relative index are computed from window
 // coordinates; neither is loaded.  Softmax in fp32 with exp2 (logits carry
 // a log2(e) factor), P rounded to bf16 for the P.V MMA, 1/rowsum applied to
-// the fp32 P.V result.
+// the fp32 P.V result.  In V2 the QKV projection has already scaled every q
+// and k head to unit length, so q.k is the cosine.
+//
+// q, k and v rows (64 bytes per head) are copied with cp.async into
+// 64-byte-swizzled tiles; v is used in that [key][d] layout as an N-major B
+// operand, so no transpose is ever written.
 //
 // Small windows (N <= 64, e.g. M = 7 or 8): one CTA takes two windows of one
 // head; window A fills rows 0..63 and window B rows 64..127 of a 128-row MMA
 // tile, so QK^T is one 128x128x32 MMA whose off-diagonal blocks are ignored,
 // and P.V is one 128x32x128 MMA with P zero outside each row's own window.
-// Large windows (N > 64, e.g. M = 24, N = 576): one CTA takes 128 queries of
-// one window and head and walks the keys in tiles of 128 with an online
-// softmax, accumulating o in registers.
+// Large windows (N > 64, e.g. M = 24, N = 576): one CTA of 256 threads takes
+// 128 queries of one window and head (two threads per query row, 64 keys
+// each) and walks the keys in double-buffered tiles of 128 with an online
+// softmax; P goes back into TMEM and P.V reads it from there.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -28,103 +36,33 @@ namespace swin {
 
 namespace {
 
-constexpr int THREADS = 128;
 constexpr float LOG2E = 1.4426950408889634f;
 
-// Shared memory: Q and K tiles as 128 rows x 128 B (first 64 B = d 32 used),
-// V^T as 32 rows x 128 keys (two 64-key K blocks), P as 128 rows x 128 keys
-// (two K blocks), all K-major 128B-swizzled.
-struct AttnSmem {
-    static constexpr int q_off = 0;
-    static constexpr int k_off = q_off + 128 * 128;
-    static constexpr int vt_off = k_off + 128 * 128;
-    static constexpr int p_off = vt_off + 2 * 32 * 128;
-    static constexpr int end = p_off + 2 * 128 * 128;
-    static size_t bytes(int M) { return 1024 + end + (size_t)(2 * M - 1) * (2 * M - 1) * 4 + 128 * 8 + 64; }
-};
+// Optional phase trace of the large-window kernel (-DSWIN_PHASE_TRACE only):
+// thread 0 of CTA (blockIdx.x = 3, head 0) records clock64() per key tile.
+#ifdef SWIN_PHASE_TRACE
+__device__ long long g_flash_trace[8 * 16];
+#define FPHASE(kt, i)                                                                              \
+    do {                                                                                           \
+        if (blockIdx.x == 3 && blockIdx.y == 0 && tid == 0 && (kt) < 8) g_flash_trace[(kt) * 16 + (i)] = clock64(); \
+    } while (0)
+#else
+#define FPHASE(kt, i) \
+    do {              \
+    } while (0)
+#endif
 
-// Loads one 32-wide head slice (64 bytes) of a qkv row.
-__device__ __forceinline__ void load_head_row(const bf16 *src, bool valid, uint4 (&v)[4])
+// Copies the 64-byte head slice of `rows` qkv rows (part 0 = q, 1 = k, 2 = v)
+// into a 64-byte-swizzled tile, zero rows where row_ok is false; each thread
+// handles chunk `tid & 3` of rows tid/4, tid/4 + nthreads/4, ...
+__device__ __forceinline__ void load_rows_sw64(uint32_t tile, int tid, int nthreads, int rows,
+                                               const bf16 *const *row_src, const bf16 *any_valid)
 {
-    if (valid) {
-        const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = s4[i];
-    } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = make_uint4(0, 0, 0, 0);
+    for (int q = tid; q < rows * 4; q += nthreads) {
+        const int r = q >> 2, c = q & 3;
+        const bf16 *src = row_src[r];
+        cp_async16(tile + sw64_offset(r, c), src ? src + c * 8 : any_valid, src ? 16u : 0u);
     }
-}
-
-// V2: scales a 32-element bf16 row to unit L2 norm (norm clamped at 1e-12)
-// in fp32 and rounds it back to bf16.
-__device__ __forceinline__ void l2_normalise(uint4 (&v)[4])
-{
-    float f[32];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 p = unpack_bf16x2(w[j]);
-            f[8 * i + 2 * j] = p.x;
-            f[8 * i + 2 * j + 1] = p.y;
-        }
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) ss = fmaf(f[i], f[i], ss);
-    const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[i].x = pack_bf16x2(f[8 * i + 0] * inv, f[8 * i + 1] * inv);
-        v[i].y = pack_bf16x2(f[8 * i + 2] * inv, f[8 * i + 3] * inv);
-        v[i].z = pack_bf16x2(f[8 * i + 4] * inv, f[8 * i + 5] * inv);
-        v[i].w = pack_bf16x2(f[8 * i + 6] * inv, f[8 * i + 7] * inv);
-    }
-}
-
-// Writes a 32-element row (4 x 16 B) into row `row` of a 128B-swizzled tile.
-__device__ __forceinline__ void store_row_sw128(uint8_t *tile, int row, const uint4 (&v)[4])
-{
-#pragma unroll
-    for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(tile + sw128_offset(row, c)) = v[c];
-}
-
-// Writes v (32 elements of key `key`, 0..127) as column `key` of V^T
-// (32 rows e x 128 keys, two 64-key K blocks of 32 x 128 B).
-__device__ __forceinline__ void store_vt_column(uint8_t *vt, int key, const uint4 (&v)[4])
-{
-    uint8_t *blk = vt + (key >> 6) * (32 * 128);
-    const int kk = key & 63;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e0 = 8 * i + 2 * j;
-            *reinterpret_cast<uint16_t *>(blk + sw128_offset(e0, kk >> 3) + (kk & 7) * 2) = (uint16_t)(w[j] & 0xFFFF);
-            *reinterpret_cast<uint16_t *>(blk + sw128_offset(e0 + 1, kk >> 3) + (kk & 7) * 2) = (uint16_t)(w[j] >> 16);
-        }
-    }
-}
-
-// Writes 64 probabilities (bf16-packed in pairs) as the 64-key K block `kb`
-// of row `row` of the P tile.
-__device__ __forceinline__ void store_p_block(uint8_t *ptile, int row, int kb, const uint32_t (&pk)[32])
-{
-    uint8_t *blk = ptile + kb * (128 * 128);
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-}
-
-__device__ __forceinline__ void zero_p_block(uint8_t *ptile, int row, int kb)
-{
-    uint8_t *blk = ptile + kb * (128 * 128);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c)) = make_uint4(0, 0, 0, 0);
 }
 
 // Region id (row band * 3 + column band) of in-window token (ti, tj) of
@@ -135,54 +73,44 @@ __device__ __forceinline__ int token_region(const Geom &g, int wi, int wj, int t
     return 3 * shift_band(wi * g.M + ti, g.H, g.M, g.s) + shift_band(wj * g.M + tj, g.W, g.M, g.s);
 }
 
-// Stores an o row (32 fp32 scaled by inv_l) as bf16 to attn.
-__device__ __forceinline__ void store_o_row(bf16 *dst, const float (&o)[32], float inv_l)
+// Stores n o values (fp32 scaled by inv_l) as bf16 to attn.
+template <int NV>
+__device__ __forceinline__ void store_o(bf16 *dst, const float *o, float inv_l)
 {
     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 u;
-        u.x = pack_bf16x2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l);
-        u.y = pack_bf16x2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l);
-        u.z = pack_bf16x2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l);
-        u.w = pack_bf16x2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l);
-        d4[q] = u;
-    }
+    for (int q = 0; q < NV / 8; ++q)
+        d4[q] = make_uint4(pack_bf16x2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l),
+                           pack_bf16x2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l),
+                           pack_bf16x2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l),
+                           pack_bf16x2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l));
 }
 
-struct KernelCommon {
-    uint8_t *smem;
-    float *sbias;
-    uint64_t *bar;
-    uint32_t *tmem_slot;
+// ---------------------------------------------------------------------------
+// Two windows per CTA, N <= 64 (128 threads, one per tile row).
+// ---------------------------------------------------------------------------
+struct Pack2Smem {
+    static constexpr int q_off = 0;                    // [128][64 B] SW64
+    static constexpr int k_off = q_off + 128 * 64;
+    static constexpr int v_off = k_off + 128 * 64;     // [128 keys][64 B] SW64 (N-major B)
+    static constexpr int p_off = v_off + 128 * 64;     // 2 K blocks x [128][128 B] SW128
+    static constexpr int end = p_off + 2 * 128 * 128;
+    static size_t bytes(int M) { return 1024 + end + (size_t)(2 * M - 1) * (2 * M - 1) * 4 + 128 * 3 * 8 + 64; }
 };
 
-__device__ __forceinline__ KernelCommon setup_smem(uint8_t *smem_raw, int M)
-{
-    KernelCommon k;
-    k.smem = smem_align(smem_raw, 1024);
-    k.sbias = reinterpret_cast<float *>(k.smem + AttnSmem::end);
-    const int L2 = (2 * M - 1) * (2 * M - 1);
-    uint8_t *after = reinterpret_cast<uint8_t *>(k.sbias + L2);
-    after = smem_align(after, 8);
-    k.bar = reinterpret_cast<uint64_t *>(after);
-    k.tmem_slot = reinterpret_cast<uint32_t *>(k.bar + 1);
-    return k;
-}
-
-// ---------------------------------------------------------------------------
-// Two windows per CTA, N <= 64.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(THREADS) attn_pack2_kernel(AttnArgs a, DeviceStatus st)
+__global__ void __launch_bounds__(128) attn_pack2_kernel(AttnArgs a, DeviceStatus st)
 {
     extern __shared__ uint8_t smem_raw[];
     const Geom g = a.g;
     const int M = g.M, N = g.N, C = g.C, L = 2 * M - 1;
-    KernelCommon kc = setup_smem(smem_raw, M);
-    uint8_t *sQ = kc.smem + AttnSmem::q_off;
-    uint8_t *sK = kc.smem + AttnSmem::k_off;
-    uint8_t *sVt = kc.smem + AttnSmem::vt_off;
-    uint8_t *sP = kc.smem + AttnSmem::p_off;
+    uint8_t *sm = smem_align(smem_raw, 1024);
+    float *sbias = reinterpret_cast<float *>(sm + Pack2Smem::end);
+    const bf16 **srcs = reinterpret_cast<const bf16 **>(smem_align(reinterpret_cast<uint8_t *>(sbias + L * L), 8));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(srcs + 3 * 128);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
+    const uint32_t sQ = smem_u32(sm + Pack2Smem::q_off), sK = smem_u32(sm + Pack2Smem::k_off),
+                   sV = smem_u32(sm + Pack2Smem::v_off);
+    uint8_t *sP = sm + Pack2Smem::p_off;
     __shared__ int8_t key_region[2][64];
     __shared__ int16_t key_off[64];
 
@@ -197,56 +125,48 @@ __global__ void __launch_bounds__(THREADS) attn_pack2_kernel(AttnArgs a, DeviceS
     const int wi = rem / g.nw, wj = rem % g.nw;
     const int ti = t / M, tj = t % M;
 
-    // bias column of this head, times log2(e)
-    for (int i = tid; i < L * L; i += THREADS) kc.sbias[i] = __bfloat162float(a.table[(int64_t)i * a.heads + head]) * LOG2E;
-    // this thread's token as a key: its region in its window (-1 for padding), its offset
+    // q, k, v rows of this thread's token (null for padding rows)
+    {
+        const bf16 *base = row_ok ? a.qkv + (win * N + t) * (int64_t)(3 * C) + head * 32 : nullptr;
+        srcs[tid] = base;
+        srcs[128 + tid] = base ? base + C : nullptr;
+        srcs[256 + tid] = base ? base + 2 * C : nullptr;
+    }
+    for (int i = tid; i < L * L; i += 128) sbias[i] = __bfloat162float(a.table[(int64_t)i * a.heads + head]) * LOG2E;
     key_region[slot][t] = (int8_t)(t < N ? token_region(g, wi, wj, ti, tj) : -1);
     if (slot == 0) key_off[t] = (int16_t)(ti * L + tj);
     if (tid == 0) {
-        mbar_init(smem_u32(kc.bar), 1);
+        mbar_init(smem_u32(bar), 1);
         mbar_init_fence();
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(kc.tmem_slot), 128);
+        tmem_alloc(smem_u32(tmem_slot), 128);
         tmem_relinquish();
     }
-
-    // q, k, v rows of this thread's token (zeros for padding rows)
-    {
-        const bf16 *base = a.qkv + ((win_ok ? win : 0) * N + (t < N ? t : 0)) * (int64_t)(3 * C) + head * 32;
-        uint4 q[4], k[4], v[4];
-        load_head_row(base, row_ok, q);
-        load_head_row(base + C, row_ok, k);
-        load_head_row(base + 2 * C, row_ok, v);
-        if (a.mode == 1 && row_ok) {
-            l2_normalise(q);
-            l2_normalise(k);
-        }
-        store_row_sw128(sQ, tid, q);
-        store_row_sw128(sK, tid, k);
-        store_vt_column(sVt, tid, v);
-    }
+    __syncthreads();
+    load_rows_sw64(sQ, tid, 128, 128, srcs, a.qkv);
+    load_rows_sw64(sK, tid, 128, 128, srcs + 128, a.qkv);
+    load_rows_sw64(sV, tid, 128, 128, srcs + 256, a.qkv);
+    cp_async_commit();
+    cp_async_wait<0>();
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *kc.tmem_slot;
-    const uint32_t bar = smem_u32(kc.bar);
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t barp = smem_u32(bar);
 
     if (tid == 0) {
         const uint32_t id = idesc_bf16(128, 128);
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
-            mma_bf16(tmem, desc_kmajor_sw128(smem_u32(sQ) + 32 * k), desc_kmajor_sw128(smem_u32(sK) + 32 * k), id, k);
-        mma_commit(bar);
+        for (int k = 0; k < 2; ++k) mma_bf16(tmem, desc_kmajor_sw64(sQ + 32 * k), desc_kmajor_sw64(sK + 32 * k), id, k);
+        mma_commit(barp);
     }
-    bool failed = !mbar_wait(bar, 0, st.wait_ns);
+    bool failed = !mbar_wait(barp, 0, st.wait_ns);
     tc_fence_after();
 
     // ---- softmax of this thread's row over its own window's 64 key columns ----
-    float scale;
-    if (a.mode == 1) scale = LOG2E / fmaxf(a.tau[head], 0.01f);
-    else scale = LOG2E * rsqrtf(32.0f);
+    const float scale = a.mode == 1 ? LOG2E / fmaxf(a.tau[head], 0.01f) : LOG2E * rsqrtf(32.0f);
     float l = 1.f;
     {
         float s[64];
@@ -269,7 +189,7 @@ __global__ void __launch_bounds__(THREADS) attn_pack2_kernel(AttnArgs a, DeviceS
         for (int j = 0; j < 64; ++j) {
             float v = -INFINITY;
             if (j < N) {
-                const float lv = fmaf(s[j], scale, kc.sbias[base - key_off[j]]);
+                const float lv = fmaf(s[j], scale, sbias[base - key_off[j]]);
                 v = key_region[slot][j] == my_region ? lv : -INFINITY;
             }
             s[j] = v;
@@ -285,9 +205,14 @@ __global__ void __launch_bounds__(THREADS) attn_pack2_kernel(AttnArgs a, DeviceS
             pk[j / 2] = pack_bf16x2(p0, p1);
         }
         l = sum;
-        if (row_ok) store_p_block(sP, tid, slot, pk);
-        else zero_p_block(sP, tid, slot);
-        zero_p_block(sP, tid, slot ^ 1);
+        // P row: own window's keys in K block `slot`, zeros in the other block
+        uint8_t *own = sP + slot * (128 * 128), *other = sP + (slot ^ 1) * (128 * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4 *>(own + sw128_offset(tid, c)) =
+                row_ok ? make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(other + sw128_offset(tid, c)) = make_uint4(0, 0, 0, 0);
+        }
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -296,21 +221,21 @@ __global__ void __launch_bounds__(THREADS) attn_pack2_kernel(AttnArgs a, DeviceS
 
     if (!failed) {
         if (tid == 0) {
-            const uint32_t id = idesc_bf16(128, 32);
+            const uint32_t id = idesc_bf16_bmn(128, 32);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int kb = k >> 2, ks = k & 3;
                 mma_bf16(tmem, desc_kmajor_sw128(smem_u32(sP) + kb * 16384 + 32 * ks),
-                         desc_kmajor_sw128(smem_u32(sVt) + kb * 4096 + 32 * ks), id, k);
+                         desc_mnmajor_sw64(sV + 1024 * k, 128 * 64), id, k);
             }
-            mma_commit(bar);
+            mma_commit(barp);
         }
-        failed = !mbar_wait(bar, 1, st.wait_ns);
+        failed = !mbar_wait(barp, 1, st.wait_ns);
         tc_fence_after();
         float o[32];
         tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), o);
         tmem_wait_ld();
-        if (row_ok && !failed) store_o_row(a.attn + (win * N + t) * (int64_t)C + head * 32, o, rcp_approx(l));
+        if (row_ok && !failed) store_o<32>(a.attn + (win * N + t) * (int64_t)C + head * 32, o, rcp_approx(l));
     }
     if (failed) atomicOr(st.err, ERR_TIMEOUT);
     tc_fence_before();
@@ -319,88 +244,119 @@ __global__ void __launch_bounds__(THREADS) attn_pack2_kernel(AttnArgs a, DeviceS
 }
 
 // ---------------------------------------------------------------------------
-// Large windows: 128 queries per CTA, keys in tiles of 128, online softmax.
+// Large windows: 128 queries per CTA, 256 threads (two per query row), keys
+// in double-buffered tiles of 128, online softmax, P in TMEM.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(THREADS) attn_flash_kernel(AttnArgs a, DeviceStatus st)
+constexpr int FL_THREADS = 256;
+
+struct FlashSmem {
+    static constexpr int q_off = 0;                    // [128][64 B] SW64
+    static constexpr int k_off = q_off + 128 * 64;     // 2 x [128][64 B] SW64
+    static constexpr int v_off = k_off + 2 * 128 * 64; // 2 x [128 keys][64 B] SW64 (N-major B)
+    static constexpr int end = v_off + 2 * 128 * 64;
+    static size_t bytes(int M)
+    {
+        return 1024 + end + (size_t)(2 * M - 1) * (2 * M - 1) * 4 + 2 * 128 * 4 * 2 + 2 * 2 * 128 * 4 + 64;
+    }
+};
+
+// (two CTAs per SM: 2 x 8 warps at <= 128 registers fit each sub-partition's
+// register file, and 2 x 256 TMEM columns fit the SM's 512)
+__global__ void __launch_bounds__(FL_THREADS, 2)
+    attn_flash_kernel(AttnArgs a, DeviceStatus st, const __grid_constant__ CUtensorMap tmap)
 {
     extern __shared__ uint8_t smem_raw[];
     const Geom g = a.g;
     const int M = g.M, N = g.N, C = g.C, L = 2 * M - 1;
-    KernelCommon kc = setup_smem(smem_raw, M);
-    uint8_t *sQ = kc.smem + AttnSmem::q_off;
-    uint8_t *sK = kc.smem + AttnSmem::k_off;
-    uint8_t *sVt = kc.smem + AttnSmem::vt_off;
-    uint8_t *sP = kc.smem + AttnSmem::p_off;
-    __shared__ int key_region[128];
-    __shared__ int key_off[128];
+    uint8_t *sm = smem_align(smem_raw, 1024);
+    // after the tiles (1024-aligned): key_off first, so that its int4 loads are
+    // 16-byte aligned, then the other per-key and per-row arrays, then the bias
+    int *key_off = reinterpret_cast<int *>(sm + FlashSmem::end);        // [2 buffers][128]
+    int *key_region = key_off + 2 * 128;                                 // [2][128], -1 past N
+    float *smax = reinterpret_cast<float *>(key_region + 2 * 128);       // [2][128]
+    float *spart = smax + 2 * 128;                                       // [2][128]
+    float *sbias = spart + 2 * 128;                                      // [L*L], times log2(e)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_align(reinterpret_cast<uint8_t *>(sbias + L * L), 8));
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4);
+    const uint32_t sQ = smem_u32(sm + FlashSmem::q_off), sK = smem_u32(sm + FlashSmem::k_off),
+                   sV = smem_u32(sm + FlashSmem::v_off);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;
     const int head = blockIdx.y;
     const int qtiles = (N + 127) / 128;
     const int64_t win = blockIdx.x / qtiles;
-    const int q0 = (blockIdx.x % qtiles) * 128;
+    const int q0 = (int)(blockIdx.x % qtiles) * 128;
     const int per = g.nh * g.nw;
     const int rem = (int)(win % per);
     const int wi = rem / g.nw, wj = rem % g.nw;
-    const int qt = q0 + tid;
+    const bool masked = g.s > 0 && (wi == g.nh - 1 || wj == g.nw - 1);
+    const int qt = q0 + row;
     const bool row_ok = qt < N;
     const int qi = row_ok ? qt / M : 0, qj = row_ok ? qt % M : 0;
     const int my_region = token_region(g, wi, wj, qi, qj);
     const int base = (qi + M - 1) * L + (qj + M - 1);
     const bf16 *wbase = a.qkv + win * N * (int64_t)(3 * C) + head * 32;
+    const int ktiles = (N + 127) / 128;
 
-    for (int i = tid; i < L * L; i += THREADS) kc.sbias[i] = __bfloat162float(a.table[(int64_t)i * a.heads + head]) * LOG2E;
+    for (int i = tid; i < L * L; i += FL_THREADS)
+        sbias[i] = __bfloat162float(a.table[(int64_t)i * a.heads + head]) * LOG2E;
+    // bars: 0 = S done, 1 = P.V done, 2 + b = key buffer b full (TMA transactions)
     if (tid == 0) {
-        mbar_init(smem_u32(kc.bar), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
         mbar_init_fence();
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(kc.tmem_slot), 256);
+        tmem_alloc(smem_u32(tmem_slot), 256);
         tmem_relinquish();
     }
-    {
-        uint4 q[4];
-        load_head_row(wbase + (int64_t)(row_ok ? qt : 0) * (3 * C), row_ok, q);
-        if (a.mode == 1 && row_ok) l2_normalise(q);
-        store_row_sw128(sQ, tid, q);
-    }
+    // key tile kt into buffer b: the k and v boxes (128 rows x 32 columns of
+    // the qkv buffer, 64-byte swizzled, rows past the tensor zero-filled) by
+    // TMA from thread 0, and the key metadata; rows past this window's N are
+    // masked below
+    const int64_t row0 = win * N;
+    // (tile 0 also brings the q rows: one arrival with all three boxes' bytes)
+    auto load_keys = [&](int kt, int b) {
+        if (tid == 0) {
+            const uint32_t full = smem_u32(&bars[2 + b]);
+            mbar_arrive_expect_tx(full, (kt == 0 ? 3 : 2) * 128 * 64);
+            if (kt == 0) tma_load_2d(sQ, &tmap, head * 32, (int)(row0 + q0), full);
+            tma_load_2d(sK + b * (128 * 64), &tmap, C + head * 32, (int)(row0 + kt * 128), full);
+            tma_load_2d(sV + b * (128 * 64), &tmap, 2 * C + head * 32, (int)(row0 + kt * 128), full);
+        }
+        if (tid < 128) {
+            const int kj = kt * 128 + tid;
+            const bool ok = kj < N;
+            key_off[b * 128 + tid] = ok ? (kj / M) * L + (kj % M) : 0;
+            key_region[b * 128 + tid] = ok ? token_region(g, wi, wj, kj / M, kj % M) : -1;
+        }
+    };
+    __syncthreads();   // barrier initialisation is visible before any TMA completes on it
+    load_keys(0, 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *kc.tmem_slot;
-    const uint32_t bar = smem_u32(kc.bar);
-    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t bar_s = smem_u32(&bars[0]), bar_pv = smem_u32(&bars[1]);
+    const float scale = a.mode == 1 ? LOG2E / fmaxf(a.tau[head], 0.01f) : LOG2E * rsqrtf(32.0f);
 
-    float scale;
-    if (a.mode == 1) scale = LOG2E / fmaxf(a.tau[head], 0.01f);
-    else scale = LOG2E * rsqrtf(32.0f);
-
-    float o[32];
+    float o[16];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) o[e] = 0.f;
+    for (int e = 0; e < 16; ++e) o[e] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
     bool failed = false;
     uint32_t phase = 0;
-    const int ktiles = (N + 127) / 128;
 
 #pragma unroll 1
     for (int kt = 0; kt < ktiles; ++kt) {
-        // K and V rows of key kt*128 + tid; the previous tile's MMAs have
-        // completed (awaited before its o update)
-        const int kj = kt * 128 + tid;
-        const bool kok = kj < N;
-        {
-            const bf16 *src = wbase + (int64_t)(kok ? kj : 0) * (3 * C);
-            uint4 k[4], v[4];
-            load_head_row(src + C, kok, k);
-            load_head_row(src + 2 * C, kok, v);
-            if (a.mode == 1 && kok) l2_normalise(k);
-            store_row_sw128(sK, tid, k);
-            store_vt_column(sVt, tid, v);
-            key_region[tid] = kok ? token_region(g, wi, wj, kj / M, kj % M) : -1;
-            key_off[tid] = kok ? (kj / M) * L + (kj % M) : 0;
-        }
-        fence_proxy_async_smem();
+        const int b = kt & 1;
+        FPHASE(kt, 0);
+        if (kt + 1 < ktiles) load_keys(kt + 1, b ^ 1);
+        FPHASE(kt, 1);
+        // tile kt (and, for kt = 0, the q rows) have landed
+        if (!mbar_wait(smem_u32(&bars[2 + b]), (kt >> 1) & 1, st.wait_ns)) failed = true;
         tc_fence_before();
         if (__syncthreads_or(failed)) { failed = true; break; }
         tc_fence_after();
@@ -408,104 +364,181 @@ __global__ void __launch_bounds__(THREADS) attn_flash_kernel(AttnArgs a, DeviceS
             const uint32_t id = idesc_bf16(128, 128);
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-                mma_bf16(tmem, desc_kmajor_sw128(smem_u32(sQ) + 32 * k), desc_kmajor_sw128(smem_u32(sK) + 32 * k), id, k);
-            mma_commit(bar);
+                mma_bf16(tmem, desc_kmajor_sw64(sQ + 32 * k), desc_kmajor_sw64(sK + b * (128 * 64) + 32 * k), id, k);
+            mma_commit(bar_s);
         }
-        if (!mbar_wait(bar, phase, st.wait_ns)) failed = true;
-        phase ^= 1;
+        FPHASE(kt, 2);
+        if (!mbar_wait(bar_s, phase, st.wait_ns)) failed = true;
         tc_fence_after();
+        FPHASE(kt, 3);
 
-        // logits of the tile's 128 keys in registers; mask by select, not by branch
-        float sv[128];
+        // logits of this thread's 64 keys (64*half .. +63 of the tile)
+        float sv[64];
+        {
+            float c0[32], c1[32];
+            tmem_ld32(t_lane + 64 * half, c0);
+            tmem_ld32(t_lane + 64 * half + 32, c1);
+            tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float s[32];
-            tmem_ld32(t_lane + 32 * c, s);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sv[32 * c + j] = s[j];
+            for (int j = 0; j < 32; ++j) { sv[j] = c0[j]; sv[32 + j] = c1[j]; }
         }
-        tmem_wait_ld();
+        const int *koff = key_off + b * 128 + 64 * half;
+        const int nvalid = N - kt * 128 - 64 * half;   // keys of this thread's 64 that exist
         float mt = -INFINITY;
+        if (masked) {
+            const int *kreg = key_region + b * 128 + 64 * half;
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-            const float lv = fmaf(sv[j], scale, kc.sbias[base - key_off[j]]);
-            sv[j] = key_region[j] == my_region ? lv : -INFINITY;
-            mt = fmaxf(mt, sv[j]);
+            for (int j = 0; j < 64; ++j) {
+                const float lv = fmaf(sv[j], scale, sbias[base - koff[j]]);
+                sv[j] = kreg[j] == my_region ? lv : -INFINITY;
+                mt = fmaxf(mt, sv[j]);
+            }
+        } else if (nvalid >= 64) {
+            // the common case: every key exists and no shift region cuts the window
+#pragma unroll
+            for (int j4 = 0; j4 < 16; ++j4) {
+                const int4 o4 = reinterpret_cast<const int4 *>(koff)[j4];
+                const int oo[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int j = 4 * j4 + i;
+                    sv[j] = fmaf(sv[j], scale, sbias[base - oo[i]]);
+                    mt = fmaxf(mt, sv[j]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const float lv = fmaf(sv[j], scale, sbias[base - koff[j]]);
+                sv[j] = j < nvalid ? lv : -INFINITY;
+                mt = fmaxf(mt, sv[j]);
+            }
         }
+        FPHASE(kt, 4);
+        smax[half * 128 + row] = mt;
+        if (__syncthreads_or(failed)) { failed = true; break; }
+        FPHASE(kt, 5);
+        mt = fmaxf(smax[row], smax[128 + row]);
         const float m_new = fmaxf(m_run, mt);
-        // no key seen yet: use 0 as the reference (every p below is then 0, and
-        // alpha = 0 leaves o = 0, l = 0 as they are)
+        // no key seen yet: 0 as the reference (every p is then 0, and alpha = 0
+        // leaves o = 0 and l = 0 as they are)
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = ex2_approx(m_run - m_use);
         float sum = 0.f;
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                const float p0 = ex2_approx(sv[32 * c + j] - m_use), p1 = ex2_approx(sv[32 * c + j + 1] - m_use);
-                sum += p0 + p1;
-                pk[j / 2] = pack_bf16x2(p0, p1);
-            }
-            // chunk c holds keys 32c..32c+31: K block c/2, 16-byte chunks 4*(c%2)..+3
-            uint8_t *blk = sP + (c >> 1) * (128 * 128);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4 *>(blk + sw128_offset(tid, 4 * (c & 1) + q)) =
-                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        for (int j = 0; j < 64; j += 2) {
+            const float p0 = ex2_approx(sv[j] - m_use), p1 = ex2_approx(sv[j + 1] - m_use);
+            sum += p0 + p1;
+            pk[j / 2] = pack_bf16x2(p0, p1);
         }
-        l_run = l_run * alpha + sum;
+        l_run = l_run * alpha + sum;     // this half's share of the row sum
         m_run = m_new;
-        fence_proxy_async_smem();
+        // P (bf16 pairs) over TMEM columns 32*half .. +31 (keys 64*half ..)
+        {
+            uint32_t lo[16], hi[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) { lo[i] = pk[i]; hi[i] = pk[16 + i]; }
+            tmem_st16(t_lane + 32 * half, lo);
+            tmem_st16(t_lane + 32 * half + 16, hi);
+            tmem_wait_st();
+        }
+        FPHASE(kt, 6);
         tc_fence_before();
         if (__syncthreads_or(failed)) { failed = true; break; }
         tc_fence_after();
+        FPHASE(kt, 7);
         if (tid == 0) {
-            const uint32_t id = idesc_bf16(128, 32);
+            const uint32_t id = idesc_bf16_bmn(128, 32);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int kb = k >> 2, ks = k & 3;
-                mma_bf16(tmem + 128, desc_kmajor_sw128(smem_u32(sP) + kb * 16384 + 32 * ks),
-                         desc_kmajor_sw128(smem_u32(sVt) + kb * 4096 + 32 * ks), id, k);
-            }
-            mma_commit(bar);
+            for (int k = 0; k < 8; ++k)
+                mma_bf16_ts(tmem + 128, tmem + 8 * k, desc_mnmajor_sw64(sV + b * (128 * 64) + 1024 * k, 128 * 64), id,
+                            k);
+            mma_commit(bar_pv);
         }
-        if (!mbar_wait(bar, phase, st.wait_ns)) failed = true;
+        if (!mbar_wait(bar_pv, phase, st.wait_ns)) failed = true;
         phase ^= 1;
         tc_fence_after();
-        float ot[32];
-        tmem_ld32(t_lane + 128, ot);
+        FPHASE(kt, 8);
+        float ot[16];
+        tmem_ld16(t_lane + 128 + 16 * half, ot);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = fmaf(o[e], alpha, ot[e]);
+        for (int e = 0; e < 16; ++e) o[e] = fmaf(o[e], alpha, ot[e]);
+        FPHASE(kt, 9);
         tc_fence_before();
         if (__syncthreads_or(failed)) { failed = true; break; }
+        FPHASE(kt, 10);
     }
-    if (!failed && row_ok) store_o_row(a.attn + (win * N + qt) * (int64_t)C + head * 32, o, rcp_approx(l_run));
+    spart[half * 128 + row] = l_run;
+    __syncthreads();
+    if (!failed && row_ok) {
+        const float l = spart[row] + spart[128 + row];
+        store_o<16>(a.attn + (win * N + qt) * (int64_t)C + head * 32 + 16 * half, o, rcp_approx(l));
+    }
     if (failed && tid == 0) atomicOr(st.err, ERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Tensor map over the window-ordered qkv buffer [rows, cols] (bf16): boxes of
+// 32 columns (one head's q, k or v) x 128 rows, 64-byte swizzle, zero fill
+// past the last row.
+cudaError_t make_qkv_tensor_map(CUtensorMap *map, const bf16 *qkv, int64_t rows, int cols)
+{
+    static EncodeTiledFn encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return cudaErrorNotSupported;
+        encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t elem[2] = {1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16 *>(qkv), dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 } // namespace
+
+#ifdef SWIN_PHASE_TRACE
+extern "C" int swin_wattn_flash_trace(long long *host, int n)
+{
+    return (int)cudaMemcpyFromSymbol(host, g_flash_trace, sizeof(long long) * (size_t)n);
+}
+#endif
 
 cudaError_t launch_attention(const AttnArgs &a, DeviceStatus st, cudaStream_t stream)
 {
     const Geom &g = a.g;
     if (g.C != a.heads * 32) return cudaErrorInvalidValue;
-    const size_t smem = AttnSmem::bytes(g.M);
     if (g.N <= 64) {
+        const size_t smem = Pack2Smem::bytes(g.M);
         cudaError_t e = cudaFuncSetAttribute(attn_pack2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         dim3 grid((unsigned)((g.nwin + 1) / 2), (unsigned)a.heads);
-        attn_pack2_kernel<<<grid, THREADS, smem, stream>>>(a, st);
+        attn_pack2_kernel<<<grid, 128, smem, stream>>>(a, st);
     } else {
+        const size_t smem = FlashSmem::bytes(g.M);
         cudaError_t e = cudaFuncSetAttribute(attn_flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        CUtensorMap tmap;
+        e = make_qkv_tensor_map(&tmap, a.qkv, g.T, 3 * g.C);
         if (e != cudaSuccess) return e;
         const int qtiles = (g.N + 127) / 128;
         dim3 grid((unsigned)(g.nwin * qtiles), (unsigned)a.heads);
-        attn_flash_kernel<<<grid, THREADS, smem, stream>>>(a, st);
+        attn_flash_kernel<<<grid, FL_THREADS, smem, stream>>>(a, st, tmap);
     }
     return cudaGetLastError();
 }

@@ -98,6 +98,8 @@ struct GemmArgs {
     int64_t rows;
     int N, K;
     Geom g;          // index maps of LOAD_GATHER / STORE_SCATTER
+    int norm_cols;   // > 0: output columns below it are scaled, 32 at a time, to
+                     // unit L2 norm (V2 q and k heads); 0: none
 };
 
 cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, DeviceStatus st,
@@ -108,6 +110,9 @@ cudaError_t launch_gemm_sw64(const GemmArgs &a, DeviceStatus st, cudaStream_t st
 // Plain GEMM with the A operand staged in TMEM (K <= 128, N <= 256): tests the
 // TMEM-A MMA form.
 cudaError_t launch_gemm_ts_test(const GemmArgs &a, DeviceStatus st, cudaStream_t stream);
+// Plain GEMM with B given [K, N] (N-major, N = 32 or 64, K <= 128): tests the
+// MN-major 64-byte-swizzled B operand form.
+cudaError_t launch_gemm_mn_test(const GemmArgs &a, DeviceStatus st, cudaStream_t stream);
 
 struct AttnArgs {
     const bf16 *qkv;      // [T, 3C] window order

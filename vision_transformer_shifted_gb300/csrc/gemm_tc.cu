@@ -180,7 +180,26 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
             float v[32];
             tmem_ld32(t_lane + c0, v);
             tmem_wait_ld();
-            if (dst_row) store_row_bf16(dst_row + c0, v, sbias + c0, 32);
+            if (n0 + c0 < a.norm_cols) {
+                // V2: this 32-column chunk is one head's q or k; bias first, then
+                // scale to unit length (norm clamped at 1e-12) before rounding
+                float ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    v[i] += sbias[c0 + i];
+                    ss = fmaf(v[i], v[i], ss);
+                }
+                const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+                float zero[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    v[i] *= inv;
+                    zero[i] = 0.f;
+                }
+                if (dst_row) store_row_bf16(dst_row + c0, v, zero, 32);
+            } else if (dst_row) {
+                store_row_bf16(dst_row + c0, v, sbias + c0, 32);
+            }
         }
         if (c0 < BN) { // 16-column tail
             float v[16];
@@ -196,10 +215,11 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
     if (warp == 0) tmem_dealloc(tmem, tmem_cols);
 }
 
-// Largest N tile <= 256 that divides N and is a multiple of 16.
-int pick_bn(int N)
+// Largest N tile <= 256 that divides N and is a multiple of `step` (16, or
+// 32 when 32-column chunks must stay whole).
+int pick_bn(int N, int step)
 {
-    for (int bn = 256; bn >= 16; bn -= 16)
+    for (int bn = 256 / step * step; bn >= step; bn -= step)
         if (N % bn == 0) return bn;
     return 0;
 }
@@ -207,7 +227,7 @@ int pick_bn(int N)
 template <int LOAD, int STORE, int BK = 64>
 cudaError_t launch_impl(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
 {
-    const int BN = pick_bn(a.N);
+    const int BN = pick_bn(a.N, a.norm_cols > 0 ? 32 : 16);
     if (BN == 0 || a.K % 16 != 0 || a.rows <= 0) return cudaErrorInvalidValue;
     const size_t smem = GemmSmem<BK>::bytes(BN);
     auto kern = gemm_tc_kernel<LOAD, STORE, BK>;
@@ -299,7 +319,86 @@ __global__ void __launch_bounds__(THREADS) gemm_ts_test_kernel(GemmArgs a, Devic
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// Test kernel of an MN-major B operand: Bmn is [K, N] row-major (N = 32 or
+// 64); each K row of a 32-wide N group is one 64-byte row of a 64B-swizzled
+// tile, K groups of 8 rows 512 B apart, N groups K*64 bytes apart.  A is
+// K-major (128-byte swizzle), K <= 128.
+__global__ void __launch_bounds__(THREADS) gemm_mn_test_kernel(GemmArgs a, DeviceStatus st)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_align(smem_raw, 1024);
+    uint8_t *sA = smem;                                          // 2 K blocks x [128 rows][128 B]
+    uint8_t *sB = smem + 2 * 128 * 128;                          // 2 N groups x [128 K rows][64 B]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sB + 2 * 128 * 64);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int64_t m0 = (int64_t)blockIdx.x * BM;
+    const int N = a.N, K = a.K;
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 64);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(smem_u32(bar), 1);
+        mbar_init_fence();
+    }
+    for (int q = tid; q < 128 * 16; q += THREADS) {               // A rows (zero past rows / K)
+        const int r = q / 16, c16 = q % 16;
+        const int64_t R = m0 + r;
+        const bool ok = R < a.rows && c16 * 8 < K;
+        cp_async16(smem_u32(sA) + (c16 >> 3) * (128 * 128) + sw128_offset(r, c16 & 7),
+                   ok ? a.A + R * a.lda + c16 * 8 : a.A, ok ? 16u : 0u);
+    }
+    for (int q = tid; q < K * (N / 8); q += THREADS) {            // B rows k, 16-byte chunks of N
+        const int k = q / (N / 8), c16 = q % (N / 8);
+        cp_async16(smem_u32(sB) + (c16 >> 2) * (K * 64) + sw64_offset(k, c16 & 3), a.Bw + (int64_t)k * N + c16 * 8,
+                   16);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (tid == 0) {
+        const uint32_t id = idesc_bf16_bmn(BM, N);
+        for (int kk = 0; kk < K / 16; ++kk)
+            mma_bf16(tmem, desc_kmajor_sw128(smem_u32(sA) + (kk >> 2) * (128 * 128) + 32 * (kk & 3)),
+                     desc_mnmajor_sw64(smem_u32(sB) + kk * 1024, K * 64), id, kk != 0);
+        mma_commit(smem_u32(bar));
+    }
+    const bool ok = mbar_wait(smem_u32(bar), 0, st.wait_ns);
+    tc_fence_after();
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    const int64_t R = m0 + tid;
+    for (int c0 = 0; c0 < N; c0 += 16) {
+        float v[16];
+        tmem_ld16(t_lane + c0, v);
+        tmem_wait_ld();
+        if (R < a.rows && ok) {
+            float b[16];
+            for (int i = 0; i < 16; ++i) b[i] = a.bias ? __bfloat162float(a.bias[c0 + i]) : 0.f;
+            store_row_bf16(a.D + R * a.ldd + c0, v, b, 16);
+        }
+    }
+    if (!ok && tid == 0) atomicOr(st.err, ERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
 } // namespace
+
+cudaError_t launch_gemm_mn_test(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
+{
+    if (a.K % 16 || a.K > 128 || (a.N != 32 && a.N != 64) || a.rows <= 0) return cudaErrorInvalidValue;
+    const size_t smem = 1024 + 2 * 128 * 128 + 2 * 128 * 64 + 64;
+    cudaError_t e = cudaFuncSetAttribute(gemm_mn_test_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    gemm_mn_test_kernel<<<(unsigned)((a.rows + BM - 1) / BM), THREADS, smem, stream>>>(a, st);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gemm_ts_test(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
 {

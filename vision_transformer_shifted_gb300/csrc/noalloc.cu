@@ -97,6 +97,7 @@ extern "C" int swin_wattn_forward_noalloc(int C, int heads, int M, int shift, in
     GemmArgs k1{};
     k1.A = (const bf16 *)x; k1.lda = C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
     k1.D = qkv; k1.ldd = 3 * C; k1.rows = g.T; k1.N = 3 * C; k1.K = C; k1.g = g;
+    k1.norm_cols = (mode & SWIN_WATTN_V2) ? 2 * C : 0;
     if (launch_gemm(k1, LOAD_GATHER, STORE_PLAIN, st, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
     AttnArgs k2{};
     k2.qkv = qkv; k2.attn = attn; k2.table = (const bf16 *)bias_table; k2.tau = logit_scale; k2.heads = heads;

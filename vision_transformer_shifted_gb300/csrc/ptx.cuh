@@ -114,6 +114,28 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// ---- TMA tensor copies ------------------------------------------------------------
+
+// Sets the barrier's expected transaction bytes and arrives once.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+        : "memory");
+}
+
+// 2D tiled TMA load of the box at (x = innermost coordinate, y) of the tensor
+// map into shared memory at dst; completes `bytes` on the mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
 // ---- bulk copies (TMA, non-tensor) ----------------------------------------------
 
 // Copies `bytes` (multiple of 16) from shared memory to global memory
@@ -281,6 +303,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 // 1024 B stacked densely (stride byte offset 1024).
 __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t addr) { return smem_desc(addr, 16, 1024, SWZ_128B); }
 
+// MN-major operand (N contiguous), 64-byte swizzle: each K row holds 32 bf16
+// of N (64 B); 8-row K groups of 512 B stacked densely (stride byte offset
+// 512); groups of 32 N at leading byte offset `lbo`.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw64(uint32_t addr, uint32_t lbo)
+{
+    return smem_desc(addr, lbo, 512, SWZ_64B);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
@@ -299,6 +329,9 @@ __device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t chunk)
 {
     return (row >> 3) * 512u + (row & 7u) * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
 }
+
+// The same with the B operand MN-major (bit 16).
+__host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) { return idesc_bf16(M, N) | (1u << 16); }
 
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a
 // K-major 128B-swizzled tile of 128-byte rows (8-row atoms of 1024 bytes).
