@@ -50,7 +50,12 @@ int swin_wattn_test_proj(swin_wattn_t h, const void *attn, int B, int H, int W,
  * 64-byte swizzled shared memory, as the fused kernel) or 0 (A staged in
  * tensor memory, the MMA form that reads A from TMEM; K <= 128, N <= 256) or
  * -64 (Bw given as [K, N] row-major and used as an N-major operand, 64-byte
- * swizzle; N = 32 or 64, K <= 128). */
+ * swizzle; N = 32 or 64, K <= 128) or 1 (lane-masked MMA pair: Bw is [2N, K]
+ * and D is [rows, 2N]; within every block of 128 rows, rows 0..63 use
+ * Bw[0:N] and rows 64..127 use Bw[N:2N], the two products written into the
+ * same accumulator columns by MMAs that mask each other's rows; D columns
+ * 0..N-1 come from the shared-memory-A form and N..2N-1 from the TMEM-A form;
+ * bias ignored; K <= 128 and a multiple of 32, N <= 128). */
 int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *D, int rows, int N,
                          int K, int swizzle_bytes, swin_stream_t stream);
 

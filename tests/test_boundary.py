@@ -65,3 +65,7 @@ def test_null_handle_calls():
                                     1, 24, 16, 128, None) == sw.EINVAL  # N % 16
     assert lib.swin_wattn_test_gemm(ctypes.c_void_p(16), ctypes.c_void_p(16), None, ctypes.c_void_p(16),
                                     1, 16, 16, 32, None) == sw.EINVAL  # swizzle
+    assert lib.swin_wattn_test_gemm(ctypes.c_void_p(16), ctypes.c_void_p(16), None, ctypes.c_void_p(16),
+                                    1, 16, 48, 1, None) == sw.EINVAL  # masked pair: K % 32
+    assert lib.swin_wattn_test_gemm(ctypes.c_void_p(16), ctypes.c_void_p(16), None, ctypes.c_void_p(16),
+                                    1, 144, 32, 1, None) == sw.EINVAL  # masked pair: N > 128

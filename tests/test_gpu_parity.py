@@ -96,6 +96,28 @@ def test_gemm_a_from_tmem(rows, N, K):
     assert (err <= ref.abs() * 2.0 ** -8 + 1e-4).all(), float(err.max())
 
 
+@pytest.mark.parametrize("rows,N,K", [(128, 64, 32), (256, 64, 96), (200, 128, 128), (77, 32, 64)])
+def test_gemm_lane_masked_pair(rows, N, K):
+    """Two MMAs into the same accumulator columns with complementary lane masks:
+    rows 0..63 of every 128-row block against one B, rows 64..127 against another
+    (both MMA forms: A from shared memory and A from tensor memory)."""
+    g = torch.Generator().manual_seed(13 * rows + N + K)
+    A = torch.randn(rows, K, generator=g).bfloat16()
+    B2 = (torch.randn(2 * N, K, generator=g) * 0.1).bfloat16()
+    D = torch.empty(rows, 2 * N, dtype=torch.bfloat16, device=DEV)
+    Ad, Bd = A.to(DEV), B2.to(DEV)
+    rc = sw.load().swin_wattn_test_gemm(ctypes.c_void_p(Ad.data_ptr()), ctypes.c_void_p(Bd.data_ptr()), None,
+                                        ctypes.c_void_p(D.data_ptr()), rows, N, K, 1, None)
+    assert rc == sw.OK
+    torch.cuda.synchronize()
+    top = (torch.arange(rows) % 128) < 64
+    ref = torch.where(top[:, None], A.double() @ B2[:N].double().T, A.double() @ B2[N:].double().T)
+    got = D.double().cpu()
+    for part in range(2):
+        err = (got[:, part * N:(part + 1) * N] - ref).abs()
+        assert (err <= ref.abs() * 2.0 ** -8 + 1e-4).all(), (part, float(err.max()))
+
+
 # ---- index maps, bit-exact ----------------------------------------------------
 
 def tagged(B, H, W, C):

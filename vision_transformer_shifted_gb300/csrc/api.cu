@@ -41,10 +41,12 @@ int check_grid(const swin_wattn_s *h, int B, int H, int W)
     return SWIN_WATTN_OK;
 }
 
-int choose_path(const swin_wattn_s *h)
+// The fused kernel indexes tokens with 32-bit integers: grids of 2^31 tokens
+// or more take the three-kernel path.
+int choose_path(const swin_wattn_s *h, int64_t T)
 {
     if (h->fp32) return 3;
-    return fused_supported(h->M, h->C, h->heads) ? 2 : 1;
+    return fused_supported(h->M, h->C, h->heads) && T < ((int64_t)1 << 31) ? 2 : 1;
 }
 
 int ensure_buffer(void **buf, size_t *have, size_t need)
@@ -73,7 +75,7 @@ int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void 
     const Geom g = make_geom(B, H, W, h->C, h->M, h->shift);
     h->last_launches = 0;
     if (B == 0) return SWIN_WATTN_OK;
-    const int path = h->path_opt ? h->path_opt : choose_path(h);
+    const int path = h->path_opt ? h->path_opt : choose_path(h, g.T);
     if (h->fp32) {
         Fp32Args a;
         a.x = (const float *)x; a.Wqkv = (const float *)Wqkv; a.bqkv = (const float *)bqkv;
@@ -260,8 +262,9 @@ int swin_wattn_path(swin_wattn_t h, int B, int H, int W)
     int rc = check_grid(h, B, H, W);
     if (rc) return rc;
     if (h->fp32) return 3;
-    const int path = h->path_opt ? h->path_opt : choose_path(h);
-    if (path == 2 && !fused_supported(h->M, h->C, h->heads)) return SWIN_WATTN_EUNSUPPORTED;
+    const int64_t T = (int64_t)B * H * W;
+    const int path = h->path_opt ? h->path_opt : choose_path(h, T);
+    if (path == 2 && (!fused_supported(h->M, h->C, h->heads) || T >= ((int64_t)1 << 31))) return SWIN_WATTN_EUNSUPPORTED;
     return path;
 }
 
@@ -339,8 +342,10 @@ int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *
                          int swizzle_bytes, swin_stream_t stream)
 {
     if (!A || !Bw || !D || rows < 0 || N <= 0 || K <= 0 || N % 16 || K % 16 || N > 2048) return SWIN_WATTN_EINVAL;
-    if (swizzle_bytes != 0 && swizzle_bytes != 64 && swizzle_bytes != 128 && swizzle_bytes != -64) return SWIN_WATTN_EINVAL;
+    if (swizzle_bytes != 0 && swizzle_bytes != 64 && swizzle_bytes != 128 && swizzle_bytes != -64 && swizzle_bytes != 1)
+        return SWIN_WATTN_EINVAL;
     if (swizzle_bytes == 0 && (K % 32 || K > 128 || N > 256)) return SWIN_WATTN_EINVAL;
+    if (swizzle_bytes == 1 && (K % 32 || K > 128 || N > 128)) return SWIN_WATTN_EINVAL;
     if (swizzle_bytes == -64 && (K > 128 || (N != 32 && N != 64))) return SWIN_WATTN_EINVAL;
     if (!aligned16(A) || !aligned16(Bw) || !aligned16(D) || (bias && !aligned16(bias))) return SWIN_WATTN_EINVAL;
     if (rows == 0) return SWIN_WATTN_OK;
@@ -354,6 +359,10 @@ int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *
     if (swizzle_bytes == 64) return cuda_status(launch_gemm_sw64(a, st, (cudaStream_t)stream));
     if (swizzle_bytes == 0) return cuda_status(launch_gemm_ts_test(a, st, (cudaStream_t)stream));
     if (swizzle_bytes == -64) return cuda_status(launch_gemm_mn_test(a, st, (cudaStream_t)stream));
+    if (swizzle_bytes == 1) {
+        a.ldd = 2 * N;
+        return cuda_status(launch_gemm_pair_test(a, st, (cudaStream_t)stream));
+    }
     return cuda_status(launch_gemm(a, LOAD_PLAIN, STORE_PLAIN, st, (cudaStream_t)stream));
 }
 

@@ -482,14 +482,13 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+} // namespace
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Tensor map over the window-ordered qkv buffer [rows, cols] (bf16): boxes of
-// 32 columns (one head's q, k or v) x 128 rows, 64-byte swizzle, zero fill
-// past the last row.
-cudaError_t make_qkv_tensor_map(CUtensorMap *map, const bf16 *qkv, int64_t rows, int cols)
+static EncodeTiledFn encode_fn()
 {
     static EncodeTiledFn encode = nullptr;
     if (!encode) {
@@ -497,20 +496,45 @@ cudaError_t make_qkv_tensor_map(CUtensorMap *map, const bf16 *qkv, int64_t rows,
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
             q != cudaDriverEntryPointSuccess || !fn)
-            return cudaErrorNotSupported;
+            return nullptr;
         encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
+    return encode;
+}
+
+// Tensor map over a row-major bf16 matrix [rows, cols]: boxes of 32 columns x
+// box_rows rows, 64-byte swizzle, zero fill past the last row.
+cudaError_t make_tensor_map_sw64(CUtensorMap *map, const void *ptr, int64_t rows, int cols, int box_rows)
+{
+    const EncodeTiledFn encode = encode_fn();
+    if (!encode) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
     const cuuint32_t elem[2] = {1, 1};
-    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16 *>(qkv), dims, strides, box, elem,
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, elem,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-} // namespace
+// Tensor map over a bf16 image batch [rows, width, cols] (rows = B*H image
+// rows, width = W tokens, cols = C channels, row-major): boxes of 32 channels
+// x box_w tokens x box_h image rows, 64-byte swizzle, zero fill outside.
+cudaError_t make_tensor_map_sw64_3d(CUtensorMap *map, const void *ptr, int64_t rows, int width, int cols, int box_w,
+                                    int box_h)
+{
+    const EncodeTiledFn encode = encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)width, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)width * cols * 2};
+    const cuuint32_t box[3] = {32, (cuuint32_t)box_w, (cuuint32_t)box_h};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 #ifdef SWIN_PHASE_TRACE
 extern "C" int swin_wattn_flash_trace(long long *host, int n)
@@ -534,7 +558,7 @@ cudaError_t launch_attention(const AttnArgs &a, DeviceStatus st, cudaStream_t st
         cudaError_t e = cudaFuncSetAttribute(attn_flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         CUtensorMap tmap;
-        e = make_qkv_tensor_map(&tmap, a.qkv, g.T, 3 * g.C);
+        e = make_tensor_map_sw64(&tmap, a.qkv, g.T, 3 * g.C, 128);
         if (e != cudaSuccess) return e;
         const int qtiles = (g.N + 127) / 128;
         dim3 grid((unsigned)(g.nwin * qtiles), (unsigned)a.heads);

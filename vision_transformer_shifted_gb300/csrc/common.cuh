@@ -1,6 +1,7 @@
 // Internal declarations shared by the kernels and the C ABI of libswin_wattn.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -113,6 +114,10 @@ cudaError_t launch_gemm_ts_test(const GemmArgs &a, DeviceStatus st, cudaStream_t
 // Plain GEMM with B given [K, N] (N-major, N = 32 or 64, K <= 128): tests the
 // MN-major 64-byte-swizzled B operand form.
 cudaError_t launch_gemm_mn_test(const GemmArgs &a, DeviceStatus st, cudaStream_t stream);
+// Lane-masked MMA forms: rows 0..63 of each 128-row block against Bw[0:N], rows
+// 64..127 against Bw[N:2N], A from shared memory (D columns 0..N-1) and from
+// TMEM (D columns N..2N-1); D is [rows, 2N].
+cudaError_t launch_gemm_pair_test(const GemmArgs &a, DeviceStatus st, cudaStream_t stream);
 
 struct AttnArgs {
     const bf16 *qkv;      // [T, 3C] window order
@@ -142,6 +147,16 @@ bool fused_supported(int M, int C, int heads);
 cudaError_t launch_fused(const bf16 *x, const bf16 *Wqkv, const bf16 *bqkv, const bf16 *table, const float *tau,
                          const bf16 *Wproj, const bf16 *bproj, bf16 *out, int mode, const Geom &g, DeviceStatus st,
                          cudaStream_t stream);
+
+// Tensor map over a row-major bf16 matrix [rows, cols] (16-byte aligned base,
+// cols * 2 a multiple of 16): boxes of 32 columns x box_rows rows (<= 256),
+// 64-byte swizzle in shared memory, zero fill past the last row.
+cudaError_t make_tensor_map_sw64(CUtensorMap *map, const void *ptr, int64_t rows, int cols, int box_rows);
+// Tensor map over a bf16 image batch [rows, width, cols] (rows = B*H image rows,
+// width = W, cols = C; strides multiples of 16 bytes): boxes of 32 channels x
+// box_w tokens x box_h image rows, 64-byte swizzle, zero fill outside.
+cudaError_t make_tensor_map_sw64_3d(CUtensorMap *map, const void *ptr, int64_t rows, int width, int cols, int box_w,
+                                    int box_h);
 
 cudaError_t launch_cpb_table(const float *W1, const float *b1, const float *W2, int hidden, int M,
                              int heads, bool out_bf16, void *table, cudaStream_t stream);

@@ -5,34 +5,44 @@
 // Steps, per tile of two windows (pages "Boosting Swin Transformer Speed",
 // Introduction / Training Optimization / Inference Optimization; "Swin
 // Transformer V2" (neura.market), How It Works):
-//   S1  the tile's 2 x N tokens are gathered from x through the cyclic shift
-//       by -s and the window partition (cp.async, one 16-byte chunk each);
-//       window A fills rows 0..63 of a 128-row tile, window B rows 64..127
+//   S1  the tile's two windows are gathered from x through the cyclic shift
+//       by -s and the window partition: window A fills rows 0..63 of a
+//       128-row tile, window B rows 64..127, token (ti, tj) of a window at
+//       row 8*ti + tj; a window arrives as one 3-D TMA box (M image rows x 8
+//       tokens x 32 channels) per 32 channels.  Windows that the shift wraps
+//       around the image edge (last window row or column) are gathered with
+//       cp.async instead
 //   S2  [q|k] = X Wqk^T (128 x 2C) and v^T = Wv X^T (C x 128), both on
 //       tcgen05 into TMEM; bias added when draining to shared memory; V2
-//       normalises q and k to unit length in fp32 while draining
-//   S3-S5 per head: S = q k^T (128 x 128 x 32) into TMEM; softmax of each
-//       row over its own window's keys with the relative bias and the shift
-//       mask computed from coordinates (fp32, exp2); P (bf16) back into TMEM
-//       over the S columns
+//       normalises q and k to unit length in fp32 while draining.  Every
+//       head's q and k is drained at once, which frees the QKV columns of
+//       TMEM for two S buffers
+//   S3-S5 per head: S = q k^T (128 x 128 x 32) into TMEM, alternating
+//       between the two S buffers so that the next head's logits are ready
+//       while this head's softmax runs; softmax of each row over its own
+//       window's keys with the relative bias and the shift mask (fp32, exp2);
+//       P (bf16) back into TMEM over the S columns
 //   S6  o_h = P v_h (128 x 32 x 128) into TMEM, with P read from TMEM as the
 //       A operand (so P never touches shared memory)
-//   S7  y = (o / rowsum) Wproj^T on tcgen05, o staged as bf16 in the freed X
-//       buffer
-//   S8  y + bproj written straight from registers through the window
-//       reverse + roll(+s) map into out[B, H, W, C]
-// Nothing but x, the weights and out touches HBM.  The next tile's x is
-// fetched with cp.async while the current one is computed.
+//   S7  y = (o / rowsum) Wproj^T on tcgen05, o staged as bf16 in the tile's
+//       x buffer
+//   S8  y + bproj staged in shared memory (token (ti, tj) at row M*ti + tj)
+//       and written through the window reverse + roll(+s) map into
+//       out[B, H, W, C]: one 3-D TMA store (M x M tokens x 32 channels) per
+//       window and 32 channels, plain stores for wrapping windows
+// Nothing but x, the weights and out touches HBM.
 //
-// Warp roles: warps 0..7 compute (warp w serves TMEM lane quarter w % 4 =
-// tile rows 32(w%4)..+31 and column half w / 4; every drain and the softmax
-// split their columns between the two halves); warp 8 issues every tcgen05
-// MMA.  They hand over through mbarriers: the compute warps arrive on
-// "ready" barriers (one arrival per warp) once operands are in shared memory,
-// the MMA warp commits "done" barriers.  The MMA warp issues the next tile's
-// QKV projection as soon as the current tile's last softmax has freed TMEM
-// columns 0..2C+127, so it runs under the current tile's P.V, o drain,
-// projection and store.
+// Warp roles.  Warps 0..7 compute: warp w serves TMEM lane quarter w % 4 =
+// tile rows 32(w%4)..+31 and column half w / 4 (every drain and the softmax
+// split their columns between the two halves).  Warp 8 issues every tcgen05
+// MMA (lane 0).  Warps 9 and 10 produce and retire tiles: the row -> token
+// map and the attention masks of a tile, its x gather into one of two x
+// buffers, and, once the compute warps have staged a tile's output rows,
+// the coalesced copy-out, after which that x buffer takes the tile two
+// ahead.  All hand-offs are mbarriers: "ready" barriers get one arrival per
+// warp, "done" barriers are tcgen05.commit targets.  Every barrier that
+// serves alternating buffers is split per buffer, so no barrier can run two
+// phases ahead of a waiter by construction.
 #include <type_traits>
 
 #include "common.cuh"
@@ -42,23 +52,37 @@ namespace swin {
 
 namespace {
 
-constexpr int FTHREADS = 288;          // 8 compute warps + 1 MMA warp
-constexpr int NCOMPUTE = 256;
-constexpr int NCWARPS = NCOMPUTE / 32;
+constexpr int NCWARPS = 8;                       // compute warps
+constexpr int NCOMPUTE = NCWARPS * 32;
+constexpr int MMA_WARP = NCWARPS;                // warp 8
+constexpr int PWARP0 = NCWARPS + 1;              // warps 9, 10
+constexpr int NPROD = 64;
+constexpr int FTHREADS = NCOMPUTE + 32 + NPROD;  // 352
+// (registers are capped as for 384 threads: 168 per thread, so that three
+// warps of one SM sub-partition fit its 16 K registers)
+constexpr int FBOUND_THREADS = 384;
 constexpr float FLOG2E = 1.4426950408889634f;
 
-// Optional phase trace (builds with -DSWIN_PHASE_TRACE only): thread 0 of
-// CTA 0 records clock64() at the phase boundaries of its first tiles.
+// Optional phase trace (builds with -DSWIN_PHASE_TRACE only): threads 0 and
+// 128 of CTA 0 record clock64() at the phase boundaries of their first tiles.
 #ifdef SWIN_PHASE_TRACE
 constexpr int TRACE_TILES = 16, TRACE_POINTS = 32;
-__device__ long long g_phase_trace[2 * TRACE_TILES * TRACE_POINTS];
+__device__ long long g_phase_trace[4 * TRACE_TILES * TRACE_POINTS];
 __device__ long long g_cta_trace[1024 * 4];
+// recorder 0: thread 0, 1: thread 128, 2: the MMA thread, 3: producer thread 0
+#define TRACE_AT(who, k, i)                                                                          \
+    do {                                                                                             \
+        if (blockIdx.x == 0 && (k) < TRACE_TILES)                                                    \
+            g_phase_trace[((who) * TRACE_TILES + (k)) * TRACE_POINTS + (i)] = clock64();             \
+    } while (0)
 #define PHASE(k, i)                                                                                  \
     do {                                                                                             \
-        if (blockIdx.x == 0 && (tid == 0 || tid == 128) && (k) < TRACE_TILES)                       \
-            g_phase_trace[((tid >> 7) * TRACE_TILES + (k)) * TRACE_POINTS + (i)] = clock64();        \
+        if (tid == 0 || tid == 128) TRACE_AT(tid >> 7, k, i);                                        \
     } while (0)
 #else
+#define TRACE_AT(who, k, i) \
+    do {                    \
+    } while (0)
 #define PHASE(k, i) \
     do {            \
     } while (0)
@@ -69,35 +93,58 @@ struct FusedCfg {
     static constexpr int N = M * M;
     static constexpr int HEADS = C / 32;
     static constexpr int L = 2 * M - 1;
-    static constexpr int KB = C / 32;         // 32-channel K blocks (64-byte swizzle)
+    static constexpr int KB = C / 32;          // 32-channel K blocks (64-byte swizzle)
+    static constexpr int CH = C / 8;           // 16-byte chunks of one output row
     // shared memory (bytes); SW64 tiles are 512-aligned, SW128 tiles 1024-aligned
     static constexpr int WQK = 0;                       // [2C rows][C]   SW64
     static constexpr int WV = WQK + 2 * C * C * 2;      // [128 rows][C]  SW64 (rows >= C zero)
     static constexpr int WP = WV + 128 * C * 2;         // [C rows][C]    SW64
-    // x tile (then o) buffers X0 and X1; each is followed by scratch that is
-    // free when the tile's output is staged (Q and K after X0, V^T after X1),
-    // so the output staging rows (stride SROW) of buffer b start at X(b)
+    // x buffers: tile k uses X(k % 2) for x, then o (the projection's A
+    // operand), then the output rows y + bproj, all in the same layout
     static constexpr int XSZ = 128 * C * 2;
-    static constexpr int X0 = WP + C * C * 2;           // [128][C]       SW64 (x, then o)
-    static constexpr int Q = X0 + XSZ;                  // [128][32]      SW64
-    static constexpr int K = Q + 128 * 64;
-    static constexpr int X1 = K + 128 * 64;
-    static constexpr int VT = X1 + XSZ;                 // 2 x [C rows][64 keys] SW128
+    static constexpr int X0 = WP + C * C * 2;
+    static constexpr int X1 = X0 + XSZ;
+    static constexpr int QA = X1 + XSZ;                 // HEADS x [128][32] SW64 (q of each head)
+    static constexpr int KA = QA + HEADS * 128 * 64;    // HEADS x [128][32] SW64 (k of each head)
+    static constexpr int VT = KA + HEADS * 128 * 64;    // 2 x [C rows][64 keys] SW128
     static constexpr int VT_BLK = C * 128;
-    static constexpr int SROW = 2 * C + 16;             // staging row stride (bank-conflict free)
-    static_assert(128 * SROW <= XSZ + 2 * 128 * 64 && 128 * SROW <= XSZ + 2 * VT_BLK, "staging fits");
-    static constexpr int P = VT + 2 * VT_BLK;           // 2 x [128 rows][64 keys] SW128
-    static constexpr int SMALL = P + 2 * 128 * 128;
-    static constexpr int BYTES = SMALL + HEADS * L * L * 4 + 3 * C * 4 + C * 4 + HEADS * 4 + 2 * 128 * 4 +
-                                 HEADS * 2 * 128 * 4 + 3 * 128 * 4 + 2 * 64 * 4 + 16 * 8 + 16 + 16;
-    // TMEM columns
-    static constexpr int T_QK = 0;                      // 2C
-    static constexpr int T_VT = 2 * C;                  // 128 (v^T), then S
-    static constexpr int T_S = T_VT;
+    static constexpr int SMALL = VT + 2 * VT_BLK;
+    // small arrays after SMALL (byte offsets)
+    static constexpr int O_BQKV = 0;                          // [3C] f32
+    static constexpr int O_BPROJ = O_BQKV + 3 * C * 4;        // [C] f32
+    static constexpr int O_SCALE = O_BPROJ + C * 4;           // [4] f32
+    static constexpr int O_MAX = O_SCALE + 16;                // [2 heads parity][2 halves][128] f32
+    static constexpr int O_PART = O_MAX + 2 * 2 * 128 * 4;    // [HEADS][2][128] f32
+    // per-tile metadata, three slots (tile k in slot k % 3): the producer fills
+    // tile k + 2's while the compute warps read tile k + 1's and it copies out
+    // tile k's
+    static constexpr int O_TOK = O_PART + HEADS * 2 * 128 * 4; // [3 slots][128] int
+    static constexpr int O_ALLOW = O_TOK + 3 * 128 * 4;       // [3 slots][lo, hi][128] u32
+    // [3 slots][2 windows] int4 {copy: 0 none, 1 TMA, 2 wraps; first token column;
+    // first image row (b*H + i); unused}
+    static constexpr int O_WIN = O_ALLOW + 3 * 2 * 128 * 4;
+    static constexpr int O_BIAS = O_WIN + 3 * 2 * 16;         // [HEADS][L*L] f32, times log2(e)
+    static constexpr int O_BARS = (O_BIAS + HEADS * L * L * 4 + 7) / 8 * 8;
+    static constexpr int NBARS = 16;
+    static constexpr int O_END = O_BARS + NBARS * 8 + 16;
+    static constexpr int BYTES = SMALL + O_END;
+    // TMEM columns: QKV accumulators, then (once drained) two S buffers, o, y
+    static constexpr int T_QK = 0;                      // 2C: q of head h at 32h, k at C + 32h
+    static constexpr int T_VT = 2 * C;                  // 128
+    static constexpr int T_SA = T_VT;                   // S of even heads
+    static constexpr int T_SB = 0;                      // S of odd heads
     static constexpr int T_O = T_VT + 128;              // C
     static constexpr int T_Y = T_O + C;                 // C
     static_assert(T_Y + C <= 512, "TMEM budget");
-    static_assert(N <= 64, "two windows per 128-row tile");
+    static_assert(2 * C >= 128, "the odd-head S buffer lies in the QK columns");
+    static_assert(M <= 8, "two windows of 8-row-aligned window rows per 128-row tile");
+    // keys (and tile rows) of one window: bit 8*ki + kj for ki, kj < M
+    static constexpr uint64_t FULL = M == 8 ? ~0ull : [] {
+        uint64_t m = 0;
+        for (int i = 0; i < M; ++i) m |= ((1ull << M) - 1ull) << (8 * i);
+        return m;
+    }();
+    static_assert(BYTES + 1024 <= 232448, "shared memory budget");
 };
 
 struct FusedArgs {
@@ -108,21 +155,24 @@ struct FusedArgs {
     Geom g;
 };
 
-// Barrier among the 256 compute threads (named barrier 1); returns the OR of
-// `v` over them, so that a failure seen by one thread is seen by all.
-__device__ __forceinline__ bool compute_sync_or(bool v)
+// Barrier among `count` threads (named barrier `id`); returns the OR of `v`
+// over them, so that a failure seen by one thread is seen by all.
+template <int ID, int COUNT>
+__device__ __forceinline__ bool named_sync_or(bool v)
 {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, 256, p;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)v)
+        : "r"((uint32_t)v), "n"(ID), "n"(COUNT)
         : "memory");
     return r != 0;
 }
+__device__ __forceinline__ bool compute_sync_or(bool v) { return named_sync_or<1, NCOMPUTE>(v); }
+__device__ __forceinline__ bool producer_sync_or(bool v) { return named_sync_or<2, NPROD>(v); }
 
 // Bounded wait that also gives up as soon as another thread has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t limit_ns, volatile int *abort)
@@ -140,8 +190,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
 }
 
 // One arrival per warp on a ready barrier: every lane's prior shared-memory
-// writes (made visible to the async proxy by the caller) and TMEM loads
-// happen before it.
+// writes (made visible to the async proxy by the caller where an MMA reads
+// them) and TMEM loads happen before it.
 __device__ __forceinline__ void warp_arrive(uint32_t bar, int lane)
 {
     tc_fence_before();
@@ -149,46 +199,61 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar, int lane)
     if (lane == 0) mbar_arrive(bar);
 }
 
+__device__ __forceinline__ uint4 pack8(const float *v, const float4 b0, const float4 b1)
+{
+    return make_uint4(pack_bf16x2(v[0] + b0.x, v[1] + b0.y), pack_bf16x2(v[2] + b0.z, v[3] + b0.w),
+                      pack_bf16x2(v[4] + b1.x, v[5] + b1.y), pack_bf16x2(v[6] + b1.z, v[7] + b1.w));
+}
+
+__device__ __forceinline__ uint4 pack8(const float *v)
+{
+    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                      pack_bf16x2(v[6], v[7]));
+}
+
 template <int M, int C>
-__global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, DeviceStatus st)
+__global__ void __launch_bounds__(FBOUND_THREADS, 1)
+    fused_block_kernel(FusedArgs a, DeviceStatus st, const __grid_constant__ CUtensorMap tmap_x,
+                       const __grid_constant__ CUtensorMap tmap_out)
+// tmap_x: x as [B*H][W][C], boxes of 32 x 8 x M; tmap_out: out as [B*H][W][C],
+// boxes of 32 x M x M
 {
     using F = FusedCfg<M, C>;
-    constexpr int N = F::N, HEADS = F::HEADS, L = F::L, KB = F::KB;
+    constexpr int N = F::N, HEADS = F::HEADS, L = F::L, KB = F::KB, CH = F::CH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_align(smem_raw, 1024);
-    float *sbias = reinterpret_cast<float *>(sm + F::SMALL);        // [HEADS][L*L], times log2(e)
-    float *sbqkv = sbias + HEADS * L * L;                             // [3C]
-    float *sbproj = sbqkv + 3 * C;                                    // [C]
-    float *sscale = sbproj + C;                                       // [HEADS]
-    float *smax = sscale + HEADS;                                     // [2][128] partial row maxima
-    float *spart = smax + 2 * 128;                                    // [HEADS][2][128] partial row sums
-    // token of each tile row (-1 if none), three rotating copies: tile k uses
-    // copy k % 3 and fills copy (k + 1) % 3 for the next tile while other warps
-    // may still read copy (k - 1) % 3 for the previous tile's stores
-    int *rowtok = reinterpret_cast<int *>(spart + HEADS * 2 * 128);   // [3][128]
-    int *key_region = rowtok + 3 * 128;                               // [2][64]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_align(reinterpret_cast<uint8_t *>(key_region + 2 * 64), 8));
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    uint8_t *small = sm + F::SMALL;
+    float *sbqkv = reinterpret_cast<float *>(small + F::O_BQKV);
+    float *sbproj = reinterpret_cast<float *>(small + F::O_BPROJ);
+    float *sscale = reinterpret_cast<float *>(small + F::O_SCALE);
+    float *smax = reinterpret_cast<float *>(small + F::O_MAX);
+    float *spart = reinterpret_cast<float *>(small + F::O_PART);
+    int *stok = reinterpret_cast<int *>(small + F::O_TOK);
+    uint32_t *sallow = reinterpret_cast<uint32_t *>(small + F::O_ALLOW);
+    int4 *swin = reinterpret_cast<int4 *>(small + F::O_WIN);
+    float *sbias = reinterpret_cast<float *>(small + F::O_BIAS);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + F::O_BARS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + F::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
-    __shared__ int slot_masked[2];
 
     const Geom g = a.g;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool is_mma = warp == NCWARPS;
-    const int quarter = warp & 3, half = (warp >> 2) & 1;
-    const int row = quarter * 32 + lane;       // tile row = TMEM lane
-    const int slot = row >> 6, t = row & 63;   // window slot and token of the row
     const uint32_t base = smem_u32(sm);
-    // done barriers (tcgen05.commit) and ready barriers (one arrival per compute warp)
-    const uint32_t B_QKV = smem_u32(&bars[0]), B_S = smem_u32(&bars[1]), B_PV = smem_u32(&bars[2]),
+    // done barriers (tcgen05.commit, count 1)
+    const uint32_t B_QKV = smem_u32(&bars[0]), B_PV = smem_u32(&bars[1]), B_O = smem_u32(&bars[2]),
                    B_Y = smem_u32(&bars[3]);
-    const uint32_t R_QK = smem_u32(&bars[4]), R_P = smem_u32(&bars[5]), R_O = smem_u32(&bars[6]),
-                   R_FREE = smem_u32(&bars[7]);
+    auto B_S = [&](int r) { return smem_u32(&bars[4 + r]); };           // S buffer r written
+    // ready barriers (one arrival per compute warp, or per producer warp for R_X)
+    const uint32_t R_QK = smem_u32(&bars[6]), R_O = smem_u32(&bars[7]);
+    auto R_P = [&](int r) { return smem_u32(&bars[8 + r]); };           // P in S buffer r
+    auto R_X = [&](int b) { return smem_u32(&bars[10 + b]); };          // x tile in X(b)
+    auto R_STAGE = [&](int b) { return smem_u32(&bars[12 + b]); };      // output rows staged in X(b)
     const int64_t ntiles = (g.nwin + 1) / 2;
     auto xbuf = [&](int buf) { return buf ? F::X1 : F::X0; };
+    auto t_s = [&](int r) { return r ? F::T_SB : F::T_SA; };
 
     // ---- once per CTA: weights, biases, tables, barriers, TMEM ---------------
-    if (!is_mma) {
+    if (warp < NCWARPS) {
         for (int q = tid; q < (2 * C) * (C / 8); q += NCOMPUTE) {     // Wq, Wk rows
             const int r = q / (C / 8), c16 = q % (C / 8);
             cp_async16(base + F::WQK + (c16 >> 2) * (2 * C * 64) + sw64_offset(r, c16 & 3),
@@ -205,6 +270,7 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
             cp_async16(base + F::WP + (c16 >> 2) * (C * 64) + sw64_offset(r, c16 & 3),
                        a.Wproj + (int64_t)r * C + c16 * 8, 16);
         }
+        cp_async_commit();
         for (int i = tid; i < HEADS * L * L; i += NCOMPUTE) {
             const int hd = i / (L * L), e = i % (L * L);
             sbias[i] = __bfloat162float(a.table[(int64_t)e * HEADS + hd]) * FLOG2E;
@@ -213,60 +279,187 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
         for (int i = tid; i < C; i += NCOMPUTE) sbproj[i] = a.bproj ? __bfloat162float(a.bproj[i]) : 0.f;
         if (tid < HEADS)
             sscale[tid] = a.mode == 1 ? FLOG2E / fmaxf(a.tau[tid], 0.01f) : FLOG2E * rsqrtf(32.0f);
-    }
-    if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
-        for (int i = 4; i < 8; ++i) mbar_init(smem_u32(&bars[i]), NCWARPS);
-        *abort_flag = 0;
-        mbar_init_fence();
-    }
-    if (is_mma) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
-        tmem_relinquish();
-    }
-
-    // token (b*H*W + i*W + j) of every row of tile `tile`, -1 for padding rows
-    // and a missing second window; rows 0..127 by threads 0..127
-    auto row_tokens = [&](int64_t tile, int *dst) {
-        if (tid < 128) {
-            const int sl = tid >> 6, tt = tid & 63;
-            const int win = (int)(2 * tile) + sl;
-            dst[tid] = (tile < ntiles && tt < N && win < g.nwin) ? window_row_to_token32(g, win * N + tt) : -1;
-        }
-    };
-    // x rows of the tile whose row tokens are in `tok` into X buffer `buf`
-    // (zeros where tok < 0); compute threads only
-    auto load_x = [&](const int *tok, int buf) {
-        const uint32_t xb = base + xbuf(buf);
-#pragma unroll
-        for (int i = 0; i < 128 * (C / 8) / NCOMPUTE; ++i) {
-            const int q = tid + NCOMPUTE * i;
-            const int r = q / (C / 8), c16 = q % (C / 8);
-            const int tk = tok[r];
-            const bf16 *src = tk >= 0 ? a.x + (int64_t)tk * C + c16 * 8 : a.x;
-            cp_async16(xb + (c16 >> 2) * (128 * 64) + sw64_offset(r, c16 & 3), src, tk >= 0 ? 16u : 0u);
-        }
-        cp_async_commit();
-    };
-#ifdef SWIN_PHASE_TRACE
-    if (tid == 0) g_cta_trace[blockIdx.x * 4 + 0] = (long long)global_timer_ns();
-#endif
-    row_tokens(blockIdx.x, rowtok);
-    __syncthreads();
-    if (!is_mma) {
-        load_x(rowtok, 0);
+        // rows that no window token fills (8*ti + tj with ti or tj >= M, a
+        // missing second window) start as zeros and only ever hold finite
+        // values after that (o = 0, y = bproj), so their masked products are 0
+        for (int i = tid; i < 2 * F::XSZ / 16; i += NCOMPUTE)
+            reinterpret_cast<uint4 *>(sm + F::X0)[i] = make_uint4(0u, 0u, 0u, 0u);
         cp_async_wait<0>();
         fence_proxy_async_smem();
     }
+    if (tid == 0) {
+        for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[i]), 1);          // B_*
+        for (int i = 6; i < 10; ++i) mbar_init(smem_u32(&bars[i]), NCWARPS);   // R_QK, R_O, R_P
+        for (int i = 10; i < 12; ++i) mbar_init(smem_u32(&bars[i]), 2);        // R_X: producer warps
+        for (int i = 12; i < 14; ++i) mbar_init(smem_u32(&bars[i]), NCWARPS);  // R_STAGE
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+#ifdef SWIN_PHASE_TRACE
+    if (tid == 0) g_cta_trace[blockIdx.x * 4 + 0] = (long long)global_timer_ns();
+#endif
     tc_fence_before();
-    __syncthreads();   // weights, tables, the first tile's x, barriers, TMEM address
+    __syncthreads();   // weights, tables, barriers, TMEM address
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (is_mma) {
+    if (warp >= PWARP0) {
+        // ===================== producer warps =====================
+        const int p = tid - PWARP0 * 32;
+        const bool tma_thread = p == 0;             // issues every TMA copy
+        const bool wrap_warp = warp == PWARP0 + 1;  // copies the rows of wrapping windows
+        // row -> token map (-1 for rows no token fills), the keys each row may
+        // attend to (bit 8*ki + kj = key (ki, kj) of its window: the whole
+        // window, or its own shift region; none for an empty row) and how
+        // each window is copied, for tile `tile` into metadata slot `ms`
+        auto meta = [&](int64_t tile, int ms) {
+#pragma unroll 1
+            for (int r = p; r < 128; r += NPROD) {
+                const int sl = r >> 6, tp = r & 63, ti = tp >> 3, tj = tp & 7;
+                const int64_t win = 2 * tile + sl;
+                const bool wvalid = win < g.nwin;
+                int bi = 0, wi = 0, wj = 0;
+                if (wvalid) {
+                    const int per = g.nh * g.nw;
+                    bi = (int)(win / per);
+                    const int rem = (int)win - bi * per;
+                    wi = rem / g.nw;
+                    wj = rem - wi * g.nw;
+                }
+                // first shifted-frame position of the window in the original frame
+                int i0 = wi * M + g.s, j0 = wj * M + g.s;
+                int tok = -1;
+                uint64_t allow = 0;
+                if (wvalid && ti < M && tj < M) {
+                    int ii = i0 + ti, jj = j0 + tj;
+                    if (ii >= g.H) ii -= g.H;
+                    if (jj >= g.W) jj -= g.W;
+                    tok = (bi * g.H + ii) * g.W + jj;
+                    if (g.s > 0 && (wi == g.nh - 1 || wj == g.nw - 1)) {
+                        // same region = same row band and same column band
+                        const int rb = shift_band(wi * M + ti, g.H, M, g.s);
+                        const int cb = shift_band(wj * M + tj, g.W, M, g.s);
+                        uint64_t cols = 0;
+                        for (int kj = 0; kj < M; ++kj)
+                            if (shift_band(wj * M + kj, g.W, M, g.s) == cb) cols |= 1ull << kj;
+                        for (int ki = 0; ki < M; ++ki)
+                            if (shift_band(wi * M + ki, g.H, M, g.s) == rb) allow |= cols << (8 * ki);
+                    } else {
+                        allow = F::FULL;
+                    }
+                }
+                stok[ms * 128 + r] = tok;
+                sallow[(ms * 2 + 0) * 128 + r] = (uint32_t)allow;
+                sallow[(ms * 2 + 1) * 128 + r] = (uint32_t)(allow >> 32);
+                // a window is one box of x unless the shift wraps it around the
+                // bottom or right edge (last window row or column)
+                if (tp == 0) {
+                    const bool wraps = g.s > 0 && (wi == g.nh - 1 || wj == g.nw - 1);
+                    swin[ms * 2 + sl] = make_int4(wvalid ? (wraps ? 2 : 1) : 0, j0, bi * g.H + i0, 0);
+                }
+            }
+        };
+        // x rows of the tile whose metadata is in slot `ms` into X(b); one
+        // arrival per producer warp on R_X(b) (the TMA thread's carries the
+        // transaction bytes)
+        auto load_x = [&](int b, int ms) {
+            const uint32_t xb = base + xbuf(b);
+            if (tma_thread) {
+                const int4 w0 = swin[ms * 2], w1 = swin[ms * 2 + 1];
+                const uint32_t bytes = ((w0.x == 1) + (w1.x == 1)) * KB * (M * 8 * 64);
+                mbar_arrive_expect_tx(R_X(b), bytes);
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    const int4 w = sl ? w1 : w0;
+                    if (w.x != 1) continue;
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_load_3d(xb + kb * (128 * 64) + sl * (64 * 64), &tmap_x, kb * 32, w.y, w.z, R_X(b));
+                }
+            }
+            if (wrap_warp) {
+                for (int sl = 0; sl < 2; ++sl) {
+                    if (swin[ms * 2 + sl].x != 2) continue;
+#pragma unroll 4
+                    for (int q = lane; q < 64 * (C / 8); q += 32) {
+                        const int r = sl * 64 + q / (C / 8), c16 = q % (C / 8);
+                        const int tk = stok[ms * 128 + r];
+                        if (tk >= 0)
+                            cp_async16(xb + (c16 >> 2) * (128 * 64) + sw64_offset(r, c16 & 3),
+                                       a.x + (int64_t)tk * C + c16 * 8, 16u);
+                    }
+                }
+                cp_async_commit();
+                cp_async_wait<0>();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(R_X(b));
+            }
+        };
+        bool failed = false;
+        for (int j = 0; j < 3; ++j) {
+            const int64_t tile = blockIdx.x + (int64_t)j * gridDim.x;
+            if (tile < ntiles) meta(tile, j);
+        }
+        producer_sync_or(false);
+        load_x(0, 0);
+        if (blockIdx.x + (int64_t)gridDim.x < ntiles) load_x(1, 1);
+        int k = 0;
+#pragma unroll 1
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+            const int b = k & 1, ms = k % 3;
+            if (!wait_or_abort(R_STAGE(b), (k >> 1) & 1, st.wait_ns, abort_flag)) failed = true;
+            if (producer_sync_or(failed)) { failed = true; break; }
+            if (p == 0) TRACE_AT(3, k, 0);
+            // staged rows -> out through the window reverse + roll(+s) map
+            const uint32_t xb = base + xbuf(b);
+            if (tma_thread) {
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    const int4 w = swin[ms * 2 + sl];
+                    if (w.x != 1) continue;
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_store_3d(&tmap_out, kb * 32, w.y, w.z, xb + kb * (128 * 64) + sl * (64 * 64));
+                }
+                bulk_commit();
+                bulk_wait_read();   // X(b) may be refilled once the stores have read it
+            }
+            if (wrap_warp) {
+                // staged row of token (ti, tj): M*ti + tj of its window's half
+                const uint8_t *stage = sm + xbuf(b);
+                for (int sl = 0; sl < 2; ++sl) {
+                    if (swin[ms * 2 + sl].x != 2) continue;
+#pragma unroll 4
+                    for (int q = lane; q < N * CH; q += 32) {
+                        const int d = q / CH, c = q % CH;
+                        const int tk = stok[ms * 128 + sl * 64 + (d / M) * 8 + d % M];
+                        *reinterpret_cast<uint4 *>(a.out + (int64_t)tk * C + c * 8) =
+                            *reinterpret_cast<const uint4 *>(stage + (c >> 2) * (128 * 64) +
+                                                             sw64_offset(sl * 64 + d, c & 3));
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            producer_sync_or(false);   // every read of X(b) and of slot ms is done
+            if (p == 0) TRACE_AT(3, k, 1);
+            // X(b) takes the tile two ahead; slot ms the tile three ahead
+            if (tile + 2 * (int64_t)gridDim.x < ntiles) load_x(b, (k + 2) % 3);
+            if (p == 0) TRACE_AT(3, k, 2);
+            if (tile + 3 * (int64_t)gridDim.x < ntiles) meta(tile + 3 * (int64_t)gridDim.x, ms);
+            if (p == 0) TRACE_AT(3, k, 3);
+        }
+        cp_async_wait<0>();
+        if (tma_thread) bulk_wait_all();
+        if (failed) *abort_flag = 1;
+    } else if (warp == MMA_WARP) {
         // ===================== MMA warp (lane 0 issues) =====================
         if (lane == 0) {
-            uint32_t ph_qk = 0, ph_p = 0, ph_o = 0, ph_free = 0, ph_pv_m = 0;
+            uint32_t ph_pv = 0, ph_rp = 0;   // ph_rp bit r: phase of R_P(r)
             const uint32_t id_qk = idesc_bf16(128, 2 * C), id_vt = idesc_bf16(128, 128);
             const uint32_t id_s = idesc_bf16(128, 128), id_pv = idesc_bf16(128, 32), id_y = idesc_bf16(128, C);
             auto issue_qkv = [&](int buf) {
@@ -285,104 +478,107 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
                                  desc_kmajor_sw64(xb + kb * (128 * 64) + 32 * ks), id_vt, (kb | ks) != 0);
                 mma_commit(B_QKV);
             };
+            auto issue_s = [&](int hd) {
+                const uint32_t d = tmem + t_s(hd & 1);
+                mma_bf16(d, desc_kmajor_sw64(base + F::QA + hd * 8192), desc_kmajor_sw64(base + F::KA + hd * 8192),
+                         id_s, 0);
+                mma_bf16(d, desc_kmajor_sw64(base + F::QA + hd * 8192 + 32),
+                         desc_kmajor_sw64(base + F::KA + hd * 8192 + 32), id_s, 1);
+                mma_commit(B_S(hd & 1));
+            };
+            bool ok = wait_or_abort(R_X(0), 0, st.wait_ns, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_qkv(0);
+            }
             int k = 0;
-            if ((int64_t)blockIdx.x < ntiles) issue_qkv(0);
 #pragma unroll 1
-            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+            for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++k) {
                 const int buf = k & 1;
-                bool ok = true;
+                // every head's q and k drained: both S buffers are free
+                if (!(ok = wait_or_abort(R_QK, k & 1, st.wait_ns, abort_flag))) break;
+                tc_fence_after();
+                issue_s(0);
+                if (HEADS > 1) issue_s(1);
 #pragma unroll 1
-                for (int hd = 0; hd < HEADS && ok; ++hd) {
-                    ok = wait_or_abort(R_QK, ph_qk, st.wait_ns, abort_flag);
-                    ph_qk ^= 1;
-                    if (!ok) break;
-                    tc_fence_after();
-                    mma_bf16(tmem + F::T_S, desc_kmajor_sw64(base + F::Q), desc_kmajor_sw64(base + F::K), id_s, 0);
-                    mma_bf16(tmem + F::T_S, desc_kmajor_sw64(base + F::Q + 32), desc_kmajor_sw64(base + F::K + 32),
-                             id_s, 1);
-                    mma_commit(B_S);
-                    ok = wait_or_abort(R_P, ph_p, st.wait_ns, abort_flag);
-                    ph_p ^= 1;
-                    if (!ok) break;
+                for (int hd = 0; hd < HEADS; ++hd) {
+                    const int r = hd & 1;
+                    if (!(ok = wait_or_abort(R_P(r), (ph_rp >> r) & 1u, st.wait_ns, abort_flag))) break;
+                    ph_rp ^= 1u << r;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const int kb = kk >> 2, ks = kk & 3;
-                        mma_bf16_ts(tmem + F::T_O + 32 * hd, tmem + F::T_S + 8 * kk,
+                        mma_bf16_ts(tmem + F::T_O + 32 * hd, tmem + t_s(r) + 8 * kk,
                                     desc_kmajor_sw128(base + F::VT + kb * F::VT_BLK + (hd * 32 / 8) * 1024 + 32 * ks),
                                     id_pv, kk != 0);
                     }
                     mma_commit(B_PV);
-                    // the next MMA that writes these TMEM columns (S of the next head,
-                    // or the next tile's QKV) waits until P.V has read P
-                    ok = wait_or_abort(B_PV, ph_pv_m, st.wait_ns, abort_flag);
-                    ph_pv_m ^= 1;
-                    if (!ok) break;
+                    if (hd == HEADS - 1) mma_commit(B_O);
+                    // S of head hd + 2 reuses this buffer once P.V has read P
+                    if (!(ok = wait_or_abort(B_PV, ph_pv, st.wait_ns, abort_flag))) break;
+                    ph_pv ^= 1;
+                    if (hd + 2 < HEADS) issue_s(hd + 2);
                 }
                 if (!ok) break;
-                // next tile's QKV as soon as this tile's softmax has freed its TMEM
-                // columns and the next x tile has landed
-                if (tile + gridDim.x < ntiles) {
-                    if (!wait_or_abort(R_FREE, ph_free, st.wait_ns, abort_flag)) break;
-                    ph_free ^= 1;
-                    tc_fence_after();
-                    issue_qkv(buf ^ 1);
+                TRACE_AT(2, k, 0);
+                // this tile's projection once o is in X(buf), and the next tile's
+                // QKV once its x has landed (all of this tile's P has been read),
+                // whichever is ready first, the projection when both are
+                bool need_x = tile + gridDim.x < ntiles, need_y = true;
+                const uint64_t t0 = global_timer_ns();
+                while (need_x || need_y) {
+                    if (need_y && mbar_try_wait(R_O, k & 1)) {
+                        tc_fence_after();
+                        const uint32_t xb = base + xbuf(buf);
+#pragma unroll
+                        for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+                            for (int ks = 0; ks < 2; ++ks)
+                                mma_bf16(tmem + F::T_Y, desc_kmajor_sw64(xb + kb * (128 * 64) + 32 * ks),
+                                         desc_kmajor_sw64(base + F::WP + kb * (C * 64) + 32 * ks), id_y,
+                                         (kb | ks) != 0);
+                        mma_commit(B_Y);
+                        need_y = false;
+                        TRACE_AT(2, k, 1);
+                        continue;
+                    }
+                    if (need_x && mbar_try_wait(R_X(buf ^ 1), ((k + 1) >> 1) & 1)) {
+                        tc_fence_after();
+                        issue_qkv(buf ^ 1);
+                        need_x = false;
+                        TRACE_AT(2, k, 2);
+                        continue;
+                    }
+                    if (*abort_flag || global_timer_ns() - t0 > st.wait_ns) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
                 }
-                if (!wait_or_abort(R_O, ph_o, st.wait_ns, abort_flag)) break;
-                ph_o ^= 1;
-                tc_fence_after();
-                const uint32_t xb = base + xbuf(buf);
-#pragma unroll
-                for (int kb = 0; kb < KB; ++kb)
-#pragma unroll
-                    for (int ks = 0; ks < 2; ++ks)
-                        mma_bf16(tmem + F::T_Y, desc_kmajor_sw64(xb + kb * (128 * 64) + 32 * ks),
-                                 desc_kmajor_sw64(base + F::WP + kb * (C * 64) + 32 * ks), id_y, (kb | ks) != 0);
-                mma_commit(B_Y);
             }
         }
     } else {
         // ===================== compute warps =====================
+        const int quarter = warp & 3, half = (warp >> 2) & 1;
+        const int row = quarter * 32 + lane;       // tile row = TMEM lane
+        const int slot = row >> 6, t = row & 63;   // window slot; token (t >> 3, t & 7) of the row
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-        uint32_t ph_qkv = 0, ph_s = 0, ph_pv = 0, ph_y = 0;
+        // relative-bias row of this token (empty rows read a valid row, then are masked)
+        const int ti = t >> 3, tj = t & 7;
+        const int bias_base = ti < M && tj < M ? (ti + M - 1) * L + (tj + M - 1) : (M - 1) * L + (M - 1);
+        uint32_t ph_s = 0;   // bit r: phase of B_S(r)
         bool failed = false;
         int k = 0;
 #pragma unroll 1
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
             const int buf = k & 1;
-            const bool has_next = tile + gridDim.x < ntiles;
             PHASE(k, 0);
-            int *tok_cur = rowtok + (k % 3) * 128, *tok_next = rowtok + ((k + 1) % 3) * 128;
-            // this tile's window geometry: key regions and whether a window is cut
-            // by the shift; the next tile's row tokens
-            if (tid < 128) {
-                const int sl = tid >> 6, tt = tid & 63;
-                const int win = (int)(2 * tile) + sl;
-                int reg = -1;
-                if (tt < N && win < g.nwin) {
-                    const int rem = win % (g.nh * g.nw);
-                    const int wi = rem / g.nw, wj = rem % g.nw;
-                    reg = 0;
-                    if (g.s > 0)
-                        reg = 3 * shift_band(wi * M + tt / M, g.H, M, g.s) + shift_band(wj * M + tt % M, g.W, M, g.s);
-                    if (tt == 0) slot_masked[sl] = g.s > 0 && (wi == g.nh - 1 || wj == g.nw - 1);
-                } else if (tt == 0) {
-                    slot_masked[sl] = 0;
-                }
-                key_region[sl * 64 + tt] = reg;
-            }
-            row_tokens(tile + gridDim.x, tok_next);
-            if (compute_sync_or(failed)) { failed = true; break; }
-            PHASE(k, 1);
-            // prefetch the next tile into the other buffer (its o and staging
-            // were consumed by the previous tile, which has completed)
-            if (has_next) load_x(tok_next, buf ^ 1);
-            PHASE(k, 2);
-
-            if (!wait_or_abort(B_QKV, ph_qkv, st.wait_ns, abort_flag)) failed = true;
-            ph_qkv ^= 1;
+            // this tile's masks are in place once its x is, and its QKV is done
+            if (!wait_or_abort(R_X(buf), (k >> 1) & 1, st.wait_ns, abort_flag)) failed = true;
+            if (!wait_or_abort(B_QKV, k & 1, st.wait_ns, abort_flag)) failed = true;
             tc_fence_after();
-            PHASE(k, 3);
+            PHASE(k, 1);
 
             // v^T drain: lane = v channel, this half's 64 token columns -> V^T K block `half`
             {
@@ -393,30 +589,31 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
                 if (row < C) {
                     const float bv = sbqkv[2 * C + row];
                     uint8_t *dst = sm + F::VT + half * F::VT_BLK;
+                    const float4 b4 = make_float4(bv, bv, bv, bv);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4 *>(dst + sw128_offset(row, c)) =
-                            make_uint4(pack_bf16x2(v0[8 * c] + bv, v0[8 * c + 1] + bv),
-                                       pack_bf16x2(v0[8 * c + 2] + bv, v0[8 * c + 3] + bv),
-                                       pack_bf16x2(v0[8 * c + 4] + bv, v0[8 * c + 5] + bv),
-                                       pack_bf16x2(v0[8 * c + 6] + bv, v0[8 * c + 7] + bv));
+                        *reinterpret_cast<uint4 *>(dst + sw128_offset(row, c)) = pack8(v0 + 8 * c, b4, b4);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4 *>(dst + sw128_offset(row, 4 + c)) =
-                            make_uint4(pack_bf16x2(v1[8 * c] + bv, v1[8 * c + 1] + bv),
-                                       pack_bf16x2(v1[8 * c + 2] + bv, v1[8 * c + 3] + bv),
-                                       pack_bf16x2(v1[8 * c + 4] + bv, v1[8 * c + 5] + bv),
-                                       pack_bf16x2(v1[8 * c + 6] + bv, v1[8 * c + 7] + bv));
+                        *reinterpret_cast<uint4 *>(dst + sw128_offset(row, 4 + c)) = pack8(v1 + 8 * c, b4, b4);
                 }
             }
-            // q_h (half 0) or k_h (half 1) of head hd to shared memory
-            auto drain_qk = [&](int hd) {
+            // q (half 0) or k (half 1) of every head to shared memory
+#pragma unroll 1
+            for (int hd = 0; hd < HEADS; ++hd) {
                 const int col = half == 0 ? hd * 32 : C + hd * 32;
                 float v[32];
                 tmem_ld32(t_lane + F::T_QK + col, v);
                 tmem_wait_ld();
+                const float4 *b4 = reinterpret_cast<const float4 *>(sbqkv + col);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] += sbqkv[col + e];
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 bb = b4[e4];
+                    v[4 * e4] += bb.x;
+                    v[4 * e4 + 1] += bb.y;
+                    v[4 * e4 + 2] += bb.z;
+                    v[4 * e4 + 3] += bb.w;
+                }
                 if (a.mode == 1) {
                     float ss = 0.f;
 #pragma unroll
@@ -425,68 +622,55 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] *= inv;
                 }
-                uint8_t *dst = sm + (half == 0 ? F::Q : F::K);
+                uint8_t *dst = sm + (half == 0 ? F::QA : F::KA) + hd * 8192;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(dst + sw64_offset(row, c)) =
-                        make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
-                                   pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
-                fence_proxy_async_smem();
-                warp_arrive(R_QK, lane);
-            };
-            drain_qk(0);
-
-            const bool row_ok = key_region[slot * 64 + t] >= 0;
-            // keys this row may attend to (bit j = key j of its window): all N keys,
-            // or those in its own shift region; none for a padding row
-            uint32_t allow_lo = 0, allow_hi = 0;
-            if (row_ok) {
-                if (slot_masked[slot]) {
-                    const int my_region = key_region[slot * 64 + t];
-                    for (int j = 0; j < N; ++j) {
-                        if (key_region[slot * 64 + j] == my_region) {
-                            if (j < 32) allow_lo |= 1u << j;
-                            else allow_hi |= 1u << (j - 32);
-                        }
-                    }
-                } else {
-                    allow_lo = 0xffffffffu;
-                    allow_hi = N >= 64 ? 0xffffffffu : ((1u << (N - 32)) - 1u);
-                }
+                    *reinterpret_cast<uint4 *>(dst + sw64_offset(row, c)) = pack8(v + 8 * c);
             }
+            fence_proxy_async_smem();
+            warp_arrive(R_QK, lane);
+            PHASE(k, 2);
+
+            const int ms = k % 3;
+            const uint32_t allow_lo = sallow[(ms * 2 + 0) * 128 + row];
+            const uint32_t allow_hi = sallow[(ms * 2 + 1) * 128 + row];
+            const bool row_ok = (allow_lo | allow_hi) != 0;   // a real token always sees itself
             const uint32_t allow = half == 0 ? allow_lo : allow_hi;
-            const int tb = row_ok ? t : 0;   // padding rows read a valid bias row (then masked)
-            const int bias_base = (tb / M + M - 1) * L + (tb % M + M - 1);
 
 #pragma unroll 1
             for (int hd = 0; hd < HEADS; ++hd) {
-                PHASE(k, 4 + 4 * hd);
-                if (!wait_or_abort(B_S, ph_s, st.wait_ns, abort_flag)) failed = true;
-                ph_s ^= 1;
+                const int r = hd & 1;
+                if (!wait_or_abort(B_S(r), (ph_s >> r) & 1u, st.wait_ns, abort_flag)) failed = true;
+                ph_s ^= 1u << r;
                 tc_fence_after();
-                PHASE(k, 5 + 4 * hd);
+                PHASE(k, 3 + 3 * hd);
 
                 // ---- softmax over this row's own window, keys 32*half .. +31 -------
                 float s[32];
-                tmem_ld32(t_lane + F::T_S + 64 * slot + 32 * half, s);
+                tmem_ld32(t_lane + t_s(r) + 64 * slot + 32 * half, s);
                 tmem_wait_ld();
                 const float scale = sscale[hd];
                 const float *bias = sbias + hd * L * L + bias_base;
                 float mx = -INFINITY;
-                // key j of the row's window: relative-bias row bias_base - ((j/M)*L + j%M);
-                // j is a compile-time constant in each unrolled loop
+                // key column j = 8*ki + kj of the row's window: relative-bias row
+                // bias_base - (ki*L + kj); j is a compile-time constant in each
+                // unrolled loop, and columns with ki or kj >= M hold no key
                 if (half == 0) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float v = fmaf(s[j], scale, bias[-((j / M) * L + j % M)]);
-                        s[j] = (allow >> j) & 1u ? v : -INFINITY;
+                        if ((j >> 3) < M && (j & 7) < M) {
+                            const float v = fmaf(s[j], scale, bias[-((j >> 3) * L + (j & 7))]);
+                            s[j] = (allow >> j) & 1u ? v : -INFINITY;
+                        } else {
+                            s[j] = -INFINITY;
+                        }
                         mx = fmaxf(mx, s[j]);
                     }
                 } else {
 #pragma unroll
                     for (int j = 32; j < 64; ++j) {
-                        if (j < N) {
-                            const float v = fmaf(s[j - 32], scale, bias[-((j / M) * L + j % M)]);
+                        if ((j >> 3) < M && (j & 7) < M) {
+                            const float v = fmaf(s[j - 32], scale, bias[-((j >> 3) * L + (j & 7))]);
                             s[j - 32] = (allow >> (j - 32)) & 1u ? v : -INFINITY;
                         } else {
                             s[j - 32] = -INFINITY;
@@ -494,16 +678,11 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
                         mx = fmaxf(mx, s[j - 32]);
                     }
                 }
-                smax[half * 128 + row] = mx;
-                if (hd == HEADS - 1 && has_next) {
-                    // this tile's last TMEM reads of the QK and S columns are done, and
-                    // the next x tile is in place: the MMA warp may start its QKV
-                    cp_async_wait<0>();
-                    fence_proxy_async_smem();
-                    warp_arrive(R_FREE, lane);
-                }
+                float *mxb = smax + r * 256;
+                mxb[half * 128 + row] = mx;
                 if (compute_sync_or(failed)) { failed = true; break; }
-                mx = row_ok ? fmaxf(smax[row], smax[128 + row]) : 0.f;   // padding rows: all -inf -> p = 0
+                PHASE(k, 4 + 3 * hd);
+                mx = row_ok ? fmaxf(mxb[row], mxb[128 + row]) : 0.f;   // padding rows: all -inf -> p = 0
                 float sum = 0.f;
                 uint32_t pk[16];
 #pragma unroll
@@ -513,34 +692,28 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
                     pk[jj / 2] = pack_bf16x2(p0, p1);
                 }
                 spart[(hd * 2 + half) * 128 + row] = sum;
-                PHASE(k, 6 + 4 * hd);
-                // P may be rewritten only once the previous head's P.V has read it
-                if (hd > 0) {
-                    if (!wait_or_abort(B_PV, ph_pv, st.wait_ns, abort_flag)) failed = true;
-                    ph_pv ^= 1;
-                }
-                // P (bf16, two keys per 32-bit column) goes to TMEM over the first 64
-                // columns of S, the A operand of the P.V MMA: row r holds its window's
-                // keys in columns 32*slot .. +31 and zeros for the other window's
+                // P (bf16, two keys per 32-bit column) over the first 64 columns of
+                // this S buffer, the A operand of the P.V MMA: row r holds its
+                // window's keys in columns 32*slot .. +31 and zeros for the other
+                // window's
                 {
-                    tmem_st16(t_lane + F::T_S + 32 * slot + 16 * half, pk);
+                    tmem_st16(t_lane + t_s(r) + 32 * slot + 16 * half, pk);
                     const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                    tmem_st16(t_lane + F::T_S + 32 * (slot ^ 1) + 16 * half, zero);
+                    tmem_st16(t_lane + t_s(r) + 32 * (slot ^ 1) + 16 * half, zero);
                     tmem_wait_st();
                 }
-                warp_arrive(R_P, lane);
-                PHASE(k, 7 + 4 * hd);
-                if (hd + 1 < HEADS) drain_qk(hd + 1);
+                warp_arrive(R_P(r), lane);
+                PHASE(k, 5 + 3 * hd);
             }
-            // (a failure here is not uniform across threads yet: carry on to the
-            // next barrier-with-OR, which makes every compute thread leave together;
-            // waits return at once once the abort flag is set)
-            if (!wait_or_abort(B_PV, ph_pv, st.wait_ns, abort_flag)) failed = true;
-            ph_pv ^= 1;
+            // (a failure above is not uniform across threads yet: the barrier
+            // below makes every compute thread leave together; waits return at
+            // once after an abort)
+            if (!wait_or_abort(B_O, k & 1, st.wait_ns, abort_flag)) failed = true;
+            if (compute_sync_or(failed)) { failed = true; break; }   // also orders spart
             tc_fence_after();
-            PHASE(k, 17);
+            PHASE(k, 20);
 
-            // ---- o / rowsum -> bf16 -> X buffer (A operand of the projection) ------
+            // ---- o / rowsum -> bf16 -> X(buf) (A operand of the projection) ------
 #pragma unroll
             for (int hd = 0; hd < HEADS; ++hd) {
                 float o[16];
@@ -548,62 +721,47 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
                 tmem_wait_ld();
                 const float l = spart[(hd * 2) * 128 + row] + spart[(hd * 2 + 1) * 128 + row];
                 const float inv = row_ok ? rcp_approx(l) : 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) o[e] *= inv;
                 uint8_t *dst = sm + xbuf(buf) + hd * (128 * 64);
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
-                    *reinterpret_cast<uint4 *>(dst + sw64_offset(row, 2 * half + c)) =
-                        make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
-                                   pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                                   pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                                   pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+                    *reinterpret_cast<uint4 *>(dst + sw64_offset(row, 2 * half + c)) = pack8(o + 8 * c);
             }
             fence_proxy_async_smem();
             warp_arrive(R_O, lane);
-            PHASE(k, 18);
-            if (!wait_or_abort(B_Y, ph_y, st.wait_ns, abort_flag)) failed = true;
-            ph_y ^= 1;
+            PHASE(k, 21);
+            if (!wait_or_abort(B_Y, k & 1, st.wait_ns, abort_flag)) failed = true;
             tc_fence_after();
-            PHASE(k, 19);
+            PHASE(k, 22);
 
-            // ---- y + bproj -> bf16 staging rows -> out through window reverse + roll(+s) ----
-            // (thread = row reads its half of y from TMEM into a staging row with a
-            // padded, bank-conflict-free stride; then all compute threads copy the
-            // rows out in 16-byte chunks, consecutive lanes on consecutive chunks,
-            // so each warp store covers whole rows that are contiguous in out
-            // within a window row)
+            // ---- y + bproj -> bf16 rows in X(buf), token (ti, tj) of a window at
+            // row M*ti + tj of its half (one dense box per window for the TMA
+            // store through the window reverse + roll(+s) map) ----
             {
                 constexpr int HC = C / 2;
                 uint8_t *stage = sm + xbuf(buf);
-                uint8_t *srow = stage + row * F::SROW + half * HC * 2;
+                const bool tok_row = ti < M && tj < M;
+                const int srow = slot * 64 + ti * M + tj;
 #pragma unroll
                 for (int c0 = 0; c0 < HC; c0 += 16) {
                     float y[16];
                     tmem_ld16(t_lane + F::T_Y + half * HC + c0, y);
                     tmem_wait_ld();
-                    const float *bp = sbproj + half * HC + c0;
-                    uint4 *d4 = reinterpret_cast<uint4 *>(srow + c0 * 2);
+                    const float4 *bp = reinterpret_cast<const float4 *>(sbproj + half * HC + c0);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        d4[c] = make_uint4(pack_bf16x2(y[8 * c] + bp[8 * c], y[8 * c + 1] + bp[8 * c + 1]),
-                                           pack_bf16x2(y[8 * c + 2] + bp[8 * c + 2], y[8 * c + 3] + bp[8 * c + 3]),
-                                           pack_bf16x2(y[8 * c + 4] + bp[8 * c + 4], y[8 * c + 5] + bp[8 * c + 5]),
-                                           pack_bf16x2(y[8 * c + 6] + bp[8 * c + 6], y[8 * c + 7] + bp[8 * c + 7]));
-                }
-                tc_fence_before();
-                if (compute_sync_or(failed)) { failed = true; break; }
-                constexpr int CH = C / 8;   // 16-byte chunks per row
-#pragma unroll 1
-                for (int q = tid; q < 128 * CH; q += NCOMPUTE) {
-                    const int r = q / CH, c16 = q % CH;
-                    const int tk = tok_cur[r];
-                    if (tk >= 0)
-                        *reinterpret_cast<uint4 *>(a.out + (int64_t)tk * C + c16 * 8) =
-                            *reinterpret_cast<const uint4 *>(stage + r * F::SROW + c16 * 16);
+                    for (int c = 0; c < 2; ++c) {
+                        const int chunk = (half * HC + c0) / 8 + c;
+                        if (tok_row)
+                            *reinterpret_cast<uint4 *>(stage + (chunk >> 2) * (128 * 64) + sw64_offset(srow, chunk & 3)) =
+                                pack8(y + 8 * c, bp[2 * c], bp[2 * c + 1]);
+                    }
                 }
             }
-            PHASE(k, 20);
+            fence_proxy_async_smem();   // the TMA stores read these rows
+            warp_arrive(R_STAGE(buf), lane);
+            PHASE(k, 23);
         }
-        cp_async_wait<0>();
         if (failed) *abort_flag = 1;
     }
 #ifdef SWIN_PHASE_TRACE
@@ -617,7 +775,7 @@ __global__ void __launch_bounds__(FTHREADS, 1) fused_block_kernel(FusedArgs a, D
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && *abort_flag) atomicOr(st.err, ERR_TIMEOUT);
-    if (is_mma) {
+    if (warp == MMA_WARP) {
         __syncwarp();
         tmem_dealloc(tmem, 512);
     }
@@ -642,9 +800,14 @@ cudaError_t launch_fused_t(const FusedArgs &a, DeviceStatus st, cudaStream_t str
     auto kern = fused_block_kernel<M, C>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    CUtensorMap tx, to;
+    e = make_tensor_map_sw64_3d(&tx, a.x, (int64_t)a.g.B * a.g.H, a.g.W, C, 8, M);
+    if (e != cudaSuccess) return e;
+    e = make_tensor_map_sw64_3d(&to, a.out, (int64_t)a.g.B * a.g.H, a.g.W, C, M, M);
+    if (e != cudaSuccess) return e;
     const int64_t ntiles = (a.g.nwin + 1) / 2;
     const int grid = (int)(ntiles < num_sms() ? ntiles : num_sms());
-    kern<<<grid, FTHREADS, smem, stream>>>(a, st);
+    kern<<<grid, FTHREADS, smem, stream>>>(a, st, tx, to);
     return cudaGetLastError();
 }
 

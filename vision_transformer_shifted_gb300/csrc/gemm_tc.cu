@@ -388,7 +388,112 @@ __global__ void __launch_bounds__(THREADS) gemm_mn_test_kernel(GemmArgs a, Devic
     if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
+// Test kernel of the lane-masked MMA forms: every 128-row block is two halves
+// that each see their own B.  Bw is [2N, K]; rows 0..63 of a block multiply
+// B0 = Bw[0:N], rows 64..127 B1 = Bw[N:2N], written into the same N columns
+// by two MMAs with complementary lane masks -- once with A from shared memory
+// (D columns 0..N-1 of the output) and once with A from TMEM (columns N..2N-1).
+// K <= 128 (multiple of 32), N <= 128 (multiple of 16).
+__global__ void __launch_bounds__(THREADS) gemm_pair_test_kernel(GemmArgs a, DeviceStatus st)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_align(smem_raw, 1024);
+    uint8_t *sA = smem;                                          // 2 K blocks x [128 rows][128 B]
+    uint8_t *sB = smem + 2 * 128 * 128;                          // 2 K blocks x [256 rows][128 B]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sB + 2 * 256 * 128);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int64_t m0 = (int64_t)blockIdx.x * BM;
+    const int N = a.N, K = a.K;
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(smem_u32(bar), 1);
+        mbar_init_fence();
+    }
+    for (int q = tid; q < 128 * 16; q += THREADS) {               // A rows (zero past rows / K)
+        const int r = q / 16, c16 = q % 16;
+        const int64_t R = m0 + r;
+        const bool ok = R < a.rows && c16 * 8 < K;
+        cp_async16(smem_u32(sA) + (c16 >> 3) * (128 * 128) + sw128_offset(r, c16 & 7),
+                   ok ? a.A + R * a.lda + c16 * 8 : a.A, ok ? 16u : 0u);
+    }
+    for (int q = tid; q < 2 * N * 16; q += THREADS) {             // B0 and B1 rows (zero past K)
+        const int n = q / 16, c16 = q % 16;
+        const bool ok = c16 * 8 < K;
+        cp_async16(smem_u32(sB) + (c16 >> 3) * (256 * 128) + sw128_offset(n, c16 & 7),
+                   ok ? a.Bw + (int64_t)n * K + c16 * 8 : a.Bw, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    {   // A row of this thread -> TMEM columns 256 + (K/2)
+        const int64_t R = m0 + tid;
+        for (int c0 = 0; c0 < K / 2; c0 += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                r[i] = R < a.rows ? *reinterpret_cast<const uint32_t *>(a.A + R * a.lda + 2 * (c0 + i)) : 0u;
+            tmem_st16(t_lane + 256 + c0, r);
+        }
+        tmem_wait_st();
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        const uint32_t id = idesc_bf16(BM, N);
+        const uint32_t keep_top[4] = {0u, 0u, ~0u, ~0u};   // lanes 64..127 masked
+        const uint32_t keep_bot[4] = {~0u, ~0u, 0u, 0u};   // lanes 0..63 masked
+        for (int half = 0; half < 2; ++half) {
+            const uint32_t b0 = smem_u32(sB) + half * N * 128;   // B row offset N: whole 8-row groups
+            for (int kk = 0; kk < K / 16; ++kk) {
+                const uint64_t bd = desc_kmajor_sw128(b0 + (kk >> 2) * (256 * 128) + 32 * (kk & 3));
+                mma_bf16_mask(tmem, desc_kmajor_sw128(smem_u32(sA) + (kk >> 2) * (128 * 128) + 32 * (kk & 3)), bd,
+                              id, kk != 0, half ? keep_bot : keep_top);
+                mma_bf16_ts_mask(tmem + 128, tmem + 256 + 8 * kk, bd, id, kk != 0, half ? keep_bot : keep_top);
+            }
+        }
+        mma_commit(smem_u32(bar));
+    }
+    const bool ok = mbar_wait(smem_u32(bar), 0, st.wait_ns);
+    tc_fence_after();
+    const int64_t R = m0 + tid;
+    for (int part = 0; part < 2; ++part)
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tmem_ld16(t_lane + 128 * part + c0, v);
+            tmem_wait_ld();
+            if (R < a.rows && ok) {
+                float b[16];
+                for (int i = 0; i < 16; ++i) b[i] = 0.f;
+                store_row_bf16(a.D + R * a.ldd + part * N + c0, v, b, 16);
+            }
+        }
+    if (!ok && tid == 0) atomicOr(st.err, ERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 } // namespace
+
+cudaError_t launch_gemm_pair_test(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
+{
+    if (a.K % 32 || a.K > 128 || a.N % 16 || a.N > 128 || a.N < 16 || a.rows <= 0) return cudaErrorInvalidValue;
+    const size_t smem = 1024 + 2 * 128 * 128 + 2 * 256 * 128 + 64;
+    cudaError_t e = cudaFuncSetAttribute(gemm_pair_test_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    gemm_pair_test_kernel<<<(unsigned)((a.rows + BM - 1) / BM), THREADS, smem, stream>>>(a, st);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gemm_mn_test(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
 {
