@@ -33,13 +33,13 @@
 //       window and 32 channels, plain stores for wrapping windows
 // Nothing but x, the weights and out touches HBM.
 //
-// Warp roles.  Warps 0..7 compute: warp w serves TMEM lane quarter w % 4 =
-// tile rows 32(w%4)..+31 and column half w / 4 (every drain and the softmax
-// split their columns between the two halves).  Three warps issue the
+// Warp roles.  Warps 4..11 compute: warp w serves TMEM lane quarter w % 4 =
+// tile rows 32(w%4)..+31 and column half w / 4 - 1 (every drain and the
+// softmax split their columns between the two halves).  Three warps issue the
 // tcgen05 MMAs (lane 0 each; an MMA costs its issuing thread some 80 cycles
 // whatever its size, so the small attention MMAs are spread over two
-// issuers): warps 8 and 9 the S and P.V halves of the first and second
-// window's rows, warp 10 the next tile's QKV and the projection.  Warp 11
+// issuers): warps 0 and 1 the S and P.V halves of the first and second
+// window's rows, warp 2 the next tile's QKV and the projection.  Warp 3
 // produces and retires tiles: the row -> token map and the attention masks
 // of a tile, its x gather into one of two x buffers (freed as soon as the
 // tile's QKV has read it), and the output store.  All hand-offs are mbarriers: "ready" barriers get one arrival per
@@ -57,9 +57,13 @@ namespace {
 
 constexpr int NCWARPS = 8;                       // compute warps
 constexpr int NCOMPUTE = NCWARPS * 32;
-constexpr int ATT_WARP0 = NCWARPS;               // warps 8, 9: S and P.V of one window's rows each
-constexpr int QKV_WARP = NCWARPS + 2;            // warp 10: QKV and the projection
-constexpr int PWARP = NCWARPS + 3;               // warp 11: producer
+// (the issuers and the producer take the lowest warp indices: a warp
+// scheduler that prefers older warps then serves them first; they wait by
+// suspending on mbarriers, so they take no issue slots while idle)
+constexpr int ATT_WARP0 = 0;                     // warps 0, 1: S and P.V of one window's rows each
+constexpr int QKV_WARP = 2;                      // warp 2: QKV and the projection
+constexpr int PWARP = 3;                         // warp 3: producer
+constexpr int CWARP0 = 4;                        // warps 4..11: compute
 constexpr int NPROD = 32;
 constexpr int FTHREADS = NCOMPUTE + 3 * 32 + NPROD;   // 384
 // (384 threads cap registers at 168 per thread, so that three warps of one
@@ -82,7 +86,7 @@ __device__ int g_trace_cta;   // the CTA whose phases are recorded
     } while (0)
 #define PHASE(k, i)                                                                                  \
     do {                                                                                             \
-        if (tid == 0 || tid == 128) TRACE_AT(tid >> 7, k, i);                                        \
+        if (tid == CWARP0 * 32 || tid == (CWARP0 + 4) * 32) TRACE_AT(tid == CWARP0 * 32 ? 0 : 1, k, i); \
     } while (0)
 #else
 #define TRACE_AT(who, k, i) \
@@ -95,7 +99,6 @@ __device__ int g_trace_cta;   // the CTA whose phases are recorded
 
 template <int M, int C>
 struct FusedCfg {
-    static constexpr int N = M * M;
     static constexpr int HEADS = C / 32;
     static constexpr int L = 2 * M - 1;
     static constexpr int KB = C / 32;          // 32-channel K blocks (64-byte swizzle)
@@ -195,21 +198,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
     }
 }
 
-// Bounded non-blocking spin (for the MMA issuers, which must react within a
-// few cycles); gives up once another thread has aborted.
-__device__ __forceinline__ bool spin_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, volatile int *abort)
-{
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_test_wait(bar, parity)) {
-        if (*abort) return false;
-        if (global_timer_ns() - t0 > limit_ns) {
-            *abort = 1;
-            return false;
-        }
-    }
-    return true;
-}
-
 // One arrival per warp on a ready barrier: every lane's prior shared-memory
 // writes (made visible to the async proxy by the caller where an MMA reads
 // them) and TMEM loads happen before it.
@@ -281,35 +269,36 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
     auto t_s = [&](int r) { return r ? F::T_SB : F::T_SA; };
 
     // ---- once per CTA: weights, biases, tables, barriers, TMEM ---------------
-    if (warp < NCWARPS) {
-        for (int q = tid; q < (2 * C) * (C / 8); q += NCOMPUTE) {     // Wq, Wk rows
+    if (warp >= CWARP0) {
+        const int ct = tid - CWARP0 * 32;   // compute thread index
+        for (int q = ct; q < (2 * C) * (C / 8); q += NCOMPUTE) {     // Wq, Wk rows
             const int r = q / (C / 8), c16 = q % (C / 8);
             cp_async16(base + F::WQK + (c16 >> 2) * (2 * C * 64) + sw64_offset(r, c16 & 3),
                        a.Wqkv + (int64_t)r * C + c16 * 8, 16);
         }
-        for (int q = tid; q < C * (C / 8); q += NCOMPUTE) {           // Wv rows
+        for (int q = ct; q < C * (C / 8); q += NCOMPUTE) {           // Wv rows
             const int r = q / (C / 8), c16 = q % (C / 8);
             cp_async16(base + F::WV + (c16 >> 2) * (C * 64) + sw64_offset(r, c16 & 3),
                        a.Wqkv + (int64_t)(2 * C + r) * C + c16 * 8, 16);
         }
-        for (int q = tid; q < C * (C / 8); q += NCOMPUTE) {           // Wproj
+        for (int q = ct; q < C * (C / 8); q += NCOMPUTE) {           // Wproj
             const int r = q / (C / 8), c16 = q % (C / 8);
             cp_async16(base + F::WP + (c16 >> 2) * (C * 64) + sw64_offset(r, c16 & 3),
                        a.Wproj + (int64_t)r * C + c16 * 8, 16);
         }
         cp_async_commit();
-        for (int i = tid; i < HEADS * L * L; i += NCOMPUTE) {
+        for (int i = ct; i < HEADS * L * L; i += NCOMPUTE) {
             const int hd = i / (L * L), e = i % (L * L);
             sbias[i] = __bfloat162float(a.table[(int64_t)e * HEADS + hd]) * FLOG2E;
         }
-        for (int i = tid; i < 3 * C; i += NCOMPUTE) sbqkv[i] = a.bqkv ? __bfloat162float(a.bqkv[i]) : 0.f;
-        for (int i = tid; i < C; i += NCOMPUTE) sbproj[i] = a.bproj ? __bfloat162float(a.bproj[i]) : 0.f;
-        if (tid < HEADS)
-            sscale[tid] = a.mode == 1 ? FLOG2E / fmaxf(a.tau[tid], 0.01f) : FLOG2E * rsqrtf(32.0f);
+        for (int i = ct; i < 3 * C; i += NCOMPUTE) sbqkv[i] = a.bqkv ? __bfloat162float(a.bqkv[i]) : 0.f;
+        for (int i = ct; i < C; i += NCOMPUTE) sbproj[i] = a.bproj ? __bfloat162float(a.bproj[i]) : 0.f;
+        if (ct < HEADS)
+            sscale[ct] = a.mode == 1 ? FLOG2E / fmaxf(a.tau[ct], 0.01f) : FLOG2E * rsqrtf(32.0f);
         // rows that no window token fills (8*ti + tj with ti or tj >= M, a
         // missing second window) start as zeros and only ever hold finite
         // values after that (o = 0, y = bproj), so their masked products are 0
-        for (int i = tid; i < 2 * F::XSZ / 16; i += NCOMPUTE)
+        for (int i = ct; i < 2 * F::XSZ / 16; i += NCOMPUTE)
             reinterpret_cast<uint4 *>(sm + F::X0)[i] = make_uint4(0u, 0u, 0u, 0u);
         cp_async_wait<0>();
         fence_proxy_async_smem();
@@ -558,11 +547,11 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
                 // head's are; P.V of head h once its P is in TMEM (head 0: and
                 // every v drained); S of head h + 2 once this issuer's P.V h has
                 // read P out of that buffer
-                if (!(ok = spin_wait(R_Q0, k & 1, st.wait_ns, abort_flag))) break;
+                if (!(ok = wait_or_abort(R_Q0, k & 1, st.wait_ns, abort_flag))) break;
                 tc_fence_after();
                 issue_s(0);
                 if (HEADS > 1) {
-                    if (!(ok = spin_wait(R_QK, k & 1, st.wait_ns, abort_flag))) break;
+                    if (!(ok = wait_or_abort(R_QK, k & 1, st.wait_ns, abort_flag))) break;
                     tc_fence_after();
                     issue_s(1);
                 }
@@ -570,14 +559,14 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
 #pragma unroll 1
                 for (int hd = 0; hd < HEADS; ++hd) {
                     const int r = hd & 1;
-                    if (!(ok = spin_wait(R_P(r), (ph_rp >> r) & 1u, st.wait_ns, abort_flag))) break;
+                    if (!(ok = wait_or_abort(R_P(r), (ph_rp >> r) & 1u, st.wait_ns, abort_flag))) break;
                     ph_rp ^= 1u << r;
-                    if (hd == 0 && !(ok = spin_wait(R_V, k & 1, st.wait_ns, abort_flag))) break;
+                    if (hd == 0 && !(ok = wait_or_abort(R_V, k & 1, st.wait_ns, abort_flag))) break;
                     tc_fence_after();
                     if (w == 0) TRACE_AT(2, k, 14 + hd);
                     issue_pv(hd);
                     if (w == 0) TRACE_AT(2, k, 4 + hd);
-                    if (!(ok = spin_wait(B_PVW(w), ph_pvw, st.wait_ns, abort_flag))) break;
+                    if (!(ok = wait_or_abort(B_PVW(w), ph_pvw, st.wait_ns, abort_flag))) break;
                     ph_pvw ^= 1;
                     if (w == 0) TRACE_AT(2, k, 7 + hd);
                     if (hd + 2 < HEADS) issue_s(hd + 2);
@@ -606,7 +595,7 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
                 mma_commit(B_QKV);
                 mma_commit(B_XFREE(buf));
             };
-            bool ok = spin_wait(R_X(0), 0, st.wait_ns, abort_flag);
+            bool ok = wait_or_abort(R_X(0), 0, st.wait_ns, abort_flag);
             if (ok) {
                 tc_fence_after();
                 issue_qkv(0);
@@ -618,14 +607,14 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
                 // the next tile's QKV once this tile's q, k and v have left TMEM
                 // and the next x has landed
                 if (tile + gridDim.x < ntiles) {
-                    if (!(ok = spin_wait(R_V, k & 1, st.wait_ns, abort_flag))) break;
-                    if (!(ok = spin_wait(R_X(buf ^ 1), ((k + 1) >> 1) & 1, st.wait_ns, abort_flag))) break;
+                    if (!(ok = wait_or_abort(R_V, k & 1, st.wait_ns, abort_flag))) break;
+                    if (!(ok = wait_or_abort(R_X(buf ^ 1), ((k + 1) >> 1) & 1, st.wait_ns, abort_flag))) break;
                     tc_fence_after();
                     issue_qkv(buf ^ 1);
                     TRACE_AT(2, k, 2);
                 }
                 // the projection once o is in the v tiles
-                if (!(ok = spin_wait(R_O, k & 1, st.wait_ns, abort_flag))) break;
+                if (!(ok = wait_or_abort(R_O, k & 1, st.wait_ns, abort_flag))) break;
                 tc_fence_after();
                 const uint32_t oa = base + F::VA;
 #pragma unroll
@@ -640,7 +629,7 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
         }
     } else {
         // ===================== compute warps =====================
-        const int quarter = warp & 3, half = (warp >> 2) & 1;
+        const int quarter = warp & 3, half = (warp >> 2) - 1;
         const int row = quarter * 32 + lane;       // tile row = TMEM lane
         const int slot = row >> 6, t = row & 63;   // window slot; token (t >> 3, t & 7) of the row
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
