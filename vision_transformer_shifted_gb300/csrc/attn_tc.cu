@@ -254,9 +254,12 @@ struct FlashSmem {
     static constexpr int k_off = q_off + 128 * 64;     // 2 x [128][64 B] SW64
     static constexpr int v_off = k_off + 2 * 128 * 64; // 2 x [128 keys][64 B] SW64 (N-major B)
     static constexpr int end = v_off + 2 * 128 * 64;
+    // per-key metadata of the whole window (key_off, key_region: keys rounded
+    // up to whole 128-key tiles), smax and spart, the bias table, barriers
     static size_t bytes(int M)
     {
-        return 1024 + end + (size_t)(2 * M - 1) * (2 * M - 1) * 4 + 2 * 128 * 4 * 2 + 2 * 2 * 128 * 4 + 64;
+        const size_t keys = (size_t)((M * M + 127) / 128) * 128;
+        return 1024 + end + keys * 4 * 2 + 2 * 2 * 128 * 4 + (size_t)(2 * M - 1) * (2 * M - 1) * 4 + 64;
     }
 };
 
@@ -271,9 +274,10 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
     uint8_t *sm = smem_align(smem_raw, 1024);
     // after the tiles (1024-aligned): key_off first, so that its int4 loads are
     // 16-byte aligned, then the other per-key and per-row arrays, then the bias
-    int *key_off = reinterpret_cast<int *>(sm + FlashSmem::end);        // [2 buffers][128]
-    int *key_region = key_off + 2 * 128;                                 // [2][128], -1 past N
-    float *smax = reinterpret_cast<float *>(key_region + 2 * 128);       // [2][128]
+    const int kpad = ((N + 127) / 128) * 128;
+    int *key_off = reinterpret_cast<int *>(sm + FlashSmem::end);        // [kpad], relative-bias offset of key
+    int *key_region = key_off + kpad;                                    // [kpad], -1 past N
+    float *smax = reinterpret_cast<float *>(key_region + kpad);          // [2][128]
     float *spart = smax + 2 * 128;                                       // [2][128]
     float *sbias = spart + 2 * 128;                                      // [L*L], times log2(e)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem_align(reinterpret_cast<uint8_t *>(sbias + L * L), 8));
@@ -302,9 +306,18 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
 
     for (int i = tid; i < L * L; i += FL_THREADS)
         sbias[i] = __bfloat162float(a.table[(int64_t)i * a.heads + head]) * LOG2E;
-    // bars: 0 = S done, 1 = P.V done, 2 + b = key buffer b full (TMA transactions)
+    // every key of the window: its offset into the relative-bias table and its
+    // shift region (once per CTA, not per key tile)
+    for (int kj = tid; kj < kpad; kj += FL_THREADS) {
+        const bool ok = kj < N;
+        const int ki = ok ? kj / M : 0, kc = ok ? kj - ki * M : 0;
+        key_off[kj] = ki * L + kc;
+        key_region[kj] = ok ? token_region(g, wi, wj, ki, kc) : -1;
+    }
+    // bars: 0 = S done, 1 = P.V done (two committing threads), 2 + b = key
+    // buffer b full (TMA transactions)
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), i == 1 ? 2 : 1);
         mbar_init_fence();
     }
     if (warp == 0) {
@@ -324,12 +337,6 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
             if (kt == 0) tma_load_2d(sQ, &tmap, head * 32, (int)(row0 + q0), full);
             tma_load_2d(sK + b * (128 * 64), &tmap, C + head * 32, (int)(row0 + kt * 128), full);
             tma_load_2d(sV + b * (128 * 64), &tmap, 2 * C + head * 32, (int)(row0 + kt * 128), full);
-        }
-        if (tid < 128) {
-            const int kj = kt * 128 + tid;
-            const bool ok = kj < N;
-            key_off[b * 128 + tid] = ok ? (kj / M) * L + (kj % M) : 0;
-            key_region[b * 128 + tid] = ok ? token_region(g, wi, wj, kj / M, kj % M) : -1;
         }
     };
     __syncthreads();   // barrier initialisation is visible before any TMA completes on it
@@ -382,11 +389,11 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
 #pragma unroll
             for (int j = 0; j < 32; ++j) { sv[j] = c0[j]; sv[32 + j] = c1[j]; }
         }
-        const int *koff = key_off + b * 128 + 64 * half;
+        const int *koff = key_off + kt * 128 + 64 * half;
         const int nvalid = N - kt * 128 - 64 * half;   // keys of this thread's 64 that exist
         float mt = -INFINITY;
         if (masked) {
-            const int *kreg = key_region + b * 128 + 64 * half;
+            const int *kreg = key_region + kt * 128 + 64 * half;
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
                 const float lv = fmaf(sv[j], scale, sbias[base - koff[j]]);
@@ -448,23 +455,28 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
         if (__syncthreads_or(failed)) { failed = true; break; }
         tc_fence_after();
         FPHASE(kt, 7);
-        if (tid == 0) {
+        // P.V in two halves over the tile's keys, issued by two threads (an MMA
+        // costs its issuing thread the same whatever its size): keys 0..63 into
+        // TMEM columns 128.., keys 64..127 into 160..; both commit to bar_pv
+        if (tid == 0 || tid == 32) {
+            const int kh = tid >> 5;
             const uint32_t id = idesc_bf16_bmn(128, 32);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mma_bf16_ts(tmem + 128, tmem + 8 * k, desc_mnmajor_sw64(sV + b * (128 * 64) + 1024 * k, 128 * 64), id,
-                            k);
+            for (int k = 0; k < 4; ++k)
+                mma_bf16_ts(tmem + 128 + 32 * kh, tmem + 32 * kh + 8 * k,
+                            desc_mnmajor_sw64(sV + b * (128 * 64) + 4096 * kh + 1024 * k, 128 * 64), id, k);
             mma_commit(bar_pv);
         }
         if (!mbar_wait(bar_pv, phase, st.wait_ns)) failed = true;
         phase ^= 1;
         tc_fence_after();
         FPHASE(kt, 8);
-        float ot[16];
+        float ot[16], ou[16];
         tmem_ld16(t_lane + 128 + 16 * half, ot);
+        tmem_ld16(t_lane + 160 + 16 * half, ou);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) o[e] = fmaf(o[e], alpha, ot[e]);
+        for (int e = 0; e < 16; ++e) o[e] = fmaf(o[e], alpha, ot[e] + ou[e]);
         FPHASE(kt, 9);
         tc_fence_before();
         if (__syncthreads_or(failed)) { failed = true; break; }
