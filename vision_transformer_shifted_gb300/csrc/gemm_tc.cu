@@ -215,11 +215,16 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
     if (warp == 0) tmem_dealloc(tmem, tmem_cols);
 }
 
-// Largest N tile <= 256 that divides N and is a multiple of `step` (16, or
-// 32 when 32-column chunks must stay whole).
+// Largest N tile <= 128 that divides N and is a multiple of `step` (16, or
+// 32 when 32-column chunks must stay whole); larger only when nothing <= 128
+// divides N.  (At most 128 columns keep a CTA's 3-stage ring under 100 KB,
+// so that two CTAs share an SM and one's epilogue overlaps the other's
+// loads.)
 int pick_bn(int N, int step)
 {
-    for (int bn = 256 / step * step; bn >= step; bn -= step)
+    for (int bn = 128 / step * step; bn >= step; bn -= step)
+        if (N % bn == 0) return bn;
+    for (int bn = 256 / step * step; bn > 128; bn -= step)
         if (N % bn == 0) return bn;
     return 0;
 }
