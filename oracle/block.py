@@ -1,0 +1,89 @@
+"""Float64 CPU oracle of the whole Swin Transformer block around the
+shifted-window attention: LayerNorm, the residual connections and the MLP.
+
+TEST INFRASTRUCTURE ONLY, under the same rule as the rest of this package:
+the tests, ``__graft_entry__.smoke()`` and the CPU legs of ``bench.py`` use
+it; the GPU library never does, and nothing here imports the library.
+
+The attention sub-layer is ``oracle.forward`` (the float64 block the rest of
+the package pins).  Around it ("Swin Transformer V2" (neura.market), How It
+Works: the original Swin normalises before each sub-layer; V2 normalises the
+output of each residual branch before adding it back to the main branch):
+
+    V1 (pre-norm):           z = x + attn(LN1(x));  y = z + MLP(LN2(z))
+    V2 (residual post-norm): z = x + LN1(attn(x));  y = z + LN2(MLP(z))
+
+The pages give no formula for the sub-layers; the readings taken (the plain
+transformer-block ones): LayerNorm over the C channels of a token with the
+biased variance, eps = 1e-5, per-channel gain and shift; MLP(u) =
+GELU(u W1^T + b1) W2^T + b2 with hidden width r*C; GELU the exact form
+x * Phi(x), Phi the standard normal CDF.  The extra LayerNorm that V2
+inserts every six blocks of its largest models is a stage-level detail and
+is not part of one block.
+
+Pins in ``tests/test_block.py``: LayerNorm statistics and its affine part,
+GELU's odd-part identity and the normal CDF at +-1, +-2 (textbook values),
+the MLP against an explicit sum, and closed forms of the whole block when a
+sub-layer is switched off.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import V1, V2, forward
+
+LN_EPS = 1e-5
+
+
+def layer_norm(x, gamma, beta, eps=LN_EPS):
+    """LayerNorm over the last axis: (x - mean) / sqrt(var + eps) * gamma +
+    beta, var the biased (1/C) variance."""
+    x = np.asarray(x, dtype=np.float64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps) * np.asarray(gamma, np.float64) + np.asarray(beta, np.float64)
+
+
+_erf = np.vectorize(math.erf, otypes=[np.float64])
+
+
+def gelu(x):
+    """Exact GELU: x * Phi(x) = x/2 * (1 + erf(x / sqrt 2))."""
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))
+
+
+def mlp(u, W1, b1, W2, b2):
+    """GELU(u W1^T + b1) W2^T + b2 over the last axis of u; W1 [rC, C],
+    W2 [C, rC]."""
+    u = np.asarray(u, dtype=np.float64)
+    h = gelu(u @ np.asarray(W1, np.float64).T + np.asarray(b1, np.float64))
+    return h @ np.asarray(W2, np.float64).T + np.asarray(b2, np.float64)
+
+
+def block(x, p, *, heads, M, shift, mode, attn_out=None):
+    """The whole block in float64.  x [B,H,W,C]; ``p`` a dict with ln1_g, ln1_b,
+    Wqkv, bqkv, table, tau, Wproj, bproj, ln2_g, ln2_b, W1, b1, W2, b2 (the
+    attention entries as ``oracle.forward`` takes them).  ``attn_out``, if
+    given, receives the attention sub-layer's output.  Returns (y, z): the
+    block output and the main branch after the attention sub-layer."""
+    x = np.asarray(x, dtype=np.float64)
+
+    def attn(u):
+        a = forward(u, p["Wqkv"], p["bqkv"], p["table"], p["tau"], p["Wproj"], p["bproj"], heads=heads, M=M,
+                    shift=shift, mode=mode)
+        if attn_out is not None:
+            attn_out[...] = a
+        return a
+
+    if mode == V1:
+        z = x + attn(layer_norm(x, p["ln1_g"], p["ln1_b"]))
+        y = z + mlp(layer_norm(z, p["ln2_g"], p["ln2_b"]), p["W1"], p["b1"], p["W2"], p["b2"])
+    elif mode == V2:
+        z = x + layer_norm(attn(x), p["ln1_g"], p["ln1_b"])
+        y = z + layer_norm(mlp(z, p["W1"], p["b1"], p["W2"], p["b2"]), p["ln2_g"], p["ln2_b"])
+    else:
+        raise ValueError("mode must be V1 or V2")
+    return y, z
