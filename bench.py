@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from vision_transformer_shifted_gb300.inputs import V2, WORKLOADS, generate  # noqa: E402
+from vision_transformer_shifted_gb300.inputs import V1, V2, WORKLOADS, generate  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 
@@ -395,6 +395,74 @@ def dominant_roofline(w, kernels, pk, ms):
             "peak_source": pk["source"] + " bf16 burst"}
 
 
+def run_block(args, w, ratio=4):
+    """The whole Swin block (LayerNorm, attention, residuals, MLP) on workload
+    ``w``, one JSON line; not the headline (that is the attention block)."""
+    from vision_transformer_shifted_gb300 import binding as sw
+    from vision_transformer_shifted_gb300.inputs import generate_block
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sw.load()
+    pk = peaks()
+    g = generate_block(w, ratio)
+    t = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in g.items()}
+    h_attn = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
+    table = table_for(w, g, dev, h_attn)
+    sw.swin_wattn_destroy(h_attn)
+    params = dict(ln1_gamma=t["ln1_gamma"], ln1_beta=t["ln1_beta"], Wqkv=t["Wqkv"], bqkv=t["bqkv"], bias_table=table,
+                  logit_scale=t.get("tau"), Wproj=t["Wproj"], bproj=t["bproj"], ln2_gamma=t["ln2_gamma"],
+                  ln2_beta=t["ln2_beta"], W1=t["mlp_W1"], b1=t["mlp_b1"], W2=t["mlp_W2"], b2=t["mlp_b2"])
+    h = sw.swin_block_create(w.C, w.heads, w.M, w.shift, w.mode, ratio)
+    io_bytes = w.tokens * w.C * 2 * 2
+    nsets = max(2, -(-(2 * L2_BYTES) // io_bytes) + 1)
+    xs = [t["x"]] + [torch.randn_like(t["x"], dtype=torch.float32).to(t["x"].dtype) for _ in range(nsets - 1)]
+    outs = [torch.empty_like(t["x"]) for _ in range(nsets)]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        sw.swin_block_forward(h, xs[i % nsets], params, outs[i % nsets], stream)
+
+    for i in range(args.warmup):
+        step(i)
+    assert sw.swin_block_sync_status(h, stream) == sw.OK
+    with ClockSampler(dev.index) as clk:
+        t_soak = time.perf_counter()
+        i = 0
+        while time.perf_counter() - t_soak < args.soak:
+            step(i)
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    assert sw.swin_block_sync_status(h, stream) == sw.OK
+    sw.swin_block_destroy(h)
+    T, C = w.tokens, w.C
+    flops = w.flops + 4 * T * C * ratio * C
+    alg_bytes = 2 * T * C * 2 + (4 * C * C + 2 * ratio * C * C) * 2
+    ai = flops / alg_bytes
+    roof_tf = min(pk["bf16_sust"], pk["hbm"] * 1e9 * ai / 1e12)
+    tflops = flops / (ms * 1e-3) / 1e12
+    line = {"metric": "swin block forward (LayerNorm, shifted-window attention, residuals, MLP) tokens/s",
+            "value": T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": C, "heads": w.heads, "M": w.M,
+                       "shift": w.shift, "mode": "V1 pre-norm" if w.mode == V1 else "V2 residual post-norm",
+                       "mlp_ratio": ratio},
+            "tflops": tflops,
+            "block_roofline": {"achieved_tflops": tflops, "roof_tflops": roof_tf, "frac": tflops / roof_tf,
+                               "ai_flop_per_byte": ai, "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
+                               "peak_source": pk["source"] + " (sustained bf16 / copy GB/s)"},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -407,11 +475,17 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--block", action="store_true",
+                    help="time the whole Swin block (LayerNorm, attention, residuals, MLP) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.block:
+        if w.dtype != "bf16" or args.impl != "ours" or args.gpus != 1:
+            ap.error("--block: bf16 workloads, our implementation, one GPU")
+        run_block(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_ours(args, w)

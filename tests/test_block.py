@@ -1,0 +1,273 @@
+"""The whole Swin block around the attention (LayerNorm, residuals, MLP).
+
+CPU (not gpu): the float64 block oracle against what the mathematics fixes
+-- LayerNorm statistics, GELU's odd part and the normal CDF at a few
+points, an MLP that reduces to the identity, closed forms of the block with
+the attention switched off -- and the C ABI's argument checks.
+GPU: the LayerNorm kernel and the whole block, through the C ABI, against
+the oracle.
+"""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import block as ob
+from vision_transformer_shifted_gb300 import binding as sw
+from vision_transformer_shifted_gb300.inputs import V1, V2, WORKLOADS, generate_block, sample_windows
+
+from helpers import oracle_table, to_f64, window_tokens
+
+DEV = "cuda"
+RNG = np.random.default_rng(20261202)
+
+# ---- oracle pins (CPU) ---------------------------------------------------------
+
+
+def test_layer_norm_statistics_and_affine_part():
+    x = RNG.normal(size=(64, 96)) * 3.0 + 1.5
+    y = ob.layer_norm(x, np.ones(96), np.zeros(96))
+    var = x.var(axis=-1)                                  # biased
+    assert np.allclose(y.mean(axis=-1), 0.0, atol=1e-12)
+    # the normalised row has variance var / (var + eps): catches an unbiased
+    # variance or eps taken outside the square root
+    assert np.allclose(y.var(axis=-1), var / (var + ob.LN_EPS), rtol=1e-12)
+    g, b = RNG.normal(size=96), RNG.normal(size=96)
+    assert np.allclose(ob.layer_norm(x, g, b), y * g + b, rtol=0, atol=1e-12)
+    # a constant row normalises to the shift
+    assert np.allclose(ob.layer_norm(np.full((1, 8), 7.0), g[:8], b[:8]), b[:8], atol=1e-12)
+
+
+def test_gelu_is_x_times_normal_cdf():
+    x = RNG.normal(size=1000) * 4
+    # odd part: GELU(x) - GELU(-x) = x (Phi(x) + Phi(-x) = 1)
+    assert np.allclose(ob.gelu(x) - ob.gelu(-x), x, atol=1e-12)
+    # standard normal CDF at 1 and 2 (textbook values); a tanh approximation
+    # misses these by ~1e-4
+    assert abs(ob.gelu(1.0) - 0.8413447460685429) < 1e-14
+    assert abs(ob.gelu(-1.0) + 0.15865525393145707) < 1e-14
+    assert abs(ob.gelu(2.0) - 2 * 0.9772498680518208) < 1e-13
+    assert ob.gelu(0.0) == 0.0
+
+
+def test_mlp_reduces_to_identity_through_gelus_odd_part():
+    C = 8
+    I = np.eye(C)
+    W1, W2 = np.vstack([I, -I]), np.hstack([I, -I])       # [2C, C], [C, 2C]
+    u = RNG.normal(size=(10, C)) * 2
+    b2 = RNG.normal(size=C)
+    assert np.allclose(ob.mlp(u, W1, np.zeros(2 * C), W2, b2), u + b2, atol=1e-12)
+    # with a first-layer bias [c; -c] the pair sees u + c: the MLP is u + c
+    # (a bias applied after the GELU would give u + 2c)
+    c = RNG.normal(size=C)
+    assert np.allclose(ob.mlp(u, W1, np.concatenate([c, -c]), W2, np.zeros(C)), u + c, atol=1e-12)
+    # even part: GELU(u) + GELU(-u) = u erf(u / sqrt 2)
+    even = ob.mlp(u, W1, np.zeros(2 * C), np.hstack([I, I]), np.zeros(C))
+    erf = np.vectorize(math.erf)
+    assert np.allclose(even, u * erf(u / math.sqrt(2.0)), atol=1e-12)
+
+
+def _tiny_params(C, heads, M, mode, zero_attention):
+    W1, W2 = np.vstack([np.eye(C), -np.eye(C)]), np.hstack([np.eye(C), -np.eye(C)])
+    p = dict(ln1_g=1 + 0.1 * RNG.normal(size=C), ln1_b=0.1 * RNG.normal(size=C),
+             ln2_g=1 + 0.1 * RNG.normal(size=C), ln2_b=0.1 * RNG.normal(size=C),
+             Wqkv=RNG.normal(size=(3 * C, C)) * 0.2, bqkv=RNG.normal(size=3 * C) * 0.02,
+             table=RNG.normal(size=((2 * M - 1) ** 2, heads)) * 0.1, tau=None if mode == V1 else np.full(heads, 0.3),
+             Wproj=np.zeros((C, C)) if zero_attention else RNG.normal(size=(C, C)) * 0.2,
+             bproj=np.zeros(C) if zero_attention else RNG.normal(size=C) * 0.02,
+             W1=W1, b1=np.zeros(2 * C), W2=W2, b2=np.zeros(C))
+    return p
+
+
+@pytest.mark.parametrize("mode", [V1, V2])
+def test_block_closed_forms_with_attention_off(mode):
+    """Attention output 0 and an identity MLP: V1 y = x + LN2(x); V2 (LN of a
+    zero vector is its shift) z = x + beta1, y = z + LN2(z)."""
+    B, H, W, C, heads, M, s = 1, 14, 14, 32, 1, 7, 3
+    x = RNG.normal(size=(B, H, W, C))
+    p = _tiny_params(C, heads, M, mode, zero_attention=True)
+    y, z = ob.block(x, p, heads=heads, M=M, shift=s, mode=mode)
+    if mode == V1:
+        assert np.allclose(z, x, atol=1e-12)
+    else:
+        assert np.allclose(z, x + p["ln1_b"], atol=1e-12)
+    assert np.allclose(y, z + ob.layer_norm(z, p["ln2_g"], p["ln2_b"]), atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", [V1, V2])
+def test_block_attention_branch_placement(mode):
+    """V1 feeds LN1(x) to the attention and adds its output; V2 feeds x and
+    adds LN1 of its output (so, with unit gain and zero shift, z - x is a
+    normalised vector: mean 0 per token)."""
+    B, H, W, C, heads, M, s = 1, 14, 14, 32, 1, 7, 3
+    x = RNG.normal(size=(B, H, W, C))
+    p = _tiny_params(C, heads, M, mode, zero_attention=False)
+    if mode == V2:
+        p["ln1_g"], p["ln1_b"] = np.ones(C), np.zeros(C)
+        p["ln2_g"], p["ln2_b"] = np.ones(C), np.zeros(C)
+        p["b2"] = RNG.normal(size=C)   # identity MLP plus a shift: MLP(z) = z + b2
+    a = np.empty_like(x)
+    y, z = ob.block(x, p, heads=heads, M=M, shift=s, mode=mode, attn_out=a)
+    if mode == V1:
+        ref = oracle.forward(ob.layer_norm(x, p["ln1_g"], p["ln1_b"]), p["Wqkv"], p["bqkv"], p["table"], p["tau"],
+                             p["Wproj"], p["bproj"], heads=heads, M=M, shift=s, mode=mode)
+        assert np.allclose(z - x, ref, atol=1e-12)
+        # identity MLP: the second sub-layer adds LN2 of the main branch z (not of x)
+        assert np.allclose(y - z, ob.layer_norm(z, p["ln2_g"], p["ln2_b"]), atol=1e-12)
+    else:
+        assert np.allclose((z - x).mean(axis=-1), 0.0, atol=1e-12)
+        assert np.allclose(z - x, ob.layer_norm(a, np.ones(C), np.zeros(C)), atol=1e-12)
+        # the second branch is normalised after the MLP: LN(z + b2), mean 0 per
+        # token (an MLP after the LayerNorm would give LN(z) + b2)
+        assert np.allclose((y - z).mean(axis=-1), 0.0, atol=1e-12)
+        assert np.allclose(y - z, ob.layer_norm(z + p["b2"], np.ones(C), np.zeros(C)), atol=1e-12)
+
+
+# ---- C ABI argument checks (CPU) ---------------------------------------------------
+
+
+def test_block_create_rejects_bad_arguments():
+    lib = sw.load()
+    h = ctypes.c_void_p(123)
+    assert lib.swin_block_create(ctypes.byref(h), 96, 3, 7, 3, sw.V1, 0) == sw.EINVAL      # mlp_ratio
+    assert h.value is None
+    assert lib.swin_block_create(ctypes.byref(h), 96, 3, 7, 3, sw.V1, 9) == sw.EINVAL
+    assert lib.swin_block_create(ctypes.byref(h), 96, 3, 7, 3, sw.V1 | sw.FP32, 4) == sw.EUNSUPPORTED
+    assert lib.swin_block_create(ctypes.byref(h), 100, 3, 7, 3, sw.V1, 4) == sw.EINVAL     # C % 16
+    assert lib.swin_block_create(None, 96, 3, 7, 3, sw.V1, 4) == sw.EINVAL
+    assert lib.swin_block_forward(None, None, 1, 7, 7, None, None, None) == sw.EINVAL
+    assert lib.swin_block_destroy(None) == sw.OK
+
+
+def test_block_layernorm_hook_rejects_bad_arguments():
+    lib = sw.load()
+    p16 = ctypes.c_void_p(16)
+    assert lib.swin_block_test_layernorm(p16, None, p16, p16, None, p16, 4, 100, 0, None) == sw.EINVAL  # C % 8
+    assert lib.swin_block_test_layernorm(p16, None, p16, p16, None, p16, 4, 96, 3, None) == sw.EINVAL   # flags
+    assert lib.swin_block_test_layernorm(p16, None, p16, p16, None, p16, 4, 96, 1, None) == sw.EINVAL   # b missing
+    assert lib.swin_block_test_layernorm(ctypes.c_void_p(18), None, p16, p16, None, p16, 4, 96, 0,
+                                         None) == sw.EINVAL                                              # alignment
+    assert lib.swin_block_test_layernorm(p16, None, p16, p16, None, p16, 0, 96, 0, None) == sw.OK     # no rows
+
+
+# ---- GPU parity ------------------------------------------------------------------------
+
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _block_compare(got, ref):
+    """bf16 block output vs float64: the residual stream z, the LayerNorm
+    outputs, the GELU activations and y are each rounded to bf16 once (2^-9
+    relative each), so the bounds scale with |y|.  In V2 the LayerNorm after
+    the attention rescales a small branch (std ~0.05) to unit variance, so the
+    attention's own relative error (~0.4% rel-L2, bf16 q/k/v/P) reaches the
+    main branch as ~4e-3 absolute: hence the mean bound 2^-8 mean|y| + 2e-3."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    stats = dict(max_abs=float(err.max()), mean_abs=float(err.mean()),
+                 rel_l2=float(np.linalg.norm(got - ref) / np.linalg.norm(ref)))
+    assert (err <= 2.0 ** -7 * np.abs(ref) + 2e-2).all(), stats
+    assert stats["mean_abs"] <= 2.0 ** -8 * float(np.abs(ref).mean()) + 2e-3, stats
+    assert stats["rel_l2"] <= 1e-2, stats
+    print("block parity", stats)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("C", [96, 128, 192, 512])
+@pytest.mark.parametrize("flags", [0, 1, 2])
+def test_layernorm_kernel(C, flags):
+    rows = 1000
+    a = _bf16(RNG.normal(size=(rows, C)) * 2 + 0.5)
+    b = _bf16(RNG.normal(size=(rows, C)))
+    g = _bf16(1 + 0.1 * RNG.normal(size=C))
+    be = _bf16(0.1 * RNG.normal(size=C))
+    out_sum = torch.empty(rows, C, dtype=torch.bfloat16, device=DEV)
+    out_ln = torch.empty(rows, C, dtype=torch.bfloat16, device=DEV)
+    sw.swin_block_test_layernorm(a.to(DEV), b.to(DEV), g.to(DEV), be.to(DEV), out_sum if flags == 1 else None,
+                                 out_ln, flags)
+    torch.cuda.synchronize()
+    A, Bm, G, Be = (to_f64(t) for t in (a, b, g, be))
+    if flags == 1:
+        s = (a.float() + b.float()).to(torch.bfloat16)   # the sum is stored, and normalised, as bf16
+        assert torch.equal(out_sum.cpu(), s)
+        ref = ob.layer_norm(to_f64(s), G, Be)
+    elif flags == 2:
+        ref = Bm + ob.layer_norm(A, G, Be)
+    else:
+        ref = ob.layer_norm(A, G, Be)
+    err = np.abs(to_f64(out_ln.cpu()) - ref)
+    assert (err <= 2.0 ** -8 * np.abs(ref) + 2e-3).all(), float(err.max())
+
+
+def _block_params_dev(g, table):
+    return dict(ln1_gamma=g["ln1_gamma"], ln1_beta=g["ln1_beta"], Wqkv=g["Wqkv"], bqkv=g["bqkv"], bias_table=table,
+                logit_scale=g["tau"], Wproj=g["Wproj"], bproj=g["bproj"], ln2_gamma=g["ln2_gamma"],
+                ln2_beta=g["ln2_beta"], W1=g["mlp_W1"], b1=g["mlp_b1"], W2=g["mlp_W2"], b2=g["mlp_b2"])
+
+
+def _oracle_params(g, table):
+    return dict(ln1_g=to_f64(g["ln1_gamma"]), ln1_b=to_f64(g["ln1_beta"]), Wqkv=to_f64(g["Wqkv"]),
+                bqkv=to_f64(g["bqkv"]), table=to_f64(table), tau=None if g["tau"] is None else to_f64(g["tau"]),
+                Wproj=to_f64(g["Wproj"]), bproj=to_f64(g["bproj"]), ln2_g=to_f64(g["ln2_gamma"]),
+                ln2_b=to_f64(g["ln2_beta"]), W1=to_f64(g["mlp_W1"]), b1=to_f64(g["mlp_b1"]), W2=to_f64(g["mlp_W2"]),
+                b2=to_f64(g["mlp_b2"]))
+
+
+def _run_block(w, g, table, ratio=4):
+    dev = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in _block_params_dev(g, table).items()}
+    x = g["x"].to(DEV)
+    out = torch.empty_like(x)
+    h = sw.swin_block_create(w.C, w.heads, w.M, w.shift, w.mode, ratio)
+    try:
+        sw.swin_block_forward(h, x, dev, out)
+        sw.swin_block_sync_status(h)
+    finally:
+        sw.swin_block_destroy(h)
+    return out.cpu()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("key,B,H,W", [("swin_t_s1", 2, 14, 21), ("swinv2_t_s1", 1, 16, 24), ("swin_t_s1", 1, 7, 7),
+                                       ("swin_b_s1", 1, 14, 14)])
+def test_block_forward_small(key, B, H, W):
+    w = WORKLOADS[key].with_(B=B, H=H, W=W)
+    g = generate_block(w)
+    table = oracle_table(w, g)
+    got = _run_block(w, g, table)
+    ref, _ = ob.block(to_f64(g["x"]), _oracle_params(g, table), heads=w.heads, M=w.M, shift=w.shift, mode=w.mode)
+    _block_compare(to_f64(got), ref)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("key", ["swin_t_s1", "swinv2_t_s1"])
+def test_block_forward_full_size_sampled(key):
+    """Full-size grid; the oracle computes the tokens of sampled windows (the
+    attention is window-local, everything else token-local)."""
+    w = WORKLOADS[key]
+    g = generate_block(w)
+    table = oracle_table(w, g)
+    got = to_f64(_run_block(w, g, table))
+    p = _oracle_params(g, table)
+    x = to_f64(g["x"])
+    wins = sample_windows(w, 6)
+    if w.mode == V1:
+        u = ob.layer_norm(x, p["ln1_g"], p["ln1_b"])
+    else:
+        u = x
+    a = oracle.forward(u, p["Wqkv"], p["bqkv"], p["table"], p["tau"], p["Wproj"], p["bproj"], heads=w.heads, M=w.M,
+                       shift=w.shift, mode=w.mode, windows=wins)
+    toks = window_tokens(w, wins)
+    xs, As = x.reshape(-1, w.C)[toks], a.reshape(-1, w.C)[toks]
+    if w.mode == V1:
+        z = xs + As
+        ref = z + ob.mlp(ob.layer_norm(z, p["ln2_g"], p["ln2_b"]), p["W1"], p["b1"], p["W2"], p["b2"])
+    else:
+        z = xs + ob.layer_norm(As, p["ln1_g"], p["ln1_b"])
+        ref = z + ob.layer_norm(ob.mlp(z, p["W1"], p["b1"], p["W2"], p["b2"]), p["ln2_g"], p["ln2_b"])
+    _block_compare(got.reshape(-1, w.C)[toks], ref)

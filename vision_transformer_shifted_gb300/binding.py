@@ -1,4 +1,5 @@
-"""ctypes binding of libswin_wattn (include/swin_wattn.h, swin_wattn_test.h).
+"""ctypes binding of libswin_wattn (include/swin_wattn.h, swin_wattn_test.h,
+swin_block.h).
 
 Argument marshalling only: every function here passes tensor pointers and
 sizes to the C ABI of the same name and raises on a non-OK status.  torch is
@@ -46,7 +47,20 @@ _SIGNATURES = {
     "swin_wattn_test_watchdog": ["p", "p"],
     "swin_wattn_forward_noalloc": ["i", "i", "i", "i", "i", "p", "i", "i", "i", "p", "p", "p", "p", "p", "p", "p",
                                    "p"],
+    "swin_block_create": ["pp", "i", "i", "i", "i", "i", "i"],
+    "swin_block_forward": ["p", "p", "i", "i", "i", "p", "p", "p"],
+    "swin_block_sync_status": ["p", "p"],
+    "swin_block_destroy": ["p"],
+    "swin_block_test_layernorm": ["p", "p", "p", "p", "p", "p", "i", "i", "i", "p"],
 }
+
+# swin_block_params (include/swin_block.h), field for field
+BLOCK_PARAM_FIELDS = ("ln1_gamma", "ln1_beta", "Wqkv", "bqkv", "bias_table", "logit_scale", "Wproj", "bproj",
+                      "ln2_gamma", "ln2_beta", "W1", "b1", "W2", "b2")
+
+
+class BlockParams(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in BLOCK_PARAM_FIELDS]
 _CT = {"p": ctypes.c_void_p, "pp": ctypes.POINTER(ctypes.c_void_p), "i": ctypes.c_int, "l": ctypes.c_int64}
 
 
@@ -191,3 +205,34 @@ def swin_wattn_test_gemm(A, Bw, bias, D, swizzle_bytes=128, stream=None):
 
 def swin_wattn_test_watchdog(h, stream=None):
     return _check("swin_wattn_test_watchdog", load().swin_wattn_test_watchdog(h, _stream(stream)))
+
+
+# ---- swin_block.h -------------------------------------------------------------
+
+def swin_block_create(C, heads, M, shift, mode, mlp_ratio=4):
+    h = ctypes.c_void_p()
+    _check("swin_block_create", load().swin_block_create(ctypes.byref(h), C, heads, M, shift, mode, mlp_ratio))
+    return h
+
+
+def swin_block_destroy(h):
+    return _check("swin_block_destroy", load().swin_block_destroy(h))
+
+
+def swin_block_forward(h, x, params, out, stream=None):
+    """params: dict with the swin_block_params fields (tensors or None)."""
+    B, H, W, _ = x.shape
+    bp = BlockParams(*[(_p(params.get(n)).value if params.get(n) is not None else None)
+                       for n in BLOCK_PARAM_FIELDS])
+    return _check("swin_block_forward", load().swin_block_forward(
+        h, _p(x), B, H, W, ctypes.cast(ctypes.byref(bp), ctypes.c_void_p), _p(out), _stream(stream)))
+
+
+def swin_block_sync_status(h, stream=None):
+    return _check("swin_block_sync_status", load().swin_block_sync_status(h, _stream(stream)))
+
+
+def swin_block_test_layernorm(a, b, gamma, beta, out_sum, out_ln, flags, stream=None):
+    rows, C = a.shape[0], a.shape[-1]
+    return _check("swin_block_test_layernorm", load().swin_block_test_layernorm(
+        _p(a), _p(b), _p(gamma), _p(beta), _p(out_sum), _p(out_ln), rows, C, flags, _stream(stream)))

@@ -101,7 +101,11 @@ struct GemmArgs {
     Geom g;          // index maps of LOAD_GATHER / STORE_SCATTER
     int norm_cols;   // > 0: output columns below it are scaled, 32 at a time, to
                      // unit L2 norm (V2 q and k heads); 0: none
+    int epi;         // EPI_NONE, EPI_GELU (GELU after the bias), EPI_RESID (add R after the bias)
+    const bf16 *R;   // EPI_RESID: [rows, ldr] row-major (plain store only)
+    int64_t ldr;
 };
+enum { EPI_NONE = 0, EPI_GELU = 1, EPI_RESID = 2 };
 
 cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, DeviceStatus st,
                         cudaStream_t stream);

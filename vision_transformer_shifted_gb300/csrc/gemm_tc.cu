@@ -59,6 +59,20 @@ __device__ __forceinline__ void store_row_bf16(bf16 *dst, const float *v, const 
     }
 }
 
+// Epilogue of the block's MLP ("Swin Transformer V2" (neura.market), How It
+// Works: the block's sub-layers): e = v + bias, then GELU(e) = e * Phi(e)
+// (exact, through erf) or e + R[row, n] (the residual branch).
+__device__ __forceinline__ void epilogue_op(const GemmArgs &a, int64_t R, int n, const float *v, const float *bias,
+                                            float *e, int cnt)
+{
+    for (int i = 0; i < cnt; ++i) {
+        float t = v[i] + bias[i];
+        if (a.epi == EPI_GELU) t = 0.5f * t * (1.0f + erff(t * 0.7071067811865476f));
+        else if (a.epi == EPI_RESID && R < a.rows) t += __bfloat162float(a.R[R * a.ldr + n + i]);
+        e[i] = t;
+    }
+}
+
 template <int LOAD, int STORE, int BK>
 __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, DeviceStatus st)
 {
@@ -198,14 +212,32 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
                 }
                 if (dst_row) store_row_bf16(dst_row + c0, v, zero, 32);
             } else if (dst_row) {
-                store_row_bf16(dst_row + c0, v, sbias + c0, 32);
+                if (a.epi == EPI_NONE) {
+                    store_row_bf16(dst_row + c0, v, sbias + c0, 32);
+                } else {
+                    float e[32], zero[32];
+                    epilogue_op(a, R, n0 + c0, v, sbias + c0, e, 32);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) zero[i] = 0.f;
+                    store_row_bf16(dst_row + c0, e, zero, 32);
+                }
             }
         }
         if (c0 < BN) { // 16-column tail
             float v[16];
             tmem_ld16(t_lane + c0, v);
             tmem_wait_ld();
-            if (dst_row) store_row_bf16(dst_row + c0, v, sbias + c0, 16);
+            if (dst_row) {
+                if (a.epi == EPI_NONE) {
+                    store_row_bf16(dst_row + c0, v, sbias + c0, 16);
+                } else {
+                    float e[16], zero[16];
+                    epilogue_op(a, R, n0 + c0, v, sbias + c0, e, 16);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) zero[i] = 0.f;
+                    store_row_bf16(dst_row + c0, e, zero, 16);
+                }
+            }
         }
     } else if (tid == 0) {
         atomicOr(st.err, ERR_TIMEOUT);

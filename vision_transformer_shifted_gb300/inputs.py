@@ -14,6 +14,12 @@ shape [(2M-1)^2, heads]; V2: tau = 0.1 per head, meta-network weights
 W1 [512, 2], W2 [heads, 512] ~ N(0, 0.02) and b1 = 0.  Everything is drawn in
 fp32 and rounded once to the workload's dtype; the same rounded values feed
 both sides.
+
+The whole block (``generate_block``, the same generator continued, seed
+2000 + workload index): LayerNorm gains 1 + N(0, 0.1) and shifts N(0, 0.1);
+MLP weights W1 [rC, C] ~ N(0, 1/C), W2 [C, rC] ~ N(0, 1/(rC)) (so that the
+MLP branch is of the same order as the main branch, not a vanishing
+correction) and biases N(0, 0.02).
 """
 from __future__ import annotations
 
@@ -138,3 +144,26 @@ def sample_windows(w: Workload, count: int, seed: int = 7):
     g = torch.Generator().manual_seed(seed)
     rnd = torch.randint(0, w.n_windows, (count,), generator=g).tolist()
     return sorted(set(fixed + rnd))
+
+
+def generate_block(w: Workload, ratio: int = 4, nonzero_bias: bool = True):
+    """Seeded CPU tensors for the whole block of workload ``w`` (bf16): the
+    attention inputs of ``generate`` plus ln1_gamma, ln1_beta, ln2_gamma,
+    ln2_beta [C], mlp_W1 [rC, C], mlp_b1 [rC], mlp_W2 [C, rC], mlp_b2 [C]."""
+    out = generate(w, nonzero_bias=nonzero_bias)
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    dt = torch_dtype(w)
+    C, R = w.C, ratio * w.C
+
+    def normal(shape, std, mean=0.0):
+        return (torch.randn(shape, generator=g, dtype=torch.float32) * std + mean).to(dt)
+
+    out["ln1_gamma"] = normal((C,), 0.1, 1.0)
+    out["ln1_beta"] = normal((C,), 0.1)
+    out["ln2_gamma"] = normal((C,), 0.1, 1.0)
+    out["ln2_beta"] = normal((C,), 0.1)
+    out["mlp_W1"] = normal((R, C), C ** -0.5)
+    out["mlp_b1"] = normal((R,), 0.02)
+    out["mlp_W2"] = normal((C, R), R ** -0.5)
+    out["mlp_b2"] = normal((C,), 0.02)
+    return out
