@@ -24,11 +24,11 @@ namespace {
 constexpr int BM = 128;
 constexpr int THREADS = 128;
 
-template <int BK>
+template <int BK, int NSTAGES = (BK == 64 ? 3 : 4)>
 struct GemmSmem {
     // dynamic layout: [A stages][B stages] (1024-aligned), then row offsets,
     // bias, barriers and the TMEM address.
-    static constexpr int STAGES = BK == 64 ? 3 : 4;
+    static constexpr int STAGES = NSTAGES;
     static constexpr int CPR = BK / 8;          // 16-byte chunks per row
     static constexpr int a_stage = BM * BK * 2;
     static size_t bytes(int BN)
@@ -73,10 +73,10 @@ __device__ __forceinline__ void epilogue_op(const GemmArgs &a, int64_t R, int n,
     }
 }
 
-template <int LOAD, int STORE, int BK>
+template <int LOAD, int STORE, int BK, int NSTAGES>
 __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, DeviceStatus st)
 {
-    using L = GemmSmem<BK>;
+    using L = GemmSmem<BK, NSTAGES>;
     constexpr int STAGES = L::STAGES, CPR = L::CPR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_align(smem_raw, 1024);
@@ -261,18 +261,28 @@ int pick_bn(int N, int step)
     return 0;
 }
 
-template <int LOAD, int STORE, int BK = 64>
-cudaError_t launch_impl(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
+template <int LOAD, int STORE, int BK, int NSTAGES>
+cudaError_t launch_stages(const GemmArgs &a, int BN, DeviceStatus st, cudaStream_t stream)
 {
-    const int BN = pick_bn(a.N, a.norm_cols > 0 ? 32 : 16);
-    if (BN == 0 || a.K % 16 != 0 || a.rows <= 0) return cudaErrorInvalidValue;
-    const size_t smem = GemmSmem<BK>::bytes(BN);
-    auto kern = gemm_tc_kernel<LOAD, STORE, BK>;
+    const size_t smem = GemmSmem<BK, NSTAGES>::bytes(BN);
+    auto kern = gemm_tc_kernel<LOAD, STORE, BK, NSTAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.rows + BM - 1) / BM), (unsigned)(a.N / BN));
     kern<<<grid, THREADS, smem, stream>>>(a, BN, st);
     return cudaGetLastError();
+}
+
+// A K of at most two 64-wide blocks gets a 2-stage ring: the smaller shared
+// footprint lets a third CTA share the SM (its loads and epilogue overlap the
+// others').
+template <int LOAD, int STORE, int BK = 64>
+cudaError_t launch_impl(const GemmArgs &a, DeviceStatus st, cudaStream_t stream)
+{
+    const int BN = pick_bn(a.N, a.norm_cols > 0 ? 32 : 16);
+    if (BN == 0 || a.K % 16 != 0 || a.rows <= 0) return cudaErrorInvalidValue;
+    if (BK == 64 && (a.K + BK - 1) / BK <= 2) return launch_stages<LOAD, STORE, BK, 2>(a, BN, st, stream);
+    return launch_stages<LOAD, STORE, BK, GemmSmem<BK>::STAGES>(a, BN, st, stream);
 }
 
 // Test kernel of the TMEM-A form of the MMA: each thread writes its A row
