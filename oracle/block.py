@@ -21,6 +21,16 @@ x * Phi(x), Phi the standard normal CDF.  The extra LayerNorm that V2
 inserts every six blocks of its largest models is a stage-level detail and
 is not part of one block.
 
+Between stages of the hierarchy ("Boosting Swin Transformer Speed",
+Introduction: a pyramid of stages; "Boost Vision Transformer with
+GPU-Friendly Sparsity and Quantization", Fig. 4: the number of blocks per
+stage) the pages give no formula for the merging step; the reading taken is
+the usual one: each 2 x 2 neighbourhood is concatenated in the order (0,0),
+(1,0), (0,1), (1,1) (row offset first), normalised over its 4C channels and
+mapped to 2C channels by a linear layer without bias.  A stage is ``depth``
+blocks with the shift alternating 0, M/2, 0, ... followed (optionally) by
+that merging.
+
 Pins in ``tests/test_block.py``: LayerNorm statistics and its affine part,
 GELU's odd-part identity and the normal CDF at +-1, +-2 (textbook values),
 the MLP against an explicit sum, and closed forms of the whole block when a
@@ -87,3 +97,32 @@ def block(x, p, *, heads, M, shift, mode, attn_out=None):
     else:
         raise ValueError("mode must be V1 or V2")
     return y, z
+
+
+def merge_concat(x):
+    """[B, H, W, C] -> [B, H/2, W/2, 4C]: the 2 x 2 neighbourhood of output
+    (i, j) in the order (2i, 2j), (2i+1, 2j), (2i, 2j+1), (2i+1, 2j+1)."""
+    x = np.asarray(x, dtype=np.float64)
+    B, H, W, C = x.shape
+    assert H % 2 == 0 and W % 2 == 0
+    out = np.empty((B, H // 2, W // 2, 4 * C))
+    for part, (di, dj) in enumerate(((0, 0), (1, 0), (0, 1), (1, 1))):
+        out[..., part * C:(part + 1) * C] = x[:, di::2, dj::2, :]
+    return out
+
+
+def patch_merge(x, gamma, beta, Wm):
+    """Merging step between stages: LN(merge_concat(x)) Wm^T, Wm [2C, 4C]."""
+    return layer_norm(merge_concat(x), gamma, beta) @ np.asarray(Wm, np.float64).T
+
+
+def stage(x, blocks, *, heads, M, mode, merge=None):
+    """``len(blocks)`` blocks (parameter dicts as ``block`` takes them) with
+    shifts 0, M/2, 0, M/2, ...; then ``patch_merge`` with merge = (gamma, beta,
+    Wm) if given."""
+    y = np.asarray(x, dtype=np.float64)
+    for i, p in enumerate(blocks):
+        y, _ = block(y, p, heads=heads, M=M, shift=0 if i % 2 == 0 else M // 2, mode=mode)
+    if merge is not None:
+        y = patch_merge(y, *merge)
+    return y
