@@ -463,6 +463,74 @@ def run_block(args, w, ratio=4):
     print(json.dumps(line), flush=True)
 
 
+def run_stage(args, w, depth, ratio=4):
+    """A whole stage on workload ``w``'s grid: ``depth`` blocks with shifts
+    0, M/2, 0, ... and the merging step (2x2 -> 2C channels); one JSON line."""
+    from vision_transformer_shifted_gb300 import binding as sw
+    from vision_transformer_shifted_gb300.inputs import generate_block
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sw.load()
+    blocks = []
+    for i in range(depth):
+        wi = w.with_(shift=0 if i % 2 == 0 else w.M // 2, seed=w.seed + 17 * i)
+        g = generate_block(wi, ratio)
+        t = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in g.items()}
+        h_attn = sw.swin_wattn_create(w.C, w.heads, w.M, wi.shift, w.mode)
+        table = table_for(wi, g, dev, h_attn)
+        sw.swin_wattn_destroy(h_attn)
+        params = dict(ln1_gamma=t["ln1_gamma"], ln1_beta=t["ln1_beta"], Wqkv=t["Wqkv"], bqkv=t["bqkv"],
+                      bias_table=table, logit_scale=t.get("tau"), Wproj=t["Wproj"], bproj=t["bproj"],
+                      ln2_gamma=t["ln2_gamma"], ln2_beta=t["ln2_beta"], W1=t["mlp_W1"], b1=t["mlp_b1"],
+                      W2=t["mlp_W2"], b2=t["mlp_b2"])
+        blocks.append((sw.swin_block_create(w.C, w.heads, w.M, wi.shift, w.mode, ratio), params, t["x"]))
+    gm = torch.Generator().manual_seed(w.seed + 555)
+    gam = (1 + 0.1 * torch.randn(4 * w.C, generator=gm)).bfloat16().to(dev)
+    bet = (0.1 * torch.randn(4 * w.C, generator=gm)).bfloat16().to(dev)
+    Wm = (torch.randn(2 * w.C, 4 * w.C, generator=gm) * (4 * w.C) ** -0.5).bfloat16().to(dev)
+    hm = sw.swin_merge_create(w.C)
+    x0 = blocks[0][2]
+    bufs = [torch.empty_like(x0) for _ in range(2)]
+    out = torch.empty(w.B, w.H // 2, w.W // 2, 2 * w.C, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(_):
+        cur = x0
+        for i, (h, params, _x) in enumerate(blocks):
+            sw.swin_block_forward(h, cur, params, bufs[i % 2], stream)
+            cur = bufs[i % 2]
+        sw.swin_merge_forward(hm, cur, gam, bet, Wm, out, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < args.soak:
+            step(0)
+            torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    for h, _p, _x in blocks:
+        assert sw.swin_block_sync_status(h, stream) == sw.OK
+        sw.swin_block_destroy(h)
+    sw.swin_merge_destroy(hm)
+    line = {"metric": "swin stage forward (%d blocks + merging) tokens/s" % depth, "value": w.tokens / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": w.C, "heads": w.heads, "M": w.M,
+                       "depth": depth, "mode": "V1 pre-norm" if w.mode == V1 else "V2 residual post-norm",
+                       "mlp_ratio": ratio, "l2": "not flushed: one input set (the stage's own intermediates, "
+                       "%.0f MB per block, exceed L2)" % (w.tokens * w.C * (3 + ratio) * 2 / 1e6)},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,11 +545,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--block", action="store_true",
                     help="time the whole Swin block (LayerNorm, attention, residuals, MLP) instead")
+    ap.add_argument("--stage", type=int, default=0,
+                    help="time a whole stage of this many blocks (alternating shifts) plus the merging step instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
-    if args.block:
+    if args.stage > 0:
+        if w.dtype != "bf16" or args.impl != "ours" or args.gpus != 1 or (w.H // 2) % 1:
+            ap.error("--stage: bf16 workloads, our implementation, one GPU")
+        run_stage(args, w, args.stage)
+    elif args.block:
         if w.dtype != "bf16" or args.impl != "ours" or args.gpus != 1:
             ap.error("--block: bf16 workloads, our implementation, one GPU")
         run_block(args, w)

@@ -84,6 +84,33 @@ int swin_block_destroy(swin_block_t h);
 int swin_block_test_layernorm(const void *a, const void *b, const void *gamma, const void *beta, void *out_sum,
                               void *out_ln, int rows, int C, int flags, swin_stream_t stream);
 
+/* ---- merging step between stages ----------------------------------------------
+ * Between stages of the hierarchy ("Boosting Swin Transformer Speed",
+ * Introduction: a pyramid of stages) the resolution halves and the channels
+ * double.  Reading (the pages give no formula): each 2 x 2 neighbourhood is
+ * concatenated in the order (0,0), (1,0), (0,1), (1,1) (row offset first),
+ * normalised over its 4C channels (as the block's LayerNorm) and mapped by a
+ * linear layer without bias:
+ *   out[b, i, j, :] = LN(concat(x[b, 2i, 2j], x[b, 2i+1, 2j], x[b, 2i, 2j+1],
+ *                               x[b, 2i+1, 2j+1])) Wm^T
+ * A stage is `depth` blocks with shifts 0, M/2, 0, ... (one swin_block handle
+ * per shift) followed by this step. */
+typedef struct swin_merge_s *swin_merge_t;
+
+/* C input channels (multiple of 8, 4C <= 2048).  The handle owns a workspace
+ * of B*H*W*C bf16 elements (allocated on first use). */
+int swin_merge_create(swin_merge_t *out, int C);
+
+/* x [B, H, W, C] bf16 (H, W even) -> out [B, H/2, W/2, 2C] bf16; gamma, beta
+ * [4C] bf16; Wm [2C, 4C] bf16.  EINVAL for odd H or W, NULL or misaligned
+ * pointers, overlap of x and out; ENOMEM if the workspace cannot be
+ * allocated; ECUDA for launch failures.  B = 0 is a no-op. */
+int swin_merge_forward(swin_merge_t h, const void *x, int B, int H, int W, const void *gamma, const void *beta,
+                       const void *Wm, void *out, swin_stream_t stream);
+
+/* Frees the handle and its workspace (NULL is a no-op). */
+int swin_merge_destroy(swin_merge_t h);
+
 #ifdef __cplusplus
 }
 #endif

@@ -126,6 +126,45 @@ def test_block_attention_branch_placement(mode):
         assert np.allclose(y - z, ob.layer_norm(z + p["b2"], np.ones(C), np.zeros(C)), atol=1e-12)
 
 
+def test_merge_concat_matches_a_reshape_statement():
+    """The 2 x 2 concatenation as a reshape: [B, H/2, 2, W/2, 2, C] with the
+    column offset outer and the row offset inner in the channel dimension."""
+    B, H, W, C = 2, 6, 8, 3
+    x = RNG.normal(size=(B, H, W, C))
+    ref = x.reshape(B, H // 2, 2, W // 2, 2, C).transpose(0, 1, 3, 4, 2, 5).reshape(B, H // 2, W // 2, 4 * C)
+    assert np.array_equal(ob.merge_concat(x), ref)
+    # every input element appears exactly once
+    assert np.allclose(np.sort(ob.merge_concat(x).ravel()), np.sort(x.ravel()))
+
+
+def test_patch_merge_selects_normalised_channels():
+    """With unit gain, zero shift and Wm selecting channels, the output is those
+    channels of the normalised concatenation (mean 0 over the 4C channels)."""
+    B, H, W, C = 1, 4, 4, 8
+    x = RNG.normal(size=(B, H, W, C)) * 2 + 1
+    Wm = np.zeros((2 * C, 4 * C))
+    Wm[np.arange(2 * C), np.arange(2 * C)] = 1.0
+    out = ob.patch_merge(x, np.ones(4 * C), np.zeros(4 * C), Wm)
+    u = ob.merge_concat(x)
+    n = (u - u.mean(-1, keepdims=True)) / np.sqrt(u.var(-1, keepdims=True) + ob.LN_EPS)
+    assert np.allclose(out, n[..., :2 * C], atol=1e-12)
+    assert out.shape == (B, H // 2, W // 2, 2 * C)
+
+
+def test_stage_alternates_shifts_starting_unshifted():
+    B, H, W, C, heads, M = 1, 14, 14, 32, 1, 7
+    x = RNG.normal(size=(B, H, W, C))
+    p0 = _tiny_params(C, heads, M, V1, zero_attention=False)
+    p1 = _tiny_params(C, heads, M, V1, zero_attention=False)
+    y = ob.stage(x, [p0, p1], heads=heads, M=M, mode=V1)
+    y0, _ = ob.block(x, p0, heads=heads, M=M, shift=0, mode=V1)
+    y1, _ = ob.block(y0, p1, heads=heads, M=M, shift=M // 2, mode=V1)
+    assert np.allclose(y, y1, atol=1e-12)
+    y_wrong, _ = ob.block(ob.block(x, p0, heads=heads, M=M, shift=M // 2, mode=V1)[0], p1, heads=heads, M=M, shift=0,
+                          mode=V1)
+    assert not np.allclose(y, y_wrong, atol=1e-6)
+
+
 # ---- C ABI argument checks (CPU) ---------------------------------------------------
 
 
@@ -140,6 +179,17 @@ def test_block_create_rejects_bad_arguments():
     assert lib.swin_block_create(None, 96, 3, 7, 3, sw.V1, 4) == sw.EINVAL
     assert lib.swin_block_forward(None, None, 1, 7, 7, None, None, None) == sw.EINVAL
     assert lib.swin_block_destroy(None) == sw.OK
+
+
+def test_merge_rejects_bad_arguments():
+    lib = sw.load()
+    h = ctypes.c_void_p(123)
+    assert lib.swin_merge_create(ctypes.byref(h), 100) == sw.EINVAL      # C % 8
+    assert h.value is None
+    assert lib.swin_merge_create(ctypes.byref(h), 1024) == sw.EINVAL     # 4C > 2048
+    assert lib.swin_merge_create(None, 96) == sw.EINVAL
+    assert lib.swin_merge_forward(None, None, 1, 8, 8, None, None, None, None, None) == sw.EINVAL
+    assert lib.swin_merge_destroy(None) == sw.OK
 
 
 def test_block_layernorm_hook_rejects_bad_arguments():
@@ -271,3 +321,67 @@ def test_block_forward_full_size_sampled(key):
         z = xs + ob.layer_norm(As, p["ln1_g"], p["ln1_b"])
         ref = z + ob.layer_norm(ob.mlp(z, p["W1"], p["b1"], p["W2"], p["b2"]), p["ln2_g"], p["ln2_b"])
     _block_compare(got.reshape(-1, w.C)[toks], ref)
+
+
+def _merge_inputs(C, seed):
+    g = torch.Generator().manual_seed(seed)
+    gam = (1 + 0.1 * torch.randn(4 * C, generator=g)).bfloat16()
+    bet = (0.1 * torch.randn(4 * C, generator=g)).bfloat16()
+    Wm = (torch.randn(2 * C, 4 * C, generator=g) * (4 * C) ** -0.5).bfloat16()
+    return gam, bet, Wm
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,H,W,C", [(2, 56, 56, 96), (1, 28, 42, 192), (3, 14, 14, 384), (1, 2, 2, 32)])
+def test_merge_forward(B, H, W, C):
+    x = torch.randn(B, H, W, C, generator=torch.Generator().manual_seed(B + H + C)).bfloat16()
+    gam, bet, Wm = _merge_inputs(C, 5 + C)
+    out = torch.empty(B, H // 2, W // 2, 2 * C, dtype=torch.bfloat16, device=DEV)
+    h = sw.swin_merge_create(C)
+    try:
+        sw.swin_merge_forward(h, x.to(DEV), gam.to(DEV), bet.to(DEV), Wm.to(DEV), out)
+        torch.cuda.synchronize()
+    finally:
+        sw.swin_merge_destroy(h)
+    ref = ob.patch_merge(to_f64(x), to_f64(gam), to_f64(bet), to_f64(Wm))
+    _block_compare(to_f64(out.cpu()), ref)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mode", [V1, V2])
+def test_stage_forward(mode):
+    """A stage of depth 2 (unshifted block, shifted block) and the merging step,
+    composed from the C ABI calls, against the oracle's stage."""
+    key = "swin_t_s1" if mode == V1 else "swinv2_t_s1"
+    w0 = WORKLOADS[key].with_(B=1, H=4 * WORKLOADS[key].M, W=2 * WORKLOADS[key].M)
+    p_blocks, dev_blocks = [], []
+    for i in range(2):
+        wi = w0.with_(shift=0 if i == 0 else w0.M // 2, seed=w0.seed + 17 * i)
+        g = generate_block(wi)
+        table = oracle_table(wi, g)
+        p_blocks.append(_oracle_params(g, table))
+        dev_blocks.append((wi, {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v)
+                               for k, v in _block_params_dev(g, table).items()}))
+        if i == 0:
+            x = g["x"]
+    gam, bet, Wm = _merge_inputs(w0.C, 99)
+    cur = x.to(DEV)
+    for wi, params in dev_blocks:
+        nxt = torch.empty_like(cur)
+        h = sw.swin_block_create(wi.C, wi.heads, wi.M, wi.shift, wi.mode, 4)
+        try:
+            sw.swin_block_forward(h, cur, params, nxt)
+            sw.swin_block_sync_status(h)
+        finally:
+            sw.swin_block_destroy(h)
+        cur = nxt
+    out = torch.empty(w0.B, w0.H // 2, w0.W // 2, 2 * w0.C, dtype=torch.bfloat16, device=DEV)
+    hm = sw.swin_merge_create(w0.C)
+    try:
+        sw.swin_merge_forward(hm, cur, gam.to(DEV), bet.to(DEV), Wm.to(DEV), out)
+        torch.cuda.synchronize()
+    finally:
+        sw.swin_merge_destroy(hm)
+    ref = ob.stage(to_f64(x), p_blocks, heads=w0.heads, M=w0.M, mode=w0.mode,
+                   merge=(to_f64(gam), to_f64(bet), to_f64(Wm)))
+    _block_compare(to_f64(out.cpu()), ref)

@@ -52,6 +52,9 @@ _SIGNATURES = {
     "swin_block_sync_status": ["p", "p"],
     "swin_block_destroy": ["p"],
     "swin_block_test_layernorm": ["p", "p", "p", "p", "p", "p", "i", "i", "i", "p"],
+    "swin_merge_create": ["pp", "i"],
+    "swin_merge_forward": ["p", "p", "i", "i", "i", "p", "p", "p", "p", "p"],
+    "swin_merge_destroy": ["p"],
 }
 
 # swin_block_params (include/swin_block.h), field for field
@@ -236,3 +239,19 @@ def swin_block_test_layernorm(a, b, gamma, beta, out_sum, out_ln, flags, stream=
     rows, C = a.shape[0], a.shape[-1]
     return _check("swin_block_test_layernorm", load().swin_block_test_layernorm(
         _p(a), _p(b), _p(gamma), _p(beta), _p(out_sum), _p(out_ln), rows, C, flags, _stream(stream)))
+
+
+def swin_merge_create(C):
+    h = ctypes.c_void_p()
+    _check("swin_merge_create", load().swin_merge_create(ctypes.byref(h), C))
+    return h
+
+
+def swin_merge_destroy(h):
+    return _check("swin_merge_destroy", load().swin_merge_destroy(h))
+
+
+def swin_merge_forward(h, x, gamma, beta, Wm, out, stream=None):
+    B, H, W, _ = x.shape
+    return _check("swin_merge_forward", load().swin_merge_forward(
+        h, _p(x), B, H, W, _p(gamma), _p(beta), _p(Wm), _p(out), _stream(stream)))

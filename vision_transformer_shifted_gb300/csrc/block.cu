@@ -26,10 +26,14 @@ constexpr float LN_EPS = 1e-5f;
 //   flags 0: out_ln = LN(a)
 //   flags 1: s = a + b (fp32, then bf16); out_sum = s; out_ln = LN(s)
 //   flags 2: out_ln = b + LN(a)
+// With mH > 0, row r of `a` is not stored: it is the 2 x 2 neighbourhood
+// concatenation of a [B, mH, mW, C/4] image (merging step between stages):
+// row r = (b, i, j) of the half-resolution grid, channel part q (of four)
+// from pixel (2i + (q & 1), 2j + (q >> 1)).
 template <int CPL>   // 16-byte chunks per lane
 __global__ void __launch_bounds__(256) layernorm_kernel(const bf16 *a, const bf16 *b, const bf16 *gamma,
                                                         const bf16 *beta, bf16 *out_sum, bf16 *out_ln, int64_t rows,
-                                                        int C, int lpr, int flags)
+                                                        int C, int lpr, int flags, int mH, int mW)
 {
     const int lane = threadIdx.x & 31;
     const int sub = lane / lpr, li = lane % lpr;
@@ -45,7 +49,17 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const bf16 *a, const bf1
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[k][e] = 0.f;
         if (ok) {
-            const uint4 ua = *reinterpret_cast<const uint4 *>(a + row * C + c * 8);
+            const bf16 *src = a + row * C + c * 8;
+            if (mH > 0) {
+                const int Cs = C / 4, cps = Cs / 8;   // source channels, 16-byte chunks per source pixel
+                const int q = c / cps, cc = c - q * cps;
+                const int Wh = mW / 2, Hh = mH / 2;
+                const int64_t bi = row / ((int64_t)Hh * Wh);
+                const int rem = (int)(row - bi * Hh * Wh);
+                const int i = rem / Wh, j = rem - (rem / Wh) * Wh;
+                src = a + ((bi * mH + 2 * i + (q & 1)) * (int64_t)mW + 2 * j + (q >> 1)) * Cs + cc * 8;
+            }
+            const uint4 ua = *reinterpret_cast<const uint4 *>(src);
             const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -120,7 +134,7 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const bf16 *a, const bf1
 }
 
 cudaError_t launch_layernorm(const bf16 *a, const bf16 *b, const bf16 *gamma, const bf16 *beta, bf16 *out_sum,
-                             bf16 *out_ln, int64_t rows, int C, int flags, cudaStream_t stream)
+                             bf16 *out_ln, int64_t rows, int C, int flags, cudaStream_t stream, int mH = 0, int mW = 0)
 {
     const int chunks = C / 8;
     int lpr = 1;
@@ -131,7 +145,7 @@ cudaError_t launch_layernorm(const bf16 *a, const bf16 *b, const bf16 *gamma, co
     if (grid == 0) return cudaSuccess;
 #define SWIN_LN_CASE(n)                                                                                       \
     case n:                                                                                                   \
-        layernorm_kernel<n><<<grid, 256, 0, stream>>>(a, b, gamma, beta, out_sum, out_ln, rows, C, lpr, flags); \
+        layernorm_kernel<n><<<grid, 256, 0, stream>>>(a, b, gamma, beta, out_sum, out_ln, rows, C, lpr, flags, mH, mW); \
         break;
     switch (cpl) {
         SWIN_LN_CASE(1)
@@ -311,6 +325,91 @@ int swin_block_test_layernorm(const void *a, const void *b, const void *gamma, c
     if (rows == 0) return SWIN_WATTN_OK;
     return cuda_status(launch_layernorm((const bf16 *)a, (const bf16 *)b, (const bf16 *)gamma, (const bf16 *)beta,
                                         (bf16 *)out_sum, (bf16 *)out_ln, rows, C, flags, (cudaStream_t)stream));
+}
+
+// ---- merging step between stages ------------------------------------------------
+
+} // extern "C"
+
+struct swin_merge_s {
+    int C;
+    int *d_err;
+    void *ws;   // the normalised 4C-channel rows, bf16
+    size_t ws_bytes;
+};
+
+extern "C" {
+
+int swin_merge_create(swin_merge_t *out, int C)
+{
+    if (!out) return SWIN_WATTN_EINVAL;
+    *out = nullptr;
+    if (C <= 0 || C % 8 || 4 * C > 2048) return SWIN_WATTN_EINVAL;
+    swin_merge_s *h = new (std::nothrow) swin_merge_s{};
+    if (!h) return SWIN_WATTN_ENOMEM;
+    h->C = C;
+    if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess || cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return SWIN_WATTN_ENOMEM;
+    }
+    *out = h;
+    return SWIN_WATTN_OK;
+}
+
+int swin_merge_destroy(swin_merge_t h)
+{
+    if (!h) return SWIN_WATTN_OK;
+    if (h->ws) cudaFree(h->ws);
+    if (h->d_err) cudaFree(h->d_err);
+    delete h;
+    return SWIN_WATTN_OK;
+}
+
+int swin_merge_forward(swin_merge_t h, const void *x, int B, int H, int W, const void *gamma, const void *beta,
+                       const void *Wm, void *out, swin_stream_t stream)
+{
+    if (!h || !x || !gamma || !beta || !Wm || !out) return SWIN_WATTN_EINVAL;
+    if (B < 0 || H <= 0 || W <= 0 || H % 2 || W % 2) return SWIN_WATTN_EINVAL;
+    const void *ps[] = {x, gamma, beta, Wm, out};
+    for (const void *q : ps)
+        if (!aligned16(q)) return SWIN_WATTN_EINVAL;
+    const int C = h->C;
+    const int64_t rows = (int64_t)B * (H / 2) * (W / 2);
+    if (rows * 4 * C > ((int64_t)1 << 40)) return SWIN_WATTN_EINVAL;
+    {
+        const char *xb = (const char *)x, *ob = (const char *)out;
+        const int64_t xbytes = rows * 4 * C * 2, obytes = rows * 2 * C * 2;
+        if (xb < ob + obytes && ob < xb + xbytes) return SWIN_WATTN_EINVAL;
+    }
+    if (B == 0) return SWIN_WATTN_OK;
+    const size_t need = (size_t)rows * 4 * C * 2;
+    if (h->ws_bytes < need) {
+        if (h->ws) cudaFree(h->ws);
+        h->ws = nullptr;
+        h->ws_bytes = 0;
+        if (cudaMalloc(&h->ws, need) != cudaSuccess) {
+            cudaGetLastError();
+            return SWIN_WATTN_ENOMEM;
+        }
+        h->ws_bytes = need;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    bf16 *u = (bf16 *)h->ws;
+    cudaError_t e = launch_layernorm((const bf16 *)x, nullptr, (const bf16 *)gamma, (const bf16 *)beta, nullptr, u,
+                                     rows, 4 * C, 0, s, H, W);
+    if (e != cudaSuccess) return cuda_status(e);
+    GemmArgs a{};
+    a.A = u;
+    a.lda = 4 * C;
+    a.Bw = (const bf16 *)Wm;
+    a.D = (bf16 *)out;
+    a.ldd = 2 * C;
+    a.rows = rows;
+    a.N = 2 * C;
+    a.K = 4 * C;
+    a.g = make_geom(1, 1, 1, 2 * C, 1, 0);
+    return cuda_status(launch_gemm(a, LOAD_PLAIN, STORE_PLAIN, DeviceStatus{h->d_err, 2000000000ull}, s));
 }
 
 } // extern "C"
