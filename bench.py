@@ -530,6 +530,70 @@ def run_stage(args, w, depth, ratio=4):
             "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
+def run_backward(args, w):
+    """Gradients of the V1 attention block (recompute of q, k, v and o, then
+    the backward) on workload ``w``; one JSON line, not the headline."""
+    from vision_transformer_shifted_gb300 import binding as sw
+    from vision_transformer_shifted_gb300.inputs import generate
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sw.load()
+    pk = peaks()
+    g = generate(w, nonzero_bias=True)
+    t = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in g.items()}
+    T, C, N, L = w.tokens, w.C, w.N, 2 * w.M - 1
+    h = sw.swin_wattn_create(C, w.heads, w.M, w.shift, sw.V1)
+    io_bytes = T * C * 2 * 3
+    nsets = max(2, -(-(2 * L2_BYTES) // io_bytes) + 1)
+    gen = torch.Generator(device=dev).manual_seed(9)
+    xs = [t["x"]] + [torch.randn(t["x"].shape, generator=gen, device=dev).bfloat16() for _ in range(nsets - 1)]
+    dys = [torch.randn(t["x"].shape, generator=gen, device=dev).bfloat16() for _ in range(nsets)]
+    dxs = [torch.empty_like(t["x"]) for _ in range(nsets)]
+    f32 = dict(device=dev, dtype=torch.float32)
+    grads = [torch.empty(3 * C, C, **f32), torch.empty(3 * C, **f32), torch.empty(L * L, w.heads, **f32),
+             torch.empty(C, C, **f32), torch.empty(C, **f32)]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        k = i % nsets
+        sw.swin_wattn_backward(h, xs[k], t["Wqkv"], t["bqkv"], t["table"], t["Wproj"], t["bproj"], dys[k], dxs[k],
+                               *grads, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    assert sw.swin_wattn_sync_status(h, stream) == sw.OK
+    with ClockSampler(dev.index) as clk:
+        t_soak = time.perf_counter()
+        i = 0
+        while time.perf_counter() - t_soak < args.soak:
+            step(i)
+            i += 1
+            if i % 16 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    assert sw.swin_wattn_sync_status(h, stream) == sw.OK
+    launches = sw.swin_wattn_backward_launches(h)
+    sw.swin_wattn_destroy(h)
+    # recompute: QKV GEMM 6TC^2, logits and P.V 4TNC; backward: do and dWproj
+    # 4TC^2, attention (S again, dP, dq, dk, dv) 10TNC, dx and dWqkv 12TC^2
+    flops = 22 * T * C * C + 14 * T * N * C
+    line = {"metric": "swin window-attention backward (V1, with recompute) tokens/s", "value": T / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": C, "heads": w.heads, "M": w.M,
+                       "shift": w.shift, "l2": "%d input sets of x and dy (%.0f MB each) in rotation" % (
+                           nsets, io_bytes / 1e6)},
+            "tflops": flops / (ms * 1e-3) / 1e12, "algorithmic_flops": flops, "gpu_launches": launches * args.steps,
+            "peak_source": pk["source"], "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -547,6 +611,8 @@ def main():
                     help="time the whole Swin block (LayerNorm, attention, residuals, MLP) instead")
     ap.add_argument("--stage", type=int, default=0,
                     help="time a whole stage of this many blocks (alternating shifts) plus the merging step instead")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the gradients of the V1 attention block (with recompute) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -555,6 +621,10 @@ def main():
         if w.dtype != "bf16" or args.impl != "ours" or args.gpus != 1 or (w.H // 2) % 1:
             ap.error("--stage: bf16 workloads, our implementation, one GPU")
         run_stage(args, w, args.stage)
+    elif args.backward:
+        if w.dtype != "bf16" or w.mode != V1 or args.impl != "ours" or args.gpus != 1:
+            ap.error("--backward: bf16 V1 workloads, our implementation, one GPU")
+        run_backward(args, w)
     elif args.block:
         if w.dtype != "bf16" or args.impl != "ours" or args.gpus != 1:
             ap.error("--block: bf16 workloads, our implementation, one GPU")

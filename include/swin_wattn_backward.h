@@ -1,0 +1,63 @@
+/*
+ * swin_wattn_backward -- gradients of the shifted-window attention block
+ * (V1 logits) on one GB300, behind a plain C ABI.
+ *
+ * Page "Boosting Swin Transformer Speed: Profiling, Mixed Precision, and
+ * Kernel Fusion Secrets", Training Optimization: training runs the block's
+ * backward pass through the fused attention kernel and through the
+ * index-mapping kernels of window partition, cyclic shift and reverse.  The
+ * pages give no formula for the gradients; they are those of the forward of
+ * swin_wattn.h (V1), by the chain rule:
+ *   dy_w = gather(dy)                 (window order: cyclic shift -s, partition)
+ *   dWproj = dy_w^T o, dbproj = sum_t dy_w, do = dy_w Wproj
+ *   per window and head:  dP = do v^T, D_i = sum_j P_ij dP_ij,
+ *     dS = P (dP - D), dq = dS k / sqrt(d), dk = dS^T q / sqrt(d), dv = P^T do,
+ *     dtable[idx(i, j), head] += dS_ij  (masked pairs have P = 0, so dS = 0)
+ *   dWqkv = dqkv^T xs, dbqkv = sum_t dqkv, dx = scatter(dqkv Wqkv)
+ * (o, P, q, k, v as in the forward; xs = gather(x); scatter = window
+ * reverse then roll by +s, the inverse map of gather).
+ *
+ * The call recomputes q, k, v and o from x (nothing of the forward is kept),
+ * then runs: two gathers, the QKV GEMM and the window attention of the
+ * forward, the do GEMM, the per-window attention backward, the dx GEMM with
+ * the scatter in its epilogue, two weight-gradient GEMMs (cuBLAS: plain
+ * long-K reductions over all tokens) and two column sums.
+ *
+ * Conventions of swin_wattn.h: device pointers, asynchronous on `stream`,
+ * caller-owned tensors, status codes SWIN_WATTN_*, no CPU fallback.
+ */
+#ifndef SWIN_WATTN_BACKWARD_H
+#define SWIN_WATTN_BACKWARD_H
+
+#include "swin_wattn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Gradients of sum(out * dy), out = the handle's block applied to x.
+ * Inputs (bf16, as swin_wattn_forward): x [B, H, W, C], Wqkv [3C, C],
+ * bqkv [3C] (NULL = zero), bias_table [(2M-1)^2, heads], Wproj [C, C],
+ * bproj [C] (NULL = zero; does not enter any gradient), dy [B, H, W, C].
+ * Outputs, overwritten: dx [B, H, W, C] bf16; dWqkv [3C, C], dbqkv [3C],
+ * dtable [(2M-1)^2, heads], dWproj [C, C], dbproj [C], all fp32.
+ * Every pointer 16-byte aligned; dx overlaps neither x nor dy.
+ * Errors: EINVAL for NULL or misaligned pointers, bad shapes, overlap;
+ * EUNSUPPORTED for a V2 or fp32 handle, windows of more than 64 tokens, or
+ * B*H*W >= 2^31; ENOMEM if the workspace (10 * B*H*W*C bf16 elements plus
+ * 4C^2) cannot be allocated; ECUDA for launch or cuBLAS failures.  B = 0
+ * zeroes the parameter gradients and returns. */
+int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
+                        const void *bias_table, const void *Wproj, const void *bproj, const void *dy, void *dx,
+                        float *dWqkv, float *dbqkv, float *dtable, float *dWproj, float *dbproj,
+                        swin_stream_t stream);
+
+/* Number of kernels (own and cuBLAS calls counted as one each) the last
+ * successful swin_wattn_backward enqueued. */
+int swin_wattn_backward_launches(swin_wattn_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIN_WATTN_BACKWARD_H */

@@ -1,8 +1,14 @@
 """Backward pass of the shifted-window attention block (V1).
 
 CPU (not gpu): the float64 torch restatement against the pinned forward
-oracle, finite differences, and two identities of the gradients.
+oracle, finite differences, and identities of the gradients.
+GPU: swin_wattn_backward through the C ABI against that oracle, every
+gradient entry, on small grids (ragged tiles, shift 0, 4 and 16 heads, full
+64-token windows, 4-token windows) and on the whole 64 x 56 x 56 x 96 batch;
+the empty batch and the refused shapes.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -56,3 +62,155 @@ def test_gradient_identities(s):
     assert np.allclose(g["dtable"].sum(axis=0), 0.0, atol=1e-9)
     assert np.allclose(g["dbproj"], dy.reshape(-1, C).sum(axis=0), atol=1e-9)
     assert g["dx"].shape == x.shape and g["dWqkv"].shape == (3 * C, C)
+
+
+def test_key_bias_gradient_is_zero():
+    """A key bias adds q_i . b_k to every logit of row i alike, which softmax
+    ignores: its gradient vanishes, while the query and value biases' do not."""
+    B, H, W, C, heads, M, s = 1, 14, 14, 32, 2, 7, 3
+    x = RNG.normal(size=(B, H, W, C))
+    dy = RNG.normal(size=(B, H, W, C))
+    g = obw.gradients(x, **_params(C, heads, M), dy=dy, heads=heads, M=M, shift=s)
+    db = g["dbqkv"]
+    assert np.abs(db[C:2 * C]).max() < 1e-9 * np.abs(db).max()
+    assert np.abs(db[:C]).max() > 1e-3 and np.abs(db[2 * C:]).max() > 1e-3
+
+
+# ---- GPU: swin_wattn_backward against the oracle --------------------------------
+
+def _rel_errors(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape and np.isfinite(got).all()
+    err = np.abs(got - ref)
+    return dict(rel_l2=float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)),
+                max_rel=float(err.max() / max(np.abs(ref).max(), 1e-30)))
+
+
+# Bound of each gradient against the float64 oracle.  Every path from the
+# inputs to a gradient crosses at most four bf16 roundings of intermediates
+# (qkv, o or do, dqkv, dx), each within 2^-9 relative; fp32 sums add far
+# less.  Normwise that is below 4 * 2^-9 ~ 0.8%, bounded here by 1e-2; the
+# largest entry error is bounded by 1.5e-2 of the largest entry.
+GRAD_REL_L2, GRAD_MAX_REL = 1e-2, 1.5e-2
+
+
+def _run_backward(w, dy_seed=5, windows_check=None):
+    import torch as _t
+    from vision_transformer_shifted_gb300 import binding as sw
+    from vision_transformer_shifted_gb300.inputs import generate
+    g = generate(w, nonzero_bias=True)
+    dy = _t.randn(g["x"].shape, generator=_t.Generator().manual_seed(dy_seed)).bfloat16()
+    dev = {k: v.cuda() for k, v in g.items() if isinstance(v, _t.Tensor)}
+    dyd = dy.cuda()
+    C, L = w.C, 2 * w.M - 1
+    out = dict(dx=_t.full_like(dev["x"], float("nan")),
+               dWqkv=_t.full((3 * C, C), float("nan"), device="cuda"),
+               dbqkv=_t.full((3 * C,), float("nan"), device="cuda"),
+               dtable=_t.full((L * L, w.heads), float("nan"), device="cuda"),
+               dWproj=_t.full((C, C), float("nan"), device="cuda"),
+               dbproj=_t.full((C,), float("nan"), device="cuda"))
+    h = sw.swin_wattn_create(C, w.heads, w.M, w.shift, sw.V1)
+    try:
+        sw.swin_wattn_backward(h, dev["x"], dev["Wqkv"], dev["bqkv"], dev["table"], dev["Wproj"], dev["bproj"], dyd,
+                               out["dx"], out["dWqkv"], out["dbqkv"], out["dtable"], out["dWproj"], out["dbproj"])
+        assert sw.swin_wattn_sync_status(h) == sw.OK
+        launches = sw.swin_wattn_backward_launches(h)
+    finally:
+        sw.swin_wattn_destroy(h)
+    f = {k: v.double().numpy() for k, v in g.items() if isinstance(v, _t.Tensor)}
+    ref = obw.gradients(f["x"], f["Wqkv"], f["bqkv"], f["table"], f["Wproj"], f["bproj"], dy.double().numpy(),
+                        heads=w.heads, M=w.M, shift=w.shift)
+    got = {k: v.double().cpu().numpy() for k, v in out.items()}
+    return got, ref, launches
+
+
+def _check_all(got, ref):
+    stats = {k: _rel_errors(got[k], ref[k]) for k in ref}
+    print("backward parity", stats)
+    for k, s in stats.items():
+        assert s["rel_l2"] <= GRAD_REL_L2 and s["max_rel"] <= GRAD_MAX_REL, (k, s)
+    return stats
+
+
+def _workload(key, **kw):
+    from vision_transformer_shifted_gb300.inputs import WORKLOADS
+    return WORKLOADS[key].with_(**kw)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("key,kw", [
+    ("swin_t_s1", dict(B=2, H=14, W=21)),             # 588 tokens: several 128-row tiles and a ragged tail
+    ("swin_t_s1", dict(B=2, H=14, W=21, shift=0)),    # the unshifted block of a pair
+    ("swin_b_s1", dict(B=1, H=21, W=14)),             # 4 heads
+    ("swin_b_s3", dict(B=2)),                         # 16 heads, 3C = 1536
+    ("swinv2_t_s1", dict(B=1, H=16, W=24, mode=0)),   # 8 x 8 windows (64 tokens, no padding), shift 4
+    ("tiny", dict(B=3, H=4, W=6, M=2, shift=1, dtype="bf16")),  # 4-token windows, 2 x 3 of them per image
+])
+def test_backward_parity_small(key, kw):
+    import torch as _t
+    if not _t.cuda.is_available():
+        pytest.skip("no GPU")
+    w = _workload(key, **kw)
+    got, ref, launches = _run_backward(w)
+    _check_all(got, ref)
+    assert launches == 13
+
+
+@pytest.mark.gpu
+def test_backward_parity_full_size_swin_t_s1():
+    """The whole 64 x 56 x 56 x 96 batch, every gradient entry (the float64
+    oracle takes a few seconds for it)."""
+    import torch as _t
+    if not _t.cuda.is_available():
+        pytest.skip("no GPU")
+    got, ref, _ = _run_backward(_workload("swin_t_s1"))
+    _check_all(got, ref)
+    # the key-bias gradient vanishes (softmax ignores a per-row constant)
+    assert np.abs(got["dbqkv"][96:192]).max() < 1e-3 * np.abs(ref["dbqkv"]).max()
+
+
+@pytest.mark.gpu
+def test_backward_empty_batch_and_refusals():
+    import torch as _t
+    if not _t.cuda.is_available():
+        pytest.skip("no GPU")
+    from vision_transformer_shifted_gb300 import binding as sw
+    C, heads, M = 96, 3, 7
+    L = 2 * M - 1
+    z = lambda *s: _t.full(s, 7.0, device="cuda")
+    Wqkv = _t.zeros(3 * C, C, dtype=_t.bfloat16, device="cuda")
+    Wp = _t.zeros(C, C, dtype=_t.bfloat16, device="cuda")
+    tab = _t.zeros(L * L, heads, dtype=_t.bfloat16, device="cuda")
+    outs = [z(3 * C, C), z(3 * C), z(L * L, heads), z(C, C), z(C)]
+    h = sw.swin_wattn_create(C, heads, M, 3, sw.V1)
+    try:
+        # B = 0: the activation pointers are never read (empty tensors have no
+        # storage, so valid dummies stand in)
+        xd, dxd = _t.zeros(16, dtype=_t.bfloat16, device="cuda"), _t.zeros(16, dtype=_t.bfloat16, device="cuda")
+        P = lambda t: ctypes.c_void_p(t.data_ptr())
+        rc = sw.load().swin_wattn_backward(h, P(xd), 0, 14, 14, P(Wqkv), None, P(tab), P(Wp), None, P(xd), P(dxd),
+                                           *[P(o) for o in outs], None)
+        assert rc == sw.OK
+        _t.cuda.synchronize()
+        assert all(float(o.abs().max()) == 0.0 for o in outs)
+        assert float(dxd.abs().max()) == 0.0
+    finally:
+        sw.swin_wattn_destroy(h)
+    x1 = _t.zeros(1, 14, 14, C, dtype=_t.bfloat16, device="cuda")
+    for args in ((C, heads, M, 3, sw.V2), (C, heads, 14, 3, sw.V1)):
+        h = sw.swin_wattn_create(*args)
+        try:
+            tabh = _t.zeros((2 * args[2] - 1) ** 2, heads, dtype=_t.bfloat16, device="cuda")
+            with pytest.raises(sw.SwinWAttnError) as ei:
+                sw.swin_wattn_backward(h, x1, Wqkv, None, tabh, Wp, None, x1, _t.empty_like(x1), *outs)
+            assert ei.value.code == sw.EUNSUPPORTED
+        finally:
+            sw.swin_wattn_destroy(h)
+    h = sw.swin_wattn_create(C, heads, M, 3, sw.V1)
+    try:
+        with pytest.raises(sw.SwinWAttnError) as ei:   # dx aliases x
+            sw.swin_wattn_backward(h, x1, Wqkv, None, tab, Wp, None, x1, x1, *outs)
+        assert ei.value.code == sw.EINVAL
+    finally:
+        sw.swin_wattn_destroy(h)

@@ -1,5 +1,5 @@
 """ctypes binding of libswin_wattn (include/swin_wattn.h, swin_wattn_test.h,
-swin_block.h).
+swin_block.h, swin_wattn_backward.h).
 
 Argument marshalling only: every function here passes tensor pointers and
 sizes to the C ABI of the same name and raises on a non-OK status.  torch is
@@ -55,6 +55,9 @@ _SIGNATURES = {
     "swin_merge_create": ["pp", "i"],
     "swin_merge_forward": ["p", "p", "i", "i", "i", "p", "p", "p", "p", "p"],
     "swin_merge_destroy": ["p"],
+    "swin_wattn_backward": ["p", "p", "i", "i", "i", "p", "p", "p", "p", "p", "p", "p", "p", "p", "p", "p", "p",
+                            "p"],
+    "swin_wattn_backward_launches": ["p"],
 }
 
 # swin_block_params (include/swin_block.h), field for field
@@ -140,6 +143,18 @@ def swin_wattn_forward(h, x, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, 
     if rc == ECUDA:
         raise SwinWAttnError("swin_wattn_forward (%s)" % swin_wattn_last_cuda_error(h), rc)
     return _check("swin_wattn_forward", rc)
+
+
+def swin_wattn_backward(h, x, Wqkv, bqkv, bias_table, Wproj, bproj, dy, dx, dWqkv, dbqkv, dtable, dWproj, dbproj,
+                        stream=None):
+    B, H, W, _ = x.shape
+    return _check("swin_wattn_backward", load().swin_wattn_backward(
+        h, _p(x), B, H, W, _p(Wqkv), _p(bqkv), _p(bias_table), _p(Wproj), _p(bproj), _p(dy), _p(dx), _p(dWqkv),
+        _p(dbqkv), _p(dtable), _p(dWproj), _p(dbproj), _stream(stream)))
+
+
+def swin_wattn_backward_launches(h):
+    return load().swin_wattn_backward_launches(h)
 
 
 def swin_wattn_last_cuda_error(h):

@@ -3,7 +3,10 @@
 #include <cstring>
 #include <new>
 
+#include <cublas_v2.h>
+
 #include "swin_wattn.h"
+#include "swin_wattn_backward.h"
 #include "swin_wattn_test.h"
 #include "common.cuh"
 
@@ -22,6 +25,10 @@ struct swin_wattn_s {
     size_t stage_bytes;
     int last_launches;
     cudaError_t last_cuda_error;
+    void *bws;         // backward workspace (see swin_wattn_backward)
+    size_t bws_bytes;
+    cublasHandle_t blas;
+    int bw_launches;
 };
 
 namespace {
@@ -147,6 +154,30 @@ int check_forward_args(const swin_wattn_s *h, const void *x, int B, int H, int W
 
 } // namespace
 
+
+// ---- backward (V1) ------------------------------------------------------------
+
+namespace {
+
+bool overlaps(const void *a, const void *b, size_t bytes)
+{
+    const char *pa = (const char *)a, *pb = (const char *)b;
+    return bytes && pa < pb + bytes && pb < pa + bytes;
+}
+
+// D [n_out, n_in] (row-major fp32) = sum over T rows of G[t, :]^T X[t, :]
+// for bf16 row-major G [T, n_out] and X [T, n_in]: in cuBLAS's column-major
+// view D^T = X^T-view . G-view^T with k = T.
+cublasStatus_t weight_grad(cublasHandle_t blas, const bf16 *G, int n_out, const bf16 *X, int n_in, int64_t T,
+                           float *D)
+{
+    const float one = 1.f, zero = 0.f;
+    return cublasGemmEx(blas, CUBLAS_OP_N, CUBLAS_OP_T, n_in, n_out, (int)T, &one, X, CUDA_R_16BF, n_in, G,
+                        CUDA_R_16BF, n_out, &zero, D, CUDA_R_32F, n_in, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+}
+
+} // namespace
+
 extern "C" {
 
 int swin_wattn_create(swin_wattn_t *out, int C, int heads, int M, int shift, int mode)
@@ -181,6 +212,8 @@ int swin_wattn_destroy(swin_wattn_t h)
     if (h->ws) cudaFree(h->ws);
     if (h->stage_x) cudaFree(h->stage_x);
     if (h->stage_out) cudaFree(h->stage_out);
+    if (h->bws) cudaFree(h->bws);
+    if (h->blas) cublasDestroy(h->blas);
     if (h->d_err) cudaFree(h->d_err);
     delete h;
     return SWIN_WATTN_OK;
@@ -289,6 +322,90 @@ const char *swin_wattn_strerror(int code)
     default: return "unknown status";
     }
 }
+
+int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
+                        const void *bias_table, const void *Wproj, const void *bproj, const void *dy, void *dx,
+                        float *dWqkv, float *dbqkv, float *dtable, float *dWproj, float *dbproj,
+                        swin_stream_t stream)
+{
+    (void)bproj;
+    if (!h || !x || !Wqkv || !bias_table || !Wproj || !dy || !dx || !dWqkv || !dbqkv || !dtable || !dWproj ||
+        !dbproj)
+        return SWIN_WATTN_EINVAL;
+    int rc = check_grid(h, B, H, W);
+    if (rc) return rc;
+    const void *ptrs[] = {x, Wqkv, bqkv, bias_table, Wproj, bproj, dy, dx, dWqkv, dbqkv, dtable, dWproj, dbproj};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return SWIN_WATTN_EINVAL;
+    const int C = h->C, L = 2 * h->M - 1;
+    const size_t act = (size_t)B * H * W * C * 2;
+    if (overlaps(dx, x, act) || overlaps(dx, dy, act)) return SWIN_WATTN_EINVAL;
+    if (h->fp32 || h->mode != SWIN_WATTN_V1 || !attn_backward_supported(h->M, C, h->heads))
+        return SWIN_WATTN_EUNSUPPORTED;
+    const Geom g = make_geom(B, H, W, C, h->M, h->shift);
+    if (g.T >= ((int64_t)1 << 31)) return SWIN_WATTN_EUNSUPPORTED;
+    cudaStream_t s = (cudaStream_t)stream;
+    h->bw_launches = 0;
+    cudaError_t e = cudaSuccess;
+    auto zero = [&](float *p, size_t n) {
+        if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, n * sizeof(float), s);
+    };
+    zero(dtable, (size_t)L * L * h->heads);
+    zero(dbqkv, (size_t)3 * C);
+    zero(dbproj, (size_t)C);
+    if (B == 0) {
+        zero(dWqkv, (size_t)3 * C * C);
+        zero(dWproj, (size_t)C * C);
+        return cuda_status(e);
+    }
+    if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
+    // workspace (bf16): xs, dyw, attn, do [T, C]; qkv, dqkv [T, 3C]; WprojT [C, C]; WqkvT [C, 3C]
+    const size_t tc = (size_t)g.T * C;
+    rc = ensure_buffer(&h->bws, &h->bws_bytes, (10 * tc + 4 * (size_t)C * C) * 2);
+    if (rc) return rc;
+    if (!h->blas) {
+        if (cublasCreate(&h->blas) != CUBLAS_STATUS_SUCCESS) { h->blas = nullptr; return SWIN_WATTN_ECUDA; }
+    }
+    if (cublasSetStream(h->blas, s) != CUBLAS_STATUS_SUCCESS) return SWIN_WATTN_ECUDA;
+    bf16 *xs = (bf16 *)h->bws, *dyw = xs + tc, *attn = dyw + tc, *dO = attn + tc, *qkv = dO + tc;
+    bf16 *dqkv = qkv + 3 * tc, *WpT = dqkv + 3 * tc, *WqkvT = WpT + (size_t)C * C;
+    int launches = 0;
+    auto step = [&](cudaError_t r) {
+        if (e == cudaSuccess) { e = r; ++launches; }
+    };
+    step(launch_gather_rows((const bf16 *)x, xs, g, C, s));
+    step(launch_gather_rows((const bf16 *)dy, dyw, g, C, s));
+    step(launch_transpose((const bf16 *)Wproj, WpT, C, C, s));
+    step(launch_transpose((const bf16 *)Wqkv, WqkvT, 3 * C, C, s));
+    // forward intermediates: qkv = xs Wqkv^T + bqkv, o = attention(qkv)
+    GemmArgs k1{};
+    k1.A = xs; k1.lda = C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
+    k1.D = qkv; k1.ldd = 3 * C; k1.rows = g.T; k1.N = 3 * C; k1.K = C; k1.g = g;
+    step(launch_gemm(k1, LOAD_PLAIN, STORE_PLAIN, dstatus(h), s));
+    AttnArgs k2{};
+    k2.qkv = qkv; k2.attn = attn; k2.table = (const bf16 *)bias_table; k2.tau = nullptr; k2.heads = h->heads;
+    k2.mode = SWIN_WATTN_V1; k2.g = g;
+    step(launch_attention(k2, dstatus(h), s));
+    // do = dy_w Wproj
+    GemmArgs k3{};
+    k3.A = dyw; k3.lda = C; k3.Bw = WpT; k3.D = dO; k3.ldd = C; k3.rows = g.T; k3.N = C; k3.K = C; k3.g = g;
+    step(launch_gemm(k3, LOAD_PLAIN, STORE_PLAIN, dstatus(h), s));
+    step(launch_attn_backward(qkv, dO, (const bf16 *)bias_table, h->heads, g, dqkv, dtable, s));
+    // dx = scatter(dqkv Wqkv)
+    GemmArgs k4{};
+    k4.A = dqkv; k4.lda = 3 * C; k4.Bw = WqkvT; k4.D = (bf16 *)dx; k4.ldd = C; k4.rows = g.T; k4.N = C;
+    k4.K = 3 * C; k4.g = g;
+    step(launch_gemm(k4, LOAD_PLAIN, STORE_SCATTER, dstatus(h), s));
+    step(launch_colsum(dyw, g.T, C, dbproj, s));
+    step(launch_colsum(dqkv, g.T, 3 * C, dbqkv, s));
+    if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
+    if (weight_grad(h->blas, dyw, C, attn, C, g.T, dWproj) != CUBLAS_STATUS_SUCCESS) return SWIN_WATTN_ECUDA;
+    if (weight_grad(h->blas, dqkv, 3 * C, xs, C, g.T, dWqkv) != CUBLAS_STATUS_SUCCESS) return SWIN_WATTN_ECUDA;
+    h->bw_launches = launches + 2;
+    return SWIN_WATTN_OK;
+}
+
+int swin_wattn_backward_launches(swin_wattn_t h) { return h ? h->bw_launches : 0; }
 
 // ---- stage hooks ------------------------------------------------------------
 
