@@ -377,20 +377,16 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     step(launch_gather_rows((const bf16 *)dy, dyw, g, C, s));
     step(launch_transpose((const bf16 *)Wproj, WpT, C, C, s));
     step(launch_transpose((const bf16 *)Wqkv, WqkvT, 3 * C, C, s));
-    // forward intermediates: qkv = xs Wqkv^T + bqkv, o = attention(qkv)
+    // forward intermediate qkv = xs Wqkv^T + bqkv (o comes out of the attention backward)
     GemmArgs k1{};
     k1.A = xs; k1.lda = C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
     k1.D = qkv; k1.ldd = 3 * C; k1.rows = g.T; k1.N = 3 * C; k1.K = C; k1.g = g;
     step(launch_gemm(k1, LOAD_PLAIN, STORE_PLAIN, dstatus(h), s));
-    AttnArgs k2{};
-    k2.qkv = qkv; k2.attn = attn; k2.table = (const bf16 *)bias_table; k2.tau = nullptr; k2.heads = h->heads;
-    k2.mode = SWIN_WATTN_V1; k2.g = g;
-    step(launch_attention(k2, dstatus(h), s));
     // do = dy_w Wproj
     GemmArgs k3{};
     k3.A = dyw; k3.lda = C; k3.Bw = WpT; k3.D = dO; k3.ldd = C; k3.rows = g.T; k3.N = C; k3.K = C; k3.g = g;
     step(launch_gemm(k3, LOAD_PLAIN, STORE_PLAIN, dstatus(h), s));
-    step(launch_attn_backward(qkv, dO, (const bf16 *)bias_table, h->heads, g, dqkv, dtable, s));
+    step(launch_attn_backward(qkv, dO, (const bf16 *)bias_table, h->heads, g, attn, dqkv, dtable, dstatus(h), s));
     // dx = scatter(dqkv Wqkv)
     GemmArgs k4{};
     k4.A = dqkv; k4.lda = 3 * C; k4.Bw = WqkvT; k4.D = (bf16 *)dx; k4.ldd = C; k4.rows = g.T; k4.N = C;

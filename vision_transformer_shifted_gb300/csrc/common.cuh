@@ -172,12 +172,13 @@ cudaError_t launch_watchdog(DeviceStatus st, cudaStream_t stream);
 cudaError_t launch_gather_rows(const bf16 *in, bf16 *out, const Geom &g, int C, cudaStream_t stream);
 // out [cols, rows] = in [rows, cols]^T.
 cudaError_t launch_transpose(const bf16 *in, bf16 *out, int rows, int cols, cudaStream_t stream);
-// out[n] += sum over rows of in[row, n] (fp32; N <= 2048).
+// out[n] += sum over rows of in[row, n] (fp32; N a multiple of 8, <= 2048).
 cudaError_t launch_colsum(const bf16 *in, int64_t rows, int N, float *out, cudaStream_t stream);
 // Windows of <= 64 tokens and 32 channels per head.
 bool attn_backward_supported(int M, int C, int heads);
-// dqkv [T, 3C] (window order) and dtable += from qkv [T, 3C], do [T, C].
+// From qkv [T, 3C] and do [T, C] (window order): the attention output
+// attn [T, C], dqkv [T, 3C] and dtable += ([(2M-1)^2, heads] fp32).
 cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, int heads, const Geom &g,
-                                 bf16 *dqkv, float *dtable, cudaStream_t stream);
+                                 bf16 *attn, bf16 *dqkv, float *dtable, DeviceStatus st, cudaStream_t stream);
 
 } // namespace swin

@@ -406,6 +406,12 @@ __device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t chunk)
 // The same with the B operand MN-major (bit 16).
 __host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) { return idesc_bf16(M, N) | (1u << 16); }
 
+// The same with both operands MN-major (bits 15 and 16): A given M-contiguous.
+__host__ __device__ constexpr uint32_t idesc_bf16_amn_bmn(int M, int N)
+{
+    return idesc_bf16(M, N) | (1u << 15) | (1u << 16);
+}
+
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a
 // K-major 128B-swizzled tile of 128-byte rows (8-row atoms of 1024 bytes).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk)
