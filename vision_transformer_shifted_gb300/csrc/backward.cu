@@ -85,37 +85,36 @@ __global__ void colsum_kernel(const bf16 *in, int64_t rows, int N, float *out)
 // ---- attention backward on the tensor cores ------------------------------------
 //
 // A unit is one head of two consecutive windows, stacked into 128 rows (window
-// 2p in rows 0..63, window 2p+1 in rows 64..127, tokens past N zero).  With the
-// head's q, k, v, do of both windows in shared memory ([128 rows][32 ch],
-// 64-byte swizzle):
+// 2p in rows 0..63, window 2p+1 in rows 64..127; rows past N stay zero).  TMA
+// brings the head's q, k, v, do of both windows into shared memory ([128 rows]
+// [32 ch], 64-byte swizzle), then
 //   S = q k^T and dP = do v^T                  (M = 128, N = 128, K = 32)
-// a thread per row turns its window's half of the two rows into P and
-// dS = P (dP - rowsum(P dP)) (bf16, block-diagonal: the other window's half
-// stays zero), then
+// two threads per row (one per 32 keys of the row's window) turn their halves
+// into P and dS = P (dP - rowsum(P dP)), merging the row's maximum, sum and
+// rowsum through shared memory, and store them as bf16 (block-diagonal: the
+// other window's block stays zero); then
 //   o = P v,  dq = dS k,  dv = P^T do,  dk = dS^T q   (M = 128, N = 32, K = 128)
-// where P^T and dS^T are the same shared-memory tiles read M-major.  Cross-
-// window products vanish because the off-diagonal blocks are zero.
-constexpr int TB_THREADS = 128;
+// with P^T and dS^T the same shared-memory tiles read M-major.  Cross-window
+// products vanish because the off-diagonal blocks are zero.  Units run head
+// by head (unit u: head u / pairs), so a CTA keeps one head's bias matrix in
+// shared memory and the table gradient of each (query, key) position in
+// registers, folding it into the table only when the head changes.
+constexpr int TB_THREADS = 256;
+constexpr int BIAS_STRIDE = 144; // bytes per bias row: 64 bf16 + 16 pad (conflict-free 16-byte loads)
 
 struct TbLayout {
     // byte offsets from the 1024-aligned base
     static constexpr uint32_t Q = 0, K = 8192, V = 16384, DO = 24576; // [128][64 B] tiles
     static constexpr uint32_t P = 32768, DS = 65536;                   // 4 panels of [128][32 keys]
-    static constexpr uint32_t KOFS = 98304;                            // int [64]
-    static constexpr uint32_t REG = KOFS + 256;                         // int [128]
-    static constexpr uint32_t TAB = REG + 512;                          // float [heads * L^2] (padded to 4)
-    __host__ __device__ static uint32_t hl(int heads, int M) { return ((uint32_t)heads * (2 * M - 1) * (2 * M - 1) + 3u) & ~3u; }
-    __host__ __device__ static uint32_t dtab(int heads, int M) { return TAB + 4 * hl(heads, M); }
-    __host__ __device__ static uint32_t bar(int heads, int M) { return dtab(heads, M) + 4 * hl(heads, M); }
-    static size_t bytes(int heads, int M) { return (size_t)bar(heads, M) + 16 + 1024; }
+    static constexpr uint32_t BIAS = 98304;                            // bf16 [64][72]
+    static constexpr uint32_t MASK = BIAS + 64 * BIAS_STRIDE;          // uint64 [4 classes][64 rows]
+    static constexpr uint32_t RED = MASK + 4 * 64 * 8;                 // float [2][128][4]
+    static constexpr uint32_t DTAB = RED + 2 * 128 * 16;               // float [(2M-1)^2 <= 225], padded
+    static constexpr uint32_t BAR = DTAB + 228 * 4;                    // 3 mbarriers + TMEM slot
+    static constexpr size_t bytes() { return (size_t)BAR + 32 + 1024; }
 };
 
-__device__ __forceinline__ int bw_region(const Geom &g, int wi, int wj, int t)
-{
-    if (g.s == 0) return 0;
-    const int ti = t / g.M, tj = t - (t / g.M) * g.M;
-    return 3 * shift_band(wi * g.M + ti, g.H, g.M, g.s) + shift_band(wj * g.M + tj, g.W, g.M, g.s);
-}
+__device__ __forceinline__ int band_in_window(int t, int M, int s) { return t < M - s ? 1 : 2; }
 
 __device__ __forceinline__ void store_row8(uint32_t dst, const float *v, float mul)
 {
@@ -138,210 +137,262 @@ __device__ __forceinline__ void store_global32(bf16 *dst, const float (&v)[32], 
 }
 
 __global__ void __launch_bounds__(TB_THREADS, 2)
-attn_backward_tc_kernel(const bf16 *qkv, const bf16 *dO, const bf16 *table, int heads, Geom g, bf16 *attn,
-                        bf16 *dqkv, float *dtable, DeviceStatus st)
+attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *dqkv, float *dtable,
+                        DeviceStatus st, const __grid_constant__ CUtensorMap tm_qkv,
+                        const __grid_constant__ CUtensorMap tm_do)
 {
     extern __shared__ uint8_t smraw[];
     using Ly = TbLayout;
     uint8_t *sm = smem_align(smraw, 1024);
     const uint32_t base = smem_u32(sm);
     const int N = g.N, M = g.M, C = g.C, L = 2 * M - 1, LL = L * L;
-    int *kofs = reinterpret_cast<int *>(sm + Ly::KOFS);
-    int *reg = reinterpret_cast<int *>(sm + Ly::REG);
-    float *tab = reinterpret_cast<float *>(sm + Ly::TAB);
-    float *dtab = reinterpret_cast<float *>(sm + Ly::dtab(heads, M));
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + Ly::bar(heads, M));
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 1);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int per = g.nh * g.nw;
+    const uint64_t *mask = reinterpret_cast<const uint64_t *>(sm + Ly::MASK);
+    float *red = reinterpret_cast<float *>(sm + Ly::RED);
+    float *dtab = reinterpret_cast<float *>(sm + Ly::DTAB);
+    const uint32_t bar_ld = base + Ly::BAR, bar_s = bar_ld + 8, bar_o = bar_ld + 16;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + Ly::BAR + 24);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, h2 = warp >> 2;     // TMEM lane quadrant; which 32 keys of the row
+    const int r = quad * 32 + lane, hf = r >> 6, i = r & 63;
     const int64_t npairs = (g.nwin + 1) / 2, nunits = npairs * heads;
     const float scale = 0.17677669529663687f; // 1 / sqrt(32)
     const float log2e = 1.4426950408889634f;
 
-    // P and dS start (and their off-diagonal blocks stay) zero
-    for (int e = tid; e < 65536 / 16; e += TB_THREADS)
-        *reinterpret_cast<uint4 *>(sm + Ly::P + 16 * e) = make_uint4(0, 0, 0, 0);
-    for (int j = tid; j < 64; j += TB_THREADS) kofs[j] = (j / M) * L + (j % M);
-    for (int e = tid; e < heads * LL; e += TB_THREADS) {
-        const int h = e / LL, idx = e - h * LL;
-        tab[e] = __bfloat162float(table[(int64_t)idx * heads + h]);
-        dtab[e] = 0.f;
+    // zero the operand tiles (rows past N are never loaded) and P, dS (their
+    // off-diagonal blocks are never written)
+    for (int e = tid; e < Ly::BIAS / 16; e += TB_THREADS)
+        *reinterpret_cast<uint4 *>(sm + 16 * e) = make_uint4(0, 0, 0, 0);
+    // visibility masks: bit j of mask[cls][i] = key j visible to query i, for
+    // the four window classes (cls bit 0: last window row, bit 1: last window
+    // column, where the shifted frame's bands split the window at M - s)
+    {
+        const int cls = tid >> 6, ii = tid & 63;
+        uint64_t m = 0;
+        if (ii < N) {
+            const int s = g.s;
+            auto region = [&](int t) {
+                if (s == 0) return 0;
+                return 3 * ((cls & 1) ? band_in_window(t / M, M, s) : 0) + ((cls & 2) ? band_in_window(t % M, M, s) : 0);
+            };
+            const int ri = region(ii);
+            for (int j = 0; j < N; ++j)
+                if (region(j) == ri) m |= 1ull << j;
+        }
+        reinterpret_cast<uint64_t *>(sm + Ly::MASK)[tid] = m;
     }
+    for (int e = tid; e < 228; e += TB_THREADS) dtab[e] = 0.f;
     if (tid == 0) {
-        mbar_init(smem_u32(bar), 1);
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 2);
         mbar_init_fence();
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tslot), 256);
         tmem_relinquish();
     }
+    fence_proxy_async_smem(); // the zeroed tiles, before any TMA or MMA touches them
 
-    // cp.async of unit u's q, k, v, do (zero rows past N or past the last
-    // window) and the shift region of this thread's row
+    // TMA of unit u's q, k, v, do (one box of N rows x 32 channels per window and tensor)
     auto load_unit = [&](int64_t u) {
-        const int64_t pair = u / heads;
-        const int head = (int)(u - pair * heads);
-        for (int e = tid; e < 2048; e += TB_THREADS) {
-            const int r = e & 127, ch = e >> 7, tsr = ch >> 2, c = ch & 3;
-            const int i = r & 63;
-            const int64_t win = 2 * pair + (r >> 6);
-            const bool ok = i < N && win < g.nwin;
-            const int64_t row = win * N + i;
-            const bf16 *src = !ok ? qkv
-                              : tsr < 3 ? qkv + row * 3 * C + tsr * C + head * 32 + c * 8
-                                        : dO + row * C + head * 32 + c * 8;
-            cp_async16(base + (uint32_t)tsr * 8192u + sw64_offset(r, c), src, ok ? 16u : 0u);
+        const int head = (int)(u / npairs);
+        const int64_t pair = u - (int64_t)head * npairs;
+        const int nw = 2 * pair + 1 < g.nwin ? 2 : 1;
+        mbar_arrive_expect_tx(bar_ld, (uint32_t)(nw * 4 * N * 64));
+        for (int w = 0; w < nw; ++w) {
+            const int y = (int)((2 * pair + w) * N);
+            const uint32_t dst = base + (uint32_t)w * 4096u;
+            tma_load_2d(dst + Ly::Q, &tm_qkv, head * 32, y, bar_ld);
+            tma_load_2d(dst + Ly::K, &tm_qkv, C + head * 32, y, bar_ld);
+            tma_load_2d(dst + Ly::V, &tm_qkv, 2 * C + head * 32, y, bar_ld);
+            tma_load_2d(dst + Ly::DO, &tm_do, head * 32, y, bar_ld);
         }
-        cp_async_commit();
-        const int i = tid & 63;
-        const int64_t win = 2 * pair + (tid >> 6);
-        int rg = -1;
-        if (i < N && win < g.nwin) {
-            const int rem = (int)(win % per);
-            rg = bw_region(g, rem / g.nw, rem % g.nw, i);
-        }
-        reg[tid] = rg;
     };
 
-    uint32_t phase = 0;
-    bool failed = false;
-    if (blockIdx.x < nunits) load_unit(blockIdx.x);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 0 && blockIdx.x < nunits) load_unit(blockIdx.x);
     const uint32_t tmem = *tslot;
-    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
-    const int r = tid, hf = r >> 6, i = r & 63;
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+
+    uint32_t phase = 0;
+    bool failed = false;
+    int cur_head = -1;
+    float acc[32]; // table gradient of (query i, key 32*h2 + j) over this CTA's units of cur_head
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+
+    // adds acc into the head's table gradient (shared, then global)
+    auto flush_head = [&]() {
+        if (i < N) {
+            const int ri = i / M, ci = i % M;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int key = 32 * h2 + j;
+                if (key < N && acc[j] != 0.f)
+                    atomicAdd(&dtab[(ri - key / M + M - 1) * L + (ci - key % M + M - 1)], acc[j]);
+                acc[j] = 0.f;
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < LL; e += TB_THREADS) {
+            if (dtab[e] != 0.f) atomicAdd(&dtable[(int64_t)e * heads + cur_head], dtab[e]);
+            dtab[e] = 0.f;
+        }
+    };
 
     for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
-        const int64_t pair = u / heads;
-        const int head = (int)(u - pair * heads);
+        const int head = (int)(u / npairs);
+        const int64_t pair = u - (int64_t)head * npairs;
         const int64_t win = 2 * pair + hf;
         const bool rv = i < N && win < g.nwin;
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 128);
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                mma_bf16(tmem, desc_kmajor_sw64(base + Ly::Q + 32 * ks), desc_kmajor_sw64(base + Ly::K + 32 * ks), id,
-                         ks);
-                mma_bf16(tmem + 128, desc_kmajor_sw64(base + Ly::DO + 32 * ks),
-                         desc_kmajor_sw64(base + Ly::V + 32 * ks), id, ks);
+        if (head != cur_head) {
+            if (cur_head >= 0) flush_head();
+            // the head's bias matrix B[i][j] = table[idx(i, j), head] (zero outside N x N)
+            for (int e = tid; e < 64 * 64; e += TB_THREADS) {
+                const int a = e >> 6, b = e & 63;
+                bf16 v = __float2bfloat16(0.f);
+                if (a < N && b < N)
+                    v = table[(int64_t)((a / M - b / M + M - 1) * L + (a % M - b % M + M - 1)) * heads + head];
+                *reinterpret_cast<bf16 *>(sm + Ly::BIAS + a * BIAS_STRIDE + 2 * b) = v;
             }
-            mma_commit(smem_u32(bar));
+            cur_head = head;
+            __syncthreads();
         }
-        bool ok = mbar_wait(smem_u32(bar), phase, st.wait_ns);
-        phase ^= 1;
+        int cls = 0;
+        if (g.s > 0 && rv) {
+            const int rem = (int)(win % (g.nh * g.nw));
+            cls = (rem / g.nw == g.nh - 1 ? 1 : 0) | (rem % g.nw == g.nw - 1 ? 2 : 0);
+        }
+        if (tid == 0) {
+            const bool okl = mbar_wait(bar_ld, phase, st.wait_ns);
+            if (okl) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16(128, 128);
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    mma_bf16(tmem, desc_kmajor_sw64(base + Ly::Q + 32 * ks), desc_kmajor_sw64(base + Ly::K + 32 * ks),
+                             id, ks);
+                    mma_bf16(tmem + 128, desc_kmajor_sw64(base + Ly::DO + 32 * ks),
+                             desc_kmajor_sw64(base + Ly::V + 32 * ks), id, ks);
+                }
+                mma_commit(bar_s);
+            }
+        }
+        bool ok = mbar_wait(bar_s, phase, st.wait_ns);
         if (__syncthreads_or(!ok)) { failed = true; break; }
         tc_fence_after();
 
-        // ---- P and dS of this thread's row (its window's 64 keys) ----
+        // ---- P and dS: this thread's 32 keys of its row ----
+        float s[32], d[32];
+        tmem_ld32(t_lane + 64 * hf + 32 * h2, s);
+        tmem_ld32(t_lane + 128 + 64 * hf + 32 * h2, d);
+        const uint32_t mb = rv ? (uint32_t)(mask[cls * 64 + i] >> (32 * h2)) : 0u;
         {
-            float s0[32], s1[32], d0[32], d1[32];
-            tmem_ld32(t_lane + 64 * hf, s0);
-            tmem_ld32(t_lane + 64 * hf + 32, s1);
-            tmem_ld32(t_lane + 128 + 64 * hf, d0);
-            tmem_ld32(t_lane + 128 + 64 * hf + 32, d1);
+            const uint4 *brow = reinterpret_cast<const uint4 *>(sm + Ly::BIAS + i * BIAS_STRIDE + 64 * h2);
+            uint4 bq[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) bq[q] = brow[q];
             tmem_wait_ld();
-            const int myreg = reg[r];
-            const int bi = rv ? (i / M + M - 1) * L + (i % M) + M - 1 : 0;
-            const float *tb = tab + head * LL;
             float mx = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                float &s = j < 32 ? s0[j] : s1[j - 32];
-                const bool ok_j = rv && j < N && reg[64 * hf + j] == myreg;
-                s = ok_j ? fmaf(s, scale, tb[bi - kofs[j]]) : -INFINITY;
-                mx = fmaxf(mx, s);
-            }
-            float sum = 0.f;
-            const float mxl = rv ? mx * log2e : 0.f;
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t w4[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                float &s = j < 32 ? s0[j] : s1[j - 32];
-                s = ex2_approx(fmaf(s, log2e, -mxl)); // -inf -> 0
-                sum += s;
-            }
-            const float inv = rv ? 1.0f / sum : 0.f;
-            float dd = 0.f;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                float &s = j < 32 ? s0[j] : s1[j - 32];
-                const float dp = j < 32 ? d0[j] : d1[j - 32];
-                s *= inv;
-                dd = fmaf(s, dp, dd);
-            }
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const float p = j < 32 ? s0[j] : s1[j - 32];
-                float &d = j < 32 ? d0[j] : d1[j - 32];
-                d = p * (d - dd);
-            }
-            // bf16 rows into the P and dS panels (keys 64*hf .. 64*hf+63)
-#pragma unroll
-            for (int q = 0; q < 2; ++q)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t off = (uint32_t)(2 * hf + q) * 8192u + sw64_offset(r, c);
-                    store_row8(base + Ly::P + off, (q == 0 ? s0 : s1) + 8 * c, 1.f);
-                    store_row8(base + Ly::DS + off, (q == 0 ? d0 : d1) + 8 * c, 1.f);
+                for (int t = 0; t < 4; ++t) {
+                    const float2 b2 = unpack_bf16x2(w4[t]);
+                    const int j = 8 * q + 2 * t;
+                    s[j] = (mb >> j) & 1u ? fmaf(s[j], scale, b2.x) : -INFINITY;
+                    s[j + 1] = (mb >> (j + 1)) & 1u ? fmaf(s[j + 1], scale, b2.y) : -INFINITY;
+                    mx = fmaxf(mx, fmaxf(s[j], s[j + 1]));
                 }
-            if (rv) {
-                float *dt = dtab + head * LL;
+            }
+            const float mxl = mb ? mx * log2e : 0.f;
+            float sum = 0.f, dsum = 0.f;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const float d = j < 32 ? d0[j] : d1[j - 32];
-                    if (j < N && d != 0.f) atomicAdd(&dt[bi - kofs[j]], d);
-                }
+            for (int j = 0; j < 32; ++j) {
+                s[j] = ex2_approx(fmaf(s[j], log2e, -mxl)); // masked: -inf -> 0
+                sum += s[j];
+                dsum = fmaf(s[j], d[j], dsum);
+            }
+            float *mine = red + (h2 * 128 + r) * 4;
+            mine[0] = mb ? mx : -INFINITY;
+            mine[1] = sum;
+            mine[2] = dsum;
+            __syncthreads();
+            const float *other = red + ((1 - h2) * 128 + r) * 4;
+            const float mo = other[0], so = other[1], dso = other[2];
+            const float mt = mb ? mx : -INFINITY;
+            const float m = fmaxf(mt, mo);
+            float p_scale = 0.f, D = 0.f;
+            if (rv && m > -INFINITY) {
+                const float ft = ex2_approx((mt - m) * log2e), fo = ex2_approx((mo - m) * log2e);
+                const float inv = 1.0f / (sum * ft + so * fo);
+                p_scale = ft * inv;
+                D = (dsum * ft + dso * fo) * inv;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                s[j] *= p_scale;
+                d[j] = s[j] * (d[j] - D);
+                acc[j] += d[j];
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t off = (uint32_t)(2 * hf + h2) * 8192u + sw64_offset(r, c);
+                store_row8(base + Ly::P + off, s + 8 * c, 1.f);
+                store_row8(base + Ly::DS + off, d + 8 * c, 1.f);
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0 || tid == 128) {
             tc_fence_after();
             const uint32_t id_k = idesc_bf16_bmn(128, 32), id_m = idesc_bf16_amn_bmn(128, 32);
+            if (tid == 0) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t kpan = (uint32_t)(kk >> 1) * 8192u + 32u * (kk & 1);
-                mma_bf16(tmem + 0, desc_kmajor_sw64(base + Ly::P + kpan), desc_mnmajor_sw64(base + Ly::V + 1024 * kk, 8192),
-                         id_k, kk);
-                mma_bf16(tmem + 32, desc_kmajor_sw64(base + Ly::DS + kpan),
-                         desc_mnmajor_sw64(base + Ly::K + 1024 * kk, 8192), id_k, kk);
-                mma_bf16(tmem + 64, desc_mnmajor_sw64(base + Ly::DS + 1024 * kk, 8192),
-                         desc_mnmajor_sw64(base + Ly::Q + 1024 * kk, 8192), id_m, kk);
-                mma_bf16(tmem + 96, desc_mnmajor_sw64(base + Ly::P + 1024 * kk, 8192),
-                         desc_mnmajor_sw64(base + Ly::DO + 1024 * kk, 8192), id_m, kk);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t kpan = (uint32_t)(kk >> 1) * 8192u + 32u * (kk & 1);
+                    mma_bf16(tmem + 0, desc_kmajor_sw64(base + Ly::P + kpan),
+                             desc_mnmajor_sw64(base + Ly::V + 1024 * kk, 8192), id_k, kk);
+                    mma_bf16(tmem + 32, desc_kmajor_sw64(base + Ly::DS + kpan),
+                             desc_mnmajor_sw64(base + Ly::K + 1024 * kk, 8192), id_k, kk);
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    mma_bf16(tmem + 64, desc_mnmajor_sw64(base + Ly::DS + 1024 * kk, 8192),
+                             desc_mnmajor_sw64(base + Ly::Q + 1024 * kk, 8192), id_m, kk);
+                    mma_bf16(tmem + 96, desc_mnmajor_sw64(base + Ly::P + 1024 * kk, 8192),
+                             desc_mnmajor_sw64(base + Ly::DO + 1024 * kk, 8192), id_m, kk);
+                }
             }
-            mma_commit(smem_u32(bar));
+            mma_commit(bar_o);
         }
-        ok = mbar_wait(smem_u32(bar), phase, st.wait_ns);
+        ok = mbar_wait(bar_o, phase, st.wait_ns);
         phase ^= 1;
         if (__syncthreads_or(!ok)) { failed = true; break; }
         tc_fence_after();
-        // q, k, v, do are free: start the next unit's loads under the epilogue
-        if (u + gridDim.x < nunits) load_unit(u + gridDim.x);
+        // q, k, v, do are free: the next unit's loads run under the epilogue
+        if (tid == 0 && u + gridDim.x < nunits) load_unit(u + gridDim.x);
 
-        // ---- o, dq, dk, dv rows out (row r: query or key token i of window win) ----
+        // ---- outputs of row r: o and dq (first four warps), dk and dv (last four) ----
         {
             float a[32], b[32];
-            const int64_t row = win * N + i;
-            tmem_ld32(t_lane + 0, a);
-            tmem_ld32(t_lane + 32, b);
+            tmem_ld32(t_lane + 64 * h2, a);
+            tmem_ld32(t_lane + 64 * h2 + 32, b);
             tmem_wait_ld();
             if (rv) {
-                store_global32(attn + row * C + head * 32, a, 1.f);
-                store_global32(dqkv + row * 3 * C + head * 32, b, scale);
-            }
-            tmem_ld32(t_lane + 64, a);
-            tmem_ld32(t_lane + 96, b);
-            tmem_wait_ld();
-            if (rv) {
-                store_global32(dqkv + row * 3 * C + C + head * 32, a, scale);
-                store_global32(dqkv + row * 3 * C + 2 * C + head * 32, b, 1.f);
+                const int64_t row = win * N + i;
+                if (h2 == 0) {
+                    store_global32(attn + row * C + head * 32, a, 1.f);
+                    store_global32(dqkv + row * 3 * C + head * 32, b, scale);
+                } else {
+                    store_global32(dqkv + row * 3 * C + C + head * 32, a, scale);
+                    store_global32(dqkv + row * 3 * C + 2 * C + head * 32, b, 1.f);
+                }
             }
         }
         tc_fence_before();
@@ -349,13 +400,13 @@ attn_backward_tc_kernel(const bf16 *qkv, const bf16 *dO, const bf16 *table, int 
     }
     if (failed) {
         if (tid == 0) atomicOr(st.err, ERR_TIMEOUT);
-        cp_async_wait<0>();
+        // a load may still be in flight: wait for it (bounded) before leaving
+        if (tid == 0) mbar_wait(bar_ld, phase, st.wait_ns);
+    } else if (cur_head >= 0) {
+        flush_head();
     }
+    tc_fence_before();
     __syncthreads();
-    for (int e = tid; e < heads * LL; e += TB_THREADS) {
-        const int h = e / LL, idx = e - h * LL;
-        if (dtab[e] != 0.f) atomicAdd(&dtable[(int64_t)idx * heads + h], dtab[e]);
-    }
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
@@ -389,18 +440,18 @@ cudaError_t launch_colsum(const bf16 *in, int64_t rows, int N, float *out, cudaS
     return cudaGetLastError();
 }
 
-bool attn_backward_supported(int M, int C, int heads)
-{
-    return M * M <= 64 && C == heads * 32 && TbLayout::bytes(heads, M) <= 227 * 1024;
-}
+bool attn_backward_supported(int M, int C, int heads) { return M * M <= 64 && C == heads * 32; }
 
 cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, int heads, const Geom &g,
                                  bf16 *attn, bf16 *dqkv, float *dtable, DeviceStatus st, cudaStream_t stream)
 {
     if (!attn_backward_supported(g.M, g.C, heads)) return cudaErrorInvalidValue;
-    const size_t smem = TbLayout::bytes(heads, g.M);
-    cudaError_t e = cudaFuncSetAttribute(attn_backward_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    CUtensorMap tm_qkv, tm_do;
+    cudaError_t e = make_tensor_map_sw64(&tm_qkv, qkv, g.T, 3 * g.C, g.N);
+    if (e == cudaSuccess) e = make_tensor_map_sw64(&tm_do, dO, g.T, g.C, g.N);
+    if (e != cudaSuccess) return e;
+    const size_t smem = TbLayout::bytes();
+    e = cudaFuncSetAttribute(attn_backward_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     static int sms = 0;
     if (!sms) {
@@ -408,11 +459,11 @@ cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *ta
         cudaGetDevice(&dev);
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
     }
-    const int per_sm = 2 * TbLayout::bytes(heads, g.M) + 2048 <= 228 * 1024 ? 2 : 1;
     const int64_t units = (g.nwin + 1) / 2 * heads;
-    const int64_t cap = (int64_t)sms * per_sm;
+    const int64_t cap = (int64_t)sms * 2;
     const unsigned grid = (unsigned)(units < cap ? units : cap);
-    attn_backward_tc_kernel<<<grid, TB_THREADS, smem, stream>>>(qkv, dO, table, heads, g, attn, dqkv, dtable, st);
+    attn_backward_tc_kernel<<<grid, TB_THREADS, smem, stream>>>(table, heads, g, attn, dqkv, dtable, st, tm_qkv,
+                                                                tm_do);
     return cudaGetLastError();
 }
 
