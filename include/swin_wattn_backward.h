@@ -17,11 +17,13 @@
  * (o, P, q, k, v as in the forward; xs = gather(x); scatter = window
  * reverse then roll by +s, the inverse map of gather).
  *
- * The call recomputes q, k, v and o from x (nothing of the forward is kept),
- * then runs: two gathers, the QKV GEMM and the window attention of the
- * forward, the do GEMM, the per-window attention backward, the dx GEMM with
- * the scatter in its epilogue, two weight-gradient GEMMs (cuBLAS: plain
- * long-K reductions over all tokens) and two column sums.
+ * The call recomputes q, k and v from x (nothing of the forward is kept) and
+ * runs: the QKV GEMM and the do GEMM, each gathering its rows into window
+ * order in its loads; the attention backward, which recomputes S and P,
+ * yields o, dq, dk, dv (written back in token order) and the table
+ * gradient; the dx GEMM; two weight-gradient GEMMs (cuBLAS: plain long-K
+ * reductions over all tokens, which do not depend on the token order) and
+ * two column sums.
  *
  * Conventions of swin_wattn.h: device pointers, asynchronous on `stream`,
  * caller-owned tensors, status codes SWIN_WATTN_*, no CPU fallback.
@@ -44,7 +46,7 @@ extern "C" {
  * Every pointer 16-byte aligned; dx overlaps neither x nor dy.
  * Errors: EINVAL for NULL or misaligned pointers, bad shapes, overlap;
  * EUNSUPPORTED for a V2 or fp32 handle, windows of more than 64 tokens, or
- * B*H*W >= 2^31; ENOMEM if the workspace (10 * B*H*W*C bf16 elements plus
+ * B*H*W >= 2^31; ENOMEM if the workspace (8 * B*H*W*C bf16 elements plus
  * 4C^2) cannot be allocated; ECUDA for launch or cuBLAS failures.  B = 0
  * zeroes the parameter gradients and returns. */
 int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,

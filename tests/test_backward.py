@@ -154,7 +154,7 @@ def test_backward_parity_small(key, kw):
     w = _workload(key, **kw)
     got, ref, launches = _run_backward(w)
     _check_all(got, ref)
-    assert launches == 12
+    assert launches == 10
 
 
 @pytest.mark.gpu

@@ -359,44 +359,45 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
         return cuda_status(e);
     }
     if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
-    // workspace (bf16): xs, dyw, attn, do [T, C]; qkv, dqkv [T, 3C]; WprojT [C, C]; WqkvT [C, 3C]
+    // workspace (bf16): attn, do [T, C]; qkv, dqkv [T, 3C]; WprojT [C, C]; WqkvT [C, 3C]
     const size_t tc = (size_t)g.T * C;
-    rc = ensure_buffer(&h->bws, &h->bws_bytes, (10 * tc + 4 * (size_t)C * C) * 2);
+    rc = ensure_buffer(&h->bws, &h->bws_bytes, (8 * tc + 4 * (size_t)C * C) * 2);
     if (rc) return rc;
     if (!h->blas) {
         if (cublasCreate(&h->blas) != CUBLAS_STATUS_SUCCESS) { h->blas = nullptr; return SWIN_WATTN_ECUDA; }
     }
     if (cublasSetStream(h->blas, s) != CUBLAS_STATUS_SUCCESS) return SWIN_WATTN_ECUDA;
-    bf16 *xs = (bf16 *)h->bws, *dyw = xs + tc, *attn = dyw + tc, *dO = attn + tc, *qkv = dO + tc;
-    bf16 *dqkv = qkv + 3 * tc, *WpT = dqkv + 3 * tc, *WqkvT = WpT + (size_t)C * C;
+    bf16 *attn = (bf16 *)h->bws, *dO = attn + tc, *qkv = dO + tc, *dqkv = qkv + 3 * tc;
+    bf16 *WpT = dqkv + 3 * tc, *WqkvT = WpT + (size_t)C * C;
     int launches = 0;
     auto step = [&](cudaError_t r) {
         if (e == cudaSuccess) { e = r; ++launches; }
     };
-    step(launch_gather_rows((const bf16 *)x, xs, g, C, s));
-    step(launch_gather_rows((const bf16 *)dy, dyw, g, C, s));
     step(launch_transpose((const bf16 *)Wproj, WpT, C, C, s));
     step(launch_transpose((const bf16 *)Wqkv, WqkvT, 3 * C, C, s));
-    // forward intermediate qkv = xs Wqkv^T + bqkv (o comes out of the attention backward)
+    // window order: qkv = gather(x) Wqkv^T + bqkv, do = gather(dy) Wproj
     GemmArgs k1{};
-    k1.A = xs; k1.lda = C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
+    k1.A = (const bf16 *)x; k1.lda = C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
     k1.D = qkv; k1.ldd = 3 * C; k1.rows = g.T; k1.N = 3 * C; k1.K = C; k1.g = g;
-    step(launch_gemm(k1, LOAD_PLAIN, STORE_PLAIN, dstatus(h), s));
-    // do = dy_w Wproj
+    step(launch_gemm(k1, LOAD_GATHER, STORE_PLAIN, dstatus(h), s));
     GemmArgs k3{};
-    k3.A = dyw; k3.lda = C; k3.Bw = WpT; k3.D = dO; k3.ldd = C; k3.rows = g.T; k3.N = C; k3.K = C; k3.g = g;
-    step(launch_gemm(k3, LOAD_PLAIN, STORE_PLAIN, dstatus(h), s));
+    k3.A = (const bf16 *)dy; k3.lda = C; k3.Bw = WpT; k3.D = dO; k3.ldd = C; k3.rows = g.T; k3.N = C; k3.K = C;
+    k3.g = g;
+    step(launch_gemm(k3, LOAD_GATHER, STORE_PLAIN, dstatus(h), s));
+    // o and dqkv in token order, dtable
     step(launch_attn_backward(qkv, dO, (const bf16 *)bias_table, h->heads, g, attn, dqkv, dtable, dstatus(h), s));
-    // dx = scatter(dqkv Wqkv)
+    // dx = dqkv Wqkv (token order already)
     GemmArgs k4{};
     k4.A = dqkv; k4.lda = 3 * C; k4.Bw = WqkvT; k4.D = (bf16 *)dx; k4.ldd = C; k4.rows = g.T; k4.N = C;
     k4.K = 3 * C; k4.g = g;
-    step(launch_gemm(k4, LOAD_PLAIN, STORE_SCATTER, dstatus(h), s));
-    step(launch_colsum(dyw, g.T, C, dbproj, s));
+    step(launch_gemm(k4, LOAD_PLAIN, STORE_PLAIN, dstatus(h), s));
+    step(launch_colsum((const bf16 *)dy, g.T, C, dbproj, s));
     step(launch_colsum(dqkv, g.T, 3 * C, dbqkv, s));
     if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
-    if (weight_grad(h->blas, dyw, C, attn, C, g.T, dWproj) != CUBLAS_STATUS_SUCCESS) return SWIN_WATTN_ECUDA;
-    if (weight_grad(h->blas, dqkv, 3 * C, xs, C, g.T, dWqkv) != CUBLAS_STATUS_SUCCESS) return SWIN_WATTN_ECUDA;
+    if (weight_grad(h->blas, (const bf16 *)dy, C, attn, C, g.T, dWproj) != CUBLAS_STATUS_SUCCESS)
+        return SWIN_WATTN_ECUDA;
+    if (weight_grad(h->blas, dqkv, 3 * C, (const bf16 *)x, C, g.T, dWqkv) != CUBLAS_STATUS_SUCCESS)
+        return SWIN_WATTN_ECUDA;
     h->bw_launches = launches + 2;
     return SWIN_WATTN_OK;
 }

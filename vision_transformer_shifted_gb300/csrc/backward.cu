@@ -9,28 +9,20 @@
 //   dP = do v^T, dS = P (dP - rowsum(P dP)), dq = dS k / sqrt(d),
 //   dk = dS^T q / sqrt(d), dv = P^T do, dB[idx(i,j)] += dS_ij,
 //   dWqkv = dqkv^T xs, dbqkv = sum dqkv, dx = scatter(dqkv Wqkv).
-// This file holds the gathers, a weight transpose, column sums and the
-// attention backward (which also yields o, so the forward attention is not
-// run again); the GEMMs are launched by the caller.
+// The weight and bias gradients are sums over tokens, so they do not depend
+// on the order of the rows: the attention backward writes o and dqkv straight
+// back in token order, dWproj = dy^T o and dWqkv = dqkv^T x then take dy and x
+// as they are, dx = dqkv Wqkv needs no scatter, and only the two GEMMs that
+// feed the attention backward (qkv and do, in window order) gather their rows.
+// This file holds a weight transpose, column sums and the attention backward
+// (which also yields o, so the forward attention is not run again); the GEMMs
+// are launched by the caller.
 #include "common.cuh"
 #include "ptx.cuh"
 
 namespace swin {
 
 namespace {
-
-// out[r, :] = in[token(r), :] for window-order rows r (16-byte chunks).
-__global__ void gather_rows_kernel(const bf16 *in, bf16 *out, Geom g, int C)
-{
-    const int cpr = C / 8;
-    const int64_t total = g.T * cpr;
-    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = q / cpr;
-        const int c = (int)(q - r * cpr);
-        const int64_t tok = window_row_to_token(g, r);
-        *reinterpret_cast<uint4 *>(out + r * C + c * 8) = *reinterpret_cast<const uint4 *>(in + tok * C + c * 8);
-    }
-}
 
 // out [cols, rows] = in [rows, cols]^T (bf16), 32 x 32 tiles through shared memory.
 __global__ void transpose_kernel(const bf16 *in, bf16 *out, int rows, int cols)
@@ -385,13 +377,14 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
             tmem_ld32(t_lane + 64 * h2 + 32, b);
             tmem_wait_ld();
             if (rv) {
-                const int64_t row = win * N + i;
+                // rows go back to their tokens' places (window reverse and roll by +s)
+                const int64_t tok = window_row_to_token(g, win * N + i);
                 if (h2 == 0) {
-                    store_global32(attn + row * C + head * 32, a, 1.f);
-                    store_global32(dqkv + row * 3 * C + head * 32, b, scale);
+                    store_global32(attn + tok * C + head * 32, a, 1.f);
+                    store_global32(dqkv + tok * 3 * C + head * 32, b, scale);
                 } else {
-                    store_global32(dqkv + row * 3 * C + C + head * 32, a, scale);
-                    store_global32(dqkv + row * 3 * C + 2 * C + head * 32, b, 1.f);
+                    store_global32(dqkv + tok * 3 * C + C + head * 32, a, scale);
+                    store_global32(dqkv + tok * 3 * C + 2 * C + head * 32, b, 1.f);
                 }
             }
         }
@@ -412,15 +405,6 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
 }
 
 } // namespace
-
-cudaError_t launch_gather_rows(const bf16 *in, bf16 *out, const Geom &g, int C, cudaStream_t stream)
-{
-    const int64_t total = g.T * (C / 8);
-    const int64_t want = (total + 255) / 256;
-    const unsigned grid = (unsigned)(want < 152 * 16 ? want : 152 * 16);
-    gather_rows_kernel<<<grid, 256, 0, stream>>>(in, out, g, C);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_transpose(const bf16 *in, bf16 *out, int rows, int cols, cudaStream_t stream)
 {

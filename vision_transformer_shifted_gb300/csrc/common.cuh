@@ -168,8 +168,6 @@ cudaError_t launch_cpb_table(const float *W1, const float *b1, const float *W2, 
 cudaError_t launch_watchdog(DeviceStatus st, cudaStream_t stream);
 
 // ---- backward (V1) ----------------------------------------------------------
-// out[r, :] = in[token(r), :] over window-order rows (C a multiple of 8).
-cudaError_t launch_gather_rows(const bf16 *in, bf16 *out, const Geom &g, int C, cudaStream_t stream);
 // out [cols, rows] = in [rows, cols]^T.
 cudaError_t launch_transpose(const bf16 *in, bf16 *out, int rows, int cols, cudaStream_t stream);
 // out[n] += sum over rows of in[row, n] (fp32; N a multiple of 8, <= 2048).
@@ -177,7 +175,8 @@ cudaError_t launch_colsum(const bf16 *in, int64_t rows, int N, float *out, cudaS
 // Windows of <= 64 tokens and 32 channels per head.
 bool attn_backward_supported(int M, int C, int heads);
 // From qkv [T, 3C] and do [T, C] (window order): the attention output
-// attn [T, C], dqkv [T, 3C] and dtable += ([(2M-1)^2, heads] fp32).
+// attn [T, C] and dqkv [T, 3C] in token order, and dtable += ([(2M-1)^2,
+// heads] fp32).
 cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, int heads, const Geom &g,
                                  bf16 *attn, bf16 *dqkv, float *dtable, DeviceStatus st, cudaStream_t stream);
 
