@@ -530,6 +530,23 @@ cudaError_t make_tensor_map_sw64(CUtensorMap *map, const void *ptr, int64_t rows
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tensor map over a row-major bf16 matrix [rows, cols] with a row stride of
+// ld elements (ld * 2 a multiple of 16): boxes of 64 columns x box_rows rows,
+// 128-byte swizzle, zero fill past the last row or column.
+cudaError_t make_tensor_map_sw128(CUtensorMap *map, const void *ptr, int64_t rows, int cols, int64_t ld, int box_rows)
+{
+    const EncodeTiledFn encode = encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Tensor map over a bf16 image batch [rows, width, cols] (rows = B*H image
 // rows, width = W tokens, cols = C channels, row-major): boxes of 32 channels
 // x box_w tokens x box_h image rows, 64-byte swizzle, zero fill outside.

@@ -53,8 +53,9 @@ __global__ void colsum_kernel(const bf16 *in, int64_t rows, int N, float *out)
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[k] = 0.f;
     if (rr < rpi) {
-        for (int64_t r = (int64_t)blockIdx.x * rpi + rr; r < rows; r += (int64_t)gridDim.x * rpi) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(in + r * N + c * 8);
+        const int64_t step = (int64_t)gridDim.x * rpi;
+        int64_t r = (int64_t)blockIdx.x * rpi + rr;
+        auto add = [&](const uint4 &u) {
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -62,7 +63,16 @@ __global__ void colsum_kernel(const bf16 *in, int64_t rows, int N, float *out)
                 acc[2 * k] += f.x;
                 acc[2 * k + 1] += f.y;
             }
+        };
+        // four rows per round, their loads issued together
+        for (; r + 3 * step < rows; r += 4 * step) {
+            uint4 u[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) u[q] = *reinterpret_cast<const uint4 *>(in + (r + q * step) * N + c * 8);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) add(u[q]);
         }
+        for (; r < rows; r += step) add(*reinterpret_cast<const uint4 *>(in + r * N + c * 8));
 #pragma unroll
         for (int k = 0; k < 8; ++k) part[rr * N + c * 8 + k] = acc[k];
     }

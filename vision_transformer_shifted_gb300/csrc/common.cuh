@@ -156,6 +156,11 @@ cudaError_t launch_fused(const bf16 *x, const bf16 *Wqkv, const bf16 *bqkv, cons
 // cols * 2 a multiple of 16): boxes of 32 columns x box_rows rows (<= 256),
 // 64-byte swizzle in shared memory, zero fill past the last row.
 cudaError_t make_tensor_map_sw64(CUtensorMap *map, const void *ptr, int64_t rows, int cols, int box_rows);
+// Tensor map over a row-major bf16 matrix [rows, cols] with row stride ld
+// (elements): boxes of 64 columns x box_rows rows, 128-byte swizzle, zero
+// fill past the last row or column.
+cudaError_t make_tensor_map_sw128(CUtensorMap *map, const void *ptr, int64_t rows, int cols, int64_t ld,
+                                  int box_rows);
 // Tensor map over a bf16 image batch [rows, width, cols] (rows = B*H image rows,
 // width = W, cols = C; strides multiples of 16 bytes): boxes of 32 channels x
 // box_w tokens x box_h image rows, 64-byte swizzle, zero fill outside.

@@ -14,6 +14,8 @@
 // swizzle atom per row, 4-stage ring), cp.async into the K-major swizzled
 // layout, one thread issuing tcgen05.mma, the fp32 accumulator in TMEM, and a
 // 4-warp epilogue reading one TMEM lane (= one output row) per thread.
+#include <cstring>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -245,6 +247,340 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, tmem_cols);
+}
+
+// ---- persistent GEMM with the weight matrix resident in shared memory -----------
+//
+// For the block's projections the whole weight matrix Bw [N, K] fits in
+// shared memory (K-major, 128-byte swizzle, 64-wide K blocks).  One CTA per
+// SM keeps it there and walks over 128-row tiles (and, for N > 256, two
+// column halves), with three warp roles:
+//   warp 0      producer: 128 x 64 A blocks into a ring of stages by TMA (plain
+//               rows); for rows gathered through the window map, warps 0 and
+//               10..16 each bring 16 rows of every block by cp.async
+//   warp 1      one thread issues the MMAs of a tile into one of two TMEM
+//               accumulators, releasing each A stage by tcgen05.commit
+//   warps 2..9  epilogue: two warps per TMEM lane quadrant (alternate 32-column
+//               chunks) drain the other accumulator while the next tile runs.
+// Every wait is bounded; a timeout sets the error word and ends the kernel.
+constexpr int RS_NEPI = 8;
+constexpr int RS_NPROD = 8; // producer warps for gathered rows (warp 0 and warps 10..16)
+constexpr int RS_THREADS = 32 * (2 + RS_NEPI + RS_NPROD - 1);
+constexpr int RS_DEPTH = 4; // cp.async groups a producer lane keeps in flight (gathered rows)
+constexpr int RS_STAGE = BM * 128;
+
+struct RsPlan {
+    int BN, nbn, KB, stages;
+    uint32_t tcols;
+    size_t b_bytes, smem;
+};
+
+__device__ __forceinline__ void rs_epilogue_chunk32(const GemmArgs &a, int64_t R, int n, bf16 *dst, float (&v)[32],
+                                                   const float *bias, bool norm)
+{
+    if (norm) {
+        // V2: this 32-column chunk is one head's q or k; bias first, then scale
+        // to unit length (norm clamped at 1e-12) before rounding
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            v[i] += bias[i];
+            ss = fmaf(v[i], v[i], ss);
+        }
+        const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+        float zero[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            v[i] *= inv;
+            zero[i] = 0.f;
+        }
+        store_row_bf16(dst, v, zero, 32);
+    } else if (a.epi == EPI_NONE) {
+        store_row_bf16(dst, v, bias, 32);
+    } else if (a.epi == EPI_RESID) {
+        // residual row read 16 bytes at a time (R < rows here)
+        const uint4 *res = reinterpret_cast<const uint4 *>(a.R + R * a.ldr + n);
+        float e[32], zero[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 u = res[q];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float2 f = unpack_bf16x2(w[t]);
+                e[8 * q + 2 * t] = v[8 * q + 2 * t] + bias[8 * q + 2 * t] + f.x;
+                e[8 * q + 2 * t + 1] = v[8 * q + 2 * t + 1] + bias[8 * q + 2 * t + 1] + f.y;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) zero[i] = 0.f;
+        store_row_bf16(dst, e, zero, 32);
+    } else {
+        float e[32], zero[32];
+        epilogue_op(a, R, n, v, bias, e, 32);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) zero[i] = 0.f;
+        store_row_bf16(dst, e, zero, 32);
+    }
+}
+
+template <int LOAD, int STORE>
+__global__ void __launch_bounds__(RS_THREADS, 1)
+gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ CUtensorMap tmA)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_align(smem_raw, 1024);
+    const int S = pl.stages, BN = pl.BN, nbn = pl.nbn, KB = pl.KB;
+    uint8_t *sB = smem;
+    uint8_t *sA = smem + pl.b_bytes;
+    float *sbias = reinterpret_cast<float *>(sA + (size_t)S * RS_STAGE);
+    int64_t *rowoff = reinterpret_cast<int64_t *>(sbias + 512); // producer's gathered rows of the tile
+    uint64_t *bars = reinterpret_cast<uint64_t *>(rowoff + BM);
+    uint64_t *full = bars, *empty = bars + S, *tfull = bars + 2 * S, *tempty = bars + 2 * S + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t mtiles = (a.rows + BM - 1) / BM, ntiles = mtiles * nbn;
+
+    // the weight matrix, once (zero past K), and the bias
+    for (int e = tid; e < a.N * KB * 8; e += RS_THREADS) {
+        const int n = e / (KB * 8), rem = e - n * (KB * 8), kb = rem >> 3, c = rem & 7;
+        const int k0 = kb * 64 + c * 8;
+        const bool ok = k0 < a.K;
+        cp_async16(smem_u32(sB) + (uint32_t)kb * (uint32_t)(a.N * 128) + sw128_offset(n, c),
+                   ok ? a.Bw + (int64_t)n * a.K + k0 : a.Bw, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+    for (int n = tid; n < a.N; n += RS_THREADS) sbias[n] = a.bias ? __bfloat162float(a.bias[n]) : 0.f;
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), LOAD == LOAD_GATHER ? 32 * RS_NPROD : 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tfull[b]), 1);
+            mbar_init(smem_u32(&tempty[b]), RS_NEPI);
+        }
+        mbar_init_fence();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tslot), pl.tcols);
+        tmem_relinquish();
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t half_cols = pl.tcols / 2;
+    bool failed = false;
+
+    if (warp == 0 || warp >= 2 + RS_NEPI) {
+        // ---------------- producer(s) ----------------
+        const int pw = warp == 0 ? 0 : warp - (1 + RS_NEPI); // 0..RS_NPROD-1
+        int64_t it = 0;
+        if (LOAD == LOAD_PLAIN) {
+            if (warp == 0 && lane == 0) {
+                for (int64_t t = blockIdx.x; t < ntiles && !failed; t += gridDim.x) {
+                    const int64_t m0 = (t / nbn) * BM;
+                    for (int kb = 0; kb < KB; ++kb, ++it) {
+                        const int s = (int)(it % S);
+                        if (!mbar_wait(smem_u32(&empty[s]), (uint32_t)((it / S) & 1) ^ 1u, st.wait_ns)) {
+                            failed = true;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(smem_u32(&full[s]), RS_STAGE);
+                        tma_load_2d(smem_u32(sA + (size_t)s * RS_STAGE), &tmA, kb * 64, (int)m0, smem_u32(&full[s]));
+                    }
+                }
+            }
+        } else {
+            for (int64_t t = blockIdx.x; t < ntiles && !failed; t += gridDim.x) {
+                const int64_t m0 = (t / nbn) * BM;
+                // this warp's rows of the tile (BM / RS_NPROD of them): source
+                // offsets (32-bit index map when it fits) into shared memory
+                constexpr int RPW = BM / RS_NPROD;
+                const bool small = a.g.T < ((int64_t)1 << 31);
+                int64_t *myoff = rowoff + RPW * pw;
+                __syncwarp();
+                if (lane < RPW) {
+                    const int64_t R = m0 + RPW * pw + lane;
+                    const int64_t tok = R >= a.rows ? -1
+                                        : small     ? (int64_t)window_row_to_token32(a.g, (int)R)
+                                                    : window_row_to_token(a.g, R);
+                    myoff[lane] = tok < 0 ? -1 : tok * a.K;
+                }
+                __syncwarp();
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = (int)(it % S);
+                    if (!mbar_wait(smem_u32(&empty[s]), (uint32_t)((it / S) & 1) ^ 1u, st.wait_ns)) {
+                        failed = true;
+                        break;
+                    }
+                    const uint32_t dst = smem_u32(sA + (size_t)s * RS_STAGE);
+                    // eight lanes per row (one 128-byte line), four rows per
+                    // instruction; 16-byte chunks past K are never read by the MMAs
+                    const int c = lane & 7, k0 = kb * 64 + c * 8;
+                    if (k0 < a.K) {
+#pragma unroll
+                        for (int j = 0; j < RPW / 4; ++j) {
+                            const int rl = 4 * j + (lane >> 3);
+                            const int64_t off = myoff[rl];
+                            cp_async16(dst + sw128_offset(RPW * pw + rl, c), off >= 0 ? a.A + off + k0 : a.A,
+                                       off >= 0 ? 16u : 0u);
+                        }
+                    }
+                    cp_async_commit();
+                    if (it >= RS_DEPTH) {
+                        cp_async_wait<RS_DEPTH>();
+                        fence_proxy_async_smem();
+                        mbar_arrive(smem_u32(&full[(it - RS_DEPTH) % S]));
+                    }
+                }
+            }
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            if (!failed)
+                for (int64_t j = it - RS_DEPTH < 0 ? 0 : it - RS_DEPTH; j < it; ++j) mbar_arrive(smem_u32(&full[j % S]));
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(BM, BN);
+            int64_t it = 0, lt = 0;
+            for (int64_t t = blockIdx.x; t < ntiles && !failed; t += gridDim.x, ++lt) {
+                const int buf = (int)(lt & 1);
+                if (!mbar_wait(smem_u32(&tempty[buf]), (uint32_t)((lt >> 1) & 1) ^ 1u, st.wait_ns)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)buf * half_cols;
+                const uint32_t b_col = (uint32_t)(t % nbn) * (uint32_t)BN * 128u;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = (int)(it % S);
+                    if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((it / S) & 1), st.wait_ns)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sA + (size_t)s * RS_STAGE);
+                    const uint32_t b_base = smem_u32(sB) + (uint32_t)kb * (uint32_t)(a.N * 128) + b_col;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (kb * 64 + k * 16 < a.K)
+                            mma_bf16(d, desc_kmajor_sw128(a_base + 32 * k), desc_kmajor_sw128(b_base + 32 * k), idesc,
+                                     (kb | k) != 0);
+                    mma_commit(smem_u32(&empty[s]));
+                }
+                if (failed) break;
+                mma_commit(smem_u32(&tfull[buf]));
+            }
+        }
+    } else {
+        // ---------------- epilogue ----------------
+        const int quad = warp & 3, half = (warp - 2) >> 2;
+        const int r = quad * 32 + lane;
+        const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+        const int nchunks = BN / 32;
+        int64_t lt = 0;
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+            const int buf = (int)(lt & 1);
+            if (!mbar_wait(smem_u32(&tfull[buf]), (uint32_t)((lt >> 1) & 1), st.wait_ns)) {
+                failed = true;
+                break;
+            }
+            tc_fence_after();
+            const int64_t R = (t / nbn) * BM + r;
+            const int n0 = (int)(t % nbn) * BN;
+            bf16 *dst_row = nullptr;
+            if (R < a.rows) {
+                if (STORE == STORE_SCATTER) dst_row = a.D + window_row_to_token(a.g, R) * (int64_t)a.N + n0;
+                else dst_row = a.D + R * a.ldd + n0;
+            }
+            const uint32_t tb = t_lane + (uint32_t)buf * half_cols;
+            for (int ci = half; ci < nchunks; ci += 2) {
+                float v[32];
+                tmem_ld32(tb + 32 * ci, v);
+                tmem_wait_ld();
+                if (dst_row)
+                    rs_epilogue_chunk32(a, R, n0 + 32 * ci, dst_row + 32 * ci, v, sbias + n0 + 32 * ci,
+                                        n0 + 32 * ci < a.norm_cols);
+            }
+            if ((BN & 31) && (nchunks & 1) == half) { // 16-column tail
+                const int c0 = 32 * nchunks;
+                float v[16];
+                tmem_ld16(tb + c0, v);
+                tmem_wait_ld();
+                if (dst_row) {
+                    if (a.epi == EPI_NONE) {
+                        store_row_bf16(dst_row + c0, v, sbias + n0 + c0, 16);
+                    } else {
+                        float e[16], zero[16];
+                        epilogue_op(a, R, n0 + c0, v, sbias + n0 + c0, e, 16);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) zero[i] = 0.f;
+                        store_row_bf16(dst_row + c0, e, zero, 16);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+        }
+    }
+    if (failed && lane == 0) atomicOr(st.err, ERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, pl.tcols);
+}
+
+// The resident-weight plan, or false when the weights (or two accumulators)
+// do not fit: N a multiple of 16, one tile column of N <= 256 or two halves,
+// the V2 normalisation's 32-column chunks whole, Bw within 140 KB.
+bool rs_plan(const GemmArgs &a, RsPlan &p)
+{
+    if (a.N <= 0 || a.N % 16 || a.N > 512 || a.K <= 0 || a.K % 16) return false;
+    p.nbn = a.N <= 256 ? 1 : 2;
+    p.BN = a.N / p.nbn;
+    if (p.BN % 16 || (a.norm_cols > 0 && p.BN % 32)) return false;
+    if (a.epi == EPI_RESID && ((a.ldr % 8) || (reinterpret_cast<uintptr_t>(a.R) & 15))) return false;
+    p.KB = (a.K + 63) / 64;
+    p.b_bytes = (size_t)a.N * p.KB * 128;
+    if (p.b_bytes > 140 * 1024) return false;
+    const size_t fixed = 1024 + p.b_bytes + 512 * 4 + BM * 8 + 256;
+    p.stages = (int)((227 * 1024 - fixed) / RS_STAGE);
+    if (p.stages > 8) p.stages = 8;
+    if (p.stages < RS_DEPTH + 1) return false; // the gathered producer keeps RS_DEPTH stages in flight
+    p.tcols = 2 * p.BN <= 256 ? 256 : 512;
+    p.smem = fixed + (size_t)p.stages * RS_STAGE;
+    return true;
+}
+
+template <int LOAD, int STORE>
+cudaError_t launch_rs(const GemmArgs &a, const RsPlan &pl, DeviceStatus st, cudaStream_t stream)
+{
+    CUtensorMap tmA;
+    memset(&tmA, 0, sizeof(tmA));
+    if (LOAD == LOAD_PLAIN) {
+        if ((a.lda * 2) % 16 || (reinterpret_cast<uintptr_t>(a.A) & 15)) return cudaErrorInvalidValue;
+        cudaError_t e = make_tensor_map_sw128(&tmA, a.A, a.rows, a.K, a.lda, BM);
+        if (e != cudaSuccess) return e;
+    }
+    auto kern = gemm_rs_kernel<LOAD, STORE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    if (e != cudaSuccess) return e;
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
+    }
+    const int64_t ntiles = (a.rows + BM - 1) / BM * pl.nbn;
+    const unsigned grid = (unsigned)(ntiles < sms ? ntiles : sms);
+    kern<<<grid, RS_THREADS, pl.smem, stream>>>(a, pl, st, tmA);
+    return cudaGetLastError();
 }
 
 // Largest N tile <= 128 that divides N and is a multiple of `step` (16, or
@@ -564,6 +900,12 @@ cudaError_t launch_gemm_ts_test(const GemmArgs &a, DeviceStatus st, cudaStream_t
 
 cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, DeviceStatus st, cudaStream_t stream)
 {
+    RsPlan pl;
+    if (a.rows > 0 && rs_plan(a, pl)) {
+        if (load_mode == LOAD_GATHER && store_mode == STORE_PLAIN) return launch_rs<LOAD_GATHER, STORE_PLAIN>(a, pl, st, stream);
+        if (load_mode == LOAD_PLAIN && store_mode == STORE_SCATTER) return launch_rs<LOAD_PLAIN, STORE_SCATTER>(a, pl, st, stream);
+        if (load_mode == LOAD_PLAIN && store_mode == STORE_PLAIN) return launch_rs<LOAD_PLAIN, STORE_PLAIN>(a, pl, st, stream);
+    }
     if (load_mode == LOAD_GATHER && store_mode == STORE_PLAIN) return launch_impl<LOAD_GATHER, STORE_PLAIN>(a, st, stream);
     if (load_mode == LOAD_PLAIN && store_mode == STORE_SCATTER) return launch_impl<LOAD_PLAIN, STORE_SCATTER>(a, st, stream);
     if (load_mode == LOAD_PLAIN && store_mode == STORE_PLAIN) return launch_impl<LOAD_PLAIN, STORE_PLAIN>(a, st, stream);
