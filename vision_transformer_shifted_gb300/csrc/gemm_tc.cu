@@ -353,7 +353,7 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
     for (int n = tid; n < a.N; n += RS_THREADS) sbias[n] = a.bias ? __bfloat162float(a.bias[n]) : 0.f;
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&full[s]), LOAD == LOAD_GATHER ? 32 * RS_NPROD : 1);
+            mbar_init(smem_u32(&full[s]), LOAD == LOAD_GATHER ? RS_NPROD : 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -413,7 +413,9 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
                 __syncwarp();
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = (int)(it % S);
-                    if (!mbar_wait(smem_u32(&empty[s]), (uint32_t)((it / S) & 1) ^ 1u, st.wait_ns)) {
+                    // warp-uniform outcome: the lanes meet at __syncwarp below
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(smem_u32(&empty[s]), (uint32_t)((it / S) & 1) ^ 1u, st.wait_ns))) {
                         failed = true;
                         break;
                     }
@@ -432,15 +434,18 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
                     }
                     cp_async_commit();
                     if (it >= RS_DEPTH) {
+                        // every lane's copies of that stage have landed: one arrival per warp
                         cp_async_wait<RS_DEPTH>();
                         fence_proxy_async_smem();
-                        mbar_arrive(smem_u32(&full[(it - RS_DEPTH) % S]));
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&full[(it - RS_DEPTH) % S]));
                     }
                 }
             }
             cp_async_wait<0>();
             fence_proxy_async_smem();
-            if (!failed)
+            __syncwarp();
+            if (!failed && lane == 0)
                 for (int64_t j = it - RS_DEPTH < 0 ? 0 : it - RS_DEPTH; j < it; ++j) mbar_arrive(smem_u32(&full[j % S]));
         }
     } else if (warp == 1) {
