@@ -104,9 +104,15 @@ int swin_wattn_forward(swin_wattn_t h, const void *x, int B, int H, int W, const
                        const void *Wproj, const void *bproj, void *out, swin_stream_t stream);
 
 /* The same forward with x and out in HOST memory (pinned memory gives
- * asynchronous copies).  On `stream`: copy x host->device into a buffer the
- * handle owns, run the forward, copy the result device->host into out_host.
- * The weights, biases, table and logit_scale are device pointers, as in
+ * asynchronous copies).  The batch is cut into up to 8 chunks of whole images
+ * (windows never cross images, so each chunk is an exact forward of its
+ * images), and each chunk is copied host->device into a buffer the handle
+ * owns, run, and copied device->host into out_host; the three steps of
+ * different chunks overlap on three streams the handle owns, so the two copy
+ * directions and the kernels run at the same time.  The call is ordered on
+ * `stream` as if it ran there: the handle's streams wait for the work already
+ * on `stream`, and `stream` waits for the last chunk's copy back.  The
+ * weights, biases, table and logit_scale are device pointers, as in
  * swin_wattn_forward.  Returns once the work is enqueued; synchronise the
  * stream before reading out_host.  Errors as swin_wattn_forward, plus ENOMEM
  * when the staging buffers cannot be allocated. */

@@ -29,6 +29,11 @@ struct swin_wattn_s {
     size_t bws_bytes;
     cublasHandle_t blas;
     int bw_launches;
+    // chunked host-buffer forward: copy-in, compute and copy-out streams and
+    // their events (created on first use)
+    cudaStream_t hs[3];
+    cudaEvent_t ev_in[8], ev_run[8], ev_fork, ev_join;
+    bool hs_ready;
 };
 
 namespace {
@@ -214,6 +219,15 @@ int swin_wattn_destroy(swin_wattn_t h)
     if (h->stage_out) cudaFree(h->stage_out);
     if (h->bws) cudaFree(h->bws);
     if (h->blas) cublasDestroy(h->blas);
+    if (h->hs_ready) {
+        for (cudaStream_t st : h->hs) cudaStreamDestroy(st);
+        for (int c = 0; c < 8; ++c) {
+            cudaEventDestroy(h->ev_in[c]);
+            cudaEventDestroy(h->ev_run[c]);
+        }
+        cudaEventDestroy(h->ev_fork);
+        cudaEventDestroy(h->ev_join);
+    }
     if (h->d_err) cudaFree(h->d_err);
     delete h;
     return SWIN_WATTN_OK;
@@ -245,10 +259,50 @@ int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, in
         h->stage_bytes = bytes;
     }
     cudaStream_t s = (cudaStream_t)stream;
-    if (cudaMemcpyAsync(h->stage_x, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
-    rc = run_forward(h, h->stage_x, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, h->stage_out, s);
-    if (rc) return rc;
-    if (cudaMemcpyAsync(out_host, h->stage_out, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    if (!h->hs_ready) {
+        bool ok = true;
+        for (cudaStream_t &st : h->hs) ok = ok && cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess;
+        for (int c = 0; c < 8; ++c) {
+            ok = ok && cudaEventCreateWithFlags(&h->ev_in[c], cudaEventDisableTiming) == cudaSuccess;
+            ok = ok && cudaEventCreateWithFlags(&h->ev_run[c], cudaEventDisableTiming) == cudaSuccess;
+        }
+        ok = ok && cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) == cudaSuccess;
+        ok = ok && cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) { cudaGetLastError(); return SWIN_WATTN_ECUDA; }
+        h->hs_ready = true;
+    }
+    cudaStream_t s_in = h->hs[0], s_run = h->hs[1], s_out = h->hs[2];
+    // fork: the handle's streams start after the work already on the caller's
+    // stream and after the previous call's last copy back (the staging buffers
+    // are reused even when calls come on different streams)
+    if (cudaEventRecord(h->ev_fork, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    for (cudaStream_t st : h->hs)
+        if (cudaStreamWaitEvent(st, h->ev_fork, 0) != cudaSuccess || cudaStreamWaitEvent(st, h->ev_join, 0) != cudaSuccess)
+            return SWIN_WATTN_ECUDA;
+    const int nchunks = B < 8 ? B : 8;
+    const size_t img = bytes / (size_t)B;
+    int launches = 0;
+    for (int c = 0; c < nchunks; ++c) {
+        const int b0 = (int)((int64_t)B * c / nchunks), b1 = (int)((int64_t)B * (c + 1) / nchunks);
+        const size_t off = img * (size_t)b0, len = img * (size_t)(b1 - b0);
+        if (cudaMemcpyAsync((char *)h->stage_x + off, (const char *)x_host + off, len, cudaMemcpyHostToDevice,
+                            s_in) != cudaSuccess ||
+            cudaEventRecord(h->ev_in[c], s_in) != cudaSuccess || cudaStreamWaitEvent(s_run, h->ev_in[c], 0) != cudaSuccess)
+            return SWIN_WATTN_ECUDA;
+        rc = run_forward(h, (char *)h->stage_x + off, b1 - b0, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj,
+                         (char *)h->stage_out + off, s_run);
+        if (rc) return rc;
+        launches += h->last_launches;
+        if (cudaEventRecord(h->ev_run[c], s_run) != cudaSuccess || cudaStreamWaitEvent(s_out, h->ev_run[c], 0) != cudaSuccess ||
+            cudaMemcpyAsync((char *)out_host + off, (const char *)h->stage_out + off, len, cudaMemcpyDeviceToHost,
+                            s_out) != cudaSuccess)
+            return SWIN_WATTN_ECUDA;
+    }
+    h->last_launches = launches;
+    // join: the caller's stream continues after the last copy back (which
+    // follows every chunk's compute, and the copy-ins precede those)
+    if (cudaEventRecord(h->ev_join, s_out) != cudaSuccess || cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess)
+        return SWIN_WATTN_ECUDA;
     return SWIN_WATTN_OK;
 }
 
