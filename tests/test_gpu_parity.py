@@ -321,6 +321,43 @@ def test_forward_host_matches_device_forward():
     assert torch.equal(out_host, dev_out.cpu())
 
 
+@pytest.mark.parametrize("path", [sw.PATH_AUTO, sw.PATH_THREE_KERNELS])
+def test_forward_host_repeated_calls(path):
+    """The host-buffer forward is pipelined in image chunks and replayed from a
+    captured graph while its arguments stay the same: new contents in the same
+    buffers, a different batch size and device forwards in between (which
+    reallocate the workspace) must all give the device forward's result."""
+    base = WORKLOADS["swin_t_s1"].with_(H=14, W=21)
+    h = sw.swin_wattn_create(base.C, base.heads, base.M, base.shift, base.mode)
+    try:
+        if path:
+            sw.swin_wattn_set_option(h, sw.OPT_PATH, path)
+        bufs = {}
+        for B, seed in ((9, 1), (9, 2), (9, 3), (3, 4), (9, 5), (17, 6), (9, 7)):
+            w = base.with_(B=B, seed=base.seed + seed)
+            g = generate(w, nonzero_bias=True)
+            t = device_inputs(g)
+            dev_out = run_forward(w, t, t["table"], path)
+            if B not in bufs:
+                bufs[B] = (g["x"].pin_memory(), torch.empty_like(g["x"]).pin_memory())
+            x_host, out_host = bufs[B]
+            x_host.copy_(g["x"])   # the same host buffers again, new contents
+            out_host.fill_(float("nan"))
+            sw.swin_wattn_forward_host(h, x_host, t["Wqkv"], t["bqkv"], t["table"], None, t["Wproj"], t["bproj"],
+                                       out_host)
+            assert sw.swin_wattn_sync_status(h) == sw.OK
+            assert torch.equal(out_host, dev_out.cpu()), (B, seed)
+            # a device forward on a larger grid with the same handle between
+            # host calls (the three-kernel path grows its workspace)
+            big = base.with_(B=B + 8)
+            gb = device_inputs(generate(big))
+            ob = torch.empty_like(gb["x"])
+            sw.swin_wattn_forward(h, gb["x"], gb["Wqkv"], gb["bqkv"], gb["table"], None, gb["Wproj"], gb["bproj"], ob)
+            assert sw.swin_wattn_sync_status(h) == sw.OK
+    finally:
+        sw.swin_wattn_destroy(h)
+
+
 def test_empty_batch_is_a_no_op():
     w = WORKLOADS["swin_t_s1"]
     h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)

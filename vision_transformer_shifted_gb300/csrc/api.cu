@@ -32,8 +32,13 @@ struct swin_wattn_s {
     // chunked host-buffer forward: copy-in, compute and copy-out streams and
     // their events (created on first use)
     cudaStream_t hs[3];
-    cudaEvent_t ev_in[8], ev_run[8], ev_fork, ev_join;
+    cudaEvent_t ev_in[8], ev_run[8], ev_fork, ev_join, ev_done;
     bool hs_ready;
+    // the chunked pipeline captured as a CUDA graph, replayed while the call's
+    // arguments stay the same
+    cudaGraphExec_t graph;
+    const void *g_args[11];   // the call's pointers and the buffers the graph uses
+    int g_B, g_H, g_W, g_path, g_launches;
 };
 
 namespace {
@@ -181,6 +186,48 @@ cublasStatus_t weight_grad(cublasHandle_t blas, const bf16 *G, int n_out, const 
                         CUDA_R_16BF, n_out, &zero, D, CUDA_R_32F, n_in, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
 }
 
+// The chunked host-buffer forward on `s` (the body of swin_wattn_forward_host):
+// up to 8 chunks of whole images; copy-in, compute and copy-out of different
+// chunks overlap on the handle's three streams, forked from and joined back
+// into `s`.  `direct`: also wait for the previous direct call's last copy.
+int enqueue_host_chunks(swin_wattn_s *h, const void *x_host, int B, int H, int W, const void *Wqkv, const void *bqkv,
+                        const void *table, const float *tau, const void *Wproj, const void *bproj, void *out_host,
+                        cudaStream_t s, bool direct)
+{
+    const size_t bytes = (size_t)B * H * W * h->C * elem_bytes(h);
+    cudaStream_t s_in = h->hs[0], s_run = h->hs[1], s_out = h->hs[2];
+    if (cudaEventRecord(h->ev_fork, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    for (cudaStream_t st : h->hs) {
+        if (cudaStreamWaitEvent(st, h->ev_fork, 0) != cudaSuccess) return SWIN_WATTN_ECUDA;
+        if (direct && cudaStreamWaitEvent(st, h->ev_join, 0) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    }
+    const int nchunks = B < 8 ? B : 8;
+    const size_t img = bytes / (size_t)B;
+    int launches = 0;
+    for (int c = 0; c < nchunks; ++c) {
+        const int b0 = (int)((int64_t)B * c / nchunks), b1 = (int)((int64_t)B * (c + 1) / nchunks);
+        const size_t off = img * (size_t)b0, len = img * (size_t)(b1 - b0);
+        if (cudaMemcpyAsync((char *)h->stage_x + off, (const char *)x_host + off, len, cudaMemcpyHostToDevice,
+                            s_in) != cudaSuccess ||
+            cudaEventRecord(h->ev_in[c], s_in) != cudaSuccess || cudaStreamWaitEvent(s_run, h->ev_in[c], 0) != cudaSuccess)
+            return SWIN_WATTN_ECUDA;
+        const int rc = run_forward(h, (char *)h->stage_x + off, b1 - b0, H, W, Wqkv, bqkv, table, tau, Wproj, bproj,
+                                   (char *)h->stage_out + off, s_run);
+        if (rc) return rc;
+        launches += h->last_launches;
+        if (cudaEventRecord(h->ev_run[c], s_run) != cudaSuccess || cudaStreamWaitEvent(s_out, h->ev_run[c], 0) != cudaSuccess ||
+            cudaMemcpyAsync((char *)out_host + off, (const char *)h->stage_out + off, len, cudaMemcpyDeviceToHost,
+                            s_out) != cudaSuccess)
+            return SWIN_WATTN_ECUDA;
+    }
+    h->last_launches = launches;
+    // join: every stream's last work leads into s (the copy-ins precede the
+    // computes, which precede the last copy-out)
+    if (cudaEventRecord(h->ev_join, s_out) != cudaSuccess || cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess)
+        return SWIN_WATTN_ECUDA;
+    return SWIN_WATTN_OK;
+}
+
 } // namespace
 
 extern "C" {
@@ -227,7 +274,9 @@ int swin_wattn_destroy(swin_wattn_t h)
         }
         cudaEventDestroy(h->ev_fork);
         cudaEventDestroy(h->ev_join);
+        cudaEventDestroy(h->ev_done);
     }
+    if (h->graph) cudaGraphExecDestroy(h->graph);
     if (h->d_err) cudaFree(h->d_err);
     delete h;
     return SWIN_WATTN_OK;
@@ -268,42 +317,70 @@ int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, in
         }
         ok = ok && cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) == cudaSuccess;
         ok = ok && cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) == cudaSuccess;
+        ok = ok && cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) == cudaSuccess;
         if (!ok) { cudaGetLastError(); return SWIN_WATTN_ECUDA; }
         h->hs_ready = true;
     }
-    cudaStream_t s_in = h->hs[0], s_run = h->hs[1], s_out = h->hs[2];
-    // fork: the handle's streams start after the work already on the caller's
-    // stream and after the previous call's last copy back (the staging buffers
-    // are reused even when calls come on different streams)
-    if (cudaEventRecord(h->ev_fork, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
-    for (cudaStream_t st : h->hs)
-        if (cudaStreamWaitEvent(st, h->ev_fork, 0) != cudaSuccess || cudaStreamWaitEvent(st, h->ev_join, 0) != cudaSuccess)
-            return SWIN_WATTN_ECUDA;
-    const int nchunks = B < 8 ? B : 8;
-    const size_t img = bytes / (size_t)B;
-    int launches = 0;
-    for (int c = 0; c < nchunks; ++c) {
-        const int b0 = (int)((int64_t)B * c / nchunks), b1 = (int)((int64_t)B * (c + 1) / nchunks);
-        const size_t off = img * (size_t)b0, len = img * (size_t)(b1 - b0);
-        if (cudaMemcpyAsync((char *)h->stage_x + off, (const char *)x_host + off, len, cudaMemcpyHostToDevice,
-                            s_in) != cudaSuccess ||
-            cudaEventRecord(h->ev_in[c], s_in) != cudaSuccess || cudaStreamWaitEvent(s_run, h->ev_in[c], 0) != cudaSuccess)
-            return SWIN_WATTN_ECUDA;
-        rc = run_forward(h, (char *)h->stage_x + off, b1 - b0, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj,
-                         (char *)h->stage_out + off, s_run);
-        if (rc) return rc;
-        launches += h->last_launches;
-        if (cudaEventRecord(h->ev_run[c], s_run) != cudaSuccess || cudaStreamWaitEvent(s_out, h->ev_run[c], 0) != cudaSuccess ||
-            cudaMemcpyAsync((char *)out_host + off, (const char *)h->stage_out + off, len, cudaMemcpyDeviceToHost,
-                            s_out) != cudaSuccess)
-            return SWIN_WATTN_ECUDA;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    if (cap != cudaStreamCaptureStatusNone)
+        // the caller is capturing this stream: enqueue into its capture
+        return enqueue_host_chunks(h, x_host, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out_host, s,
+                                   false);
+    // the previous call (on whatever stream) has finished with the staging buffers
+    if (cudaStreamWaitEvent(s, h->ev_done, 0) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    // the three-kernel path's workspace for the largest chunk, before any
+    // capture (no allocation may happen inside one)
+    {
+        const int nchunks = B < 8 ? B : 8, bmax = (B + nchunks - 1) / nchunks;
+        const int64_t Tc = (int64_t)bmax * H * W;
+        const int path = h->path_opt ? h->path_opt : choose_path(h, Tc);
+        if (!h->fp32 && path == 1) {
+            rc = ensure_buffer(&h->ws, &h->ws_bytes, (size_t)Tc * 4 * h->C * 2);
+            if (rc) return rc;
+        }
     }
-    h->last_launches = launches;
-    // join: the caller's stream continues after the last copy back (which
-    // follows every chunk's compute, and the copy-ins precede those)
-    if (cudaEventRecord(h->ev_join, s_out) != cudaSuccess || cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess)
-        return SWIN_WATTN_ECUDA;
-    return SWIN_WATTN_OK;
+    // the graph bakes in the call's pointers and the handle's buffers (a forward
+    // on device buffers may have reallocated the workspace since)
+    const void *args[11] = {x_host, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out_host,
+                            h->ws, h->stage_x, h->stage_out};
+    bool same = h->graph && h->g_B == B && h->g_H == H && h->g_W == W && h->g_path == h->path_opt;
+    for (int i = 0; i < 11 && same; ++i) same = h->g_args[i] == args[i];
+    if (!same) {
+        if (h->graph) {
+            cudaGraphExecDestroy(h->graph);
+            h->graph = nullptr;
+        }
+        cudaGraph_t graph = nullptr;
+        cudaError_t ce = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+        if (ce == cudaSuccess) {
+            // (the legacy default stream cannot be captured: direct enqueue below)
+            rc = enqueue_host_chunks(h, x_host, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out_host,
+                                     s, false);
+            ce = cudaStreamEndCapture(s, &graph);
+        }
+        if (rc == SWIN_WATTN_OK && ce == cudaSuccess && graph && args[8] == h->ws &&
+            cudaGraphInstantiate(&h->graph, graph, 0) == cudaSuccess) {
+            h->g_B = B; h->g_H = H; h->g_W = W; h->g_path = h->path_opt;
+            for (int i = 0; i < 11; ++i) h->g_args[i] = args[i];
+            h->g_launches = h->last_launches;
+        } else {
+            h->graph = nullptr;
+        }
+        if (graph) cudaGraphDestroy(graph);
+        cudaGetLastError();
+        if (!h->graph) {
+            // capture refused (e.g. the three-kernel workspace had to be
+            // allocated first): enqueue directly; the next call captures
+            rc = enqueue_host_chunks(h, x_host, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out_host,
+                                     s, true);
+            if (rc) return rc;
+            return cudaEventRecord(h->ev_done, s) == cudaSuccess ? SWIN_WATTN_OK : SWIN_WATTN_ECUDA;
+        }
+    }
+    if (cudaGraphLaunch(h->graph, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    h->last_launches = h->g_launches;
+    return cudaEventRecord(h->ev_done, s) == cudaSuccess ? SWIN_WATTN_OK : SWIN_WATTN_ECUDA;
 }
 
 int swin_wattn_cpb_table(swin_wattn_t h, const float *W1, const float *b1, const float *W2, int hidden, void *table,
