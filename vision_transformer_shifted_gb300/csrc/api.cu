@@ -12,6 +12,9 @@
 
 using namespace swin;
 
+// Chunks of whole images of the pipelined host-buffer forward (at most).
+constexpr int HOST_CHUNKS = 8;
+
 struct swin_wattn_s {
     int C, heads, d, M, shift, mode;
     bool fp32;
@@ -32,7 +35,7 @@ struct swin_wattn_s {
     // chunked host-buffer forward: copy-in, compute and copy-out streams and
     // their events (created on first use)
     cudaStream_t hs[3];
-    cudaEvent_t ev_in[8], ev_run[8], ev_fork, ev_join, ev_done;
+    cudaEvent_t ev_in[HOST_CHUNKS], ev_run[HOST_CHUNKS], ev_fork, ev_join, ev_done;
     bool hs_ready;
     // the chunked pipeline captured as a CUDA graph, replayed while the call's
     // arguments stay the same
@@ -187,7 +190,7 @@ cublasStatus_t weight_grad(cublasHandle_t blas, const bf16 *G, int n_out, const 
 }
 
 // The chunked host-buffer forward on `s` (the body of swin_wattn_forward_host):
-// up to 8 chunks of whole images; copy-in, compute and copy-out of different
+// up to HOST_CHUNKS chunks of whole images; copy-in, compute and copy-out of different
 // chunks overlap on the handle's three streams, forked from and joined back
 // into `s`.  `direct`: also wait for the previous direct call's last copy.
 int enqueue_host_chunks(swin_wattn_s *h, const void *x_host, int B, int H, int W, const void *Wqkv, const void *bqkv,
@@ -201,7 +204,7 @@ int enqueue_host_chunks(swin_wattn_s *h, const void *x_host, int B, int H, int W
         if (cudaStreamWaitEvent(st, h->ev_fork, 0) != cudaSuccess) return SWIN_WATTN_ECUDA;
         if (direct && cudaStreamWaitEvent(st, h->ev_join, 0) != cudaSuccess) return SWIN_WATTN_ECUDA;
     }
-    const int nchunks = B < 8 ? B : 8;
+    const int nchunks = B < HOST_CHUNKS ? B : HOST_CHUNKS;
     const size_t img = bytes / (size_t)B;
     int launches = 0;
     for (int c = 0; c < nchunks; ++c) {
@@ -268,7 +271,7 @@ int swin_wattn_destroy(swin_wattn_t h)
     if (h->blas) cublasDestroy(h->blas);
     if (h->hs_ready) {
         for (cudaStream_t st : h->hs) cudaStreamDestroy(st);
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < HOST_CHUNKS; ++c) {
             cudaEventDestroy(h->ev_in[c]);
             cudaEventDestroy(h->ev_run[c]);
         }
@@ -311,7 +314,7 @@ int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, in
     if (!h->hs_ready) {
         bool ok = true;
         for (cudaStream_t &st : h->hs) ok = ok && cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess;
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < HOST_CHUNKS; ++c) {
             ok = ok && cudaEventCreateWithFlags(&h->ev_in[c], cudaEventDisableTiming) == cudaSuccess;
             ok = ok && cudaEventCreateWithFlags(&h->ev_run[c], cudaEventDisableTiming) == cudaSuccess;
         }
@@ -332,7 +335,7 @@ int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, in
     // the three-kernel path's workspace for the largest chunk, before any
     // capture (no allocation may happen inside one)
     {
-        const int nchunks = B < 8 ? B : 8, bmax = (B + nchunks - 1) / nchunks;
+        const int nchunks = B < HOST_CHUNKS ? B : HOST_CHUNKS, bmax = (B + nchunks - 1) / nchunks;
         const int64_t Tc = (int64_t)bmax * H * W;
         const int path = h->path_opt ? h->path_opt : choose_path(h, Tc);
         if (!h->fp32 && path == 1) {
