@@ -516,7 +516,8 @@ static EncodeTiledFn encode_fn()
 
 // Tensor map over a row-major bf16 matrix [rows, cols]: boxes of 32 columns x
 // box_rows rows, 64-byte swizzle, zero fill past the last row.
-cudaError_t make_tensor_map_sw64(CUtensorMap *map, const void *ptr, int64_t rows, int cols, int box_rows)
+cudaError_t make_tensor_map_sw64(CUtensorMap *map, const void *ptr, int64_t rows, int cols, int box_rows,
+                                 bool promote128)
 {
     const EncodeTiledFn encode = encode_fn();
     if (!encode) return cudaErrorNotSupported;
@@ -525,7 +526,8 @@ cudaError_t make_tensor_map_sw64(CUtensorMap *map, const void *ptr, int64_t rows
     const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
     const cuuint32_t elem[2] = {1, 1};
     CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, elem,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        promote128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

@@ -96,7 +96,9 @@ __global__ void colsum_kernel(const bf16 *in, int64_t rows, int N, float *out)
 // rowsum through shared memory, and store them as bf16 (block-diagonal: the
 // other window's block stays zero); then
 //   o = P v,  dq = dS k,  dv = P^T do,  dk = dS^T q   (M = 128, N = 32, K = 128)
-// with P^T and dS^T the same shared-memory tiles read M-major.  Cross-window
+// with P^T and dS^T the same shared-memory tiles read M-major (S and dP come
+// from two issuing threads, the four outputs from four, so that the MMAs'
+// issue costs overlap).  Cross-window
 // products vanish because the off-diagonal blocks are zero.  Units run head
 // by head (unit u: head u / pairs), so a CTA keeps one head's bias matrix in
 // shared memory and the table gradient of each (query, key) position in
@@ -185,8 +187,8 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
     for (int e = tid; e < 228; e += TB_THREADS) dtab[e] = 0.f;
     if (tid == 0) {
         mbar_init(bar_ld, 1);
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 2);
+        mbar_init(bar_s, 2);
+        mbar_init(bar_o, 4);
         mbar_init_fence();
     }
     if (warp == 0) {
@@ -267,18 +269,17 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
             const int rem = (int)(win % (g.nh * g.nw));
             cls = (rem / g.nw == g.nh - 1 ? 1 : 0) | (rem % g.nw == g.nw - 1 ? 2 : 0);
         }
-        if (tid == 0) {
+        if (tid == 0 || tid == 128) {
+            // S by thread 0, dP by thread 128 (their issue costs overlap)
             const bool okl = mbar_wait(bar_ld, phase, st.wait_ns);
             if (okl) {
                 tc_fence_after();
                 const uint32_t id = idesc_bf16(128, 128);
+                const uint32_t a = tid == 0 ? Ly::Q : Ly::DO, b = tid == 0 ? Ly::K : Ly::V;
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    mma_bf16(tmem, desc_kmajor_sw64(base + Ly::Q + 32 * ks), desc_kmajor_sw64(base + Ly::K + 32 * ks),
-                             id, ks);
-                    mma_bf16(tmem + 128, desc_kmajor_sw64(base + Ly::DO + 32 * ks),
-                             desc_kmajor_sw64(base + Ly::V + 32 * ks), id, ks);
-                }
+                for (int ks = 0; ks < 2; ++ks)
+                    mma_bf16(tmem + (tid == 0 ? 0 : 128), desc_kmajor_sw64(base + a + 32 * ks),
+                             desc_kmajor_sw64(base + b + 32 * ks), id, ks);
                 mma_commit(bar_s);
             }
         }
@@ -350,26 +351,24 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0 || tid == 128) {
+        if (lane == 0 && (warp & 2) == 0) {
+            // one issuer per output (warps 0, 1, 4, 5): o, dq, dk, dv
             tc_fence_after();
-            const uint32_t id_k = idesc_bf16_bmn(128, 32), id_m = idesc_bf16_amn_bmn(128, 32);
-            if (tid == 0) {
+            const int which = (warp & 1) | ((warp >> 2) << 1); // 0 o, 1 dq, 2 dk, 3 dv
+            if (which < 2) {
+                const uint32_t a = which == 0 ? Ly::P : Ly::DS, b = which == 0 ? Ly::V : Ly::K;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t kpan = (uint32_t)(kk >> 1) * 8192u + 32u * (kk & 1);
-                    mma_bf16(tmem + 0, desc_kmajor_sw64(base + Ly::P + kpan),
-                             desc_mnmajor_sw64(base + Ly::V + 1024 * kk, 8192), id_k, kk);
-                    mma_bf16(tmem + 32, desc_kmajor_sw64(base + Ly::DS + kpan),
-                             desc_mnmajor_sw64(base + Ly::K + 1024 * kk, 8192), id_k, kk);
+                    mma_bf16(tmem + 32 * which, desc_kmajor_sw64(base + a + kpan),
+                             desc_mnmajor_sw64(base + b + 1024 * kk, 8192), idesc_bf16_bmn(128, 32), kk);
                 }
             } else {
+                const uint32_t a = which == 2 ? Ly::DS : Ly::P, b = which == 2 ? Ly::Q : Ly::DO;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    mma_bf16(tmem + 64, desc_mnmajor_sw64(base + Ly::DS + 1024 * kk, 8192),
-                             desc_mnmajor_sw64(base + Ly::Q + 1024 * kk, 8192), id_m, kk);
-                    mma_bf16(tmem + 96, desc_mnmajor_sw64(base + Ly::P + 1024 * kk, 8192),
-                             desc_mnmajor_sw64(base + Ly::DO + 1024 * kk, 8192), id_m, kk);
-                }
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + 32 * which, desc_mnmajor_sw64(base + a + 1024 * kk, 8192),
+                             desc_mnmajor_sw64(base + b + 1024 * kk, 8192), idesc_bf16_amn_bmn(128, 32), kk);
             }
             mma_commit(bar_o);
         }
@@ -441,8 +440,10 @@ cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *ta
 {
     if (!attn_backward_supported(g.M, g.C, heads)) return cudaErrorInvalidValue;
     CUtensorMap tm_qkv, tm_do;
-    cudaError_t e = make_tensor_map_sw64(&tm_qkv, qkv, g.T, 3 * g.C, g.N);
-    if (e == cudaSuccess) e = make_tensor_map_sw64(&tm_do, dO, g.T, g.C, g.N);
+    // units run head by head: the other heads' 64-byte slices of a row are
+    // read much later, so no 128-byte L2 promotion
+    cudaError_t e = make_tensor_map_sw64(&tm_qkv, qkv, g.T, 3 * g.C, g.N, false);
+    if (e == cudaSuccess) e = make_tensor_map_sw64(&tm_do, dO, g.T, g.C, g.N, false);
     if (e != cudaSuccess) return e;
     const size_t smem = TbLayout::bytes();
     e = cudaFuncSetAttribute(attn_backward_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

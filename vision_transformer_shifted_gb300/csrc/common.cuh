@@ -154,8 +154,11 @@ cudaError_t launch_fused(const bf16 *x, const bf16 *Wqkv, const bf16 *bqkv, cons
 
 // Tensor map over a row-major bf16 matrix [rows, cols] (16-byte aligned base,
 // cols * 2 a multiple of 16): boxes of 32 columns x box_rows rows (<= 256),
-// 64-byte swizzle in shared memory, zero fill past the last row.
-cudaError_t make_tensor_map_sw64(CUtensorMap *map, const void *ptr, int64_t rows, int cols, int box_rows);
+// 64-byte swizzle in shared memory, zero fill past the last row.  L2 fetches
+// are promoted to 128 bytes, or kept at 64 (promote128 false) when the
+// neighbouring 64 bytes of a row are not read soon after.
+cudaError_t make_tensor_map_sw64(CUtensorMap *map, const void *ptr, int64_t rows, int cols, int box_rows,
+                                 bool promote128 = true);
 // Tensor map over a row-major bf16 matrix [rows, cols] with row stride ld
 // (elements): boxes of 64 columns x box_rows rows, 128-byte swizzle, zero
 // fill past the last row or column.
