@@ -15,18 +15,15 @@
 // the fp32 P.V result.  In V2 the QKV projection has already scaled every q
 // and k head to unit length, so q.k is the cosine.
 //
-// q, k and v rows (64 bytes per head) are copied with cp.async into
-// 64-byte-swizzled tiles; v is used in that [key][d] layout as an N-major B
-// operand, so no transpose is ever written.
-//
-// Small windows (N <= 64, e.g. M = 7 or 8): one CTA takes two windows of one
-// head; window A fills rows 0..63 and window B rows 64..127 of a 128-row MMA
-// tile, so QK^T is one 128x128x32 MMA whose off-diagonal blocks are ignored,
-// and P.V is one 128x32x128 MMA with P zero outside each row's own window.
-// Large windows (N > 64, e.g. M = 24, N = 576): one CTA of 256 threads takes
-// 128 queries of one window and head (two threads per query row, 64 keys
-// each) and walks the keys in double-buffered tiles of 128 with an online
-// softmax; P goes back into TMEM and P.V reads it from there.
+// Windows of at most 64 tokens (M = 7 or 8) go to the tcgen05 attention
+// kernel shared with the backward pass (csrc/backward.cu, forward mode: two
+// windows of one head per 128-row tile, TMA loads, P.V with P block-diagonal).
+// This file holds the large-window kernel (N > 64, e.g. M = 24, N = 576): one
+// CTA of 256 threads takes 128 queries of one window and head (two threads per
+// query row, 64 keys each) and walks the keys in double-buffered tiles of 128
+// loaded by 2-D TMA into 64-byte-swizzled tiles, with an online softmax; P goes
+// back into TMEM and P.V reads it from there, v used in its [key][d] layout as
+// an N-major B operand (no transpose is ever written).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -52,19 +49,6 @@ __device__ long long g_flash_trace[8 * 16];
     } while (0)
 #endif
 
-// Copies the 64-byte head slice of `rows` qkv rows (part 0 = q, 1 = k, 2 = v)
-// into a 64-byte-swizzled tile, zero rows where row_ok is false; each thread
-// handles chunk `tid & 3` of rows tid/4, tid/4 + nthreads/4, ...
-__device__ __forceinline__ void load_rows_sw64(uint32_t tile, int tid, int nthreads, int rows,
-                                               const bf16 *const *row_src, const bf16 *any_valid)
-{
-    for (int q = tid; q < rows * 4; q += nthreads) {
-        const int r = q >> 2, c = q & 3;
-        const bf16 *src = row_src[r];
-        cp_async16(tile + sw64_offset(r, c), src ? src + c * 8 : any_valid, src ? 16u : 0u);
-    }
-}
-
 // Region id (row band * 3 + column band) of in-window token (ti, tj) of
 // window (wi, wj); 0 everywhere when shift == 0.
 __device__ __forceinline__ int token_region(const Geom &g, int wi, int wj, int ti, int tj)
@@ -84,163 +68,6 @@ __device__ __forceinline__ void store_o(bf16 *dst, const float *o, float inv_l)
                            pack_bf16x2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l),
                            pack_bf16x2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l),
                            pack_bf16x2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l));
-}
-
-// ---------------------------------------------------------------------------
-// Two windows per CTA, N <= 64 (128 threads, one per tile row).
-// ---------------------------------------------------------------------------
-struct Pack2Smem {
-    static constexpr int q_off = 0;                    // [128][64 B] SW64
-    static constexpr int k_off = q_off + 128 * 64;
-    static constexpr int v_off = k_off + 128 * 64;     // [128 keys][64 B] SW64 (N-major B)
-    static constexpr int p_off = v_off + 128 * 64;     // 2 K blocks x [128][128 B] SW128
-    static constexpr int end = p_off + 2 * 128 * 128;
-    static size_t bytes(int M) { return 1024 + end + (size_t)(2 * M - 1) * (2 * M - 1) * 4 + 128 * 3 * 8 + 64; }
-};
-
-__global__ void __launch_bounds__(128) attn_pack2_kernel(AttnArgs a, DeviceStatus st)
-{
-    extern __shared__ uint8_t smem_raw[];
-    const Geom g = a.g;
-    const int M = g.M, N = g.N, C = g.C, L = 2 * M - 1;
-    uint8_t *sm = smem_align(smem_raw, 1024);
-    float *sbias = reinterpret_cast<float *>(sm + Pack2Smem::end);
-    const bf16 **srcs = reinterpret_cast<const bf16 **>(smem_align(reinterpret_cast<uint8_t *>(sbias + L * L), 8));
-    uint64_t *bar = reinterpret_cast<uint64_t *>(srcs + 3 * 128);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
-    const uint32_t sQ = smem_u32(sm + Pack2Smem::q_off), sK = smem_u32(sm + Pack2Smem::k_off),
-                   sV = smem_u32(sm + Pack2Smem::v_off);
-    uint8_t *sP = sm + Pack2Smem::p_off;
-    __shared__ int8_t key_region[2][64];
-    __shared__ int16_t key_off[64];
-
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int head = blockIdx.y;
-    const int slot = tid >> 6, t = tid & 63;
-    const int64_t win = 2 * (int64_t)blockIdx.x + slot;
-    const bool win_ok = win < g.nwin;
-    const bool row_ok = win_ok && t < N;
-    const int per = g.nh * g.nw;
-    const int rem = win_ok ? (int)(win % per) : 0;
-    const int wi = rem / g.nw, wj = rem % g.nw;
-    const int ti = t / M, tj = t % M;
-
-    // q, k, v rows of this thread's token (null for padding rows)
-    {
-        const bf16 *base = row_ok ? a.qkv + (win * N + t) * (int64_t)(3 * C) + head * 32 : nullptr;
-        srcs[tid] = base;
-        srcs[128 + tid] = base ? base + C : nullptr;
-        srcs[256 + tid] = base ? base + 2 * C : nullptr;
-    }
-    for (int i = tid; i < L * L; i += 128) sbias[i] = __bfloat162float(a.table[(int64_t)i * a.heads + head]) * LOG2E;
-    key_region[slot][t] = (int8_t)(t < N ? token_region(g, wi, wj, ti, tj) : -1);
-    if (slot == 0) key_off[t] = (int16_t)(ti * L + tj);
-    if (tid == 0) {
-        mbar_init(smem_u32(bar), 1);
-        mbar_init_fence();
-    }
-    if (warp == 0) {
-        tmem_alloc(smem_u32(tmem_slot), 128);
-        tmem_relinquish();
-    }
-    __syncthreads();
-    load_rows_sw64(sQ, tid, 128, 128, srcs, a.qkv);
-    load_rows_sw64(sK, tid, 128, 128, srcs + 128, a.qkv);
-    load_rows_sw64(sV, tid, 128, 128, srcs + 256, a.qkv);
-    cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t barp = smem_u32(bar);
-
-    if (tid == 0) {
-        const uint32_t id = idesc_bf16(128, 128);
-#pragma unroll
-        for (int k = 0; k < 2; ++k) mma_bf16(tmem, desc_kmajor_sw64(sQ + 32 * k), desc_kmajor_sw64(sK + 32 * k), id, k);
-        mma_commit(barp);
-    }
-    bool failed = !mbar_wait(barp, 0, st.wait_ns);
-    tc_fence_after();
-
-    // ---- softmax of this thread's row over its own window's 64 key columns ----
-    const float scale = a.mode == 1 ? LOG2E / fmaxf(a.tau[head], 0.01f) : LOG2E * rsqrtf(32.0f);
-    float l = 1.f;
-    {
-        float s[64];
-        const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(slot * 64);
-        {
-            float c0[32], c1[32];
-            tmem_ld32(t_row, c0);
-            tmem_ld32(t_row + 32, c1);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) { s[j] = c0[j]; s[32 + j] = c1[j]; }
-        }
-        const int my_region = key_region[slot][t];   // -1 for a padding row: nothing matches
-        const int tb = row_ok ? t : 0;                 // padding rows read a valid bias row
-        const int base = (tb / M + M - 1) * L + (tb % M + M - 1);
-        float mx = -INFINITY;
-        // branch-free over the lanes: every lane computes the logit and a select
-        // applies the mask (j < N is the same for the whole warp)
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-            float v = -INFINITY;
-            if (j < N) {
-                const float lv = fmaf(s[j], scale, sbias[base - key_off[j]]);
-                v = key_region[slot][j] == my_region ? lv : -INFINITY;
-            }
-            s[j] = v;
-            mx = fmaxf(mx, v);
-        }
-        if (!row_ok) mx = 0.f;
-        float sum = 0.f;
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-            const float p0 = ex2_approx(s[j] - mx), p1 = ex2_approx(s[j + 1] - mx);
-            sum += p0 + p1;
-            pk[j / 2] = pack_bf16x2(p0, p1);
-        }
-        l = sum;
-        // P row: own window's keys in K block `slot`, zeros in the other block
-        uint8_t *own = sP + slot * (128 * 128), *other = sP + (slot ^ 1) * (128 * 128);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            *reinterpret_cast<uint4 *>(own + sw128_offset(tid, c)) =
-                row_ok ? make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(other + sw128_offset(tid, c)) = make_uint4(0, 0, 0, 0);
-        }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(failed)) failed = true;
-    tc_fence_after();
-
-    if (!failed) {
-        if (tid == 0) {
-            const uint32_t id = idesc_bf16_bmn(128, 32);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int kb = k >> 2, ks = k & 3;
-                mma_bf16(tmem, desc_kmajor_sw128(smem_u32(sP) + kb * 16384 + 32 * ks),
-                         desc_mnmajor_sw64(sV + 1024 * k, 128 * 64), id, k);
-            }
-            mma_commit(barp);
-        }
-        failed = !mbar_wait(barp, 1, st.wait_ns);
-        tc_fence_after();
-        float o[32];
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), o);
-        tmem_wait_ld();
-        if (row_ok && !failed) store_o<32>(a.attn + (win * N + t) * (int64_t)C + head * 32, o, rcp_approx(l));
-    }
-    if (failed) atomicOr(st.err, ERR_TIMEOUT);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // ---------------------------------------------------------------------------
@@ -579,11 +406,7 @@ cudaError_t launch_attention(const AttnArgs &a, DeviceStatus st, cudaStream_t st
     const Geom &g = a.g;
     if (g.C != a.heads * 32) return cudaErrorInvalidValue;
     if (g.N <= 64) {
-        const size_t smem = Pack2Smem::bytes(g.M);
-        cudaError_t e = cudaFuncSetAttribute(attn_pack2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        dim3 grid((unsigned)((g.nwin + 1) / 2), (unsigned)a.heads);
-        attn_pack2_kernel<<<grid, 128, smem, stream>>>(a, st);
+        return launch_attn_forward_tc(a.qkv, a.table, a.tau, a.heads, a.mode == 1 ? 1 : 0, g, a.attn, st, stream);
     } else {
         const size_t smem = FlashSmem::bytes(g.M);
         cudaError_t e = cudaFuncSetAttribute(attn_flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

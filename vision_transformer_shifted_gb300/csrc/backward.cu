@@ -14,9 +14,11 @@
 // back in token order, dWproj = dy^T o and dWqkv = dqkv^T x then take dy and x
 // as they are, dx = dqkv Wqkv needs no scatter, and only the two GEMMs that
 // feed the attention backward (qkv and do, in window order) gather their rows.
-// This file holds a weight transpose, column sums and the attention backward
-// (which also yields o, so the forward attention is not run again); the GEMMs
-// are launched by the caller.
+// This file holds a weight transpose, column sums and the tcgen05 attention
+// kernel in two modes: the backward (which also yields o, so the forward
+// attention is not run again) and the forward attention step of the
+// three-kernel path for windows of at most 64 tokens; the GEMMs are launched
+// by the caller.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -100,7 +102,8 @@ __global__ void colsum_kernel(const bf16 *in, int64_t rows, int N, float *out)
 // from two issuing threads, the four outputs from four, so that the MMAs'
 // issue costs overlap).  Cross-window
 // products vanish because the off-diagonal blocks are zero.  Units run head
-// by head (unit u: head u / pairs), so a CTA keeps one head's bias matrix in
+// by head (unit u: head u / pairs; a CTA takes a contiguous range of units),
+// so a CTA keeps one head's bias matrix in
 // shared memory and the table gradient of each (query, key) position in
 // registers, folding it into the table only when the head changes.
 constexpr int TB_THREADS = 256;
@@ -140,10 +143,13 @@ __device__ __forceinline__ void store_global32(bf16 *dst, const float (&v)[32], 
     }
 }
 
+// BW = false: the forward attention alone (S, P, o = P v; V1 scale 1/sqrt(32)
+// or V2 1/max(tau, 0.01) per head), o written in window order.
+// BW = true: the backward of the V1 block as described above.
+template <bool BW>
 __global__ void __launch_bounds__(TB_THREADS, 2)
-attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *dqkv, float *dtable,
-                        DeviceStatus st, const __grid_constant__ CUtensorMap tm_qkv,
-                        const __grid_constant__ CUtensorMap tm_do)
+attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, bf16 *attn, bf16 *dqkv, float *dtable,
+               DeviceStatus st, const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do)
 {
     extern __shared__ uint8_t smraw[];
     using Ly = TbLayout;
@@ -159,7 +165,8 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
     const int quad = warp & 3, h2 = warp >> 2;     // TMEM lane quadrant; which 32 keys of the row
     const int r = quad * 32 + lane, hf = r >> 6, i = r & 63;
     const int64_t npairs = (g.nwin + 1) / 2, nunits = npairs * heads;
-    const float scale = 0.17677669529663687f; // 1 / sqrt(32)
+    const float rsqrt_d = 0.17677669529663687f; // 1 / sqrt(32)
+    float scale = rsqrt_d;                       // logit scale of the current head
     const float log2e = 1.4426950408889634f;
 
     // zero the operand tiles (rows past N are never loaded) and P, dS (their
@@ -187,8 +194,8 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
     for (int e = tid; e < 228; e += TB_THREADS) dtab[e] = 0.f;
     if (tid == 0) {
         mbar_init(bar_ld, 1);
-        mbar_init(bar_s, 2);
-        mbar_init(bar_o, 4);
+        mbar_init(bar_s, BW ? 2 : 1);
+        mbar_init(bar_o, BW ? 4 : 1);
         mbar_init_fence();
     }
     if (warp == 0) {
@@ -197,26 +204,28 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
     }
     fence_proxy_async_smem(); // the zeroed tiles, before any TMA or MMA touches them
 
-    // TMA of unit u's q, k, v, do (one box of N rows x 32 channels per window and tensor)
+    // TMA of unit u's q, k, v (and do) (one box of N rows x 32 channels per window and tensor)
     auto load_unit = [&](int64_t u) {
         const int head = (int)(u / npairs);
         const int64_t pair = u - (int64_t)head * npairs;
         const int nw = 2 * pair + 1 < g.nwin ? 2 : 1;
-        mbar_arrive_expect_tx(bar_ld, (uint32_t)(nw * 4 * N * 64));
+        mbar_arrive_expect_tx(bar_ld, (uint32_t)(nw * (BW ? 4 : 3) * N * 64));
         for (int w = 0; w < nw; ++w) {
             const int y = (int)((2 * pair + w) * N);
             const uint32_t dst = base + (uint32_t)w * 4096u;
             tma_load_2d(dst + Ly::Q, &tm_qkv, head * 32, y, bar_ld);
             tma_load_2d(dst + Ly::K, &tm_qkv, C + head * 32, y, bar_ld);
             tma_load_2d(dst + Ly::V, &tm_qkv, 2 * C + head * 32, y, bar_ld);
-            tma_load_2d(dst + Ly::DO, &tm_do, head * 32, y, bar_ld);
+            if (BW) tma_load_2d(dst + Ly::DO, &tm_do, head * 32, y, bar_ld);
         }
     };
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0 && blockIdx.x < nunits) load_unit(blockIdx.x);
+    // a contiguous range of units per CTA (head changes at most a few times)
+    const int64_t u_begin = nunits * blockIdx.x / gridDim.x, u_end = nunits * (blockIdx.x + 1) / gridDim.x;
+    if (tid == 0 && u_begin < u_end) load_unit(u_begin);
     const uint32_t tmem = *tslot;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
 
@@ -246,13 +255,14 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
         }
     };
 
-    for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
+    for (int64_t u = u_begin; u < u_end; ++u) {
         const int head = (int)(u / npairs);
         const int64_t pair = u - (int64_t)head * npairs;
         const int64_t win = 2 * pair + hf;
         const bool rv = i < N && win < g.nwin;
         if (head != cur_head) {
-            if (cur_head >= 0) flush_head();
+            if (BW && cur_head >= 0) flush_head();
+            if (!BW && v2) scale = 1.0f / fmaxf(tau[head], 0.01f);
             // the head's bias matrix B[i][j] = table[idx(i, j), head] (zero outside N x N)
             for (int e = tid; e < 64 * 64; e += TB_THREADS) {
                 const int a = e >> 6, b = e & 63;
@@ -269,7 +279,7 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
             const int rem = (int)(win % (g.nh * g.nw));
             cls = (rem / g.nw == g.nh - 1 ? 1 : 0) | (rem % g.nw == g.nw - 1 ? 2 : 0);
         }
-        if (tid == 0 || tid == 128) {
+        if (tid == 0 || (BW && tid == 128)) {
             // S by thread 0, dP by thread 128 (their issue costs overlap)
             const bool okl = mbar_wait(bar_ld, phase, st.wait_ns);
             if (okl) {
@@ -287,10 +297,10 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
         if (__syncthreads_or(!ok)) { failed = true; break; }
         tc_fence_after();
 
-        // ---- P and dS: this thread's 32 keys of its row ----
+        // ---- P (and dS): this thread's 32 keys of its row ----
         float s[32], d[32];
         tmem_ld32(t_lane + 64 * hf + 32 * h2, s);
-        tmem_ld32(t_lane + 128 + 64 * hf + 32 * h2, d);
+        if (BW) tmem_ld32(t_lane + 128 + 64 * hf + 32 * h2, d);
         const uint32_t mb = rv ? (uint32_t)(mask[cls * 64 + i] >> (32 * h2)) : 0u;
         {
             const uint4 *brow = reinterpret_cast<const uint4 *>(sm + Ly::BIAS + i * BIAS_STRIDE + 64 * h2);
@@ -317,7 +327,7 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
             for (int j = 0; j < 32; ++j) {
                 s[j] = ex2_approx(fmaf(s[j], log2e, -mxl)); // masked: -inf -> 0
                 sum += s[j];
-                dsum = fmaf(s[j], d[j], dsum);
+                if (BW) dsum = fmaf(s[j], d[j], dsum);
             }
             float *mine = red + (h2 * 128 + r) * 4;
             mine[0] = mb ? mx : -INFINITY;
@@ -338,21 +348,23 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 s[j] *= p_scale;
-                d[j] = s[j] * (d[j] - D);
-                acc[j] += d[j];
+                if (BW) {
+                    d[j] = s[j] * (d[j] - D);
+                    acc[j] += d[j];
+                }
             }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint32_t off = (uint32_t)(2 * hf + h2) * 8192u + sw64_offset(r, c);
                 store_row8(base + Ly::P + off, s + 8 * c, 1.f);
-                store_row8(base + Ly::DS + off, d + 8 * c, 1.f);
+                if (BW) store_row8(base + Ly::DS + off, d + 8 * c, 1.f);
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (lane == 0 && (warp & 2) == 0) {
-            // one issuer per output (warps 0, 1, 4, 5): o, dq, dk, dv
+        if (lane == 0 && (warp & 2) == 0 && (BW || warp == 0)) {
+            // one issuer per output (warps 0, 1, 4, 5): o, dq, dk, dv (forward: o only)
             tc_fence_after();
             const int which = (warp & 1) | ((warp >> 2) << 1); // 0 o, 1 dq, 2 dk, 3 dv
             if (which < 2) {
@@ -377,10 +389,11 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
         if (__syncthreads_or(!ok)) { failed = true; break; }
         tc_fence_after();
         // q, k, v, do are free: the next unit's loads run under the epilogue
-        if (tid == 0 && u + gridDim.x < nunits) load_unit(u + gridDim.x);
+        if (tid == 0 && u + 1 < u_end) load_unit(u + 1);
 
-        // ---- outputs of row r: o and dq (first four warps), dk and dv (last four) ----
-        {
+        // ---- outputs of row r ----
+        if (BW) {
+            // o and dq (first four warps), dk and dv (last four)
             float a[32], b[32];
             tmem_ld32(t_lane + 64 * h2, a);
             tmem_ld32(t_lane + 64 * h2 + 32, b);
@@ -390,11 +403,23 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
                 const int64_t tok = window_row_to_token(g, win * N + i);
                 if (h2 == 0) {
                     store_global32(attn + tok * C + head * 32, a, 1.f);
-                    store_global32(dqkv + tok * 3 * C + head * 32, b, scale);
+                    store_global32(dqkv + tok * 3 * C + head * 32, b, rsqrt_d);
                 } else {
-                    store_global32(dqkv + tok * 3 * C + C + head * 32, a, scale);
+                    store_global32(dqkv + tok * 3 * C + C + head * 32, a, rsqrt_d);
                     store_global32(dqkv + tok * 3 * C + 2 * C + head * 32, b, 1.f);
                 }
+            }
+        } else {
+            // o in window order, 16 channels per thread
+            float a[16];
+            tmem_ld16(t_lane + 16 * h2, a);
+            tmem_wait_ld();
+            if (rv) {
+                uint4 *dst = reinterpret_cast<uint4 *>(attn + (win * N + i) * C + head * 32 + 16 * h2);
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    dst[q] = make_uint4(pack_bf16x2(a[8 * q], a[8 * q + 1]), pack_bf16x2(a[8 * q + 2], a[8 * q + 3]),
+                                        pack_bf16x2(a[8 * q + 4], a[8 * q + 5]), pack_bf16x2(a[8 * q + 6], a[8 * q + 7]));
             }
         }
         tc_fence_before();
@@ -404,7 +429,7 @@ attn_backward_tc_kernel(const bf16 *table, int heads, Geom g, bf16 *attn, bf16 *
         if (tid == 0) atomicOr(st.err, ERR_TIMEOUT);
         // a load may still be in flight: wait for it (bounded) before leaving
         if (tid == 0) mbar_wait(bar_ld, phase, st.wait_ns);
-    } else if (cur_head >= 0) {
+    } else if (BW && cur_head >= 0) {
         flush_head();
     }
     tc_fence_before();
@@ -435,18 +460,23 @@ cudaError_t launch_colsum(const bf16 *in, int64_t rows, int N, float *out, cudaS
 
 bool attn_backward_supported(int M, int C, int heads) { return M * M <= 64 && C == heads * 32; }
 
-cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, int heads, const Geom &g,
-                                 bf16 *attn, bf16 *dqkv, float *dtable, DeviceStatus st, cudaStream_t stream)
+namespace {
+
+template <bool BW>
+cudaError_t launch_attn_tc(const bf16 *qkv, const bf16 *dO, const bf16 *table, const float *tau, int heads, int v2,
+                           const Geom &g, bf16 *attn, bf16 *dqkv, float *dtable, DeviceStatus st,
+                           cudaStream_t stream)
 {
     if (!attn_backward_supported(g.M, g.C, heads)) return cudaErrorInvalidValue;
     CUtensorMap tm_qkv, tm_do;
     // units run head by head: the other heads' 64-byte slices of a row are
     // read much later, so no 128-byte L2 promotion
     cudaError_t e = make_tensor_map_sw64(&tm_qkv, qkv, g.T, 3 * g.C, g.N, false);
-    if (e == cudaSuccess) e = make_tensor_map_sw64(&tm_do, dO, g.T, g.C, g.N, false);
+    if (e == cudaSuccess) e = BW ? make_tensor_map_sw64(&tm_do, dO, g.T, g.C, g.N, false) : cudaSuccess;
+    if (!BW) tm_do = tm_qkv; // unused
     if (e != cudaSuccess) return e;
     const size_t smem = TbLayout::bytes();
-    e = cudaFuncSetAttribute(attn_backward_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(attn_tc_kernel<BW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     static int sms = 0;
     if (!sms) {
@@ -457,9 +487,23 @@ cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *ta
     const int64_t units = (g.nwin + 1) / 2 * heads;
     const int64_t cap = (int64_t)sms * 2;
     const unsigned grid = (unsigned)(units < cap ? units : cap);
-    attn_backward_tc_kernel<<<grid, TB_THREADS, smem, stream>>>(table, heads, g, attn, dqkv, dtable, st, tm_qkv,
-                                                                tm_do);
+    attn_tc_kernel<BW><<<grid, TB_THREADS, smem, stream>>>(table, tau, heads, v2, g, attn, dqkv, dtable, st, tm_qkv,
+                                                            tm_do);
     return cudaGetLastError();
+}
+
+} // namespace
+
+cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, int heads, const Geom &g,
+                                 bf16 *attn, bf16 *dqkv, float *dtable, DeviceStatus st, cudaStream_t stream)
+{
+    return launch_attn_tc<true>(qkv, dO, table, nullptr, heads, 0, g, attn, dqkv, dtable, st, stream);
+}
+
+cudaError_t launch_attn_forward_tc(const bf16 *qkv, const bf16 *table, const float *tau, int heads, int v2,
+                                   const Geom &g, bf16 *attn, DeviceStatus st, cudaStream_t stream)
+{
+    return launch_attn_tc<false>(qkv, nullptr, table, tau, heads, v2, g, attn, nullptr, nullptr, st, stream);
 }
 
 } // namespace swin

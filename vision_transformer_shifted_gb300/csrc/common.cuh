@@ -187,5 +187,10 @@ bool attn_backward_supported(int M, int C, int heads);
 // heads] fp32).
 cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, int heads, const Geom &g,
                                  bf16 *attn, bf16 *dqkv, float *dtable, DeviceStatus st, cudaStream_t stream);
+// The forward attention step alone on the same kernel (windows of <= 64
+// tokens): attn [T, C] (window order) = P v from qkv [T, 3C] (window order);
+// v2: cosine logits over the already normalised q, k, scaled by 1/max(tau, 0.01).
+cudaError_t launch_attn_forward_tc(const bf16 *qkv, const bf16 *table, const float *tau, int heads, int v2,
+                                   const Geom &g, bf16 *attn, DeviceStatus st, cudaStream_t stream);
 
 } // namespace swin
