@@ -109,16 +109,22 @@ __global__ void colsum_kernel(const bf16 *in, int64_t rows, int N, float *out)
 constexpr int TB_THREADS = 256;
 constexpr int BIAS_STRIDE = 144; // bytes per bias row: 64 bf16 + 16 pad (conflict-free 16-byte loads)
 
+template <bool BW>
 struct TbLayout {
-    // byte offsets from the 1024-aligned base
-    static constexpr uint32_t Q = 0, K = 8192, V = 16384, DO = 24576; // [128][64 B] tiles
-    static constexpr uint32_t P = 32768, DS = 65536;                   // 4 panels of [128][32 keys]
-    static constexpr uint32_t BIAS = 98304;                            // bf16 [64][72]
+    // byte offsets from the 1024-aligned base; the forward mode has no do tile,
+    // no dS panels and no table gradient, so three CTAs share an SM
+    static constexpr uint32_t Q = 0, K = 8192, V = 16384, DO = 24576;  // [128][64 B] tiles
+    static constexpr uint32_t P = BW ? 32768 : 24576;                   // 4 panels of [128][32 keys]
+    static constexpr uint32_t DS = P + 32768;                          // (backward only)
+    static constexpr uint32_t BIAS = BW ? 98304 : 57344;               // bf16 [64][72]
     static constexpr uint32_t MASK = BIAS + 64 * BIAS_STRIDE;          // uint64 [4 classes][64 rows]
     static constexpr uint32_t RED = MASK + 4 * 64 * 8;                 // float [2][128][4]
     static constexpr uint32_t DTAB = RED + 2 * 128 * 16;               // float [(2M-1)^2 <= 225], padded
-    static constexpr uint32_t BAR = DTAB + 228 * 4;                    // 3 mbarriers + TMEM slot
+    static constexpr uint32_t BAR = DTAB + (BW ? 228 * 4 : 0);         // 3 mbarriers + TMEM slot
     static constexpr size_t bytes() { return (size_t)BAR + 32 + 1024; }
+    // TMEM: S and dP (backward); S, then o over S's first 32 columns (forward)
+    static constexpr uint32_t TCOLS = BW ? 256 : 128;
+    static constexpr int CTAS_PER_SM = BW ? 2 : 3;
 };
 
 __device__ __forceinline__ int band_in_window(int t, int M, int s) { return t < M - s ? 1 : 2; }
@@ -147,12 +153,12 @@ __device__ __forceinline__ void store_global32(bf16 *dst, const float (&v)[32], 
 // or V2 1/max(tau, 0.01) per head), o written in window order.
 // BW = true: the backward of the V1 block as described above.
 template <bool BW>
-__global__ void __launch_bounds__(TB_THREADS, 2)
+__global__ void __launch_bounds__(TB_THREADS, TbLayout<BW>::CTAS_PER_SM)
 attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, bf16 *attn, bf16 *dqkv, float *dtable,
                DeviceStatus st, const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do)
 {
     extern __shared__ uint8_t smraw[];
-    using Ly = TbLayout;
+    using Ly = TbLayout<BW>;
     uint8_t *sm = smem_align(smraw, 1024);
     const uint32_t base = smem_u32(sm);
     const int N = g.N, M = g.M, C = g.C, L = 2 * M - 1, LL = L * L;
@@ -191,7 +197,8 @@ attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, b
         }
         reinterpret_cast<uint64_t *>(sm + Ly::MASK)[tid] = m;
     }
-    for (int e = tid; e < 228; e += TB_THREADS) dtab[e] = 0.f;
+    if (BW)
+        for (int e = tid; e < 228; e += TB_THREADS) dtab[e] = 0.f;
     if (tid == 0) {
         mbar_init(bar_ld, 1);
         mbar_init(bar_s, BW ? 2 : 1);
@@ -199,7 +206,7 @@ attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, b
         mbar_init_fence();
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(tslot), 256);
+        tmem_alloc(smem_u32(tslot), Ly::TCOLS);
         tmem_relinquish();
     }
     fence_proxy_async_smem(); // the zeroed tiles, before any TMA or MMA touches them
@@ -435,7 +442,7 @@ attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, b
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, Ly::TCOLS);
 }
 
 } // namespace
@@ -475,7 +482,7 @@ cudaError_t launch_attn_tc(const bf16 *qkv, const bf16 *dO, const bf16 *table, c
     if (e == cudaSuccess) e = BW ? make_tensor_map_sw64(&tm_do, dO, g.T, g.C, g.N, false) : cudaSuccess;
     if (!BW) tm_do = tm_qkv; // unused
     if (e != cudaSuccess) return e;
-    const size_t smem = TbLayout::bytes();
+    const size_t smem = TbLayout<BW>::bytes();
     e = cudaFuncSetAttribute(attn_tc_kernel<BW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     static int sms = 0;
@@ -485,7 +492,7 @@ cudaError_t launch_attn_tc(const bf16 *qkv, const bf16 *dO, const bf16 *table, c
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
     }
     const int64_t units = (g.nwin + 1) / 2 * heads;
-    const int64_t cap = (int64_t)sms * 2;
+    const int64_t cap = (int64_t)sms * TbLayout<BW>::CTAS_PER_SM;
     const unsigned grid = (unsigned)(units < cap ? units : cap);
     attn_tc_kernel<BW><<<grid, TB_THREADS, smem, stream>>>(table, tau, heads, v2, g, attn, dqkv, dtable, st, tm_qkv,
                                                             tm_do);
