@@ -282,13 +282,14 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
 //
 // For the block's projections the whole weight matrix Bw [N, K] fits in
 // shared memory (K-major, 128-byte swizzle, 64-wide K blocks).  One CTA per
-// SM keeps it there and walks over 128-row tiles (and, for N > 256, two
-// column halves), with three warp roles:
+// SM keeps it there and walks over 128-row tiles (for N > 256 as two column
+// halves from the same A stages), with three warp roles:
 //   warp 0      producer: 128 x 64 A blocks into a ring of stages by TMA (plain
 //               rows); for rows gathered through the window map, warps 0 and
 //               10..16 each bring 16 rows of every block by cp.async
 //   warp 1      one thread issues the MMAs of a tile into one of two TMEM
-//               accumulators, releasing each A stage by tcgen05.commit
+//               accumulators (N > 256: half 0 into one, half 1 into the other),
+//               releasing each A stage by tcgen05.commit once the last half read it
 //   warps 2..9  epilogue: two warps per TMEM lane quadrant (alternate 32-column
 //               chunks) drain the other accumulator while the next tile runs.
 // Every wait is bounded; a timeout sets the error word and ends the kernel.
@@ -368,7 +369,9 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
     uint64_t *full = bars, *empty = bars + S, *tfull = bars + 2 * S, *tempty = bars + 2 * S + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t mtiles = (a.rows + BM - 1) / BM, ntiles = mtiles * nbn;
+    // row blocks of 128 rows; for N > 256 each block is done as two column
+    // halves, one per TMEM accumulator, from the same A stages (loaded once)
+    const int64_t mtiles = (a.rows + BM - 1) / BM;
 
     // the weight matrix, once (zero past K), and the bias
     for (int e = tid; e < a.N * KB * 8; e += RS_THREADS) {
@@ -410,8 +413,8 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
         int64_t it = 0;
         if (LOAD == LOAD_PLAIN) {
             if (warp == 0 && lane == 0) {
-                for (int64_t t = blockIdx.x; t < ntiles && !failed; t += gridDim.x) {
-                    const int64_t m0 = (t / nbn) * BM;
+                for (int64_t m = blockIdx.x; m < mtiles && !failed; m += gridDim.x) {
+                    const int64_t m0 = m * BM;
                     for (int kb = 0; kb < KB; ++kb, ++it) {
                         const int s = (int)(it % S);
                         if (!mbar_wait(smem_u32(&empty[s]), (uint32_t)((it / S) & 1) ^ 1u, st.wait_ns)) {
@@ -424,8 +427,8 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
                 }
             }
         } else {
-            for (int64_t t = blockIdx.x; t < ntiles && !failed; t += gridDim.x) {
-                const int64_t m0 = (t / nbn) * BM;
+            for (int64_t m = blockIdx.x; m < mtiles && !failed; m += gridDim.x) {
+                const int64_t m0 = m * BM;
                 // this warp's rows of the tile (BM / RS_NPROD of them): source
                 // offsets (32-bit index map when it fits) into shared memory
                 constexpr int RPW = BM / RS_NPROD;
@@ -481,34 +484,44 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(BM, BN);
-            int64_t it = 0, lt = 0;
-            for (int64_t t = blockIdx.x; t < ntiles && !failed; t += gridDim.x, ++lt) {
-                const int buf = (int)(lt & 1);
-                if (!mbar_wait(smem_u32(&tempty[buf]), (uint32_t)((lt >> 1) & 1) ^ 1u, st.wait_ns)) {
-                    failed = true;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)buf * half_cols;
-                const uint32_t b_col = (uint32_t)(t % nbn) * (uint32_t)BN * 128u;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = (int)(it % S);
-                    if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((it / S) & 1), st.wait_ns)) {
+            int64_t it = 0, lm = 0;
+            for (int64_t m = blockIdx.x; m < mtiles && !failed; m += gridDim.x, ++lm) {
+                const int64_t it0 = it;
+                for (int nb = 0; nb < nbn && !failed; ++nb) {
+                    // accumulator: alternate per row block (one half), or one per half
+                    const int buf = nbn == 2 ? nb : (int)(lm & 1);
+                    const uint32_t par = nbn == 2 ? (uint32_t)(lm & 1) : (uint32_t)((lm >> 1) & 1);
+                    if (!mbar_wait(smem_u32(&tempty[buf]), par ^ 1u, st.wait_ns)) {
                         failed = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(sA + (size_t)s * RS_STAGE);
-                    const uint32_t b_base = smem_u32(sB) + (uint32_t)kb * (uint32_t)(a.N * 128) + b_col;
+                    const uint32_t d = tmem + (uint32_t)buf * half_cols;
+                    const uint32_t b_col = (uint32_t)nb * (uint32_t)BN * 128u;
+                    for (int kb = 0; kb < KB; ++kb) {
+                        const int64_t i = it0 + kb;
+                        const int s = (int)(i % S);
+                        if (nb == 0) {
+                            if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((i / S) & 1), st.wait_ns)) {
+                                failed = true;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        const uint32_t a_base = smem_u32(sA + (size_t)s * RS_STAGE);
+                        const uint32_t b_base = smem_u32(sB) + (uint32_t)kb * (uint32_t)(a.N * 128) + b_col;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (kb * 64 + k * 16 < a.K)
-                            mma_bf16(d, desc_kmajor_sw128(a_base + 32 * k), desc_kmajor_sw128(b_base + 32 * k), idesc,
-                                     (kb | k) != 0);
-                    mma_commit(smem_u32(&empty[s]));
+                        for (int k = 0; k < 4; ++k)
+                            if (kb * 64 + k * 16 < a.K)
+                                mma_bf16(d, desc_kmajor_sw128(a_base + 32 * k), desc_kmajor_sw128(b_base + 32 * k), idesc,
+                                         (kb | k) != 0);
+                        // the stage is free once the last half has read it
+                        if (nb == nbn - 1) mma_commit(smem_u32(&empty[s]));
+                    }
+                    if (failed) break;
+                    mma_commit(smem_u32(&tfull[buf]));
                 }
-                if (failed) break;
-                mma_commit(smem_u32(&tfull[buf]));
+                it = it0 + KB;
             }
         }
     } else {
@@ -517,16 +530,18 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
         const int r = quad * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
         const int nchunks = BN / 32;
-        int64_t lt = 0;
-        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
-            const int buf = (int)(lt & 1);
-            if (!mbar_wait(smem_u32(&tfull[buf]), (uint32_t)((lt >> 1) & 1), st.wait_ns)) {
+        int64_t lm = 0;
+        for (int64_t m = blockIdx.x; m < mtiles && !failed; m += gridDim.x, ++lm)
+        for (int nb = 0; nb < nbn; ++nb) {
+            const int buf = nbn == 2 ? nb : (int)(lm & 1);
+            const uint32_t par = nbn == 2 ? (uint32_t)(lm & 1) : (uint32_t)((lm >> 1) & 1);
+            if (!mbar_wait(smem_u32(&tfull[buf]), par, st.wait_ns)) {
                 failed = true;
                 break;
             }
             tc_fence_after();
-            const int64_t R = (t / nbn) * BM + r;
-            const int n0 = (int)(t % nbn) * BN;
+            const int64_t R = m * BM + r;
+            const int n0 = nb * BN;
             bf16 *dst_row = nullptr;
             if (R < a.rows) {
                 if (STORE == STORE_SCATTER) dst_row = a.D + window_row_to_token(a.g, R) * (int64_t)a.N + n0;
@@ -587,6 +602,7 @@ bool rs_plan(const GemmArgs &a, RsPlan &p)
     p.stages = (int)((227 * 1024 - fixed) / RS_STAGE);
     if (p.stages > 8) p.stages = 8;
     if (p.stages < RS_DEPTH + 1) return false; // the gathered producer keeps RS_DEPTH stages in flight
+    if (p.nbn == 2 && p.KB > p.stages) return false; // both halves read a block's stages
     p.tcols = 2 * p.BN <= 256 ? 256 : 512;
     p.smem = fixed + (size_t)p.stages * RS_STAGE;
     return true;
@@ -611,8 +627,8 @@ cudaError_t launch_rs(const GemmArgs &a, const RsPlan &pl, DeviceStatus st, cuda
         cudaGetDevice(&dev);
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
     }
-    const int64_t ntiles = (a.rows + BM - 1) / BM * pl.nbn;
-    const unsigned grid = (unsigned)(ntiles < sms ? ntiles : sms);
+    const int64_t mtiles = (a.rows + BM - 1) / BM;
+    const unsigned grid = (unsigned)(mtiles < sms ? mtiles : sms);
     kern<<<grid, RS_THREADS, pl.smem, stream>>>(a, pl, st, tmA);
     return cudaGetLastError();
 }
