@@ -1,5 +1,6 @@
 """Float64 CPU oracle of the backward pass of the shifted-window attention
-block (V1: dot-product logits with a learned relative-bias table).
+block: V1 (dot-product logits with a learned relative-bias table) and V2
+(scaled-cosine logits, the table from the meta-network G).
 
 TEST INFRASTRUCTURE ONLY, under the same rule as the rest of this package.
 
@@ -12,11 +13,21 @@ shift, reshape / permute for the window partition and reverse, explicit
 relative indices and region masks -- independently of ``swin_oracle.c``,
 and takes the gradients with torch.autograd.
 
-Pins in ``tests/test_backward.py``: its forward equals the pinned
-``oracle.forward``; gradients match central finite differences
-(torch.autograd.gradcheck) on a small grid; each head's column of the table
+V2 ("Swin Transformer V2" (neura.market), How It Works: the logit is the
+cosine of query and key divided by a learned per-head tau clipped at 0.01,
+plus the bias that G maps from log-spaced relative coordinates): q and k
+scaled to unit length (norm clamped at 1e-12), logit = cos / max(tau, 0.01)
++ G-table, no 1/sqrt(d); G(u) = W2 relu(W1 u + b1) over u = (sign(dr)
+ln(1+|dr|), sign(dc) ln(1+|dc|)).
+
+Pins in ``tests/test_backward.py``: the forward equals the pinned
+``oracle.forward`` (both modes) and the G table the pinned
+``oracle.cpb_table``; gradients match central finite differences
+(torch.autograd.gradcheck) on small grids; each head's column of the table
 gradient sums to zero (every softmax row's logit gradients sum to zero);
-the projection-bias gradient is the sum of the output gradient over tokens.
+the projection-bias gradient is the sum of the output gradient over tokens;
+V1's key-bias gradient vanishes; V2's tau gradient equals its closed form
+-sum(dS cos) / tau^2, and vanishes below the 0.01 clip.
 """
 from __future__ import annotations
 
@@ -46,6 +57,24 @@ def _rel_index(M):
 
 def block_v1(x, Wqkv, bqkv, table, Wproj, bproj, *, heads, M, shift):
     """The V1 block in torch (differentiable).  x [B, H, W, C]."""
+    return _block(x, Wqkv, bqkv, table, None, Wproj, bproj, heads=heads, M=M, shift=shift)
+
+
+def block_v2(x, Wqkv, bqkv, table, tau, Wproj, bproj, *, heads, M, shift):
+    """The V2 block in torch (differentiable); tau [heads]."""
+    return _block(x, Wqkv, bqkv, table, tau, Wproj, bproj, heads=heads, M=M, shift=shift)
+
+
+def cpb_table(W1, b1, W2, *, M):
+    """G over the relative coordinates of an M x M window (differentiable):
+    [(2M-1)^2, heads], row (dr+M-1)(2M-1) + (dc+M-1)."""
+    d = torch.arange(-(M - 1), M, dtype=torch.float64)
+    dr, dc = d.repeat_interleave(2 * M - 1), d.repeat(2 * M - 1)
+    u = torch.stack([torch.sign(dr) * torch.log1p(dr.abs()), torch.sign(dc) * torch.log1p(dc.abs())], 1)
+    return torch.relu(u @ W1.T + b1) @ W2.T
+
+
+def _block(x, Wqkv, bqkv, table, tau, Wproj, bproj, *, heads, M, shift):
     B, H, W, C = x.shape
     d, N = C // heads, M * M
     nh, nw = H // M, W // M
@@ -53,7 +82,12 @@ def block_v1(x, Wqkv, bqkv, table, Wproj, bproj, *, heads, M, shift):
     win = xs.reshape(B, nh, M, nw, M, C).permute(0, 1, 3, 2, 4, 5).reshape(B * nh * nw, N, C)
     qkv = win @ Wqkv.T + bqkv                                    # [nW, N, 3C]
     q, k, v = (qkv[..., i * C:(i + 1) * C].reshape(-1, N, heads, d).transpose(1, 2) for i in range(3))
-    logits = q @ k.transpose(-1, -2) / np.sqrt(d)                # [nW, h, N, N]
+    if tau is None:
+        logits = q @ k.transpose(-1, -2) / np.sqrt(d)            # [nW, h, N, N]
+    else:
+        qn = q / q.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+        kn = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+        logits = (qn @ kn.transpose(-1, -2)) / tau.clamp_min(0.01)[None, :, None, None]
     bias = table[_rel_index(M)]                                  # [N, N, h]
     logits = logits + bias.permute(2, 0, 1)[None]
     if shift > 0:
@@ -77,3 +111,22 @@ def gradients(x, Wqkv, bqkv, table, Wproj, bproj, dy, *, heads, M, shift):
     y = block_v1(t["x"], t["Wqkv"], t["bqkv"], t["table"], t["Wproj"], t["bproj"], heads=heads, M=M, shift=shift)
     (y * torch.tensor(np.asarray(dy, dtype=np.float64))).sum().backward()
     return {"d" + n: v.grad.numpy() for n, v in t.items()}
+
+
+def gradients_v2(x, Wqkv, bqkv, tau, W1, b1, W2, Wproj, bproj, dy, *, heads, M, shift):
+    """V2: gradients of sum(block(x) * dy) with respect to x, Wqkv, bqkv,
+    tau, the table (as the block consumes it), G's W1, b1, W2, Wproj and
+    bproj, as float64 numpy arrays (dict; the table gradient under
+    "dtable")."""
+    t = {n: torch.tensor(np.asarray(a, dtype=np.float64), requires_grad=True)
+         for n, a in dict(x=x, Wqkv=Wqkv, bqkv=bqkv, tau=tau, W1=W1, b1=b1, W2=W2, Wproj=Wproj,
+                          bproj=bproj).items()}
+    table = cpb_table(t["W1"], t["b1"], t["W2"], M=M)
+    table.retain_grad()
+    y = block_v2(t["x"], t["Wqkv"], t["bqkv"], table, t["tau"], t["Wproj"], t["bproj"], heads=heads, M=M,
+                 shift=shift)
+    (y * torch.tensor(np.asarray(dy, dtype=np.float64))).sum().backward()
+    out = {"d" + n: v.grad.numpy() for n, v in t.items()}
+    out["dtable"] = table.grad.numpy()
+    out["table"] = table.detach().numpy()
+    return out

@@ -76,6 +76,75 @@ def test_key_bias_gradient_is_zero():
     assert np.abs(db[:C]).max() > 1e-3 and np.abs(db[2 * C:]).max() > 1e-3
 
 
+# ---- V2 (scaled cosine logits, table from G) ----------------------------------------
+
+def _g_params(heads, hidden=32):
+    return dict(W1=RNG.normal(size=(hidden, 2)) * 0.5, b1=RNG.normal(size=hidden) * 0.1,
+                W2=RNG.normal(size=(heads, hidden)) * 0.2)
+
+
+def test_torch_g_table_equals_the_pinned_oracle():
+    g = _g_params(3, 512)
+    for M in (3, 7, 8):
+        got = obw.cpb_table(*(torch.tensor(g[k]) for k in ("W1", "b1", "W2")), M=M).numpy()
+        assert np.allclose(got, oracle.cpb_table(g["W1"], g["b1"], g["W2"], M=M, heads=3), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("B,H,W,C,heads,M,s", [(1, 16, 16, 32, 1, 8, 4), (2, 8, 12, 64, 2, 4, 2),
+                                               (1, 6, 6, 32, 2, 3, 0)])
+def test_torch_v2_forward_equals_the_pinned_oracle(B, H, W, C, heads, M, s):
+    x = RNG.normal(size=(B, H, W, C))
+    p = _params(C, heads, M)
+    tau = np.array([0.1, 0.005, 0.3, 1.0][:heads])          # one head below the 0.01 clip
+    ref = oracle.forward(x, p["Wqkv"], p["bqkv"], p["table"], tau, p["Wproj"], p["bproj"], heads=heads, M=M,
+                         shift=s, mode=oracle.V2)
+    t = {k: torch.tensor(v) for k, v in p.items()}
+    got = obw.block_v2(torch.tensor(x), t["Wqkv"], t["bqkv"], t["table"], torch.tensor(tau), t["Wproj"],
+                       t["bproj"], heads=heads, M=M, shift=s).numpy()
+    assert np.allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_v2_gradients_match_finite_differences():
+    B, H, W, C, heads, M, s = 1, 6, 6, 8, 2, 3, 1
+    x = torch.tensor(RNG.normal(size=(B, H, W, C)), requires_grad=True)
+    p = {k: torch.tensor(v, requires_grad=True) for k, v in _params(C, heads, M).items()}
+    g = {k: torch.tensor(v, requires_grad=True) for k, v in _g_params(heads, 8).items()}
+    tau = torch.tensor([0.2, 0.5], dtype=torch.float64, requires_grad=True)
+
+    def f(x, Wqkv, bqkv, tau, W1, b1, W2, Wproj, bproj):
+        table = obw.cpb_table(W1, b1, W2, M=M)
+        return obw.block_v2(x, Wqkv, bqkv, table, tau, Wproj, bproj, heads=heads, M=M, shift=s)
+
+    assert torch.autograd.gradcheck(f, (x, p["Wqkv"], p["bqkv"], tau, g["W1"], g["b1"], g["W2"], p["Wproj"],
+                                        p["bproj"]), eps=1e-6, atol=1e-7, rtol=1e-5)
+
+
+def test_v2_gradient_identities():
+    """q and k enter only through their unit vectors, so each head's logits are
+    unchanged when that head's q rows (weights and bias) are scaled: the
+    gradient is orthogonal to them (Euler, degree 0), likewise for k.  tau
+    below the 0.01 clip gets no gradient; the table columns' gradients sum to
+    zero as in V1."""
+    B, H, W, C, heads, M, s = 2, 16, 16, 64, 2, 8, 4
+    x = RNG.normal(size=(B, H, W, C))
+    dy = RNG.normal(size=(B, H, W, C))
+    p = _params(C, heads, M)
+    gp = _g_params(heads, 64)
+    tau = np.array([0.005, 0.2])
+    g = obw.gradients_v2(x, p["Wqkv"], p["bqkv"], tau, gp["W1"], gp["b1"], gp["W2"], p["Wproj"], p["bproj"],
+                         dy, heads=heads, M=M, shift=s)
+    d = C // heads
+    scale = np.abs(g["dWqkv"]).max()
+    for part in (0, 1):
+        for hd in range(heads):
+            rows = slice(part * C + hd * d, part * C + (hd + 1) * d)
+            euler = (g["dWqkv"][rows] * p["Wqkv"][rows]).sum() + (g["dbqkv"][rows] * p["bqkv"][rows]).sum()
+            assert abs(euler) < 1e-9 * scale, (part, hd, euler)
+    assert g["dtau"][0] == 0.0 and abs(g["dtau"][1]) > 1e-6
+    assert np.allclose(g["dtable"].sum(axis=0), 0.0, atol=1e-9)
+    assert np.allclose(g["dbproj"], dy.reshape(-1, C).sum(axis=0), atol=1e-9)
+
+
 # ---- GPU: swin_wattn_backward against the oracle --------------------------------
 
 def _rel_errors(got, ref):
