@@ -529,8 +529,9 @@ def run_stage(args, w, depth, ratio=4):
     print(json.dumps(line), flush=True)
 
 def run_backward(args, w):
-    """Gradients of the V1 attention block (recompute of q, k, v and o, then
-    the backward) on workload ``w``; one JSON line, not the headline."""
+    """Gradients of the attention block (recompute of q, k, v and o, then the
+    backward; V2 also the tau gradient) on workload ``w``; one JSON line, not
+    the headline."""
     from vision_transformer_shifted_gb300 import binding as sw
     from vision_transformer_shifted_gb300.inputs import generate
     dev = torch.device("cuda", 0)
@@ -540,7 +541,9 @@ def run_backward(args, w):
     g = generate(w, nonzero_bias=True)
     t = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in g.items()}
     T, C, N, L = w.tokens, w.C, w.N, 2 * w.M - 1
-    h = sw.swin_wattn_create(C, w.heads, w.M, w.shift, sw.V1)
+    h = sw.swin_wattn_create(C, w.heads, w.M, w.shift, w.mode)
+    table = table_for(w, g, dev, h)
+    dtau = torch.empty(w.heads, device=dev, dtype=torch.float32) if w.mode == V2 else None
     io_bytes = T * C * 2 * 3
     nsets = max(2, -(-(2 * L2_BYTES) // io_bytes) + 1)
     gen = torch.Generator(device=dev).manual_seed(9)
@@ -554,8 +557,8 @@ def run_backward(args, w):
 
     def step(i):
         k = i % nsets
-        sw.swin_wattn_backward(h, xs[k], t["Wqkv"], t["bqkv"], t["table"], t["Wproj"], t["bproj"], dys[k], dxs[k],
-                               *grads, stream=stream)
+        sw.swin_wattn_backward(h, xs[k], t["Wqkv"], t["bqkv"], table, t["Wproj"], t["bproj"], dys[k], dxs[k],
+                               *grads, logit_scale=t.get("tau"), dlogit_scale=dtau, stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -582,7 +585,8 @@ def run_backward(args, w):
     # recompute: QKV GEMM 6TC^2, logits and P.V 4TNC; backward: do and dWproj
     # 4TC^2, attention (S again, dP, dq, dk, dv) 10TNC, dx and dWqkv 12TC^2
     flops = 22 * T * C * C + 14 * T * N * C
-    line = {"metric": "swin window-attention backward (V1, with recompute) tokens/s", "value": T / (ms * 1e-3),
+    line = {"metric": "swin window-attention backward (%s, with recompute) tokens/s" % ("V2" if w.mode == V2 else "V1"),
+            "value": T / (ms * 1e-3),
             "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": C, "heads": w.heads, "M": w.M,
@@ -620,8 +624,8 @@ def main():
             ap.error("--stage: bf16 workloads, our implementation, one GPU")
         run_stage(args, w, args.stage)
     elif args.backward:
-        if w.dtype != "bf16" or w.mode != V1 or args.impl != "ours" or args.gpus != 1:
-            ap.error("--backward: bf16 V1 workloads, our implementation, one GPU")
+        if w.dtype != "bf16" or w.M * w.M > 64 or args.impl != "ours" or args.gpus != 1:
+            ap.error("--backward: bf16 workloads with windows of at most 64 tokens, our implementation, one GPU")
         run_backward(args, w)
     elif args.block:
         if w.dtype != "bf16" or args.impl != "ours" or args.gpus != 1:

@@ -1,6 +1,6 @@
 /*
  * swin_wattn_backward -- gradients of the shifted-window attention block
- * (V1 logits) on one GB300, behind a plain C ABI.
+ * (V1 and V2 logits) on one GB300, behind a plain C ABI.
  *
  * Page "Boosting Swin Transformer Speed: Profiling, Mixed Precision, and
  * Kernel Fusion Secrets", Training Optimization: training runs the block's
@@ -39,20 +39,43 @@ extern "C" {
 
 /* Gradients of sum(out * dy), out = the handle's block applied to x.
  * Inputs (bf16, as swin_wattn_forward): x [B, H, W, C], Wqkv [3C, C],
- * bqkv [3C] (NULL = zero), bias_table [(2M-1)^2, heads], Wproj [C, C],
- * bproj [C] (NULL = zero; does not enter any gradient), dy [B, H, W, C].
+ * bqkv [3C] (NULL = zero), bias_table [(2M-1)^2, heads], logit_scale (fp32
+ * [heads], tau; V2 only, NULL in V1), Wproj [C, C], bproj [C] (NULL = zero;
+ * does not enter any gradient), dy [B, H, W, C].
  * Outputs, overwritten: dx [B, H, W, C] bf16; dWqkv [3C, C], dbqkv [3C],
- * dtable [(2M-1)^2, heads], dWproj [C, C], dbproj [C], all fp32.
+ * dtable [(2M-1)^2, heads], dlogit_scale [heads] (V2; may be NULL in V1),
+ * dWproj [C, C], dbproj [C], all fp32.
+ * V2 (page "Swin Transformer V2" (neura.market), How It Works: cosine
+ * logits over a learned tau clipped at 0.01): with q^ = q / max(|q|, 1e-12)
+ * and sigma = 1 / max(tau, 0.01) per head, logit = sigma q^.k^ + table, and
+ *   dq^ = sigma dS k^, dk^ = sigma dS^T q^,
+ *   dq = (dq^ - q^ (q^ . dq^)) / |q| (likewise k),
+ *   dtau = -sum(dS q^.k^) / tau^2 where tau > 0.01, else 0;
+ * the table gradient flows on to G's weights through swin_wattn_cpb_backward.
  * Every pointer 16-byte aligned; dx overlaps neither x nor dy.
- * Errors: EINVAL for NULL or misaligned pointers, bad shapes, overlap;
- * EUNSUPPORTED for a V2 or fp32 handle, windows of more than 64 tokens, or
- * B*H*W >= 2^31; ENOMEM if the workspace (8 * B*H*W*C bf16 elements plus
- * 4C^2) cannot be allocated; ECUDA for launch or cuBLAS failures.  B = 0
- * zeroes the parameter gradients and returns. */
+ * Errors: EINVAL for NULL or misaligned pointers (logit_scale and
+ * dlogit_scale are required in V2), bad shapes, overlap; EUNSUPPORTED for an
+ * fp32 handle, windows of more than 64 tokens, or B*H*W >= 2^31; ENOMEM if
+ * the workspace (8 * B*H*W*C bf16 elements plus 4C^2, plus 2 B*H*W*heads
+ * fp32 in V2) cannot be allocated; ECUDA for launch or cuBLAS failures.
+ * B = 0 zeroes the parameter gradients and returns. */
 int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
-                        const void *bias_table, const void *Wproj, const void *bproj, const void *dy, void *dx,
-                        float *dWqkv, float *dbqkv, float *dtable, float *dWproj, float *dbproj,
-                        swin_stream_t stream);
+                        const void *bias_table, const float *logit_scale, const void *Wproj, const void *bproj,
+                        const void *dy, void *dx, float *dWqkv, float *dbqkv, float *dtable, float *dlogit_scale,
+                        float *dWproj, float *dbproj, swin_stream_t stream);
+
+/* V2: the gradients of G's weights (as swin_wattn_cpb_table: W1 [hidden, 2],
+ * b1 [hidden] (may be NULL), W2 [heads, hidden], fp32) from the gradient of
+ * its table, dtable [(2M-1)^2, heads] fp32 (swin_wattn_backward's output):
+ * dW2[h, k] = sum_idx dtable[idx, h] relu(a_k(idx)), and through the ReLU
+ * (a_k > 0) da_k = sum_h dtable[idx, h] W2[h, k], dW1[k] = sum_idx da_k u(idx),
+ * db1[k] = sum_idx da_k, with a_k(idx) = W1[k] . u(idx) + b1[k] over the
+ * log-spaced coordinates u.  Outputs overwritten: dW1 [hidden, 2], db1
+ * [hidden] (may be NULL), dW2 [heads, hidden], fp32 device pointers.
+ * Errors: EINVAL for NULL pointers or hidden outside 1..4096; EUNSUPPORTED
+ * for more than 16 heads. */
+int swin_wattn_cpb_backward(swin_wattn_t h, const float *W1, const float *b1, const float *W2, int hidden,
+                            const float *dtable, float *dW1, float *db1, float *dW2, swin_stream_t stream);
 
 /* Number of kernels (own and cuBLAS calls counted as one each) the last
  * successful swin_wattn_backward enqueued. */

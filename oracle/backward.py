@@ -74,7 +74,7 @@ def cpb_table(W1, b1, W2, *, M):
     return torch.relu(u @ W1.T + b1) @ W2.T
 
 
-def _block(x, Wqkv, bqkv, table, tau, Wproj, bproj, *, heads, M, shift):
+def _block(x, Wqkv, bqkv, table, tau, Wproj, bproj, *, heads, M, shift, aux=None):
     B, H, W, C = x.shape
     d, N = C // heads, M * M
     nh, nw = H // M, W // M
@@ -87,7 +87,10 @@ def _block(x, Wqkv, bqkv, table, tau, Wproj, bproj, *, heads, M, shift):
     else:
         qn = q / q.norm(dim=-1, keepdim=True).clamp_min(1e-12)
         kn = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
-        logits = (qn @ kn.transpose(-1, -2)) / tau.clamp_min(0.01)[None, :, None, None]
+        cos = qn @ kn.transpose(-1, -2)
+        logits = cos / tau.clamp_min(0.01)[None, :, None, None]
+        if aux is not None:
+            aux["cos"] = cos
     bias = table[_rel_index(M)]                                  # [N, N, h]
     logits = logits + bias.permute(2, 0, 1)[None]
     if shift > 0:
@@ -95,6 +98,9 @@ def _block(x, Wqkv, bqkv, table, tau, Wproj, bproj, *, heads, M, shift):
         masked = reg[:, :, None] != reg[:, None, :]              # [nh*nw, N, N]
         masked = masked.repeat(B, 1, 1)[:, None]
         logits = logits.masked_fill(masked, float("-inf"))
+    if aux is not None and logits.requires_grad:
+        logits.retain_grad()
+        aux["logits"] = logits
     P = torch.softmax(logits, dim=-1)
     o = (P @ v).transpose(1, 2).reshape(-1, N, C)
     y = o @ Wproj.T + bproj
@@ -123,10 +129,18 @@ def gradients_v2(x, Wqkv, bqkv, tau, W1, b1, W2, Wproj, bproj, dy, *, heads, M, 
                           bproj=bproj).items()}
     table = cpb_table(t["W1"], t["b1"], t["W2"], M=M)
     table.retain_grad()
-    y = block_v2(t["x"], t["Wqkv"], t["bqkv"], table, t["tau"], t["Wproj"], t["bproj"], heads=heads, M=M,
-                 shift=shift)
+    aux = {}
+    y = _block(t["x"], t["Wqkv"], t["bqkv"], table, t["tau"], t["Wproj"], t["bproj"], heads=heads, M=M,
+               shift=shift, aux=aux)
     (y * torch.tensor(np.asarray(dy, dtype=np.float64))).sum().backward()
     out = {"d" + n: v.grad.numpy() for n, v in t.items()}
     out["dtable"] = table.grad.numpy()
     out["table"] = table.detach().numpy()
+    # dtau = -sum(dS cos) / tau^2 is a sum with heavy cancellation (every row of
+    # dS sums to zero): the size of its terms, sum |dS cos| / tau^2, bounds the
+    # effect of rounding the terms
+    tau = t["tau"].detach()
+    dS = aux["logits"].grad                                  # gradient of the logits (0 where masked)
+    terms = (dS * aux["cos"]).abs().sum(dim=(0, 2, 3)).detach()
+    out["dtau_terms"] = torch.where(tau > 0.01, terms / tau ** 2, torch.zeros_like(terms)).numpy()
     return out

@@ -58,7 +58,8 @@ def test_null_handle_calls():
     assert lib.swin_wattn_forward(None, None, 1, 7, 7, None, None, None, None, None, None, None, None) == sw.EINVAL
     assert lib.swin_wattn_destroy(None) == sw.OK
     assert lib.swin_wattn_set_option(None, 1, 0) == sw.EINVAL
-    assert lib.swin_wattn_backward(None, None, 1, 7, 7, *([None] * 13)) == sw.EINVAL
+    assert lib.swin_wattn_backward(None, None, 1, 7, 7, *([None] * 15)) == sw.EINVAL
+    assert lib.swin_wattn_cpb_backward(None, None, None, None, 512, None, None, None, None, None) == sw.EINVAL
     assert lib.swin_wattn_backward_launches(None) == 0
     assert lib.swin_wattn_path(None, 1, 7, 7) == sw.EINVAL
     assert lib.swin_wattn_sync_status(None, None) == sw.EINVAL

@@ -56,7 +56,8 @@ _SIGNATURES = {
     "swin_merge_forward": ["p", "p", "i", "i", "i", "p", "p", "p", "p", "p"],
     "swin_merge_destroy": ["p"],
     "swin_wattn_backward": ["p", "p", "i", "i", "i", "p", "p", "p", "p", "p", "p", "p", "p", "p", "p", "p", "p",
-                            "p"],
+                            "p", "p", "p"],
+    "swin_wattn_cpb_backward": ["p", "p", "p", "p", "i", "p", "p", "p", "p", "p"],
     "swin_wattn_backward_launches": ["p"],
 }
 
@@ -146,11 +147,16 @@ def swin_wattn_forward(h, x, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, 
 
 
 def swin_wattn_backward(h, x, Wqkv, bqkv, bias_table, Wproj, bproj, dy, dx, dWqkv, dbqkv, dtable, dWproj, dbproj,
-                        stream=None):
+                        logit_scale=None, dlogit_scale=None, stream=None):
     B, H, W, _ = x.shape
     return _check("swin_wattn_backward", load().swin_wattn_backward(
-        h, _p(x), B, H, W, _p(Wqkv), _p(bqkv), _p(bias_table), _p(Wproj), _p(bproj), _p(dy), _p(dx), _p(dWqkv),
-        _p(dbqkv), _p(dtable), _p(dWproj), _p(dbproj), _stream(stream)))
+        h, _p(x), B, H, W, _p(Wqkv), _p(bqkv), _p(bias_table), _p(logit_scale), _p(Wproj), _p(bproj), _p(dy), _p(dx),
+        _p(dWqkv), _p(dbqkv), _p(dtable), _p(dlogit_scale), _p(dWproj), _p(dbproj), _stream(stream)))
+
+
+def swin_wattn_cpb_backward(h, W1, b1, W2, dtable, dW1, db1, dW2, stream=None):
+    return _check("swin_wattn_cpb_backward", load().swin_wattn_cpb_backward(
+        h, _p(W1), _p(b1), _p(W2), W1.shape[0], _p(dtable), _p(dW1), _p(db1), _p(dW2), _stream(stream)))
 
 
 def swin_wattn_backward_launches(h):

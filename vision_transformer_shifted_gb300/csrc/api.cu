@@ -458,14 +458,16 @@ const char *swin_wattn_strerror(int code)
 }
 
 int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
-                        const void *bias_table, const void *Wproj, const void *bproj, const void *dy, void *dx,
-                        float *dWqkv, float *dbqkv, float *dtable, float *dWproj, float *dbproj,
-                        swin_stream_t stream)
+                        const void *bias_table, const float *logit_scale, const void *Wproj, const void *bproj,
+                        const void *dy, void *dx, float *dWqkv, float *dbqkv, float *dtable, float *dlogit_scale,
+                        float *dWproj, float *dbproj, swin_stream_t stream)
 {
     (void)bproj;
     if (!h || !x || !Wqkv || !bias_table || !Wproj || !dy || !dx || !dWqkv || !dbqkv || !dtable || !dWproj ||
         !dbproj)
         return SWIN_WATTN_EINVAL;
+    const bool v2 = h->mode == SWIN_WATTN_V2;
+    if (v2 && (!logit_scale || !dlogit_scale)) return SWIN_WATTN_EINVAL;
     int rc = check_grid(h, B, H, W);
     if (rc) return rc;
     const void *ptrs[] = {x, Wqkv, bqkv, bias_table, Wproj, bproj, dy, dx, dWqkv, dbqkv, dtable, dWproj, dbproj};
@@ -474,8 +476,7 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     const int C = h->C, L = 2 * h->M - 1;
     const size_t act = (size_t)B * H * W * C * 2;
     if (overlaps(dx, x, act) || overlaps(dx, dy, act)) return SWIN_WATTN_EINVAL;
-    if (h->fp32 || h->mode != SWIN_WATTN_V1 || !attn_backward_supported(h->M, C, h->heads))
-        return SWIN_WATTN_EUNSUPPORTED;
+    if (h->fp32 || !attn_backward_supported(h->M, C, h->heads)) return SWIN_WATTN_EUNSUPPORTED;
     const Geom g = make_geom(B, H, W, C, h->M, h->shift);
     if (g.T >= ((int64_t)1 << 31)) return SWIN_WATTN_EUNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream;
@@ -487,15 +488,18 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     zero(dtable, (size_t)L * L * h->heads);
     zero(dbqkv, (size_t)3 * C);
     zero(dbproj, (size_t)C);
+    if (dlogit_scale) zero(dlogit_scale, (size_t)h->heads);
     if (B == 0) {
         zero(dWqkv, (size_t)3 * C * C);
         zero(dWproj, (size_t)C * C);
         return cuda_status(e);
     }
     if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
-    // workspace (bf16): attn, do [T, C]; qkv, dqkv [T, 3C]; WprojT [C, C]; WqkvT [C, 3C]
+    // workspace (bf16): attn, do [T, C]; qkv, dqkv [T, 3C]; WprojT [C, C]; WqkvT [C, 3C];
+    // V2: the norms of q and k, [T, 2 heads] fp32
     const size_t tc = (size_t)g.T * C;
-    rc = ensure_buffer(&h->bws, &h->bws_bytes, (8 * tc + 4 * (size_t)C * C) * 2);
+    const size_t norm_bytes = v2 ? (size_t)g.T * 2 * h->heads * 4 : 0;
+    rc = ensure_buffer(&h->bws, &h->bws_bytes, (8 * tc + 4 * (size_t)C * C) * 2 + norm_bytes);
     if (rc) return rc;
     if (!h->blas) {
         if (cublasCreate(&h->blas) != CUBLAS_STATUS_SUCCESS) { h->blas = nullptr; return SWIN_WATTN_ECUDA; }
@@ -503,6 +507,7 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     if (cublasSetStream(h->blas, s) != CUBLAS_STATUS_SUCCESS) return SWIN_WATTN_ECUDA;
     bf16 *attn = (bf16 *)h->bws, *dO = attn + tc, *qkv = dO + tc, *dqkv = qkv + 3 * tc;
     bf16 *WpT = dqkv + 3 * tc, *WqkvT = WpT + (size_t)C * C;
+    float *norms = v2 ? reinterpret_cast<float *>(WqkvT + 3 * (size_t)C * C) : nullptr;
     int launches = 0;
     auto step = [&](cudaError_t r) {
         if (e == cudaSuccess) { e = r; ++launches; }
@@ -513,13 +518,15 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     GemmArgs k1{};
     k1.A = (const bf16 *)x; k1.lda = C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
     k1.D = qkv; k1.ldd = 3 * C; k1.rows = g.T; k1.N = 3 * C; k1.K = C; k1.g = g;
+    if (v2) { k1.norm_cols = 2 * C; k1.norms = norms; }
     step(launch_gemm(k1, LOAD_GATHER, STORE_PLAIN, dstatus(h), s));
     GemmArgs k3{};
     k3.A = (const bf16 *)dy; k3.lda = C; k3.Bw = WpT; k3.D = dO; k3.ldd = C; k3.rows = g.T; k3.N = C; k3.K = C;
     k3.g = g;
     step(launch_gemm(k3, LOAD_GATHER, STORE_PLAIN, dstatus(h), s));
     // o and dqkv in token order, dtable
-    step(launch_attn_backward(qkv, dO, (const bf16 *)bias_table, h->heads, g, attn, dqkv, dtable, dstatus(h), s));
+    step(launch_attn_backward(qkv, dO, (const bf16 *)bias_table, logit_scale, h->heads, v2 ? 1 : 0, g, attn, dqkv,
+                              dtable, norms, dlogit_scale, dstatus(h), s));
     // dx = dqkv Wqkv (token order already)
     GemmArgs k4{};
     k4.A = dqkv; k4.lda = 3 * C; k4.Bw = WqkvT; k4.D = (bf16 *)dx; k4.ldd = C; k4.rows = g.T; k4.N = C;
@@ -537,6 +544,15 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
 }
 
 int swin_wattn_backward_launches(swin_wattn_t h) { return h ? h->bw_launches : 0; }
+
+int swin_wattn_cpb_backward(swin_wattn_t h, const float *W1, const float *b1, const float *W2, int hidden,
+                            const float *dtable, float *dW1, float *db1, float *dW2, swin_stream_t stream)
+{
+    if (!h || !W1 || !W2 || !dtable || !dW1 || !dW2 || hidden <= 0 || hidden > 4096) return SWIN_WATTN_EINVAL;
+    if (h->heads > 16) return SWIN_WATTN_EUNSUPPORTED;
+    return cuda_status(launch_cpb_backward(W1, b1, W2, dtable, hidden, h->M, h->heads, dW1, db1, dW2,
+                                           (cudaStream_t)stream));
+}
 
 // ---- stage hooks ------------------------------------------------------------
 

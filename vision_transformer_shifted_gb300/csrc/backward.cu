@@ -149,13 +149,45 @@ __device__ __forceinline__ void store_global32(bf16 *dst, const float (&v)[32], 
     }
 }
 
+// With u = v / n (unit length) and du the gradient of u: dv = (du - u (u . du))
+// / n.  du (32 channels of one row) is scaled by f = scale / n, u is the row's
+// bf16 copy in the 64-byte-swizzled tile at `tile`.
+__device__ __forceinline__ void unit_scale_backward(float (&du)[32], uint32_t tile, int row, float f)
+{
+    // two passes over the row in shared memory (u . du, then the update), so
+    // that u never needs 32 registers of its own
+    float dot = 0.f;
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t w[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                         : "r"(tile + sw64_offset(row, c)));
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float2 p = unpack_bf16x2(w[t]);
+                const int e = 8 * c + 2 * t;
+                if (pass == 0) {
+                    dot = fmaf(p.x, du[e], fmaf(p.y, du[e + 1], dot));
+                } else {
+                    du[e] = (du[e] - p.x * dot) * f;
+                    du[e + 1] = (du[e + 1] - p.y * dot) * f;
+                }
+            }
+        }
+    }
+}
+
 // BW = false: the forward attention alone (S, P, o = P v; V1 scale 1/sqrt(32)
 // or V2 1/max(tau, 0.01) per head), o written in window order.
 // BW = true: the backward of the V1 block as described above.
 template <bool BW>
 __global__ void __launch_bounds__(TB_THREADS, TbLayout<BW>::CTAS_PER_SM)
 attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, bf16 *attn, bf16 *dqkv, float *dtable,
-               DeviceStatus st, const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do)
+               const float *norms, float *dtau, DeviceStatus st, const __grid_constant__ CUtensorMap tm_qkv,
+               const __grid_constant__ CUtensorMap tm_do)
 {
     extern __shared__ uint8_t smraw[];
     using Ly = TbLayout<BW>;
@@ -171,8 +203,8 @@ attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, b
     const int quad = warp & 3, h2 = warp >> 2;     // TMEM lane quadrant; which 32 keys of the row
     const int r = quad * 32 + lane, hf = r >> 6, i = r & 63;
     const int64_t npairs = (g.nwin + 1) / 2, nunits = npairs * heads;
-    const float rsqrt_d = 0.17677669529663687f; // 1 / sqrt(32)
-    float scale = rsqrt_d;                       // logit scale of the current head
+    float scale = 0.17677669529663687f;          // logit scale of the current head (V1: 1 / sqrt(32))
+    float tau_acc = 0.f;                         // V2 backward: sum of dS * cos over this CTA's rows of the head
     const float log2e = 1.4426950408889634f;
 
     // zero the operand tiles (rows past N are never loaded) and P, dS (their
@@ -255,6 +287,15 @@ attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, b
                 acc[j] = 0.f;
             }
         }
+        if (v2) {
+            // dtau = -sum(dS cos) / tau^2 above the 0.01 clip, 0 below it
+            float t = tau_acc;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            const float tv = tau[cur_head];
+            if (lane == 0 && tv > 0.01f && t != 0.f) atomicAdd(&dtau[cur_head], -t / (tv * tv));
+            tau_acc = 0.f;
+        }
         __syncthreads();
         for (int e = tid; e < LL; e += TB_THREADS) {
             if (dtab[e] != 0.f) atomicAdd(&dtable[(int64_t)e * heads + cur_head], dtab[e]);
@@ -269,7 +310,7 @@ attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, b
         const bool rv = i < N && win < g.nwin;
         if (head != cur_head) {
             if (BW && cur_head >= 0) flush_head();
-            if (!BW && v2) scale = 1.0f / fmaxf(tau[head], 0.01f);
+            if (v2) scale = 1.0f / fmaxf(tau[head], 0.01f);
             // the head's bias matrix B[i][j] = table[idx(i, j), head] (zero outside N x N)
             for (int e = tid; e < 64 * 64; e += TB_THREADS) {
                 const int a = e >> 6, b = e & 63;
@@ -366,6 +407,18 @@ attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, b
                 store_row8(base + Ly::P + off, s + 8 * c, 1.f);
                 if (BW) store_row8(base + Ly::DS + off, d + 8 * c, 1.f);
             }
+            if (BW && v2) {
+                // V2: d logit / d(1/tau) = cos = the raw S (still in TMEM), read
+                // back 16 columns at a time
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float c16[16];
+                    tmem_ld16(t_lane + 64 * hf + 32 * h2 + 16 * hh, c16);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) tau_acc = fmaf(d[16 * hh + j], c16[j], tau_acc);
+                }
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -396,24 +449,30 @@ attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, b
         if (__syncthreads_or(!ok)) { failed = true; break; }
         tc_fence_after();
         // q, k, v, do are free: the next unit's loads run under the epilogue
-        if (tid == 0 && u + 1 < u_end) load_unit(u + 1);
+        // (V2 backward: after it, which still reads the q and k rows)
+        if (!(BW && v2) && tid == 0 && u + 1 < u_end) load_unit(u + 1);
 
         // ---- outputs of row r ----
         if (BW) {
-            // o and dq (first four warps), dk and dv (last four)
-            float a[32], b[32];
-            tmem_ld32(t_lane + 64 * h2, a);
-            tmem_ld32(t_lane + 64 * h2 + 32, b);
-            tmem_wait_ld();
-            if (rv) {
-                // rows go back to their tokens' places (window reverse and roll by +s)
-                const int64_t tok = window_row_to_token(g, win * N + i);
-                if (h2 == 0) {
-                    store_global32(attn + tok * C + head * 32, a, 1.f);
-                    store_global32(dqkv + tok * 3 * C + head * 32, b, rsqrt_d);
-                } else {
-                    store_global32(dqkv + tok * 3 * C + C + head * 32, a, rsqrt_d);
-                    store_global32(dqkv + tok * 3 * C + 2 * C + head * 32, b, 1.f);
+            // o and dq (first four warps), dk and dv (last four), one after the
+            // other; rows go back to their tokens' places (window reverse and
+            // roll by +s).  V2: dq and dk through the unit-length scaling of q
+            // and k (dS k and dS^T q are the gradients of the unit vectors).
+            const int64_t tok = rv ? window_row_to_token(g, win * N + i) : 0;
+            const float nrm = v2 && rv ? norms[(win * N + i) * (2 * heads) + h2 * heads + head] : 1.f;
+#pragma unroll 1
+            for (int part = 0; part < 2; ++part) {
+                float a[32];
+                tmem_ld32(t_lane + 64 * h2 + 32 * part, a);
+                tmem_wait_ld();
+                // part 0: o (h2 0) or dS^T q (h2 1); part 1: dS k (h2 0) or dv (h2 1)
+                const bool qk = (h2 == 0) == (part == 1);
+                if (qk && v2) unit_scale_backward(a, base + (h2 == 0 ? Ly::Q : Ly::K), r, scale / nrm);
+                if (rv) {
+                    const int col = h2 == 0 ? (part == 0 ? 0 : 0) : (part == 0 ? C : 2 * C);
+                    bf16 *dst = h2 == 0 && part == 0 ? attn + tok * C + head * 32
+                                                     : dqkv + tok * 3 * C + col + head * 32;
+                    store_global32(dst, a, qk && !v2 ? scale : 1.f);
                 }
             }
         } else {
@@ -431,6 +490,7 @@ attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, b
         }
         tc_fence_before();
         __syncthreads();
+        if (BW && v2 && tid == 0 && u + 1 < u_end) load_unit(u + 1);
     }
     if (failed) {
         if (tid == 0) atomicOr(st.err, ERR_TIMEOUT);
@@ -471,8 +531,8 @@ namespace {
 
 template <bool BW>
 cudaError_t launch_attn_tc(const bf16 *qkv, const bf16 *dO, const bf16 *table, const float *tau, int heads, int v2,
-                           const Geom &g, bf16 *attn, bf16 *dqkv, float *dtable, DeviceStatus st,
-                           cudaStream_t stream)
+                           const Geom &g, bf16 *attn, bf16 *dqkv, float *dtable, const float *norms, float *dtau,
+                           DeviceStatus st, cudaStream_t stream)
 {
     if (!attn_backward_supported(g.M, g.C, heads)) return cudaErrorInvalidValue;
     CUtensorMap tm_qkv, tm_do;
@@ -494,23 +554,25 @@ cudaError_t launch_attn_tc(const bf16 *qkv, const bf16 *dO, const bf16 *table, c
     const int64_t units = (g.nwin + 1) / 2 * heads;
     const int64_t cap = (int64_t)sms * TbLayout<BW>::CTAS_PER_SM;
     const unsigned grid = (unsigned)(units < cap ? units : cap);
-    attn_tc_kernel<BW><<<grid, TB_THREADS, smem, stream>>>(table, tau, heads, v2, g, attn, dqkv, dtable, st, tm_qkv,
-                                                            tm_do);
+    attn_tc_kernel<BW><<<grid, TB_THREADS, smem, stream>>>(table, tau, heads, v2, g, attn, dqkv, dtable, norms, dtau,
+                                                            st, tm_qkv, tm_do);
     return cudaGetLastError();
 }
 
 } // namespace
 
-cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, int heads, const Geom &g,
-                                 bf16 *attn, bf16 *dqkv, float *dtable, DeviceStatus st, cudaStream_t stream)
+cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, const float *tau, int heads,
+                                 int v2, const Geom &g, bf16 *attn, bf16 *dqkv, float *dtable, const float *norms,
+                                 float *dtau, DeviceStatus st, cudaStream_t stream)
 {
-    return launch_attn_tc<true>(qkv, dO, table, nullptr, heads, 0, g, attn, dqkv, dtable, st, stream);
+    return launch_attn_tc<true>(qkv, dO, table, tau, heads, v2, g, attn, dqkv, dtable, norms, dtau, st, stream);
 }
 
 cudaError_t launch_attn_forward_tc(const bf16 *qkv, const bf16 *table, const float *tau, int heads, int v2,
                                    const Geom &g, bf16 *attn, DeviceStatus st, cudaStream_t stream)
 {
-    return launch_attn_tc<false>(qkv, nullptr, table, tau, heads, v2, g, attn, nullptr, nullptr, st, stream);
+    return launch_attn_tc<false>(qkv, nullptr, table, tau, heads, v2, g, attn, nullptr, nullptr, nullptr, nullptr, st,
+                                 stream);
 }
 
 } // namespace swin

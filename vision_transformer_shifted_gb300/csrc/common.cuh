@@ -101,6 +101,8 @@ struct GemmArgs {
     Geom g;          // index maps of LOAD_GATHER / STORE_SCATTER
     int norm_cols;   // > 0: output columns below it are scaled, 32 at a time, to
                      // unit L2 norm (V2 q and k heads); 0: none
+    float *norms;    // norm_cols > 0 and not null: the clamped norm max(|v|, 1e-12) of each
+                     // normalised 32-column chunk, [rows, norm_cols / 32] fp32
     int epi;         // EPI_NONE, EPI_GELU (GELU after the bias), EPI_RESID (add R after the bias)
     const bf16 *R;   // EPI_RESID: [rows, ldr] row-major (plain store only)
     int64_t ldr;
@@ -173,6 +175,10 @@ cudaError_t make_tensor_map_sw64_3d(CUtensorMap *map, const void *ptr, int64_t r
 cudaError_t launch_cpb_table(const float *W1, const float *b1, const float *W2, int hidden, int M,
                              int heads, bool out_bf16, void *table, cudaStream_t stream);
 
+// G's weight gradients from its table gradient (fp32; heads <= 16).
+cudaError_t launch_cpb_backward(const float *W1, const float *b1, const float *W2, const float *dtable, int hidden,
+                                int M, int heads, float *dW1, float *db1, float *dW2, cudaStream_t stream);
+
 cudaError_t launch_watchdog(DeviceStatus st, cudaStream_t stream);
 
 // ---- backward (V1) ----------------------------------------------------------
@@ -184,9 +190,12 @@ cudaError_t launch_colsum(const bf16 *in, int64_t rows, int N, float *out, cudaS
 bool attn_backward_supported(int M, int C, int heads);
 // From qkv [T, 3C] and do [T, C] (window order): the attention output
 // attn [T, C] and dqkv [T, 3C] in token order, and dtable += ([(2M-1)^2,
-// heads] fp32).
-cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, int heads, const Geom &g,
-                                 bf16 *attn, bf16 *dqkv, float *dtable, DeviceStatus st, cudaStream_t stream);
+// heads] fp32).  v2: qkv holds unit-length q and k, norms [T, 2 heads] their
+// norms (the QKV GEMM's), tau [heads]; dqkv is then the gradient of the raw
+// q and k, and dtau += ([heads] fp32).
+cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, const float *tau, int heads,
+                                 int v2, const Geom &g, bf16 *attn, bf16 *dqkv, float *dtable, const float *norms,
+                                 float *dtau, DeviceStatus st, cudaStream_t stream);
 // The forward attention step alone on the same kernel (windows of <= 64
 // tokens): attn [T, C] (window order) = P v from qkv [T, 3C] (window order);
 // v2: cosine logits over the already normalised q, k, scaled by 1/max(tau, 0.01).

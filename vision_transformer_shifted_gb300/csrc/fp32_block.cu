@@ -141,6 +141,61 @@ __global__ void cpb_table_kernel(const float *W1, const float *b1, const float *
     }
 }
 
+// Gradient of G's weights from the gradient of its table (the chain rule
+// through table[idx, h] = sum_k W2[h, k] relu(W1[k] . u(idx) + b1[k])): one
+// thread per hidden unit k recomputes its pre-activation at every relative
+// offset and accumulates dW2[:, k], dW1[k, :] and db1[k] in registers (no
+// atomics).  dtable and the coordinates u come through shared memory.
+constexpr int CPB_MAX_HEADS = 16;
+
+__global__ void cpb_backward_kernel(const float *W1, const float *b1, const float *W2, const float *dtable, int hidden,
+                                    int M, int heads, float *dW1, float *db1, float *dW2)
+{
+    extern __shared__ float cpb_sm[];
+    const int L = 2 * M - 1, LL = L * L;
+    float *sdt = cpb_sm, *su = cpb_sm + LL * heads;
+    for (int e = threadIdx.x; e < LL * heads; e += blockDim.x) sdt[e] = dtable[e];
+    for (int idx = threadIdx.x; idx < LL; idx += blockDim.x) {
+        const int dr = idx / L - (M - 1), dc = idx % L - (M - 1);
+        su[2 * idx] = dr == 0 ? 0.f : copysignf(log1pf(fabsf((float)dr)), (float)dr);
+        su[2 * idx + 1] = dc == 0 ? 0.f : copysignf(log1pf(fabsf((float)dc)), (float)dc);
+    }
+    __syncthreads();
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= hidden) return;
+    const float w0 = W1[2 * k], w1 = W1[2 * k + 1], bb = b1 ? b1[k] : 0.f;
+    float w2[CPB_MAX_HEADS], acc[CPB_MAX_HEADS];
+#pragma unroll
+    for (int hd = 0; hd < CPB_MAX_HEADS; ++hd) {
+        w2[hd] = hd < heads ? W2[(int64_t)hd * hidden + k] : 0.f;
+        acc[hd] = 0.f;
+    }
+    float dw0 = 0.f, dw1 = 0.f, db = 0.f;
+    for (int idx = 0; idx < LL; ++idx) {
+        const float u0 = su[2 * idx], u1 = su[2 * idx + 1];
+        const float pre = fmaf(w0, u0, fmaf(w1, u1, bb));
+        if (pre <= 0.f) continue;
+        float dh = 0.f;
+#pragma unroll
+        for (int hd = 0; hd < CPB_MAX_HEADS; ++hd) {
+            if (hd < heads) {
+                const float g = sdt[idx * heads + hd];
+                dh = fmaf(g, w2[hd], dh);
+                acc[hd] = fmaf(g, pre, acc[hd]);
+            }
+        }
+        dw0 = fmaf(dh, u0, dw0);
+        dw1 = fmaf(dh, u1, dw1);
+        db += dh;
+    }
+    dW1[2 * k] = dw0;
+    dW1[2 * k + 1] = dw1;
+    if (db1) db1[k] = db;
+#pragma unroll
+    for (int hd = 0; hd < CPB_MAX_HEADS; ++hd)
+        if (hd < heads) dW2[(int64_t)hd * hidden + k] = acc[hd];
+}
+
 // Waits on an mbarrier that nothing arrives on, with the caller's limit, and
 // records the timeout: exercises the bounded-wait exit of the kernels.
 __global__ void watchdog_kernel(DeviceStatus st)
@@ -178,6 +233,19 @@ cudaError_t launch_cpb_table(const float *W1, const float *b1, const float *W2, 
     const int L = 2 * M - 1;
     cpb_table_kernel<<<L * L, 256, hidden * sizeof(float), stream>>>(W1, b1, W2, hidden, M, heads, out_bf16 ? 1 : 0,
                                                                    table);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cpb_backward(const float *W1, const float *b1, const float *W2, const float *dtable, int hidden,
+                                int M, int heads, float *dW1, float *db1, float *dW2, cudaStream_t stream)
+{
+    if (heads > CPB_MAX_HEADS || hidden <= 0) return cudaErrorInvalidValue;
+    const int L = 2 * M - 1;
+    const size_t smem = ((size_t)L * L * heads + 2 * (size_t)L * L) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(cpb_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cpb_backward_kernel<<<(hidden + 127) / 128, 128, smem, stream>>>(W1, b1, W2, dtable, hidden, M, heads, dW1, db1,
+                                                                     dW2);
     return cudaGetLastError();
 }
 

@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
                     v[i] += sbias[c0 + i];
                     ss = fmaf(v[i], v[i], ss);
                 }
-                const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+                const float nrm = fmaxf(sqrtf(ss), 1e-12f), inv = 1.0f / nrm;
                 float zero[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
                     zero[i] = 0.f;
                 }
                 if (dst_row) store_row_bf16(dst_row + c0, v, zero, 32);
+                if (a.norms && R < a.rows) a.norms[R * (a.norm_cols / 32) + (n0 + c0) / 32] = nrm;
             } else if (dst_row) {
                 if (a.epi == EPI_NONE) {
                     store_row_bf16(dst_row + c0, v, sbias + c0, 32);
@@ -317,7 +318,8 @@ __device__ __forceinline__ void rs_epilogue_chunk32(const GemmArgs &a, int64_t R
             v[i] += bias[i];
             ss = fmaf(v[i], v[i], ss);
         }
-        const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+        const float nrm = fmaxf(sqrtf(ss), 1e-12f), inv = 1.0f / nrm;
+        if (a.norms) a.norms[R * (a.norm_cols / 32) + n / 32] = nrm;
         float zero[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
