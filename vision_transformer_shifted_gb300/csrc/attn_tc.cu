@@ -128,7 +128,6 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
     const int qi = row_ok ? qt / M : 0, qj = row_ok ? qt % M : 0;
     const int my_region = token_region(g, wi, wj, qi, qj);
     const int base = (qi + M - 1) * L + (qj + M - 1);
-    const bf16 *wbase = a.qkv + win * N * (int64_t)(3 * C) + head * 32;
     const int ktiles = (N + 127) / 128;
 
     for (int i = tid; i < L * L; i += FL_THREADS)
