@@ -224,6 +224,7 @@ def _workload(key, **kw):
     ("swin_b_s3", dict(B=2)),                         # 16 heads, 3C = 1536
     ("swinv2_t_s1", dict(B=1, H=16, W=24, mode=0)),   # 8 x 8 windows (64 tokens, no padding), shift 4
     ("tiny", dict(B=3, H=4, W=6, M=2, shift=1, dtype="bf16")),  # 4-token windows, 2 x 3 of them per image
+    ("swin_t_s1", dict(B=1, H=7, W=21)),              # 3 windows: the last pair holds one window
 ])
 def test_backward_parity_small(key, kw):
     import torch as _t
@@ -349,6 +350,7 @@ def _check_dtau(dtau, factor):
     ("swinv2_t_s1", dict(B=1, H=14, W=21, M=7, shift=3), [0.1, 0.2, 1.0]),  # 7 x 7 windows, ragged tiles
     ("swinv2_t_s1", dict(B=1, H=16, W=24), [0.05, 0.2, 1.0]),
     ("swinv2_t_s1", dict(B=1, H=14, W=21, M=7, shift=3), [0.05, 0.2, 1.0]),
+    ("swinv2_t_s1", dict(B=1, H=8, W=24), [0.1, 0.2, 0.3]),                # 3 windows of 64 tokens
 ])
 def test_backward_v2_parity_small(key, kw, taus):
     import torch as _t
