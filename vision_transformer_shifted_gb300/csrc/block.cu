@@ -136,9 +136,12 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const bf16 *a, const bf1
 cudaError_t launch_layernorm(const bf16 *a, const bf16 *b, const bf16 *gamma, const bf16 *beta, bf16 *out_sum,
                              bf16 *out_ln, int64_t rows, int C, int flags, cudaStream_t stream, int mH = 0, int mW = 0)
 {
+    // lanes per row: a power of two with at least three 16-byte chunks per
+    // lane (several loads in flight per thread), at most 32; a row's lanes
+    // reduce its statistics by shuffles
     const int chunks = C / 8;
     int lpr = 1;
-    while (lpr < chunks && lpr < 32) lpr <<= 1;
+    while (lpr < 32 && 2 * lpr * 3 <= chunks) lpr <<= 1;
     const int cpl = (chunks + lpr - 1) / lpr;
     const int rows_per_block = (256 / 32) * (32 / lpr);
     const unsigned grid = (unsigned)((rows + rows_per_block - 1) / rows_per_block);
