@@ -589,7 +589,7 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
 
 // The resident-weight plan, or false when the weights (or two accumulators)
 // do not fit: N a multiple of 16, one tile column of N <= 256 or two halves,
-// the V2 normalisation's 32-column chunks whole, Bw within 140 KB.
+// the V2 normalisation's 32-column chunks whole, Bw within 152 KB.
 bool rs_plan(const GemmArgs &a, RsPlan &p)
 {
     if (a.N <= 0 || a.N % 16 || a.N > 512 || a.K <= 0 || a.K % 16) return false;
@@ -599,11 +599,11 @@ bool rs_plan(const GemmArgs &a, RsPlan &p)
     if (a.epi == EPI_RESID && ((a.ldr % 8) || (reinterpret_cast<uintptr_t>(a.R) & 15))) return false;
     p.KB = (a.K + 63) / 64;
     p.b_bytes = (size_t)a.N * p.KB * 128;
-    if (p.b_bytes > 140 * 1024) return false;
+    if (p.b_bytes > 152 * 1024) return false;
     const size_t fixed = 1024 + p.b_bytes + 512 * 4 + BM * 8 + 256;
     p.stages = (int)((227 * 1024 - fixed) / RS_STAGE);
     if (p.stages > 8) p.stages = 8;
-    if (p.stages < RS_DEPTH + 1) return false; // the gathered producer keeps RS_DEPTH stages in flight
+    if (p.stages < 3) return false;
     if (p.nbn == 2 && p.KB > p.stages) return false; // both halves read a block's stages
     p.tcols = 2 * p.BN <= 256 ? 256 : 512;
     p.smem = fixed + (size_t)p.stages * RS_STAGE;
@@ -953,7 +953,8 @@ cudaError_t launch_gemm_ts_test(const GemmArgs &a, DeviceStatus st, cudaStream_t
 cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, DeviceStatus st, cudaStream_t stream)
 {
     RsPlan pl;
-    if (a.rows > 0 && rs_plan(a, pl)) {
+    // (gathered rows: the producer keeps RS_DEPTH stages in flight)
+    if (a.rows > 0 && rs_plan(a, pl) && (load_mode != LOAD_GATHER || pl.stages >= RS_DEPTH + 1)) {
         if (load_mode == LOAD_GATHER && store_mode == STORE_PLAIN) return launch_rs<LOAD_GATHER, STORE_PLAIN>(a, pl, st, stream);
         if (load_mode == LOAD_PLAIN && store_mode == STORE_SCATTER) return launch_rs<LOAD_PLAIN, STORE_SCATTER>(a, pl, st, stream);
         if (load_mode == LOAD_PLAIN && store_mode == STORE_PLAIN) return launch_rs<LOAD_PLAIN, STORE_PLAIN>(a, pl, st, stream);
