@@ -188,12 +188,12 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
         FPHASE(kt, 0);
         if (kt + 1 < ktiles) load_keys(kt + 1, b ^ 1);
         FPHASE(kt, 1);
-        // tile kt (and, for kt = 0, the q rows) have landed
+        // tile kt (and, for kt = 0, the q rows) have landed.  (No CTA barrier
+        // here: the S MMA overwrites TMEM columns that every thread finished
+        // reading before the previous tile's P store barrier, and a failed
+        // wait becomes uniform at the next barrier.)
         if (!mbar_wait(smem_u32(&bars[2 + b]), (kt >> 1) & 1, st.wait_ns)) failed = true;
-        tc_fence_before();
-        if (__syncthreads_or(failed)) { failed = true; break; }
-        tc_fence_after();
-        if (tid == 0) {
+        if (tid == 0 && !failed) {
             const uint32_t id = idesc_bf16(128, 128);
 #pragma unroll
             for (int k = 0; k < 2; ++k)
@@ -304,8 +304,9 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
 #pragma unroll
         for (int e = 0; e < 16; ++e) o[e] = fmaf(o[e], alpha, ot[e] + ou[e]);
         FPHASE(kt, 9);
+        // (no CTA barrier: the next tile's max exchange and P store barriers
+        // order every reuse of TMEM and of the shared row maxima)
         tc_fence_before();
-        if (__syncthreads_or(failed)) { failed = true; break; }
         FPHASE(kt, 10);
     }
     spart[half * 128 + row] = l_run;
