@@ -412,7 +412,9 @@ cudaError_t launch_attention(const AttnArgs &a, DeviceStatus st, cudaStream_t st
         cudaError_t e = cudaFuncSetAttribute(attn_flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         CUtensorMap tmap;
-        e = make_tensor_map_sw64(&tmap, a.qkv, g.T, 3 * g.C, 128);
+        // CTAs of one head run together (grid y = head): the neighbouring
+        // head's 64 bytes of a row are read much later, so no 128-byte promotion
+        e = make_tensor_map_sw64(&tmap, a.qkv, g.T, 3 * g.C, 128, false);
         if (e != cudaSuccess) return e;
         const int qtiles = (g.N + 127) / 128;
         dim3 grid((unsigned)(g.nwin * qtiles), (unsigned)a.heads);
