@@ -237,6 +237,24 @@ def test_backward_parity_small(key, kw):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("key,kw", [
+    ("swin_t_s1", dict(B=1, H=24, W=36, M=12, shift=6)),   # 144-token windows: tiles of 128 and 16
+    ("swin_t_s1", dict(B=2, H=32, W=32, M=16, shift=0)),   # 256 tokens: two full tiles, no mask
+    ("swin_b_s1", dict(B=1, H=48, W=48, M=24, shift=12)),  # 576 tokens (4 tiles and 64), 4 heads
+    ("swin_t_s1", dict(B=1, H=24, W=48, M=24, shift=12)),  # 2 windows in a row, both masked
+])
+def test_backward_parity_large_windows(key, kw):
+    """Windows of more than 64 tokens: the forward keeps each row's
+    normaliser and the backward runs over (head, window, key tile) units."""
+    import torch as _t
+    if not _t.cuda.is_available():
+        pytest.skip("no GPU")
+    got, ref, launches = _run_backward(_workload(key, **kw))
+    _check_all(got, ref)
+    assert launches == 13
+
+
+@pytest.mark.gpu
 def test_backward_parity_full_size_swin_t_s1():
     """The whole 64 x 56 x 56 x 96 batch, every gradient entry (the float64
     oracle takes a few seconds for it)."""
@@ -278,13 +296,16 @@ def test_backward_empty_batch_and_refusals():
     finally:
         sw.swin_wattn_destroy(h)
     x1 = _t.zeros(1, 14, 14, C, dtype=_t.bfloat16, device="cuda")
-    for args, code in (((C, heads, 14, 3, sw.V1), sw.EUNSUPPORTED), ((C, heads, M, 3, sw.V2), sw.EINVAL)):
-        # windows of 196 tokens; V2 without tau
+    x32 = _t.zeros(1, 32, 32, C, dtype=_t.bfloat16, device="cuda")
+    for args, code, xa in (((C, heads, 32, 16, sw.V1), sw.EUNSUPPORTED, x32), ((C, heads, M, 3, sw.V2), sw.EINVAL, x1)):
+        # windows of 1024 tokens (their table gradient does not fit in shared
+        # memory); V2 without tau
         h = sw.swin_wattn_create(*args)
         try:
             tabh = _t.zeros((2 * args[2] - 1) ** 2, heads, dtype=_t.bfloat16, device="cuda")
+            outs_h = [z(3 * C, C), z(3 * C), z((2 * args[2] - 1) ** 2, heads), z(C, C), z(C)]
             with pytest.raises(sw.SwinWAttnError) as ei:
-                sw.swin_wattn_backward(h, x1, Wqkv, None, tabh, Wp, None, x1, _t.empty_like(x1), *outs)
+                sw.swin_wattn_backward(h, xa, Wqkv, None, tabh, Wp, None, xa, _t.empty_like(xa), *outs_h)
             assert ei.value.code == code
         finally:
             sw.swin_wattn_destroy(h)
@@ -363,6 +384,22 @@ def test_backward_v2_parity_small(key, kw, taus):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("key,kw,taus", [
+    ("swinv2_l_w24", dict(B=1, H=48, W=48), None),                                   # window 24, shift 12
+    ("swinv2_l_w24", dict(B=1, H=48, W=72, shift=0), [0.1, 0.005, 0.3, 1.0, 0.05, 0.2]),  # one head below the clip
+    ("swinv2_t_s1", dict(B=1, H=24, W=36, M=12, shift=6), [0.05, 0.2, 1.0]),        # 144 tokens
+])
+def test_backward_v2_parity_large_windows(key, kw, taus):
+    import torch as _t
+    if not _t.cuda.is_available():
+        pytest.skip("no GPU")
+    got, ref, dtau = _run_backward_v2(_workload(key, **kw), taus)
+    factor = _v2_factor(taus if taus is not None else [0.1])
+    _check_all(got, ref, factor)
+    _check_dtau(dtau, factor)
+
+
+@pytest.mark.gpu
 def test_backward_v2_parity_full_size_swinv2_t_s1():
     """The whole 32 x 64 x 64 x 96 SwinV2-T stage-1 batch, every gradient entry."""
     import torch as _t
@@ -371,3 +408,50 @@ def test_backward_v2_parity_full_size_swinv2_t_s1():
     got, ref, dtau = _run_backward_v2(_workload("swinv2_t_s1"))
     _check_all(got, ref)
     _check_dtau(dtau, 1.0)
+
+
+@pytest.mark.gpu
+def test_backward_v2_full_size_swinv2_l_w24_sampled_windows():
+    """The whole 4 x 384 x 384 x 192 batch (window 24, shift 12) through the
+    backward; the float64 oracle cannot hold its attention matrices, so dx is
+    checked on sampled unmasked windows: such a window's tokens form a plain
+    24 x 24 block of the original image, whose dx the oracle computes as a
+    one-window image without shift."""
+    import torch as _t
+    if not _t.cuda.is_available():
+        pytest.skip("no GPU")
+    from vision_transformer_shifted_gb300 import binding as sw
+    from vision_transformer_shifted_gb300.inputs import generate
+    w = _workload("swinv2_l_w24")
+    g = generate(w, nonzero_bias=True)
+    dy = _t.randn(g["x"].shape, generator=_t.Generator().manual_seed(6)).bfloat16()
+    f = {k: v.double().numpy() for k, v in g.items() if isinstance(v, _t.Tensor) and k != "x"}
+    table = obw.cpb_table(*(_t.tensor(f[k]) for k in ("W1", "b1", "W2")), M=w.M).to(_t.bfloat16).cuda()
+    dev = {k: v.cuda() for k, v in g.items() if isinstance(v, _t.Tensor)}
+    C, L = w.C, 2 * w.M - 1
+    dx = _t.empty_like(dev["x"])
+    outs = [_t.empty(3 * C, C, device="cuda"), _t.empty(3 * C, device="cuda"), _t.empty(L * L, w.heads, device="cuda"),
+            _t.empty(C, C, device="cuda"), _t.empty(C, device="cuda")]
+    dtau = _t.empty(w.heads, device="cuda")
+    h = sw.swin_wattn_create(C, w.heads, w.M, w.shift, sw.V2)
+    try:
+        sw.swin_wattn_backward(h, dev["x"], dev["Wqkv"], dev["bqkv"], table, dev["Wproj"], dev["bproj"], dy.cuda(),
+                               dx, *outs, logit_scale=dev["tau"], dlogit_scale=dtau)
+        assert sw.swin_wattn_sync_status(h) == sw.OK
+    finally:
+        sw.swin_wattn_destroy(h)
+    assert all(bool(_t.isfinite(o).all()) for o in outs + [dtau])
+    M, s = w.M, w.shift
+    rng = np.random.default_rng(11)
+    for _ in range(4):
+        b = int(rng.integers(w.B))
+        wi, wj = (int(v) for v in rng.integers(0, w.H // M - 1, size=2))
+        r0, c0 = wi * M + s, wj * M + s
+        xb = g["x"][b:b + 1, r0:r0 + M, c0:c0 + M].double().numpy()
+        dyb = dy[b:b + 1, r0:r0 + M, c0:c0 + M].double().numpy()
+        ref = obw.gradients_v2(xb, f["Wqkv"], f["bqkv"], f["tau"], f["W1"], f["b1"], f["W2"], f["Wproj"], f["bproj"],
+                               dyb, heads=w.heads, M=M, shift=0)["dx"]
+        got = dx[b:b + 1, r0:r0 + M, c0:c0 + M].double().cpu().numpy()
+        st = _rel_errors(got, ref)
+        print("window", b, wi, wj, st)
+        assert st["rel_l2"] <= GRAD_REL_L2 and st["max_rel"] <= GRAD_MAX_REL, (b, wi, wj, st)

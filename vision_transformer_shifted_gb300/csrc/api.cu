@@ -476,7 +476,12 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     const int C = h->C, L = 2 * h->M - 1;
     const size_t act = (size_t)B * H * W * C * 2;
     if (overlaps(dx, x, act) || overlaps(dx, dy, act)) return SWIN_WATTN_EINVAL;
-    if (h->fp32 || !attn_backward_supported(h->M, C, h->heads)) return SWIN_WATTN_EUNSUPPORTED;
+    // windows of <= 64 tokens: one kernel per (head, window pair); larger
+    // windows: the forward keeps its normaliser, then key-tile units
+    const bool flash = h->M * h->M > 64;
+    if (h->fp32 || !(flash ? attn_flash_backward_supported(h->M, C, h->heads)
+                           : attn_backward_supported(h->M, C, h->heads)))
+        return SWIN_WATTN_EUNSUPPORTED;
     const Geom g = make_geom(B, H, W, C, h->M, h->shift);
     if (g.T >= ((int64_t)1 << 31)) return SWIN_WATTN_EUNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream;
@@ -496,10 +501,13 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     }
     if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
     // workspace (bf16): attn, do [T, C]; qkv, dqkv [T, 3C]; WprojT [C, C]; WqkvT [C, 3C];
-    // V2: the norms of q and k, [T, 2 heads] fp32
+    // V2: the norms of q and k, [T, 2 heads] fp32; large windows: the
+    // forward's log2 normaliser and D = do.o, [T, heads] fp32 each, and the
+    // fp32 sums of dq [T, C]
     const size_t tc = (size_t)g.T * C;
     const size_t norm_bytes = v2 ? (size_t)g.T * 2 * h->heads * 4 : 0;
-    rc = ensure_buffer(&h->bws, &h->bws_bytes, (8 * tc + 4 * (size_t)C * C) * 2 + norm_bytes);
+    const size_t flash_bytes = flash ? (size_t)g.T * 2 * h->heads * 4 + tc * 4 : 0;
+    rc = ensure_buffer(&h->bws, &h->bws_bytes, (8 * tc + 4 * (size_t)C * C) * 2 + norm_bytes + flash_bytes);
     if (rc) return rc;
     if (!h->blas) {
         if (cublasCreate(&h->blas) != CUBLAS_STATUS_SUCCESS) { h->blas = nullptr; return SWIN_WATTN_ECUDA; }
@@ -507,7 +515,10 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     if (cublasSetStream(h->blas, s) != CUBLAS_STATUS_SUCCESS) return SWIN_WATTN_ECUDA;
     bf16 *attn = (bf16 *)h->bws, *dO = attn + tc, *qkv = dO + tc, *dqkv = qkv + 3 * tc;
     bf16 *WpT = dqkv + 3 * tc, *WqkvT = WpT + (size_t)C * C;
-    float *norms = v2 ? reinterpret_cast<float *>(WqkvT + 3 * (size_t)C * C) : nullptr;
+    float *fws = reinterpret_cast<float *>(WqkvT + 3 * (size_t)C * C);
+    float *norms = v2 ? fws : nullptr;
+    if (v2) fws += (size_t)g.T * 2 * h->heads;
+    float *lse = fws, *Drow = lse + (size_t)g.T * h->heads, *dq_acc = Drow + (size_t)g.T * h->heads;
     int launches = 0;
     auto step = [&](cudaError_t r) {
         if (e == cudaSuccess) { e = r; ++launches; }
@@ -525,8 +536,20 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     k3.g = g;
     step(launch_gemm(k3, LOAD_GATHER, STORE_PLAIN, dstatus(h), s));
     // o and dqkv in token order, dtable
-    step(launch_attn_backward(qkv, dO, (const bf16 *)bias_table, logit_scale, h->heads, v2 ? 1 : 0, g, attn, dqkv,
-                              dtable, norms, dlogit_scale, dstatus(h), s));
+    if (!flash) {
+        step(launch_attn_backward(qkv, dO, (const bf16 *)bias_table, logit_scale, h->heads, v2 ? 1 : 0, g, attn, dqkv,
+                                  dtable, norms, dlogit_scale, dstatus(h), s));
+    } else {
+        AttnArgs k2{};
+        k2.qkv = qkv; k2.attn = attn; k2.table = (const bf16 *)bias_table; k2.tau = logit_scale;
+        k2.heads = h->heads; k2.mode = h->mode; k2.g = g; k2.lse = lse; k2.o_token_order = 1;
+        step(launch_attention(k2, dstatus(h), s));
+        zero(dq_acc, tc);
+        // D, the key-tile kernel and the dq conversion: three launches
+        step(launch_attn_flash_backward(qkv, dO, attn, (const bf16 *)bias_table, logit_scale, h->heads, v2 ? 1 : 0,
+                                        g, lse, Drow, norms, dqkv, dq_acc, dtable, dlogit_scale, dstatus(h), s));
+        launches += 2;
+    }
     // dx = dqkv Wqkv (token order already)
     GemmArgs k4{};
     k4.A = dqkv; k4.lda = 3 * C; k4.Bw = WqkvT; k4.D = (bf16 *)dx; k4.ldd = C; k4.rows = g.T; k4.N = C;

@@ -313,7 +313,10 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
     __syncthreads();
     if (!failed && row_ok) {
         const float l = spart[row] + spart[128 + row];
-        store_o<16>(a.attn + (win * N + qt) * (int64_t)C + head * 32 + 16 * half, o, rcp_approx(l));
+        const int64_t orow = a.o_token_order ? window_row_to_token(g, win * N + qt) : win * N + qt;
+        store_o<16>(a.attn + orow * (int64_t)C + head * 32 + 16 * half, o, rcp_approx(l));
+        // log2 of the normaliser: p = exp2(logit2 - lse) for the log2-scaled logits
+        if (a.lse && half == 0) a.lse[(win * N + qt) * a.heads + head] = m_run + log2f(l);
     }
     if (failed && tid == 0) atomicOr(st.err, ERR_TIMEOUT);
     tc_fence_before();

@@ -127,11 +127,14 @@ cudaError_t launch_gemm_pair_test(const GemmArgs &a, DeviceStatus st, cudaStream
 
 struct AttnArgs {
     const bf16 *qkv;      // [T, 3C] window order
-    bf16 *attn;           // [T, C] window order
+    bf16 *attn;           // [T, C] window order (token order with o_token_order)
     const bf16 *table;    // [(2M-1)^2, heads]
     const float *tau;     // [heads] (V2)
     int heads, mode;      // mode 0 = V1, 1 = V2
     Geom g;
+    float *lse;           // windows of more than 64 tokens, not null: log2 of each row's softmax
+                          // normaliser over the log2-scaled logits, [T, heads] (window order)
+    int o_token_order;    // windows of more than 64 tokens: write attn in token order
 };
 
 cudaError_t launch_attention(const AttnArgs &a, DeviceStatus st, cudaStream_t stream);
@@ -196,6 +199,16 @@ bool attn_backward_supported(int M, int C, int heads);
 cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, const float *tau, int heads,
                                  int v2, const Geom &g, bf16 *attn, bf16 *dqkv, float *dtable, const float *norms,
                                  float *dtau, DeviceStatus st, cudaStream_t stream);
+// Windows of more than 64 tokens (up to 24 x 24) and 32 channels per head.
+bool attn_flash_backward_supported(int M, int C, int heads);
+// The same gradients for large windows from the forward's outputs: attn
+// [T, C] (token order) and lse [T, heads] (window order; log2 of each row's
+// softmax normaliser over the log2-scaled logits).  D [T, heads] is
+// scratch; dq_acc [T, C] fp32 must be zero on entry.  Three launches.
+cudaError_t launch_attn_flash_backward(const bf16 *qkv, const bf16 *dO, const bf16 *attn, const bf16 *table,
+                                       const float *tau, int heads, int v2, const Geom &g, const float *lse, float *D,
+                                       const float *norms, bf16 *dqkv, float *dq_acc, float *dtable, float *dtau,
+                                       DeviceStatus st, cudaStream_t stream);
 // The forward attention step alone on the same kernel (windows of <= 64
 // tokens): attn [T, C] (window order) = P v from qkv [T, 3C] (window order);
 // v2: cosine logits over the already normalised q, k, scaled by 1/max(tau, 0.01).
