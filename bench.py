@@ -603,6 +603,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="swin_t_s1", choices=sorted(WORKLOADS))
+    ap.add_argument("--batch", type=int, default=0, help="images per step (0: the workload's own batch)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 three kernels, 2 fused")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
@@ -619,6 +620,10 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
+    if args.batch > 0 and args.batch != w.B:
+        # another batch is another workload: it carries its own name (and no
+        # profiled traffic figure)
+        w = w.with_(B=args.batch, key="%s_b%d" % (w.key, args.batch))
     if args.stage > 0:
         if w.dtype != "bf16" or args.impl != "ours" or args.gpus != 1 or (w.H // 2) % 1:
             ap.error("--stage: bf16 workloads, our implementation, one GPU")

@@ -23,21 +23,65 @@ namespace swin {
 namespace {
 
 constexpr int FB_THREADS = 256;
+constexpr int FB_MAX_TILES = 5;   // windows of up to 640 tokens
+
+// Table-gradient terms are summed in shared memory as fixed-point integers
+// (shared-memory integer atomics are far cheaper than floating-point ones):
+// a term x with |x| < FIX_MAX becomes round(x * 2^19).  One table entry gets at
+// most one term per key of a (key tile, query tile) pair, so a unit (at most
+// FB_MAX_TILES query tiles of 128 keys) adds at most 640 terms, each below
+// 2^21 in size: the 32-bit sum cannot overflow, and it is moved into the fp32
+// table after every unit.  Larger terms go to the fp32 table directly.
+constexpr float FIX_SCALE = 524288.0f, FIX_INV = 1.0f / 524288.0f, FIX_MAX = 4.0f;
+static_assert(FB_MAX_TILES * 128 * 4.0 * 524288.0 < 2147483647.0, "fixed-point table sums may overflow");
+// round(y) for |y| < 2^22 through the float adder: y + 1.5 * 2^23 lies in
+// [2^23, 2^24), where floats are spaced by exactly 1, so the addition rounds y
+// to the nearest integer and the low mantissa bits hold it (offset by the
+// bits of 1.5 * 2^23).
+__device__ __forceinline__ int fb_round_fix(float x)
+{
+    return __float_as_int(fmaf(x, FIX_SCALE, 12582912.0f)) - 0x4B400000;
+}
+
+// Optional phase trace (-DSWIN_PHASE_TRACE only): threads 0 and 224 of CTA 5
+// record clock64() at seven points of each of the first 16 query-tile steps.
+#ifdef SWIN_PHASE_TRACE
+__device__ long long g_fbw_trace[2 * 16 * 8];
+#define BPHASE(step, i)                                                                            \
+    do {                                                                                           \
+        if (blockIdx.x == 5 && (tid == 0 || tid == 224) && (step) < 16)                            \
+            g_fbw_trace[((tid ? 1 : 0) * 16 + (step)) * 8 + (i)] = clock64();                      \
+    } while (0)
+#else
+#define BPHASE(step, i) \
+    do {                \
+    } while (0)
+#endif
 
 struct FbLayout {
-    // byte offsets from the 1024-aligned base
+    // byte offsets from the 512-aligned base
     static constexpr uint32_t K = 0, V = 8192, Q = 16384, DO = 24576; // [128 rows][64 B] tiles
-    static constexpr uint32_t P = 32768, DS = 65536;                   // 4 panels [128 keys][32 queries]
-    static constexpr uint32_t QB = 98304;                              // int [128]: relative-index base of each query (-1: none)
-    static constexpr uint32_t QR = QB + 512;                           // int [128]: shift region of each query
-    static constexpr uint32_t LSE = QR + 512;                          // float [128]
+    static constexpr uint32_t DS = 32768;                              // 4 panels [128 keys][32 queries]
+    // per query of the tile: its relative-index bases in the bias table and in
+    // the padded gradient table, and its shift region (-1: no query)
+    static constexpr uint32_t QC = 65536;                              // int [128]
+    static constexpr uint32_t LSE = QC + 512;                          // float [128]
     static constexpr uint32_t DD = LSE + 512;                          // float [128]
     static constexpr uint32_t BIAS = DD + 512;                         // bf16 [(2M-1)^2] of the current head
     __host__ __device__ static uint32_t ll_pad(int M) { return ((uint32_t)(2 * M - 1) * (2 * M - 1) + 7u) & ~7u; }
+    // Row stride of the shared table gradient (>= 2M-1, = M mod 32): for one
+    // query, a warp's 32 consecutive keys address consecutive words within a
+    // window row, and the step to the next row (-(stride - M + 1)) is then
+    // also -1 modulo 32, so the 32 lanes of one atomic add fall in 32 banks.
+    __host__ __device__ static int lp(int M) { return M + 32 * ((M - 1 + 31) / 32); }
+    __host__ __device__ static uint32_t dt_pad(int M) { return ((uint32_t)(2 * M - 1) * lp(M) + 3u) & ~3u; }
+    // the table gradient: fp32, and the fixed-point sums of the current unit
     __host__ __device__ static uint32_t dtab(int M) { return BIAS + 2 * ll_pad(M); }
-    __host__ __device__ static uint32_t bar(int M) { return dtab(M) + 4 * ll_pad(M); }
+    __host__ __device__ static uint32_t dti(int M) { return dtab(M) + 4 * dt_pad(M); }
+    __host__ __device__ static uint32_t bar(int M) { return dti(M) + 4 * dt_pad(M); }
     // four mbarriers, then the TMEM address slot
-    static size_t bytes(int M) { return (size_t)bar(M) + 48 + 1024; }
+    // (64-byte swizzle atoms repeat every 512 bytes: the base is 512-aligned)
+    static size_t bytes(int M) { return (size_t)bar(M) + 48 + 512; }
 };
 
 __device__ __forceinline__ int fb_band(int p, int n, int M, int s) { return p < n - M ? 0 : (p < n - s ? 1 : 2); }
@@ -100,16 +144,16 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
 {
     extern __shared__ uint8_t smraw[];
     using Ly = FbLayout;
-    uint8_t *sm = smem_align(smraw, 1024);
+    uint8_t *sm = smem_align(smraw, 512);
     const uint32_t base = smem_u32(sm);
-    const int N = g.N, M = g.M, C = g.C, L = 2 * M - 1, LL = L * L;
+    const int N = g.N, M = g.M, C = g.C, L = 2 * M - 1, LL = L * L, LP = Ly::lp(M);
     const int KT = (N + 127) / 128;                 // key tiles and query tiles per window
-    int *qbase = reinterpret_cast<int *>(sm + Ly::QB);
-    int *qreg = reinterpret_cast<int *>(sm + Ly::QR);
+    int *qcode = reinterpret_cast<int *>(sm + Ly::QC);
     float *slse = reinterpret_cast<float *>(sm + Ly::LSE);
     float *sdd = reinterpret_cast<float *>(sm + Ly::DD);
     const bf16 *sbias = reinterpret_cast<const bf16 *>(sm + Ly::BIAS);
     float *dtab = reinterpret_cast<float *>(sm + Ly::dtab(M));
+    int *dti = reinterpret_cast<int *>(sm + Ly::dti(M));
     const uint32_t bar_kv = base + Ly::bar(M), bar_q = bar_kv + 8, bar_s = bar_kv + 16, bar_o = bar_kv + 24;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + Ly::bar(M) + 32);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -119,7 +163,10 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
     const int64_t nunits = (int64_t)heads * g.nwin * KT;
     const float LOG2E = 1.4426950408889634f;
 
-    for (int e = tid; e < (int)Ly::ll_pad(M); e += FB_THREADS) dtab[e] = 0.f;
+    for (int e = tid; e < (int)Ly::dt_pad(M); e += FB_THREADS) {
+        dtab[e] = 0.f;
+        dti[e] = 0;
+    }
     if (tid == 0) {
         mbar_init(bar_kv, 1);
         mbar_init(bar_q, 1);
@@ -167,6 +214,19 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
     int cur_head = -1;
     float scale = 0.17677669529663687f; // logit scale of the current head (V1: 1 / sqrt(32))
     float tau_acc = 0.f;
+    // threads 0..127: lse and D of query `tid` of the next query tile, fetched
+    // one tile ahead so that their latency hides under the previous epilogue
+    float nl = 0.f, nd = 0.f;
+    auto fetch_rows = [&](int hd, int64_t w, int qt_) {
+        if (tid < 128) {
+            const int q = qt_ * 128 + tid;
+            nl = nd = 0.f;
+            if (q < N) {
+                nl = lse[(w * N + q) * heads + hd];
+                nd = Dr[(w * N + q) * heads + hd];
+            }
+        }
+    };
 
     auto flush_head = [&]() {
         if (v2) {
@@ -179,8 +239,9 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
         }
         __syncthreads();
         for (int e = tid; e < LL; e += FB_THREADS) {
-            if (dtab[e] != 0.f) atomicAdd(&dtable[(int64_t)e * heads + cur_head], dtab[e]);
-            dtab[e] = 0.f;
+            float *t = dtab + (e / L) * LP + (e - (e / L) * L);
+            if (*t != 0.f) atomicAdd(&dtable[(int64_t)e * heads + cur_head], *t);
+            *t = 0.f;
         }
     };
 
@@ -193,7 +254,10 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
             load_q(h0, w0, 0);
         }
         kv_pend = q_pend = true;
+        fetch_rows(h0, w0, 0);
     }
+    int step = 0;   // query-tile steps of this CTA (phase trace only)
+    (void)step;
     for (int64_t u = u_begin; u < u_end && !failed; ++u) {
         int head, kt;
         int64_t win;
@@ -206,47 +270,48 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
                 reinterpret_cast<bf16 *>(sm + Ly::BIAS)[e] = table[(int64_t)e * heads + head];
             if (v2) scale = 1.0f / fmaxf(tau[head], 0.01f);
             cur_head = head;
-            __syncthreads();
+            // (the barrier before the first MMA below orders these writes)
         }
         const float sc2 = scale * LOG2E;
-        // this thread's key (S^T row r)
+        // this thread's key (S^T row r); keys past the window match no query
         const int j = kt * 128 + r;
         const bool kvalid = j < N;
         const int kofs = kvalid ? (j / M) * L + (j % M) : 0;
-        const int kreg = kvalid ? fb_region(g, wi, wj, j) : -2;
+        const int kofsp = kvalid ? (j / M) * LP + (j % M) : 0;
+        const int kreg = kvalid ? fb_region(g, wi, wj, j) : 0x7FFF;
         float acc[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) acc[c] = 0.f;
 
-        for (int qt = 0; qt < KT; ++qt) {
-            // the query tile's metadata
+        for (int qt = 0; qt < KT; ++qt, ++step) {
+            BPHASE(step, 0);
+            // the query tile's metadata (its previous readers passed the P
+            // store barrier of the last tile)
             if (tid < 128) {
                 const int q = qt * 128 + tid;
-                int qb = -1, qr = -1;
-                float lv = 0.f, dv = 0.f;
+                int code = -1;
                 if (q < N) {
                     const int qi = q / M, qj = q - (q / M) * M;
-                    qb = (qi + M - 1) * L + (qj + M - 1);
-                    qr = fb_region(g, wi, wj, q);
-                    lv = lse[(win * N + q) * heads + head];
-                    dv = Dr[(win * N + q) * heads + head];
+                    code = ((qi + M - 1) * L + (qj + M - 1)) | (((qi + M - 1) * LP + (qj + M - 1)) << 12) |
+                           (fb_region(g, wi, wj, q) << 24);
                 }
-                qbase[tid] = qb;
-                qreg[tid] = qr;
-                slse[tid] = lv;
-                sdd[tid] = dv;
+                qcode[tid] = code;
+                slse[tid] = nl;
+                sdd[tid] = nd;
             }
             bool ok = true;
             if (qt == 0) ok = mbar_wait(bar_kv, ph_kv, st.wait_ns);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
+            ok = ok && mbar_wait(bar_q, ph_q, st.wait_ns);
+            // A: tiles landed, metadata visible, the last TMEM reads done
+            tc_fence_before();
+            if (__syncthreads_or(!ok || failed)) { failed = true; break; }
+            tc_fence_after();
+            BPHASE(step, 1);
             if (qt == 0) { ph_kv ^= 1; kv_pend = false; }
-            ok = mbar_wait(bar_q, ph_q, st.wait_ns);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
             ph_q ^= 1;
             q_pend = false;
             if (tid == 0 || tid == 128) {
                 // S^T by thread 0, dP^T by thread 128
-                tc_fence_after();
                 const uint32_t id = idesc_bf16(128, 128);
                 const uint32_t a = tid == 0 ? Ly::K : Ly::V, b = tid == 0 ? Ly::Q : Ly::DO;
 #pragma unroll
@@ -256,91 +321,129 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
                 mma_commit(bar_s);
             }
             s_pend = true;
-            ok = mbar_wait(bar_s, ph_mma, st.wait_ns);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-            s_pend = false;
+            if (mbar_wait(bar_s, ph_mma, st.wait_ns)) s_pend = false;
+            else failed = true;     // (uniform at the next barrier)
             tc_fence_after();
+            BPHASE(step, 2);
 
-            // ---- P^T and dS^T of key row r, queries 64*h2 .. +63, 16 at a time ----
+            // ---- P^T and dS^T of key row r, queries 64*h2 .. +63, 8 at a time ----
 #pragma unroll 1
-            for (int hh = 0; hh < 4; ++hh) {
-                const int i0 = 64 * h2 + 16 * hh;
-                float s[16], d[16];
-                tmem_ld16(t_lane + i0, s);
-                tmem_ld16(t_lane + 128 + i0, d);
-                tmem_wait_ld();
+            for (int hh = 0; hh < 8; ++hh) {
+                const int i0 = 64 * h2 + 8 * hh;
+                float s[8], d[8];
+                tmem_ld8(t_lane + i0, s);
+                tmem_ld8(t_lane + 128 + i0, d);
+                int idx[8], idxp[8];   // bias and gradient table entries (-1: masked pair)
+                {
+                    const int4 *c4 = reinterpret_cast<const int4 *>(qcode + i0);
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int i = i0 + jj;
-                    const int qb = qbase[i];
-                    const bool valid = kvalid && qb >= 0 && qreg[i] == kreg;
-                    const int idx = valid ? qb - kofs : 0;
-                    const float b = __bfloat162float(sbias[idx]);
-                    const float p = valid ? ex2_approx(fmaf(s[jj], sc2, fmaf(b, LOG2E, -slse[i]))) : 0.f;
-                    const float ds = p * (d[jj] - sdd[i]);
-                    if (v2) tau_acc = fmaf(ds, s[jj], tau_acc);
-                    if (ds != 0.f) atomicAdd(&dtab[idx], ds);
-                    s[jj] = p;
-                    d[jj] = ds;
+                    for (int v = 0; v < 2; ++v) {
+                        const int4 c = c4[v];
+                        const int cc[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const bool valid = (cc[t] >> 24) == kreg;
+                            idx[4 * v + t] = valid ? (cc[t] & 0xFFF) - kofs : -1;
+                            idxp[4 * v + t] = ((cc[t] >> 12) & 0xFFF) - kofsp;
+                        }
+                    }
                 }
-                // queries i0 .. i0+15: panel i0 / 32, 16-byte chunks 2 (i0 / 16 mod 2) ..
+                // every bias load ahead of the table-gradient atomics below
+                float bv[8];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const uint32_t off = (uint32_t)(i0 >> 5) * 8192u + sw64_offset(r, 2 * (hh & 1) + c);
-                    fb_store8(base + Ly::P + off, s + 8 * c);
-                    fb_store8(base + Ly::DS + off, d + 8 * c);
+                for (int jj = 0; jj < 8; ++jj)
+                    bv[jj] = __bfloat162float(sbias[idx[jj] >= 0 ? idx[jj] : 0]);
+                tmem_wait_ld();
+                {
+                    const float4 *l4 = reinterpret_cast<const float4 *>(slse + i0);
+                    const float4 *d4 = reinterpret_cast<const float4 *>(sdd + i0);
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        const float4 lv = l4[v], dv = d4[v];
+                        const float ll[4] = {lv.x, lv.y, lv.z, lv.w}, dd[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int jj = 4 * v + t;
+                            const float p = idx[jj] >= 0 ? ex2_approx(fmaf(s[jj], sc2, fmaf(bv[jj], LOG2E, -ll[t])))
+                                                         : 0.f;
+                            const float ds = p * (d[jj] - dd[t]);
+                            if (v2) tau_acc = fmaf(ds, s[jj], tau_acc);
+                            s[jj] = p;
+                            d[jj] = ds;
+                        }
+                    }
+                }
+                // P^T of queries i0 .. i0+7 as bf16 pairs over TMEM columns
+                // 64 h2 + 4 hh .. +3 (S^T columns this thread has read already);
+                // dS^T to shared panel i0 / 32, 16-byte chunk i0 / 8 mod 4
+                tmem_st4(t_lane + 64 * h2 + 4 * hh, pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]),
+                         pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
+                fb_store8(base + Ly::DS + (uint32_t)(i0 >> 5) * 8192u + sw64_offset(r, hh & 3), d);
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    if (idx[jj] < 0) continue;
+                    if (fabsf(d[jj]) < FIX_MAX) atomicAdd(&dti[idxp[jj]], fb_round_fix(d[jj]));
+                    else atomicAdd(&dtab[idxp[jj]], d[jj]);
                 }
             }
+            BPHASE(step, 3);
+            tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
-            __syncthreads();
+            // B: P^T and dS^T panels complete
+            if (__syncthreads_or(failed)) { failed = true; break; }
+            BPHASE(step, 4);
             if (lane == 0 && (warp == 0 || warp == 1 || warp == 4)) {
-                // dv (warp 0), dk (warp 1), dq (warp 4)
+                // TMEM columns: P^T over 0..31 and 64..95; dv (warp 0) into
+                // 32..63, dk (warp 1) into 96..127, dq (warp 4) into 160..191
                 tc_fence_after();
                 const int which = warp == 0 ? 0 : (warp == 1 ? 1 : 2);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t kpan = (uint32_t)(kk >> 1) * 8192u + 32u * (kk & 1);
                     if (which == 0)
-                        mma_bf16(tmem + 0, desc_kmajor_sw64(base + Ly::P + kpan),
-                                 desc_mnmajor_sw64(base + Ly::DO + 1024 * kk, 8192), idesc_bf16_bmn(128, 32), kk);
+                        mma_bf16_ts(tmem + 32, tmem + 64 * (kk >> 2) + 8 * (kk & 3),
+                                    desc_mnmajor_sw64(base + Ly::DO + 1024 * kk, 8192), idesc_bf16_bmn(128, 32), kk);
                     else if (which == 1)
-                        mma_bf16(tmem + 32, desc_kmajor_sw64(base + Ly::DS + kpan),
+                        mma_bf16(tmem + 96, desc_kmajor_sw64(base + Ly::DS + kpan),
                                  desc_mnmajor_sw64(base + Ly::Q + 1024 * kk, 8192), idesc_bf16_bmn(128, 32), kk);
                     else
-                        mma_bf16(tmem + 64, desc_mnmajor_sw64(base + Ly::DS + 1024 * kk, 8192),
+                        mma_bf16(tmem + 160, desc_mnmajor_sw64(base + Ly::DS + 1024 * kk, 8192),
                                  desc_mnmajor_sw64(base + Ly::K + 1024 * kk, 8192), idesc_bf16_amn_bmn(128, 32), kk);
                 }
                 mma_commit(bar_o);
             }
             o_pend = true;
-            ok = mbar_wait(bar_o, ph_mma, st.wait_ns);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
+            if (mbar_wait(bar_o, ph_mma, st.wait_ns)) o_pend = false;
+            else failed = true;     // (uniform at the next barrier)
             ph_mma ^= 1;
-            o_pend = false;
             tc_fence_after();
-            // q and do are free: the next query tile's (or the next unit's first)
-            // loads run under the epilogue
+            BPHASE(step, 5);
+            // q and do are free (every MMA reading them has completed): the
+            // next query tile's (or the next unit's first) loads and row data
+            // come in under the epilogue
             if (qt + 1 < KT) {
-                if (tid == 0) load_q(head, win, qt + 1);
+                if (tid == 0 && !failed) load_q(head, win, qt + 1);
                 q_pend = true;
+                fetch_rows(head, win, qt + 1);
             } else if (u + 1 < u_end) {
                 int h1, k1;
                 int64_t w1;
                 decode(u + 1, h1, w1, k1);
-                if (tid == 0) load_q(h1, w1, 0);
+                if (tid == 0 && !failed) load_q(h1, w1, 0);
                 q_pend = true;
+                fetch_rows(h1, w1, 0);
             }
 
             // ---- dv / dk of key row r into registers; dq of query row r to the fp32 buffer ----
             {
                 float a[32];
-                tmem_ld32(t_lane + 32 * h2, a);
+                tmem_ld32(t_lane + 32 + 64 * h2, a);
                 tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < 32; ++c) acc[c] += a[c];
                 float dq[16];
-                tmem_ld16(t_lane + 64 + 16 * h2, dq);
+                tmem_ld16(t_lane + 160 + 16 * h2, dq);
                 tmem_wait_ld();
                 const int q = qt * 128 + r;
                 if (q < N) {
@@ -350,8 +453,7 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
                         atomicAdd(dst + c, make_float4(dq[4 * c], dq[4 * c + 1], dq[4 * c + 2], dq[4 * c + 3]));
                 }
             }
-            tc_fence_before();
-            __syncthreads();
+            BPHASE(step, 6);
         }
         if (failed) break;
         // the next unit's k and v (this unit's MMAs are done; V2 reads the k
@@ -379,7 +481,18 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
                 *reinterpret_cast<uint4 *>(dst + 8 * q4) = w;
             }
         }
+        // the k tile and the bias matrix are read by now; TMEM reads done
+        tc_fence_before();
         __syncthreads();
+        // this unit's fixed-point table sums into the fp32 table (the next
+        // unit's first barrier orders this before its atomics)
+        for (int e = tid; e < (int)Ly::dt_pad(M); e += FB_THREADS) {
+            const int v = dti[e];
+            if (v != 0) {
+                dtab[e] = fmaf((float)v, FIX_INV, dtab[e]);
+                dti[e] = 0;
+            }
+        }
         if (v2 && u + 1 < u_end) {
             if (tid == 0) load_kv(u + 1);
             kv_pend = true;
@@ -491,9 +604,19 @@ unsigned grid_for(int64_t n)
 
 } // namespace
 
+#ifdef SWIN_PHASE_TRACE
+extern "C" int swin_wattn_fbw_trace(long long *host, int n)
+{
+    return (int)cudaMemcpyFromSymbol(host, g_fbw_trace, sizeof(long long) * (size_t)n);
+}
+#endif
+
 bool attn_flash_backward_supported(int M, int C, int heads)
 {
-    return M * M > 64 && C == heads * 32 && FbLayout::bytes(M) <= 113 * 1024;
+    // (the table bases of a query are packed in 12 bits each)
+    return M * M > 64 && (M * M + 127) / 128 <= FB_MAX_TILES && C == heads * 32 &&
+           (2 * M - 2) * (FbLayout::lp(M) + 1) < 4096 &&
+           FbLayout::bytes(M) <= 113 * 1024;
 }
 
 cudaError_t launch_attn_flash_backward(const bf16 *qkv, const bf16 *dO, const bf16 *attn, const bf16 *table,
