@@ -102,7 +102,8 @@ struct GemmArgs {
     int norm_cols;   // > 0: output columns below it are scaled, 32 at a time, to
                      // unit L2 norm (V2 q and k heads); 0: none
     float *norms;    // norm_cols > 0 and not null: the clamped norm max(|v|, 1e-12) of each
-                     // normalised 32-column chunk, [rows, norm_cols / 32] fp32
+                     // normalised 32-column chunk, [rows, norms_ld] fp32
+    int norms_ld;    // row stride of norms (0: norm_cols / 32)
     int epi;         // EPI_NONE, EPI_GELU (GELU after the bias), EPI_RESID (add R after the bias)
     const bf16 *R;   // EPI_RESID: [rows, ldr] row-major (plain store only)
     int64_t ldr;

@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
                     zero[i] = 0.f;
                 }
                 if (dst_row) store_row_bf16(dst_row + c0, v, zero, 32);
-                if (a.norms && R < a.rows) a.norms[R * (a.norm_cols / 32) + (n0 + c0) / 32] = nrm;
+                if (a.norms && R < a.rows) a.norms[R * (a.norms_ld ? a.norms_ld : a.norm_cols / 32) + (n0 + c0) / 32] = nrm;
             } else if (dst_row) {
                 if (a.epi == EPI_NONE) {
                     store_row_bf16(dst_row + c0, v, sbias + c0, 32);
@@ -319,7 +319,7 @@ __device__ __forceinline__ void rs_epilogue_chunk32(const GemmArgs &a, int64_t R
             ss = fmaf(v[i], v[i], ss);
         }
         const float nrm = fmaxf(sqrtf(ss), 1e-12f), inv = 1.0f / nrm;
-        if (a.norms) a.norms[R * (a.norm_cols / 32) + n / 32] = nrm;
+        if (a.norms) a.norms[R * (a.norms_ld ? a.norms_ld : a.norm_cols / 32) + n / 32] = nrm;
         float zero[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -950,14 +950,54 @@ cudaError_t launch_gemm_ts_test(const GemmArgs &a, DeviceStatus st, cudaStream_t
     return cudaGetLastError();
 }
 
+// Column chunk c0 .. c0+n of a plain-store GEMM as a GEMM of its own (its
+// weight rows, bias, output columns, residual columns and normalised chunks).
+static GemmArgs column_chunk(const GemmArgs &a, int c0, int n)
+{
+    GemmArgs c = a;
+    c.Bw = a.Bw + (int64_t)c0 * a.K;
+    if (a.bias) c.bias = a.bias + c0;
+    c.D = a.D + c0;
+    c.N = n;
+    if (a.R) c.R = a.R + c0;
+    if (a.norm_cols > 0) {
+        c.norm_cols = a.norm_cols - c0 < 0 ? 0 : (a.norm_cols - c0 > n ? n : a.norm_cols - c0);
+        c.norms_ld = a.norms_ld ? a.norms_ld : a.norm_cols / 32;
+        c.norms = a.norms && c.norm_cols > 0 ? a.norms + c0 / 32 : nullptr;
+    }
+    return c;
+}
+
 cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, DeviceStatus st, cudaStream_t stream)
 {
     RsPlan pl;
     // (gathered rows: the producer keeps RS_DEPTH stages in flight)
-    if (a.rows > 0 && rs_plan(a, pl) && (load_mode != LOAD_GATHER || pl.stages >= RS_DEPTH + 1)) {
+    auto rs_ok = [&](const GemmArgs &x, RsPlan &p) {
+        return x.rows > 0 && rs_plan(x, p) && (load_mode != LOAD_GATHER || p.stages >= RS_DEPTH + 1);
+    };
+    if (rs_ok(a, pl)) {
         if (load_mode == LOAD_GATHER && store_mode == STORE_PLAIN) return launch_rs<LOAD_GATHER, STORE_PLAIN>(a, pl, st, stream);
         if (load_mode == LOAD_PLAIN && store_mode == STORE_SCATTER) return launch_rs<LOAD_PLAIN, STORE_SCATTER>(a, pl, st, stream);
         if (load_mode == LOAD_PLAIN && store_mode == STORE_PLAIN) return launch_rs<LOAD_PLAIN, STORE_PLAIN>(a, pl, st, stream);
+    }
+    // weights too large to stay resident: 2 to 4 column chunks that each fit,
+    // one launch per chunk.  Each launch reads A again, so only where A is no
+    // wider than the output (the QKV and the first MLP projections).
+    if (store_mode == STORE_PLAIN && a.rows > 0 && a.K <= a.N) {
+        for (int nc = 2; nc <= 4; ++nc) {
+            if (a.N % nc || (a.N / nc) % 16) continue;
+            const int n = a.N / nc;
+            if (a.norm_cols > 0 && (n % 32 || a.norm_cols % 32)) continue;
+            GemmArgs c0 = column_chunk(a, 0, n);
+            if (!rs_ok(c0, pl)) continue;
+            for (int i = 0; i < nc; ++i) {
+                const GemmArgs c = column_chunk(a, i * n, n);
+                cudaError_t e = load_mode == LOAD_GATHER ? launch_rs<LOAD_GATHER, STORE_PLAIN>(c, pl, st, stream)
+                                                         : launch_rs<LOAD_PLAIN, STORE_PLAIN>(c, pl, st, stream);
+                if (e != cudaSuccess) return e;
+            }
+            return cudaSuccess;
+        }
     }
     if (load_mode == LOAD_GATHER && store_mode == STORE_PLAIN) return launch_impl<LOAD_GATHER, STORE_PLAIN>(a, st, stream);
     if (load_mode == LOAD_PLAIN && store_mode == STORE_SCATTER) return launch_impl<LOAD_PLAIN, STORE_SCATTER>(a, st, stream);
