@@ -25,6 +25,14 @@
  * reductions over all tokens, which do not depend on the token order) and
  * two column sums.
  *
+ * Windows of more than 64 tokens (up to 24 x 24): the large-window forward
+ * kernel runs first and keeps, besides o, the log2 of each row's softmax
+ * normaliser (lse), so that P = exp2(logit * log2 e - lse) needs no row pass;
+ * D_i = do_i . o_i (equal to sum_j P_ij dP_ij); the attention backward then
+ * runs over (head, window, tile of 128 keys) units, summing dq over the key
+ * tiles in fp32 and the table gradient as fixed-point integers on a 2^-19
+ * grid (terms of magnitude 4 or more in fp32).
+ *
  * Conventions of swin_wattn.h: device pointers, asynchronous on `stream`,
  * caller-owned tensors, status codes SWIN_WATTN_*, no CPU fallback.
  */
@@ -55,9 +63,11 @@ extern "C" {
  * Every pointer 16-byte aligned; dx overlaps neither x nor dy.
  * Errors: EINVAL for NULL or misaligned pointers (logit_scale and
  * dlogit_scale are required in V2), bad shapes, overlap; EUNSUPPORTED for an
- * fp32 handle, windows of more than 64 tokens, or B*H*W >= 2^31; ENOMEM if
- * the workspace (8 * B*H*W*C bf16 elements plus 4C^2, plus 2 B*H*W*heads
- * fp32 in V2) cannot be allocated; ECUDA for launch or cuBLAS failures.
+ * fp32 handle, windows of more than 24 x 24 tokens, C != 32 heads, or
+ * B*H*W >= 2^31; ENOMEM if the workspace (8 * B*H*W*C bf16 elements plus
+ * 4C^2, plus 2 B*H*W*heads fp32 in V2, plus (2 heads + C) B*H*W fp32 for
+ * windows of more than 64 tokens) cannot be allocated; ECUDA for launch or
+ * cuBLAS failures.
  * B = 0 zeroes the parameter gradients and returns. */
 int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
                         const void *bias_table, const float *logit_scale, const void *Wproj, const void *bproj,
