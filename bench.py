@@ -279,7 +279,7 @@ def run_ours(args, w):
 
     # per-kernel durations of the three-kernel path (stage hooks, same stream)
     kernels = {}
-    if launches_per_step == 3:
+    if launches_per_step >= 3:   # the three-kernel path (the QKV GEMM may take several launches)
         kernels = per_kernel_times(sw, h, w, t, table, xs, stream, args.steps)
     roof = dominant_roofline(w, kernels, pk, ms)
     roof["traffic"] = profiled_traffic(w.key, roof["kernel"])
@@ -320,7 +320,7 @@ def run_ours(args, w):
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": w.C, "heads": w.heads, "M": w.M,
                        "shift": w.shift, "mode": "V2" if w.mode == V2 else "V1",
-                       "path": ("three kernels" if launches_per_step == 3 else
+                       "path": ("three kernels" if launches_per_step >= 3 else
                                 "fp32 block" if w.dtype == "fp32" else "fused"),
                        "l2": "inputs rotated over %d buffer sets of %.0f MB (x + out), %.0f MB > 2x L2" %
                              (nsets, io_bytes / 2 ** 20, nsets * io_bytes / 2 ** 20),
