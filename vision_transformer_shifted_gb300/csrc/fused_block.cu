@@ -181,6 +181,21 @@ __device__ __forceinline__ bool named_sync_or(bool v)
     return r != 0;
 }
 __device__ __forceinline__ bool compute_sync_or(bool v) { return named_sync_or<1, NCOMPUTE>(v); }
+// The two compute warps of TMEM lane quarter q (the two halves of the same
+// 32 rows) only: named barrier 3 + q, 64 threads.
+__device__ __forceinline__ bool pair_sync_or(int q, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred t, %2, 64, p;\n\t"
+        "selp.u32 %0, 1, 0, t;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(3 + q)
+        : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ bool producer_sync_or(bool v) { return named_sync_or<2, NPROD>(v); }
 
 // Bounded wait that also gives up as soon as another thread has aborted.
@@ -756,7 +771,10 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
                 }
                 float *mxb = smax + r * 256;
                 mxb[half * 128 + row] = mx;
-                if (compute_sync_or(failed)) { failed = true; break; }
+                // only the other half of the same rows is waited for; a failure
+                // stays local to the pair until the compute-wide barrier after
+                // the heads (every wait returns at once after an abort)
+                if (pair_sync_or(quarter, failed)) failed = true;
                 PHASE(k, 4 + 3 * hd);
                 mx = row_ok ? fmaxf(mxb[row], mxb[128 + row]) : 0.f;   // padding rows: all -inf -> p = 0
                 float sum = 0.f;
