@@ -419,3 +419,31 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     g = generate(w, nonzero_bias=True)
     out = run_forward(w, device_inputs(g), g["table"].to(DEV))
     compare(out.double().cpu().numpy(), oracle_forward(w, g, g["table"]), "bf16")
+
+
+# ---- the stored oracle outputs (tests/golden) --------------------------------
+
+@pytest.mark.parametrize("name", ["v1", "v2"])
+def test_stored_golden_case(name):
+    """The tiny stored case (8 x 8 tokens, C = 32, one head, M = 4, shift 2)
+    against the oracle output kept in tests/golden/ (no oracle run here); the
+    inputs are bf16 values, so the kernel consumes exactly what the oracle did."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.join(os.path.dirname(__file__), "golden"))
+    import make_golden as mg
+    mode = mg.CASES[name]["mode"]
+    p = mg.inputs()
+    bf = lambda a: torch.tensor(a).bfloat16().to(DEV)  # noqa: E731
+    h = sw.swin_wattn_create(mg.C, mg.HEADS, mg.M, mg.SHIFT, V2 if mode else V1)
+    try:
+        x = bf(p["x"])
+        out = torch.full_like(x, float("nan"))
+        tau = torch.tensor(p["tau"], dtype=torch.float32, device=DEV) if mode else None
+        sw.swin_wattn_forward(h, x, bf(p["Wqkv"]), bf(p["bqkv"]), bf(p["table"]), tau, bf(p["Wproj"]),
+                              bf(p["bproj"]), out)
+        assert sw.swin_wattn_sync_status(h) == sw.OK
+    finally:
+        sw.swin_wattn_destroy(h)
+    stored = np.loadtxt(mg.path(name)).reshape(mg.B, mg.H, mg.W, mg.C)
+    compare(out.double().cpu().numpy(), stored, "bf16")

@@ -325,3 +325,19 @@ def test_tiny_workload_both_formulations():
                         heads=w.heads, M=w.M, shift=w.shift, mode=w.mode)
     assert np.max(np.abs(out - ref)) < 1e-12
     assert np.isfinite(out).all()
+
+
+# ---- stored oracle outputs (tests/golden) ----------------------------------
+
+@pytest.mark.parametrize("name", ["v1", "v2"])
+def test_oracle_still_matches_its_stored_outputs(name):
+    """The files under tests/golden/ were written by tests/golden/make_golden.py
+    from this oracle; any later change to its arithmetic shows up here (and
+    must then name the passage that justifies it)."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.join(os.path.dirname(__file__), "golden"))
+    import make_golden as mg
+    stored = np.loadtxt(mg.path(name)).reshape(mg.B, mg.H, mg.W, mg.C)
+    _, out = mg.compute(mg.CASES[name]["mode"])
+    assert np.allclose(out, stored, rtol=1e-12, atol=1e-13)
