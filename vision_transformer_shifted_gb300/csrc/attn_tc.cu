@@ -217,14 +217,15 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
         }
         const int *koff = key_off + kt * 128 + 64 * half;
         const int nvalid = N - kt * 128 - 64 * half;   // keys of this thread's 64 that exist
-        float mt = -INFINITY;
+        // four partial maxima (short dependency chains), combined below
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (masked) {
             const int *kreg = key_region + kt * 128 + 64 * half;
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
                 const float lv = fmaf(sv[j], scale, sbias[base - koff[j]]);
                 sv[j] = kreg[j] == my_region ? lv : -INFINITY;
-                mt = fmaxf(mt, sv[j]);
+                mq[j & 3] = fmaxf(mq[j & 3], sv[j]);
             }
         } else if (nvalid >= 64) {
             // the common case: every key exists and no shift region cuts the window
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
                 for (int i = 0; i < 4; ++i) {
                     const int j = 4 * j4 + i;
                     sv[j] = fmaf(sv[j], scale, sbias[base - oo[i]]);
-                    mt = fmaxf(mt, sv[j]);
+                    mq[j & 3] = fmaxf(mq[j & 3], sv[j]);
                 }
             }
         } else {
@@ -244,9 +245,10 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
             for (int j = 0; j < 64; ++j) {
                 const float lv = fmaf(sv[j], scale, sbias[base - koff[j]]);
                 sv[j] = j < nvalid ? lv : -INFINITY;
-                mt = fmaxf(mt, sv[j]);
+                mq[j & 3] = fmaxf(mq[j & 3], sv[j]);
             }
         }
+        float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         FPHASE(kt, 4);
         smax[half * 128 + row] = mt;
         if (__syncthreads_or(failed)) { failed = true; break; }
@@ -257,15 +259,15 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
         // leaves o = 0 and l = 0 as they are)
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = ex2_approx(m_run - m_use);
-        float sum = 0.f;
+        float sq[4] = {0.f, 0.f, 0.f, 0.f};   // four partial sums
         uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < 64; j += 2) {
             const float p0 = ex2_approx(sv[j] - m_use), p1 = ex2_approx(sv[j + 1] - m_use);
-            sum += p0 + p1;
+            sq[(j >> 1) & 3] += p0 + p1;
             pk[j / 2] = pack_bf16x2(p0, p1);
         }
-        l_run = l_run * alpha + sum;     // this half's share of the row sum
+        l_run = l_run * alpha + ((sq[0] + sq[1]) + (sq[2] + sq[3]));   // this half's share of the row sum
         m_run = m_new;
         // P (bf16 pairs) over TMEM columns 32*half .. +31 (keys 64*half ..)
         {

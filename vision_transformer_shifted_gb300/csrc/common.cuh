@@ -51,6 +51,22 @@ __device__ __forceinline__ int64_t window_row_to_token(const Geom &g, int64_t r)
     return ((int64_t)b * g.H + i) * g.W + j;
 }
 
+// The inverse map: token t = b*H*W + i*W + j -> its window-order row (the
+// token sits at shifted position (i-s mod H, j-s mod W)).
+__device__ __forceinline__ int64_t token_to_window_row(const Geom &g, int64_t t)
+{
+    const int64_t hw = (int64_t)g.H * g.W;
+    const int64_t b = t / hw;
+    const int rem = (int)(t - b * hw);
+    const int i = rem / g.W, j = rem - (rem / g.W) * g.W;
+    int si = i - g.s;
+    if (si < 0) si += g.H;
+    int sj = j - g.s;
+    if (sj < 0) sj += g.W;
+    const int wi = si / g.M, wj = sj / g.M;
+    return ((b * g.nh + wi) * g.nw + wj) * g.N + (si - wi * g.M) * g.M + (sj - wj * g.M);
+}
+
 // 32-bit form of window_row_to_token for callers that know B*H*W < 2^31.
 __device__ __forceinline__ int window_row_to_token32(const Geom &g, int r)
 {
@@ -88,6 +104,10 @@ struct DeviceStatus {
 
 enum { LOAD_PLAIN = 0, LOAD_GATHER = 1 };
 enum { STORE_PLAIN = 0, STORE_SCATTER = 1 };
+// (inside launch_gemm: LOAD_GATHER + STORE_PLAIN on the resident-weight kernel
+// runs as plain token-order loads whose output rows go to their window-order
+// places, STORE_WINDOW: the same result, without gathered loads)
+enum { STORE_WINDOW = 2 };
 
 struct GemmArgs {
     const bf16 *A;   // LOAD_PLAIN: [rows, lda]; LOAD_GATHER: x [B, H, W, K]

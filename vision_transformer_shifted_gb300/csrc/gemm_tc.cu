@@ -542,12 +542,18 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
                 break;
             }
             tc_fence_after();
-            const int64_t R = m * BM + r;
+            int64_t R = m * BM + r;
             const int n0 = nb * BN;
             bf16 *dst_row = nullptr;
             if (R < a.rows) {
-                if (STORE == STORE_SCATTER) dst_row = a.D + window_row_to_token(a.g, R) * (int64_t)a.N + n0;
-                else dst_row = a.D + R * a.ldd + n0;
+                if (STORE == STORE_SCATTER) {
+                    dst_row = a.D + window_row_to_token(a.g, R) * (int64_t)a.N + n0;
+                } else if (STORE == STORE_WINDOW) {
+                    R = token_to_window_row(a.g, R);   // the output row (and its norms' row)
+                    dst_row = a.D + R * a.ldd + n0;
+                } else {
+                    dst_row = a.D + R * a.ldd + n0;
+                }
             }
             const uint32_t tb = t_lane + (uint32_t)buf * half_cols;
             for (int ci = half; ci < nchunks; ci += 2) {
@@ -975,6 +981,12 @@ cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, Device
     auto rs_ok = [&](const GemmArgs &x, RsPlan &p) {
         return x.rows > 0 && rs_plan(x, p) && (load_mode != LOAD_GATHER || p.stages >= RS_DEPTH + 1);
     };
+    // gathered rows with a plain store: plain token-order loads, output rows
+    // sent to their window-order places (same result, no gathered loads)
+    GemmArgs aw = a;
+    if (load_mode == LOAD_GATHER && store_mode == STORE_PLAIN) aw.lda = a.K;
+    const bool to_window = load_mode == LOAD_GATHER && store_mode == STORE_PLAIN && a.epi != EPI_RESID;
+    if (to_window && a.rows > 0 && rs_plan(aw, pl)) return launch_rs<LOAD_PLAIN, STORE_WINDOW>(aw, pl, st, stream);
     if (rs_ok(a, pl)) {
         if (load_mode == LOAD_GATHER && store_mode == STORE_PLAIN) return launch_rs<LOAD_GATHER, STORE_PLAIN>(a, pl, st, stream);
         if (load_mode == LOAD_PLAIN && store_mode == STORE_SCATTER) return launch_rs<LOAD_PLAIN, STORE_SCATTER>(a, pl, st, stream);
@@ -988,12 +1000,13 @@ cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, Device
             if (a.N % nc || (a.N / nc) % 16) continue;
             const int n = a.N / nc;
             if (a.norm_cols > 0 && (n % 32 || a.norm_cols % 32)) continue;
-            GemmArgs c0 = column_chunk(a, 0, n);
-            if (!rs_ok(c0, pl)) continue;
+            GemmArgs c0 = column_chunk(aw, 0, n);
+            if (!(to_window ? rs_plan(c0, pl) : rs_ok(c0, pl))) continue;
             for (int i = 0; i < nc; ++i) {
-                const GemmArgs c = column_chunk(a, i * n, n);
-                cudaError_t e = load_mode == LOAD_GATHER ? launch_rs<LOAD_GATHER, STORE_PLAIN>(c, pl, st, stream)
-                                                         : launch_rs<LOAD_PLAIN, STORE_PLAIN>(c, pl, st, stream);
+                const GemmArgs c = column_chunk(aw, i * n, n);
+                cudaError_t e = to_window ? launch_rs<LOAD_PLAIN, STORE_WINDOW>(c, pl, st, stream)
+                                : load_mode == LOAD_GATHER ? launch_rs<LOAD_GATHER, STORE_PLAIN>(c, pl, st, stream)
+                                                           : launch_rs<LOAD_PLAIN, STORE_PLAIN>(c, pl, st, stream);
                 if (e != cudaSuccess) return e;
             }
             return cudaSuccess;
