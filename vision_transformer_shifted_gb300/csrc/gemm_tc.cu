@@ -304,7 +304,26 @@ struct RsPlan {
     int BN, nbn, KB, stages;
     uint32_t tcols;
     size_t b_bytes, smem;
+    int ng;   // column groups: CTA b does column chunk b % ng of every ng-th row block (1: none)
 };
+
+// Column chunk c0 .. c0+n of a plain-store GEMM as a GEMM of its own (its
+// weight rows, bias, output columns, residual columns and normalised chunks).
+__host__ __device__ inline GemmArgs column_chunk(const GemmArgs &a, int c0, int n)
+{
+    GemmArgs c = a;
+    c.Bw = a.Bw + (int64_t)c0 * a.K;
+    if (a.bias) c.bias = a.bias + c0;
+    c.D = a.D + c0;
+    c.N = n;
+    if (a.R) c.R = a.R + c0;
+    if (a.norm_cols > 0) {
+        c.norm_cols = a.norm_cols - c0 < 0 ? 0 : (a.norm_cols - c0 > n ? n : a.norm_cols - c0);
+        c.norms_ld = a.norms_ld ? a.norms_ld : a.norm_cols / 32;
+        c.norms = a.norms && c.norm_cols > 0 ? a.norms + c0 / 32 : nullptr;
+    }
+    return c;
+}
 
 __device__ __forceinline__ void rs_epilogue_chunk32(const GemmArgs &a, int64_t R, int n, bf16 *dst, float (&v)[32],
                                                    const float *bias, bool norm)
@@ -356,10 +375,19 @@ __device__ __forceinline__ void rs_epilogue_chunk32(const GemmArgs &a, int64_t R
     }
 }
 
-template <int LOAD, int STORE>
+template <int LOAD, int STORE, bool GROUPS>
 __global__ void __launch_bounds__(RS_THREADS, 1)
-gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ CUtensorMap tmA)
+gemm_rs_kernel(GemmArgs a_full, RsPlan pl, DeviceStatus st, const __grid_constant__ CUtensorMap tmA)
 {
+    // GROUPS (column groups): this CTA's chunk of the output columns (its
+    // weights stay resident), every ng-th row block; the ng CTAs of a row
+    // block run about together, so its A rows come from DRAM once and from L2
+    // after that.  (Without, the arguments stay in the parameter space.)
+    const int ng = GROUPS ? pl.ng : 1;
+    const int m_first = (int)(blockIdx.x / ng), m_step = (int)(gridDim.x / ng);
+    GemmArgs a_chunk;
+    if (GROUPS) a_chunk = column_chunk(a_full, (int)(blockIdx.x % ng) * (a_full.N / ng), a_full.N / ng);
+    const GemmArgs &a = GROUPS ? a_chunk : a_full;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_align(smem_raw, 1024);
     const int S = pl.stages, BN = pl.BN, nbn = pl.nbn, KB = pl.KB;
@@ -415,7 +443,7 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
         int64_t it = 0;
         if (LOAD == LOAD_PLAIN) {
             if (warp == 0 && lane == 0) {
-                for (int64_t m = blockIdx.x; m < mtiles && !failed; m += gridDim.x) {
+                for (int64_t m = m_first; m < mtiles && !failed; m += m_step) {
                     const int64_t m0 = m * BM;
                     for (int kb = 0; kb < KB; ++kb, ++it) {
                         const int s = (int)(it % S);
@@ -429,7 +457,7 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
                 }
             }
         } else {
-            for (int64_t m = blockIdx.x; m < mtiles && !failed; m += gridDim.x) {
+            for (int64_t m = m_first; m < mtiles && !failed; m += m_step) {
                 const int64_t m0 = m * BM;
                 // this warp's rows of the tile (BM / RS_NPROD of them): source
                 // offsets (32-bit index map when it fits) into shared memory
@@ -487,7 +515,7 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(BM, BN);
             int64_t it = 0, lm = 0;
-            for (int64_t m = blockIdx.x; m < mtiles && !failed; m += gridDim.x, ++lm) {
+            for (int64_t m = m_first; m < mtiles && !failed; m += m_step, ++lm) {
                 const int64_t it0 = it;
                 for (int nb = 0; nb < nbn && !failed; ++nb) {
                     // accumulator: alternate per row block (one half), or one per half
@@ -533,7 +561,7 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
         const int nchunks = BN / 32;
         int64_t lm = 0;
-        for (int64_t m = blockIdx.x; m < mtiles && !failed; m += gridDim.x, ++lm)
+        for (int64_t m = m_first; m < mtiles && !failed; m += m_step, ++lm)
         for (int nb = 0; nb < nbn; ++nb) {
             const int buf = nbn == 2 ? nb : (int)(lm & 1);
             const uint32_t par = nbn == 2 ? (uint32_t)(lm & 1) : (uint32_t)((lm >> 1) & 1);
@@ -599,6 +627,7 @@ gemm_rs_kernel(GemmArgs a, RsPlan pl, DeviceStatus st, const __grid_constant__ C
 bool rs_plan(const GemmArgs &a, RsPlan &p)
 {
     if (a.N <= 0 || a.N % 16 || a.N > 512 || a.K <= 0 || a.K % 16) return false;
+    p.ng = 1;
     p.nbn = a.N <= 256 ? 1 : 2;
     p.BN = a.N / p.nbn;
     if (p.BN % 16 || (a.norm_cols > 0 && p.BN % 32)) return false;
@@ -626,7 +655,7 @@ cudaError_t launch_rs(const GemmArgs &a, const RsPlan &pl, DeviceStatus st, cuda
         cudaError_t e = make_tensor_map_sw128(&tmA, a.A, a.rows, a.K, a.lda, BM);
         if (e != cudaSuccess) return e;
     }
-    auto kern = gemm_rs_kernel<LOAD, STORE>;
+    auto kern = pl.ng > 1 ? gemm_rs_kernel<LOAD, STORE, true> : gemm_rs_kernel<LOAD, STORE, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
     if (e != cudaSuccess) return e;
     static int sms = 0;
@@ -636,7 +665,9 @@ cudaError_t launch_rs(const GemmArgs &a, const RsPlan &pl, DeviceStatus st, cuda
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
     }
     const int64_t mtiles = (a.rows + BM - 1) / BM;
-    const unsigned grid = (unsigned)(mtiles < sms ? mtiles : sms);
+    const int ng = pl.ng > 1 ? pl.ng : 1;
+    const int64_t per = sms / ng;   // CTAs per column group
+    const unsigned grid = (unsigned)((mtiles < per ? mtiles : per) * ng);
     kern<<<grid, RS_THREADS, pl.smem, stream>>>(a, pl, st, tmA);
     return cudaGetLastError();
 }
@@ -956,24 +987,6 @@ cudaError_t launch_gemm_ts_test(const GemmArgs &a, DeviceStatus st, cudaStream_t
     return cudaGetLastError();
 }
 
-// Column chunk c0 .. c0+n of a plain-store GEMM as a GEMM of its own (its
-// weight rows, bias, output columns, residual columns and normalised chunks).
-static GemmArgs column_chunk(const GemmArgs &a, int c0, int n)
-{
-    GemmArgs c = a;
-    c.Bw = a.Bw + (int64_t)c0 * a.K;
-    if (a.bias) c.bias = a.bias + c0;
-    c.D = a.D + c0;
-    c.N = n;
-    if (a.R) c.R = a.R + c0;
-    if (a.norm_cols > 0) {
-        c.norm_cols = a.norm_cols - c0 < 0 ? 0 : (a.norm_cols - c0 > n ? n : a.norm_cols - c0);
-        c.norms_ld = a.norms_ld ? a.norms_ld : a.norm_cols / 32;
-        c.norms = a.norms && c.norm_cols > 0 ? a.norms + c0 / 32 : nullptr;
-    }
-    return c;
-}
-
 cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, DeviceStatus st, cudaStream_t stream)
 {
     RsPlan pl;
@@ -993,8 +1006,9 @@ cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, Device
         if (load_mode == LOAD_PLAIN && store_mode == STORE_PLAIN) return launch_rs<LOAD_PLAIN, STORE_PLAIN>(a, pl, st, stream);
     }
     // weights too large to stay resident: 2 to 4 column chunks that each fit,
-    // one launch per chunk.  Each launch reads A again, so only where A is no
-    // wider than the output (the QKV and the first MLP projections).
+    // one column group of CTAs per chunk in one launch (the groups walk the
+    // row blocks together, so A is read from DRAM about once); only where A
+    // is no wider than the output (the QKV and the first MLP projections).
     if (store_mode == STORE_PLAIN && a.rows > 0 && a.K <= a.N) {
         for (int nc = 2; nc <= 4; ++nc) {
             if (a.N % nc || (a.N / nc) % 16) continue;
@@ -1002,14 +1016,10 @@ cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, Device
             if (a.norm_cols > 0 && (n % 32 || a.norm_cols % 32)) continue;
             GemmArgs c0 = column_chunk(aw, 0, n);
             if (!(to_window ? rs_plan(c0, pl) : rs_ok(c0, pl))) continue;
-            for (int i = 0; i < nc; ++i) {
-                const GemmArgs c = column_chunk(aw, i * n, n);
-                cudaError_t e = to_window ? launch_rs<LOAD_PLAIN, STORE_WINDOW>(c, pl, st, stream)
-                                : load_mode == LOAD_GATHER ? launch_rs<LOAD_GATHER, STORE_PLAIN>(c, pl, st, stream)
-                                                           : launch_rs<LOAD_PLAIN, STORE_PLAIN>(c, pl, st, stream);
-                if (e != cudaSuccess) return e;
-            }
-            return cudaSuccess;
+            pl.ng = nc;
+            return to_window ? launch_rs<LOAD_PLAIN, STORE_WINDOW>(aw, pl, st, stream)
+                   : load_mode == LOAD_GATHER ? launch_rs<LOAD_GATHER, STORE_PLAIN>(aw, pl, st, stream)
+                                              : launch_rs<LOAD_PLAIN, STORE_PLAIN>(aw, pl, st, stream);
         }
     }
     if (load_mode == LOAD_GATHER && store_mode == STORE_PLAIN) return launch_impl<LOAD_GATHER, STORE_PLAIN>(a, st, stream);
