@@ -84,6 +84,11 @@ struct FbLayout {
     static size_t bytes(int M) { return (size_t)bar(M) + 48 + 512; }
 };
 
+template <bool B>
+struct FbTag {
+    static constexpr bool value = B;
+};
+
 __device__ __forceinline__ int fb_band(int p, int n, int M, int s) { return p < n - M ? 0 : (p < n - s ? 1 : 2); }
 
 // shift region of token t of window (wi, wj) (0 everywhere without a shift)
@@ -327,8 +332,10 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
             BPHASE(step, 2);
 
             // ---- P^T and dS^T of key row r, queries 64*h2 .. +63, 8 at a time ----
-#pragma unroll 1
-            for (int hh = 0; hh < 8; ++hh) {
+            // (FULL: every pair of the pass is valid -- an unmasked window, a real
+            // key, eight real queries -- so no pair needs a check)
+            auto pass = [&](auto full_tag, int hh) {
+                constexpr bool FULL = decltype(full_tag)::value;
                 const int i0 = 64 * h2 + 8 * hh;
                 float s[8], d[8];
                 tmem_ld8(t_lane + i0, s);
@@ -342,7 +349,7 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
                         const int cc[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
-                            const bool valid = (cc[t] >> 24) == kreg;
+                            const bool valid = FULL || (cc[t] >> 24) == kreg;
                             idx[4 * v + t] = valid ? (cc[t] & 0xFFF) - kofs : -1;
                             idxp[4 * v + t] = ((cc[t] >> 12) & 0xFFF) - kofsp;
                         }
@@ -352,8 +359,9 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
                 float bv[8];
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj)
-                    bv[jj] = __bfloat162float(sbias[idx[jj] >= 0 ? idx[jj] : 0]);
+                    bv[jj] = __bfloat162float(sbias[FULL || idx[jj] >= 0 ? idx[jj] : 0]);
                 tmem_wait_ld();
+                float amax = 0.f;
                 {
                     const float4 *l4 = reinterpret_cast<const float4 *>(slse + i0);
                     const float4 *d4 = reinterpret_cast<const float4 *>(sdd + i0);
@@ -364,12 +372,13 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
                             const int jj = 4 * v + t;
-                            const float p = idx[jj] >= 0 ? ex2_approx(fmaf(s[jj], sc2, fmaf(bv[jj], LOG2E, -ll[t])))
-                                                         : 0.f;
+                            const float e = ex2_approx(fmaf(s[jj], sc2, fmaf(bv[jj], LOG2E, -ll[t])));
+                            const float p = FULL || idx[jj] >= 0 ? e : 0.f;
                             const float ds = p * (d[jj] - dd[t]);
                             if (v2) tau_acc = fmaf(ds, s[jj], tau_acc);
                             s[jj] = p;
                             d[jj] = ds;
+                            amax = fmaxf(amax, fabsf(ds));
                         }
                     }
                 }
@@ -379,12 +388,30 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
                 tmem_st4(t_lane + 64 * h2 + 4 * hh, pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]),
                          pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
                 fb_store8(base + Ly::DS + (uint32_t)(i0 >> 5) * 8192u + sw64_offset(r, hh & 3), d);
+                if (__all_sync(0xffffffffu, amax < FIX_MAX)) {
+                    // the common case: every term of the warp on the fixed-point grid
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    if (idx[jj] < 0) continue;
-                    if (fabsf(d[jj]) < FIX_MAX) atomicAdd(&dti[idxp[jj]], fb_round_fix(d[jj]));
-                    else atomicAdd(&dtab[idxp[jj]], d[jj]);
+                    for (int jj = 0; jj < 8; ++jj)
+                        if (FULL || idx[jj] >= 0) atomicAdd(&dti[idxp[jj]], fb_round_fix(d[jj]));
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        if (!FULL && idx[jj] < 0) continue;
+                        if (fabsf(d[jj]) < FIX_MAX) atomicAdd(&dti[idxp[jj]], fb_round_fix(d[jj]));
+                        else atomicAdd(&dtab[idxp[jj]], d[jj]);
+                    }
                 }
+            };
+            const bool unmasked = g.s == 0 || (wi != g.nh - 1 && wj != g.nw - 1);
+#pragma unroll 1
+            for (int hh = 0; hh < 8; ++hh) {
+                // the choice is made for the whole warp (a window's last key tile
+                // can end inside a warp): both passes hold warp-collective TMEM
+                // accesses and a vote, which every lane must reach together
+                if (__all_sync(0xffffffffu, unmasked && kvalid && qt * 128 + 64 * h2 + 8 * hh + 8 <= N))
+                    pass(FbTag<true>(), hh);
+                else
+                    pass(FbTag<false>(), hh);
             }
             BPHASE(step, 3);
             tmem_wait_st();
