@@ -5,16 +5,18 @@
 // row-wise softmax normaliser of the forward (its log2, lse, kept by the
 // large-window forward kernel) P = exp2(logit2 - lse) needs no row reduction,
 // so a CTA can own a tile of 128 KEYS of one window and head and walk over
-// the window's query tiles (the FlashAttention backward order):
+// the window's query tiles (key-stationary order):
 //   S^T  = k q^T and dP^T = v do^T            (M = 128 keys, N = 128 queries, K = 32)
 //   P^T, dS^T = P^T (dP^T - D), D_i = do_i . o_i (computed beforehand)
-//   dv  += P^T do,  dk += dS^T q             (kept in registers across query tiles)
+//   dv  += P^T do,  dk += dS^T q             (P^T from TMEM; both kept in registers
+//                                             across query tiles)
 //   dq_i += dS k                             (M = 128 queries: dS^T read M-major;
 //                                             added to an fp32 buffer by atomics, since
 //                                             every key tile of the window contributes)
 // and the table gradient of each relative offset summed in shared memory per
-// head (units run head by head, a contiguous range per CTA).  A last kernel
-// turns the fp32 dq into bf16 (scale, and for V2 the unit-length backward).
+// head as fixed-point integers (units run head by head, a contiguous range per
+// CTA).  A last kernel turns the fp32 dq into bf16 (scale, and for V2 the
+// unit-length backward).
 #include "common.cuh"
 #include "ptx.cuh"
 
