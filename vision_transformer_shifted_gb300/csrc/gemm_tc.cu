@@ -1005,12 +1005,14 @@ cudaError_t launch_gemm(const GemmArgs &a, int load_mode, int store_mode, Device
         if (load_mode == LOAD_PLAIN && store_mode == STORE_SCATTER) return launch_rs<LOAD_PLAIN, STORE_SCATTER>(a, pl, st, stream);
         if (load_mode == LOAD_PLAIN && store_mode == STORE_PLAIN) return launch_rs<LOAD_PLAIN, STORE_PLAIN>(a, pl, st, stream);
     }
-    // weights too large to stay resident: 2 to 4 column chunks that each fit,
+    // weights too large to stay resident: 2 to 4 (16) column chunks that each fit,
     // one column group of CTAs per chunk in one launch (the groups walk the
     // row blocks together, so A is read from DRAM about once); only where A
     // is no wider than the output (the QKV and the first MLP projections).
     if (store_mode == STORE_PLAIN && a.rows > 0 && a.K <= a.N) {
-        for (int nc = 2; nc <= 4; ++nc) {
+        // (more than four groups only while A stays in L2 for all of them)
+        const bool a_in_l2 = a.rows * a.K * 2 <= ((int64_t)64 << 20);
+        for (int nc = 2; nc <= (a_in_l2 ? 16 : 4); ++nc) {
             if (a.N % nc || (a.N / nc) % 16) continue;
             const int n = a.N / nc;
             if (a.norm_cols > 0 && (n % 32 || a.norm_cols % 32)) continue;
