@@ -126,14 +126,19 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend=None):
+    """(rank, world, local rank, torch.distributed or None) from the torchrun
+    environment; NCCL on GPUs, gloo where there is none (the CPU tests)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
         return rank, world, local, dist
     return 0, 1, 0, None
 
@@ -146,9 +151,20 @@ def barrier(dist):
 def max_over_ranks(v, dist):
     if dist is None:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_workload(w, rank):
+    """Each rank's own batch: the same shapes, its own seed (weak scaling)."""
+    return w.with_(seed=w.seed + rank)
+
+
+def job_rate(tokens_per_rank, world, seconds):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / seconds
 
 
 def oracle_sample_rate(w, g, table_np, seconds=10.0, threads=None):
@@ -227,7 +243,7 @@ def run_ours(args, w):
     h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, mode)
     if args.path:
         sw.swin_wattn_set_option(h, sw.OPT_PATH, args.path)
-    g = generate(w.with_(seed=w.seed + rank))
+    g = generate(rank_workload(w, rank))
     t = {k: (v.to(dev) if v is not None else None) for k, v in g.items()}
     table = table_for(w, g, dev, h)
     io_bytes = w.tokens * w.C * w.elem_bytes * 2
@@ -267,7 +283,7 @@ def run_ours(args, w):
         barrier(dist)
     ms = max_over_ranks(e0.elapsed_time(e1), dist) / args.steps
     assert sw.swin_wattn_sync_status(h, stream) == sw.OK
-    tokens_s = w.tokens * world / (ms * 1e-3)
+    tokens_s = job_rate(w.tokens, world, ms * 1e-3)
     tflops = w.flops * world / (ms * 1e-3) / 1e12
 
     # whole-block roofline: min(dense bf16 peak, HBM x algorithmic intensity)
@@ -327,7 +343,7 @@ def run_ours(args, w):
                        "parallelism": "dp%d (independent batches)" % world},
             "tflops": tflops, "block_roofline": block_roof, "roofline": roof, "kernels_us": kernels,
             "cpu_baseline": cpu,
-            "e2e": {"value": w.tokens * world / e2e_s, "unit": "tokens/s",
+            "e2e": {"value": job_rate(w.tokens, world, e2e_s), "unit": "tokens/s",
                     "h2d_bytes_per_step": w.tokens * w.C * w.elem_bytes,
                     "d2h_bytes_per_step": w.tokens * w.C * w.elem_bytes},
             "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary()}
