@@ -65,8 +65,11 @@ enum {
     SWIN_WATTN_OPT_PATH = 1,       /* 0 = automatic, 1 = three kernels (QKV GEMM,
                                       window attention, projection GEMM),
                                       2 = the fused single-kernel block */
-    SWIN_WATTN_OPT_WAIT_LIMIT_US = 2 /* limit of every device-side wait, microseconds
-                                        (default 2,000,000) */
+    SWIN_WATTN_OPT_WAIT_LIMIT_US = 2, /* limit of every device-side wait, microseconds
+                                         (default 2,000,000) */
+    SWIN_WATTN_OPT_HOST_CHUNKS = 3   /* chunks of whole images that
+                                        swin_wattn_forward_host overlaps (1..16,
+                                        default 8; fewer when B is smaller) */
 };
 
 /* Creates a handle for blocks with C channels, `heads` heads (d = C/heads),
@@ -105,6 +108,7 @@ int swin_wattn_forward(swin_wattn_t h, const void *x, int B, int H, int W, const
 
 /* The same forward with x and out in HOST memory (pinned memory gives
  * asynchronous copies).  The batch is cut into up to 8 chunks of whole images
+ * (SWIN_WATTN_OPT_HOST_CHUNKS sets the count)
  * (windows never cross images, so each chunk is an exact forward of its
  * images), and each chunk is copied host->device into a buffer the handle
  * owns, run, and copied device->host into out_host; the three steps of

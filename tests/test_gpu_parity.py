@@ -304,18 +304,24 @@ def test_cpb_table(key):
 
 # ---- host-buffer entry point, edge cases, argument errors, watchdog ---------------
 
-def test_forward_host_matches_device_forward():
-    w = WORKLOADS["swin_t_s1"].with_(B=2, H=14, W=14)
+@pytest.mark.parametrize("chunks", [None, 1, 3, 16])
+def test_forward_host_matches_device_forward(chunks):
+    w = WORKLOADS["swin_t_s1"].with_(B=5, H=14, W=14)
     g = generate(w, nonzero_bias=True)
     t = device_inputs(g)
     dev_out = run_forward(w, t, t["table"])
     h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
     try:
+        if chunks:   # (16 chunks of a 5-image batch: one image each)
+            sw.swin_wattn_set_option(h, sw.OPT_HOST_CHUNKS, chunks)
         x_host = g["x"].pin_memory()
         out_host = torch.empty_like(x_host).pin_memory()
         sw.swin_wattn_forward_host(h, x_host, t["Wqkv"], t["bqkv"], t["table"], None, t["Wproj"], t["bproj"],
                                    out_host)
         assert sw.swin_wattn_sync_status(h) == sw.OK
+        for bad in (0, 17):
+            with pytest.raises(sw.SwinWAttnError):
+                sw.swin_wattn_set_option(h, sw.OPT_HOST_CHUNKS, bad)
     finally:
         sw.swin_wattn_destroy(h)
     assert torch.equal(out_host, dev_out.cpu())

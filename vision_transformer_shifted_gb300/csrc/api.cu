@@ -13,7 +13,7 @@
 using namespace swin;
 
 // Chunks of whole images of the pipelined host-buffer forward (at most).
-constexpr int HOST_CHUNKS = 8;
+constexpr int HOST_CHUNKS = 16;   // most chunks of the host-buffer forward (default 8)
 
 struct swin_wattn_s {
     int C, heads, d, M, shift, mode;
@@ -41,7 +41,8 @@ struct swin_wattn_s {
     // arguments stay the same
     cudaGraphExec_t graph;
     const void *g_args[11];   // the call's pointers and the buffers the graph uses
-    int g_B, g_H, g_W, g_path, g_launches;
+    int g_B, g_H, g_W, g_path, g_launches, g_chunks;
+    int host_chunks;   // chunks of the host-buffer forward (1..HOST_CHUNKS)
 };
 
 namespace {
@@ -190,7 +191,7 @@ cublasStatus_t weight_grad(cublasHandle_t blas, const bf16 *G, int n_out, const 
 }
 
 // The chunked host-buffer forward on `s` (the body of swin_wattn_forward_host):
-// up to HOST_CHUNKS chunks of whole images; copy-in, compute and copy-out of different
+// up to h->host_chunks chunks of whole images; copy-in, compute and copy-out of different
 // chunks overlap on the handle's three streams, forked from and joined back
 // into `s`.  `direct`: also wait for the previous direct call's last copy.
 int enqueue_host_chunks(swin_wattn_s *h, const void *x_host, int B, int H, int W, const void *Wqkv, const void *bqkv,
@@ -204,7 +205,7 @@ int enqueue_host_chunks(swin_wattn_s *h, const void *x_host, int B, int H, int W
         if (cudaStreamWaitEvent(st, h->ev_fork, 0) != cudaSuccess) return SWIN_WATTN_ECUDA;
         if (direct && cudaStreamWaitEvent(st, h->ev_join, 0) != cudaSuccess) return SWIN_WATTN_ECUDA;
     }
-    const int nchunks = B < HOST_CHUNKS ? B : HOST_CHUNKS;
+    const int nchunks = B < h->host_chunks ? B : h->host_chunks;
     const size_t img = bytes / (size_t)B;
     int launches = 0;
     for (int c = 0; c < nchunks; ++c) {
@@ -252,6 +253,7 @@ int swin_wattn_create(swin_wattn_t *out, int C, int heads, int M, int shift, int
     h->C = C; h->heads = heads; h->d = d; h->M = M; h->shift = shift;
     h->mode = mode & SWIN_WATTN_V2; h->fp32 = fp32;
     h->path_opt = 0;
+    h->host_chunks = 8;
     h->wait_ns = 2000000000ull;
     if (cudaGetDevice(&h->device) != cudaSuccess) { delete h; cudaGetLastError(); return SWIN_WATTN_ECUDA; }
     if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess) { delete h; cudaGetLastError(); return SWIN_WATTN_ENOMEM; }
@@ -335,7 +337,7 @@ int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, in
     // the three-kernel path's workspace for the largest chunk, before any
     // capture (no allocation may happen inside one)
     {
-        const int nchunks = B < HOST_CHUNKS ? B : HOST_CHUNKS, bmax = (B + nchunks - 1) / nchunks;
+        const int nchunks = B < h->host_chunks ? B : h->host_chunks, bmax = (B + nchunks - 1) / nchunks;
         const int64_t Tc = (int64_t)bmax * H * W;
         const int path = h->path_opt ? h->path_opt : choose_path(h, Tc);
         if (!h->fp32 && path == 1) {
@@ -347,7 +349,8 @@ int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, in
     // on device buffers may have reallocated the workspace since)
     const void *args[11] = {x_host, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out_host,
                             h->ws, h->stage_x, h->stage_out};
-    bool same = h->graph && h->g_B == B && h->g_H == H && h->g_W == W && h->g_path == h->path_opt;
+    bool same = h->graph && h->g_B == B && h->g_H == H && h->g_W == W && h->g_path == h->path_opt &&
+                h->g_chunks == h->host_chunks;
     for (int i = 0; i < 11 && same; ++i) same = h->g_args[i] == args[i];
     if (!same) {
         if (h->graph) {
@@ -364,7 +367,7 @@ int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, in
         }
         if (rc == SWIN_WATTN_OK && ce == cudaSuccess && graph && args[8] == h->ws &&
             cudaGraphInstantiate(&h->graph, graph, 0) == cudaSuccess) {
-            h->g_B = B; h->g_H = H; h->g_W = W; h->g_path = h->path_opt;
+            h->g_B = B; h->g_H = H; h->g_W = W; h->g_path = h->path_opt; h->g_chunks = h->host_chunks;
             for (int i = 0; i < 11; ++i) h->g_args[i] = args[i];
             h->g_launches = h->last_launches;
         } else {
@@ -417,6 +420,10 @@ int swin_wattn_set_option(swin_wattn_t h, int option, int64_t value)
     case SWIN_WATTN_OPT_WAIT_LIMIT_US:
         if (value <= 0 || value > 60000000) return SWIN_WATTN_EINVAL;
         h->wait_ns = (uint64_t)value * 1000ull;
+        return SWIN_WATTN_OK;
+    case SWIN_WATTN_OPT_HOST_CHUNKS:
+        if (value < 1 || value > HOST_CHUNKS) return SWIN_WATTN_EINVAL;
+        h->host_chunks = (int)value;
         return SWIN_WATTN_OK;
     default:
         return SWIN_WATTN_EINVAL;
