@@ -168,7 +168,7 @@ const char *swin_wattn_last_cuda_error(swin_wattn_t h);
 #define SWIN_WATTN_NOALLOC_MAX_INTERMEDIATE_BYTES (SWIN_WATTN_NOALLOC_SCRATCH_BYTES - 256)
 
 /* The forward pass of swin_wattn_forward for callers that cannot allocate
- * device memory.  The paper has no counterpart: this is a deployment
+ * device memory.  None of the sources describes one: this is a deployment
  * convenience of this library.
  *
  * Who needs it: code that runs where it does not own the device allocator
