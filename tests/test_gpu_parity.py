@@ -1,9 +1,10 @@
 """GPU parity: every kernel against the float64 oracle, through the C ABI.
 
-Index maps are compared bit-exactly on integer-tagged tokens; floating-point
-results within the tolerances in tests/helpers.py.  Small cases span several
-128-row tiles and a ragged tail; full-size workloads are checked on sampled
-windows (corners, where the mask and the wrap-around act, plus random ones).
+Index maps are compared bit-exactly on integer-tagged tokens (through the
+stage hooks, and through the whole forward with one-hot attention);
+floating-point results within the tolerances in tests/helpers.py.  Small
+cases span several 128-row tiles and a ragged tail; the full-size workloads
+are compared on every output element.
 """
 import ctypes
 
@@ -13,9 +14,9 @@ import torch
 
 import oracle
 from vision_transformer_shifted_gb300 import binding as sw
-from vision_transformer_shifted_gb300.inputs import V1, V2, WORKLOADS, generate, sample_windows
+from vision_transformer_shifted_gb300.inputs import V1, V2, WORKLOADS, generate
 
-from helpers import compare, device_inputs, oracle_forward, oracle_table, to_f64, window_tokens
+from helpers import compare, device_inputs, oracle_forward, oracle_table, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -254,23 +255,97 @@ def test_fp32_v2_small():
     compare(out.double().cpu().numpy(), oracle_forward(w, g, table), "fp32")
 
 
-# ---- full-size workloads on sampled windows ------------------------------------
+# ---- full-size workloads, every output element ------------------------------
+
+# float64 oracle outputs of the full-size workloads, shared by the two paths
+_FULL_REF = {}
+
+
+def full_reference(key):
+    w = WORKLOADS[key]
+    if key not in _FULL_REF:
+        g = generate(w)
+        table = oracle_table(w, g)
+        _FULL_REF.clear()   # one workload at a time (SwinV2-L window 24: 0.9 GB)
+        _FULL_REF[key] = (g, table, oracle_forward(w, g, table))
+    return _FULL_REF[key]
+
 
 @pytest.mark.parametrize("key,path", [("swin_t_s1", sw.PATH_AUTO), ("swin_t_s1", sw.PATH_THREE_KERNELS),
                                       ("swin_b_s1", sw.PATH_AUTO), ("swin_b_s3", sw.PATH_AUTO),
                                       ("swinv2_t_s1", sw.PATH_AUTO), ("swinv2_t_s1", sw.PATH_THREE_KERNELS),
                                       ("swinv2_l_w24", sw.PATH_AUTO)])
-def test_forward_full_size_sampled(key, path):
+def test_forward_full_size(key, path):
+    """The whole output of every full-size workload against the oracle: every
+    tile of every CTA, the persistent kernels' tile order and buffer / phase
+    alternation (which only grids of more tiles than SMs reach), every edge
+    window."""
     w = WORKLOADS[key]
-    g = generate(w)
+    g, table, ref = full_reference(key)
+    out = run_forward(w, device_inputs(g), table.to(DEV), path)
+    compare(out.double().cpu().numpy(), ref, w.dtype)
+
+
+# ---- V2 with a different tau per head, below the clip too ------------------------
+
+# tau per head: above the clip, at it, below it (clipped to 0.01), ...
+TAUS = {3: (0.3, 0.01, 0.004), 6: (0.3, 0.01, 0.004, 0.05, 1.0, 0.02)}
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("key,B,H,W", [("swinv2_t_s1", 2, 16, 24), ("swinv2_t_s1", 32, 64, 64),
+                                       ("swinv2_l_w24", 1, 48, 72)])
+def test_forward_v2_tau_per_head(key, B, H, W, path):
+    """Distinct tau per head, one of them below the 0.01 clip: a wrong head
+    index into tau, or a missing clip, changes the result.  The fused kernel
+    (windows of 8 x 8), the three-kernel path and the large-window kernel
+    (window 24) all take this case."""
+    w = WORKLOADS[key].with_(B=B, H=H, W=W)
+    if path == sw.PATH_AUTO and w.M > 8:
+        pytest.skip("window 24 runs the three-kernel path either way")
+    g = generate(w, nonzero_bias=True, tau=TAUS[w.heads])
     table = oracle_table(w, g)
     out = run_forward(w, device_inputs(g), table.to(DEV), path)
-    wins = sample_windows(w, 8 if w.M > 8 else 24)
-    ref = oracle_forward(w, g, table, windows=wins)
-    tok = window_tokens(w, wins)
-    got = out.double().cpu().numpy().reshape(-1, w.C)[tok]
-    compare(got, ref.reshape(-1, w.C)[tok], w.dtype)
-    assert torch.isfinite(out).all()
+    compare(out.double().cpu().numpy(), oracle_forward(w, g, table), w.dtype)
+
+
+# ---- the index maps through the whole forward, bit-exact -----------------------
+
+def one_hot_attention_inputs(w, x):
+    """Weights under which the block returns x exactly: Wq = Wk = 0 (every
+    logit is its bias), Wv = I, Wproj = I, zero biases, and a table that is 0
+    at displacement (0, 0) and -1e4 elsewhere.  Each row's softmax is then
+    exactly one-hot on the token itself (every other exp2 underflows to 0),
+    so out = x bit for bit on bf16-exact x whatever the shift mask does."""
+    C, L = w.C, 2 * w.M - 1
+    Wqkv = torch.zeros(3 * C, C, dtype=torch.bfloat16)
+    Wqkv[2 * C:] = torch.eye(C)
+    table = torch.full((L * L, w.heads), -1e4, dtype=torch.bfloat16)
+    table[(w.M - 1) * L + (w.M - 1)] = 0
+    t = {"x": torch.from_numpy(x).bfloat16().to(DEV), "Wqkv": Wqkv.to(DEV), "bqkv": None,
+         "Wproj": torch.eye(C, dtype=torch.bfloat16).to(DEV), "bproj": None}
+    if w.mode == V2:
+        t["tau"] = torch.full((w.heads,), 0.1, dtype=torch.float32, device=DEV)
+    return t, table.to(DEV)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("key,B,H,W", [("swin_t_s1", 64, 56, 56), ("swin_t_s1", 3, 21, 35),
+                                       ("swinv2_t_s1", 32, 64, 64), ("swinv2_t_s1", 1, 24, 16),
+                                       ("swin_b_s1", 5, 28, 28), ("swinv2_l_w24", 2, 48, 72)])
+def test_index_maps_bit_exact_through_whole_forward(key, B, H, W, path):
+    """S1 (roll by -s, partition) and S8 (reverse, roll by +s) compared bit
+    for bit through the whole forward on integer-tagged tokens: with the
+    one-hot weights above the block is the identity exactly when both maps
+    are right.  The full-size grids run every tile of the persistent fused
+    kernel (its TMA boxes for windows the shift does not wrap, cp.async and
+    plain stores for those it does)."""
+    w = WORKLOADS[key].with_(B=B, H=H, W=W)
+    if path == sw.PATH_AUTO and w.M > 8:
+        pytest.skip("window 24 runs the three-kernel path either way")
+    t, table = one_hot_attention_inputs(w, tagged(B, H, W, w.C))
+    out = run_forward(w, t, table, path)
+    assert torch.equal(out, t["x"]), int((out != t["x"]).sum())
 
 
 # ---- meta-network G table ---------------------------------------------------------

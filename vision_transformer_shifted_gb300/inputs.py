@@ -102,10 +102,11 @@ def torch_dtype(w: Workload):
     return torch.bfloat16 if w.dtype == "bf16" else torch.float32
 
 
-def generate(w: Workload, nonzero_bias: bool = False, tau: float = 0.1):
+def generate(w: Workload, nonzero_bias: bool = False, tau=0.1):
     """Seeded CPU tensors for workload ``w`` (already rounded to its dtype):
     x, Wqkv, bqkv, Wproj, bproj, and either ``table`` (V1) or the meta-network
-    weights W1, b1, W2 (V2, the table is built from them) plus ``tau``."""
+    weights W1, b1, W2 (V2, the table is built from them) plus ``tau``
+    (``tau``: one value for every head, or a sequence of one per head)."""
     g = torch.Generator().manual_seed(w.seed)
     dt = torch_dtype(w)
     C, h, M = w.C, w.heads, w.M
@@ -126,7 +127,11 @@ def generate(w: Workload, nonzero_bias: bool = False, tau: float = 0.1):
         out["W1"] = torch.randn((CPB_HIDDEN, 2), generator=g, dtype=torch.float32) * 0.02
         out["b1"] = torch.zeros(CPB_HIDDEN, dtype=torch.float32)
         out["W2"] = torch.randn((h, CPB_HIDDEN), generator=g, dtype=torch.float32) * 0.02
-        out["tau"] = torch.full((h,), float(tau), dtype=torch.float32)
+        if isinstance(tau, (int, float)):
+            out["tau"] = torch.full((h,), float(tau), dtype=torch.float32)
+        else:
+            assert len(tau) == h, "one tau per head"
+            out["tau"] = torch.tensor([float(t) for t in tau], dtype=torch.float32)
     return out
 
 
