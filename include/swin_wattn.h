@@ -56,9 +56,23 @@ enum {
     SWIN_WATTN_ENOMEM = -4,       /* device allocation of the handle's workspace failed */
     SWIN_WATTN_ETIMEOUT = -5,     /* a kernel gave up a bounded wait (reported by
                                      swin_wattn_sync_status) */
-    SWIN_WATTN_ESCRATCH = -6      /* the call needs more intermediate memory than the
+    SWIN_WATTN_ESCRATCH = -6,     /* the call needs more intermediate memory than the
                                      fixed scratch of swin_wattn_forward_noalloc holds */
+    SWIN_WATTN_ECORRUPT = -7      /* with SWIN_WATTN_DEBUG set only: a guard band
+                                     around a handle's workspace was overwritten */
 };
+
+/* Environment switches (read whenever a handle allocates or grows a device
+ * workspace; no effect on calls that need no new workspace):
+ *   SWIN_WATTN_FAIL_ALLOC  set and not "0": every such allocation fails as if
+ *       the device were out of memory, and the call returns SWIN_WATTN_ENOMEM
+ *       (the handle stays usable; a later call with the switch unset
+ *       allocates normally).  For testing a caller's error path.
+ *   SWIN_WATTN_DEBUG       set and not "0": each such workspace is allocated
+ *       with a 4 KiB guard band on either side, filled with a byte pattern.
+ *       After every call that used the workspace the library synchronises the
+ *       call's stream and reads the bands back; a changed byte returns
+ *       SWIN_WATTN_ECORRUPT.  For debugging only (it serialises the stream). */
 
 /* Options for swin_wattn_set_option. */
 enum {
@@ -192,12 +206,15 @@ const char *swin_wattn_last_cuda_error(swin_wattn_t h);
  * before any launch.
  * Set-up: the first call on a device looks up the device address of the
  * array (this can load the library's device code on that device); make that
- * first call before any stream capture.  Later calls reuse the address.
+ * first call before any stream capture.  Later calls reuse the address while
+ * the device's context stays the same; after a device reset (a new context)
+ * the next call looks it up again, and counts as a first call.
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents; the call clears the status word it needs itself.  Calls
  * whose work overlaps on the GPU (different streams, or several host threads)
  * race on the array and corrupt each other's results: serialise them.
- * A bounded-wait timeout inside the kernels is not reported by this call.
+ * A bounded-wait timeout inside the kernels is recorded in the array's status
+ * word and read back by swin_wattn_noalloc_sync_status.
  * Errors: EINVAL / EUNSUPPORTED as swin_wattn_create and swin_wattn_forward
  * (fp32 mode is EUNSUPPORTED), ESCRATCH as above, ECUDA if a launch fails.
  * B == 0 is a no-op. */
@@ -205,6 +222,15 @@ int swin_wattn_forward_noalloc(int C, int heads, int M, int shift, int mode, con
                                int W, const void *Wqkv, const void *bqkv, const void *bias_table,
                                const float *logit_scale, const void *Wproj, const void *bproj, void *out,
                                swin_stream_t stream);
+
+/* Status of the swin_wattn_forward_noalloc calls made on the current device
+ * so far: waits for `stream` (the stream of those calls), reads the status
+ * word of the fixed array (one small device-to-host copy, no allocation) and
+ * clears it.  Returns SWIN_WATTN_ETIMEOUT if a kernel of one of those calls
+ * gave up a bounded wait (its output is then incomplete), SWIN_WATTN_OK if
+ * none did, SWIN_WATTN_ECUDA if the wait or the copy failed.  Like the entry
+ * point itself, it has no counterpart in the sources. */
+int swin_wattn_noalloc_sync_status(swin_stream_t stream);
 
 #ifdef __cplusplus
 }

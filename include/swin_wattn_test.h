@@ -59,11 +59,22 @@ int swin_wattn_test_proj(swin_wattn_t h, const void *attn, int B, int H, int W,
 int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *D, int rows, int N,
                          int K, int swizzle_bytes, swin_stream_t stream);
 
+/* Overwrites one byte of a guard band of the handle's forward workspace
+ * (side 0: the band before it, 1: the band after it), so that the
+ * SWIN_WATTN_DEBUG check can be tested.  EINVAL unless the workspace was
+ * allocated with guard bands. */
+int swin_wattn_test_corrupt_workspace(swin_wattn_t h, int side);
+
 /* Runs a one-block kernel that waits on a barrier nothing completes, with the
  * handle's wait limit, so that the bounded-wait path can be tested: the
  * kernel records a timeout in the handle's error word and returns; the
  * caller then reads ETIMEOUT from swin_wattn_sync_status. */
 int swin_wattn_test_watchdog(swin_wattn_t h, swin_stream_t stream);
+
+/* The same kernel, reporting into the status word of the fixed array of
+ * swin_wattn_forward_noalloc, with a wait limit of wait_limit_us (1 us to
+ * 60 s): swin_wattn_noalloc_sync_status then returns ETIMEOUT once. */
+int swin_wattn_test_noalloc_watchdog(int64_t wait_limit_us, swin_stream_t stream);
 
 #ifdef __cplusplus
 }

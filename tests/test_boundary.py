@@ -30,7 +30,7 @@ def test_library_exports_every_declared_function():
 
 
 def test_strerror_covers_every_status():
-    for code in (sw.OK, sw.EINVAL, sw.EUNSUPPORTED, sw.ECUDA, sw.ENOMEM, sw.ETIMEOUT, sw.ESCRATCH):
+    for code in (sw.OK, sw.EINVAL, sw.EUNSUPPORTED, sw.ECUDA, sw.ENOMEM, sw.ETIMEOUT, sw.ESCRATCH, sw.ECORRUPT):
         assert sw.strerror(code) != "unknown status"
     assert sw.strerror(12345) == "unknown status"
 

@@ -5,10 +5,14 @@ not own (a framework caching allocator that must account for every byte, an
 embedded runtime with a fixed budget) or code that must not allocate once it
 is serving (a cudaMalloc would synchronise the device).  The entry point
 keeps its intermediates in a fixed array inside the library.  These tests
-call it through the C ABI and check it against swin_wattn_forward, the entry
-point with a handle-owned workspace, on two calls in a row (the array keeps
-the previous call's contents, so the second call must not depend on them),
-and check that a call too large for the array is refused before any launch.
+call it through the C ABI and check it on two calls in a row (the array
+keeps the previous call's contents, so the second call must not depend on
+them): against the float64 oracle within the bf16 tolerances, and bit for
+bit against swin_wattn_forward (the entry point with a handle-owned
+workspace) forced onto the same three kernels.  They also check that the
+device's free memory does not move across calls, that a call too large for
+the array is refused before any launch, and that a kernel's bounded-wait
+timeout reaches the caller through swin_wattn_noalloc_sync_status.
 
 This file is collected last on purpose, and it needs no state from the
 other test files.
@@ -19,7 +23,7 @@ import torch
 from vision_transformer_shifted_gb300 import binding as sw
 from vision_transformer_shifted_gb300.inputs import V2, WORKLOADS, generate
 
-from helpers import compare, device_inputs, oracle_table
+from helpers import compare, device_inputs, oracle_forward, oracle_table
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -32,9 +36,10 @@ def _lib():
     sw.load()
 
 
-def forward_with_handle(w, t, table):
+def forward_with_handle(w, t, table, path):
     h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
     try:
+        sw.swin_wattn_set_option(h, sw.OPT_PATH, path)
         out = torch.full_like(t["x"], float("nan"))
         sw.swin_wattn_forward(h, t["x"], t["Wqkv"], t["bqkv"], table, t.get("tau"), t["Wproj"], t["bproj"], out)
         assert sw.swin_wattn_sync_status(h) == sw.OK
@@ -43,24 +48,44 @@ def forward_with_handle(w, t, table):
         sw.swin_wattn_destroy(h)
 
 
+def noalloc(w, t, table, out):
+    sw.swin_wattn_forward_noalloc(w.C, w.heads, w.M, w.shift, w.mode, t["x"], t["Wqkv"], t["bqkv"], table,
+                                  t.get("tau"), t["Wproj"], t["bproj"], out)
+
+
 @pytest.mark.parametrize("key,B,H,W", [("swin_t_s1", 4, 56, 56), ("swinv2_t_s1", 2, 64, 64),
                                        ("swinv2_l_w24", 1, 48, 96)])
-def test_noalloc_matches_forward_on_two_calls_in_a_row(key, B, H, W):
+def test_noalloc_matches_oracle_and_forward_on_two_calls_in_a_row(key, B, H, W):
     w = WORKLOADS[key].with_(B=B, H=H, W=W)
     assert 8 * w.tokens * w.C <= sw.NOALLOC_MAX_INTERMEDIATE_BYTES
     results = []
     for seed_shift in (0, 1):   # two different inputs, one call after the other
-        g = generate(w.with_(seed=w.seed + 17 * seed_shift), nonzero_bias=True)
+        g = generate(w.with_(seed=w.seed + 17 * seed_shift), nonzero_bias=True,
+                     tau=(0.3, 0.01, 0.004, 0.05, 1.0, 0.02)[:w.heads] if w.mode == V2 else 0.1)
         t = device_inputs(g)
-        table = oracle_table(w, g).to(DEV)
+        table = oracle_table(w, g)
+        td = table.to(DEV)
         out = torch.full_like(t["x"], float("nan"))
-        sw.swin_wattn_forward_noalloc(w.C, w.heads, w.M, w.shift, w.mode, t["x"], t["Wqkv"], t["bqkv"], table,
-                                      t.get("tau"), t["Wproj"], t["bproj"], out)
         torch.cuda.synchronize()
-        results.append((out, forward_with_handle(w, t, table)))
-    for got, want in results:
-        compare(got.double().cpu().numpy(), want.double().cpu().numpy(), "bf16")
-    assert not torch.equal(results[0][0], results[1][0])
+        noalloc(w, t, td, out)
+        assert sw.swin_wattn_noalloc_sync_status() == sw.OK
+        results.append((g, table, out, forward_with_handle(w, t, td, sw.PATH_THREE_KERNELS)))
+    for g, table, got, same_kernels in results:
+        compare(got.double().cpu().numpy(), oracle_forward(w, g, table), "bf16")
+        # the same three kernels on the same inputs: the same bits
+        assert torch.equal(got, same_kernels)
+    assert not torch.equal(results[0][2], results[1][2])
+    # a third call on the first inputs: no device memory taken or given back
+    g, table, first, _ = results[0]
+    t = device_inputs(g)
+    td = table.to(DEV)
+    out = torch.full_like(t["x"], float("nan"))
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    noalloc(w, t, td, out)
+    assert sw.swin_wattn_noalloc_sync_status() == sw.OK
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert torch.equal(out, first)
 
 
 def test_noalloc_refuses_calls_larger_than_its_scratch():
@@ -88,3 +113,19 @@ def test_noalloc_rejects_bad_arguments():
         with pytest.raises(sw.SwinWAttnError) as ei:
             sw.swin_wattn_forward_noalloc(*params, *args)
         assert ei.value.code == code
+
+
+def test_noalloc_reports_a_bounded_wait_timeout():
+    """A kernel that waits on a barrier nothing completes (20 ms limit)
+    records the timeout in the fixed array's status word: the status call
+    reports it once, clears it, and a normal call then succeeds."""
+    sw.swin_wattn_test_noalloc_watchdog(20000)
+    assert sw.swin_wattn_noalloc_sync_status() == sw.ETIMEOUT
+    assert sw.swin_wattn_noalloc_sync_status() == sw.OK
+    w = WORKLOADS["swin_t_s1"].with_(B=2, H=14, W=21)
+    g = generate(w, nonzero_bias=True)
+    t = device_inputs(g)
+    out = torch.full_like(t["x"], float("nan"))
+    noalloc(w, t, t["table"], out)
+    assert sw.swin_wattn_noalloc_sync_status() == sw.OK
+    compare(out.double().cpu().numpy(), oracle_forward(w, g, g["table"]), "bf16")

@@ -16,7 +16,7 @@ import torch
 from . import build as _build
 
 V1, V2, FP32 = 0, 1, 0x10
-OK, EINVAL, EUNSUPPORTED, ECUDA, ENOMEM, ETIMEOUT, ESCRATCH = 0, -1, -2, -3, -4, -5, -6
+OK, EINVAL, EUNSUPPORTED, ECUDA, ENOMEM, ETIMEOUT, ESCRATCH, ECORRUPT = 0, -1, -2, -3, -4, -5, -6, -7
 NOALLOC_MAX_INTERMEDIATE_BYTES = (64 << 20) - 256
 OPT_PATH, OPT_WAIT_LIMIT_US, OPT_HOST_CHUNKS = 1, 2, 3
 PATH_AUTO, PATH_THREE_KERNELS, PATH_FUSED, PATH_FP32 = 0, 1, 2, 3
@@ -45,8 +45,11 @@ _SIGNATURES = {
     "swin_wattn_test_proj": ["p", "p", "i", "i", "i", "p", "p", "p", "p"],
     "swin_wattn_test_gemm": ["p", "p", "p", "p", "i", "i", "i", "i", "p"],
     "swin_wattn_test_watchdog": ["p", "p"],
+    "swin_wattn_test_corrupt_workspace": ["p", "i"],
     "swin_wattn_forward_noalloc": ["i", "i", "i", "i", "i", "p", "i", "i", "i", "p", "p", "p", "p", "p", "p", "p",
                                    "p"],
+    "swin_wattn_noalloc_sync_status": ["p"],
+    "swin_wattn_test_noalloc_watchdog": ["l", "p"],
     "swin_block_create": ["pp", "i", "i", "i", "i", "i", "i"],
     "swin_block_forward": ["p", "p", "i", "i", "i", "p", "p", "p"],
     "swin_block_sync_status": ["p", "p"],
@@ -204,6 +207,17 @@ def swin_wattn_forward_noalloc(C, heads, M, shift, mode, x, Wqkv, bqkv, bias_tab
         _p(bproj), _p(out), _stream(stream)))
 
 
+def swin_wattn_noalloc_sync_status(stream=None):
+    """Status of the swin_wattn_forward_noalloc calls on the current device:
+    the status code (OK, ETIMEOUT or ECUDA), without raising."""
+    return load().swin_wattn_noalloc_sync_status(_stream(stream))
+
+
+def swin_wattn_test_noalloc_watchdog(wait_limit_us, stream=None):
+    return _check("swin_wattn_test_noalloc_watchdog",
+                  load().swin_wattn_test_noalloc_watchdog(int(wait_limit_us), _stream(stream)))
+
+
 def swin_wattn_test_qkv(h, x, Wqkv, bqkv, qkv, stream=None):
     B, H, W, _ = x.shape
     return _check("swin_wattn_test_qkv", load().swin_wattn_test_qkv(
@@ -225,6 +239,10 @@ def swin_wattn_test_gemm(A, Bw, bias, D, swizzle_bytes=128, stream=None):
     N = Bw.shape[0]
     return _check("swin_wattn_test_gemm", load().swin_wattn_test_gemm(
         _p(A), _p(Bw), _p(bias), _p(D), rows, N, K, swizzle_bytes, _stream(stream)))
+
+
+def swin_wattn_test_corrupt_workspace(h, side):
+    return _check("swin_wattn_test_corrupt_workspace", load().swin_wattn_test_corrupt_workspace(h, side))
 
 
 def swin_wattn_test_watchdog(h, stream=None):

@@ -70,24 +70,17 @@ int choose_path(const swin_wattn_s *h, int64_t T)
     return fused_supported(h->M, h->C, h->heads) && T < ((int64_t)1 << 31) ? 2 : 1;
 }
 
-int ensure_buffer(void **buf, size_t *have, size_t need)
+DeviceStatus dstatus(const swin_wattn_s *h) { return DeviceStatus{h->d_err, h->wait_ns}; }
+
+// Guard bands (SWIN_WATTN_DEBUG) of the buffers the host-buffer forward uses.
+int check_host_guards(const swin_wattn_s *h, cudaStream_t s)
 {
-    if (*have >= need) return SWIN_WATTN_OK;
-    if (*buf) {
-        cudaFree(*buf);
-        *buf = nullptr;
-        *have = 0;
+    for (const void *b : {h->stage_x, h->stage_out, h->ws}) {
+        const int rc = ws_check(b, s);
+        if (rc) return rc;
     }
-    if (cudaMalloc(buf, need) != cudaSuccess) {
-        *buf = nullptr;
-        cudaGetLastError();
-        return SWIN_WATTN_ENOMEM;
-    }
-    *have = need;
     return SWIN_WATTN_OK;
 }
-
-DeviceStatus dstatus(const swin_wattn_s *h) { return DeviceStatus{h->d_err, h->wait_ns}; }
 
 int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
                 const void *table, const float *tau, const void *Wproj, const void *bproj, void *out,
@@ -122,7 +115,7 @@ int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void 
     }
     if (path != 1) return SWIN_WATTN_EUNSUPPORTED;
     const size_t qkv_bytes = (size_t)g.T * 3 * h->C * 2, attn_bytes = (size_t)g.T * h->C * 2;
-    int rc = ensure_buffer(&h->ws, &h->ws_bytes, qkv_bytes + attn_bytes);
+    int rc = ws_ensure(&h->ws, &h->ws_bytes, qkv_bytes + attn_bytes);
     if (rc) return rc;
     bf16 *qkv = (bf16 *)h->ws;
     bf16 *attn = (bf16 *)((char *)h->ws + qkv_bytes);
@@ -266,10 +259,11 @@ int swin_wattn_destroy(swin_wattn_t h)
 {
     if (!h) return SWIN_WATTN_OK;
     cudaDeviceSynchronize();
-    if (h->ws) cudaFree(h->ws);
-    if (h->stage_x) cudaFree(h->stage_x);
-    if (h->stage_out) cudaFree(h->stage_out);
-    if (h->bws) cudaFree(h->bws);
+    ws_free(&h->ws, &h->ws_bytes);
+    size_t have = 0;
+    ws_free(&h->stage_x, &have);
+    ws_free(&h->stage_out, &have);
+    ws_free(&h->bws, &h->bws_bytes);
     if (h->blas) cublasDestroy(h->blas);
     if (h->hs_ready) {
         for (cudaStream_t st : h->hs) cudaStreamDestroy(st);
@@ -293,7 +287,9 @@ int swin_wattn_forward(swin_wattn_t h, const void *x, int B, int H, int W, const
 {
     int rc = check_forward_args(h, x, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out, true);
     if (rc) return rc;
-    return run_forward(h, x, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out, (cudaStream_t)stream);
+    rc = run_forward(h, x, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out, (cudaStream_t)stream);
+    if (rc) return rc;
+    return ws_check(h->ws, (cudaStream_t)stream);
 }
 
 int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, int W, const void *Wqkv,
@@ -307,8 +303,8 @@ int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, in
     if (bytes == 0) return SWIN_WATTN_OK;
     if (h->stage_bytes < bytes) {
         size_t have_x = h->stage_bytes, have_o = h->stage_bytes;
-        rc = ensure_buffer(&h->stage_x, &have_x, bytes);
-        if (!rc) rc = ensure_buffer(&h->stage_out, &have_o, bytes);
+        rc = ws_ensure(&h->stage_x, &have_x, bytes);
+        if (!rc) rc = ws_ensure(&h->stage_out, &have_o, bytes);
         if (rc) return rc;
         h->stage_bytes = bytes;
     }
@@ -341,7 +337,7 @@ int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, in
         const int64_t Tc = (int64_t)bmax * H * W;
         const int path = h->path_opt ? h->path_opt : choose_path(h, Tc);
         if (!h->fp32 && path == 1) {
-            rc = ensure_buffer(&h->ws, &h->ws_bytes, (size_t)Tc * 4 * h->C * 2);
+            rc = ws_ensure(&h->ws, &h->ws_bytes, (size_t)Tc * 4 * h->C * 2);
             if (rc) return rc;
         }
     }
@@ -381,12 +377,14 @@ int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, in
             rc = enqueue_host_chunks(h, x_host, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out_host,
                                      s, true);
             if (rc) return rc;
-            return cudaEventRecord(h->ev_done, s) == cudaSuccess ? SWIN_WATTN_OK : SWIN_WATTN_ECUDA;
+            if (cudaEventRecord(h->ev_done, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
+            return check_host_guards(h, s);
         }
     }
     if (cudaGraphLaunch(h->graph, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
     h->last_launches = h->g_launches;
-    return cudaEventRecord(h->ev_done, s) == cudaSuccess ? SWIN_WATTN_OK : SWIN_WATTN_ECUDA;
+    if (cudaEventRecord(h->ev_done, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    return check_host_guards(h, s);
 }
 
 int swin_wattn_cpb_table(swin_wattn_t h, const float *W1, const float *b1, const float *W2, int hidden, void *table,
@@ -460,6 +458,7 @@ const char *swin_wattn_strerror(int code)
     case SWIN_WATTN_ENOMEM: return "device allocation failed";
     case SWIN_WATTN_ETIMEOUT: return "a kernel gave up a bounded wait";
     case SWIN_WATTN_ESCRATCH: return "intermediates exceed the fixed scratch of swin_wattn_forward_noalloc";
+    case SWIN_WATTN_ECORRUPT: return "a guard band around a workspace was overwritten (SWIN_WATTN_DEBUG)";
     default: return "unknown status";
     }
 }
@@ -514,7 +513,7 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     const size_t tc = (size_t)g.T * C;
     const size_t norm_bytes = v2 ? (size_t)g.T * 2 * h->heads * 4 : 0;
     const size_t flash_bytes = flash ? (size_t)g.T * 2 * h->heads * 4 + tc * 4 : 0;
-    rc = ensure_buffer(&h->bws, &h->bws_bytes, (8 * tc + 4 * (size_t)C * C) * 2 + norm_bytes + flash_bytes);
+    rc = ws_ensure(&h->bws, &h->bws_bytes, (8 * tc + 4 * (size_t)C * C) * 2 + norm_bytes + flash_bytes);
     if (rc) return rc;
     if (!h->blas) {
         if (cublasCreate(&h->blas) != CUBLAS_STATUS_SUCCESS) { h->blas = nullptr; return SWIN_WATTN_ECUDA; }
@@ -570,7 +569,7 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     if (weight_grad(h->blas, dqkv, 3 * C, (const bf16 *)x, C, g.T, dWqkv) != CUBLAS_STATUS_SUCCESS)
         return SWIN_WATTN_ECUDA;
     h->bw_launches = launches + 2;
-    return SWIN_WATTN_OK;
+    return ws_check(h->bws, s);
 }
 
 int swin_wattn_backward_launches(swin_wattn_t h) { return h ? h->bw_launches : 0; }
@@ -658,6 +657,12 @@ int swin_wattn_test_gemm(const void *A, const void *Bw, const void *bias, void *
         return cuda_status(launch_gemm_pair_test(a, st, (cudaStream_t)stream));
     }
     return cuda_status(launch_gemm(a, LOAD_PLAIN, STORE_PLAIN, st, (cudaStream_t)stream));
+}
+
+int swin_wattn_test_corrupt_workspace(swin_wattn_t h, int side)
+{
+    if (!h || (side != 0 && side != 1)) return SWIN_WATTN_EINVAL;
+    return ws_test_corrupt(h->ws, side);
 }
 
 int swin_wattn_test_watchdog(swin_wattn_t h, swin_stream_t stream)

@@ -216,7 +216,7 @@ int swin_block_create(swin_block_t *out, int C, int heads, int M, int shift, int
 int swin_block_destroy(swin_block_t h)
 {
     if (!h) return SWIN_WATTN_OK;
-    if (h->ws) cudaFree(h->ws);
+    ws_free(&h->ws, &h->ws_bytes);
     if (h->d_err) cudaFree(h->d_err);
     swin_wattn_destroy(h->attn);
     delete h;
@@ -258,16 +258,8 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
     }
     if (B == 0) return SWIN_WATTN_OK;
     const size_t need = (size_t)T * (3 * C + R) * 2;
-    if (h->ws_bytes < need) {
-        if (h->ws) cudaFree(h->ws);
-        h->ws = nullptr;
-        h->ws_bytes = 0;
-        if (cudaMalloc(&h->ws, need) != cudaSuccess) {
-            cudaGetLastError();
-            return SWIN_WATTN_ENOMEM;
-        }
-        h->ws_bytes = need;
-    }
+    int wrc = ws_ensure(&h->ws, &h->ws_bytes, need);
+    if (wrc) return wrc;
     cudaStream_t s = (cudaStream_t)stream;
     bf16 *z = (bf16 *)h->ws, *t1 = z + T * C, *t2 = t1 + T * C, *m1 = t2 + T * C;
     const bf16 *xx = (const bf16 *)x;
@@ -313,7 +305,7 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
         if ((e = gemm(m1, R, p->W2, p->b2, t1, C, EPI_NONE, nullptr)) != cudaSuccess) return cuda_status(e);
         if ((e = launch_layernorm(t1, z, g2, be2, nullptr, yy, T, C, 2, s)) != cudaSuccess) return cuda_status(e);
     }
-    return SWIN_WATTN_OK;
+    return ws_check(h->ws, s);
 }
 
 int swin_block_test_layernorm(const void *a, const void *b, const void *gamma, const void *beta, void *out_sum,
@@ -363,7 +355,7 @@ int swin_merge_create(swin_merge_t *out, int C)
 int swin_merge_destroy(swin_merge_t h)
 {
     if (!h) return SWIN_WATTN_OK;
-    if (h->ws) cudaFree(h->ws);
+    ws_free(&h->ws, &h->ws_bytes);
     if (h->d_err) cudaFree(h->d_err);
     delete h;
     return SWIN_WATTN_OK;
@@ -387,16 +379,8 @@ int swin_merge_forward(swin_merge_t h, const void *x, int B, int H, int W, const
     }
     if (B == 0) return SWIN_WATTN_OK;
     const size_t need = (size_t)rows * 4 * C * 2;
-    if (h->ws_bytes < need) {
-        if (h->ws) cudaFree(h->ws);
-        h->ws = nullptr;
-        h->ws_bytes = 0;
-        if (cudaMalloc(&h->ws, need) != cudaSuccess) {
-            cudaGetLastError();
-            return SWIN_WATTN_ENOMEM;
-        }
-        h->ws_bytes = need;
-    }
+    int wrc = ws_ensure(&h->ws, &h->ws_bytes, need);
+    if (wrc) return wrc;
     cudaStream_t s = (cudaStream_t)stream;
     bf16 *u = (bf16 *)h->ws;
     cudaError_t e = launch_layernorm((const bf16 *)x, nullptr, (const bf16 *)gamma, (const bf16 *)beta, nullptr, u,
@@ -412,7 +396,8 @@ int swin_merge_forward(swin_merge_t h, const void *x, int B, int H, int W, const
     a.N = 2 * C;
     a.K = 4 * C;
     a.g = make_geom(1, 1, 1, 2 * C, 1, 0);
-    return cuda_status(launch_gemm(a, LOAD_PLAIN, STORE_PLAIN, DeviceStatus{h->d_err, 2000000000ull}, s));
+    const int rc = cuda_status(launch_gemm(a, LOAD_PLAIN, STORE_PLAIN, DeviceStatus{h->d_err, 2000000000ull}, s));
+    return rc ? rc : ws_check(h->ws, s);
 }
 
 } // extern "C"

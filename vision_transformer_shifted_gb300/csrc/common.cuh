@@ -100,6 +100,19 @@ struct DeviceStatus {
     uint64_t wait_ns;  // limit of every bounded wait
 };
 
+// ---- handle-owned workspaces (workspace.cu) ------------------------------------
+
+// Grows *buf to at least `need` bytes (freeing the old buffer): SWIN_WATTN_OK,
+// SWIN_WATTN_ENOMEM (also whenever the environment sets SWIN_WATTN_FAIL_ALLOC)
+// or SWIN_WATTN_ECUDA.  With SWIN_WATTN_DEBUG set the buffer gets guard bands.
+int ws_ensure(void **buf, size_t *have, size_t need);
+void ws_free(void **buf, size_t *have);
+// For a buffer with guard bands: synchronises `stream` and returns
+// SWIN_WATTN_ECORRUPT if a band changed; SWIN_WATTN_OK at once otherwise.
+int ws_check(const void *buf, cudaStream_t stream);
+// Test hook: overwrites one byte of a guard band (side 0: before, 1: after).
+int ws_test_corrupt(const void *buf, int side);
+
 // ---- kernel launchers (return cudaSuccess or the error) ----------------------
 
 enum { LOAD_PLAIN = 0, LOAD_GATHER = 1 };

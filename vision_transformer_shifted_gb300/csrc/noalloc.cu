@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "swin_wattn.h"
+#include "swin_wattn_test.h"
 #include "common.cuh"
 
 using namespace swin;
@@ -26,11 +27,33 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void *g_scratch_on_device[kMaxDevices]; // device address of the array, per device
+// Per device: the device address of the array and the context it was looked
+// up in.  A device reset (or the primary context released and created again)
+// gives the device a new context, in which the library's device code -- and
+// so the array -- is loaded again, possibly at another address: the address
+// is looked up again whenever the current context differs.
+void *g_scratch_on_device[kMaxDevices];
+void *g_scratch_context[kMaxDevices];
+
+// cuCtxGetCurrent through the runtime's driver entry point (the library does
+// not link libcuda itself).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+CtxGetCurrentFn ctx_get_current()
+{
+    static CtxGetCurrentFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(f);
+    }();
+    return fn;
+}
 
 // The device address of the scratch on the current device.  The first call on
-// a device looks it up (this may load the library's device code on that
-// device); later calls reuse it.
+// a device (and the first after its context changed) looks it up, which may
+// load the library's device code on that device; later calls reuse it.
 int scratch_address(void **out)
 {
     int dev = 0;
@@ -39,16 +62,25 @@ int scratch_address(void **out)
         return SWIN_WATTN_ECUDA;
     }
     if (dev < 0 || dev >= kMaxDevices) return SWIN_WATTN_EUNSUPPORTED;
+    // (cudaGetSymbolAddress below makes the device's primary context current
+    // if none is; the context is read after it)
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_on_device[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return SWIN_WATTN_ECUDA;
-        }
-        g_scratch_on_device[dev] = p;
+    CUcontext ctx = nullptr;
+    CtxGetCurrentFn get = ctx_get_current();
+    if (g_scratch_on_device[dev] && get && get(&ctx) == CUDA_SUCCESS && ctx == g_scratch_context[dev]) {
+        *out = g_scratch_on_device[dev];
+        return SWIN_WATTN_OK;
     }
-    *out = g_scratch_on_device[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return SWIN_WATTN_ECUDA;
+    }
+    ctx = nullptr;
+    if (!get || get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+    g_scratch_on_device[dev] = p;
+    g_scratch_context[dev] = ctx;   // null: looked up again on every call
+    *out = p;
     return SWIN_WATTN_OK;
 }
 
@@ -108,4 +140,29 @@ extern "C" int swin_wattn_forward_noalloc(int C, int heads, int M, int shift, in
     k3.D = (bf16 *)out; k3.ldd = C; k3.rows = g.T; k3.N = C; k3.K = C; k3.g = g;
     if (launch_gemm(k3, LOAD_PLAIN, STORE_SCATTER, st, s) != cudaSuccess) return SWIN_WATTN_ECUDA;
     return SWIN_WATTN_OK;
+}
+
+extern "C" int swin_wattn_noalloc_sync_status(swin_stream_t stream)
+{
+    void *base = nullptr;
+    int rc = scratch_address(&base);
+    if (rc) return rc;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    int err = 0;
+    if (cudaMemcpy(&err, base, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SWIN_WATTN_ECUDA;
+    if (err) {
+        if (cudaMemset(base, 0, sizeof(int)) != cudaSuccess) return SWIN_WATTN_ECUDA;
+        if (err & ERR_TIMEOUT) return SWIN_WATTN_ETIMEOUT;
+    }
+    return SWIN_WATTN_OK;
+}
+
+extern "C" int swin_wattn_test_noalloc_watchdog(int64_t wait_limit_us, swin_stream_t stream)
+{
+    if (wait_limit_us <= 0 || wait_limit_us > 60000000) return SWIN_WATTN_EINVAL;
+    void *base = nullptr;
+    int rc = scratch_address(&base);
+    if (rc) return rc;
+    const DeviceStatus st{reinterpret_cast<int *>(base), (uint64_t)wait_limit_us * 1000ull};
+    return launch_watchdog(st, (cudaStream_t)stream) == cudaSuccess ? SWIN_WATTN_OK : SWIN_WATTN_ECUDA;
 }
