@@ -40,7 +40,7 @@ from vision_transformer_shifted_gb300.inputs import V1, V2, WORKLOADS, generate 
 
 L2_BYTES = 129 * 1024 * 1024
 
-# DRAM bytes (read + write) per launch from ncu captures (profiles/*.md), keyed by
+# DRAM bytes (read + write) per launch from ncu captures, keyed by
 # workload and kernel, with the sha1 prefix of the kernel source they were taken
 # on: reported only while the source is unchanged.
 PROFILED_TRAFFIC = {
@@ -61,6 +61,8 @@ def profiled_traffic(workload, kernel):
         return None
     return ent[0] if sha == ent[2] else None
 METRIC = "fused shifted-window attn block tokens/s & TFLOP/s; % of bf16/HBM roofline"
+# the workloads of the 'configs' record, in their order of definition
+CONFIG_KEYS = ["tiny", "swin_t_s1", "swin_b_s1", "swin_b_s3", "swinv2_t_s1", "swinv2_l_w24"]
 
 
 def peaks():
@@ -232,17 +234,15 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, w):
-    from vision_transformer_shifted_gb300 import binding as sw
-    rank, world, local, dist = dist_setup(args.gpus)
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
-    sw.load()
-    pk = peaks()
+def measure_forward(sw, w, dev, pk, args, steps, soak, rank=0, world=1, dist=None, path=0):
+    """Times `steps` forwards of workload `w` (CUDA events on the launching
+    stream, inputs rotated over buffer sets larger than 2x L2), then each
+    kernel of the three-kernel path on its own.  Returns a dict of figures and
+    the objects the end-to-end leg reuses."""
     mode = w.mode | (sw.FP32 if w.dtype == "fp32" else 0)
     h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, mode)
-    if args.path:
-        sw.swin_wattn_set_option(h, sw.OPT_PATH, args.path)
+    if path:
+        sw.swin_wattn_set_option(h, sw.OPT_PATH, path)
     g = generate(rank_workload(w, rank))
     t = {k: (v.to(dev) if v is not None else None) for k, v in g.items()}
     table = table_for(w, g, dev, h)
@@ -261,44 +261,84 @@ def run_ours(args, w):
         step(i)
     assert sw.swin_wattn_sync_status(h, stream) == sw.OK
     launches_per_step = sw.swin_wattn_last_launches(h)
-
-    with ClockSampler(dev.index) as clk:
-        # soak (untimed) so that the clock record covers a loaded GPU, then time K steps
-        t_soak = time.perf_counter()
-        i = 0
-        while time.perf_counter() - t_soak < args.soak:
-            step(i)
-            i += 1
-            if i % 64 == 0:
-                torch.cuda.synchronize()
-        torch.cuda.synchronize()
-        barrier(dist)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(args.steps):
-            step(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier(dist)
-    ms = max_over_ranks(e0.elapsed_time(e1), dist) / args.steps
+    # soak (untimed) so that the clock record covers a loaded GPU, then time the steps
+    t_soak = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_soak < soak:
+        step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms = max_over_ranks(e0.elapsed_time(e1), dist) / steps
     assert sw.swin_wattn_sync_status(h, stream) == sw.OK
-    tokens_s = job_rate(w.tokens, world, ms * 1e-3)
     tflops = w.flops * world / (ms * 1e-3) / 1e12
+    path = ("three kernels" if launches_per_step >= 3 else "fp32 block" if w.dtype == "fp32" else "fused")
+    res = {"ms_per_step": ms, "tokens_per_s": job_rate(w.tokens, world, ms * 1e-3), "tflops": tflops,
+           "path": path, "launches_per_step": launches_per_step,
+           "l2": "inputs rotated over %d buffer sets of %.0f MB (x + out), %.0f MB > 2x L2" %
+                 (nsets, io_bytes / 2 ** 20, nsets * io_bytes / 2 ** 20)}
+    if w.dtype == "bf16":
+        # whole-block roofline: min(dense bf16 peak, HBM x algorithmic intensity)
+        ai = w.flops / w.io_bytes
+        bound_tf = min(pk["bf16_sust"], pk["hbm"] * 1e9 * ai / 1e12)
+        res["block_roofline"] = {"achieved_tflops": tflops / world, "roof_tflops": bound_tf,
+                                 "frac": tflops / world / bound_tf, "ai_flop_per_byte": ai,
+                                 "algorithmic_bytes": w.io_bytes, "algorithmic_flops": w.flops,
+                                 "peak_source": pk["source"] + " (sustained bf16 / copy GB/s)"}
+        kernels = {}
+        if launches_per_step >= 3:   # the three-kernel path (the QKV GEMM may take several launches)
+            kernels = per_kernel_times(sw, h, w, t, table, xs, stream, steps)
+        roof = dominant_roofline(w, kernels, pk, ms)
+        roof["traffic"] = profiled_traffic(w.key, roof["kernel"])
+        res["roofline"] = roof
+        res["kernels_us"] = kernels
+    else:
+        # the tiny fp32 workload is a correctness case: no roofline
+        res["block_roofline"] = None
+        res["roofline"] = None
+    return res, (h, g, t, table, stream)
 
-    # whole-block roofline: min(dense bf16 peak, HBM x algorithmic intensity)
-    ai = w.flops / w.io_bytes
-    bound_tf = min(pk["bf16_sust"], pk["hbm"] * 1e9 * ai / 1e12)
-    block_roof = {"achieved_tflops": tflops / world, "roof_tflops": bound_tf, "frac": tflops / world / bound_tf,
-                  "ai_flop_per_byte": ai, "algorithmic_bytes": w.io_bytes, "algorithmic_flops": w.flops,
-                  "peak_source": pk["source"] + " (sustained bf16 / copy GB/s)"}
 
-    # per-kernel durations of the three-kernel path (stage hooks, same stream)
-    kernels = {}
-    if launches_per_step >= 3:   # the three-kernel path (the QKV GEMM may take several launches)
-        kernels = per_kernel_times(sw, h, w, t, table, xs, stream, args.steps)
-    roof = dominant_roofline(w, kernels, pk, ms)
-    roof["traffic"] = profiled_traffic(w.key, roof["kernel"])
+def oracle_baseline(w, g, seconds):
+    import oracle
+    if w.mode == V2:
+        tab_np = oracle.cpb_table(g["W1"].double().numpy(), g["b1"].double().numpy(), g["W2"].double().numpy(),
+                                  M=w.M, heads=w.heads)
+    else:
+        tab_np = g["table"].double().numpy()
+    rate, threads, nw = oracle_sample_rate(w, g, tab_np, seconds=seconds)
+    return {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "%d random windows of this workload (%d tokens), float64, OpenMP over windows" %
+                      (nw, nw * w.N)}
+
+
+def workload_config(w, world):
+    return {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": w.C, "heads": w.heads, "M": w.M,
+            "shift": w.shift, "mode": "V2" if w.mode == V2 else "V1", "dtype": w.dtype,
+            "parallelism": "dp%d (independent batches)" % world}
+
+
+def run_ours(args, w):
+    from vision_transformer_shifted_gb300 import binding as sw
+    rank, world, local, dist = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    sw.load()
+    pk = peaks()
+    with ClockSampler(dev.index) as clk:
+        res, (h, g, t, table, stream) = measure_forward(sw, w, dev, pk, args, args.steps, args.soak, rank, world,
+                                                        dist, args.path)
+    ms = res["ms_per_step"]
 
     # end to end through the host-buffer entry point (pinned buffers)
     x_host = g["x"].pin_memory()
@@ -315,38 +355,43 @@ def run_ours(args, w):
                                    out_host, stream)
         stream.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / k_e2e, dist)
+    sw.swin_wattn_destroy(h)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
-        if w.mode == V2:
-            tab_np = oracle.cpb_table(g["W1"].double().numpy(), g["b1"].double().numpy(), g["W2"].double().numpy(),
-                                      M=w.M, heads=w.heads)
-        else:
-            tab_np = g["table"].double().numpy()
-        rate, threads, nw = oracle_sample_rate(w, g, tab_np, seconds=args.cpu_seconds)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": "%d random windows of this workload (%d tokens), float64, OpenMP over windows" %
-                         (nw, nw * w.N)}
-    sw.swin_wattn_destroy(h)
+        cpu = oracle_baseline(w, g, args.cpu_seconds)
+
+    # every other workload, each in the same way but shorter (one line; not the headline)
+    configs = {}
+    if args.configs and world == 1:
+        for key in CONFIG_KEYS:
+            if key == w.key:
+                continue
+            wk = WORKLOADS[key]
+            with ClockSampler(dev.index) as clk_k:
+                rk, (hk, gk, *_rest) = measure_forward(sw, wk, dev, pk, args, args.config_steps, 0.3)
+            sw.swin_wattn_destroy(hk)
+            rk["config"] = workload_config(wk, 1)
+            rk["clocks"] = clk_k.summary()
+            if not args.no_cpu_baseline:
+                rk["cpu_baseline"] = oracle_baseline(wk, gk, args.config_cpu_seconds)
+            configs[key] = rk
     if rank != 0:
         return
-    line = {"metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+    cfg = workload_config(w, world)
+    cfg.update({"path": res["path"], "l2": res["l2"]})
+    line = {"metric": METRIC, "value": res["tokens_per_s"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": w.C, "heads": w.heads, "M": w.M,
-                       "shift": w.shift, "mode": "V2" if w.mode == V2 else "V1",
-                       "path": ("three kernels" if launches_per_step >= 3 else
-                                "fp32 block" if w.dtype == "fp32" else "fused"),
-                       "l2": "inputs rotated over %d buffer sets of %.0f MB (x + out), %.0f MB > 2x L2" %
-                             (nsets, io_bytes / 2 ** 20, nsets * io_bytes / 2 ** 20),
-                       "parallelism": "dp%d (independent batches)" % world},
-            "tflops": tflops, "block_roofline": block_roof, "roofline": roof, "kernels_us": kernels,
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": cfg,
+            "tflops": res["tflops"], "block_roofline": res["block_roofline"], "roofline": res["roofline"],
+            "kernels_us": res.get("kernels_us", {}),
             "cpu_baseline": cpu,
             "e2e": {"value": job_rate(w.tokens, world, e2e_s), "unit": "tokens/s",
                     "h2d_bytes_per_step": w.tokens * w.C * w.elem_bytes,
                     "d2h_bytes_per_step": w.tokens * w.C * w.elem_bytes},
-            "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary()}
+            "gpu_launches": res["launches_per_step"] * args.steps, "clocks": clk.summary()}
+    if configs:
+        line["configs"] = configs
     print(json.dumps(line), flush=True)
 
 
@@ -626,6 +671,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", type=int, default=1,
+                    help="1: also time every other workload (shorter), in a 'configs' key of the line")
+    ap.add_argument("--config-steps", type=int, default=30)
+    ap.add_argument("--config-cpu-seconds", type=float, default=3.0)
     ap.add_argument("--block", action="store_true",
                     help="time the whole Swin block (LayerNorm, attention, residuals, MLP) instead")
     ap.add_argument("--stage", type=int, default=0,

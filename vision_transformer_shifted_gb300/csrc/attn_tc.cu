@@ -35,20 +35,6 @@ namespace {
 
 constexpr float LOG2E = 1.4426950408889634f;
 
-// Optional phase trace of the large-window kernel (-DSWIN_PHASE_TRACE only):
-// thread 0 of CTA (blockIdx.x = 3, head 0) records clock64() per key tile.
-#ifdef SWIN_PHASE_TRACE
-__device__ long long g_flash_trace[8 * 16];
-#define FPHASE(kt, i)                                                                              \
-    do {                                                                                           \
-        if (blockIdx.x == 3 && blockIdx.y == 0 && tid == 0 && (kt) < 8) g_flash_trace[(kt) * 16 + (i)] = clock64(); \
-    } while (0)
-#else
-#define FPHASE(kt, i) \
-    do {              \
-    } while (0)
-#endif
-
 // Region id (row band * 3 + column band) of in-window token (ti, tj) of
 // window (wi, wj); 0 everywhere when shift == 0.
 __device__ __forceinline__ int token_region(const Geom &g, int wi, int wj, int ti, int tj)
@@ -185,9 +171,7 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
 #pragma unroll 1
     for (int kt = 0; kt < ktiles; ++kt) {
         const int b = kt & 1;
-        FPHASE(kt, 0);
         if (kt + 1 < ktiles) load_keys(kt + 1, b ^ 1);
-        FPHASE(kt, 1);
         // tile kt (and, for kt = 0, the q rows) have landed.  (No CTA barrier
         // here: the S MMA overwrites TMEM columns that every thread finished
         // reading before the previous tile's P store barrier, and a failed
@@ -200,10 +184,8 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
                 mma_bf16(tmem, desc_kmajor_sw64(sQ + 32 * k), desc_kmajor_sw64(sK + b * (128 * 64) + 32 * k), id, k);
             mma_commit(bar_s);
         }
-        FPHASE(kt, 2);
         if (!mbar_wait(bar_s, phase, st.wait_ns)) failed = true;
         tc_fence_after();
-        FPHASE(kt, 3);
 
         // logits of this thread's 64 keys (64*half .. +63 of the tile)
         float sv[64];
@@ -249,10 +231,8 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
             }
         }
         float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-        FPHASE(kt, 4);
         smax[half * 128 + row] = mt;
         if (__syncthreads_or(failed)) { failed = true; break; }
-        FPHASE(kt, 5);
         mt = fmaxf(smax[row], smax[128 + row]);
         const float m_new = fmaxf(m_run, mt);
         // no key seen yet: 0 as the reference (every p is then 0, and alpha = 0
@@ -278,11 +258,9 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
             tmem_st16(t_lane + 32 * half + 16, hi);
             tmem_wait_st();
         }
-        FPHASE(kt, 6);
         tc_fence_before();
         if (__syncthreads_or(failed)) { failed = true; break; }
         tc_fence_after();
-        FPHASE(kt, 7);
         // P.V in two halves over the tile's keys, issued by two threads (an MMA
         // costs its issuing thread the same whatever its size): keys 0..63 into
         // TMEM columns 128.., keys 64..127 into 160..; both commit to bar_pv
@@ -298,18 +276,15 @@ __global__ void __launch_bounds__(FL_THREADS, 2)
         if (!mbar_wait(bar_pv, phase, st.wait_ns)) failed = true;
         phase ^= 1;
         tc_fence_after();
-        FPHASE(kt, 8);
         float ot[16], ou[16];
         tmem_ld16(t_lane + 128 + 16 * half, ot);
         tmem_ld16(t_lane + 160 + 16 * half, ou);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 16; ++e) o[e] = fmaf(o[e], alpha, ot[e] + ou[e]);
-        FPHASE(kt, 9);
         // (no CTA barrier: the next tile's max exchange and P store barriers
         // order every reuse of TMEM and of the shared row maxima)
         tc_fence_before();
-        FPHASE(kt, 10);
     }
     spart[half * 128 + row] = l_run;
     __syncthreads();
@@ -398,13 +373,6 @@ cudaError_t make_tensor_map_sw64_3d(CUtensorMap *map, const void *ptr, int64_t r
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
-
-#ifdef SWIN_PHASE_TRACE
-extern "C" int swin_wattn_flash_trace(long long *host, int n)
-{
-    return (int)cudaMemcpyFromSymbol(host, g_flash_trace, sizeof(long long) * (size_t)n);
-}
-#endif
 
 cudaError_t launch_attention(const AttnArgs &a, DeviceStatus st, cudaStream_t stream)
 {

@@ -45,21 +45,6 @@ __device__ __forceinline__ int fb_round_fix(float x)
     return __float_as_int(fmaf(x, FIX_SCALE, 12582912.0f)) - 0x4B400000;
 }
 
-// Optional phase trace (-DSWIN_PHASE_TRACE only): threads 0 and 224 of CTA 5
-// record clock64() at seven points of each of the first 16 query-tile steps.
-#ifdef SWIN_PHASE_TRACE
-__device__ long long g_fbw_trace[2 * 16 * 8];
-#define BPHASE(step, i)                                                                            \
-    do {                                                                                           \
-        if (blockIdx.x == 5 && (tid == 0 || tid == 224) && (step) < 16)                            \
-            g_fbw_trace[((tid ? 1 : 0) * 16 + (step)) * 8 + (i)] = clock64();                      \
-    } while (0)
-#else
-#define BPHASE(step, i) \
-    do {                \
-    } while (0)
-#endif
-
 struct FbLayout {
     // byte offsets from the 512-aligned base
     static constexpr uint32_t K = 0, V = 8192, Q = 16384, DO = 24576; // [128 rows][64 B] tiles
@@ -291,7 +276,6 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
         for (int c = 0; c < 32; ++c) acc[c] = 0.f;
 
         for (int qt = 0; qt < KT; ++qt, ++step) {
-            BPHASE(step, 0);
             // the query tile's metadata (its previous readers passed the P
             // store barrier of the last tile)
             if (tid < 128) {
@@ -313,7 +297,6 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
             tc_fence_before();
             if (__syncthreads_or(!ok || failed)) { failed = true; break; }
             tc_fence_after();
-            BPHASE(step, 1);
             if (qt == 0) { ph_kv ^= 1; kv_pend = false; }
             ph_q ^= 1;
             q_pend = false;
@@ -331,7 +314,6 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
             if (mbar_wait(bar_s, ph_mma, st.wait_ns)) s_pend = false;
             else failed = true;     // (uniform at the next barrier)
             tc_fence_after();
-            BPHASE(step, 2);
 
             // ---- P^T and dS^T of key row r, queries 64*h2 .. +63, 8 at a time ----
             // (FULL: every pair of the pass is valid -- an unmasked window, a real
@@ -415,13 +397,11 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
                 else
                     pass(FbTag<false>(), hh);
             }
-            BPHASE(step, 3);
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             // B: P^T and dS^T panels complete
             if (__syncthreads_or(failed)) { failed = true; break; }
-            BPHASE(step, 4);
             if (lane == 0 && (warp == 0 || warp == 1 || warp == 4)) {
                 // TMEM columns: P^T over 0..31 and 64..95; dv (warp 0) into
                 // 32..63, dk (warp 1) into 96..127, dq (warp 4) into 160..191
@@ -447,7 +427,6 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
             else failed = true;     // (uniform at the next barrier)
             ph_mma ^= 1;
             tc_fence_after();
-            BPHASE(step, 5);
             // q and do are free (every MMA reading them has completed): the
             // next query tile's (or the next unit's first) loads and row data
             // come in under the epilogue
@@ -482,7 +461,6 @@ attn_flash_backward_kernel(const bf16 *table, const float *tau, int heads, int v
                         atomicAdd(dst + c, make_float4(dq[4 * c], dq[4 * c + 1], dq[4 * c + 2], dq[4 * c + 3]));
                 }
             }
-            BPHASE(step, 6);
         }
         if (failed) break;
         // the next unit's k and v (this unit's MMAs are done; V2 reads the k
@@ -632,13 +610,6 @@ unsigned grid_for(int64_t n)
 }
 
 } // namespace
-
-#ifdef SWIN_PHASE_TRACE
-extern "C" int swin_wattn_fbw_trace(long long *host, int n)
-{
-    return (int)cudaMemcpyFromSymbol(host, g_fbw_trace, sizeof(long long) * (size_t)n);
-}
-#endif
 
 bool attn_flash_backward_supported(int M, int C, int heads)
 {

@@ -71,32 +71,6 @@ constexpr int FTHREADS = NCOMPUTE + 3 * 32 + NPROD;   // 384
 constexpr int FBOUND_THREADS = 384;
 constexpr float FLOG2E = 1.4426950408889634f;
 
-// Optional phase trace (builds with -DSWIN_PHASE_TRACE only): threads 0 and
-// 128 of CTA 0 record clock64() at the phase boundaries of their first tiles.
-#ifdef SWIN_PHASE_TRACE
-constexpr int TRACE_TILES = 16, TRACE_POINTS = 32;
-__device__ long long g_phase_trace[4 * TRACE_TILES * TRACE_POINTS];
-__device__ long long g_cta_trace[1024 * 4];
-__device__ int g_trace_cta;   // the CTA whose phases are recorded
-// recorder 0: thread 0, 1: thread 128, 2: the MMA thread, 3: producer thread 0
-#define TRACE_AT(who, k, i)                                                                          \
-    do {                                                                                             \
-        if (blockIdx.x == (unsigned)g_trace_cta && (k) < TRACE_TILES)                                \
-            g_phase_trace[((who) * TRACE_TILES + (k)) * TRACE_POINTS + (i)] = clock64();             \
-    } while (0)
-#define PHASE(k, i)                                                                                  \
-    do {                                                                                             \
-        if (tid == CWARP0 * 32 || tid == (CWARP0 + 4) * 32) TRACE_AT(tid == CWARP0 * 32 ? 0 : 1, k, i); \
-    } while (0)
-#else
-#define TRACE_AT(who, k, i) \
-    do {                    \
-    } while (0)
-#define PHASE(k, i) \
-    do {            \
-    } while (0)
-#endif
-
 template <int M, int C>
 struct FusedCfg {
     static constexpr int HEADS = C / 32;
@@ -422,9 +396,6 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
         for (int j = 0; j < 3; ++j)
             if (blockIdx.x + (int64_t)j * gridDim.x < ntiles) next_meta(j);
     }
-#ifdef SWIN_PHASE_TRACE
-    if (tid == 0) g_cta_trace[blockIdx.x * 4 + 0] = (long long)global_timer_ns();
-#endif
     tc_fence_before();
     __syncthreads();   // weights, tables, metadata of tiles 0..2, barriers, TMEM address
     tc_fence_after();
@@ -493,12 +464,10 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
             if (producer_sync_or(failed)) { failed = true; break; }
             const bool load2 = tile + 2 * (int64_t)gridDim.x < ntiles;
             if (load2) load_x(b, (k + 2) % 3);   // (its cp.async copies are waited for below)
-            if (p == 0) TRACE_AT(3, k, 0);
             // this tile's output rows (in the v tiles) -> out through the window
             // reverse + roll(+s) map
             if (!wait_or_abort(R_STAGE, k & 1, st.wait_ns, abort_flag)) failed = true;
             if (producer_sync_or(failed)) { failed = true; break; }
-            if (p == 0) TRACE_AT(3, k, 1);
             const uint32_t ya = base + F::VA;
             if (tma_thread) {
 #pragma unroll
@@ -516,10 +485,8 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(R_VFREE);
             producer_sync_or(false);   // every read of slot ms is done
-            if (p == 0) TRACE_AT(3, k, 2);
             // slot ms takes the tile three ahead
             if (tile + 3 * (int64_t)gridDim.x < ntiles) next_meta(ms);
-            if (p == 0) TRACE_AT(3, k, 3);
             if (load2) x_landed(b);
         }
         cp_async_wait<0>();
@@ -570,7 +537,6 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
                     tc_fence_after();
                     issue_s(1);
                 }
-                if (w == 0) TRACE_AT(2, k, 0);
 #pragma unroll 1
                 for (int hd = 0; hd < HEADS; ++hd) {
                     const int r = hd & 1;
@@ -578,12 +544,9 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
                     ph_rp ^= 1u << r;
                     if (hd == 0 && !(ok = wait_or_abort(R_V, k & 1, st.wait_ns, abort_flag))) break;
                     tc_fence_after();
-                    if (w == 0) TRACE_AT(2, k, 14 + hd);
                     issue_pv(hd);
-                    if (w == 0) TRACE_AT(2, k, 4 + hd);
                     if (!(ok = wait_or_abort(B_PVW(w), ph_pvw, st.wait_ns, abort_flag))) break;
                     ph_pvw ^= 1;
-                    if (w == 0) TRACE_AT(2, k, 7 + hd);
                     if (hd + 2 < HEADS) issue_s(hd + 2);
                 }
                 if (!ok) break;
@@ -626,7 +589,6 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
                     if (!(ok = wait_or_abort(R_X(buf ^ 1), ((k + 1) >> 1) & 1, st.wait_ns, abort_flag))) break;
                     tc_fence_after();
                     issue_qkv(buf ^ 1);
-                    TRACE_AT(2, k, 2);
                 }
                 // the projection once o is in the v tiles
                 if (!(ok = wait_or_abort(R_O, k & 1, st.wait_ns, abort_flag))) break;
@@ -639,7 +601,6 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
                         mma_bf16(tmem + F::T_O, desc_kmajor_sw64(oa + kb * (128 * 64) + 32 * ks),
                                  desc_kmajor_sw64(base + F::WP + kb * (C * 64) + 32 * ks), id_y, (kb | ks) != 0);
                 mma_commit(B_Y);
-                TRACE_AT(2, k, 1);
             }
         }
     } else {
@@ -656,14 +617,12 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
         int k = 0;
 #pragma unroll 1
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
-            PHASE(k, 0);
             // this tile's QKV is done.  (Its metadata -- masks -- was written
             // before the CTA-wide barrier for tiles 0..2, and three tiles ahead
             // before the producer's R_VFREE arrival, which is waited below
             // before the masks are read, for the others.)
             if (!wait_or_abort(B_QKV, k & 1, st.wait_ns, abort_flag)) failed = true;
             tc_fence_after();
-            PHASE(k, 1);
 
             // q (half 0) or k (half 1) of every head to shared memory
 #pragma unroll 1
@@ -720,7 +679,6 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
             }
             fence_proxy_async_smem();
             warp_arrive(R_V, lane);
-            PHASE(k, 2);
 
             const int ms = k % 3;
             const uint32_t allow_lo = sallow[(ms * 2 + 0) * 128 + row];
@@ -734,7 +692,6 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
                 if (!wait_or_abort(B_S(r), (ph_s >> r) & 1u, st.wait_ns, abort_flag)) failed = true;
                 ph_s ^= 1u << r;
                 tc_fence_after();
-                PHASE(k, 3 + 3 * hd);
 
                 // ---- softmax over this row's own window, keys 32*half .. +31 -------
                 float s[32];
@@ -775,7 +732,6 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
                 // stays local to the pair until the compute-wide barrier after
                 // the heads (every wait returns at once after an abort)
                 if (pair_sync_or(quarter, failed)) failed = true;
-                PHASE(k, 4 + 3 * hd);
                 mx = row_ok ? fmaxf(mxb[row], mxb[128 + row]) : 0.f;   // padding rows: all -inf -> p = 0
                 float sum = 0.f;
                 uint32_t pk[16];
@@ -791,7 +747,6 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
                 tmem_st16(t_lane + t_s(r) + 16 * half, pk);
                 tmem_wait_st();
                 warp_arrive(R_P(r), lane);
-                PHASE(k, 5 + 3 * hd);
             }
             // (a failure above is not uniform across threads yet: the barriers
             // below make every compute thread leave together; waits return at
@@ -814,20 +769,16 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
             if (!wait_or_abort(B_O1, k & 1, st.wait_ns, abort_flag)) failed = true;
             if (compute_sync_or(failed)) { failed = true; break; }   // also orders spart
             tc_fence_after();
-            PHASE(k, 20);
 #pragma unroll 1
             for (int hd = 0; hd < HEADS - 1; ++hd) drain_o(hd);
             if (!wait_or_abort(B_O, k & 1, st.wait_ns, abort_flag)) failed = true;
             if (compute_sync_or(failed)) { failed = true; break; }
             tc_fence_after();
-            PHASE(k, 24);
             drain_o(HEADS - 1);
             fence_proxy_async_smem();
             warp_arrive(R_O, lane);
-            PHASE(k, 21);
             if (!wait_or_abort(B_Y, k & 1, st.wait_ns, abort_flag)) failed = true;
             tc_fence_after();
-            PHASE(k, 22);
 
             // ---- y + bproj -> bf16 rows in the v tiles, token (ti, tj) of a window at
             // row M*ti + tj of its half (one dense box per window for the TMA
@@ -859,18 +810,9 @@ __global__ void __launch_bounds__(FBOUND_THREADS, 1)
             }
             fence_proxy_async_smem();   // the TMA stores read these rows
             warp_arrive(R_STAGE, lane);
-            PHASE(k, 23);
         }
         if (failed) *abort_flag = 1;
     }
-#ifdef SWIN_PHASE_TRACE
-    if (tid == 0) {
-        unsigned smid;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        g_cta_trace[blockIdx.x * 4 + 1] = (long long)global_timer_ns();
-        g_cta_trace[blockIdx.x * 4 + 3] = smid;
-    }
-#endif
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && *abort_flag) atomicOr(st.err, ERR_TIMEOUT);
@@ -930,21 +872,6 @@ cudaError_t launch_fused_t(const FusedArgs &a, DeviceStatus st, cudaStream_t str
 }
 
 } // namespace
-
-#ifdef SWIN_PHASE_TRACE
-extern "C" int swin_wattn_phase_trace(long long *host, int n)
-{
-    return (int)cudaMemcpyFromSymbol(host, g_phase_trace, sizeof(long long) * (size_t)n);
-}
-extern "C" int swin_wattn_set_trace_cta(int cta)
-{
-    return (int)cudaMemcpyToSymbol(g_trace_cta, &cta, sizeof(int));
-}
-extern "C" int swin_wattn_cta_trace(long long *host, int n)
-{
-    return (int)cudaMemcpyFromSymbol(host, g_cta_trace, sizeof(long long) * (size_t)n);
-}
-#endif
 
 bool fused_supported(int M, int C, int heads)
 {
