@@ -38,10 +38,10 @@
 // threads one tile row, so a row's softmax needs no exchange between threads.
 // Warp roles:
 //   warp 0      producer: x gathers into X(g) (TMA; cp.async for wrapping
-//               windows) and the output stores from the group's staged rows
+//               windows)
 //   warp 1      tcgen05 issuer of every QKV MMA; owns TMEM
 //   warps 2, 3  tcgen05 issuers of group 0's / group 1's S, P.V and
-//               projection MMAs
+//               projection MMAs; they also issue the group's output stores
 //   warps 4..7, 8..11  compute groups 0 and 1
 // TMEM (512 columns): [0, 2C) q|k of the tile whose QKV ran last (the groups
 // take turns), then 128 columns per group: v of its tile; then its two
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     };
 
     if (warp == PWARP) {
-        // ===================== producer warp =====================
+        // ===================== producer warp: x gathers =====================
         const bool tma_thread = lane == 0;
         // x rows of tile `tile` into X(grp): TMA boxes (the TMA thread's arrival
         // on BR_X carries their bytes) and, for wrapping windows, cp.async
@@ -437,47 +437,16 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             if (lane == 0) mbar_arrive(BAR(grp, BR_X));
         };
         bool ok = true;
-        int p_load = perm0, p_store = perm0;
-        for (int j = 0; j < 2 && j < my_tiles; ++j) {
-            if (load_x(j, p_load)) x_landed(j);
-            p_load = perm_next(p_load);
-        }
+        int p_load = perm0;
 #pragma unroll 1
         for (int j = 0; j < my_tiles; ++j) {
             const int grp = j & 1, kg = j >> 1;
-            // X(grp) takes tile j + 2 once the group's S MMAs of tile j have read q
-            bool pending = false;
-            if (j + 2 < my_tiles) {
-                if (!(ok = warp_wait(BAR(grp, BR_XFREE), kg & 1, st.wait_ns, abort_flag))) break;
-                pending = load_x(grp, p_load);
-                p_load = perm_next(p_load);
-            }
-            // tile j's output rows (in V(grp)) -> out through the window reverse +
-            // roll(+s) map; V(grp) may take the group's next v once the stores
-            // have read it
-            if (!(ok = warp_wait(BAR(grp, BR_STAGE), kg & 1, st.wait_ns, abort_flag))) break;
-            if (tma_thread) {
-                const uint32_t ya = V(grp);
-#pragma unroll
-                for (int sl = 0; sl < 2; ++sl) {
-                    const WinInfo w = window_info(g, p_store, sl);
-                    if (w.kind != 1) continue;
-#pragma unroll
-                    for (int kb = 0; kb < KB; ++kb)
-                        tma_store_3d(&tmap_out, kb * 32, w.col0, w.img_row0, ya + kb * HT + sl * (64 * 64));
-                }
-                bulk_commit();
-            }
-            if (pending) x_landed(grp);
-            if (tma_thread) {
-                bulk_wait_read();
-                mbar_arrive(BAR(grp, BR_VFREE));
-            }
-            __syncwarp();
-            p_store = perm_next(p_store);
+            // X(grp) takes tile j once the group's S MMAs of tile j - 2 have read q
+            if (j >= 2 && !(ok = warp_wait(BAR(grp, BR_XFREE), (kg - 1) & 1, st.wait_ns, abort_flag))) break;
+            if (load_x(grp, p_load)) x_landed(grp);
+            p_load = perm_next(p_load);
         }
         cp_async_wait<0>();
-        if (tma_thread) bulk_wait_all();
         if (!ok) *abort_flag = 1;
     } else if (warp == QWARP) {
         // ============ QKV issuer: the CTA's tiles in order ============
@@ -555,6 +524,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             uint32_t ph_p = 0;
             uint32_t od_n[2] = {0u, 0u};
             bool ok = true;
+            int p_tile = grp ? perm_next(perm0) : perm0;
 #pragma unroll 1
             for (int j = grp; ok && j < my_tiles; j += 2) {
                 const int kg = j >> 1;
@@ -598,7 +568,24 @@ __global__ void __launch_bounds__(FTHREADS, 1)
                         mma_bf16(t_r, desc_add(doa, kb * HT + 32 * ks), desc_add(d_wp, kb * (C * 64) + 32 * ks), id_y,
                                  (kb | ks) != 0);
                 mma_commit(BAR(grp, BR_Y));
+                // tile j's output rows (staged in V(grp) by the compute warps) -> out
+                // through the window reverse + roll(+s) map; V(grp) may take the
+                // group's next v once the stores have read them
+                if (!(ok = wait_or_abort(BAR(grp, BR_STAGE), kg & 1, st.wait_ns, abort_flag))) break;
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    const WinInfo w = window_info(g, p_tile, sl);
+                    if (w.kind != 1) continue;
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_store_3d(&tmap_out, kb * 32, w.col0, w.img_row0, V(grp) + kb * HT + sl * (64 * 64));
+                }
+                bulk_commit();
+                bulk_wait_read();
+                mbar_arrive(BAR(grp, BR_VFREE));
+                p_tile = perm_next(perm_next(p_tile));
             }
+            bulk_wait_all();
             if (!ok) *abort_flag = 1;
         }
     } else {
