@@ -380,6 +380,8 @@ cudaError_t launch_attention(const AttnArgs &a, DeviceStatus st, cudaStream_t st
     if (g.C != a.heads * 32) return cudaErrorInvalidValue;
     if (g.N <= 64) {
         return launch_attn_forward_tc(a.qkv, a.table, a.tau, a.heads, a.mode == 1 ? 1 : 0, g, a.attn, st, stream);
+    } else if (attn_window_supported(g.M, a.heads)) {
+        return launch_attn_window(a, st, stream);
     } else {
         const size_t smem = FlashSmem::bytes(g.M);
         cudaError_t e = cudaFuncSetAttribute(attn_flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

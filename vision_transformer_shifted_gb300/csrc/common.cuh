@@ -172,6 +172,10 @@ struct AttnArgs {
 };
 
 cudaError_t launch_attention(const AttnArgs &a, DeviceStatus st, cudaStream_t stream);
+// The persistent large-window kernel (attn_window.cu): M = 12, 16, 20, 24 and
+// every head's bias table within shared memory.
+bool attn_window_supported(int M, int heads);
+cudaError_t launch_attn_window(const AttnArgs &a, DeviceStatus st, cudaStream_t stream);
 
 struct Fp32Args {
     const float *x, *Wqkv, *bqkv, *table, *tau, *Wproj, *bproj;
