@@ -294,7 +294,7 @@ def test_block_forward_small(key, B, H, W):
     table = oracle_table(w, g)
     got = _run_block(w, g, table)
     ref, _ = ob.block(to_f64(g["x"]), _oracle_params(g, table), heads=w.heads, M=w.M, shift=w.shift, mode=w.mode)
-    _block_compare(to_f64(got), ref)
+    _block_compare(to_f64(got), ref, w.mode)
 
 
 @pytest.mark.gpu
