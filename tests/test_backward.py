@@ -233,7 +233,9 @@ def test_backward_parity_small(key, kw):
     w = _workload(key, **kw)
     got, ref, launches = _run_backward(w)
     _check_all(got, ref)
-    assert launches == 10
+    # two transposes, the qkv and do GEMMs, the attention backward, dx, two column
+    # sums, and the two weight-gradient GEMMs (partial blocks + their sum, each)
+    assert launches == 12
 
 
 @pytest.mark.gpu
@@ -251,7 +253,9 @@ def test_backward_parity_large_windows(key, kw):
         pytest.skip("no GPU")
     got, ref, launches = _run_backward(_workload(key, **kw))
     _check_all(got, ref)
-    assert launches == 13
+    # (the large-window forward, D, the key-tile kernel and the dq conversion
+    # replace the one attention backward launch)
+    assert launches == 15
 
 
 @pytest.mark.gpu

@@ -59,7 +59,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = LIB + ".%d.tmp" % os.getpid()
-    res = subprocess.run([cc, *ARCH, "-shared", "-cudart", "shared", *objs, "-lcublas", "-o", tmp], capture_output=True, text=True)
+    res = subprocess.run([cc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", tmp], capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("link failed:\n" + res.stdout + res.stderr)
     os.replace(tmp, LIB)

@@ -3,8 +3,6 @@
 #include <cstring>
 #include <new>
 
-#include <cublas_v2.h>
-
 #include "swin_wattn.h"
 #include "swin_wattn_backward.h"
 #include "swin_wattn_test.h"
@@ -30,7 +28,6 @@ struct swin_wattn_s {
     cudaError_t last_cuda_error;
     void *bws;         // backward workspace (see swin_wattn_backward)
     size_t bws_bytes;
-    cublasHandle_t blas;
     int bw_launches;
     // chunked host-buffer forward: copy-in, compute and copy-out streams and
     // their events (created on first use)
@@ -172,17 +169,6 @@ bool overlaps(const void *a, const void *b, size_t bytes)
     return bytes && pa < pb + bytes && pb < pa + bytes;
 }
 
-// D [n_out, n_in] (row-major fp32) = sum over T rows of G[t, :]^T X[t, :]
-// for bf16 row-major G [T, n_out] and X [T, n_in]: in cuBLAS's column-major
-// view D^T = X^T-view . G-view^T with k = T.
-cublasStatus_t weight_grad(cublasHandle_t blas, const bf16 *G, int n_out, const bf16 *X, int n_in, int64_t T,
-                           float *D)
-{
-    const float one = 1.f, zero = 0.f;
-    return cublasGemmEx(blas, CUBLAS_OP_N, CUBLAS_OP_T, n_in, n_out, (int)T, &one, X, CUDA_R_16BF, n_in, G,
-                        CUDA_R_16BF, n_out, &zero, D, CUDA_R_32F, n_in, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-}
-
 // The chunked host-buffer forward on `s` (the body of swin_wattn_forward_host):
 // up to h->host_chunks chunks of whole images; copy-in, compute and copy-out of different
 // chunks overlap on the handle's three streams, forked from and joined back
@@ -264,7 +250,6 @@ int swin_wattn_destroy(swin_wattn_t h)
     ws_free(&h->stage_x, &have);
     ws_free(&h->stage_out, &have);
     ws_free(&h->bws, &h->bws_bytes);
-    if (h->blas) cublasDestroy(h->blas);
     if (h->hs_ready) {
         for (cudaStream_t st : h->hs) cudaStreamDestroy(st);
         for (int c = 0; c < HOST_CHUNKS; ++c) {
@@ -497,10 +482,10 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
         if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, n * sizeof(float), s);
     };
     zero(dtable, (size_t)L * L * h->heads);
-    zero(dbqkv, (size_t)3 * C);
-    zero(dbproj, (size_t)C);
     if (dlogit_scale) zero(dlogit_scale, (size_t)h->heads);
     if (B == 0) {
+        zero(dbqkv, (size_t)3 * C);
+        zero(dbproj, (size_t)C);
         zero(dWqkv, (size_t)3 * C * C);
         zero(dWproj, (size_t)C * C);
         return cuda_status(e);
@@ -513,18 +498,19 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     const size_t tc = (size_t)g.T * C;
     const size_t norm_bytes = v2 ? (size_t)g.T * 2 * h->heads * 4 : 0;
     const size_t flash_bytes = flash ? (size_t)g.T * 2 * h->heads * 4 + tc * 4 : 0;
-    rc = ws_ensure(&h->bws, &h->bws_bytes, (8 * tc + 4 * (size_t)C * C) * 2 + norm_bytes + flash_bytes);
+    // (and the split-K partial sums of the weight gradients, fp32)
+    size_t wg_bytes = wgrad_workspace_bytes(3 * C, C, g.T);
+    if (wgrad_workspace_bytes(C, C, g.T) > wg_bytes) wg_bytes = wgrad_workspace_bytes(C, C, g.T);
+    const size_t base_bytes = (8 * tc + 4 * (size_t)C * C) * 2 + norm_bytes + flash_bytes;
+    rc = ws_ensure(&h->bws, &h->bws_bytes, base_bytes + wg_bytes);
     if (rc) return rc;
-    if (!h->blas) {
-        if (cublasCreate(&h->blas) != CUBLAS_STATUS_SUCCESS) { h->blas = nullptr; return SWIN_WATTN_ECUDA; }
-    }
-    if (cublasSetStream(h->blas, s) != CUBLAS_STATUS_SUCCESS) return SWIN_WATTN_ECUDA;
     bf16 *attn = (bf16 *)h->bws, *dO = attn + tc, *qkv = dO + tc, *dqkv = qkv + 3 * tc;
     bf16 *WpT = dqkv + 3 * tc, *WqkvT = WpT + (size_t)C * C;
     float *fws = reinterpret_cast<float *>(WqkvT + 3 * (size_t)C * C);
     float *norms = v2 ? fws : nullptr;
     if (v2) fws += (size_t)g.T * 2 * h->heads;
     float *lse = fws, *Drow = lse + (size_t)g.T * h->heads, *dq_acc = Drow + (size_t)g.T * h->heads;
+    float *wg_ws = reinterpret_cast<float *>((char *)h->bws + base_bytes);
     int launches = 0;
     auto step = [&](cudaError_t r) {
         if (e == cudaSuccess) { e = r; ++launches; }
@@ -561,14 +547,14 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     k4.A = dqkv; k4.lda = 3 * C; k4.Bw = WqkvT; k4.D = (bf16 *)dx; k4.ldd = C; k4.rows = g.T; k4.N = C;
     k4.K = 3 * C; k4.g = g;
     step(launch_gemm(k4, LOAD_PLAIN, STORE_PLAIN, dstatus(h), s));
-    step(launch_colsum((const bf16 *)dy, g.T, C, dbproj, s));
-    step(launch_colsum(dqkv, g.T, 3 * C, dbqkv, s));
+    // dWproj = dy^T attn and dbproj, dWqkv = dqkv^T x and dbqkv: split-K tcgen05
+    // GEMMs over the tokens (three launches each: partial blocks, then their
+    // sum in two levels)
+    step(launch_wgrad((const bf16 *)dy, C, attn, C, g.T, dWproj, dbproj, wg_ws, dstatus(h), s));
+    step(launch_wgrad(dqkv, 3 * C, (const bf16 *)x, C, g.T, dWqkv, dbqkv, wg_ws, dstatus(h), s));
+    launches += 4;
     if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
-    if (weight_grad(h->blas, (const bf16 *)dy, C, attn, C, g.T, dWproj) != CUBLAS_STATUS_SUCCESS)
-        return SWIN_WATTN_ECUDA;
-    if (weight_grad(h->blas, dqkv, 3 * C, (const bf16 *)x, C, g.T, dWqkv) != CUBLAS_STATUS_SUCCESS)
-        return SWIN_WATTN_ECUDA;
-    h->bw_launches = launches + 2;
+    h->bw_launches = launches;
     return ws_check(h->bws, s);
 }
 

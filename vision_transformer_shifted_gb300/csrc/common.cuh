@@ -223,6 +223,14 @@ cudaError_t launch_cpb_backward(const float *W1, const float *b1, const float *W
 cudaError_t launch_watchdog(DeviceStatus st, cudaStream_t stream);
 
 // ---- backward (V1) ----------------------------------------------------------
+// dW [n_out, n_in] = G^T X and db [n_out] = the column sums of G (fp32,
+// overwritten; db may be null) for bf16 row-major G [T, n_out] and X [T,
+// n_in] (n_in a multiple of 32, n_out of 8): split-K tcgen05 GEMM into
+// `workspace` (wgrad_workspace_bytes), then a fixed-order sum; three
+// launches.
+size_t wgrad_workspace_bytes(int n_out, int n_in, int64_t T);
+cudaError_t launch_wgrad(const bf16 *G, int n_out, const bf16 *X, int n_in, int64_t T, float *dW, float *db,
+                         float *workspace, DeviceStatus st, cudaStream_t stream);
 // out [cols, rows] = in [rows, cols]^T.
 cudaError_t launch_transpose(const bf16 *in, bf16 *out, int rows, int cols, cudaStream_t stream);
 // out[n] += sum over rows of in[row, n] (fp32; N a multiple of 8, <= 2048).
