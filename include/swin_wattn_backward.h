@@ -21,9 +21,10 @@
  * runs: the QKV GEMM and the do GEMM, each gathering its rows into window
  * order in its loads; the attention backward, which recomputes S and P,
  * yields o, dq, dk, dv (written back in token order) and the table
- * gradient; the dx GEMM; two weight-gradient GEMMs (cuBLAS: plain long-K
- * reductions over all tokens, which do not depend on the token order) and
- * two column sums.
+ * gradient; the dx GEMM; two weight-gradient GEMMs (split-K over all
+ * tokens, which do not depend on the token order; each also yields its
+ * bias gradient, the column sums of dy and dqkv, and adds its per-CTA
+ * partial sums in a fixed order).
  *
  * Windows of more than 64 tokens (up to 24 x 24): the large-window forward
  * kernel runs first and keeps, besides o, the log2 of each row's softmax
@@ -66,8 +67,8 @@ extern "C" {
  * fp32 handle, windows of more than 24 x 24 tokens, C != 32 heads, or
  * B*H*W >= 2^31; ENOMEM if the workspace (8 * B*H*W*C bf16 elements plus
  * 4C^2, plus 2 B*H*W*heads fp32 in V2, plus (2 heads + C) B*H*W fp32 for
- * windows of more than 64 tokens) cannot be allocated; ECUDA for launch or
- * cuBLAS failures.
+ * windows of more than 64 tokens, plus the weight gradients' partial sums)
+ * cannot be allocated; ECUDA for launch failures.
  * B = 0 zeroes the parameter gradients and returns. */
 int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
                         const void *bias_table, const float *logit_scale, const void *Wproj, const void *bproj,
@@ -87,8 +88,7 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
 int swin_wattn_cpb_backward(swin_wattn_t h, const float *W1, const float *b1, const float *W2, int hidden,
                             const float *dtable, float *dW1, float *db1, float *dW2, swin_stream_t stream);
 
-/* Number of kernels (own and cuBLAS calls counted as one each) the last
- * successful swin_wattn_backward enqueued. */
+/* Number of kernels the last successful swin_wattn_backward enqueued. */
 int swin_wattn_backward_launches(swin_wattn_t h);
 
 #ifdef __cplusplus
