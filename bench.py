@@ -547,6 +547,9 @@ def run_stage(args, w, depth, ratio=4):
     gam = (1 + 0.1 * torch.randn(4 * w.C, generator=gm)).bfloat16().to(dev)
     bet = (0.1 * torch.randn(4 * w.C, generator=gm)).bfloat16().to(dev)
     Wm = (torch.randn(2 * w.C, 4 * w.C, generator=gm) * (4 * w.C) ** -0.5).bfloat16().to(dev)
+    # V2's extra LayerNorm after every `extra_norm`-th block (0: none)
+    en_gam = (1 + 0.1 * torch.randn(w.C, generator=gm)).bfloat16().to(dev)
+    en_bet = (0.1 * torch.randn(w.C, generator=gm)).bfloat16().to(dev)
     hm = sw.swin_merge_create(w.C)
     x0 = blocks[0][2]
     bufs = [torch.empty_like(x0) for _ in range(2)]
@@ -558,6 +561,8 @@ def run_stage(args, w, depth, ratio=4):
         for i, (h, params, _x) in enumerate(blocks):
             sw.swin_block_forward(h, cur, params, bufs[i % 2], stream)
             cur = bufs[i % 2]
+            if args.extra_norm and (i + 1) % args.extra_norm == 0:
+                sw.swin_stage_norm(cur, en_gam, en_bet, cur, stream)
         sw.swin_merge_forward(hm, cur, gam, bet, Wm, out, stream)
 
     for i in range(args.warmup):
@@ -583,7 +588,8 @@ def run_stage(args, w, depth, ratio=4):
             "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": w.C, "heads": w.heads, "M": w.M,
-                       "depth": depth, "mode": "V1 pre-norm" if w.mode == V1 else "V2 residual post-norm",
+                       "depth": depth, "extra_norm_every": args.extra_norm,
+                       "mode": "V1 pre-norm" if w.mode == V1 else "V2 residual post-norm",
                        "mlp_ratio": ratio, "l2": "not flushed: one input set (the stage's own intermediates, "
                        "%.0f MB per block, exceed L2)" % (w.tokens * w.C * (3 + ratio) * 2 / 1e6)},
             "clocks": clk.summary()}
@@ -679,6 +685,8 @@ def main():
                     help="time the whole Swin block (LayerNorm, attention, residuals, MLP) instead")
     ap.add_argument("--stage", type=int, default=0,
                     help="time a whole stage of this many blocks (alternating shifts) plus the merging step instead")
+    ap.add_argument("--extra-norm", type=int, default=0,
+                    help="with --stage: V2's extra LayerNorm on the main branch after every this many blocks")
     ap.add_argument("--backward", action="store_true",
                     help="time the gradients of the attention block (with recompute) instead")
     args = ap.parse_args()

@@ -15,7 +15,7 @@
  * variance and eps = 1e-5, per-channel gain and shift; MLP(u) =
  * GELU(u W1^T + b1) W2^T + b2 with hidden width mlp_ratio * C and the exact
  * GELU u * Phi(u).  The extra LayerNorm that V2 inserts every six blocks of
- * its largest models belongs to the stage, not to a block.
+ * its largest models belongs to the stage, not to a block: swin_stage_norm.
  *
  * bf16 tensors, fp32 arithmetic inside each step; the residual stream z, the
  * LayerNorm outputs and the MLP hidden activations are rounded to bf16
@@ -83,6 +83,19 @@ int swin_block_destroy(swin_block_t h);
  * of 8 and at most 2048. */
 int swin_block_test_layernorm(const void *a, const void *b, const void *gamma, const void *beta, void *out_sum,
                               void *out_ln, int rows, int C, int flags, swin_stream_t stream);
+
+/* The extra LayerNorm of V2's largest models ("Swin Transformer V2"
+ * (neura.market), How It Works: a layer normalisation inserted every six
+ * blocks), applied to the main branch between blocks of a stage: per token of
+ * C channels, out = LN(x) (biased variance, eps = 1e-5, gain gamma, shift
+ * beta).  Reading (the page gives no more): it follows blocks 6, 12, ... of
+ * a stage, before the merging step, with a gain and shift of its own.
+ * x, out [rows, C] bf16 (out may be x itself, not a partial overlap); gamma,
+ * beta [C] bf16; C a multiple of 8, at most 2048.  EINVAL for bad sizes,
+ * NULL, misaligned or partly overlapping pointers; ECUDA for a launch
+ * failure.  rows = 0 is a no-op. */
+int swin_stage_norm(const void *x, int rows, int C, const void *gamma, const void *beta, void *out,
+                    swin_stream_t stream);
 
 /* ---- merging step between stages ----------------------------------------------
  * Between stages of the hierarchy ("Boosting Swin Transformer Speed",

@@ -116,13 +116,24 @@ def patch_merge(x, gamma, beta, Wm):
     return layer_norm(merge_concat(x), gamma, beta) @ np.asarray(Wm, np.float64).T
 
 
-def stage(x, blocks, *, heads, M, mode, merge=None):
+def stage(x, blocks, *, heads, M, mode, merge=None, extra_norm=None):
     """``len(blocks)`` blocks (parameter dicts as ``block`` takes them) with
     shifts 0, M/2, 0, M/2, ...; then ``patch_merge`` with merge = (gamma, beta,
-    Wm) if given."""
+    Wm) if given.
+
+    extra_norm = (every, [(gamma, beta), ...]): the extra LayerNorm of V2's
+    largest models ("Swin Transformer V2" (neura.market), How It Works: a
+    layer normalisation inserted every six blocks).  Reading: applied to the
+    main branch after blocks every, 2 every, ... (the k-th time with the k-th
+    gain and shift), before the merging step."""
     y = np.asarray(x, dtype=np.float64)
+    k = 0
     for i, p in enumerate(blocks):
         y, _ = block(y, p, heads=heads, M=M, shift=0 if i % 2 == 0 else M // 2, mode=mode)
+        if extra_norm is not None and (i + 1) % extra_norm[0] == 0:
+            g, b = extra_norm[1][k]
+            y = layer_norm(y, g, b)
+            k += 1
     if merge is not None:
         y = patch_merge(y, *merge)
     return y

@@ -165,6 +165,34 @@ def test_stage_alternates_shifts_starting_unshifted():
     assert not np.allclose(y, y_wrong, atol=1e-6)
 
 
+def test_stage_extra_norm_every_six_blocks():
+    """V2's extra LayerNorm: after block 6 of a stage, not before and not when
+    the stage has fewer blocks; with gain 1 and shift 0 each output token then
+    has mean 0 and variance var / (var + eps) exactly (a LayerNorm's output),
+    which the stage without it does not."""
+    B, H, W, C, heads, M = 1, 8, 8, 32, 1, 4
+    x = RNG.normal(size=(B, H, W, C))
+    blocks = [_tiny_params(C, heads, M, V2, zero_attention=False) for _ in range(7)]
+    one, zero = np.ones(C), np.zeros(C)
+    gam, bet = 1 + 0.1 * RNG.normal(size=C), 0.1 * RNG.normal(size=C)
+    plain6 = ob.stage(x, blocks[:6], heads=heads, M=M, mode=V2)
+    # placement: LN of the main branch after block 6
+    y6 = ob.stage(x, blocks[:6], heads=heads, M=M, mode=V2, extra_norm=(6, [(gam, bet)]))
+    assert np.allclose(y6, ob.layer_norm(plain6, gam, bet), atol=1e-12)
+    # five blocks: nothing inserted
+    y5 = ob.stage(x, blocks[:5], heads=heads, M=M, mode=V2, extra_norm=(6, [(gam, bet)]))
+    assert np.array_equal(y5, ob.stage(x, blocks[:5], heads=heads, M=M, mode=V2))
+    # block 7 runs on the normalised branch
+    y7 = ob.stage(x, blocks, heads=heads, M=M, mode=V2, extra_norm=(6, [(gam, bet)]))
+    assert np.allclose(y7, ob.block(y6, blocks[6], heads=heads, M=M, shift=0, mode=V2)[0], atol=1e-12)
+    # the closed form of a LayerNorm's output rows
+    yn = ob.stage(x, blocks[:6], heads=heads, M=M, mode=V2, extra_norm=(6, [(one, zero)]))
+    var = plain6.var(axis=-1)
+    assert np.allclose(yn.mean(axis=-1), 0.0, atol=1e-12)
+    assert np.allclose(yn.var(axis=-1), var / (var + ob.LN_EPS), atol=1e-12)
+    assert not np.allclose(plain6.mean(axis=-1), 0.0, atol=1e-3)
+
+
 # ---- C ABI argument checks (CPU) ---------------------------------------------------
 
 
@@ -190,6 +218,17 @@ def test_merge_rejects_bad_arguments():
     assert lib.swin_merge_create(None, 96) == sw.EINVAL
     assert lib.swin_merge_forward(None, None, 1, 8, 8, None, None, None, None, None) == sw.EINVAL
     assert lib.swin_merge_destroy(None) == sw.OK
+
+
+def test_stage_norm_rejects_bad_arguments():
+    lib = sw.load()
+    p16, p32 = ctypes.c_void_p(16), ctypes.c_void_p(32)
+    assert lib.swin_stage_norm(p16, 4, 100, p16, p16, p16, None) == sw.EINVAL   # C % 8
+    assert lib.swin_stage_norm(p16, -1, 96, p16, p16, p16, None) == sw.EINVAL   # rows
+    assert lib.swin_stage_norm(None, 4, 96, p16, p16, p16, None) == sw.EINVAL
+    assert lib.swin_stage_norm(ctypes.c_void_p(18), 4, 96, p16, p16, p32, None) == sw.EINVAL   # misaligned
+    assert lib.swin_stage_norm(p16, 4, 96, p16, p16, p32, None) == sw.EINVAL   # partial overlap
+    assert lib.swin_stage_norm(p16, 0, 96, p16, p16, p16, None) == sw.OK
 
 
 def test_block_layernorm_hook_rejects_bad_arguments():
@@ -371,3 +410,49 @@ def test_stage_forward(mode):
     ref = ob.stage(to_f64(x), p_blocks, heads=w0.heads, M=w0.M, mode=w0.mode,
                    merge=(to_f64(gam), to_f64(bet), to_f64(Wm)))
     _block_compare(to_f64(out.cpu()), ref)
+
+
+@pytest.mark.gpu
+def test_stage_with_extra_norm_forward():
+    """A V2 stage of seven blocks with the extra LayerNorm after the sixth
+    (swin_stage_norm in place on the main branch) and the merging step,
+    against the oracle's stage."""
+    key = "swinv2_t_s1"
+    M = WORKLOADS[key].M
+    w0 = WORKLOADS[key].with_(B=1, H=2 * M, W=2 * M)
+    p_blocks, dev_blocks = [], []
+    for i in range(7):
+        wi = w0.with_(shift=0 if i % 2 == 0 else M // 2, seed=w0.seed + 31 * i)
+        g = generate_block(wi)
+        table = oracle_table(wi, g)
+        p_blocks.append(_oracle_params(g, table))
+        dev_blocks.append((wi, {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v)
+                               for k, v in _block_params_dev(g, table).items()}))
+        if i == 0:
+            x = g["x"]
+    gn = torch.Generator().manual_seed(123)
+    gam = (1 + 0.1 * torch.randn(w0.C, generator=gn)).bfloat16()
+    bet = (0.1 * torch.randn(w0.C, generator=gn)).bfloat16()
+    mg, mb, mW = _merge_inputs(w0.C, 77)
+    cur = x.to(DEV)
+    for i, (wi, params) in enumerate(dev_blocks):
+        nxt = torch.empty_like(cur)
+        h = sw.swin_block_create(wi.C, wi.heads, wi.M, wi.shift, wi.mode, 4)
+        try:
+            sw.swin_block_forward(h, cur, params, nxt)
+            sw.swin_block_sync_status(h)
+        finally:
+            sw.swin_block_destroy(h)
+        cur = nxt
+        if i == 5:
+            sw.swin_stage_norm(cur, gam.to(DEV), bet.to(DEV), cur)
+    out = torch.empty(w0.B, w0.H // 2, w0.W // 2, 2 * w0.C, dtype=torch.bfloat16, device=DEV)
+    hm = sw.swin_merge_create(w0.C)
+    try:
+        sw.swin_merge_forward(hm, cur, mg.to(DEV), mb.to(DEV), mW.to(DEV), out)
+        torch.cuda.synchronize()
+    finally:
+        sw.swin_merge_destroy(hm)
+    ref = ob.stage(to_f64(x), p_blocks, heads=w0.heads, M=w0.M, mode=w0.mode,
+                   merge=(to_f64(mg), to_f64(mb), to_f64(mW)), extra_norm=(6, [(to_f64(gam), to_f64(bet))]))
+    _block_compare(to_f64(out.cpu()), ref, w0.mode)

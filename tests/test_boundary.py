@@ -16,7 +16,7 @@ def declared_functions():
     names = set()
     for hdr in os.listdir(os.path.join(ROOT, "include")):
         text = open(os.path.join(ROOT, "include", hdr)).read()
-        names |= set(re.findall(r"^\s*(?:int|const char \*)\s*(swin_(?:wattn|block|merge)_\w+)\s*\(", text, re.M))
+        names |= set(re.findall(r"^\s*(?:int|const char \*)\s*(swin_(?:wattn|block|merge|stage)_\w+)\s*\(", text, re.M))
     return names
 
 

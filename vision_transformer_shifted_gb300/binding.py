@@ -55,6 +55,7 @@ _SIGNATURES = {
     "swin_block_sync_status": ["p", "p"],
     "swin_block_destroy": ["p"],
     "swin_block_test_layernorm": ["p", "p", "p", "p", "p", "p", "i", "i", "i", "p"],
+    "swin_stage_norm": ["p", "i", "i", "p", "p", "p", "p"],
     "swin_merge_create": ["pp", "i"],
     "swin_merge_forward": ["p", "p", "i", "i", "i", "p", "p", "p", "p", "p"],
     "swin_merge_destroy": ["p"],
@@ -278,6 +279,14 @@ def swin_block_test_layernorm(a, b, gamma, beta, out_sum, out_ln, flags, stream=
     rows, C = a.shape[0], a.shape[-1]
     return _check("swin_block_test_layernorm", load().swin_block_test_layernorm(
         _p(a), _p(b), _p(gamma), _p(beta), _p(out_sum), _p(out_ln), rows, C, flags, _stream(stream)))
+
+
+def swin_stage_norm(x, gamma, beta, out, stream=None):
+    """out = LN(x) over the last axis of x [..., C] (the extra LayerNorm of a V2
+    stage); out may be x."""
+    C = x.shape[-1]
+    return _check("swin_stage_norm", load().swin_stage_norm(
+        _p(x), x.numel() // C, C, _p(gamma), _p(beta), _p(out), _stream(stream)))
 
 
 def swin_merge_create(C):

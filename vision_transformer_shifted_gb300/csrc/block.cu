@@ -322,6 +322,20 @@ int swin_block_test_layernorm(const void *a, const void *b, const void *gamma, c
                                         (bf16 *)out_sum, (bf16 *)out_ln, rows, C, flags, (cudaStream_t)stream));
 }
 
+int swin_stage_norm(const void *x, int rows, int C, const void *gamma, const void *beta, void *out, swin_stream_t stream)
+{
+    if (!x || !gamma || !beta || !out || rows < 0 || C <= 0 || C % 8 || C > 2048) return SWIN_WATTN_EINVAL;
+    const void *ps[] = {x, gamma, beta, out};
+    for (const void *q : ps)
+        if (!aligned16(q)) return SWIN_WATTN_EINVAL;
+    const char *xb = (const char *)x, *ob = (const char *)out;
+    const int64_t bytes = (int64_t)rows * C * 2;
+    if (xb != ob && xb < ob + bytes && ob < xb + bytes) return SWIN_WATTN_EINVAL;
+    if (rows == 0) return SWIN_WATTN_OK;
+    return cuda_status(launch_layernorm((const bf16 *)x, nullptr, (const bf16 *)gamma, (const bf16 *)beta, nullptr,
+                                        (bf16 *)out, rows, C, 0, (cudaStream_t)stream));
+}
+
 // ---- merging step between stages ------------------------------------------------
 
 } // extern "C"
