@@ -186,7 +186,8 @@ def test_attention_stage(key, B, H, W):
 
 SMALL = [
     ("swin_t_s1", 2, 14, 21, False), ("swin_t_s1", 3, 7, 21, True),     # odd window count
-    ("swin_b_s1", 2, 28, 28, True), ("swin_b_s3", 3, 14, 14, False),
+    ("swin_b_s1", 2, 28, 28, True), ("swin_b_s1", 3, 21, 14, True),   # C = 128: one tile in flight
+    ("swin_b_s3", 3, 14, 14, False),
     ("swinv2_t_s1", 2, 16, 24, True), ("swinv2_t_s1", 1, 8, 8, False),   # one window, mask everywhere
     ("swinv2_l_w24", 1, 48, 48, True),
 ]
@@ -219,7 +220,7 @@ def test_forward_ragged_tiles(key, B, H, W, path):
 
 
 def test_fused_path_is_chosen_where_supported():
-    for key, want in [("swin_t_s1", sw.PATH_FUSED), ("swinv2_t_s1", sw.PATH_FUSED), ("swin_b_s1", 1),
+    for key, want in [("swin_t_s1", sw.PATH_FUSED), ("swinv2_t_s1", sw.PATH_FUSED), ("swin_b_s1", sw.PATH_FUSED),
                       ("swin_b_s3", 1), ("swinv2_l_w24", 1), ("tiny", sw.PATH_FP32)]:
         w = WORKLOADS[key]
         h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode | (sw.FP32 if w.dtype == "fp32" else 0))
@@ -227,6 +228,18 @@ def test_fused_path_is_chosen_where_supported():
             assert sw.swin_wattn_path(h, w.B, w.H, w.W) == want, key
         finally:
             sw.swin_wattn_destroy(h)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M,B,H,W", [(8, 2, 16, 24), (7, 3, 21, 14)])
+def test_forward_v2_four_heads(M, B, H, W, path):
+    """V2 cosine attention with C = 128 (four heads): the fused kernel's
+    one-tile-in-flight variant, whose q passes through TMEM."""
+    w = WORKLOADS["swinv2_t_s1"].with_(B=B, H=H, W=W, C=128, heads=4, M=M, shift=M // 2)
+    g = generate(w, nonzero_bias=True)
+    table = oracle_table(w, g)
+    out = run_forward(w, device_inputs(g), table.to(DEV), path)
+    compare(out.double().cpu().numpy(), oracle_forward(w, g, table), w.dtype)
 
 
 @pytest.mark.parametrize("path", PATHS)

@@ -189,7 +189,7 @@ struct Fp32Args {
 cudaError_t launch_fp32_block(const Fp32Args &a, cudaStream_t stream);
 size_t fp32_block_smem_bytes(int N, int C);
 
-// The whole block in one persistent kernel (windows of <= 64 tokens, C = 64 or 96).
+// The whole block in one persistent kernel (windows of <= 64 tokens, C = 64, 96 or 128).
 bool fused_supported(int M, int C, int heads);
 cudaError_t launch_fused(const bf16 *x, const bf16 *Wqkv, const bf16 *bqkv, const bf16 *table, const float *tau,
                          const bf16 *Wproj, const bf16 *bproj, bf16 *out, int mode, const Geom &g, DeviceStatus st,

@@ -1,6 +1,6 @@
 // The whole shifted-window attention block in one persistent kernel
 // (sm_103a, tcgen05 + TMEM), for windows of at most 64 tokens (M = 7, 8) and
-// C = 64 or 96 channels (2 or 3 heads of 32).
+// C = 64, 96 or 128 channels (2, 3 or 4 heads of 32).
 //
 // Steps, per tile of two windows (pages "Boosting Swin Transformer Speed",
 // Introduction / Training Optimization / Inference Optimization; "Swin
@@ -51,7 +51,11 @@
 // group X(g) (its tile's x; once the QKV MMAs have read it, the same bytes
 // hold q), K(g) (k of each head) and V(g) (v of each head, the N-major B
 // operand of P.V; then o, the projection's A operand; then the staged output
-// rows).  All hand-offs are mbarriers: "ready" barriers get one arrival per
+// rows).  C = 128 leaves room for one tile in flight only (the weights take
+// 128 KB): group 1 idles, k goes into X once the QKV MMAs have read x, and q
+// is written back into TMEM as bf16 (16 columns per head after the group's
+// 128), from where the S MMAs read it as their A operand.
+// All hand-offs are mbarriers: "ready" barriers get one arrival per
 // compute warp of the group, "done" barriers are tcgen05.commit targets.
 // Every wait is bounded: a timeout sets the error word, and every role
 // leaves at its next wait.
@@ -70,38 +74,45 @@ constexpr int GWARPS = 4;     // compute warps per group
 constexpr int FTHREADS = 12 * 32;
 constexpr float FLOG2E = 1.4426950408889634f;
 
-template <int M, int C>
+// G = 2: two tiles in flight (C = 64, 96): per group X(g) (x, then q), K(g)
+// and V(g) in shared memory.  G = 1 (C = 128, whose resident weights leave
+// shared memory for one tile only): q goes back into TMEM (bf16, the A
+// operand of S), k into X once the QKV MMAs have read x, and there is no K.
+template <int M, int C, int G>
 struct FusedCfg {
     static constexpr int HEADS = C / 32;
     static constexpr int L = 2 * M - 1;
     static constexpr int KB = C / 32;          // 32-channel K blocks (64-byte swizzle)
     static constexpr int HT = 128 * 64;        // one [128 rows][32 channels] SW64 tile
+    static constexpr bool Q_TMEM = G == 1;
     // shared memory (bytes); SW64 tiles are 512-aligned
     static constexpr int WQK = 0;                       // [2C rows][C]
     static constexpr int WV = WQK + 2 * C * C * 2;      // [C rows][C]
     static constexpr int WP = WV + C * C * 2;           // [C rows][C]
     static constexpr int XT = WP + C * C * 2;           // X(g) = XT + g * KB * HT
-    static constexpr int KT = XT + 2 * KB * HT;         // K(g)
-    static constexpr int VT = KT + 2 * KB * HT;         // V(g)
-    static constexpr int SMALL = VT + 2 * KB * HT;
+    static constexpr int KT = XT + G * KB * HT;         // K(g) (G = 2)
+    static constexpr int VT = KT + (Q_TMEM ? 0 : G * KB * HT);   // V(g)
+    static constexpr int SMALL = VT + G * KB * HT;
     static constexpr int O_BQKV = 0;                          // [3C] f32
     static constexpr int O_BPROJ = O_BQKV + 3 * C * 4;        // [C] f32
     static constexpr int O_SCALE = O_BPROJ + C * 4;           // [4] f32
     static constexpr int O_BIAS = O_SCALE + 16;               // [HEADS][L*L] f32, times log2(e)
     static constexpr int O_BARS = (O_BIAS + HEADS * L * L * 4 + 7) / 8 * 8;
-    static constexpr int NBARS = 2 * 19 + 1;
+    static constexpr int NBARS = 2 * 20 + 1;
     static constexpr int O_END = O_BARS + NBARS * 8 + 16;
     static constexpr int BYTES = SMALL + O_END;
     // TMEM columns
     static constexpr int T_QK = 0;                      // [0, 2C): q of head h at 32h, k at C + 32h
     static constexpr int T_R0 = 2 * C;                  // group g's 128 columns at T_R0 + 128 g
-    static_assert(T_R0 + 256 <= 512, "TMEM budget");
+    static constexpr int T_Q = T_R0 + 128 * G;          // (G = 1) q of head h (bf16 pairs) at 16h
+    static_assert(T_Q + (Q_TMEM ? 16 * HEADS : 0) <= 512, "TMEM budget");
+    static_assert(G == 1 || G == 2, "one or two tiles in flight");
     static_assert(C <= 128, "v and y fit the group's 128 columns");
     static_assert(M <= 8, "two windows of 8-row-aligned window rows per 128-row tile");
     static_assert(BYTES + 1024 <= 232448, "shared memory budget");
 };
 
-// Barriers: group g's at 19 g + ..., and one shared by the groups.
+// Barriers: group g's at 20 g + ..., and one shared by the groups.
 enum {
     BR_X = 0,       // x of the group's tile landed in X(g) (TMA bytes + producer arrival)
     BR_XFREE = 1,   // the group's last S MMA of its tile done: X(g) (q) may take the next x
@@ -116,8 +127,8 @@ enum {
     BR_RFREE = 14,  // y drained from TMEM: the group's columns are free (compute warps)
     BR_STAGE = 15,  // output rows staged in V(g) (compute warps)
     BR_VFREE = 16,  // output stored: V(g) may take the next v (producer)
-    BR_QKR1 = 17,   // + h - 1: q and k of head h = 1, 2 drained (compute warps)
-    BR_QKFREE = 38  // (shared) q and k of the last QKV drained from TMEM (compute warps)
+    BR_QKR1 = 17,   // + h - 1: q and k of head h = 1, 2, 3 drained (compute warps)
+    BR_QKFREE = 40  // (shared) q and k of the last QKV drained from TMEM (compute warps)
 };
 
 struct FusedArgs {
@@ -247,14 +258,14 @@ __device__ __forceinline__ int window_token(const Geom &g, const WinInfo &w, int
     return (w.b * g.H + i) * g.W + j;
 }
 
-template <int M, int C>
+template <int M, int C, int G>
 __global__ void __launch_bounds__(FTHREADS, 1)
     fused_block_kernel(FusedArgs a, DeviceStatus st, const __grid_constant__ CUtensorMap tmap_x,
                        const __grid_constant__ CUtensorMap tmap_out)
 // tmap_x: x as [B*H][W][C], boxes of 32 x 8 x M; tmap_out: out as [B*H][W][C],
 // boxes of 32 x M x M
 {
-    using F = FusedCfg<M, C>;
+    using F = FusedCfg<M, C, G>;
     constexpr int HEADS = F::HEADS, L = F::L, KB = F::KB, HT = F::HT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_align(smem_raw, 1024);
@@ -270,7 +281,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     const Geom g = a.g;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = smem_u32(sm);
-    auto BAR = [&](int grp, int i) { return smem_u32(&bars[19 * grp + i]); };
+    auto BAR = [&](int grp, int i) { return smem_u32(&bars[20 * grp + i]); };
     // q and k of head h drained (and, for h = 0, v before them)
     auto QKR = [&](int grp, int h) { return BAR(grp, h == 0 ? BR_QKR : BR_QKR1 + h - 1); };
     const uint32_t B_QKFREE = smem_u32(&bars[BR_QKFREE]);
@@ -278,7 +289,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     // this CTA's tiles: j = 0, 1, ... while blockIdx.x + j * gridDim.x < ntiles
     const int my_tiles = ntiles > (int)blockIdx.x ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     auto X = [&](int grp) { return base + F::XT + grp * KB * HT; };
-    auto K = [&](int grp) { return base + F::KT + grp * KB * HT; };
+    auto K = [&](int grp) { return F::Q_TMEM ? base + F::XT : base + F::KT + grp * KB * HT; };
     auto V = [&](int grp) { return base + F::VT + grp * KB * HT; };
 
     // ---- once per CTA: weights, biases, tables, barriers, TMEM ---------------
@@ -311,7 +322,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         // with ti or tj >= M, a missing second window) then only ever hold
         // finite values (zeros, other tokens, q of earlier tiles), so the v
         // rows of keys that do not exist -- multiplied by P = 0 -- stay finite
-        for (int i = tid; i < 2 * KB * HT / 16; i += FTHREADS)
+        for (int i = tid; i < G * KB * HT / 16; i += FTHREADS)
             reinterpret_cast<uint4 *>(sm + F::XT)[i] = make_uint4(0u, 0u, 0u, 0u);
         cp_async_wait<0>();
         fence_proxy_async_smem();
@@ -342,14 +353,13 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         sbproj[tid] += acc;
     }
     if (tid == 0) {
-        for (int grp = 0; grp < 2; ++grp) {
-            const int b0 = 19 * grp;
+        for (int grp = 0; grp < G; ++grp) {
+            const int b0 = 20 * grp;
             mbar_init(smem_u32(&bars[b0 + BR_X]), 2);
             mbar_init(smem_u32(&bars[b0 + BR_XFREE]), 1);
             mbar_init(smem_u32(&bars[b0 + BR_QKV]), 1);
             mbar_init(smem_u32(&bars[b0 + BR_QKR]), GWARPS);
-            mbar_init(smem_u32(&bars[b0 + BR_QKR1]), GWARPS);
-            mbar_init(smem_u32(&bars[b0 + BR_QKR1 + 1]), GWARPS);
+            for (int h = 1; h < 4; ++h) mbar_init(smem_u32(&bars[b0 + BR_QKR1 + h - 1]), GWARPS);
             for (int r = 0; r < 2; ++r) {
                 mbar_init(smem_u32(&bars[b0 + BR_S + r]), 1);
                 mbar_init(smem_u32(&bars[b0 + BR_P + r]), GWARPS);
@@ -440,9 +450,10 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         int p_load = perm0;
 #pragma unroll 1
         for (int j = 0; j < my_tiles; ++j) {
-            const int grp = j & 1, kg = j >> 1;
-            // X(grp) takes tile j once the group's S MMAs of tile j - 2 have read q
-            if (j >= 2 && !(ok = warp_wait(BAR(grp, BR_XFREE), (kg - 1) & 1, st.wait_ns, abort_flag))) break;
+            const int grp = j % G, kg = j / G;
+            // X(grp) takes tile j once the group's S MMAs of its previous tile have
+            // read q (G = 1: k)
+            if (j >= G && !(ok = warp_wait(BAR(grp, BR_XFREE), (kg - 1) & 1, st.wait_ns, abort_flag))) break;
             if (load_x(grp, p_load)) x_landed(grp);
             p_load = perm_next(p_load);
         }
@@ -456,9 +467,9 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             bool ok = true;
 #pragma unroll 1
             for (int j = 0; j < my_tiles; ++j) {
-                const int grp = j & 1, kg = j >> 1;
+                const int grp = j % G, kg = j / G;
                 // tile j's x has landed, the q|k columns are free (tile j - 1's
-                // drained) and the group's columns are free (y of its tile j - 2
+                // drained) and the group's columns are free (y of its previous tile
                 // drained)
                 if (!(ok = wait_or_abort(BAR(grp, BR_X), kg & 1, st.wait_ns, abort_flag))) break;
                 if (j > 0 && !(ok = wait_or_abort(B_QKFREE, (j - 1) & 1, st.wait_ns, abort_flag))) break;
@@ -484,7 +495,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     } else if (warp < CWARP0) {
         // ============ issuer of group warp - 2: S, P.V, the projection ============
         const int grp = warp - AWARP0;
-        if (lane == 0) {
+        if (lane == 0 && grp < G) {
             constexpr uint32_t id_s = idesc_bf16(128, 64), id_pv = idesc_bf16_bmn(128, 32), id_y = idesc_bf16(128, C);
             const uint64_t d_wp = desc_kmajor_sw64(base + F::WP);
             // output-lane masks: every row but window A's / window B's
@@ -493,17 +504,19 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             const uint64_t dq = desc_kmajor_sw64(X(grp)), dk = desc_kmajor_sw64(K(grp));
             const uint64_t dv = desc_mnmajor_sw64(V(grp), 8192);
             // S of head hd into buffer r: all 128 q rows against each window's 64
-            // keys, each MMA keeping only its window's rows
+            // keys, each MMA keeping only its window's rows (G = 1: q from TMEM)
             auto issue_s = [&](int hd, int r) {
                 const uint32_t d = t_r + 64 * r;
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
-                    mma_bf16_mask(d, desc_add(dq, hd * HT + 32 * ks), desc_add(dk, hd * HT + 32 * ks), id_s, ks,
-                                  mask_a);
+                for (int w = 0; w < 2; ++w)
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
-                    mma_bf16_mask(d, desc_add(dq, hd * HT + 32 * ks), desc_add(dk, hd * HT + 4096 + 32 * ks), id_s,
-                                  ks, mask_b);
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const uint64_t bk = desc_add(dk, hd * HT + 4096 * w + 32 * ks);
+                        if (F::Q_TMEM)
+                            mma_bf16_ts_mask(d, tmem + F::T_Q + 16 * hd + 8 * ks, bk, id_s, ks, w ? mask_b : mask_a);
+                        else
+                            mma_bf16_mask(d, desc_add(dq, hd * HT + 32 * ks), bk, id_s, ks, w ? mask_b : mask_a);
+                    }
                 mma_commit(BAR(grp, BR_S + r));
             };
             // o_h = P v_h over each window's 64 keys, for its rows, into the upper
@@ -524,10 +537,11 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             uint32_t ph_p = 0;
             uint32_t od_n[2] = {0u, 0u};
             bool ok = true;
-            int p_tile = grp ? perm_next(perm0) : perm0;
+            int p_tile = perm0;
+            for (int i = 0; i < grp; ++i) p_tile = perm_next(p_tile);
 #pragma unroll 1
-            for (int j = grp; ok && j < my_tiles; j += 2) {
-                const int kg = j >> 1;
+            for (int j = grp; ok && j < my_tiles; j += G) {
+                const int kg = j / G;
                 // S of heads 0 and 1 as soon as their q and k are in shared memory
                 // (v, drained first, has then left the TMEM columns S takes)
                 if (!(ok = wait_or_abort(QKR(grp, 0), kg & 1, st.wait_ns, abort_flag))) break;
@@ -583,7 +597,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
                 bulk_commit();
                 bulk_wait_read();
                 mbar_arrive(BAR(grp, BR_VFREE));
-                p_tile = perm_next(perm_next(p_tile));
+                for (int i = 0; i < G; ++i) p_tile = perm_next(p_tile);
             }
             bulk_wait_all();
             if (!ok) *abort_flag = 1;
@@ -591,24 +605,28 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     } else {
         // ===================== compute warps =====================
         const int grp = (warp - CWARP0) / GWARPS, quarter = warp & 3;
+        if (grp >= G) goto done;   // (G = 1: the second group's warps have no work)
         const int row = quarter * 32 + lane;        // tile row = TMEM lane
         const int slot = row >> 6, t = row & 63;    // window slot; token (t >> 3, t & 7) of the row
         const int ti = t >> 3, tj = t & 7;
         const bool tok_row = ti < M && tj < M;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         const uint32_t t_r = t_lane + F::T_R0 + 128 * grp;
-        uint8_t *xg = sm + F::XT + grp * KB * HT, *kgs = sm + F::KT + grp * KB * HT, *vg = sm + F::VT + grp * KB * HT;
+        uint8_t *xg = sm + F::XT + grp * KB * HT, *vg = sm + F::VT + grp * KB * HT;
+        uint8_t *kgs = F::Q_TMEM ? xg : sm + F::KT + grp * KB * HT;
         // relative-bias row of this token (rows no token fills read a valid row;
         // their results are never stored)
         const int bias_base = tok_row ? (ti + M - 1) * L + (tj + M - 1) : (M - 1) * L + (M - 1);
         uint32_t ph_s = 0, ph_pv = 0;   // bit r: phase of BR_S + r / BR_PV + r
-        float l0 = 1.f, l1 = 1.f, l2 = 1.f;   // each head's row sum (heads 0..2)
+        // row sum of the head whose softmax last used S buffer r (each drain of
+        // head h comes before the softmax of head h + 2)
+        float l0 = 1.f, l1 = 1.f;
         bool ok = true;
         int p_tile = perm0;
-        if (grp == 1) p_tile = perm_next(p_tile);
+        for (int i = 0; i < grp; ++i) p_tile = perm_next(p_tile);
 #pragma unroll 1
-        for (int j = grp; j < my_tiles; j += 2) {
-            const int kg = j >> 1;
+        for (int j = grp; j < my_tiles; j += G) {
+            const int kg = j / G;
             const WinInfo win = window_info(g, p_tile, slot);
             if (!(ok = warp_wait(BAR(grp, BR_QKV), kg & 1, st.wait_ns, abort_flag))) break;
             tc_fence_after();
@@ -661,7 +679,31 @@ __global__ void __launch_bounds__(FTHREADS, 1)
                 tmem_ld32(t_lane + F::T_QK + 32 * hd, vq);
                 tmem_ld32(t_lane + F::T_QK + C + 32 * hd, vk);
                 tmem_wait_ld();
-                put(vq, sbqkv + 32 * hd, xg + hd * HT, v2);
+                if (F::Q_TMEM) {
+                    // (G = 1) q back into TMEM as bf16 pairs, the A operand of S
+                    const float4 *b4 = reinterpret_cast<const float4 *>(sbqkv + 32 * hd);
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 bb = b4[e4];
+                        fadd2(vq[4 * e4], vq[4 * e4 + 1], bb.x, bb.y);
+                        fadd2(vq[4 * e4 + 2], vq[4 * e4 + 3], bb.z, bb.w);
+                    }
+                    if (v2) {
+                        float ss = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ss = fmaf(vq[e], vq[e], ss);
+                        const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) fmul2(vq[e], vq[e + 1], inv);
+                    }
+                    uint32_t qp[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) qp[e] = pack_bf16x2(vq[2 * e], vq[2 * e + 1]);
+                    tmem_st16(t_lane + F::T_Q + 16 * hd, qp);
+                    tmem_wait_st();
+                } else {
+                    put(vq, sbqkv + 32 * hd, xg + hd * HT, v2);
+                }
                 put(vk, v2 ? sbqkv + C + 32 * hd : nullptr, kgs + hd * HT, v2);
                 fence_proxy_async_smem();   // read by the S (and P.V) MMAs
                 warp_arrive(QKR(grp, hd), lane);
@@ -681,10 +723,13 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             }
             // action i of a tile: the softmax of head a (a >= 0) or the o drain of
             // head -a - 1 (a < 0)
+            // (after softmax 0 and 1: drain h, softmax h + 2 while h + 2 < HEADS,
+            // then the last two drains; three heads: S0 S1 D0 S2 D1 D2)
             auto head_action = [](int i) -> int {
                 if (i < 2) return i;
-                if (HEADS == 2) return 1 - i;          // drains 0, 1
-                return i == 2 ? -1 : i == 3 ? 2 : 2 - i;   // drain 0, softmax 2, drains 1, 2
+                const int k = i - 2;
+                if (k < 2 * (HEADS - 2)) return (k & 1) ? (k >> 1) + 2 : -(k >> 1) - 1;
+                return -(HEADS - 2 + k - 2 * (HEADS - 2)) - 1;
             };
             // ---- softmax of head hd (buffer hd & 1) over the row's window keys ----
             auto softmax = [&](int hd) -> bool {
@@ -754,9 +799,8 @@ __global__ void __launch_bounds__(FTHREADS, 1)
                     pk[jj / 2] = pack_bf16x2(p0, p1);
                 }
                 const float sum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
-                if (hd == 0) l0 = sum;
-                else if (hd == 1) l1 = sum;
-                else l2 = sum;
+                if (r) l1 = sum;
+                else l0 = sum;
                 // P (bf16, two keys per 32-bit column) over the first 32 columns
                 tmem_st16(t_r + 64 * r, *reinterpret_cast<uint32_t(*)[16]>(pk));
                 tmem_st16(t_r + 64 * r + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
@@ -774,7 +818,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
                 float o[32];
                 tmem_ld32(t_r + 64 * r + 32, o);
                 tmem_wait_ld();
-                const float inv = rcp_approx(hd == 0 ? l0 : hd == 1 ? l1 : l2);
+                const float inv = rcp_approx(r ? l1 : l0);
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) fmul2(o[e], o[e + 1], inv);
 #pragma unroll
@@ -837,10 +881,11 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             }
             fence_proxy_async_smem();   // the TMA stores read these rows
             warp_arrive(BAR(grp, BR_STAGE), lane);
-            p_tile = perm_next(perm_next(p_tile));
+            for (int i = 0; i < G; ++i) p_tile = perm_next(p_tile);
         }
         if (!ok) *abort_flag = 1;
     }
+done:
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && *abort_flag) atomicOr(st.err, ERR_TIMEOUT);
@@ -877,12 +922,12 @@ int64_t coprime_near(int64_t n, int64_t start)
         if (gcd(v, n) == 1) return v % n ? v : 1;
 }
 
-template <int M, int C>
+template <int M, int C, int G>
 cudaError_t launch_fused_t(const FusedArgs &a, DeviceStatus st, cudaStream_t stream)
 {
-    using F = FusedCfg<M, C>;
+    using F = FusedCfg<M, C, G>;
     const size_t smem = F::BYTES + 1024;
-    auto kern = fused_block_kernel<M, C>;
+    auto kern = fused_block_kernel<M, C, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     CUtensorMap tx, to;
@@ -903,7 +948,7 @@ cudaError_t launch_fused_t(const FusedArgs &a, DeviceStatus st, cudaStream_t str
 
 bool fused_supported(int M, int C, int heads)
 {
-    return (M == 7 || M == 8) && (C == 64 || C == 96) && C == heads * 32;
+    return (M == 7 || M == 8) && (C == 64 || C == 96 || C == 128) && C == heads * 32;
 }
 
 cudaError_t launch_fused(const bf16 *x, const bf16 *Wqkv, const bf16 *bqkv, const bf16 *table, const float *tau,
@@ -911,10 +956,12 @@ cudaError_t launch_fused(const bf16 *x, const bf16 *Wqkv, const bf16 *bqkv, cons
                          cudaStream_t stream)
 {
     FusedArgs a{x, Wqkv, bqkv, table, Wproj, bproj, tau, out, mode, g, 1, 0};
-    if (g.M == 7 && g.C == 96) return launch_fused_t<7, 96>(a, st, stream);
-    if (g.M == 8 && g.C == 96) return launch_fused_t<8, 96>(a, st, stream);
-    if (g.M == 7 && g.C == 64) return launch_fused_t<7, 64>(a, st, stream);
-    if (g.M == 8 && g.C == 64) return launch_fused_t<8, 64>(a, st, stream);
+    if (g.M == 7 && g.C == 96) return launch_fused_t<7, 96, 2>(a, st, stream);
+    if (g.M == 8 && g.C == 96) return launch_fused_t<8, 96, 2>(a, st, stream);
+    if (g.M == 7 && g.C == 64) return launch_fused_t<7, 64, 2>(a, st, stream);
+    if (g.M == 8 && g.C == 64) return launch_fused_t<8, 64, 2>(a, st, stream);
+    if (g.M == 7 && g.C == 128) return launch_fused_t<7, 128, 1>(a, st, stream);
+    if (g.M == 8 && g.C == 128) return launch_fused_t<8, 128, 1>(a, st, stream);
     return cudaErrorInvalidValue;
 }
 
