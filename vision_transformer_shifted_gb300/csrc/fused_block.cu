@@ -52,9 +52,12 @@
 // hold q), K(g) (k of each head) and V(g) (v of each head, the N-major B
 // operand of P.V; then o, the projection's A operand; then the staged output
 // rows).  C = 128 leaves room for one tile in flight only (the weights take
-// 128 KB): group 1 idles, k goes into X once the QKV MMAs have read x, and q
-// is written back into TMEM as bf16 (16 columns per head after the group's
-// 128), from where the S MMAs read it as their A operand.
+// 128 KB), so there the two groups split each tile's heads instead (group g:
+// heads 2g, 2g + 1, with issuer warp 2 + g and its own S buffers in the
+// second 128 TMEM columns of the pair; group 0 also drains v, and each group
+// drains half of y).  k goes into X once the QKV MMAs have read x, and q is
+// written back into TMEM as bf16 over its own fp32 columns, from where the S
+// MMAs read it as their A operand.
 // All hand-offs are mbarriers: "ready" barriers get one arrival per
 // compute warp of the group, "done" barriers are tcgen05.commit targets.
 // Every wait is bounded: a timeout sets the error word, and every role
@@ -76,7 +79,8 @@ constexpr float FLOG2E = 1.4426950408889634f;
 
 // G = 2: two tiles in flight (C = 64, 96): per group X(g) (x, then q), K(g)
 // and V(g) in shared memory.  G = 1 (C = 128, whose resident weights leave
-// shared memory for one tile only): q goes back into TMEM (bf16, the A
+// shared memory for one tile only): the two compute groups split the tile's
+// heads, q goes back into TMEM (bf16, over its own fp32 columns: the A
 // operand of S), k into X once the QKV MMAs have read x, and there is no K.
 template <int M, int C, int G>
 struct FusedCfg {
@@ -84,14 +88,16 @@ struct FusedCfg {
     static constexpr int L = 2 * M - 1;
     static constexpr int KB = C / 32;          // 32-channel K blocks (64-byte swizzle)
     static constexpr int HT = 128 * 64;        // one [128 rows][32 channels] SW64 tile
-    static constexpr bool Q_TMEM = G == 1;
+    static constexpr bool SPLIT = G == 1;                 // one tile, heads split over the groups
+    static constexpr int HPG = SPLIT ? HEADS / 2 : HEADS;  // heads per compute group
+    static constexpr int TW = (SPLIT ? 2 : 1) * 4;         // warps arriving on a tile barrier
     // shared memory (bytes); SW64 tiles are 512-aligned
     static constexpr int WQK = 0;                       // [2C rows][C]
     static constexpr int WV = WQK + 2 * C * C * 2;      // [C rows][C]
     static constexpr int WP = WV + C * C * 2;           // [C rows][C]
     static constexpr int XT = WP + C * C * 2;           // X(g) = XT + g * KB * HT
     static constexpr int KT = XT + G * KB * HT;         // K(g) (G = 2)
-    static constexpr int VT = KT + (Q_TMEM ? 0 : G * KB * HT);   // V(g)
+    static constexpr int VT = KT + (SPLIT ? 0 : G * KB * HT);    // V(g)
     static constexpr int SMALL = VT + G * KB * HT;
     static constexpr int O_BQKV = 0;                          // [3C] f32
     static constexpr int O_BPROJ = O_BQKV + 3 * C * 4;        // [C] f32
@@ -104,9 +110,9 @@ struct FusedCfg {
     // TMEM columns
     static constexpr int T_QK = 0;                      // [0, 2C): q of head h at 32h, k at C + 32h
     static constexpr int T_R0 = 2 * C;                  // group g's 128 columns at T_R0 + 128 g
-    static constexpr int T_Q = T_R0 + 128 * G;          // (G = 1) q of head h (bf16 pairs) at 16h
-    static_assert(T_Q + (Q_TMEM ? 16 * HEADS : 0) <= 512, "TMEM budget");
+    static_assert(T_R0 + 256 <= 512, "TMEM budget");
     static_assert(G == 1 || G == 2, "one or two tiles in flight");
+    static_assert(!SPLIT || HEADS % 2 == 0, "the groups split the heads evenly");
     static_assert(C <= 128, "v and y fit the group's 128 columns");
     static_assert(M <= 8, "two windows of 8-row-aligned window rows per 128-row tile");
     static_assert(BYTES + 1024 <= 232448, "shared memory budget");
@@ -114,6 +120,8 @@ struct FusedCfg {
 
 // Barriers: group g's at 20 g + ..., and one shared by the groups.
 enum {
+    // (G = 1: the tile barriers -- X, XFREE, QKV, O, Y, RFREE, STAGE, VFREE --
+    // are group 0's, and O, RFREE, STAGE and QKFREE take both groups' warps)
     BR_X = 0,       // x of the group's tile landed in X(g) (TMA bytes + producer arrival)
     BR_XFREE = 1,   // the group's last S MMA of its tile done: X(g) (q) may take the next x
     BR_QKV = 2,     // QKV MMAs of the group's tile done
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     // this CTA's tiles: j = 0, 1, ... while blockIdx.x + j * gridDim.x < ntiles
     const int my_tiles = ntiles > (int)blockIdx.x ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     auto X = [&](int grp) { return base + F::XT + grp * KB * HT; };
-    auto K = [&](int grp) { return F::Q_TMEM ? base + F::XT : base + F::KT + grp * KB * HT; };
+    auto K = [&](int grp) { return F::SPLIT ? base + F::XT : base + F::KT + grp * KB * HT; };
     auto V = [&](int grp) { return base + F::VT + grp * KB * HT; };
 
     // ---- once per CTA: weights, biases, tables, barriers, TMEM ---------------
@@ -353,10 +361,10 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         sbproj[tid] += acc;
     }
     if (tid == 0) {
-        for (int grp = 0; grp < G; ++grp) {
+        for (int grp = 0; grp < 2; ++grp) {
             const int b0 = 20 * grp;
             mbar_init(smem_u32(&bars[b0 + BR_X]), 2);
-            mbar_init(smem_u32(&bars[b0 + BR_XFREE]), 1);
+            mbar_init(smem_u32(&bars[b0 + BR_XFREE]), F::SPLIT ? 2 : 1);   // a commit per S issuer
             mbar_init(smem_u32(&bars[b0 + BR_QKV]), 1);
             mbar_init(smem_u32(&bars[b0 + BR_QKR]), GWARPS);
             for (int h = 1; h < 4; ++h) mbar_init(smem_u32(&bars[b0 + BR_QKR1 + h - 1]), GWARPS);
@@ -366,13 +374,13 @@ __global__ void __launch_bounds__(FTHREADS, 1)
                 mbar_init(smem_u32(&bars[b0 + BR_PV + r]), 1);
                 mbar_init(smem_u32(&bars[b0 + BR_OD + r]), GWARPS);
             }
-            mbar_init(smem_u32(&bars[b0 + BR_O]), GWARPS);
+            mbar_init(smem_u32(&bars[b0 + BR_O]), F::TW);
             mbar_init(smem_u32(&bars[b0 + BR_Y]), 1);
-            mbar_init(smem_u32(&bars[b0 + BR_RFREE]), GWARPS);
-            mbar_init(smem_u32(&bars[b0 + BR_STAGE]), GWARPS);
+            mbar_init(smem_u32(&bars[b0 + BR_RFREE]), F::TW);
+            mbar_init(smem_u32(&bars[b0 + BR_STAGE]), F::TW);
             mbar_init(smem_u32(&bars[b0 + BR_VFREE]), 1);
         }
-        mbar_init(smem_u32(&bars[BR_QKFREE]), GWARPS);
+        mbar_init(smem_u32(&bars[BR_QKFREE]), F::TW);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -494,26 +502,32 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         }
     } else if (warp < CWARP0) {
         // ============ issuer of group warp - 2: S, P.V, the projection ============
+        // (G = 1: issuer g takes group g's heads of every tile; group 0's issuer
+        // also the projection and the stores)
         const int grp = warp - AWARP0;
-        if (lane == 0 && grp < G) {
+        const int tg = F::SPLIT ? 0 : grp;         // the tile's buffers and tile barriers
+        const int h0 = F::SPLIT ? grp * F::HPG : 0;   // the group's first head
+        if (lane == 0) {
             constexpr uint32_t id_s = idesc_bf16(128, 64), id_pv = idesc_bf16_bmn(128, 32), id_y = idesc_bf16(128, C);
             const uint64_t d_wp = desc_kmajor_sw64(base + F::WP);
             // output-lane masks: every row but window A's / window B's
             const uint32_t mask_a[4] = {0u, 0u, ~0u, ~0u}, mask_b[4] = {~0u, ~0u, 0u, 0u};
-            const uint32_t t_r = tmem + F::T_R0 + 128 * grp;
-            const uint64_t dq = desc_kmajor_sw64(X(grp)), dk = desc_kmajor_sw64(K(grp));
-            const uint64_t dv = desc_mnmajor_sw64(V(grp), 8192);
-            // S of head hd into buffer r: all 128 q rows against each window's 64
-            // keys, each MMA keeping only its window's rows (G = 1: q from TMEM)
-            auto issue_s = [&](int hd, int r) {
+            const uint32_t t_r = tmem + F::T_R0 + 128 * grp, t_y = tmem + F::T_R0 + 128 * tg;
+            const uint64_t dq = desc_kmajor_sw64(X(tg)), dk = desc_kmajor_sw64(K(tg));
+            const uint64_t dv = desc_mnmajor_sw64(V(tg), 8192);
+            // S of the group's head hl into buffer r: all 128 q rows against each
+            // window's 64 keys, each MMA keeping only its window's rows (G = 1: q
+            // from TMEM)
+            auto issue_s = [&](int hl, int r) {
+                const int hd = h0 + hl;
                 const uint32_t d = t_r + 64 * r;
 #pragma unroll
                 for (int w = 0; w < 2; ++w)
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {
                         const uint64_t bk = desc_add(dk, hd * HT + 4096 * w + 32 * ks);
-                        if (F::Q_TMEM)
-                            mma_bf16_ts_mask(d, tmem + F::T_Q + 16 * hd + 8 * ks, bk, id_s, ks, w ? mask_b : mask_a);
+                        if (F::SPLIT)
+                            mma_bf16_ts_mask(d, tmem + F::T_QK + 32 * hd + 8 * ks, bk, id_s, ks, w ? mask_b : mask_a);
                         else
                             mma_bf16_mask(d, desc_add(dq, hd * HT + 32 * ks), bk, id_s, ks, w ? mask_b : mask_a);
                     }
@@ -521,7 +535,8 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             };
             // o_h = P v_h over each window's 64 keys, for its rows, into the upper
             // 32 columns of buffer r
-            auto issue_pv = [&](int hd, int r) {
+            auto issue_pv = [&](int hl, int r) {
+                const int hd = h0 + hl;
                 const uint32_t pa = t_r + 64 * r, d = t_r + 64 * r + 32;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
@@ -538,65 +553,71 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             uint32_t od_n[2] = {0u, 0u};
             bool ok = true;
             int p_tile = perm0;
-            for (int i = 0; i < grp; ++i) p_tile = perm_next(p_tile);
+            if (!F::SPLIT)
+                for (int i = 0; i < grp; ++i) p_tile = perm_next(p_tile);
 #pragma unroll 1
-            for (int j = grp; ok && j < my_tiles; j += G) {
+            for (int j = F::SPLIT ? 0 : grp; ok && j < my_tiles; j += G) {
                 const int kg = j / G;
-                // S of heads 0 and 1 as soon as their q and k are in shared memory
-                // (v, drained first, has then left the TMEM columns S takes)
+                // S of the group's first two heads as soon as their q and k are
+                // stored (v, drained first, has then left the TMEM columns S takes)
                 if (!(ok = wait_or_abort(QKR(grp, 0), kg & 1, st.wait_ns, abort_flag))) break;
                 tc_fence_after();
                 issue_s(0, 0);
-                if (HEADS > 1) {
+                if (F::HPG > 1) {
                     if (!(ok = wait_or_abort(QKR(grp, 1), kg & 1, st.wait_ns, abort_flag))) break;
                     tc_fence_after();
                     issue_s(1, 1);
                 }
-                if (HEADS <= 2) mma_commit(BAR(grp, BR_XFREE));   // the tile's last S has read q
+                if (F::HPG <= 2) mma_commit(BAR(tg, BR_XFREE));   // the group's last S has read q / k
 #pragma unroll 1
-                for (int hd = 0; hd < HEADS; ++hd) {
-                    const int r = hd & 1;
+                for (int hl = 0; hl < F::HPG; ++hl) {
+                    const int r = hl & 1;
                     if (!(ok = wait_or_abort(BAR(grp, BR_P + r), (ph_p >> r) & 1u, st.wait_ns, abort_flag))) break;
                     ph_p ^= 1u << r;
+                    // (G = 1: group 1's P.V reads the v that group 0 drains)
+                    if (F::SPLIT && grp == 1 && hl == 0 &&
+                        !(ok = wait_or_abort(QKR(0, 0), kg & 1, st.wait_ns, abort_flag)))
+                        break;
                     tc_fence_after();
-                    issue_pv(hd, r);
-                    if (hd + 2 < HEADS) {
-                        // S of head hd + 2 into buffer r once o_hd has left it
+                    issue_pv(hl, r);
+                    if (hl + 2 < F::HPG) {
+                        // S of head hl + 2 into buffer r once o_hl has left it
                         if (!(ok = wait_or_abort(BAR(grp, BR_OD + r), od_n[r] & 1u, st.wait_ns, abort_flag))) break;
-                        if (!(ok = wait_or_abort(QKR(grp, hd + 2), kg & 1, st.wait_ns, abort_flag))) break;
+                        if (!(ok = wait_or_abort(QKR(grp, hl + 2), kg & 1, st.wait_ns, abort_flag))) break;
                         tc_fence_after();
-                        issue_s(hd + 2, r);
-                        if (hd + 2 == HEADS - 1) mma_commit(BAR(grp, BR_XFREE));
+                        issue_s(hl + 2, r);
+                        if (hl + 2 == F::HPG - 1) mma_commit(BAR(tg, BR_XFREE));
                     }
                     ++od_n[r];
                 }
                 if (!ok) break;
-                // y = o Wproj^T into the group's columns once every o_h is staged
-                if (!(ok = wait_or_abort(BAR(grp, BR_O), kg & 1, st.wait_ns, abort_flag))) break;
+                if (F::SPLIT && grp == 1) continue;   // (tg's issuer: the projection and the stores)
+                // y = o Wproj^T into the tile's columns once every o_h is staged
+                if (!(ok = wait_or_abort(BAR(tg, BR_O), kg & 1, st.wait_ns, abort_flag))) break;
                 tc_fence_after();
-                const uint64_t doa = desc_kmajor_sw64(V(grp));
+                const uint64_t doa = desc_kmajor_sw64(V(tg));
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks)
-                        mma_bf16(t_r, desc_add(doa, kb * HT + 32 * ks), desc_add(d_wp, kb * (C * 64) + 32 * ks), id_y,
+                        mma_bf16(t_y, desc_add(doa, kb * HT + 32 * ks), desc_add(d_wp, kb * (C * 64) + 32 * ks), id_y,
                                  (kb | ks) != 0);
-                mma_commit(BAR(grp, BR_Y));
-                // tile j's output rows (staged in V(grp) by the compute warps) -> out
-                // through the window reverse + roll(+s) map; V(grp) may take the
-                // group's next v once the stores have read them
-                if (!(ok = wait_or_abort(BAR(grp, BR_STAGE), kg & 1, st.wait_ns, abort_flag))) break;
+                mma_commit(BAR(tg, BR_Y));
+                // tile j's output rows (staged in V(tg) by the compute warps) -> out
+                // through the window reverse + roll(+s) map; V(tg) may take the
+                // next v once the stores have read them
+                if (!(ok = wait_or_abort(BAR(tg, BR_STAGE), kg & 1, st.wait_ns, abort_flag))) break;
 #pragma unroll
                 for (int sl = 0; sl < 2; ++sl) {
                     const WinInfo w = window_info(g, p_tile, sl);
                     if (w.kind != 1) continue;
 #pragma unroll
                     for (int kb = 0; kb < KB; ++kb)
-                        tma_store_3d(&tmap_out, kb * 32, w.col0, w.img_row0, V(grp) + kb * HT + sl * (64 * 64));
+                        tma_store_3d(&tmap_out, kb * 32, w.col0, w.img_row0, V(tg) + kb * HT + sl * (64 * 64));
                 }
                 bulk_commit();
                 bulk_wait_read();
-                mbar_arrive(BAR(grp, BR_VFREE));
+                mbar_arrive(BAR(tg, BR_VFREE));
                 for (int i = 0; i < G; ++i) p_tile = perm_next(p_tile);
             }
             bulk_wait_all();
@@ -604,16 +625,21 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         }
     } else {
         // ===================== compute warps =====================
+        // (G = 1: group g takes heads [g HPG, (g + 1) HPG) of every tile, group 0
+        // also v, and each group half of y)
         const int grp = (warp - CWARP0) / GWARPS, quarter = warp & 3;
-        if (grp >= G) goto done;   // (G = 1: the second group's warps have no work)
+        const int tg = F::SPLIT ? 0 : grp;            // the tile's buffers and tile barriers
+        const int h0 = F::SPLIT ? grp * F::HPG : 0;   // the group's first head
+        constexpr int KBG = F::SPLIT ? KB / 2 : KB;   // y's 32-column blocks per group
+        const int kb0 = F::SPLIT ? grp * KBG : 0;
         const int row = quarter * 32 + lane;        // tile row = TMEM lane
         const int slot = row >> 6, t = row & 63;    // window slot; token (t >> 3, t & 7) of the row
         const int ti = t >> 3, tj = t & 7;
         const bool tok_row = ti < M && tj < M;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t t_r = t_lane + F::T_R0 + 128 * grp;
-        uint8_t *xg = sm + F::XT + grp * KB * HT, *vg = sm + F::VT + grp * KB * HT;
-        uint8_t *kgs = F::Q_TMEM ? xg : sm + F::KT + grp * KB * HT;
+        const uint32_t t_r = t_lane + F::T_R0 + 128 * grp, t_y = t_lane + F::T_R0 + 128 * tg;
+        uint8_t *xg = sm + F::XT + tg * KB * HT, *vg = sm + F::VT + tg * KB * HT;
+        uint8_t *kgs = F::SPLIT ? xg : sm + F::KT + tg * KB * HT;
         // relative-bias row of this token (rows no token fills read a valid row;
         // their results are never stored)
         const int bias_base = tok_row ? (ti + M - 1) * L + (tj + M - 1) : (M - 1) * L + (M - 1);
@@ -623,12 +649,13 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         float l0 = 1.f, l1 = 1.f;
         bool ok = true;
         int p_tile = perm0;
-        for (int i = 0; i < grp; ++i) p_tile = perm_next(p_tile);
+        if (!F::SPLIT)
+            for (int i = 0; i < grp; ++i) p_tile = perm_next(p_tile);
 #pragma unroll 1
-        for (int j = grp; j < my_tiles; j += G) {
+        for (int j = F::SPLIT ? 0 : grp; j < my_tiles; j += G) {
             const int kg = j / G;
             const WinInfo win = window_info(g, p_tile, slot);
-            if (!(ok = warp_wait(BAR(grp, BR_QKV), kg & 1, st.wait_ns, abort_flag))) break;
+            if (!(ok = warp_wait(BAR(tg, BR_QKV), kg & 1, st.wait_ns, abort_flag))) break;
             tc_fence_after();
 
             // ---- q and k of every head -> X(grp), K(grp) (bf16; V2: unit length),
@@ -664,23 +691,25 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             // length; V1 drops the key bias: it adds q.bk / sqrt(d) to every logit
             // of a row, which the softmax cancels; V2 normalises k + bk, so keeps
             // it), each head's S MMA issued as soon as its q and k are stored.
-            if (kg > 0 && !(ok = warp_wait(BAR(grp, BR_VFREE), (kg - 1) & 1, st.wait_ns, abort_flag))) break;
-            {
+            if (!F::SPLIT || grp == 0) {
+                if (kg > 0 && !(ok = warp_wait(BAR(tg, BR_VFREE), (kg - 1) & 1, st.wait_ns, abort_flag))) break;
                 float vv[HEADS][32];
 #pragma unroll
-                for (int hd = 0; hd < HEADS; ++hd) tmem_ld32(t_r + 32 * hd, vv[hd]);
+                for (int hd = 0; hd < HEADS; ++hd) tmem_ld32(t_y + 32 * hd, vv[hd]);
                 tmem_wait_ld();
 #pragma unroll
                 for (int hd = 0; hd < HEADS; ++hd) put(vv[hd], nullptr, vg + hd * HT, false);
             }
 #pragma unroll 1
-            for (int hd = 0; hd < HEADS; ++hd) {
+            for (int hl = 0; hl < F::HPG; ++hl) {
+                const int hd = h0 + hl;
                 float vq[32], vk[32];
                 tmem_ld32(t_lane + F::T_QK + 32 * hd, vq);
                 tmem_ld32(t_lane + F::T_QK + C + 32 * hd, vk);
                 tmem_wait_ld();
-                if (F::Q_TMEM) {
-                    // (G = 1) q back into TMEM as bf16 pairs, the A operand of S
+                if (F::SPLIT) {
+                    // (G = 1) q back into TMEM as bf16 pairs over its first 16 fp32
+                    // columns (this thread's lane, already read): the A operand of S
                     const float4 *b4 = reinterpret_cast<const float4 *>(sbqkv + 32 * hd);
 #pragma unroll
                     for (int e4 = 0; e4 < 8; ++e4) {
@@ -699,14 +728,14 @@ __global__ void __launch_bounds__(FTHREADS, 1)
                     uint32_t qp[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) qp[e] = pack_bf16x2(vq[2 * e], vq[2 * e + 1]);
-                    tmem_st16(t_lane + F::T_Q + 16 * hd, qp);
+                    tmem_st16(t_lane + F::T_QK + 32 * hd, qp);
                     tmem_wait_st();
                 } else {
                     put(vq, sbqkv + 32 * hd, xg + hd * HT, v2);
                 }
                 put(vk, v2 ? sbqkv + C + 32 * hd : nullptr, kgs + hd * HT, v2);
                 fence_proxy_async_smem();   // read by the S (and P.V) MMAs
-                warp_arrive(QKR(grp, hd), lane);
+                warp_arrive(QKR(grp, hl), lane);
             }
             warp_arrive(B_QKFREE, lane);   // the q|k columns may take the next QKV
 
@@ -723,17 +752,19 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             }
             // action i of a tile: the softmax of head a (a >= 0) or the o drain of
             // head -a - 1 (a < 0)
-            // (after softmax 0 and 1: drain h, softmax h + 2 while h + 2 < HEADS,
-            // then the last two drains; three heads: S0 S1 D0 S2 D1 D2)
+            // (the group's heads hl: after softmax 0 and 1, drain h and softmax
+            // h + 2 while h + 2 < HPG, then the last two drains; three heads: S0
+            // S1 D0 S2 D1 D2)
             auto head_action = [](int i) -> int {
+                constexpr int NH = F::HPG;
                 if (i < 2) return i;
                 const int k = i - 2;
-                if (k < 2 * (HEADS - 2)) return (k & 1) ? (k >> 1) + 2 : -(k >> 1) - 1;
-                return -(HEADS - 2 + k - 2 * (HEADS - 2)) - 1;
+                if (k < 2 * (NH - 2)) return (k & 1) ? (k >> 1) + 2 : -(k >> 1) - 1;
+                return -(NH - 2 + k - 2 * (NH - 2)) - 1;
             };
             // ---- softmax of head hd (buffer hd & 1) over the row's window keys ----
-            auto softmax = [&](int hd) -> bool {
-                const int r = hd & 1;
+            auto softmax = [&](int hl) -> bool {
+                const int r = hl & 1, hd = h0 + hl;
                 if (!warp_wait(BAR(grp, BR_S + r), (ph_s >> r) & 1u, st.wait_ns, abort_flag)) return false;
                 ph_s ^= 1u << r;
                 tc_fence_after();
@@ -810,8 +841,8 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             };
             // ---- o_h / rowsum -> bf16 -> head hd's tile of V(grp) (the
             // projection's A operand), once P.V has read v_h ----
-            auto drain_o = [&](int hd) -> bool {
-                const int r = hd & 1;
+            auto drain_o = [&](int hl) -> bool {
+                const int r = hl & 1, hd = h0 + hl;
                 if (!warp_wait(BAR(grp, BR_PV + r), (ph_pv >> r) & 1u, st.wait_ns, abort_flag)) return false;
                 ph_pv ^= 1u << r;
                 tc_fence_after();
@@ -832,29 +863,30 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             // 0, softmax 2, drain 1, 2 (one rolled loop: one copy of each body,
             // which keeps the kernel's code within the instruction caches)
 #pragma unroll 1
-            for (int i = 0; i < 2 * HEADS; ++i) {
-                const int hd = head_action(i);
-                if (!(ok = hd >= 0 ? softmax(hd) : drain_o(-hd - 1))) break;
+            for (int i = 0; i < 2 * F::HPG; ++i) {
+                const int hl = head_action(i);
+                if (!(ok = hl >= 0 ? softmax(hl) : drain_o(-hl - 1))) break;
             }
             if (!ok) break;
             fence_proxy_async_smem();   // o is read by the projection MMA
-            warp_arrive(BAR(grp, BR_O), lane);
+            warp_arrive(BAR(tg, BR_O), lane);
 
             // ---- y + bproj -> bf16 rows in V(grp), token (ti, tj) of a window at
             // row M*ti + tj of its half (one dense box per window for the TMA
             // store through the window reverse + roll(+s) map); the rows of
             // windows that wrap go straight to out ----
-            if (!(ok = warp_wait(BAR(grp, BR_Y), kg & 1, st.wait_ns, abort_flag))) break;
+            if (!(ok = warp_wait(BAR(tg, BR_Y), kg & 1, st.wait_ns, abort_flag))) break;
             tc_fence_after();
             {
-                float y[KB][32];
+                // y's 32-column blocks kb0 + kb, kb < KBG
+                float y[KBG][32];
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb) tmem_ld32(t_r + 32 * kb, y[kb]);
+                for (int kb = 0; kb < KBG; ++kb) tmem_ld32(t_y + 32 * (kb0 + kb), y[kb]);
                 tmem_wait_ld();
-                warp_arrive(BAR(grp, BR_RFREE), lane);   // the group's TMEM columns are free
+                warp_arrive(BAR(tg, BR_RFREE), lane);   // the tile's TMEM columns are free
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb) {
-                    const float4 *bp = reinterpret_cast<const float4 *>(sbproj + 32 * kb);
+                for (int kb = 0; kb < KBG; ++kb) {
+                    const float4 *bp = reinterpret_cast<const float4 *>(sbproj + 32 * (kb0 + kb));
 #pragma unroll
                     for (int e4 = 0; e4 < 8; ++e4) {
                         const float4 bb = bp[e4];
@@ -866,26 +898,26 @@ __global__ void __launch_bounds__(FTHREADS, 1)
                     if (tok_row) {
                         uint4 *dst = reinterpret_cast<uint4 *>(a.out + (int64_t)window_token(g, win, ti, tj) * C);
 #pragma unroll
-                        for (int kb = 0; kb < KB; ++kb)
+                        for (int kb = 0; kb < KBG; ++kb)
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) dst[4 * kb + c] = pack8(y[kb] + 8 * c);
+                            for (int c = 0; c < 4; ++c) dst[4 * (kb0 + kb) + c] = pack8(y[kb] + 8 * c);
                     }
                 } else if (win.kind == 1 && tok_row) {
                     const int srow = slot * 64 + ti * M + tj;
 #pragma unroll
-                    for (int kb = 0; kb < KB; ++kb)
+                    for (int kb = 0; kb < KBG; ++kb)
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
-                            *reinterpret_cast<uint4 *>(vg + kb * HT + sw64_offset(srow, c)) = pack8(y[kb] + 8 * c);
+                            *reinterpret_cast<uint4 *>(vg + (kb0 + kb) * HT + sw64_offset(srow, c)) =
+                                pack8(y[kb] + 8 * c);
                 }
             }
             fence_proxy_async_smem();   // the TMA stores read these rows
-            warp_arrive(BAR(grp, BR_STAGE), lane);
+            warp_arrive(BAR(tg, BR_STAGE), lane);
             for (int i = 0; i < G; ++i) p_tile = perm_next(p_tile);
         }
         if (!ok) *abort_flag = 1;
     }
-done:
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && *abort_flag) atomicOr(st.err, ERR_TIMEOUT);
