@@ -326,9 +326,17 @@ def _run_block(w, g, table, ratio=4):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("key,B,H,W", [("swin_t_s1", 2, 14, 21), ("swinv2_t_s1", 1, 16, 24), ("swin_t_s1", 1, 7, 7),
-                                       ("swin_b_s1", 1, 14, 14)])
+                                       ("swin_b_s1", 1, 14, 14), ("swin_b_s1", 8, 56, 56), ("swin_b_s3", 2, 14, 14),
+                                       ("swinv2_b_s1", 2, 16, 24)])
 def test_block_forward_small(key, B, H, W):
-    w = WORKLOADS[key].with_(B=B, H=H, W=W)
+    """Grids of one to two tiles per CTA.  Where the attention is the fused
+    kernel (C = 64, 96, 128 with windows of 7 or 8) the block folds LayerNorm 1
+    and the first residual into it; V2 at C = 128 and the C = 512 stage take
+    the separate LayerNorm kernel."""
+    if key == "swinv2_b_s1":   # V2 at C = 128, four heads
+        w = WORKLOADS["swinv2_t_s1"].with_(B=B, H=H, W=W, C=128, heads=4)
+    else:
+        w = WORKLOADS[key].with_(B=B, H=H, W=W)
     g = generate_block(w)
     table = oracle_table(w, g)
     got = _run_block(w, g, table)

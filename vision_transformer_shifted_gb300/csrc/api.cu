@@ -213,6 +213,38 @@ int enqueue_host_chunks(swin_wattn_s *h, const void *x_host, int B, int H, int W
 
 } // namespace
 
+namespace swin {
+
+// The transformer block's use of the fused path with its LayerNorm (ln_g,
+// ln_b) and residual folded in (fold 1: V1 pre-norm, 2: V2 post-norm; see
+// launch_fused).  EUNSUPPORTED where this handle's forward would not take the
+// fused path for the grid, or the fold does not apply to it.
+int attn_forward_folded(swin_wattn_t h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
+                        const void *bias_table, const float *logit_scale, const void *Wproj, const void *bproj,
+                        const void *ln_g, const void *ln_b, int fold, void *out, cudaStream_t stream)
+{
+    int rc = check_forward_args(h, x, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out, true);
+    if (rc) return rc;
+    if (!ln_g || !ln_b) return SWIN_WATTN_EINVAL;
+    const Geom g = make_geom(B, H, W, h->C, h->M, h->shift);
+    const int path = h->fp32 ? 3 : h->path_opt ? h->path_opt : choose_path(h, g.T);
+    if (path != 2 || g.T >= ((int64_t)1 << 31) || !fused_fold_supported(h->M, h->C, h->heads, fold))
+        return SWIN_WATTN_EUNSUPPORTED;
+    h->last_launches = 0;
+    if (B == 0) return SWIN_WATTN_OK;
+    cudaError_t e = launch_fused((const bf16 *)x, (const bf16 *)Wqkv, (const bf16 *)bqkv, (const bf16 *)bias_table,
+                                 logit_scale, (const bf16 *)Wproj, (const bf16 *)bproj, (bf16 *)out, h->mode, g,
+                                 dstatus(h), stream, (const bf16 *)ln_g, (const bf16 *)ln_b, fold);
+    if (e != cudaSuccess) {
+        h->last_cuda_error = e;
+        return SWIN_WATTN_ECUDA;
+    }
+    h->last_launches = 1;
+    return SWIN_WATTN_OK;
+}
+
+} // namespace swin
+
 extern "C" {
 
 int swin_wattn_create(swin_wattn_t *out, int C, int heads, int M, int shift, int mode)
@@ -276,6 +308,7 @@ int swin_wattn_forward(swin_wattn_t h, const void *x, int B, int H, int W, const
     if (rc) return rc;
     return ws_check(h->ws, (cudaStream_t)stream);
 }
+
 
 int swin_wattn_forward_host(swin_wattn_t h, const void *x_host, int B, int H, int W, const void *Wqkv,
                             const void *bqkv, const void *bias_table, const float *logit_scale, const void *Wproj,

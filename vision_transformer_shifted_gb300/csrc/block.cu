@@ -6,7 +6,9 @@
 // Steps: the swin_wattn forward for attn; one LayerNorm kernel that also
 // does the residual add (add-then-normalise for V1, normalise-then-add for
 // V2); the MLP as two tcgen05 GEMMs whose epilogues apply GELU and the
-// residual add.
+// residual add.  Where the attention is the fused kernel, LayerNorm 1 and
+// the first residual are folded into it (its x tiles' prologue, V1; its
+// output rows' epilogue, V2) and z is its output.
 #include <cmath>
 #include <new>
 
@@ -288,7 +290,28 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
     const bf16 *g2 = (const bf16 *)p->ln2_gamma, *be2 = (const bf16 *)p->ln2_beta;
     int rc;
     cudaError_t e;
-    if ((h->mode & 0xf) == SWIN_WATTN_V1) {
+    // Where the attention runs as the fused kernel, LayerNorm 1 and the first
+    // residual go into it (V1: LN of its x tiles before the QKV MMAs, x added
+    // to its output rows; V2: LN of its output rows, then x added), and z
+    // comes straight out of it.
+    const bool v1 = (h->mode & 0xf) == SWIN_WATTN_V1;
+    rc = attn_forward_folded(h->attn, x, B, H, W, p->Wqkv, p->bqkv, p->bias_table, p->logit_scale, p->Wproj, p->bproj,
+                             g1, be1, v1 ? 1 : 2, z, s);
+    if (rc == SWIN_WATTN_OK) {
+        if (v1) {
+            if ((e = launch_layernorm(z, nullptr, g2, be2, nullptr, t1, T, C, 0, s)) != cudaSuccess)
+                return cuda_status(e);
+            if ((e = gemm(t1, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return cuda_status(e);
+            if ((e = gemm(m1, R, p->W2, p->b2, yy, C, EPI_RESID, z)) != cudaSuccess) return cuda_status(e);
+        } else {
+            if ((e = gemm(z, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return cuda_status(e);
+            if ((e = gemm(m1, R, p->W2, p->b2, t1, C, EPI_NONE, nullptr)) != cudaSuccess) return cuda_status(e);
+            if ((e = launch_layernorm(t1, z, g2, be2, nullptr, yy, T, C, 2, s)) != cudaSuccess) return cuda_status(e);
+        }
+        return ws_check(h->ws, s);
+    }
+    if (rc != SWIN_WATTN_EUNSUPPORTED) return rc;
+    if (v1) {
         if ((e = launch_layernorm(xx, nullptr, g1, be1, nullptr, t1, T, C, 0, s)) != cudaSuccess) return cuda_status(e);
         rc = swin_wattn_forward(h->attn, t1, B, H, W, p->Wqkv, p->bqkv, p->bias_table, p->logit_scale, p->Wproj,
                                 p->bproj, t2, stream);

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+struct swin_wattn_s;   // a forward handle (swin_wattn.h)
+
 namespace swin {
 
 using bf16 = __nv_bfloat16;
@@ -191,9 +193,18 @@ size_t fp32_block_smem_bytes(int N, int C);
 
 // The whole block in one persistent kernel (windows of <= 64 tokens, C = 64, 96 or 128).
 bool fused_supported(int M, int C, int heads);
+// With the transformer block's LayerNorm (gamma ln_g, beta ln_b) and residual
+// folded in: fold 1 = pre-norm (V1), out = x + attn(LN(x)); 2 = residual
+// post-norm (V2), out = x + LN(attn(x)); 0 = attn(x) alone.
+bool fused_fold_supported(int M, int C, int heads, int fold);
+// The same through a forward handle (its path choice, status word and wait
+// limit); SWIN_WATTN_EUNSUPPORTED where that handle would not fuse the grid.
+int attn_forward_folded(::swin_wattn_s *h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
+                        const void *bias_table, const float *logit_scale, const void *Wproj, const void *bproj,
+                        const void *ln_g, const void *ln_b, int fold, void *out, cudaStream_t stream);
 cudaError_t launch_fused(const bf16 *x, const bf16 *Wqkv, const bf16 *bqkv, const bf16 *table, const float *tau,
                          const bf16 *Wproj, const bf16 *bproj, bf16 *out, int mode, const Geom &g, DeviceStatus st,
-                         cudaStream_t stream);
+                         cudaStream_t stream, const bf16 *ln_g = nullptr, const bf16 *ln_b = nullptr, int fold = 0);
 
 // Tensor map over a row-major bf16 matrix [rows, cols] (16-byte aligned base,
 // cols * 2 a multiple of 16): boxes of 32 columns x box_rows rows (<= 256),
