@@ -45,7 +45,10 @@ L2_BYTES = 129 * 1024 * 1024
 # on: reported only while the source is unchanged.
 PROFILED_TRAFFIC = {
     ("swin_t_s1", "window_attention"): (133.61e6, "backward.cu", "a69d4d4c668c"),
-    ("swin_t_s1", "fused_block"): (40.14e6, "fused_block.cu", "e6782dbcb753"),
+    ("swin_t_s1", "fused_block"): (40.10e6, "fused_block.cuh", "fe815e14a9f0"),
+    ("swin_b_s1", "fused_block"): (60.28e6, "fused_block.cuh", "fe815e14a9f0"),
+    ("swinv2_t_s1", "fused_block"): (59.92e6, "fused_block.cuh", "fe815e14a9f0"),
+    ("swinv2_l_w24", "window_attention"): (896.00e6, "attn_window.cu", "57e8522dd245"),
 }
 
 
@@ -501,6 +504,7 @@ def run_block(args, w, ratio=4):
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     assert sw.swin_block_sync_status(h, stream) == sw.OK
+    launches = sw.swin_block_last_launches(h)
     sw.swin_block_destroy(h)
     T, C = w.tokens, w.C
     flops = w.flops + 4 * T * C * ratio * C
@@ -518,7 +522,7 @@ def run_block(args, w, ratio=4):
             "block_roofline": {"achieved_tflops": tflops, "roof_tflops": roof_tf, "frac": tflops / roof_tf,
                                "ai_flop_per_byte": ai, "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
                                "peak_source": pk["source"] + " (sustained bf16 / copy GB/s)"},
-            "clocks": clk.summary()}
+            "gpu_launches": launches * args.steps, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
 
@@ -580,6 +584,9 @@ def run_stage(args, w, depth, ratio=4):
         e1.record(stream)
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
+    # per step: each block's launches, the extra LayerNorms, the merging step (LayerNorm + GEMM)
+    launches = sum(sw.swin_block_last_launches(h) for h, _p, _x in blocks) + 2
+    launches += (len(blocks) // args.extra_norm) if args.extra_norm else 0
     for h, _p, _x in blocks:
         assert sw.swin_block_sync_status(h, stream) == sw.OK
         sw.swin_block_destroy(h)
@@ -592,7 +599,7 @@ def run_stage(args, w, depth, ratio=4):
                        "mode": "V1 pre-norm" if w.mode == V1 else "V2 residual post-norm",
                        "mlp_ratio": ratio, "l2": "not flushed: one input set (the stage's own intermediates, "
                        "%.0f MB per block, exceed L2)" % (w.tokens * w.C * (3 + ratio) * 2 / 1e6)},
-            "clocks": clk.summary()}
+            "gpu_launches": launches * args.steps, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
 def run_backward(args, w):

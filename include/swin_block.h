@@ -72,6 +72,12 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
  * since the last call (SWIN_WATTN_ETIMEOUT), else SWIN_WATTN_OK. */
 int swin_block_sync_status(swin_block_t h, swin_stream_t stream);
 
+/* Number of kernel launches the last swin_block_forward on this handle
+ * enqueued (4 where the attention runs as the fused kernel with LayerNorm 1
+ * and the residual folded in; more on the three-kernel path); 0 before the
+ * first forward or after one that failed its checks, -1 for a NULL handle. */
+int swin_block_last_launches(swin_block_t h);
+
 /* Frees the handle and its workspace (NULL is a no-op). */
 int swin_block_destroy(swin_block_t h);
 

@@ -345,6 +345,31 @@ def test_block_forward_small(key, B, H, W):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("key,C,heads,folded", [("swin_t_s1", 96, 3, True), ("swinv2_t_s1", 96, 3, True),
+                                                ("swin_b_s1", 128, 4, True), ("swinv2_t_s1", 128, 4, False),
+                                                ("swin_b_s3", 512, 16, False)])
+def test_block_launches_show_the_fold(key, C, heads, folded):
+    """Where the attention is the fused kernel, LayerNorm 1 and the first
+    residual are inside it: four launches (attention, LayerNorm 2, two MLP
+    GEMMs); elsewhere the separate LayerNorm pass and the attention's own."""
+    w = WORKLOADS[key].with_(B=1, H=2 * WORKLOADS[key].M, W=2 * WORKLOADS[key].M, C=C, heads=heads)
+    g = generate_block(w)
+    table = oracle_table(w, g)
+    dev = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in _block_params_dev(g, table).items()}
+    x = g["x"].to(DEV)
+    out = torch.empty_like(x)
+    h = sw.swin_block_create(w.C, w.heads, w.M, w.shift, w.mode, 4)
+    try:
+        assert sw.swin_block_last_launches(h) == 0
+        sw.swin_block_forward(h, x, dev, out)
+        sw.swin_block_sync_status(h)
+        n = sw.swin_block_last_launches(h)
+    finally:
+        sw.swin_block_destroy(h)
+    assert (n == 4) if folded else (n >= 5), n
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("key", ["swin_t_s1", "swinv2_t_s1"])
 def test_block_forward_full_size(key):
     """Full-size grid, every output element against the block oracle."""

@@ -54,6 +54,7 @@ _SIGNATURES = {
     "swin_block_forward": ["p", "p", "i", "i", "i", "p", "p", "p"],
     "swin_block_sync_status": ["p", "p"],
     "swin_block_destroy": ["p"],
+    "swin_block_last_launches": ["p"],
     "swin_block_test_layernorm": ["p", "p", "p", "p", "p", "p", "i", "i", "i", "p"],
     "swin_stage_norm": ["p", "i", "i", "p", "p", "p", "p"],
     "swin_merge_create": ["pp", "i"],
@@ -269,6 +270,10 @@ def swin_block_forward(h, x, params, out, stream=None):
                        for n in BLOCK_PARAM_FIELDS])
     return _check("swin_block_forward", load().swin_block_forward(
         h, _p(x), B, H, W, ctypes.cast(ctypes.byref(bp), ctypes.c_void_p), _p(out), _stream(stream)))
+
+
+def swin_block_last_launches(h):
+    return load().swin_block_last_launches(h)
 
 
 def swin_block_sync_status(h, stream=None):

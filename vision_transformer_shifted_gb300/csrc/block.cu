@@ -180,6 +180,7 @@ struct swin_block_s {
     int *d_err;
     void *ws;   // z, t1, t2 [T, C] and m1 [T, rC], bf16
     size_t ws_bytes;
+    int last_launches;   // of the last forward
 };
 
 extern "C" {
@@ -214,6 +215,8 @@ int swin_block_create(swin_block_t *out, int C, int heads, int M, int shift, int
     *out = h;
     return SWIN_WATTN_OK;
 }
+
+int swin_block_last_launches(swin_block_t h) { return h ? h->last_launches : -1; }
 
 int swin_block_destroy(swin_block_t h)
 {
@@ -258,6 +261,7 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
         const int64_t bytes = T * C * 2;
         if (xb < ob + bytes && ob < xb + bytes) return SWIN_WATTN_EINVAL;
     }
+    h->last_launches = 0;
     if (B == 0) return SWIN_WATTN_OK;
     const size_t need = (size_t)T * (3 * C + R) * 2;
     int wrc = ws_ensure(&h->ws, &h->ws_bytes, need);
@@ -298,6 +302,7 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
     rc = attn_forward_folded(h->attn, x, B, H, W, p->Wqkv, p->bqkv, p->bias_table, p->logit_scale, p->Wproj, p->bproj,
                              g1, be1, v1 ? 1 : 2, z, s);
     if (rc == SWIN_WATTN_OK) {
+        h->last_launches = 1 + 3;   // the folded attention; LayerNorm 2 and the two MLP GEMMs
         if (v1) {
             if ((e = launch_layernorm(z, nullptr, g2, be2, nullptr, t1, T, C, 0, s)) != cudaSuccess)
                 return cuda_status(e);
@@ -311,11 +316,13 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
         return ws_check(h->ws, s);
     }
     if (rc != SWIN_WATTN_EUNSUPPORTED) return rc;
+    h->last_launches = 4;   // two LayerNorm passes and the two MLP GEMMs, plus the attention's (below)
     if (v1) {
         if ((e = launch_layernorm(xx, nullptr, g1, be1, nullptr, t1, T, C, 0, s)) != cudaSuccess) return cuda_status(e);
         rc = swin_wattn_forward(h->attn, t1, B, H, W, p->Wqkv, p->bqkv, p->bias_table, p->logit_scale, p->Wproj,
                                 p->bproj, t2, stream);
         if (rc != SWIN_WATTN_OK) return rc;
+        h->last_launches += swin_wattn_last_launches(h->attn);
         if ((e = launch_layernorm(t2, xx, g2, be2, z, t1, T, C, 1, s)) != cudaSuccess) return cuda_status(e);
         if ((e = gemm(t1, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return cuda_status(e);
         if ((e = gemm(m1, R, p->W2, p->b2, yy, C, EPI_RESID, z)) != cudaSuccess) return cuda_status(e);
@@ -323,6 +330,7 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
         rc = swin_wattn_forward(h->attn, x, B, H, W, p->Wqkv, p->bqkv, p->bias_table, p->logit_scale, p->Wproj,
                                 p->bproj, t2, stream);
         if (rc != SWIN_WATTN_OK) return rc;
+        h->last_launches += swin_wattn_last_launches(h->attn);
         if ((e = launch_layernorm(t2, xx, g1, be1, nullptr, z, T, C, 2, s)) != cudaSuccess) return cuda_status(e);
         if ((e = gemm(z, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return cuda_status(e);
         if ((e = gemm(m1, R, p->W2, p->b2, t1, C, EPI_NONE, nullptr)) != cudaSuccess) return cuda_status(e);
