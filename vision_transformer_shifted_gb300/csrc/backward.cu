@@ -42,50 +42,6 @@ __global__ void transpose_kernel(const bf16 *in, bf16 *out, int rows, int cols)
     }
 }
 
-// out[n] += sum over rows of in[row, n] in fp32.  A thread owns one 16-byte
-// chunk (8 columns) and a row offset, so that a CTA reads whole rows with
-// coalesced 16-byte loads; the row offsets' partial sums meet in shared
-// memory and leave with one atomic add per column and CTA.
-__global__ void colsum_kernel(const bf16 *in, int64_t rows, int N, float *out)
-{
-    extern __shared__ float part[]; // [rows per iteration][N]
-    const int cpr = N / 8, rpi = blockDim.x / cpr;
-    const int c = threadIdx.x % cpr, rr = threadIdx.x / cpr;
-    float acc[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-    if (rr < rpi) {
-        const int64_t step = (int64_t)gridDim.x * rpi;
-        int64_t r = (int64_t)blockIdx.x * rpi + rr;
-        auto add = [&](const uint4 &u) {
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 f = unpack_bf16x2(w[k]);
-                acc[2 * k] += f.x;
-                acc[2 * k + 1] += f.y;
-            }
-        };
-        // four rows per round, their loads issued together
-        for (; r + 3 * step < rows; r += 4 * step) {
-            uint4 u[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) u[q] = *reinterpret_cast<const uint4 *>(in + (r + q * step) * N + c * 8);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) add(u[q]);
-        }
-        for (; r < rows; r += step) add(*reinterpret_cast<const uint4 *>(in + r * N + c * 8));
-#pragma unroll
-        for (int k = 0; k < 8; ++k) part[rr * N + c * 8 + k] = acc[k];
-    }
-    __syncthreads();
-    for (int n = threadIdx.x; n < N; n += blockDim.x) {
-        float s = 0.f;
-        for (int q = 0; q < rpi; ++q) s += part[q * N + n];
-        atomicAdd(&out[n], s);
-    }
-}
-
 // ---- attention backward on the tensor cores ------------------------------------
 //
 // A unit is one head of two consecutive windows, stacked into 128 rows (window
@@ -511,17 +467,6 @@ cudaError_t launch_transpose(const bf16 *in, bf16 *out, int rows, int cols, cuda
 {
     dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32)), block(32, 8);
     transpose_kernel<<<grid, block, 0, stream>>>(in, out, rows, cols);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_colsum(const bf16 *in, int64_t rows, int N, float *out, cudaStream_t stream)
-{
-    if (N <= 0 || N % 8 || N > 8 * 256) return cudaErrorInvalidValue;
-    if (rows <= 0) return cudaSuccess;
-    const int threads = 256, rpi = threads / (N / 8);
-    const int64_t want = (rows + rpi - 1) / rpi;
-    const unsigned grid = (unsigned)(want < 152 * 8 ? want : 152 * 8);
-    colsum_kernel<<<grid, threads, (size_t)rpi * N * 4, stream>>>(in, rows, N, out);
     return cudaGetLastError();
 }
 

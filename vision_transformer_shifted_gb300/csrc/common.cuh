@@ -244,8 +244,6 @@ cudaError_t launch_wgrad(const bf16 *G, int n_out, const bf16 *X, int n_in, int6
                          float *workspace, DeviceStatus st, cudaStream_t stream);
 // out [cols, rows] = in [rows, cols]^T.
 cudaError_t launch_transpose(const bf16 *in, bf16 *out, int rows, int cols, cudaStream_t stream);
-// out[n] += sum over rows of in[row, n] (fp32; N a multiple of 8, <= 2048).
-cudaError_t launch_colsum(const bf16 *in, int64_t rows, int N, float *out, cudaStream_t stream);
 // Windows of <= 64 tokens and 32 channels per head.
 bool attn_backward_supported(int M, int C, int heads);
 // From qkv [T, 3C] and do [T, C] (window order): the attention output
