@@ -102,7 +102,7 @@ int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void 
         if (!fused_supported(h->M, h->C, h->heads) || g.T >= ((int64_t)1 << 31)) return SWIN_WATTN_EUNSUPPORTED;
         cudaError_t e = launch_fused((const bf16 *)x, (const bf16 *)Wqkv, (const bf16 *)bqkv, (const bf16 *)table, tau,
                                      (const bf16 *)Wproj, (const bf16 *)bproj, (bf16 *)out, h->mode, g, dstatus(h),
-                                     stream);
+                                     h->d_err + 2, stream);
         if (e != cudaSuccess) {
             h->last_cuda_error = e;
             return SWIN_WATTN_ECUDA;
@@ -234,7 +234,7 @@ int attn_forward_folded(swin_wattn_t h, const void *x, int B, int H, int W, cons
     if (B == 0) return SWIN_WATTN_OK;
     cudaError_t e = launch_fused((const bf16 *)x, (const bf16 *)Wqkv, (const bf16 *)bqkv, (const bf16 *)bias_table,
                                  logit_scale, (const bf16 *)Wproj, (const bf16 *)bproj, (bf16 *)out, h->mode, g,
-                                 dstatus(h), stream, (const bf16 *)ln_g, (const bf16 *)ln_b, fold);
+                                 dstatus(h), h->d_err + 2, stream, (const bf16 *)ln_g, (const bf16 *)ln_b, fold);
     if (e != cudaSuccess) {
         h->last_cuda_error = e;
         return SWIN_WATTN_ECUDA;
@@ -267,8 +267,9 @@ int swin_wattn_create(swin_wattn_t *out, int C, int heads, int M, int shift, int
     h->host_chunks = 8;
     h->wait_ns = 2000000000ull;
     if (cudaGetDevice(&h->device) != cudaSuccess) { delete h; cudaGetLastError(); return SWIN_WATTN_ECUDA; }
-    if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess) { delete h; cudaGetLastError(); return SWIN_WATTN_ENOMEM; }
-    if (cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess) { cudaFree(h->d_err); delete h; return SWIN_WATTN_ECUDA; }
+    // [0] the error word, [2..3] the fused kernel's tile counter and CTAs done
+    if (cudaMalloc(&h->d_err, 4 * sizeof(int)) != cudaSuccess) { delete h; cudaGetLastError(); return SWIN_WATTN_ENOMEM; }
+    if (cudaMemset(h->d_err, 0, 4 * sizeof(int)) != cudaSuccess) { cudaFree(h->d_err); delete h; return SWIN_WATTN_ECUDA; }
     *out = h;
     return SWIN_WATTN_OK;
 }

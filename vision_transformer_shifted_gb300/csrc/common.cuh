@@ -202,9 +202,12 @@ bool fused_fold_supported(int M, int C, int heads, int fold);
 int attn_forward_folded(::swin_wattn_s *h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
                         const void *bias_table, const float *logit_scale, const void *Wproj, const void *bproj,
                         const void *ln_g, const void *ln_b, int fold, void *out, cudaStream_t stream);
+// sched: two device ints, zero before the first launch (the kernel's tile
+// counter; each launch leaves them zero); one launch at a time per pair.
 cudaError_t launch_fused(const bf16 *x, const bf16 *Wqkv, const bf16 *bqkv, const bf16 *table, const float *tau,
                          const bf16 *Wproj, const bf16 *bproj, bf16 *out, int mode, const Geom &g, DeviceStatus st,
-                         cudaStream_t stream, const bf16 *ln_g = nullptr, const bf16 *ln_b = nullptr, int fold = 0);
+                         int *sched, cudaStream_t stream, const bf16 *ln_g = nullptr, const bf16 *ln_b = nullptr,
+                         int fold = 0);
 
 // Tensor map over a row-major bf16 matrix [rows, cols] (16-byte aligned base,
 // cols * 2 a multiple of 16): boxes of 32 columns x box_rows rows (<= 256),

@@ -74,8 +74,7 @@ struct FusedArgs {
     bf16 *out;
     int mode;
     Geom g;
-    int64_t tile_mul;   // tile visiting order: j * tile_mul mod ntiles (coprime to ntiles) ...
-    int perm_step;      // ... and gridDim.x * tile_mul mod ntiles
+    int *sched;         // [2] zero before the launch: next tile to hand out, CTAs done
     // The transformer block's LayerNorm and residual folded in: fold 0 = the
     // attention output alone; 1 = pre-norm (V1): attention of LN(x), out =
     // x + that; 2 = residual post-norm (V2): out = x + LN(attention of x).
@@ -131,7 +130,8 @@ struct FusedCfg {
     static constexpr int O_BIAS = O_REF + 16;                 // [HEADS][L][LP] f32, times log2(e)
     static constexpr int O_LN = (O_BIAS + HEADS * L * LP * 4 + 15) / 16 * 16;   // [2][C] f32: LayerNorm gamma, beta
     static constexpr int O_CSUM = O_LN + 2 * C * 4;           // [3C] f32: column sums of the scaled Wqkv
-    static constexpr int O_BARS = O_CSUM + 3 * C * 4;
+    static constexpr int O_RING = O_CSUM + 3 * C * 4;         // [4] int: tile of the CTA's j-th tile (j mod 4)
+    static constexpr int O_BARS = O_RING + 16;
     static constexpr int NBARS = 2 * 21 + 1;
     static constexpr int O_END = O_BARS + NBARS * 8 + 16;
     static constexpr int BYTES = SMALL + O_END;
@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     float *sbias = reinterpret_cast<float *>(small + F::O_BIAS);
     float *sln = reinterpret_cast<float *>(small + F::O_LN);
     float *scsum = reinterpret_cast<float *>(small + F::O_CSUM);
+    volatile int *sring = reinterpret_cast<volatile int *>(small + F::O_RING);
     uint64_t *bars = reinterpret_cast<uint64_t *>(small + F::O_BARS);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + F::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
@@ -317,8 +318,6 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     auto QKR = [&](int grp, int h) { return BAR(grp, h == 0 ? BR_QKR : BR_QKR1 + h - 1); };
     const uint32_t B_QKFREE = smem_u32(&bars[BR_QKFREE]);
     const int ntiles = (int)((g.nwin + 1) / 2);
-    // this CTA's tiles: j = 0, 1, ... while blockIdx.x + j * gridDim.x < ntiles
-    const int my_tiles = ntiles > (int)blockIdx.x ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     auto X = [&](int grp) { return base + F::XT + grp * KB * HT; };
     auto K = [&](int grp) { return F::SPLIT ? base + F::XT : base + F::KT + grp * KB * HT; };
     auto V = [&](int grp) { return base + F::VT + grp * KB * HT; };
@@ -502,16 +501,15 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // Tiles are visited in a permuted order: the CTA's j-th tile is
-    // (blockIdx.x + j*gridDim.x) * tile_mul mod ntiles, tile_mul coprime to
-    // ntiles, so that every CTA gets its share of the windows on the shifted
-    // edges (those cost the producer and the masked softmax more).
-    const int perm0 = (int)(((unsigned long long)blockIdx.x * (unsigned long long)a.tile_mul) %
-                            (unsigned long long)ntiles);
-    auto perm_next = [&](int p) {
-        p += a.perm_step;
-        return p >= ntiles ? p - ntiles : p;
-    };
+    // Tiles are handed out at run time: the producer takes the next one from
+    // a counter shared by the CTAs (windows on the shifted edges cost more, so
+    // a fixed share per CTA left some CTAs running 20% longer than others)
+    // and writes the CTA's j-th tile into ring slot j mod 4 before its first
+    // arrival on BR_X; once the tiles run out it writes -1 into the next G
+    // slots and completes their BR_X phases without loads.  Every other role
+    // reads the slot after its wait on BR_X of tile j, and leaves at -1.  A
+    // slot is written again four tiles later, after XFREE of tile j + 4 - G,
+    // which every reader of tile j has passed by then.
 
     if (warp == PWARP) {
         // ===================== producer warp: x gathers =====================
@@ -564,15 +562,31 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             if (lane == 0) mbar_arrive(BAR(grp, BR_X));
         };
         bool ok = true;
-        int p_load = perm0;
+        int ends = 0;   // end marks written
 #pragma unroll 1
-        for (int j = 0; j < my_tiles; ++j) {
+        for (int j = 0; ends < G; ++j) {
             const int grp = j % G, kg = j / G;
             // X(grp) takes tile j once the group's S MMAs of its previous tile have
             // read q (G = 1: k)
             if (j >= G && !(ok = warp_wait(BAR(grp, BR_XFREE), (kg - 1) & 1, st.wait_ns, abort_flag))) break;
-            if (load_x(grp, p_load)) x_landed(grp);
-            p_load = perm_next(p_load);
+            int tile = -1;
+            if (ends == 0) {
+                if (lane == 0) tile = atomicAdd(a.sched, 1);
+                tile = __shfl_sync(0xffffffffu, tile, 0);
+                if (tile >= ntiles) tile = -1;
+            }
+            if (tile < 0) {
+                ++ends;
+                if (lane == 0) {
+                    sring[j & 3] = -1;
+                    mbar_arrive(BAR(grp, BR_X));
+                    mbar_arrive(BAR(grp, BR_X));
+                }
+                continue;
+            }
+            if (lane == 0) sring[j & 3] = tile;
+            __syncwarp();
+            if (load_x(grp, tile)) x_landed(grp);
         }
         cp_async_wait<0>();
         if (!ok) *abort_flag = 1;
@@ -583,12 +597,13 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             const uint64_t d_wqk = desc_kmajor_sw64(base + F::WQK), d_wv = desc_kmajor_sw64(base + F::WV);
             bool ok = true;
 #pragma unroll 1
-            for (int j = 0; j < my_tiles; ++j) {
+            for (int j = 0;; ++j) {
                 const int grp = j % G, kg = j / G;
                 // tile j's x has landed, the q|k columns are free (tile j - 1's
                 // drained) and the group's columns are free (y of its previous tile
                 // drained)
                 if (!(ok = wait_or_abort(BAR(grp, BR_X), kg & 1, st.wait_ns, abort_flag))) break;
+                if (sring[j & 3] < 0) break;
                 if (j > 0 && !(ok = wait_or_abort(B_QKFREE, (j - 1) & 1, st.wait_ns, abort_flag))) break;
                 if (kg > 0 && !(ok = wait_or_abort(BAR(grp, BR_RFREE), (kg - 1) & 1, st.wait_ns, abort_flag))) break;
                 tc_fence_after();
@@ -661,12 +676,12 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             uint32_t ph_p = 0;
             uint32_t od_n[2] = {0u, 0u};
             bool ok = true;
-            int p_tile = perm0;
-            if (!F::SPLIT)
-                for (int i = 0; i < grp; ++i) p_tile = perm_next(p_tile);
 #pragma unroll 1
-            for (int j = F::SPLIT ? 0 : grp; ok && j < my_tiles; j += G) {
+            for (int j = F::SPLIT ? 0 : grp; ok; j += G) {
                 const int kg = j / G;
+                if (!(ok = wait_or_abort(BAR(tg, BR_X), kg & 1, st.wait_ns, abort_flag))) break;
+                const int p_tile = sring[j & 3];
+                if (p_tile < 0) break;
                 // S of the group's first two heads as soon as their q and k are
                 // stored (v, drained first, has then left the TMEM columns S takes)
                 if (!(ok = wait_or_abort(QKR(grp, 0), kg & 1, st.wait_ns, abort_flag))) break;
@@ -727,7 +742,6 @@ __global__ void __launch_bounds__(FTHREADS, 1)
                 bulk_commit();
                 bulk_wait_read();
                 mbar_arrive(BAR(tg, BR_VFREE));
-                for (int i = 0; i < G; ++i) p_tile = perm_next(p_tile);
             }
             bulk_wait_all();
             if (!ok) *abort_flag = 1;
@@ -758,12 +772,12 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         // head h comes before the softmax of head h + 2)
         float l0 = 1.f, l1 = 1.f;
         bool ok = true;
-        int p_tile = perm0;
-        if (!F::SPLIT)
-            for (int i = 0; i < grp; ++i) p_tile = perm_next(p_tile);
 #pragma unroll 1
-        for (int j = F::SPLIT ? 0 : grp; j < my_tiles; j += G) {
+        for (int j = F::SPLIT ? 0 : grp;; j += G) {
             const int kg = j / G;
+            if (!(ok = warp_wait(BAR(tg, BR_X), kg & 1, st.wait_ns, abort_flag))) break;
+            const int p_tile = sring[j & 3];
+            if (p_tile < 0) break;
             const WinInfo win = window_info(g, p_tile, slot);
             if (!(ok = warp_wait(BAR(tg, BR_QKV), kg & 1, st.wait_ns, abort_flag))) break;
             tc_fence_after();
@@ -1183,13 +1197,21 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             }
             fence_proxy_async_smem();   // the TMA stores read these rows
             warp_arrive(BAR(tg, BR_STAGE), lane);
-            for (int i = 0; i < G; ++i) p_tile = perm_next(p_tile);
         }
         if (!ok) *abort_flag = 1;
     }
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && *abort_flag) atomicOr(st.err, ERR_TIMEOUT);
+    if (tid == 0) {
+        // every producer of this launch is past its last take from the counter
+        // once the last CTA gets here: it zeroes both for the next launch
+        __threadfence();
+        if (atomicAdd(a.sched + 1, 1) == (int)gridDim.x - 1) {
+            atomicExch(a.sched, 0);
+            atomicExch(a.sched + 1, 0);
+        }
+    }
     if (warp == QWARP) {
         __syncwarp();
         tmem_dealloc(tmem, 512);
@@ -1207,22 +1229,6 @@ int num_sms()
     return n;
 }
 
-// Smallest v >= start (and >= 1) with gcd(v, n) == 1.
-int64_t coprime_near(int64_t n, int64_t start)
-{
-    auto gcd = [](int64_t x, int64_t y) {
-        while (y) {
-            const int64_t t = x % y;
-            x = y;
-            y = t;
-        }
-        return x;
-    };
-    if (n <= 1) return 1;
-    for (int64_t v = start < 1 ? 1 : start;; ++v)
-        if (gcd(v, n) == 1) return v % n ? v : 1;
-}
-
 template <int M, int C, int G, int FOLD>
 cudaError_t launch_fused_t(const FusedArgs &a, DeviceStatus st, cudaStream_t stream)
 {
@@ -1238,10 +1244,7 @@ cudaError_t launch_fused_t(const FusedArgs &a, DeviceStatus st, cudaStream_t str
     if (e != cudaSuccess) return e;
     const int64_t ntiles = (a.g.nwin + 1) / 2;
     const int grid = (int)(ntiles < num_sms() ? ntiles : num_sms());
-    FusedArgs b = a;
-    b.tile_mul = coprime_near(ntiles, (ntiles * 5) / 8 + 1);
-    b.perm_step = (int)(((unsigned long long)grid * (unsigned long long)b.tile_mul) % (unsigned long long)ntiles);
-    kern<<<grid, FTHREADS, smem, stream>>>(b, st, tx, to);
+    kern<<<grid, FTHREADS, smem, stream>>>(a, st, tx, to);
     return cudaGetLastError();
 }
 
