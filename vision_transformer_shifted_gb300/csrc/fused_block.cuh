@@ -322,151 +322,10 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     auto K = [&](int grp) { return F::SPLIT ? base + F::XT : base + F::KT + grp * KB * HT; };
     auto V = [&](int grp) { return base + F::VT + grp * KB * HT; };
 
-    // ---- once per CTA: weights, biases, tables, barriers, TMEM ---------------
-    {
-        for (int q = tid; q < (2 * C) * (C / 8); q += FTHREADS) {     // Wq, Wk rows
-            const int r = q / (C / 8), c16 = q % (C / 8);
-            cp_async16(base + F::WQK + (c16 >> 2) * (2 * C * 64) + sw64_offset(r, c16 & 3),
-                       a.Wqkv + (int64_t)r * C + c16 * 8, 16);
-        }
-        for (int q = tid; q < C * (C / 8); q += FTHREADS) {           // Wv rows
-            const int r = q / (C / 8), c16 = q % (C / 8);
-            cp_async16(base + F::WV + (c16 >> 2) * (C * 64) + sw64_offset(r, c16 & 3),
-                       a.Wqkv + (int64_t)(2 * C + r) * C + c16 * 8, 16);
-        }
-        for (int q = tid; q < C * (C / 8); q += FTHREADS) {           // Wproj
-            const int r = q / (C / 8), c16 = q % (C / 8);
-            cp_async16(base + F::WP + (c16 >> 2) * (C * 64) + sw64_offset(r, c16 & 3),
-                       a.Wproj + (int64_t)r * C + c16 * 8, 16);
-        }
-        cp_async_commit();
-        for (int i = tid; i < HEADS * L * L; i += FTHREADS) {
-            const int hd = i / (L * L), e = i % (L * L);
-            sbias[(hd * L + e / L) * F::LP + e % L] = __bfloat162float(a.table[(int64_t)e * HEADS + hd]) * FLOG2E;
-        }
-        for (int i = tid; i < 3 * C; i += FTHREADS) sbqkv[i] = a.bqkv ? __bfloat162float(a.bqkv[i]) : 0.f;
-        for (int i = tid; i < C; i += FTHREADS) sbproj[i] = a.bproj ? __bfloat162float(a.bproj[i]) : 0.f;
-        if (FOLD)
-            for (int i = tid; i < C; i += FTHREADS) {
-                sln[i] = __bfloat162float(a.ln_g[i]);
-                sln[C + i] = __bfloat162float(a.ln_b[i]);
-            }
-        if (tid < HEADS)
-            sscale[tid] = a.mode == 1 ? FLOG2E / fmaxf(a.tau[tid], 0.01f) : FLOG2E * rsqrtf(32.0f);
-        // the x tiles start as zeros: rows that no window token fills (8*ti + tj
-        // with ti or tj >= M, a missing second window) then only ever hold
-        // finite values (zeros, other tokens, q of earlier tiles), so the v
-        // rows of keys that do not exist -- multiplied by P = 0 -- stay finite
-        for (int i = tid; i < G * KB * HT / 16; i += FTHREADS)
-            reinterpret_cast<uint4 *>(sm + F::XT)[i] = make_uint4(0u, 0u, 0u, 0u);
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-    }
-    __syncthreads();   // the weights and bias vectors are in shared memory
-    if (FOLD == 1) {
-        // Pre-norm: LN(x) = xh * gamma + beta with xh = (x - mean) * rstd, so
-        // LN(x) Wqkv^T + bqkv = rstd (x W'^T - mean c) + b' with W' = Wqkv
-        // diag(gamma), c its row sums (over the input channels) and b' =
-        // Wqkv beta + bqkv: the MMAs take x as it is, and each row's rstd and
-        // mean (each compute thread's, of its own row) enter as the q, k, v
-        // columns are drained.
-        // The bias first (fp32, the unscaled weights, one thread per output in
-        // a fixed order), then every weight scaled by its column's gamma (bf16,
-        // in place), then c from the scaled bf16 weights the MMAs use.
-        auto wrow = [&](int n, int c16) -> uint8_t * {
-            return n < 2 * C ? sm + F::WQK + (c16 >> 2) * (2 * C * 64) + sw64_offset(n, c16 & 3)
-                             : sm + F::WV + (c16 >> 2) * (C * 64) + sw64_offset(n - 2 * C, c16 & 3);
-        };
-        for (int n = tid; n < 3 * C; n += FTHREADS) {
-            float acc = 0.f;
-#pragma unroll 1
-            for (int c16 = 0; c16 < C / 8; ++c16) {
-                const uint4 w8 = *reinterpret_cast<const uint4 *>(wrow(n, c16));
-                const uint32_t wd[4] = {w8.x, w8.y, w8.z, w8.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 w2 = unpack_bf16x2(wd[e]);
-                    acc = fmaf(w2.x, sln[C + 8 * c16 + 2 * e], acc);
-                    acc = fmaf(w2.y, sln[C + 8 * c16 + 2 * e + 1], acc);
-                }
-            }
-            sbqkv[n] += acc;
-        }
-        __syncthreads();   // (every bias read the unscaled weights)
-#pragma unroll 1
-        for (int q = tid; q < 3 * C * (C / 8); q += FTHREADS) {
-            const int n = q / (C / 8), c16 = q % (C / 8);
-            uint4 *p = reinterpret_cast<uint4 *>(wrow(n, c16));
-            const uint4 w8 = *p;
-            const uint32_t wd[4] = {w8.x, w8.y, w8.z, w8.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 w2 = unpack_bf16x2(wd[e]);
-                o[e] = pack_bf16x2(w2.x * sln[8 * c16 + 2 * e], w2.y * sln[8 * c16 + 2 * e + 1]);
-            }
-            *p = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        fence_proxy_async_smem();   // read by the QKV MMAs
-        __syncthreads();
-        for (int n = tid; n < 3 * C; n += FTHREADS) {
-            float acc = 0.f;
-#pragma unroll 1
-            for (int c16 = 0; c16 < C / 8; ++c16) {
-                const uint4 w8 = *reinterpret_cast<const uint4 *>(wrow(n, c16));
-                const uint32_t wd[4] = {w8.x, w8.y, w8.z, w8.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 w2 = unpack_bf16x2(wd[e]);
-                    acc += w2.x;
-                    acc += w2.y;
-                }
-            }
-            scsum[n] = acc;
-        }
-        __syncthreads();
-    }
-    // The value bias moves behind the softmax: a row's attention weights sum to
-    // 1, so o = P (v + bv) = P v + bv, and (P v + bv) Wproj^T + bproj =
-    // (P v) Wproj^T + (Wproj bv + bproj).  The projection bias used below is
-    // that sum (fp32), and v is drained without a bias.  One thread per
-    // output channel, in a fixed order (the result is the same on every CTA
-    // and every call).
-    if (tid >= C && tid < C + HEADS) {
-        // V2: a head's logits (log2 units) lie in [-scale + min B, scale + max B]
-        // (|cos| <= 1).  Where that span is at most 96, scale + max B serves
-        // as the softmax reference instead of the row maximum: every weight is
-        // then at least 2^-96 of it (no underflow to zero) and the normalised
-        // result is the same.  V1 logits have no such bound: NaN, row maxima.
-        const int hd = tid - C;
-        float bmax = -INFINITY, bmin = INFINITY;
-        for (int r = 0; r < L; ++r)
-            for (int c = 0; c < L; ++c) {
-                const float v = sbias[(hd * L + r) * F::LP + c];
-                bmax = fmaxf(bmax, v);
-                bmin = fminf(bmin, v);
-            }
-        const float sc = sscale[hd];
-        sref[hd] = a.mode == 1 && 2.f * sc + (bmax - bmin) <= 96.f ? sc + bmax : __int_as_float(0x7fffffff);
-    }
-    if ((a.bqkv || FOLD == 1) && tid < C) {
-        float acc = 0.f;
-        for (int c8 = 0; c8 < C / 8; ++c8) {
-            const uint4 w8 = *reinterpret_cast<const uint4 *>(sm + F::WP + (c8 >> 2) * (C * 64) + sw64_offset(tid, c8 & 3));
-            const float *bv = sbqkv + 2 * C + 8 * c8;
-            const float2 w01 = unpack_bf16x2(w8.x), w23 = unpack_bf16x2(w8.y), w45 = unpack_bf16x2(w8.z),
-                         w67 = unpack_bf16x2(w8.w);
-            acc = fmaf(w01.x, bv[0], acc);
-            acc = fmaf(w01.y, bv[1], acc);
-            acc = fmaf(w23.x, bv[2], acc);
-            acc = fmaf(w23.y, bv[3], acc);
-            acc = fmaf(w45.x, bv[4], acc);
-            acc = fmaf(w45.y, bv[5], acc);
-            acc = fmaf(w67.x, bv[6], acc);
-            acc = fmaf(w67.y, bv[7], acc);
-        }
-        sbproj[tid] += acc;
-    }
+    // ---- once per CTA: barriers and zeroed x tiles first, so that the
+    // producer starts gathering at once; the other eleven warps meanwhile
+    // bring in the weights and tables (their own barrier, 352 threads) and
+    // allocate TMEM ---------------------------------------------------------
     if (tid == 0) {
         for (int grp = 0; grp < 2; ++grp) {
             const int b0 = 21 * grp;
@@ -492,14 +351,167 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         *abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == QWARP) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
-        tmem_relinquish();
+    // the x tiles start as zeros: rows that no window token fills (8*ti + tj
+    // with ti or tj >= M, a missing second window) then only ever hold
+    // finite values (zeros, other tokens, q of earlier tiles), so the v
+    // rows of keys that do not exist -- multiplied by P = 0 -- stay finite
+    for (int i = tid; i < G * KB * HT / 16; i += FTHREADS)
+        reinterpret_cast<uint4 *>(sm + F::XT)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();   // (TMA writes and MMA reads of these bytes come after)
+    __syncthreads();   // barriers, zeroed x tiles
+    uint32_t tmem = 0;
+    if (warp != PWARP) {
+        const int stid = tid - 32;   // setup thread index (the producer warp excluded)
+        constexpr int NS = FTHREADS - 32;
+        auto setup_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(FTHREADS - 32) : "memory"); };
+        {
+            for (int q = stid; q < (2 * C) * (C / 8); q += NS) {     // Wq, Wk rows
+                const int r = q / (C / 8), c16 = q % (C / 8);
+                cp_async16(base + F::WQK + (c16 >> 2) * (2 * C * 64) + sw64_offset(r, c16 & 3),
+                           a.Wqkv + (int64_t)r * C + c16 * 8, 16);
+            }
+            for (int q = stid; q < C * (C / 8); q += NS) {           // Wv rows
+                const int r = q / (C / 8), c16 = q % (C / 8);
+                cp_async16(base + F::WV + (c16 >> 2) * (C * 64) + sw64_offset(r, c16 & 3),
+                           a.Wqkv + (int64_t)(2 * C + r) * C + c16 * 8, 16);
+            }
+            for (int q = stid; q < C * (C / 8); q += NS) {           // Wproj
+                const int r = q / (C / 8), c16 = q % (C / 8);
+                cp_async16(base + F::WP + (c16 >> 2) * (C * 64) + sw64_offset(r, c16 & 3),
+                           a.Wproj + (int64_t)r * C + c16 * 8, 16);
+            }
+            cp_async_commit();
+            for (int i = stid; i < HEADS * L * L; i += NS) {
+                const int hd = i / (L * L), e = i % (L * L);
+                sbias[(hd * L + e / L) * F::LP + e % L] = __bfloat162float(a.table[(int64_t)e * HEADS + hd]) * FLOG2E;
+            }
+            for (int i = stid; i < 3 * C; i += NS) sbqkv[i] = a.bqkv ? __bfloat162float(a.bqkv[i]) : 0.f;
+            for (int i = stid; i < C; i += NS) sbproj[i] = a.bproj ? __bfloat162float(a.bproj[i]) : 0.f;
+            if (FOLD)
+                for (int i = stid; i < C; i += NS) {
+                    sln[i] = __bfloat162float(a.ln_g[i]);
+                    sln[C + i] = __bfloat162float(a.ln_b[i]);
+                }
+            if (stid < HEADS)
+                sscale[stid] = a.mode == 1 ? FLOG2E / fmaxf(a.tau[stid], 0.01f) : FLOG2E * rsqrtf(32.0f);
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+        }
+        setup_sync();   // the weights and bias vectors are in shared memory
+        if (FOLD == 1) {
+            // Pre-norm: LN(x) = xh * gamma + beta with xh = (x - mean) * rstd, so
+            // LN(x) Wqkv^T + bqkv = rstd (x W'^T - mean c) + b' with W' = Wqkv
+            // diag(gamma), c its row sums (over the input channels) and b' =
+            // Wqkv beta + bqkv: the MMAs take x as it is, and each row's rstd and
+            // mean (each compute thread's, of its own row) enter as the q, k, v
+            // columns are drained.
+            // The bias first (fp32, the unscaled weights, one thread per output in
+            // a fixed order), then every weight scaled by its column's gamma (bf16,
+            // in place), then c from the scaled bf16 weights the MMAs use.
+            auto wrow = [&](int n, int c16) -> uint8_t * {
+                return n < 2 * C ? sm + F::WQK + (c16 >> 2) * (2 * C * 64) + sw64_offset(n, c16 & 3)
+                                 : sm + F::WV + (c16 >> 2) * (C * 64) + sw64_offset(n - 2 * C, c16 & 3);
+            };
+            for (int n = stid; n < 3 * C; n += NS) {
+                float acc = 0.f;
+    #pragma unroll 1
+                for (int c16 = 0; c16 < C / 8; ++c16) {
+                    const uint4 w8 = *reinterpret_cast<const uint4 *>(wrow(n, c16));
+                    const uint32_t wd[4] = {w8.x, w8.y, w8.z, w8.w};
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 w2 = unpack_bf16x2(wd[e]);
+                        acc = fmaf(w2.x, sln[C + 8 * c16 + 2 * e], acc);
+                        acc = fmaf(w2.y, sln[C + 8 * c16 + 2 * e + 1], acc);
+                    }
+                }
+                sbqkv[n] += acc;
+            }
+            setup_sync();   // (every bias read the unscaled weights)
+    #pragma unroll 1
+            for (int q = stid; q < 3 * C * (C / 8); q += NS) {
+                const int n = q / (C / 8), c16 = q % (C / 8);
+                uint4 *p = reinterpret_cast<uint4 *>(wrow(n, c16));
+                const uint4 w8 = *p;
+                const uint32_t wd[4] = {w8.x, w8.y, w8.z, w8.w};
+                uint32_t o[4];
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 w2 = unpack_bf16x2(wd[e]);
+                    o[e] = pack_bf16x2(w2.x * sln[8 * c16 + 2 * e], w2.y * sln[8 * c16 + 2 * e + 1]);
+                }
+                *p = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            fence_proxy_async_smem();   // read by the QKV MMAs
+            setup_sync();
+            for (int n = stid; n < 3 * C; n += NS) {
+                float acc = 0.f;
+    #pragma unroll 1
+                for (int c16 = 0; c16 < C / 8; ++c16) {
+                    const uint4 w8 = *reinterpret_cast<const uint4 *>(wrow(n, c16));
+                    const uint32_t wd[4] = {w8.x, w8.y, w8.z, w8.w};
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 w2 = unpack_bf16x2(wd[e]);
+                        acc += w2.x;
+                        acc += w2.y;
+                    }
+                }
+                scsum[n] = acc;
+            }
+            setup_sync();
+        }
+        // The value bias moves behind the softmax: a row's attention weights sum to
+        // 1, so o = P (v + bv) = P v + bv, and (P v + bv) Wproj^T + bproj =
+        // (P v) Wproj^T + (Wproj bv + bproj).  The projection bias used below is
+        // that sum (fp32), and v is drained without a bias.  One thread per
+        // output channel, in a fixed order (the result is the same on every CTA
+        // and every call).
+        if (stid >= C && stid < C + HEADS) {
+            // V2: a head's logits (log2 units) lie in [-scale + min B, scale + max B]
+            // (|cos| <= 1).  Where that span is at most 96, scale + max B serves
+            // as the softmax reference instead of the row maximum: every weight is
+            // then at least 2^-96 of it (no underflow to zero) and the normalised
+            // result is the same.  V1 logits have no such bound: NaN, row maxima.
+            const int hd = stid - C;
+            float bmax = -INFINITY, bmin = INFINITY;
+            for (int r = 0; r < L; ++r)
+                for (int c = 0; c < L; ++c) {
+                    const float v = sbias[(hd * L + r) * F::LP + c];
+                    bmax = fmaxf(bmax, v);
+                    bmin = fminf(bmin, v);
+                }
+            const float sc = sscale[hd];
+            sref[hd] = a.mode == 1 && 2.f * sc + (bmax - bmin) <= 96.f ? sc + bmax : __int_as_float(0x7fffffff);
+        }
+        if ((a.bqkv || FOLD == 1) && stid < C) {
+            float acc = 0.f;
+            for (int c8 = 0; c8 < C / 8; ++c8) {
+                const uint4 w8 =
+                    *reinterpret_cast<const uint4 *>(sm + F::WP + (c8 >> 2) * (C * 64) + sw64_offset(stid, c8 & 3));
+                const float *bv = sbqkv + 2 * C + 8 * c8;
+                const float2 w01 = unpack_bf16x2(w8.x), w23 = unpack_bf16x2(w8.y), w45 = unpack_bf16x2(w8.z),
+                             w67 = unpack_bf16x2(w8.w);
+                acc = fmaf(w01.x, bv[0], acc);
+                acc = fmaf(w01.y, bv[1], acc);
+                acc = fmaf(w23.x, bv[2], acc);
+                acc = fmaf(w23.y, bv[3], acc);
+                acc = fmaf(w45.x, bv[4], acc);
+                acc = fmaf(w45.y, bv[5], acc);
+                acc = fmaf(w67.x, bv[6], acc);
+                acc = fmaf(w67.y, bv[7], acc);
+            }
+            sbproj[stid] += acc;
+        }
+        if (warp == QWARP) {
+            tmem_alloc(smem_u32(tmem_slot), 512);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        setup_sync();   // weights, tables, TMEM address
+        tc_fence_after();
+        tmem = *tmem_slot;
     }
-    tc_fence_before();
-    __syncthreads();   // weights, tables, barriers, TMEM address
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
 
     // Tiles are handed out at run time: the producer takes the next one from
     // a counter shared by the CTAs (windows on the shifted edges cost more, so
