@@ -327,7 +327,7 @@ def _run_block(w, g, table, ratio=4):
 @pytest.mark.gpu
 @pytest.mark.parametrize("key,B,H,W", [("swin_t_s1", 2, 14, 21), ("swinv2_t_s1", 1, 16, 24), ("swin_t_s1", 1, 7, 7),
                                        ("swin_b_s1", 1, 14, 14), ("swin_b_s1", 8, 56, 56), ("swin_b_s3", 2, 14, 14),
-                                       ("swinv2_b_s1", 2, 16, 24)])
+                                       ("swinv2_b_s1", 2, 16, 24), ("swin_c64", 3, 14, 21), ("swinv2_c64", 2, 16, 16)])
 def test_block_forward_small(key, B, H, W):
     """Grids of one to two tiles per CTA.  Where the attention is the fused
     kernel (C = 64, 96, 128 with windows of 7 or 8) the block folds LayerNorm 1
@@ -335,6 +335,8 @@ def test_block_forward_small(key, B, H, W):
     the separate LayerNorm kernel."""
     if key == "swinv2_b_s1":   # V2 at C = 128, four heads
         w = WORKLOADS["swinv2_t_s1"].with_(B=B, H=H, W=W, C=128, heads=4)
+    elif key in ("swin_c64", "swinv2_c64"):   # C = 64, two heads (the fused MLP's second shape)
+        w = WORKLOADS["swin_t_s1" if key == "swin_c64" else "swinv2_t_s1"].with_(B=B, H=H, W=W, C=64, heads=2)
     else:
         w = WORKLOADS[key].with_(B=B, H=H, W=W)
     g = generate_block(w)
@@ -345,13 +347,17 @@ def test_block_forward_small(key, B, H, W):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("key,C,heads,folded", [("swin_t_s1", 96, 3, True), ("swinv2_t_s1", 96, 3, True),
-                                                ("swin_b_s1", 128, 4, True), ("swinv2_t_s1", 128, 4, False),
-                                                ("swin_b_s3", 512, 16, False)])
-def test_block_launches_show_the_fold(key, C, heads, folded):
+@pytest.mark.parametrize("key,C,heads,want", [("swin_t_s1", 96, 3, 3), ("swinv2_t_s1", 96, 3, 2),
+                                              ("swin_t_s1", 64, 2, 3), ("swinv2_t_s1", 64, 2, 2),
+                                              ("swin_b_s1", 128, 4, 4), ("swinv2_t_s1", 128, 4, 5),
+                                              ("swin_b_s3", 512, 16, None)])
+def test_block_launches_show_the_fusions(key, C, heads, want):
     """Where the attention is the fused kernel, LayerNorm 1 and the first
-    residual are inside it: four launches (attention, LayerNorm 2, two MLP
-    GEMMs); elsewhere the separate LayerNorm pass and the attention's own."""
+    residual are inside it; where the MLP's weights fit one SM (C = 64, 96) the
+    MLP is one kernel (V2: with its LayerNorm and residual).  V1 at C = 96:
+    attention, LayerNorm 2, MLP; V2: attention, MLP; C = 128: attention,
+    LayerNorm 2, two GEMMs (V2 without the fold: attention, LayerNorm, two
+    GEMMs, LayerNorm); C = 512: the unfused sequence."""
     w = WORKLOADS[key].with_(B=1, H=2 * WORKLOADS[key].M, W=2 * WORKLOADS[key].M, C=C, heads=heads)
     g = generate_block(w)
     table = oracle_table(w, g)
@@ -366,7 +372,7 @@ def test_block_launches_show_the_fold(key, C, heads, folded):
         n = sw.swin_block_last_launches(h)
     finally:
         sw.swin_block_destroy(h)
-    assert (n == 4) if folded else (n >= 5), n
+    assert (n == want) if want else (n >= 7), n
 
 
 @pytest.mark.gpu

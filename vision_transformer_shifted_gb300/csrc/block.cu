@@ -5,7 +5,9 @@
 //   V2  z = x + LN1(attn(x));  y = z + LN2(MLP(z))
 // Steps: the swin_wattn forward for attn; one LayerNorm kernel that also
 // does the residual add (add-then-normalise for V1, normalise-then-add for
-// V2); the MLP as two tcgen05 GEMMs whose epilogues apply GELU and the
+// V2); the MLP as one kernel that keeps the hidden activation on chip where
+// its weights fit an SM's shared memory (mlp_fused.cu; V2 with its LayerNorm
+// and residual), else as two tcgen05 GEMMs whose epilogues apply GELU and the
 // residual add.  Where the attention is the fused kernel, LayerNorm 1 and
 // the first residual are folded into it (its x tiles' prologue, V1; its
 // output rows' epilogue, V2) and z is its output.
@@ -299,24 +301,44 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
     // to its output rows; V2: LN of its output rows, then x added), and z
     // comes straight out of it.
     const bool v1 = (h->mode & 0xf) == SWIN_WATTN_V1;
+    // The MLP sub-layer, out = res + MLP(A) (V1) or res + LN2(MLP(A)) (V2): one
+    // kernel with the hidden activation kept on chip where the weights fit its
+    // shared memory, else two GEMMs (GELU and residual epilogues; V2 a
+    // LayerNorm + residual pass after them, t1 as scratch).
+    h->last_launches = 0;
+    auto mlp = [&](const bf16 *A, const bf16 *res, bf16 *dst) -> cudaError_t {
+        if (mlp_fused_supported(C, R)) {
+            h->last_launches += 1;
+            return launch_mlp_fused(A, (const bf16 *)p->W1, (const bf16 *)p->b1, (const bf16 *)p->W2,
+                                    (const bf16 *)p->b2, res, v1 ? nullptr : g2, v1 ? nullptr : be2, dst, T, C, R, st,
+                                    s);
+        }
+        cudaError_t e2;
+        if ((e2 = gemm(A, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return e2;
+        if (v1) {
+            h->last_launches += 2;
+            return gemm(m1, R, p->W2, p->b2, dst, C, EPI_RESID, res);
+        }
+        h->last_launches += 3;
+        if ((e2 = gemm(m1, R, p->W2, p->b2, t1, C, EPI_NONE, nullptr)) != cudaSuccess) return e2;
+        return launch_layernorm(t1, res, g2, be2, nullptr, dst, T, C, 2, s);
+    };
     rc = attn_forward_folded(h->attn, x, B, H, W, p->Wqkv, p->bqkv, p->bias_table, p->logit_scale, p->Wproj, p->bproj,
                              g1, be1, v1 ? 1 : 2, z, s);
     if (rc == SWIN_WATTN_OK) {
-        h->last_launches = 1 + 3;   // the folded attention; LayerNorm 2 and the two MLP GEMMs
+        h->last_launches = 1;   // the folded attention
         if (v1) {
             if ((e = launch_layernorm(z, nullptr, g2, be2, nullptr, t1, T, C, 0, s)) != cudaSuccess)
                 return cuda_status(e);
-            if ((e = gemm(t1, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return cuda_status(e);
-            if ((e = gemm(m1, R, p->W2, p->b2, yy, C, EPI_RESID, z)) != cudaSuccess) return cuda_status(e);
+            h->last_launches += 1;
+            if ((e = mlp(t1, z, yy)) != cudaSuccess) return cuda_status(e);
         } else {
-            if ((e = gemm(z, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return cuda_status(e);
-            if ((e = gemm(m1, R, p->W2, p->b2, t1, C, EPI_NONE, nullptr)) != cudaSuccess) return cuda_status(e);
-            if ((e = launch_layernorm(t1, z, g2, be2, nullptr, yy, T, C, 2, s)) != cudaSuccess) return cuda_status(e);
+            if ((e = mlp(z, z, yy)) != cudaSuccess) return cuda_status(e);
         }
         return ws_check(h->ws, s);
     }
     if (rc != SWIN_WATTN_EUNSUPPORTED) return rc;
-    h->last_launches = 4;   // two LayerNorm passes and the two MLP GEMMs, plus the attention's (below)
+    h->last_launches = 2;   // the two LayerNorm passes around the attention, plus its own and the MLP's
     if (v1) {
         if ((e = launch_layernorm(xx, nullptr, g1, be1, nullptr, t1, T, C, 0, s)) != cudaSuccess) return cuda_status(e);
         rc = swin_wattn_forward(h->attn, t1, B, H, W, p->Wqkv, p->bqkv, p->bias_table, p->logit_scale, p->Wproj,
@@ -324,17 +346,15 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
         if (rc != SWIN_WATTN_OK) return rc;
         h->last_launches += swin_wattn_last_launches(h->attn);
         if ((e = launch_layernorm(t2, xx, g2, be2, z, t1, T, C, 1, s)) != cudaSuccess) return cuda_status(e);
-        if ((e = gemm(t1, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return cuda_status(e);
-        if ((e = gemm(m1, R, p->W2, p->b2, yy, C, EPI_RESID, z)) != cudaSuccess) return cuda_status(e);
+        if ((e = mlp(t1, z, yy)) != cudaSuccess) return cuda_status(e);
     } else {
         rc = swin_wattn_forward(h->attn, x, B, H, W, p->Wqkv, p->bqkv, p->bias_table, p->logit_scale, p->Wproj,
                                 p->bproj, t2, stream);
         if (rc != SWIN_WATTN_OK) return rc;
         h->last_launches += swin_wattn_last_launches(h->attn);
         if ((e = launch_layernorm(t2, xx, g1, be1, nullptr, z, T, C, 2, s)) != cudaSuccess) return cuda_status(e);
-        if ((e = gemm(z, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return cuda_status(e);
-        if ((e = gemm(m1, R, p->W2, p->b2, t1, C, EPI_NONE, nullptr)) != cudaSuccess) return cuda_status(e);
-        if ((e = launch_layernorm(t1, z, g2, be2, nullptr, yy, T, C, 2, s)) != cudaSuccess) return cuda_status(e);
+        h->last_launches -= 1;   // (V2: one LayerNorm pass before the MLP)
+        if ((e = mlp(z, z, yy)) != cudaSuccess) return cuda_status(e);
     }
     return ws_check(h->ws, s);
 }

@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "gelu.cuh"
 
 namespace swin {
 
@@ -59,35 +60,6 @@ __device__ __forceinline__ void store_row_bf16(bf16 *dst, const float *v, const 
         u.w = pack_bf16x2(v[8 * q + 6] + bias[8 * q + 6], v[8 * q + 7] + bias[8 * q + 7]);
         d4[q] = u;
     }
-}
-
-// GELU(x) = x Phi(x) = x (1 + erf(x / sqrt 2)) / 2 with erf(u) from an odd
-// polynomial u P(u^2) of this file's own making: a weighted least-squares fit
-// of erf(u)/u in the Chebyshev basis over u^2 in [0, 3.7^2] (degree 12, weight
-// u, float64), rewritten as a power series in s = 2 u^2 / 3.7^2 - 1 and
-// evaluated by Horner in fp32; erf = sign(u) beyond |u| = 3.7 (1 - erf(3.7) =
-// 1.7e-7).  Measured against float64 erf on 800,001 points in [-8, 8]: erf
-// error <= 9.9e-7, GELU error <= 2.8e-6 -- far below the bf16 rounding of the
-// result -- in 13 FMAs and no special-function unit instruction.
-__device__ __forceinline__ float gelu_poly(float x)
-{
-    const float u = x * 0.70710678118654752f, t = u * u;
-    const float s = fmaf(t, 0.14609204f, -1.0f);
-    float p = 3.387000179e-03f;
-    p = fmaf(p, s, -8.247348480e-03f);
-    p = fmaf(p, s, 6.714036223e-03f);
-    p = fmaf(p, s, -8.770867251e-03f);
-    p = fmaf(p, s, 2.361703850e-02f);
-    p = fmaf(p, s, -3.920292482e-02f);
-    p = fmaf(p, s, 5.219075084e-02f);
-    p = fmaf(p, s, -6.962815672e-02f);
-    p = fmaf(p, s, 9.047554433e-02f);
-    p = fmaf(p, s, -1.127380058e-01f);
-    p = fmaf(p, s, 1.408007443e-01f);
-    p = fmaf(p, s, -1.904647499e-01f);
-    p = fmaf(p, s, 3.821373880e-01f);
-    const float e = t < 13.69f ? u * p : copysignf(1.0f, u);
-    return 0.5f * x * (1.0f + e);
 }
 
 // Epilogue of the block's MLP ("Swin Transformer V2" (neura.market), How It

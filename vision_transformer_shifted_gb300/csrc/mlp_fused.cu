@@ -1,0 +1,412 @@
+// The Swin block's MLP sub-layer as one persistent kernel (sm_103a, tcgen05 +
+// TMEM) ("Swin Transformer V2" (neura.market), How It Works: pre-norm in the
+// original Swin, residual post-norm in V2):
+//   V1   y = res + GELU(A W1^T + b1) W2^T + b2        (A = LN2(z), res = z)
+//   V2   y = res + LN(GELU(A W1^T + b1) W2^T + b2)    (A = res = z)
+// with the exact GELU of gelu.cuh.  The hidden activation (4C per token)
+// never leaves the SM.  Per 128-row tile of tokens the hidden units go in
+// chunks of 128: H = A W1[chunk]^T (128 x 128 x C) into one of two TMEM
+// buffers; eight compute warps (two per TMEM lane quarter, 64 columns each)
+// add b1, apply GELU and write H back as bf16 over the first half of their own
+// fp32 columns; Y += H W2[:, chunk]^T (128 x C x 128, H read from TMEM as the
+// A operand) into one of two Y buffers (tiles alternate).  GEMM1 of chunk n is
+// issued before GEMM2 of chunk n - 1, so the tensor cores work while the
+// compute warps apply GELU.  The epilogue adds b2 and the residual (V2: the
+// LayerNorm of the row first; there one warp of the quarter takes the whole
+// row) and stores y in token order.
+// Warp roles: 0 loads A tiles (2-D TMA, two buffers), 1 issues every MMA and
+// owns TMEM, 2 and 3 idle, 4..11 compute.  Weights stay in shared memory (one
+// CTA per SM, tiles round-robin).  Every wait is bounded.
+#include "common.cuh"
+#include "gelu.cuh"
+#include "ptx.cuh"
+
+namespace swin {
+
+namespace {
+
+constexpr int MT_THREADS = 12 * 32;
+constexpr int MT_CWARP0 = 4;
+constexpr float MT_EPS = 1e-5f;
+
+template <int C, int R>
+struct MlpCfg {
+    static constexpr int KB = C / 32;    // 32-wide K blocks of A and W1 (64-byte swizzle)
+    static constexpr int NC = R / 128;   // hidden chunks of 128
+    static constexpr int HT = 128 * 64;  // one [128 rows][32] SW64 tile
+    static constexpr int W1 = 0;                   // [R rows][C]: KB blocks of R * 64 bytes
+    static constexpr int W2 = W1 + R * C * 2;      // [C rows][R]: R / 32 blocks of C * 64 bytes
+    static constexpr int AT = W2 + C * R * 2;      // A tile buffer a at AT + a * KB * HT
+    static constexpr int SMALL = AT + 2 * KB * HT;
+    static constexpr int O_B1 = 0;                 // [R] f32
+    static constexpr int O_B2 = O_B1 + R * 4;      // [C] f32
+    static constexpr int O_LN = O_B2 + C * 4;      // [2][C] f32: gamma, beta (V2)
+    static constexpr int O_BARS = O_LN + 2 * C * 4;
+    static constexpr int NBARS = 14;
+    static constexpr int O_END = O_BARS + NBARS * 8 + 16;
+    static constexpr int BYTES = SMALL + O_END;
+    // TMEM: H buffers at 128 b, Y buffers at 256 + C yb
+    static constexpr int T_H = 0, T_Y = 256;
+    static_assert(C % 32 == 0 && C <= 128 && R % 128 == 0, "shapes");
+    static_assert(T_Y + 2 * C <= 512, "TMEM budget");
+    static_assert(BYTES + 1024 <= 232448, "shared memory budget");
+};
+
+enum {
+    MB_AFULL = 0,    // + a: A tile landed (TMA bytes)
+    MB_AFREE = 2,    // + a: the tile's last GEMM1 has read it
+    MB_HREADY = 4,   // + b: GEMM1 into H buffer b done
+    MB_HBF = 6,      // + b: H buffer b holds GELU(H) as bf16 (compute warps)
+    MB_HFREE = 8,    // + b: GEMM2 has read H buffer b
+    MB_YREADY = 10,  // + yb: the tile's last GEMM2 done
+    MB_YFREE = 12    // + yb: Y buffer yb drained (compute warps)
+};
+
+struct MlpArgs {
+    const bf16 *W1, *b1, *W2, *b2, *res, *ln_g, *ln_b;
+    bf16 *out;
+    int64_t T;
+};
+
+__device__ __forceinline__ bool mt_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool mt_warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, volatile int *abort)
+{
+    const bool ok = mt_wait(bar, parity, limit_ns, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// A shared-memory descriptor whose start address (16-byte units) is moved by `bytes`.
+__device__ __forceinline__ uint64_t mt_desc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
+__device__ __forceinline__ void mt_warp_arrive(uint32_t bar, int lane)
+{
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
+template <int C, int R, bool POST>
+__global__ void __launch_bounds__(MT_THREADS, 1)
+    mlp_fused_kernel(MlpArgs a, DeviceStatus st, const __grid_constant__ CUtensorMap tmap_a)
+// tmap_a: A as [T][C] bf16, boxes of 32 columns x 128 rows
+{
+    using F = MlpCfg<C, R>;
+    constexpr int KB = F::KB, NC = F::NC, HT = F::HT;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_align(smem_raw, 1024);
+    uint8_t *small = sm + F::SMALL;
+    float *sb1 = reinterpret_cast<float *>(small + F::O_B1);
+    float *sb2 = reinterpret_cast<float *>(small + F::O_B2);
+    float *sln = reinterpret_cast<float *>(small + F::O_LN);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + F::O_BARS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + F::NBARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t base = smem_u32(sm);
+    auto BAR = [&](int i) { return smem_u32(&bars[i]); };
+    const int64_t ntiles = (a.T + 127) / 128;
+
+    // ---- once per CTA: weights (64-byte-swizzled K-major), bias vectors,
+    // barriers, TMEM --------------------------------------------------------
+    for (int q = tid; q < R * (C / 8); q += MT_THREADS) {   // W1 [R][C]
+        const int r = q / (C / 8), c16 = q % (C / 8);
+        cp_async16(base + F::W1 + (c16 >> 2) * (R * 64) + sw64_offset(r, c16 & 3), a.W1 + (int64_t)r * C + c16 * 8,
+                   16);
+    }
+    for (int q = tid; q < C * (R / 8); q += MT_THREADS) {   // W2 [C][R]
+        const int r = q / (R / 8), c16 = q % (R / 8);
+        cp_async16(base + F::W2 + (c16 >> 2) * (C * 64) + sw64_offset(r, c16 & 3), a.W2 + (int64_t)r * R + c16 * 8,
+                   16);
+    }
+    cp_async_commit();
+    for (int i = tid; i < R; i += MT_THREADS) sb1[i] = a.b1 ? __bfloat162float(a.b1[i]) : 0.f;
+    for (int i = tid; i < C; i += MT_THREADS) {
+        sb2[i] = a.b2 ? __bfloat162float(a.b2[i]) : 0.f;
+        if (POST) {
+            sln[i] = __bfloat162float(a.ln_g[i]);
+            sln[C + i] = __bfloat162float(a.ln_b[i]);
+        }
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(BAR(MB_AFULL + i), 1);
+            mbar_init(BAR(MB_AFREE + i), 1);
+            mbar_init(BAR(MB_HREADY + i), 1);
+            mbar_init(BAR(MB_HBF + i), 8);
+            mbar_init(BAR(MB_HFREE + i), 1);
+            mbar_init(BAR(MB_YREADY + i), 1);
+            mbar_init(BAR(MB_YFREE + i), 8);
+        }
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();   // the weights are read by the MMAs
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto A = [&](int buf) { return base + F::AT + buf * KB * HT; };
+
+    if (warp == 0) {
+        // ===================== producer: A tiles =====================
+        bool ok = true;
+        if (lane == 0) {
+#pragma unroll 1
+            for (int j = 0;; ++j) {
+                const int64_t tile = (int64_t)blockIdx.x + (int64_t)j * gridDim.x;
+                if (tile >= ntiles) break;
+                const int ab = j & 1;
+                if (j >= 2 && !(ok = mt_wait(BAR(MB_AFREE + ab), ((j >> 1) - 1) & 1, st.wait_ns, abort_flag))) break;
+                mbar_arrive_expect_tx(BAR(MB_AFULL + ab), KB * HT);
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_load_2d(A(ab) + kb * HT, &tmap_a, kb * 32, (int)(tile * 128), BAR(MB_AFULL + ab));
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer =====================
+        if (lane == 0) {
+            constexpr uint32_t id1 = idesc_bf16(128, 128), id2 = idesc_bf16(128, C);
+            const uint64_t dw1 = desc_kmajor_sw64(base + F::W1), dw2 = desc_kmajor_sw64(base + F::W2);
+            bool ok = true;
+            // GEMM2 of global chunk m: Y[yb] (+)= GELU(H[b]) W2[:, chunk]^T
+            auto gemm2 = [&](int m) -> bool {
+                const int b = m & 1, cm = m % NC, jm = m / NC, yb = jm & 1;
+                if (!mt_wait(BAR(MB_HBF + b), (m >> 1) & 1, st.wait_ns, abort_flag)) return false;
+                if (cm == 0 && jm >= 2 && !mt_wait(BAR(MB_YFREE + yb), ((jm >> 1) - 1) & 1, st.wait_ns, abort_flag))
+                    return false;
+                tc_fence_after();
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    // K step s (16 hidden units): bf16 pairs at column 64 (s / 4) + 8 (s % 4) of the buffer
+                    const uint32_t at = tmem + F::T_H + 128 * b + 64 * (s >> 2) + 8 * (s & 3);
+                    const uint64_t bd = mt_desc_add(dw2, (4 * cm + (s >> 1)) * (C * 64) + 32 * (s & 1));
+                    mma_bf16_ts(tmem + F::T_Y + C * yb, at, bd, id2, (cm | s) != 0);
+                }
+                mma_commit(BAR(MB_HFREE + b));
+                if (cm == NC - 1) mma_commit(BAR(MB_YREADY + yb));
+                return true;
+            };
+            int n = 0;   // global chunk index
+#pragma unroll 1
+            for (int j = 0; ok; ++j) {
+                const int64_t tile = (int64_t)blockIdx.x + (int64_t)j * gridDim.x;
+                if (tile >= ntiles) break;
+                const int ab = j & 1;
+                if (!(ok = mt_wait(BAR(MB_AFULL + ab), (j >> 1) & 1, st.wait_ns, abort_flag))) break;
+                const uint64_t da = desc_kmajor_sw64(A(ab));
+#pragma unroll 1
+                for (int c = 0; c < NC; ++c, ++n) {
+                    const int b = n & 1;
+                    if (n >= 2 && !(ok = mt_wait(BAR(MB_HFREE + b), ((n >> 1) - 1) & 1, st.wait_ns, abort_flag)))
+                        break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks)
+                            mma_bf16(tmem + F::T_H + 128 * b, mt_desc_add(da, kb * HT + 32 * ks),
+                                     mt_desc_add(dw1, kb * (R * 64) + c * (128 * 64) + 32 * ks), id1, (kb | ks) != 0);
+                    mma_commit(BAR(MB_HREADY + b));
+                    if (c == NC - 1) mma_commit(BAR(MB_AFREE + ab));
+                    if (n >= 1 && !(ok = gemm2(n - 1))) break;
+                }
+            }
+            if (ok && n >= 1) ok = gemm2(n - 1);
+            if (!ok) *abort_flag = 1;
+        }
+    } else if (warp >= MT_CWARP0) {
+        // ===================== compute warps =====================
+        const int quarter = warp & 3, half = (warp - MT_CWARP0) >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        bool ok = true;
+        int n = 0;
+#pragma unroll 1
+        for (int j = 0; ok; ++j) {
+            const int64_t tile = (int64_t)blockIdx.x + (int64_t)j * gridDim.x;
+            if (tile >= ntiles) break;
+            const int64_t tok = tile * 128 + row;
+            const bool valid = tok < a.T;
+            // ---- GELU of each chunk's 64 columns of this warp's half ----
+#pragma unroll 1
+            for (int c = 0; c < NC; ++c, ++n) {
+                const int b = n & 1;
+                if (!(ok = mt_warp_wait(BAR(MB_HREADY + b), (n >> 1) & 1, st.wait_ns, abort_flag))) break;
+                tc_fence_after();
+                const uint32_t tcol = t_lane + F::T_H + 128 * b + 64 * half;
+                float v[64];
+                tmem_ld32(tcol, *reinterpret_cast<float(*)[32]>(v));
+                tmem_ld32(tcol + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+                tmem_wait_ld();
+                const float4 *b4 = reinterpret_cast<const float4 *>(sb1 + 128 * c + 64 * half);
+                uint32_t pk[32];
+#pragma unroll
+                for (int e4 = 0; e4 < 16; ++e4) {
+                    const float4 bb = b4[e4];
+                    float x0 = v[4 * e4] + bb.x, x1 = v[4 * e4 + 1] + bb.y, x2 = v[4 * e4 + 2] + bb.z,
+                          x3 = v[4 * e4 + 3] + bb.w;
+                    gelu_poly2(x0, x1);
+                    gelu_poly2(x2, x3);
+                    pk[2 * e4] = pack_bf16x2(x0, x1);
+                    pk[2 * e4 + 1] = pack_bf16x2(x2, x3);
+                }
+                tmem_st16(tcol, *reinterpret_cast<uint32_t(*)[16]>(pk));
+                tmem_st16(tcol + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
+                tmem_wait_st();
+                mt_warp_arrive(BAR(MB_HBF + b), lane);   // read by GEMM2
+            }
+            if (!ok) break;
+            // ---- y = Y + b2 (V2: LayerNorm) + res -> out ----
+            const int yb = j & 1;
+            if (!(ok = mt_warp_wait(BAR(MB_YREADY + yb), (j >> 1) & 1, st.wait_ns, abort_flag))) break;
+            tc_fence_after();
+            if (!POST) {
+                // this warp's half of the row's C columns
+                constexpr int CH = C / 2;   // 32 or 48
+                static_assert(CH == 32 || CH == 48, "columns per warp");
+                float y[48];
+                const uint32_t ycol = t_lane + F::T_Y + C * yb + CH * half;
+                tmem_ld32(ycol, *reinterpret_cast<float(*)[32]>(y));
+                if (CH == 48) tmem_ld16(ycol + 32, *reinterpret_cast<float(*)[16]>(y + 32));
+                tmem_wait_ld();
+                mt_warp_arrive(BAR(MB_YFREE + yb), lane);
+                if (valid) {
+                    const uint4 *rs = reinterpret_cast<const uint4 *>(a.res + tok * C + CH * half);
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.out + tok * C + CH * half);
+#pragma unroll
+                    for (int q = 0; q < CH / 8; ++q) {
+                        const uint4 u = rs[q];
+                        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 r2 = unpack_bf16x2(wd[e]);
+                            const int k = 8 * q + 2 * e;
+                            o[e] = pack_bf16x2(y[k] + sb2[CH * half + k] + r2.x, y[k + 1] + sb2[CH * half + k + 1] + r2.y);
+                        }
+                        dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+            } else {
+                // residual post-norm: the half-0 warp takes the whole row
+                if (half == 0) {
+                    float y[C];
+                    const uint32_t ycol = t_lane + F::T_Y + C * yb;
+#pragma unroll
+                    for (int k = 0; k < C / 32; ++k) tmem_ld32(ycol + 32 * k, *reinterpret_cast<float(*)[32]>(y + 32 * k));
+                    tmem_wait_ld();
+                    mt_warp_arrive(BAR(MB_YFREE + yb), lane);
+                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int k = 0; k < C; ++k) {
+                        y[k] += sb2[k];
+                        s4[k & 3] += y[k];
+                    }
+                    const float mean = ((s4[0] + s4[1]) + (s4[2] + s4[3])) / (float)C;
+                    float q4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int k = 0; k < C; ++k) {
+                        const float d = y[k] - mean;
+                        q4[k & 3] = fmaf(d, d, q4[k & 3]);
+                    }
+                    const float rstd = rsqrtf(((q4[0] + q4[1]) + (q4[2] + q4[3])) / (float)C + MT_EPS);
+                    if (valid) {
+                        const uint4 *rs = reinterpret_cast<const uint4 *>(a.res + tok * C);
+                        uint4 *dst = reinterpret_cast<uint4 *>(a.out + tok * C);
+#pragma unroll
+                        for (int q = 0; q < C / 8; ++q) {
+                            const uint4 u = rs[q];
+                            const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 r2 = unpack_bf16x2(wd[e]);
+                                const int k = 8 * q + 2 * e;
+                                o[e] = pack_bf16x2((y[k] - mean) * rstd * sln[k] + sln[C + k] + r2.x,
+                                                   (y[k + 1] - mean) * rstd * sln[k + 1] + sln[C + k + 1] + r2.y);
+                            }
+                            dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                } else {
+                    mt_warp_arrive(BAR(MB_YFREE + yb), lane);   // (reads nothing)
+                }
+            }
+        }
+        if (!ok) *abort_flag = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && *abort_flag) atomicOr(st.err, ERR_TIMEOUT);
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+int mlp_num_sms()
+{
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    }
+    return n;
+}
+
+template <int C, int R, bool POST>
+cudaError_t launch_mlp_t(const bf16 *A, const MlpArgs &a, DeviceStatus st, cudaStream_t stream)
+{
+    using F = MlpCfg<C, R>;
+    const size_t smem = F::BYTES + 1024;
+    auto kern = mlp_fused_kernel<C, R, POST>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    CUtensorMap ta;
+    e = make_tensor_map_sw64(&ta, A, a.T, C, 128);
+    if (e != cudaSuccess) return e;
+    const int64_t ntiles = (a.T + 127) / 128;
+    const int grid = (int)(ntiles < mlp_num_sms() ? ntiles : mlp_num_sms());
+    kern<<<grid, MT_THREADS, smem, stream>>>(a, st, ta);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+bool mlp_fused_supported(int C, int R) { return (C == 96 && R == 384) || (C == 64 && R == 256); }
+
+cudaError_t launch_mlp_fused(const bf16 *A, const bf16 *W1, const bf16 *b1, const bf16 *W2, const bf16 *b2,
+                             const bf16 *res, const bf16 *ln_g, const bf16 *ln_b, bf16 *out, int64_t T, int C, int R,
+                             DeviceStatus st, cudaStream_t stream)
+{
+    if (!mlp_fused_supported(C, R) || !A || !W1 || !W2 || !res || !out || T <= 0) return cudaErrorInvalidValue;
+    if ((ln_g == nullptr) != (ln_b == nullptr)) return cudaErrorInvalidValue;
+    const MlpArgs a{W1, b1, W2, b2, res, ln_g, ln_b, out, T};
+    const bool post = ln_g != nullptr;
+    if (C == 96) return post ? launch_mlp_t<96, 384, true>(A, a, st, stream) : launch_mlp_t<96, 384, false>(A, a, st, stream);
+    return post ? launch_mlp_t<64, 256, true>(A, a, st, stream) : launch_mlp_t<64, 256, false>(A, a, st, stream);
+}
+
+} // namespace swin
