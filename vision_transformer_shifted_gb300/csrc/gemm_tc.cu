@@ -70,7 +70,7 @@ __device__ __forceinline__ void epilogue_op(const GemmArgs &a, int64_t R, int n,
 {
     for (int i = 0; i < cnt; ++i) {
         float t = v[i] + bias[i];
-        if (a.epi == EPI_GELU) t = gelu_poly(t);
+        if (a.epi == EPI_GELU) t = gelu_exact(t);
         else if (a.epi == EPI_RESID && R < a.rows) t += __bfloat162float(a.R[R * a.ldr + n + i]);
         e[i] = t;
     }

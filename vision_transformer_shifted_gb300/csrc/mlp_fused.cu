@@ -6,16 +6,17 @@
 // with the exact GELU of gelu.cuh.  The hidden activation (4C per token)
 // never leaves the SM.  Per 128-row tile of tokens the hidden units go in
 // chunks of 128: H = A W1[chunk]^T (128 x 128 x C) into one of two TMEM
-// buffers; eight compute warps (two per TMEM lane quarter, 64 columns each)
-// add b1, apply GELU and write H back as bf16 over the first half of their own
-// fp32 columns; Y += H W2[:, chunk]^T (128 x C x 128, H read from TMEM as the
+// buffers; sixteen compute warps (four per TMEM lane quarter, 32 columns
+// each) add b1, apply GELU and write H back as bf16 over the first half of
+// their own fp32 columns; Y += H W2[:, chunk]^T (128 x C x 128, H read from TMEM as the
 // A operand) into one of two Y buffers (tiles alternate).  GEMM1 of chunk n is
 // issued before GEMM2 of chunk n - 1, so the tensor cores work while the
 // compute warps apply GELU.  The epilogue adds b2 and the residual (V2: the
 // LayerNorm of the row first; there one warp of the quarter takes the whole
-// row) and stores y in token order.
+// row, reading Y from TMEM once per pass) and stores y in token order.
 // Warp roles: 0 loads A tiles (2-D TMA, two buffers), 1 issues every MMA and
-// owns TMEM, 2 and 3 idle, 4..11 compute.  Weights stay in shared memory (one
+// owns TMEM, 2 and 3 idle, 4..19 compute (four warps per scheduler: the work
+// per element is short chains, so latency is hidden by warps).  Weights stay in shared memory (one
 // CTA per SM, tiles round-robin).  Every wait is bounded.
 #include "common.cuh"
 #include "gelu.cuh"
@@ -25,7 +26,8 @@ namespace swin {
 
 namespace {
 
-constexpr int MT_THREADS = 12 * 32;
+constexpr int MT_THREADS = 20 * 32;
+constexpr int MT_CWARPS = 16;
 constexpr int MT_CWARP0 = 4;
 constexpr float MT_EPS = 1e-5f;
 
@@ -146,10 +148,10 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
             mbar_init(BAR(MB_AFULL + i), 1);
             mbar_init(BAR(MB_AFREE + i), 1);
             mbar_init(BAR(MB_HREADY + i), 1);
-            mbar_init(BAR(MB_HBF + i), 8);
+            mbar_init(BAR(MB_HBF + i), MT_CWARPS);
             mbar_init(BAR(MB_HFREE + i), 1);
             mbar_init(BAR(MB_YREADY + i), 1);
-            mbar_init(BAR(MB_YFREE + i), 8);
+            mbar_init(BAR(MB_YFREE + i), MT_CWARPS);
         }
         *abort_flag = 0;
         mbar_init_fence();
@@ -198,8 +200,8 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
-                    // K step s (16 hidden units): bf16 pairs at column 64 (s / 4) + 8 (s % 4) of the buffer
-                    const uint32_t at = tmem + F::T_H + 128 * b + 64 * (s >> 2) + 8 * (s & 3);
+                    // K step s (16 hidden units): bf16 pairs at column 32 (s / 2) + 8 (s % 2) of the buffer
+                    const uint32_t at = tmem + F::T_H + 128 * b + 32 * (s >> 1) + 8 * (s & 1);
                     const uint64_t bd = mt_desc_add(dw2, (4 * cm + (s >> 1)) * (C * 64) + 32 * (s & 1));
                     mma_bf16_ts(tmem + F::T_Y + C * yb, at, bd, id2, (cm | s) != 0);
                 }
@@ -237,9 +239,10 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
         }
     } else if (warp >= MT_CWARP0) {
         // ===================== compute warps =====================
-        const int quarter = warp & 3, half = (warp - MT_CWARP0) >> 2;
+        const int quarter = warp & 3, part = (warp - MT_CWARP0) >> 2;   // part: 0..3 within the quarter
         const int row = quarter * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        constexpr int CP = C / 4;   // epilogue columns per warp (V1): 24 or 16
         bool ok = true;
         int n = 0;
 #pragma unroll 1
@@ -248,31 +251,38 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
             if (tile >= ntiles) break;
             const int64_t tok = tile * 128 + row;
             const bool valid = tok < a.T;
-            // ---- GELU of each chunk's 64 columns of this warp's half ----
+            const bool epi = !POST || part == 0;   // this warp writes output
+            // ---- GELU of each chunk's 32 columns of this warp's part ----
 #pragma unroll 1
             for (int c = 0; c < NC; ++c, ++n) {
                 const int b = n & 1;
+                if (c == NC - 1 && valid && epi) {
+                    // the epilogue's residual slice into L1 while this chunk runs
+                    const char *rp = reinterpret_cast<const char *>(a.res + tok * C + (POST ? 0 : CP * part));
+                    constexpr int RB = (POST ? C : CP) * 2;
+#pragma unroll
+                    for (int o = 0; o < RB; o += 64) prefetch_l1(rp + o);
+                    prefetch_l1(rp + RB - 1);
+                }
                 if (!(ok = mt_warp_wait(BAR(MB_HREADY + b), (n >> 1) & 1, st.wait_ns, abort_flag))) break;
                 tc_fence_after();
-                const uint32_t tcol = t_lane + F::T_H + 128 * b + 64 * half;
-                float v[64];
-                tmem_ld32(tcol, *reinterpret_cast<float(*)[32]>(v));
-                tmem_ld32(tcol + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+                const uint32_t tcol = t_lane + F::T_H + 128 * b + 32 * part;
+                float v[32];
+                tmem_ld32(tcol, v);
                 tmem_wait_ld();
-                const float4 *b4 = reinterpret_cast<const float4 *>(sb1 + 128 * c + 64 * half);
-                uint32_t pk[32];
+                const float4 *b4 = reinterpret_cast<const float4 *>(sb1 + 128 * c + 32 * part);
+                uint32_t pk[16];
 #pragma unroll
-                for (int e4 = 0; e4 < 16; ++e4) {
+                for (int e4 = 0; e4 < 8; ++e4) {
                     const float4 bb = b4[e4];
                     float x0 = v[4 * e4] + bb.x, x1 = v[4 * e4 + 1] + bb.y, x2 = v[4 * e4 + 2] + bb.z,
                           x3 = v[4 * e4 + 3] + bb.w;
-                    gelu_poly2(x0, x1);
-                    gelu_poly2(x2, x3);
+                    gelu_exact2(x0, x1);
+                    gelu_exact2(x2, x3);
                     pk[2 * e4] = pack_bf16x2(x0, x1);
                     pk[2 * e4 + 1] = pack_bf16x2(x2, x3);
                 }
-                tmem_st16(tcol, *reinterpret_cast<uint32_t(*)[16]>(pk));
-                tmem_st16(tcol + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
+                tmem_st16(tcol, pk);
                 tmem_wait_st();
                 mt_warp_arrive(BAR(MB_HBF + b), lane);   // read by GEMM2
             }
@@ -281,21 +291,20 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
             const int yb = j & 1;
             if (!(ok = mt_warp_wait(BAR(MB_YREADY + yb), (j >> 1) & 1, st.wait_ns, abort_flag))) break;
             tc_fence_after();
+            const uint32_t ybase = t_lane + F::T_Y + C * yb;
             if (!POST) {
-                // this warp's half of the row's C columns
-                constexpr int CH = C / 2;   // 32 or 48
-                static_assert(CH == 32 || CH == 48, "columns per warp");
-                float y[48];
-                const uint32_t ycol = t_lane + F::T_Y + C * yb + CH * half;
-                tmem_ld32(ycol, *reinterpret_cast<float(*)[32]>(y));
-                if (CH == 48) tmem_ld16(ycol + 32, *reinterpret_cast<float(*)[16]>(y + 32));
+                // this warp's CP columns of the row
+                float y[24];
+                const uint32_t ycol = ybase + CP * part;
+                tmem_ld16(ycol, *reinterpret_cast<float(*)[16]>(y));
+                if (CP == 24) tmem_ld8(ycol + 16, *reinterpret_cast<float(*)[8]>(y + 16));
                 tmem_wait_ld();
                 mt_warp_arrive(BAR(MB_YFREE + yb), lane);
                 if (valid) {
-                    const uint4 *rs = reinterpret_cast<const uint4 *>(a.res + tok * C + CH * half);
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.out + tok * C + CH * half);
+                    const uint4 *rs = reinterpret_cast<const uint4 *>(a.res + tok * C + CP * part);
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.out + tok * C + CP * part);
 #pragma unroll
-                    for (int q = 0; q < CH / 8; ++q) {
+                    for (int q = 0; q < CP / 8; ++q) {
                         const uint4 u = rs[q];
                         const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
                         uint32_t o[4];
@@ -303,55 +312,66 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
                         for (int e = 0; e < 4; ++e) {
                             const float2 r2 = unpack_bf16x2(wd[e]);
                             const int k = 8 * q + 2 * e;
-                            o[e] = pack_bf16x2(y[k] + sb2[CH * half + k] + r2.x, y[k + 1] + sb2[CH * half + k + 1] + r2.y);
+                            o[e] = pack_bf16x2(y[k] + sb2[CP * part + k] + r2.x, y[k + 1] + sb2[CP * part + k + 1] + r2.y);
                         }
                         dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 }
-            } else {
-                // residual post-norm: the half-0 warp takes the whole row
-                if (half == 0) {
-                    float y[C];
-                    const uint32_t ycol = t_lane + F::T_Y + C * yb;
-#pragma unroll
-                    for (int k = 0; k < C / 32; ++k) tmem_ld32(ycol + 32 * k, *reinterpret_cast<float(*)[32]>(y + 32 * k));
+            } else if (part == 0) {
+                // residual post-norm: the row's LayerNorm over its C values, read
+                // from TMEM 32 columns at a time in each of three passes (mean,
+                // mean square deviation, output)
+                float sum = 0.f;
+#pragma unroll 1
+                for (int k0 = 0; k0 < C; k0 += 32) {
+                    float y[32];
+                    tmem_ld32(ybase + k0, y);
                     tmem_wait_ld();
-                    mt_warp_arrive(BAR(MB_YFREE + yb), lane);
-                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int k = 0; k < C; ++k) {
-                        y[k] += sb2[k];
-                        s4[k & 3] += y[k];
-                    }
-                    const float mean = ((s4[0] + s4[1]) + (s4[2] + s4[3])) / (float)C;
-                    float q4[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int k = 0; k < 32; ++k) sum += y[k] + sb2[k0 + k];
+                }
+                const float mean = sum / (float)C;
+                float sq = 0.f;
+#pragma unroll 1
+                for (int k0 = 0; k0 < C; k0 += 32) {
+                    float y[32];
+                    tmem_ld32(ybase + k0, y);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < C; ++k) {
-                        const float d = y[k] - mean;
-                        q4[k & 3] = fmaf(d, d, q4[k & 3]);
+                    for (int k = 0; k < 32; ++k) {
+                        const float d = y[k] + sb2[k0 + k] - mean;
+                        sq = fmaf(d, d, sq);
                     }
-                    const float rstd = rsqrtf(((q4[0] + q4[1]) + (q4[2] + q4[3])) / (float)C + MT_EPS);
+                }
+                const float rstd = rsqrtf(sq / (float)C + MT_EPS);
+#pragma unroll 1
+                for (int k0 = 0; k0 < C; k0 += 32) {
+                    float y[32];
+                    tmem_ld32(ybase + k0, y);
+                    tmem_wait_ld();
                     if (valid) {
-                        const uint4 *rs = reinterpret_cast<const uint4 *>(a.res + tok * C);
-                        uint4 *dst = reinterpret_cast<uint4 *>(a.out + tok * C);
+                        const uint4 *rs = reinterpret_cast<const uint4 *>(a.res + tok * C + k0);
+                        uint4 *dst = reinterpret_cast<uint4 *>(a.out + tok * C + k0);
 #pragma unroll
-                        for (int q = 0; q < C / 8; ++q) {
+                        for (int q = 0; q < 4; ++q) {
                             const uint4 u = rs[q];
                             const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
                             uint32_t o[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float2 r2 = unpack_bf16x2(wd[e]);
-                                const int k = 8 * q + 2 * e;
-                                o[e] = pack_bf16x2((y[k] - mean) * rstd * sln[k] + sln[C + k] + r2.x,
-                                                   (y[k + 1] - mean) * rstd * sln[k + 1] + sln[C + k + 1] + r2.y);
+                                const int k = 8 * q + 2 * e, kk = k0 + k;
+                                o[e] = pack_bf16x2((y[k] + sb2[kk] - mean) * rstd * sln[kk] + sln[C + kk] + r2.x,
+                                                   (y[k + 1] + sb2[kk + 1] - mean) * rstd * sln[kk + 1] + sln[C + kk + 1] +
+                                                       r2.y);
                             }
                             dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
                         }
                     }
-                } else {
-                    mt_warp_arrive(BAR(MB_YFREE + yb), lane);   // (reads nothing)
                 }
+                mt_warp_arrive(BAR(MB_YFREE + yb), lane);
+            } else {
+                mt_warp_arrive(BAR(MB_YFREE + yb), lane);   // (reads nothing)
             }
         }
         if (!ok) *abort_flag = 1;
