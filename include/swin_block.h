@@ -73,10 +73,11 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
 int swin_block_sync_status(swin_block_t h, swin_stream_t stream);
 
 /* Number of kernel launches the last swin_block_forward on this handle
- * enqueued (C = 96 or 64 with windows of 7 or 8: 3 in V1 -- the attention
- * with LayerNorm 1 and the residual folded in, LayerNorm 2, the MLP as one
- * kernel -- and 2 in V2; more where those kernels do not apply); 0 before the
- * first forward or after one that failed its checks, -1 for a NULL handle. */
+ * enqueued (C = 96 or 64 with windows of 7 or 8: 2 -- the attention with
+ * LayerNorm 1 and the first residual folded in, the MLP with LayerNorm 2 and
+ * the second residual -- in either mode; more where those kernels do not
+ * apply); 0 before the first forward or after one that failed its checks, -1
+ * for a NULL handle. */
 int swin_block_last_launches(swin_block_t h);
 
 /* Frees the handle and its workspace (NULL is a no-op). */

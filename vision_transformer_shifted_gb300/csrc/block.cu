@@ -301,40 +301,39 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
     // to its output rows; V2: LN of its output rows, then x added), and z
     // comes straight out of it.
     const bool v1 = (h->mode & 0xf) == SWIN_WATTN_V1;
-    // The MLP sub-layer, out = res + MLP(A) (V1) or res + LN2(MLP(A)) (V2): one
-    // kernel with the hidden activation kept on chip where the weights fit its
-    // shared memory, else two GEMMs (GELU and residual epilogues; V2 a
-    // LayerNorm + residual pass after them, t1 as scratch).
+    // The MLP sub-layer on the residual stream z, out = z + MLP(LN2(z)) (V1) or
+    // z + LN2(MLP(z)) (V2): one kernel (LayerNorm 2 folded in, the hidden
+    // activation kept on chip) where the weights fit its shared memory, else
+    // LayerNorm 2 (V1; unless ln2_done: t1 already holds it) and two GEMMs
+    // (GELU and residual epilogues; V2 a LayerNorm + residual pass after them,
+    // t1 as scratch).
     h->last_launches = 0;
-    auto mlp = [&](const bf16 *A, const bf16 *res, bf16 *dst) -> cudaError_t {
+    auto mlp = [&](bool ln2_done) -> cudaError_t {
         if (mlp_fused_supported(C, R)) {
             h->last_launches += 1;
-            return launch_mlp_fused(A, (const bf16 *)p->W1, (const bf16 *)p->b1, (const bf16 *)p->W2,
-                                    (const bf16 *)p->b2, res, v1 ? nullptr : g2, v1 ? nullptr : be2, dst, T, C, R, st,
-                                    s);
+            return launch_mlp_fused(z, (const bf16 *)p->W1, (const bf16 *)p->b1, (const bf16 *)p->W2,
+                                    (const bf16 *)p->b2, g2, be2, !v1, yy, T, C, R, st, s);
         }
         cudaError_t e2;
-        if ((e2 = gemm(A, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return e2;
         if (v1) {
+            if (!ln2_done) {
+                h->last_launches += 1;
+                if ((e2 = launch_layernorm(z, nullptr, g2, be2, nullptr, t1, T, C, 0, s)) != cudaSuccess) return e2;
+            }
             h->last_launches += 2;
-            return gemm(m1, R, p->W2, p->b2, dst, C, EPI_RESID, res);
+            if ((e2 = gemm(t1, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return e2;
+            return gemm(m1, R, p->W2, p->b2, yy, C, EPI_RESID, z);
         }
         h->last_launches += 3;
+        if ((e2 = gemm(z, C, p->W1, p->b1, m1, R, EPI_GELU, nullptr)) != cudaSuccess) return e2;
         if ((e2 = gemm(m1, R, p->W2, p->b2, t1, C, EPI_NONE, nullptr)) != cudaSuccess) return e2;
-        return launch_layernorm(t1, res, g2, be2, nullptr, dst, T, C, 2, s);
+        return launch_layernorm(t1, z, g2, be2, nullptr, yy, T, C, 2, s);
     };
     rc = attn_forward_folded(h->attn, x, B, H, W, p->Wqkv, p->bqkv, p->bias_table, p->logit_scale, p->Wproj, p->bproj,
                              g1, be1, v1 ? 1 : 2, z, s);
     if (rc == SWIN_WATTN_OK) {
         h->last_launches = 1;   // the folded attention
-        if (v1) {
-            if ((e = launch_layernorm(z, nullptr, g2, be2, nullptr, t1, T, C, 0, s)) != cudaSuccess)
-                return cuda_status(e);
-            h->last_launches += 1;
-            if ((e = mlp(t1, z, yy)) != cudaSuccess) return cuda_status(e);
-        } else {
-            if ((e = mlp(z, z, yy)) != cudaSuccess) return cuda_status(e);
-        }
+        if ((e = mlp(false)) != cudaSuccess) return cuda_status(e);
         return ws_check(h->ws, s);
     }
     if (rc != SWIN_WATTN_EUNSUPPORTED) return rc;
@@ -346,7 +345,7 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
         if (rc != SWIN_WATTN_OK) return rc;
         h->last_launches += swin_wattn_last_launches(h->attn);
         if ((e = launch_layernorm(t2, xx, g2, be2, z, t1, T, C, 1, s)) != cudaSuccess) return cuda_status(e);
-        if ((e = mlp(t1, z, yy)) != cudaSuccess) return cuda_status(e);
+        if ((e = mlp(true)) != cudaSuccess) return cuda_status(e);
     } else {
         rc = swin_wattn_forward(h->attn, x, B, H, W, p->Wqkv, p->bqkv, p->bias_table, p->logit_scale, p->Wproj,
                                 p->bproj, t2, stream);
@@ -354,7 +353,7 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
         h->last_launches += swin_wattn_last_launches(h->attn);
         if ((e = launch_layernorm(t2, xx, g1, be1, nullptr, z, T, C, 2, s)) != cudaSuccess) return cuda_status(e);
         h->last_launches -= 1;   // (V2: one LayerNorm pass before the MLP)
-        if ((e = mlp(z, z, yy)) != cudaSuccess) return cuda_status(e);
+        if ((e = mlp(true)) != cudaSuccess) return cuda_status(e);
     }
     return ws_check(h->ws, s);
 }

@@ -202,13 +202,14 @@ bool fused_fold_supported(int M, int C, int heads, int fold);
 int attn_forward_folded(::swin_wattn_s *h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
                         const void *bias_table, const float *logit_scale, const void *Wproj, const void *bproj,
                         const void *ln_g, const void *ln_b, int fold, void *out, cudaStream_t stream);
-// The block's MLP sub-layer in one kernel (hidden activation kept on chip):
-// out = res + GELU(A W1^T + b1) W2^T + b2, or with ln_g / ln_b (V2 residual
-// post-norm) out = res + LN(GELU(A W1^T + b1) W2^T + b2).  A, res, out [T, C];
-// W1 [R, C]; W2 [C, R].  Where mlp_fused_supported(C, R).
+// The block's MLP sub-layer in one kernel (hidden activation kept on chip),
+// on the residual stream z [T, C]: out = z + GELU(LN(z) W1^T + b1) W2^T + b2
+// (V1 pre-norm, post false) or out = z + LN(GELU(z W1^T + b1) W2^T + b2) (V2,
+// post true); LN with gain ln_g and shift ln_b; W1 [R, C], W2 [C, R].  Where
+// mlp_fused_supported(C, R).
 bool mlp_fused_supported(int C, int R);
-cudaError_t launch_mlp_fused(const bf16 *A, const bf16 *W1, const bf16 *b1, const bf16 *W2, const bf16 *b2,
-                             const bf16 *res, const bf16 *ln_g, const bf16 *ln_b, bf16 *out, int64_t T, int C, int R,
+cudaError_t launch_mlp_fused(const bf16 *z, const bf16 *W1, const bf16 *b1, const bf16 *W2, const bf16 *b2,
+                             const bf16 *ln_g, const bf16 *ln_b, bool post, bf16 *out, int64_t T, int C, int R,
                              DeviceStatus st, cudaStream_t stream);
 
 // sched: two device ints, zero before the first launch (the kernel's tile
