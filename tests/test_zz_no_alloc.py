@@ -12,7 +12,8 @@ bit against swin_wattn_forward (the entry point with a handle-owned
 workspace) forced onto the same three kernels.  They also check that the
 device's free memory does not move across calls, that a call too large for
 the array is refused before any launch, and that a kernel's bounded-wait
-timeout reaches the caller through swin_wattn_noalloc_sync_status.
+timeout reaches the caller through swin_wattn_noalloc_sync_status, and
+that a call can be captured into a CUDA graph in global capture mode.
 
 This file is collected last on purpose, and it needs no state from the
 other test files.
@@ -85,6 +86,31 @@ def test_noalloc_matches_oracle_and_forward_on_two_calls_in_a_row(key, B, H, W):
     noalloc(w, t, td, out)
     assert sw.swin_wattn_noalloc_sync_status() == sw.OK
     assert torch.cuda.mem_get_info()[0] == free_before
+    assert torch.equal(out, first)
+
+
+def test_noalloc_call_captures_into_a_cuda_graph():
+    """After one call, a second one on the same arguments is captured into a
+    CUDA graph in global capture mode, which refuses cudaMalloc and every
+    call that synchronises the device: the capture goes through, nothing runs
+    until the replay, and the replay writes the first call's bits."""
+    w = WORKLOADS["swin_t_s1"].with_(B=2)
+    g = generate(w, nonzero_bias=True)
+    t = device_inputs(g)
+    table = t["table"]
+    out = torch.full_like(t["x"], float("nan"))
+    noalloc(w, t, table, out)
+    assert sw.swin_wattn_noalloc_sync_status() == sw.OK
+    first = out.clone()
+    out.fill_(float("nan"))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="global"):
+        noalloc(w, t, table, out)
+    torch.cuda.synchronize()
+    assert bool(torch.isnan(out).all())   # captured, not run
+    graph.replay()
+    assert sw.swin_wattn_noalloc_sync_status() == sw.OK
     assert torch.equal(out, first)
 
 
