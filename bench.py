@@ -276,23 +276,29 @@ def measure_forward(sw, w, dev, pk, args, steps, soak, rank=0, world=1, dist=Non
     barrier(dist)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # (an event after each step as well: the spread of the per-step times)
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     e0.record(stream)
     for i in range(steps):
         step(i)
-        marks[i].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(dist)
     ms = max_over_ranks(e0.elapsed_time(e1), dist) / steps
-    per_step = sorted([e0.elapsed_time(marks[0])] + [marks[i - 1].elapsed_time(marks[i]) for i in range(1, steps)])
+    # the spread of single steps, from a second pass with an event after every
+    # step (outside the timed region above: each event adds about 2 us)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    marks[0].record(stream)
+    for i in range(steps):
+        step(i)
+        marks[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per_step = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(steps))
     pct = lambda q: per_step[min(len(per_step) - 1, int(q * (len(per_step) - 1) + 0.5))] * 1e3  # noqa: E731
     assert sw.swin_wattn_sync_status(h, stream) == sw.OK
     tflops = w.flops * world / (ms * 1e-3) / 1e12
     path = ("three kernels" if launches_per_step >= 3 else "fp32 block" if w.dtype == "fp32" else "fused")
     res = {"ms_per_step": ms, "tokens_per_s": job_rate(w.tokens, world, ms * 1e-3), "tflops": tflops,
-           "step_us": {"median": pct(0.5), "p10": pct(0.1), "p90": pct(0.9)},
+           "step_us": {"median": pct(0.5), "p10": pct(0.1), "p90": pct(0.9),
+                       "note": "second pass, an event after every step (adds about 2 us a step)"},
            "path": path, "launches_per_step": launches_per_step,
            "l2": "inputs rotated over %d buffer sets of %.0f MB (x + out), %.0f MB > 2x L2" %
                  (nsets, io_bytes / 2 ** 20, nsets * io_bytes / 2 ** 20)}

@@ -277,6 +277,11 @@ struct RsPlan {
     uint32_t tcols;
     size_t b_bytes, smem;
     int ng;   // column groups: CTA b does column chunk b % ng of every ng-th row block (1: none)
+    // stores staged through shared memory (rs_warp_store): for epilogues that
+    // only add the bias (and V2's unit length), whose time goes to the stores;
+    // the GELU and residual epilogues store directly and keep the 16 KB for a
+    // deeper A ring
+    int staged;
 };
 
 // Column chunk c0 .. c0+n of a plain-store GEMM as a GEMM of its own (its
@@ -297,6 +302,8 @@ __host__ __device__ inline GemmArgs column_chunk(const GemmArgs &a, int c0, int 
     return c;
 }
 
+// One 32-column chunk of this thread's output row, stored directly (the
+// GELU and residual epilogues).
 __device__ __forceinline__ void rs_epilogue_chunk32(const GemmArgs &a, int64_t R, int n, bf16 *dst, float (&v)[32],
                                                    const float *bias, bool norm)
 {
@@ -347,6 +354,77 @@ __device__ __forceinline__ void rs_epilogue_chunk32(const GemmArgs &a, int64_t R
     }
 }
 
+// One 32-column chunk of this thread's output row as 16 packed bf16 pairs:
+// bias, then (V2) unit length, the residual or the MLP's activation.  (The
+// additions of zero keep the bits of a plain bias-add store: -0 becomes +0.)
+// `valid`: the row exists (rows past the end compute on whatever TMEM holds
+// and are never stored).
+__device__ __forceinline__ void rs_chunk_words(const GemmArgs &a, int64_t R, bool valid, int n, float (&v)[32],
+                                               const float *bias, bool norm, uint32_t (&w)[16])
+{
+    if (norm) {
+        // V2: this 32-column chunk is one head's q or k; bias first, then scale
+        // to unit length (norm clamped at 1e-12) before rounding
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            v[i] += bias[i];
+            ss = fmaf(v[i], v[i], ss);
+        }
+        const float nrm = fmaxf(sqrtf(ss), 1e-12f), inv = 1.0f / nrm;
+        if (valid && a.norms) a.norms[R * (a.norms_ld ? a.norms_ld : a.norm_cols / 32) + n / 32] = nrm;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i] * inv + 0.f, v[2 * i + 1] * inv + 0.f);
+    } else if (a.epi == EPI_NONE) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i] + bias[2 * i], v[2 * i + 1] + bias[2 * i + 1]);
+    } else if (a.epi == EPI_RESID) {
+        // residual row read 16 bytes at a time
+        const uint4 *res = reinterpret_cast<const uint4 *>(a.R + R * a.ldr + n);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 u = valid ? res[q] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t wr[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float2 f = unpack_bf16x2(wr[t]);
+                const int i = 8 * q + 2 * t;
+                w[4 * q + t] = pack_bf16x2(v[i] + bias[i] + f.x + 0.f, v[i + 1] + bias[i + 1] + f.y + 0.f);
+            }
+        }
+    } else {
+        float e[32];
+        epilogue_op(a, R, n, v, bias, e, 32);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(e[2 * i] + 0.f, e[2 * i + 1] + 0.f);
+    }
+}
+
+// The warp's 32 rows of one 32-column chunk (this thread's: w) to global
+// memory: staged in the warp's 2 KB of shared memory (16-byte pieces XOR-
+// swizzled by row: no bank conflicts either way), then written back with
+// four lanes per row, 8 rows x 64 bytes per instruction, instead of 32 rows x
+// 16 bytes (a quarter of the L2 write requests, whole sectors).  dk[k]: the
+// output row of warp row 8k + lane / 4 (null: not stored), col its offset.
+__device__ __forceinline__ void rs_warp_store(uint8_t *stage, const uint32_t (&w)[16], bf16 *const (&dk)[4], int col,
+                                              int lane)
+{
+    const uint32_t sw = (uint32_t)((lane >> 1) & 3);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4 *>(stage + lane * 64 + ((c ^ sw) << 4)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    __syncwarp();
+    const int c = lane & 3;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int rr = 8 * k + (lane >> 2);
+        const uint4 u = *reinterpret_cast<const uint4 *>(stage + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4));
+        if (dk[k]) *reinterpret_cast<uint4 *>(dk[k] + col + 8 * c) = u;
+    }
+    __syncwarp();   // (the stage is written again by the next chunk)
+}
+
 template <int LOAD, int STORE, bool GROUPS>
 __global__ void __launch_bounds__(RS_THREADS, 1)
 gemm_rs_kernel(GemmArgs a_full, RsPlan pl, DeviceStatus st, const __grid_constant__ CUtensorMap tmA)
@@ -365,7 +443,8 @@ gemm_rs_kernel(GemmArgs a_full, RsPlan pl, DeviceStatus st, const __grid_constan
     const int S = pl.stages, BN = pl.BN, nbn = pl.nbn, KB = pl.KB;
     uint8_t *sB = smem;
     uint8_t *sA = smem + pl.b_bytes;
-    float *sbias = reinterpret_cast<float *>(sA + (size_t)S * RS_STAGE);
+    uint8_t *sstage = sA + (size_t)S * RS_STAGE;   // (staged) [RS_NEPI warps][32 rows][64 B]: the stores' staging
+    float *sbias = reinterpret_cast<float *>(sstage + (pl.staged ? RS_NEPI * 2048 : 0));
     int64_t *rowoff = reinterpret_cast<int64_t *>(sbias + 512); // producer's gathered rows of the tile
     uint64_t *bars = reinterpret_cast<uint64_t *>(rowoff + BM);
     uint64_t *full = bars, *empty = bars + S, *tfull = bars + 2 * S, *tempty = bars + 2 * S + 2;
@@ -556,13 +635,32 @@ gemm_rs_kernel(GemmArgs a_full, RsPlan pl, DeviceStatus st, const __grid_constan
                 }
             }
             const uint32_t tb = t_lane + (uint32_t)buf * half_cols;
-            for (int ci = half; ci < nchunks; ci += 2) {
-                float v[32];
-                tmem_ld32(tb + 32 * ci, v);
-                tmem_wait_ld();
-                if (dst_row)
-                    rs_epilogue_chunk32(a, R, n0 + 32 * ci, dst_row + 32 * ci, v, sbias + n0 + 32 * ci,
-                                        n0 + 32 * ci < a.norm_cols);
+            // the output rows this lane writes back for the warp (rows 8k + lane / 4)
+            bf16 *dk[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                dk[k] = reinterpret_cast<bf16 *>(
+                    __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst_row), 8 * k + (lane >> 2)));
+            uint8_t *stage = sstage + (warp - 2) * 2048;
+            if (pl.staged) {   // (uniform over the CTA)
+                for (int ci = half; ci < nchunks; ci += 2) {
+                    float v[32];
+                    uint32_t w[16];
+                    tmem_ld32(tb + 32 * ci, v);
+                    tmem_wait_ld();
+                    rs_chunk_words(a, R, dst_row != nullptr, n0 + 32 * ci, v, sbias + n0 + 32 * ci,
+                                   n0 + 32 * ci < a.norm_cols, w);
+                    rs_warp_store(stage, w, dk, 32 * ci, lane);
+                }
+            } else {
+                for (int ci = half; ci < nchunks; ci += 2) {
+                    float v[32];
+                    tmem_ld32(tb + 32 * ci, v);
+                    tmem_wait_ld();
+                    if (dst_row)
+                        rs_epilogue_chunk32(a, R, n0 + 32 * ci, dst_row + 32 * ci, v, sbias + n0 + 32 * ci,
+                                            n0 + 32 * ci < a.norm_cols);
+                }
             }
             if ((BN & 31) && (nchunks & 1) == half) { // 16-column tail
                 const int c0 = 32 * nchunks;
@@ -607,7 +705,8 @@ bool rs_plan(const GemmArgs &a, RsPlan &p)
     p.KB = (a.K + 63) / 64;
     p.b_bytes = (size_t)a.N * p.KB * 128;
     if (p.b_bytes > 152 * 1024) return false;
-    const size_t fixed = 1024 + p.b_bytes + 512 * 4 + BM * 8 + 256;
+    p.staged = a.epi == EPI_NONE;
+    const size_t fixed = 1024 + p.b_bytes + (p.staged ? RS_NEPI * 2048 : 0) + 512 * 4 + BM * 8 + 256;
     p.stages = (int)((227 * 1024 - fixed) / RS_STAGE);
     if (p.stages > 8) p.stages = 8;
     if (p.stages < 3) return false;
