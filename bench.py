@@ -317,6 +317,13 @@ def measure_forward(sw, w, dev, pk, args, steps, soak, rank=0, world=1, dist=Non
             kernels = per_kernel_times(sw, h, w, t, table, xs, stream, steps)
         roof = dominant_roofline(w, kernels, pk, ms)
         roof["traffic"] = profiled_traffic(w.key, roof["kernel"])
+        if roof["traffic"] is not None:
+            # ncu's DRAM counters see what reached DRAM during the launch: output
+            # still dirty in L2 when the kernel ends is written back later (and
+            # counted for whatever runs then), so traffic can read below the
+            # algorithmic bytes; above them it would mean re-reads
+            roof["traffic_note"] = ("DRAM bytes read + written during one launch (ncu); output left dirty in "
+                                    "L2 at the end is not counted")
         res["roofline"] = roof
         res["kernels_us"] = kernels
     else:
