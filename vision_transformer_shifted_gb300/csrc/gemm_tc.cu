@@ -616,7 +616,9 @@ gemm_rs_kernel(GemmArgs a_full, RsPlan pl, DeviceStatus st, const __grid_constan
         for (int nb = 0; nb < nbn; ++nb) {
             const int buf = nbn == 2 ? nb : (int)(lm & 1);
             const uint32_t par = nbn == 2 ? (uint32_t)(lm & 1) : (uint32_t)((lm >> 1) & 1);
-            if (!mbar_wait(smem_u32(&tfull[buf]), par, st.wait_ns)) {
+            // (warp-uniform outcome: the warp's TMEM loads, shuffles and staged
+            // stores below are warp-collective)
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[buf]), par, st.wait_ns))) {
                 failed = true;
                 break;
             }
