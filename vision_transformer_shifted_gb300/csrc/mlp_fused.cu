@@ -326,29 +326,25 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
             }
             return s;
         };
-#pragma unroll 1
-        for (int j = 0; ok; ++j) {
-            const int64_t tile = (int64_t)blockIdx.x + (int64_t)j * gridDim.x;
-            if (tile >= ntiles) break;
-            const int64_t tok = tile * 128 + row;
-            const bool valid = tok < a.T;
+        auto tile_of = [&](int j) { return (int64_t)blockIdx.x + (int64_t)j * gridDim.x; };
+        auto zchunk_of = [&](int ab, int col) {   // 8 channels from col (a multiple of 8) of z tile buffer ab
+            return *reinterpret_cast<const uint4 *>(sm + F::AT + ab * KB * HT + (col >> 5) * HT +
+                                                    sw64_offset(row, (col & 31) >> 3));
+        };
+        // ---- the start of tile j: its z tile landed; PRE: the row's LayerNorm
+        // statistics (rstd and -rstd mean), shifted sums (shift: the row's first
+        // channel) over this warp's channels, then over the quarter ----
+        auto begin_tile = [&](int j, float &rstd, float &nms) -> bool {
             const int ab = j & 1;
-            // this warp's CP channels of the row's z (the residual; PRE: the
-            // LayerNorm statistics too), from the tile in shared memory
-            if (!(ok = mt_warp_wait(BAR(MB_AFULL + ab), (j >> 1) & 1, st.wait_ns, abort_flag))) break;
-            auto zchunk = [&](int col) {   // 8 channels from col (a multiple of 8)
-                return *reinterpret_cast<const uint4 *>(sm + F::AT + ab * KB * HT + (col >> 5) * HT +
-                                                        sw64_offset(row, (col & 31) >> 3));
-            };
-            float rstd = 1.f, nms = 0.f;   // PRE: rstd and -rstd mean
+            if (!(ok = mt_warp_wait(BAR(MB_AFULL + ab), (j >> 1) & 1, st.wait_ns, abort_flag))) return false;
+            rstd = 1.f;
+            nms = 0.f;
             if (MODE == MLP_PRE) {
-                // shifted sums (shift: the row's first channel) over this warp's
-                // channels, then over the quarter
-                const float K = unpack_bf16x2(zchunk(0).x).x;
+                const float K = unpack_bf16x2(zchunk_of(ab, 0).x).x;
                 float s1 = 0.f, s2 = 0.f;
 #pragma unroll
                 for (int q = 0; q < CP / 8; ++q) {
-                    const uint4 u = zchunk(CP * part + 8 * q);
+                    const uint4 u = zchunk_of(ab, CP * part + 8 * q);
                     const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -359,55 +355,63 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
                     }
                 }
                 const float2 s = qsum(make_float2(s1, s2));
-                if (!ok) break;
+                if (!ok) return false;
                 const float m1 = s.x / (float)C;   // mean - K
                 rstd = rsqrtf(fmaxf(s.y / (float)C - m1 * m1, 0.f) + MT_EPS);
                 nms = -rstd * (K + m1);
             }
-            // ---- GELU of each chunk's 32 columns of this warp's part ----
-#pragma unroll 1
-            for (int c = 0; c < NC; ++c, ++n) {
-                const int b = n & 1;
-                if (!(ok = mt_warp_wait(BAR(MB_HREADY + b), (n >> 1) & 1, st.wait_ns, abort_flag))) break;
-                tc_fence_after();
-                const uint32_t tcol = t_lane + F::T_H + 128 * b + 32 * part;
-                float v[32];
-                tmem_ld32(tcol, v);
-                tmem_wait_ld();
-                const float4 *b4 = reinterpret_cast<const float4 *>(sb1 + 128 * c + 32 * part);
-                const float4 *c4 = reinterpret_cast<const float4 *>(sc1 + 128 * c + 32 * part);
-                uint32_t pk[16];
+            return true;
+        };
+        // ---- GELU of chunk c (the CTA's n-th) of a tile: this warp's 32 columns ----
+        auto gelu_chunk = [&](int c, float rstd, float nms) -> bool {
+            const int b = n & 1;
+            if (!(ok = mt_warp_wait(BAR(MB_HREADY + b), (n >> 1) & 1, st.wait_ns, abort_flag))) return false;
+            tc_fence_after();
+            const uint32_t tcol = t_lane + F::T_H + 128 * b + 32 * part;
+            float v[32];
+            tmem_ld32(tcol, v);
+            tmem_wait_ld();
+            const float4 *b4 = reinterpret_cast<const float4 *>(sb1 + 128 * c + 32 * part);
+            const float4 *c4 = reinterpret_cast<const float4 *>(sc1 + 128 * c + 32 * part);
+            uint32_t pk[16];
 #pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 bb = b4[e4];
-                    float x0, x1, x2, x3;
-                    if (MODE == MLP_PRE) {
-                        // rstd acc + (c (-rstd mean) + b')
-                        const float4 cc = c4[e4];
-                        float t0, t1, t2, t3;
-                        g2_fma(t0, t1, cc.x, cc.y, nms, nms, bb.x, bb.y);
-                        g2_fma(t2, t3, cc.z, cc.w, nms, nms, bb.z, bb.w);
-                        g2_fma(x0, x1, v[4 * e4], v[4 * e4 + 1], rstd, rstd, t0, t1);
-                        g2_fma(x2, x3, v[4 * e4 + 2], v[4 * e4 + 3], rstd, rstd, t2, t3);
-                    } else {
-                        x0 = v[4 * e4] + bb.x;
-                        x1 = v[4 * e4 + 1] + bb.y;
-                        x2 = v[4 * e4 + 2] + bb.z;
-                        x3 = v[4 * e4 + 3] + bb.w;
-                    }
-                    gelu_exact2(x0, x1);
-                    gelu_exact2(x2, x3);
-                    pk[2 * e4] = pack_bf16x2(x0, x1);
-                    pk[2 * e4 + 1] = pack_bf16x2(x2, x3);
+            for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 bb = b4[e4];
+                float x0, x1, x2, x3;
+                if (MODE == MLP_PRE) {
+                    // rstd acc + (c (-rstd mean) + b')
+                    const float4 cc = c4[e4];
+                    float t0, t1, t2, t3;
+                    g2_fma(t0, t1, cc.x, cc.y, nms, nms, bb.x, bb.y);
+                    g2_fma(t2, t3, cc.z, cc.w, nms, nms, bb.z, bb.w);
+                    g2_fma(x0, x1, v[4 * e4], v[4 * e4 + 1], rstd, rstd, t0, t1);
+                    g2_fma(x2, x3, v[4 * e4 + 2], v[4 * e4 + 3], rstd, rstd, t2, t3);
+                } else {
+                    x0 = v[4 * e4] + bb.x;
+                    x1 = v[4 * e4 + 1] + bb.y;
+                    x2 = v[4 * e4 + 2] + bb.z;
+                    x3 = v[4 * e4 + 3] + bb.w;
                 }
-                tmem_st16(tcol, pk);
-                tmem_wait_st();
-                mt_warp_arrive(BAR(MB_HBF + b), lane);   // read by GEMM2
+                gelu_exact2(x0, x1);
+                gelu_exact2(x2, x3);
+                pk[2 * e4] = pack_bf16x2(x0, x1);
+                pk[2 * e4 + 1] = pack_bf16x2(x2, x3);
             }
-            if (!ok) break;
+            tmem_st16(tcol, pk);
+            tmem_wait_st();
+            mt_warp_arrive(BAR(MB_HBF + b), lane);   // read by GEMM2
+            ++n;
+            return true;
+        };
+        // ---- the end of tile j ----
+        auto end_tile = [&](int j) -> bool {
+            const int64_t tok = tile_of(j) * 128 + row;
+            const bool valid = tok < a.T;
+            const int ab = j & 1;
+            auto zchunk = [&](int col) { return zchunk_of(ab, col); };
             // ---- this warp's CP columns: y = z + Y + b2 (POST: z + LN(Y + b2)) ----
             const int yb = j & 1;
-            if (!(ok = mt_warp_wait(BAR(MB_YREADY + yb), (j >> 1) & 1, st.wait_ns, abort_flag))) break;
+            if (!(ok = mt_warp_wait(BAR(MB_YREADY + yb), (j >> 1) & 1, st.wait_ns, abort_flag))) return false;
             tc_fence_after();
             float y[24];
             const uint32_t ycol = t_lane + F::T_Y + C * yb + CP * part;
@@ -423,7 +427,7 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
 #pragma unroll
                 for (int k = 0; k < CP; ++k) s1 += y[k];
                 const float mean = qsum(make_float2(s1, 0.f)).x / (float)C;
-                if (!ok) break;
+                if (!ok) return false;
                 float s2 = 0.f;
 #pragma unroll
                 for (int k = 0; k < CP; ++k) {
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
                     s2 = fmaf(d, d, s2);
                 }
                 const float var = qsum(make_float2(s2, 0.f)).x / (float)C;
-                if (!ok) break;
+                if (!ok) return false;
                 scale = rsqrtf(var + MT_EPS);
                 shift = -mean * scale;
             }
@@ -457,6 +461,25 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
                 }
             }
             mt_warp_arrive(BAR(MB_AFREE + ab), lane);   // (this warp's reads of the z tile are done)
+            return true;
+        };
+        // Software-pipelined over the CTA's tiles: after tile j's last chunk the
+        // warps start tile j + 1 (its statistics and first chunk) and only then
+        // take tile j's output, so that the wait for tile j's last GEMM2 runs
+        // under that work.  (Chunks stay in order n = 0, 1, ...: GEMM1 of tile j
+        // + 1's first chunk is issued before GEMM2 of tile j's last one.)
+        float r_cur = 1.f, m_cur = 0.f;
+        if (tile_of(0) < ntiles) ok = begin_tile(0, r_cur, m_cur) && gelu_chunk(0, r_cur, m_cur);
+#pragma unroll 1
+        for (int j = 0; ok && tile_of(j) < ntiles; ++j) {
+#pragma unroll 1
+            for (int c = 1; c < NC && ok; ++c) ok = gelu_chunk(c, r_cur, m_cur);
+            if (!ok) break;
+            float r_nxt = 1.f, m_nxt = 0.f;
+            if (tile_of(j + 1) < ntiles && !(ok = begin_tile(j + 1, r_nxt, m_nxt) && gelu_chunk(0, r_nxt, m_nxt))) break;
+            if (!(ok = end_tile(j))) break;
+            r_cur = r_nxt;
+            m_cur = m_nxt;
         }
         if (!ok) *abort_flag = 1;
     }
