@@ -791,6 +791,48 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             const int p_tile = sring[j & 3];
             if (p_tile < 0) break;
             const WinInfo win = window_info(g, p_tile, slot);
+            // (pre-norm fold: the row's statistics come from x while the QKV MMAs
+            // run on it)
+            float2 rs = make_float2(1.f, 0.f);
+            if (FOLD == 1) {
+                // (pre-norm fold) this row's LayerNorm statistics, from its x in
+                // X (read before the drains overwrite it, and while the QKV MMAs
+                // read it too): fp32 mean, then mean square deviation.  Rows that hold no token get finite values
+                // from whatever finite data the row holds; never stored.
+                auto xchunk = [&](int c) {
+                    return *reinterpret_cast<const uint4 *>(xg + (c >> 2) * HT + sw64_offset(row, c & 3));
+                };
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < C / 8; ++c) {
+                    const uint4 u = xchunk(c);
+                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = unpack_bf16x2(wd[e]);
+                        s4[2 * (e & 1)] += f.x;
+                        s4[2 * (e & 1) + 1] += f.y;
+                    }
+                }
+                const float mean = ((s4[0] + s4[1]) + (s4[2] + s4[3])) / (float)C;
+                float q4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < C / 8; ++c) {
+                    const uint4 u = xchunk(c);   // (read again: fewer live registers)
+                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = unpack_bf16x2(wd[e]);
+                        const float d0 = f.x - mean, d1 = f.y - mean;
+                        q4[2 * (e & 1)] = fmaf(d0, d0, q4[2 * (e & 1)]);
+                        q4[2 * (e & 1) + 1] = fmaf(d1, d1, q4[2 * (e & 1) + 1]);
+                    }
+                }
+                const float rstd = rsqrtf(((q4[0] + q4[1]) + (q4[2] + q4[3])) / (float)C + 1e-5f);
+                rs = make_float2(rstd, -rstd * mean);
+                // (G = 1: the other group writes k over these x rows)
+                if (F::SPLIT) warp_arrive(BAR(tg, BR_XREAD), lane);
+            }
             if (!(ok = warp_wait(BAR(tg, BR_QKV), kg & 1, st.wait_ns, abort_flag))) break;
             tc_fence_after();
 
@@ -801,7 +843,6 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             // [128][32] tile at dst
             // (pre-norm fold: v = rstd (acc - mean c) + bias = acc rs.x + (c rs.y +
             // bias), c the 32 column sums at csum)
-            float2 rs = make_float2(1.f, 0.f);
             auto fold_in = [&](float (&v)[32], const float *bias, const float *csum) {
                 const float4 *c4 = reinterpret_cast<const float4 *>(csum);
                 const float4 *b4 = reinterpret_cast<const float4 *>(bias);
@@ -845,45 +886,6 @@ __global__ void __launch_bounds__(FTHREADS, 1)
             // length; V1 drops the key bias: it adds q.bk / sqrt(d) to every logit
             // of a row, which the softmax cancels; V2 normalises k + bk, so keeps
             // it), each head's S MMA issued as soon as its q and k are stored.
-            if (FOLD == 1) {
-                // (pre-norm fold) this row's LayerNorm statistics, from its x in
-                // X (read before the drains overwrite it): fp32 mean, then mean
-                // square deviation.  Rows that hold no token get finite values
-                // from whatever finite data the row holds; never stored.
-                auto xchunk = [&](int c) {
-                    return *reinterpret_cast<const uint4 *>(xg + (c >> 2) * HT + sw64_offset(row, c & 3));
-                };
-                float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < C / 8; ++c) {
-                    const uint4 u = xchunk(c);
-                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = unpack_bf16x2(wd[e]);
-                        s4[2 * (e & 1)] += f.x;
-                        s4[2 * (e & 1) + 1] += f.y;
-                    }
-                }
-                const float mean = ((s4[0] + s4[1]) + (s4[2] + s4[3])) / (float)C;
-                float q4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < C / 8; ++c) {
-                    const uint4 u = xchunk(c);   // (read again: fewer live registers)
-                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = unpack_bf16x2(wd[e]);
-                        const float d0 = f.x - mean, d1 = f.y - mean;
-                        q4[2 * (e & 1)] = fmaf(d0, d0, q4[2 * (e & 1)]);
-                        q4[2 * (e & 1) + 1] = fmaf(d1, d1, q4[2 * (e & 1) + 1]);
-                    }
-                }
-                const float rstd = rsqrtf(((q4[0] + q4[1]) + (q4[2] + q4[3])) / (float)C + 1e-5f);
-                rs = make_float2(rstd, -rstd * mean);
-                // (G = 1: the other group writes k over these x rows)
-                if (F::SPLIT) warp_arrive(BAR(tg, BR_XREAD), lane);
-            }
             if (!F::SPLIT || grp == 0) {
                 if (kg > 0 && !(ok = warp_wait(BAR(tg, BR_VFREE), (kg - 1) & 1, st.wait_ns, abort_flag))) break;
                 if (FOLD == 1) {
