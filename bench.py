@@ -248,6 +248,9 @@ def measure_forward(sw, w, dev, pk, args, steps, soak, rank=0, world=1, dist=Non
     h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, mode)
     if path:
         sw.swin_wattn_set_option(h, sw.OPT_PATH, path)
+    # fixed weights across the steps, as in serving: each step's fused kernel
+    # may load them while the step before finishes
+    sw.swin_wattn_set_option(h, sw.OPT_OVERLAP_CALLS, args.overlap)
     g = generate(rank_workload(w, rank))
     t = {k: (v.to(dev) if v is not None else None) for k, v in g.items()}
     table = table_for(w, g, dev, h)
@@ -396,6 +399,7 @@ def run_ours(args, w):
                 rk, (hk, gk, *_rest) = measure_forward(sw, wk, dev, pk, args, args.config_steps, 0.3)
             sw.swin_wattn_destroy(hk)
             rk["config"] = workload_config(wk, 1)
+            rk["config"]["overlap_calls"] = bool(args.overlap)
             rk["clocks"] = clk_k.summary()
             if not args.no_cpu_baseline:
                 rk["cpu_baseline"] = oracle_baseline(wk, gk, args.config_cpu_seconds)
@@ -403,7 +407,7 @@ def run_ours(args, w):
     if rank != 0:
         return
     cfg = workload_config(w, world)
-    cfg.update({"path": res["path"], "l2": res["l2"]})
+    cfg.update({"path": res["path"], "l2": res["l2"], "overlap_calls": bool(args.overlap)})
     line = {"metric": METRIC, "value": res["tokens_per_s"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": cfg,
@@ -702,6 +706,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="images per step (0: the workload's own batch)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 three kernels, 2 fused")
+    ap.add_argument("--overlap", type=int, default=1, choices=[0, 1],
+                    help="1: successive forwards overlap (fixed weights; SWIN_WATTN_OPT_OVERLAP_CALLS)")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=3.0)

@@ -81,9 +81,21 @@ enum {
                                       2 = the fused single-kernel block */
     SWIN_WATTN_OPT_WAIT_LIMIT_US = 2, /* limit of every device-side wait, microseconds
                                          (default 2,000,000) */
-    SWIN_WATTN_OPT_HOST_CHUNKS = 3   /* chunks of whole images that
+    SWIN_WATTN_OPT_HOST_CHUNKS = 3,  /* chunks of whole images that
                                         swin_wattn_forward_host overlaps (1..16,
                                         default 8; fewer when B is smaller) */
+    SWIN_WATTN_OPT_OVERLAP_CALLS = 4 /* 0 (default) or 1: swin_wattn_forward's
+                                        fused kernel may start while the kernels
+                                        queued before it on the stream finish
+                                        (programmatic dependent launch): it loads
+                                        the parameters (Wqkv, bqkv, the bias table,
+                                        logit_scale, Wproj, bproj) during that time
+                                        and waits for the earlier work before it
+                                        reads x or writes out.  With 1 the caller
+                                        guarantees that no work queued before a
+                                        call writes that call's parameters (fixed
+                                        weights, as in serving).  Other paths and
+                                        the host-buffer forward are unaffected. */
 };
 
 /* Creates a handle for blocks with C channels, `heads` heads (d = C/heads),

@@ -517,6 +517,45 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 
 # ---- the stored oracle outputs (tests/golden) --------------------------------
 
+@pytest.mark.parametrize("key", ["swin_t_s1", "swinv2_t_s1"])
+def test_overlapped_calls_give_the_same_bits(key):
+    """SWIN_WATTN_OPT_OVERLAP_CALLS lets a call's fused kernel start while the
+    previous call's kernel finishes: three chained calls on one stream (each
+    call's x the previous call's output) give the bits of the same calls
+    without the option."""
+    w = WORKLOADS[key].with_(B=8)
+    g = generate(w, nonzero_bias=True, tau=(0.3, 0.01, 0.05)[: w.heads] if w.mode == V2 else 0.1)
+    t = device_inputs(g)
+    table = oracle_table(w, g).to(DEV)
+
+    def chain(overlap):
+        h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
+        try:
+            sw.swin_wattn_set_option(h, sw.OPT_OVERLAP_CALLS, overlap)
+            outs, cur = [], t["x"]
+            for _ in range(3):
+                o = torch.full_like(t["x"], float("nan"))
+                sw.swin_wattn_forward(h, cur, t["Wqkv"], t["bqkv"], table, t.get("tau"), t["Wproj"], t["bproj"], o)
+                outs.append(o)
+                cur = o
+            assert sw.swin_wattn_sync_status(h) == sw.OK
+            assert sw.swin_wattn_last_launches(h) == 1   # the fused kernel
+            return outs
+        finally:
+            sw.swin_wattn_destroy(h)
+
+    plain, overlapped = chain(0), chain(1)
+    for a, b in zip(plain, overlapped):
+        assert torch.equal(a, b)
+    with pytest.raises(sw.SwinWAttnError):
+        h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
+        try:
+            sw.swin_wattn_set_option(h, sw.OPT_OVERLAP_CALLS, 2)
+        finally:
+            sw.swin_wattn_destroy(h)
+
+
+
 @pytest.mark.parametrize("name", ["v1", "v2"])
 def test_stored_golden_case(name):
     """The tiny stored case (8 x 8 tokens, C = 32, one head, M = 4, shift 2)

@@ -18,7 +18,7 @@ from . import build as _build
 V1, V2, FP32 = 0, 1, 0x10
 OK, EINVAL, EUNSUPPORTED, ECUDA, ENOMEM, ETIMEOUT, ESCRATCH, ECORRUPT = 0, -1, -2, -3, -4, -5, -6, -7
 NOALLOC_MAX_INTERMEDIATE_BYTES = (64 << 20) - 256
-OPT_PATH, OPT_WAIT_LIMIT_US, OPT_HOST_CHUNKS = 1, 2, 3
+OPT_PATH, OPT_WAIT_LIMIT_US, OPT_HOST_CHUNKS, OPT_OVERLAP_CALLS = 1, 2, 3, 4
 PATH_AUTO, PATH_THREE_KERNELS, PATH_FUSED, PATH_FP32 = 0, 1, 2, 3
 
 _lib = None

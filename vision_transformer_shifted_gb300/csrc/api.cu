@@ -40,6 +40,7 @@ struct swin_wattn_s {
     const void *g_args[11];   // the call's pointers and the buffers the graph uses
     int g_B, g_H, g_W, g_path, g_launches, g_chunks;
     int host_chunks;   // chunks of the host-buffer forward (1..HOST_CHUNKS)
+    int overlap;       // SWIN_WATTN_OPT_OVERLAP_CALLS
 };
 
 namespace {
@@ -79,9 +80,11 @@ int check_host_guards(const swin_wattn_s *h, cudaStream_t s)
     return SWIN_WATTN_OK;
 }
 
+// (overlap: the fused kernel may start while the stream's earlier kernels
+// finish, see SWIN_WATTN_OPT_OVERLAP_CALLS)
 int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void *Wqkv, const void *bqkv,
                 const void *table, const float *tau, const void *Wproj, const void *bproj, void *out,
-                cudaStream_t stream)
+                cudaStream_t stream, bool overlap = false)
 {
     const Geom g = make_geom(B, H, W, h->C, h->M, h->shift);
     h->last_launches = 0;
@@ -102,7 +105,7 @@ int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void 
         if (!fused_supported(h->M, h->C, h->heads) || g.T >= ((int64_t)1 << 31)) return SWIN_WATTN_EUNSUPPORTED;
         cudaError_t e = launch_fused((const bf16 *)x, (const bf16 *)Wqkv, (const bf16 *)bqkv, (const bf16 *)table, tau,
                                      (const bf16 *)Wproj, (const bf16 *)bproj, (bf16 *)out, h->mode, g, dstatus(h),
-                                     h->d_err + 2, stream);
+                                     h->d_err + 2, stream, nullptr, nullptr, 0, overlap ? 1 : 0);
         if (e != cudaSuccess) {
             h->last_cuda_error = e;
             return SWIN_WATTN_ECUDA;
@@ -265,6 +268,7 @@ int swin_wattn_create(swin_wattn_t *out, int C, int heads, int M, int shift, int
     h->mode = mode & SWIN_WATTN_V2; h->fp32 = fp32;
     h->path_opt = 0;
     h->host_chunks = 8;
+    h->overlap = 0;
     h->wait_ns = 2000000000ull;
     if (cudaGetDevice(&h->device) != cudaSuccess) { delete h; cudaGetLastError(); return SWIN_WATTN_ECUDA; }
     // [0] the error word, [2..3] the fused kernel's tile counter and CTAs done
@@ -305,7 +309,8 @@ int swin_wattn_forward(swin_wattn_t h, const void *x, int B, int H, int W, const
 {
     int rc = check_forward_args(h, x, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out, true);
     if (rc) return rc;
-    rc = run_forward(h, x, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out, (cudaStream_t)stream);
+    rc = run_forward(h, x, B, H, W, Wqkv, bqkv, bias_table, logit_scale, Wproj, bproj, out, (cudaStream_t)stream,
+                     h->overlap != 0);
     if (rc) return rc;
     return ws_check(h->ws, (cudaStream_t)stream);
 }
@@ -441,6 +446,10 @@ int swin_wattn_set_option(swin_wattn_t h, int option, int64_t value)
     case SWIN_WATTN_OPT_HOST_CHUNKS:
         if (value < 1 || value > HOST_CHUNKS) return SWIN_WATTN_EINVAL;
         h->host_chunks = (int)value;
+        return SWIN_WATTN_OK;
+    case SWIN_WATTN_OPT_OVERLAP_CALLS:
+        if (value < 0 || value > 1) return SWIN_WATTN_EINVAL;
+        h->overlap = (int)value;
         return SWIN_WATTN_OK;
     default:
         return SWIN_WATTN_EINVAL;

@@ -217,7 +217,7 @@ cudaError_t launch_mlp_fused(const bf16 *z, const bf16 *W1, const bf16 *b1, cons
 cudaError_t launch_fused(const bf16 *x, const bf16 *Wqkv, const bf16 *bqkv, const bf16 *table, const float *tau,
                          const bf16 *Wproj, const bf16 *bproj, bf16 *out, int mode, const Geom &g, DeviceStatus st,
                          int *sched, cudaStream_t stream, const bf16 *ln_g = nullptr, const bf16 *ln_b = nullptr,
-                         int fold = 0);
+                         int fold = 0, int overlap = 0);
 
 // Tensor map over a row-major bf16 matrix [rows, cols] (16-byte aligned base,
 // cols * 2 a multiple of 16): boxes of 32 columns x box_rows rows (<= 256),

@@ -81,6 +81,10 @@ struct FusedArgs {
     // (The kernel takes it as its FOLD parameter.)
     const bf16 *ln_g, *ln_b;
     int fold;
+    // (host side) launched with programmatic stream serialization: the kernel's
+    // prologue (weights, biases, tables) may run while the kernels queued
+    // before it finish; everything after it waits for them
+    int overlap;
 };
 
 // The folded variants (fold 1, 2), built in their own translation unit.
@@ -523,6 +527,11 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     // slot is written again four tiles later, after XFREE of tile j + 4 - G,
     // which every reader of tile j has passed by then.
 
+    // The prologue above reads only the parameters; x, the tile counter and out
+    // wait for the kernels queued before this one (a no-op unless launched to
+    // overlap them), and the next such kernel may start its own prologue.
+    griddep_launch_dependents();
+    griddep_wait();
     if (warp == PWARP) {
         // ===================== producer warp: x gathers =====================
         const bool tma_thread = lane == 0;
@@ -1258,7 +1267,18 @@ cudaError_t launch_fused_t(const FusedArgs &a, DeviceStatus st, cudaStream_t str
     if (e != cudaSuccess) return e;
     const int64_t ntiles = (a.g.nwin + 1) / 2;
     const int grid = (int)(ntiles < num_sms() ? ntiles : num_sms());
-    kern<<<grid, FTHREADS, smem, stream>>>(a, st, tx, to);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(FTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = a.overlap ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a, st, tx, to);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -281,6 +281,14 @@ __device__ __forceinline__ void mma_bf16_ts_mask(uint32_t d_tmem, uint32_t a_tme
         : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream serialization attribute may start while the kernels before it in the
+// stream run; griddep_wait() returns once they have completed and their memory
+// is visible (at once without the attribute), and griddep_launch_dependents()
+// lets the next such kernel start once every CTA has called it or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Arrives once on the mbarrier when every tcgen05 operation this thread issued
 // before it has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
