@@ -501,6 +501,7 @@ def run_block(args, w, ratio=4):
                   logit_scale=t.get("tau"), Wproj=t["Wproj"], bproj=t["bproj"], ln2_gamma=t["ln2_gamma"],
                   ln2_beta=t["ln2_beta"], W1=t["mlp_W1"], b1=t["mlp_b1"], W2=t["mlp_W2"], b2=t["mlp_b2"])
     h = sw.swin_block_create(w.C, w.heads, w.M, w.shift, w.mode, ratio)
+    sw.swin_block_set_option(h, sw.BLOCK_OPT_OVERLAP_CALLS, args.overlap)   # fixed weights across steps
     io_bytes = w.tokens * w.C * 2 * 2
     nsets = max(2, -(-(2 * L2_BYTES) // io_bytes) + 1)
     xs = [t["x"]] + [torch.randn_like(t["x"], dtype=torch.float32).to(t["x"].dtype) for _ in range(nsets - 1)]
@@ -543,7 +544,7 @@ def run_block(args, w, ratio=4):
             "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": C, "heads": w.heads, "M": w.M,
                        "shift": w.shift, "mode": "V1 pre-norm" if w.mode == V1 else "V2 residual post-norm",
-                       "mlp_ratio": ratio},
+                       "mlp_ratio": ratio, "overlap_calls": bool(args.overlap)},
             "tflops": tflops,
             "block_roofline": {"achieved_tflops": tflops, "roof_tflops": roof_tf, "frac": tflops / roof_tf,
                                "ai_flop_per_byte": ai, "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
@@ -573,6 +574,7 @@ def run_stage(args, w, depth, ratio=4):
                       ln2_gamma=t["ln2_gamma"], ln2_beta=t["ln2_beta"], W1=t["mlp_W1"], b1=t["mlp_b1"],
                       W2=t["mlp_W2"], b2=t["mlp_b2"])
         blocks.append((sw.swin_block_create(w.C, w.heads, w.M, wi.shift, w.mode, ratio), params, t["x"]))
+        sw.swin_block_set_option(blocks[-1][0], sw.BLOCK_OPT_OVERLAP_CALLS, args.overlap)
     gm = torch.Generator().manual_seed(w.seed + 555)
     gam = (1 + 0.1 * torch.randn(4 * w.C, generator=gm)).bfloat16().to(dev)
     bet = (0.1 * torch.randn(4 * w.C, generator=gm)).bfloat16().to(dev)
@@ -623,7 +625,8 @@ def run_stage(args, w, depth, ratio=4):
             "config": {"workload": w.key, "B": w.B, "H": w.H, "W": w.W, "C": w.C, "heads": w.heads, "M": w.M,
                        "depth": depth, "extra_norm_every": args.extra_norm,
                        "mode": "V1 pre-norm" if w.mode == V1 else "V2 residual post-norm",
-                       "mlp_ratio": ratio, "l2": "not flushed: one input set (the stage's own intermediates, "
+                       "mlp_ratio": ratio, "overlap_calls": bool(args.overlap),
+                       "l2": "not flushed: one input set (the stage's own intermediates, "
                        "%.0f MB per block, exceed L2)" % (w.tokens * w.C * (3 + ratio) * 2 / 1e6)},
             "gpu_launches": launches * args.steps, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)

@@ -80,6 +80,25 @@ int swin_block_sync_status(swin_block_t h, swin_stream_t stream);
  * for a NULL handle. */
 int swin_block_last_launches(swin_block_t h);
 
+/* Options for swin_block_set_option. */
+enum {
+    SWIN_BLOCK_OPT_OVERLAP_CALLS = 1 /* 0 (default) or 1: the block's fused kernels
+                                        (the attention with LayerNorm 1 folded in
+                                        and the MLP) may start while the kernels
+                                        queued before them on the stream finish
+                                        (programmatic dependent launch): each loads
+                                        its parameters during that time and waits
+                                        for the earlier work before it reads its
+                                        input or writes its output.  With 1 the
+                                        caller guarantees that no work queued before
+                                        a forward writes that forward's parameters
+                                        (fixed weights, as in serving). */
+};
+
+/* Sets an option (see SWIN_BLOCK_OPT_*).  EINVAL for a NULL handle, unknown
+ * options or values. */
+int swin_block_set_option(swin_block_t h, int option, int64_t value);
+
 /* Frees the handle and its workspace (NULL is a no-op). */
 int swin_block_destroy(swin_block_t h);
 

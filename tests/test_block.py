@@ -376,6 +376,39 @@ def test_block_launches_show_the_fusions(key, C, heads, want):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("key", ["swin_t_s1", "swinv2_t_s1", "swin_b_s1"])
+def test_overlapped_block_calls_give_the_same_bits(key):
+    """SWIN_BLOCK_OPT_OVERLAP_CALLS lets each of the block's fused kernels start
+    while the kernel before it finishes: three chained blocks on one stream
+    (each block's x the previous block's output, so every kernel reads what
+    the one before wrote) give the bits of the same blocks without it."""
+    w = WORKLOADS[key].with_(B=4)
+    g = generate_block(w)
+    table = oracle_table(w, g)
+    dev = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in _block_params_dev(g, table).items()}
+    x = g["x"].to(DEV)
+
+    def chain(overlap):
+        h = sw.swin_block_create(w.C, w.heads, w.M, w.shift, w.mode, 4)
+        try:
+            sw.swin_block_set_option(h, sw.BLOCK_OPT_OVERLAP_CALLS, overlap)
+            outs, cur = [], x
+            for _ in range(3):
+                o = torch.full_like(x, float("nan"))
+                sw.swin_block_forward(h, cur, dev, o)
+                outs.append(o)
+                cur = o
+            assert sw.swin_block_sync_status(h) == sw.OK
+            return outs
+        finally:
+            sw.swin_block_destroy(h)
+
+    plain, overlapped = chain(0), chain(1)
+    for a, b in zip(plain, overlapped):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("key", ["swin_t_s1", "swinv2_t_s1"])
 def test_block_forward_full_size(key):
     """Full-size grid, every output element against the block oracle."""

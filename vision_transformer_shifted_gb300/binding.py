@@ -19,6 +19,7 @@ V1, V2, FP32 = 0, 1, 0x10
 OK, EINVAL, EUNSUPPORTED, ECUDA, ENOMEM, ETIMEOUT, ESCRATCH, ECORRUPT = 0, -1, -2, -3, -4, -5, -6, -7
 NOALLOC_MAX_INTERMEDIATE_BYTES = (64 << 20) - 256
 OPT_PATH, OPT_WAIT_LIMIT_US, OPT_HOST_CHUNKS, OPT_OVERLAP_CALLS = 1, 2, 3, 4
+BLOCK_OPT_OVERLAP_CALLS = 1
 PATH_AUTO, PATH_THREE_KERNELS, PATH_FUSED, PATH_FP32 = 0, 1, 2, 3
 
 _lib = None
@@ -55,6 +56,7 @@ _SIGNATURES = {
     "swin_block_sync_status": ["p", "p"],
     "swin_block_destroy": ["p"],
     "swin_block_last_launches": ["p"],
+    "swin_block_set_option": ["p", "i", "l"],
     "swin_block_test_layernorm": ["p", "p", "p", "p", "p", "p", "i", "i", "i", "p"],
     "swin_stage_norm": ["p", "i", "i", "p", "p", "p", "p"],
     "swin_merge_create": ["pp", "i"],
@@ -274,6 +276,10 @@ def swin_block_forward(h, x, params, out, stream=None):
 
 def swin_block_last_launches(h):
     return load().swin_block_last_launches(h)
+
+
+def swin_block_set_option(h, option, value):
+    return _check("swin_block_set_option", load().swin_block_set_option(h, option, int(value)))
 
 
 def swin_block_sync_status(h, stream=None):

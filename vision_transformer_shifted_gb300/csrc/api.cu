@@ -237,7 +237,8 @@ int attn_forward_folded(swin_wattn_t h, const void *x, int B, int H, int W, cons
     if (B == 0) return SWIN_WATTN_OK;
     cudaError_t e = launch_fused((const bf16 *)x, (const bf16 *)Wqkv, (const bf16 *)bqkv, (const bf16 *)bias_table,
                                  logit_scale, (const bf16 *)Wproj, (const bf16 *)bproj, (bf16 *)out, h->mode, g,
-                                 dstatus(h), h->d_err + 2, stream, (const bf16 *)ln_g, (const bf16 *)ln_b, fold);
+                                 dstatus(h), h->d_err + 2, stream, (const bf16 *)ln_g, (const bf16 *)ln_b, fold,
+                                 h->overlap);
     if (e != cudaSuccess) {
         h->last_cuda_error = e;
         return SWIN_WATTN_ECUDA;

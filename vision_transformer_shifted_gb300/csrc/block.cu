@@ -183,6 +183,7 @@ struct swin_block_s {
     void *ws;   // z, t1, t2 [T, C] and m1 [T, rC], bf16
     size_t ws_bytes;
     int last_launches;   // of the last forward
+    int overlap;         // SWIN_BLOCK_OPT_OVERLAP_CALLS
 };
 
 extern "C" {
@@ -219,6 +220,22 @@ int swin_block_create(swin_block_t *out, int C, int heads, int M, int shift, int
 }
 
 int swin_block_last_launches(swin_block_t h) { return h ? h->last_launches : -1; }
+
+int swin_block_set_option(swin_block_t h, int option, int64_t value)
+{
+    if (!h) return SWIN_WATTN_EINVAL;
+    switch (option) {
+    case SWIN_BLOCK_OPT_OVERLAP_CALLS: {
+        if (value < 0 || value > 1) return SWIN_WATTN_EINVAL;
+        const int rc = swin_wattn_set_option(h->attn, SWIN_WATTN_OPT_OVERLAP_CALLS, value);
+        if (rc != SWIN_WATTN_OK) return rc;
+        h->overlap = (int)value;
+        return SWIN_WATTN_OK;
+    }
+    default:
+        return SWIN_WATTN_EINVAL;
+    }
+}
 
 int swin_block_destroy(swin_block_t h)
 {
@@ -312,7 +329,7 @@ int swin_block_forward(swin_block_t h, const void *x, int B, int H, int W, const
         if (mlp_fused_supported(C, R)) {
             h->last_launches += 1;
             return launch_mlp_fused(z, (const bf16 *)p->W1, (const bf16 *)p->b1, (const bf16 *)p->W2,
-                                    (const bf16 *)p->b2, g2, be2, !v1, yy, T, C, R, st, s);
+                                    (const bf16 *)p->b2, g2, be2, !v1, yy, T, C, R, st, s, h->overlap);
         }
         cudaError_t e2;
         if (v1) {

@@ -210,7 +210,7 @@ int attn_forward_folded(::swin_wattn_s *h, const void *x, int B, int H, int W, c
 bool mlp_fused_supported(int C, int R);
 cudaError_t launch_mlp_fused(const bf16 *z, const bf16 *W1, const bf16 *b1, const bf16 *W2, const bf16 *b2,
                              const bf16 *ln_g, const bf16 *ln_b, bool post, bf16 *out, int64_t T, int C, int R,
-                             DeviceStatus st, cudaStream_t stream);
+                             DeviceStatus st, cudaStream_t stream, int overlap = 0);
 
 // sched: two device ints, zero before the first launch (the kernel's tile
 // counter; each launch leaves them zero); one launch at a time per pair.

@@ -232,6 +232,11 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     auto A = [&](int buf) { return base + F::AT + buf * KB * HT; };
 
+    // The prologue above reads only the parameters; z and out wait for the
+    // kernels queued before this one (a no-op unless launched to overlap them),
+    // and the next such kernel may start its own prologue.
+    griddep_launch_dependents();
+    griddep_wait();
     if (warp == 0) {
         // ===================== producer: z tiles =====================
         bool ok = true;
@@ -504,7 +509,7 @@ int mlp_num_sms()
 }
 
 template <int C, int R, int MODE>
-cudaError_t launch_mlp_t(const bf16 *z, const MlpArgs &a, DeviceStatus st, cudaStream_t stream)
+cudaError_t launch_mlp_t(const bf16 *z, const MlpArgs &a, DeviceStatus st, cudaStream_t stream, int overlap)
 {
     using F = MlpCfg<C, R>;
     const size_t smem = F::BYTES + 1024;
@@ -516,7 +521,19 @@ cudaError_t launch_mlp_t(const bf16 *z, const MlpArgs &a, DeviceStatus st, cudaS
     if (e != cudaSuccess) return e;
     const int64_t ntiles = (a.T + 127) / 128;
     const int grid = (int)(ntiles < mlp_num_sms() ? ntiles : mlp_num_sms());
-    kern<<<grid, MT_THREADS, smem, stream>>>(a, st, tz);
+    // (overlap: programmatic stream serialization, see the prologue's end)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(MT_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a, st, tz);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -526,14 +543,16 @@ bool mlp_fused_supported(int C, int R) { return (C == 96 && R == 384) || (C == 6
 
 cudaError_t launch_mlp_fused(const bf16 *z, const bf16 *W1, const bf16 *b1, const bf16 *W2, const bf16 *b2,
                              const bf16 *ln_g, const bf16 *ln_b, bool post, bf16 *out, int64_t T, int C, int R,
-                             DeviceStatus st, cudaStream_t stream)
+                             DeviceStatus st, cudaStream_t stream, int overlap)
 {
     if (!mlp_fused_supported(C, R) || !z || !W1 || !W2 || !ln_g || !ln_b || !out || T <= 0)
         return cudaErrorInvalidValue;
     const MlpArgs a{W1, b1, W2, b2, ln_g, ln_b, out, T};
     if (C == 96)
-        return post ? launch_mlp_t<96, 384, MLP_POST>(z, a, st, stream) : launch_mlp_t<96, 384, MLP_PRE>(z, a, st, stream);
-    return post ? launch_mlp_t<64, 256, MLP_POST>(z, a, st, stream) : launch_mlp_t<64, 256, MLP_PRE>(z, a, st, stream);
+        return post ? launch_mlp_t<96, 384, MLP_POST>(z, a, st, stream, overlap)
+                    : launch_mlp_t<96, 384, MLP_PRE>(z, a, st, stream, overlap);
+    return post ? launch_mlp_t<64, 256, MLP_POST>(z, a, st, stream, overlap)
+                : launch_mlp_t<64, 256, MLP_PRE>(z, a, st, stream, overlap);
 }
 
 } // namespace swin
