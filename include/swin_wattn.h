@@ -85,17 +85,19 @@ enum {
                                         swin_wattn_forward_host overlaps (1..16,
                                         default 8; fewer when B is smaller) */
     SWIN_WATTN_OPT_OVERLAP_CALLS = 4 /* 0 (default) or 1: swin_wattn_forward's
-                                        fused kernel may start while the kernels
+                                        kernels may start while the kernels
                                         queued before it on the stream finish
-                                        (programmatic dependent launch): it loads
+                                        (programmatic dependent launch): they load
                                         the parameters (Wqkv, bqkv, the bias table,
                                         logit_scale, Wproj, bproj) during that time
-                                        and waits for the earlier work before it
-                                        reads x or writes out.  With 1 the caller
+                                        and wait for the earlier work before they
+                                        read x or write out.  With 1 the caller
                                         guarantees that no work queued before a
                                         call writes that call's parameters (fixed
-                                        weights, as in serving).  Other paths and
-                                        the host-buffer forward are unaffected. */
+                                        weights, as in serving).  The three-kernel
+                                        path's kernels overlap the same way, each
+                                        with the one before it; the host-buffer
+                                        forward is unaffected. */
 };
 
 /* Creates a handle for blocks with C channels, `heads` heads (d = C/heads),

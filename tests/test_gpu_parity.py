@@ -517,14 +517,16 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 
 # ---- the stored oracle outputs (tests/golden) --------------------------------
 
-@pytest.mark.parametrize("key", ["swin_t_s1", "swinv2_t_s1"])
-def test_overlapped_calls_give_the_same_bits(key):
-    """SWIN_WATTN_OPT_OVERLAP_CALLS lets a call's fused kernel start while the
-    previous call's kernel finishes: three chained calls on one stream (each
-    call's x the previous call's output) give the bits of the same calls
-    without the option."""
-    w = WORKLOADS[key].with_(B=8)
-    g = generate(w, nonzero_bias=True, tau=(0.3, 0.01, 0.05)[: w.heads] if w.mode == V2 else 0.1)
+@pytest.mark.parametrize("key,path,B,H,W", [("swin_t_s1", 0, 8, 56, 56), ("swinv2_t_s1", 0, 8, 64, 64),
+                                            ("swin_t_s1", 1, 8, 56, 56), ("swinv2_l_w24", 0, 1, 96, 96)])
+def test_overlapped_calls_give_the_same_bits(key, path, B, H, W):
+    """SWIN_WATTN_OPT_OVERLAP_CALLS lets a call's kernels start while the
+    kernels before them finish (the fused kernel the previous call's; on the
+    three-kernel path each kernel the one before it): three chained calls on
+    one stream (each call's x the previous call's output) give the bits of the
+    same calls without the option."""
+    w = WORKLOADS[key].with_(B=B, H=H, W=W)
+    g = generate(w, nonzero_bias=True, tau=(0.3, 0.01, 0.05, 0.1, 0.2, 0.02)[: w.heads] if w.mode == V2 else 0.1)
     t = device_inputs(g)
     table = oracle_table(w, g).to(DEV)
 
@@ -532,6 +534,8 @@ def test_overlapped_calls_give_the_same_bits(key):
         h = sw.swin_wattn_create(w.C, w.heads, w.M, w.shift, w.mode)
         try:
             sw.swin_wattn_set_option(h, sw.OPT_OVERLAP_CALLS, overlap)
+            if path:
+                sw.swin_wattn_set_option(h, sw.OPT_PATH, path)
             outs, cur = [], t["x"]
             for _ in range(3):
                 o = torch.full_like(t["x"], float("nan"))
@@ -539,7 +543,7 @@ def test_overlapped_calls_give_the_same_bits(key):
                 outs.append(o)
                 cur = o
             assert sw.swin_wattn_sync_status(h) == sw.OK
-            assert sw.swin_wattn_last_launches(h) == 1   # the fused kernel
+            assert sw.swin_wattn_last_launches(h) == (3 if path == 1 or w.M > 8 else 1)
             return outs
         finally:
             sw.swin_wattn_destroy(h)

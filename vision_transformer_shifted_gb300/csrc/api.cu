@@ -123,16 +123,21 @@ int run_forward(swin_wattn_s *h, const void *x, int B, int H, int W, const void 
     k1.A = (const bf16 *)x; k1.lda = h->C; k1.Bw = (const bf16 *)Wqkv; k1.bias = (const bf16 *)bqkv;
     k1.D = qkv; k1.ldd = 3 * h->C; k1.rows = g.T; k1.N = 3 * h->C; k1.K = h->C; k1.g = g;
     k1.norm_cols = h->mode == SWIN_WATTN_V2 ? 2 * h->C : 0;
+    // (overlap: each kernel's prologue -- weights, tables -- runs while the one
+    // before it finishes; the workspace is written only after the previous
+    // kernel, and so every earlier one, has completed)
+    k1.overlap = overlap ? 1 : 0;
     cudaError_t e = launch_gemm(k1, LOAD_GATHER, STORE_PLAIN, dstatus(h), stream);
     if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
     AttnArgs k2{};
     k2.qkv = qkv; k2.attn = attn; k2.table = (const bf16 *)table; k2.tau = tau; k2.heads = h->heads;
-    k2.mode = h->mode; k2.g = g;
+    k2.mode = h->mode; k2.g = g; k2.overlap = overlap ? 1 : 0;
     e = launch_attention(k2, dstatus(h), stream);
     if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
     GemmArgs k3{};
     k3.A = attn; k3.lda = h->C; k3.Bw = (const bf16 *)Wproj; k3.bias = (const bf16 *)bproj;
     k3.D = (bf16 *)out; k3.ldd = h->C; k3.rows = g.T; k3.N = h->C; k3.K = h->C; k3.g = g;
+    k3.overlap = overlap ? 1 : 0;
     e = launch_gemm(k3, LOAD_PLAIN, STORE_SCATTER, dstatus(h), stream);
     if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
     h->last_launches = 3;

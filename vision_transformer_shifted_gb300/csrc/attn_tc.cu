@@ -379,7 +379,8 @@ cudaError_t launch_attention(const AttnArgs &a, DeviceStatus st, cudaStream_t st
     const Geom &g = a.g;
     if (g.C != a.heads * 32) return cudaErrorInvalidValue;
     if (g.N <= 64) {
-        return launch_attn_forward_tc(a.qkv, a.table, a.tau, a.heads, a.mode == 1 ? 1 : 0, g, a.attn, st, stream);
+        return launch_attn_forward_tc(a.qkv, a.table, a.tau, a.heads, a.mode == 1 ? 1 : 0, g, a.attn, st, stream,
+                                      a.overlap);
     } else if (attn_window_supported(g.M, a.heads)) {
         return launch_attn_window(a, st, stream);
     } else {

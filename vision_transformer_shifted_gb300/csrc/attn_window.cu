@@ -278,6 +278,11 @@ __global__ void __launch_bounds__(AW_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // the prologue read only the tables and tau: q, k, v and the output wait
+    // for the kernels queued before this one (a no-op unless launched to
+    // overlap them)
+    griddep_launch_dependents();
+    griddep_wait();
 
     if (warp == 0) {
         // ===================== loads =====================
@@ -595,7 +600,8 @@ cudaError_t launch_window_t(const AttnArgs &a, DeviceStatus st, cudaStream_t str
     if (e != cudaSuccess) return e;
     const int64_t units = a.g.nwin * a.heads;
     const int grid = (int)(units < aw_num_sms() ? units : aw_num_sms());
-    kern<<<grid, AW_THREADS, smem, stream>>>(a, st, tq, tkv);
+    e = launch_maybe_overlapped(kern, dim3(grid), dim3(AW_THREADS), smem, stream, a.overlap, a, st, tq, tkv);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -218,6 +218,10 @@ attn_tc_kernel(const bf16 *table, const float *tau, int heads, int v2, Geom g, b
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // (every read of q, k, v, dO comes after: a no-op unless launched to
+    // overlap the kernels before it)
+    griddep_launch_dependents();
+    griddep_wait();
     // a contiguous range of units per CTA (head changes at most a few times)
     const int64_t u_begin = nunits * blockIdx.x / gridDim.x, u_end = nunits * (blockIdx.x + 1) / gridDim.x;
     if (tid == 0 && u_begin < u_end) load_unit(u_begin);
@@ -477,7 +481,7 @@ namespace {
 template <bool BW>
 cudaError_t launch_attn_tc(const bf16 *qkv, const bf16 *dO, const bf16 *table, const float *tau, int heads, int v2,
                            const Geom &g, bf16 *attn, bf16 *dqkv, float *dtable, const float *norms, float *dtau,
-                           DeviceStatus st, cudaStream_t stream)
+                           DeviceStatus st, cudaStream_t stream, int overlap = 0)
 {
     if (!attn_backward_supported(g.M, g.C, heads)) return cudaErrorInvalidValue;
     CUtensorMap tm_qkv, tm_do;
@@ -499,8 +503,9 @@ cudaError_t launch_attn_tc(const bf16 *qkv, const bf16 *dO, const bf16 *table, c
     const int64_t units = (g.nwin + 1) / 2 * heads;
     const int64_t cap = (int64_t)sms * TbLayout<BW>::CTAS_PER_SM;
     const unsigned grid = (unsigned)(units < cap ? units : cap);
-    attn_tc_kernel<BW><<<grid, TB_THREADS, smem, stream>>>(table, tau, heads, v2, g, attn, dqkv, dtable, norms, dtau,
-                                                            st, tm_qkv, tm_do);
+    e = launch_maybe_overlapped(attn_tc_kernel<BW>, dim3(grid), dim3(TB_THREADS), smem, stream, overlap, table, tau,
+                                heads, v2, g, attn, dqkv, dtable, norms, dtau, st, tm_qkv, tm_do);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -514,10 +519,10 @@ cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *ta
 }
 
 cudaError_t launch_attn_forward_tc(const bf16 *qkv, const bf16 *table, const float *tau, int heads, int v2,
-                                   const Geom &g, bf16 *attn, DeviceStatus st, cudaStream_t stream)
+                                   const Geom &g, bf16 *attn, DeviceStatus st, cudaStream_t stream, int overlap)
 {
     return launch_attn_tc<false>(qkv, nullptr, table, tau, heads, v2, g, attn, nullptr, nullptr, nullptr, nullptr, st,
-                                 stream);
+                                 stream, overlap);
 }
 
 } // namespace swin

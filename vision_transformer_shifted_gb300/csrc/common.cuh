@@ -142,6 +142,8 @@ struct GemmArgs {
     int epi;         // EPI_NONE, EPI_GELU (GELU after the bias), EPI_RESID (add R after the bias)
     const bf16 *R;   // EPI_RESID: [rows, ldr] row-major (plain store only)
     int64_t ldr;
+    int overlap;     // launched to overlap the kernels before it (programmatic dependent
+                     // launch): its prologue reads Bw and bias before they finish
 };
 enum { EPI_NONE = 0, EPI_GELU = 1, EPI_RESID = 2 };
 
@@ -171,6 +173,8 @@ struct AttnArgs {
     float *lse;           // windows of more than 64 tokens, not null: log2 of each row's softmax
                           // normaliser over the log2-scaled logits, [T, heads] (window order)
     int o_token_order;    // windows of more than 64 tokens: write attn in token order
+    int overlap;          // launched to overlap the kernels before it (programmatic dependent
+                          // launch): its prologue reads table and tau before they finish
 };
 
 cudaError_t launch_attention(const AttnArgs &a, DeviceStatus st, cudaStream_t stream);
@@ -281,6 +285,7 @@ cudaError_t launch_attn_flash_backward(const bf16 *qkv, const bf16 *dO, const bf
 // tokens): attn [T, C] (window order) = P v from qkv [T, 3C] (window order);
 // v2: cosine logits over the already normalised q, k, scaled by 1/max(tau, 0.01).
 cudaError_t launch_attn_forward_tc(const bf16 *qkv, const bf16 *table, const float *tau, int heads, int v2,
-                                   const Geom &g, bf16 *attn, DeviceStatus st, cudaStream_t stream);
+                                   const Geom &g, bf16 *attn, DeviceStatus st, cudaStream_t stream,
+                                   int overlap = 0);
 
 } // namespace swin

@@ -117,6 +117,10 @@ __global__ void __launch_bounds__(THREADS) gemm_tc_kernel(GemmArgs a, int BN, De
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // (every global read comes after: a no-op unless launched to overlap the
+    // kernels before it)
+    griddep_launch_dependents();
+    griddep_wait();
 
     auto load_stage = [&](int kb, int s) {
         const uint32_t a_base = smem_u32(sA + s * L::a_stage);
@@ -486,6 +490,10 @@ gemm_rs_kernel(GemmArgs a_full, RsPlan pl, DeviceStatus st, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t half_cols = pl.tcols / 2;
+    // the prologue read only the weights and the bias: A, R and D wait for the
+    // kernels queued before this one (a no-op unless launched to overlap them)
+    griddep_launch_dependents();
+    griddep_wait();
     bool failed = false;
 
     if (warp == 0 || warp >= 2 + RS_NEPI) {
@@ -741,7 +749,8 @@ cudaError_t launch_rs(const GemmArgs &a, const RsPlan &pl, DeviceStatus st, cuda
     const int ng = pl.ng > 1 ? pl.ng : 1;
     const int64_t per = sms / ng;   // CTAs per column group
     const unsigned grid = (unsigned)((mtiles < per ? mtiles : per) * ng);
-    kern<<<grid, RS_THREADS, pl.smem, stream>>>(a, pl, st, tmA);
+    e = launch_maybe_overlapped(kern, dim3(grid), dim3(RS_THREADS), pl.smem, stream, a.overlap, a, pl, st, tmA);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -767,7 +776,8 @@ cudaError_t launch_stages(const GemmArgs &a, int BN, DeviceStatus st, cudaStream
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.rows + BM - 1) / BM), (unsigned)(a.N / BN));
-    kern<<<grid, THREADS, smem, stream>>>(a, BN, st);
+    e = launch_maybe_overlapped(kern, grid, dim3(THREADS), smem, stream, a.overlap, a, BN, st);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
