@@ -97,7 +97,12 @@ enum {
                                         weights, as in serving).  The three-kernel
                                         path's kernels overlap the same way, each
                                         with the one before it; the host-buffer
-                                        forward is unaffected. */
+                                        forward is unaffected.  swin_wattn_backward
+                                        then overlaps its own kernels after the
+                                        recompute GEMM (all but the large-window
+                                        attention ones), never the work queued
+                                        before the call, so it needs no such
+                                        guarantee. */
 };
 
 /* Creates a handle for blocks with C channels, `heads` heads (d = C/heads),

@@ -322,6 +322,29 @@ def test_forward_v2_tau_per_head(key, B, H, W, path):
     compare(out.double().cpu().numpy(), oracle_forward(w, g, table), w.dtype)
 
 
+@pytest.mark.parametrize("key,kw", [
+    ("swin_t_s1", dict(B=1, H=24, W=36, M=12, shift=6)),                      # V1: 144-token windows (tiles 128, 16)
+    ("swin_t_s1", dict(B=2, H=32, W=32, M=16, shift=8, C=64, heads=2)),       # window 16: two full query tiles
+    ("swin_t_s1", dict(B=1, H=40, W=40, M=20, shift=10, C=64, heads=2)),      # window 20: 400 tokens
+    ("swinv2_t_s1", dict(B=1, H=24, W=24, M=12, shift=6, C=768, heads=24)),   # more heads than the kernel's warps
+])
+def test_forward_large_windows(key, kw):
+    """The large-window kernel (windows of more than 64 tokens) at every window
+    size it is built for, V1 (online softmax) and V2 with 24 heads whose tau
+    puts some on the fixed reference and some on the online softmax (each
+    head's choice is made in the kernel's prologue, a warp per head).  At C =
+    768, Wqkv and Wproj are halved (exact in bf16) so that v, and the output
+    (a sum over 4x the channels of the C = 192 cases), keep the magnitude the
+    absolute bounds are set for."""
+    w = WORKLOADS[key].with_(**kw)
+    g = generate(w, nonzero_bias=True, tau=TAUS[6] * 4 if w.heads == 24 else 0.1)
+    if w.C == 768:
+        g["Wqkv"], g["Wproj"] = g["Wqkv"] * 0.5, g["Wproj"] * 0.5
+    table = oracle_table(w, g)
+    out = run_forward(w, device_inputs(g), table.to(DEV), sw.PATH_AUTO)
+    compare(out.double().cpu().numpy(), oracle_forward(w, g, table), w.dtype)
+
+
 # ---- the index maps through the whole forward, bit-exact -----------------------
 
 def one_hot_attention_inputs(w, x):

@@ -564,6 +564,13 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     auto step = [&](cudaError_t r) {
         if (e == cudaSuccess) { e = r; ++launches; }
     };
+    // With the overlap option the kernels after the QKV recompute start while
+    // the one before them finishes.  The transposes and the recompute stay
+    // ordinary launches, so every later kernel starts after both transposed
+    // weights are complete (the GEMMs read their weights before they wait; the
+    // attention and weight-gradient kernels read nothing before it).  The
+    // large-window kernels and the dq conversion stay ordinary launches too.
+    const int ov = h->overlap ? 1 : 0;
     step(launch_transpose((const bf16 *)Wproj, WpT, C, C, s));
     step(launch_transpose((const bf16 *)Wqkv, WqkvT, 3 * C, C, s));
     // window order: qkv = gather(x) Wqkv^T + bqkv, do = gather(dy) Wproj
@@ -574,12 +581,12 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     step(launch_gemm(k1, LOAD_GATHER, STORE_PLAIN, dstatus(h), s));
     GemmArgs k3{};
     k3.A = (const bf16 *)dy; k3.lda = C; k3.Bw = WpT; k3.D = dO; k3.ldd = C; k3.rows = g.T; k3.N = C; k3.K = C;
-    k3.g = g;
+    k3.g = g; k3.overlap = ov;
     step(launch_gemm(k3, LOAD_GATHER, STORE_PLAIN, dstatus(h), s));
     // o and dqkv in token order, dtable
     if (!flash) {
         step(launch_attn_backward(qkv, dO, (const bf16 *)bias_table, logit_scale, h->heads, v2 ? 1 : 0, g, attn, dqkv,
-                                  dtable, norms, dlogit_scale, dstatus(h), s));
+                                  dtable, norms, dlogit_scale, dstatus(h), s, ov));
     } else {
         AttnArgs k2{};
         k2.qkv = qkv; k2.attn = attn; k2.table = (const bf16 *)bias_table; k2.tau = logit_scale;
@@ -594,13 +601,13 @@ int swin_wattn_backward(swin_wattn_t h, const void *x, int B, int H, int W, cons
     // dx = dqkv Wqkv (token order already)
     GemmArgs k4{};
     k4.A = dqkv; k4.lda = 3 * C; k4.Bw = WqkvT; k4.D = (bf16 *)dx; k4.ldd = C; k4.rows = g.T; k4.N = C;
-    k4.K = 3 * C; k4.g = g;
+    k4.K = 3 * C; k4.g = g; k4.overlap = ov;
     step(launch_gemm(k4, LOAD_PLAIN, STORE_PLAIN, dstatus(h), s));
     // dWproj = dy^T attn and dbproj, dWqkv = dqkv^T x and dbqkv: split-K tcgen05
     // GEMMs over the tokens (three launches each: partial blocks, then their
     // sum in two levels)
-    step(launch_wgrad((const bf16 *)dy, C, attn, C, g.T, dWproj, dbproj, wg_ws, dstatus(h), s));
-    step(launch_wgrad(dqkv, 3 * C, (const bf16 *)x, C, g.T, dWqkv, dbqkv, wg_ws, dstatus(h), s));
+    step(launch_wgrad((const bf16 *)dy, C, attn, C, g.T, dWproj, dbproj, wg_ws, dstatus(h), s, ov));
+    step(launch_wgrad(dqkv, 3 * C, (const bf16 *)x, C, g.T, dWqkv, dbqkv, wg_ws, dstatus(h), s, ov));
     launches += 4;
     if (e != cudaSuccess) { h->last_cuda_error = e; return SWIN_WATTN_ECUDA; }
     h->bw_launches = launches;

@@ -248,9 +248,10 @@ __global__ void __launch_bounds__(AW_THREADS, 1)
     // bias - m, p = exp2(s sigma + table) is one FMA and an exp2, and P.V
     // accumulates across the key tiles in TMEM with no rescaling.  Otherwise
     // (V1, whose q.k is unbounded, or a wide span) sref is NaN and the online
-    // softmax runs.  One warp per head.
-    if (warp < a.heads) {
-        const float *tb = sbias + warp * LL;
+    // softmax runs.  One warp per head (a head count above the warp count
+    // takes further rounds).
+    for (int hd = warp; hd < a.heads; hd += AW_THREADS / 32) {
+        const float *tb = sbias + hd * LL;
         float mx = -INFINITY, mn = INFINITY;
         for (int e = lane; e < LL; e += 32) {
             const int dc = e % BS;
@@ -266,13 +267,13 @@ __global__ void __launch_bounds__(AW_THREADS, 1)
         }
         float ref = __int_as_float(0x7fc00000);   // NaN: online softmax
         if (a.mode == 1) {
-            const float sigma = AW_LOG2E / fmaxf(a.tau[warp], 0.01f);
+            const float sigma = AW_LOG2E / fmaxf(a.tau[hd], 0.01f);
             if (2.f * sigma + (mx - mn) <= 96.f) ref = sigma + mx;
         }
         __syncwarp();
         if (ref == ref)
-            for (int e = lane; e < LL; e += 32) sbias[warp * LL + e] -= ref;
-        if (lane == 0) sref[warp] = ref;
+            for (int e = lane; e < LL; e += 32) sbias[hd * LL + e] -= ref;
+        if (lane == 0) sref[hd] = ref;
     }
     tc_fence_before();
     __syncthreads();

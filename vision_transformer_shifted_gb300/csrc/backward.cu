@@ -513,9 +513,10 @@ cudaError_t launch_attn_tc(const bf16 *qkv, const bf16 *dO, const bf16 *table, c
 
 cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, const float *tau, int heads,
                                  int v2, const Geom &g, bf16 *attn, bf16 *dqkv, float *dtable, const float *norms,
-                                 float *dtau, DeviceStatus st, cudaStream_t stream)
+                                 float *dtau, DeviceStatus st, cudaStream_t stream, int overlap)
 {
-    return launch_attn_tc<true>(qkv, dO, table, tau, heads, v2, g, attn, dqkv, dtable, norms, dtau, st, stream);
+    return launch_attn_tc<true>(qkv, dO, table, tau, heads, v2, g, attn, dqkv, dtable, norms, dtau, st, stream,
+                                overlap);
 }
 
 cudaError_t launch_attn_forward_tc(const bf16 *qkv, const bf16 *table, const float *tau, int heads, int v2,

@@ -255,10 +255,12 @@ cudaError_t launch_watchdog(DeviceStatus st, cudaStream_t stream);
 // overwritten; db may be null) for bf16 row-major G [T, n_out] and X [T,
 // n_in] (n_in a multiple of 32, n_out of 8): split-K tcgen05 GEMM into
 // `workspace` (wgrad_workspace_bytes), then a fixed-order sum; three
-// launches.
+// launches.  overlap: each of the three may start while the kernel before it
+// finishes (programmatic dependent launch); they touch global memory only
+// after it has completed.
 size_t wgrad_workspace_bytes(int n_out, int n_in, int64_t T);
 cudaError_t launch_wgrad(const bf16 *G, int n_out, const bf16 *X, int n_in, int64_t T, float *dW, float *db,
-                         float *workspace, DeviceStatus st, cudaStream_t stream);
+                         float *workspace, DeviceStatus st, cudaStream_t stream, int overlap = 0);
 // out [cols, rows] = in [rows, cols]^T.
 cudaError_t launch_transpose(const bf16 *in, bf16 *out, int rows, int cols, cudaStream_t stream);
 // Windows of <= 64 tokens and 32 channels per head.
@@ -267,10 +269,11 @@ bool attn_backward_supported(int M, int C, int heads);
 // attn [T, C] and dqkv [T, 3C] in token order, and dtable += ([(2M-1)^2,
 // heads] fp32).  v2: qkv holds unit-length q and k, norms [T, 2 heads] their
 // norms (the QKV GEMM's), tau [heads]; dqkv is then the gradient of the raw
-// q and k, and dtau += ([heads] fp32).
+// q and k, and dtau += ([heads] fp32).  overlap as for launch_wgrad (the
+// prologue reads no global memory).
 cudaError_t launch_attn_backward(const bf16 *qkv, const bf16 *dO, const bf16 *table, const float *tau, int heads,
                                  int v2, const Geom &g, bf16 *attn, bf16 *dqkv, float *dtable, const float *norms,
-                                 float *dtau, DeviceStatus st, cudaStream_t stream);
+                                 float *dtau, DeviceStatus st, cudaStream_t stream, int overlap = 0);
 // Windows of more than 64 tokens (up to 24 x 24) and 32 channels per head.
 bool attn_flash_backward_supported(int M, int C, int heads);
 // The same gradients for large windows from the forward's outputs: attn

@@ -107,6 +107,11 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // (the prologue touched no global memory: G and X are read, and the partial
+    // sums written, only after the kernels queued before this one complete; a
+    // no-op unless launched to overlap them)
+    griddep_launch_dependents();
+    griddep_wait();
     bool ok = true;
 
     if (warp == 0) {
@@ -191,6 +196,8 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
 // Level 1: part1[y][e] = sum of partial[s][e] over s = y, y + RS, ... (in order).
 __global__ void wgrad_reduce1_kernel(const float *partial, int splits, int RS, int64_t n_tot, float *part1)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y;
     if (i4 * 4 >= n_tot) return;
@@ -208,6 +215,8 @@ __global__ void wgrad_reduce1_kernel(const float *partial, int splits, int RS, i
 // Level 2: the RS level-1 sums in order, into dW (the first n_w entries) and db.
 __global__ void wgrad_reduce2_kernel(const float *part1, int RS, int64_t n_w, int n_b, float *dW, float *db)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= n_w + n_b) return;
     const int64_t n_tot = ((n_w + n_b + 3) / 4) * 4;
@@ -268,7 +277,7 @@ size_t wgrad_workspace_bytes(int n_out, int n_in, int64_t T)
 }
 
 cudaError_t launch_wgrad(const bf16 *G, int n_out, const bf16 *X, int n_in, int64_t T, float *dW, float *db,
-                         float *workspace, DeviceStatus st, cudaStream_t stream)
+                         float *workspace, DeviceStatus st, cudaStream_t stream, int overlap)
 {
     WgPlan p;
     if (!wg_plan(n_out, n_in, T, p) || T >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
@@ -282,16 +291,18 @@ cudaError_t launch_wgrad(const bf16 *G, int n_out, const bf16 *X, int n_in, int6
     if (e != cudaSuccess) return e;
     const int64_t n_tot = wg_ntot(n_out, n_in);
     WgArgs a{n_out, n_in, T, workspace, n_tot};
-    wgrad_kernel<<<p.tiles_m * p.tiles_n * p.splits, WG_THREADS, smem, stream>>>(a, p, st, tg, tx);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_maybe_overlapped(wgrad_kernel, dim3(p.tiles_m * p.tiles_n * p.splits), dim3(WG_THREADS), smem, stream,
+                                overlap, a, p, st, tg, tx);
+    if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
     const int RS = wg_rs(p);
     float *part1 = workspace + (int64_t)p.splits * n_tot;
-    wgrad_reduce1_kernel<<<dim3((unsigned)((n_tot / 4 + 255) / 256), (unsigned)RS), 256, 0, stream>>>(
-        workspace, p.splits, RS, n_tot, part1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_maybe_overlapped(wgrad_reduce1_kernel, dim3((unsigned)((n_tot / 4 + 255) / 256), (unsigned)RS),
+                                dim3(256), 0, stream, overlap, (const float *)workspace, p.splits, RS, n_tot, part1);
+    if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t n = (int64_t)n_out * n_in + n_out;
-    wgrad_reduce2_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(part1, RS, (int64_t)n_out * n_in, n_out,
-                                                                          dW, db);
+    e = launch_maybe_overlapped(wgrad_reduce2_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream, overlap,
+                                (const float *)part1, RS, (int64_t)n_out * n_in, n_out, dW, db);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
