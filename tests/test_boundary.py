@@ -72,3 +72,28 @@ def test_null_handle_calls():
                                     1, 16, 48, 1, None) == sw.EINVAL  # masked pair: K % 32
     assert lib.swin_wattn_test_gemm(ctypes.c_void_p(16), ctypes.c_void_p(16), None, ctypes.c_void_p(16),
                                     1, 144, 32, 1, None) == sw.EINVAL  # masked pair: N > 128
+
+
+def header_enums():
+    vals = {}
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        text = open(os.path.join(ROOT, "include", hdr)).read()
+        for name, v in re.findall(r"\b(SWIN_(?:WATTN|BLOCK)_[A-Z0-9_]+)\s*=\s*(-?(?:0x[0-9a-fA-F]+|\d+))\b", text):
+            vals[name] = int(v, 0)
+    return vals
+
+
+def test_binding_constants_match_the_headers():
+    """Every mode, status and option constant of the binding has the value the
+    headers give it (SWIN_WATTN_X is the binding's X, SWIN_BLOCK_OPT_X its
+    BLOCK_OPT_X), and every enumerator of the headers has its binding name."""
+    vals = header_enums()
+    assert len(vals) >= 16
+    missing = []
+    for name, v in vals.items():
+        py = name[len("SWIN_WATTN_"):] if name.startswith("SWIN_WATTN_") else name[len("SWIN_"):]
+        if not hasattr(sw, py):
+            missing.append(name)
+            continue
+        assert getattr(sw, py) == v, (name, getattr(sw, py), v)
+    assert not missing, missing
