@@ -68,3 +68,26 @@ def test_two_gloo_ranks(tmp_path):
     d = json.loads(lines[0].splitlines()[-1])
     assert d["impl"] == "reference" and d["n_gpus"] == world and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_stored_traffic_is_reported_only_for_the_source_it_was_taken_on(monkeypatch):
+    """bench.py's roofline.traffic comes from ncu counters stored with the sha1
+    prefix of the kernel source they were taken on: it is reported while that
+    source is unchanged and null once it has changed (or the file is gone),
+    and every stored entry names an existing source file."""
+    import hashlib
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = os.path.join(ROOT, "vision_transformer_shifted_gb300", "csrc")
+    for (_wl, _k), (traffic, fname, _sha) in bench.PROFILED_TRAFFIC.items():
+        assert traffic > 0 and os.path.exists(os.path.join(csrc, fname)), fname
+    sha = hashlib.sha1(open(os.path.join(csrc, "attn_window.cu"), "rb").read()).hexdigest()[:12]
+    monkeypatch.setattr(bench, "PROFILED_TRAFFIC", {
+        ("w", "same"): (1.0e6, "attn_window.cu", sha),
+        ("w", "changed"): (1.0e6, "attn_window.cu", "000000000000"),
+        ("w", "gone"): (1.0e6, "no_such_file.cu", sha),
+    })
+    assert bench.profiled_traffic("w", "same") == 1.0e6
+    assert bench.profiled_traffic("w", "changed") is None
+    assert bench.profiled_traffic("w", "gone") is None
+    assert bench.profiled_traffic("w", "absent") is None
